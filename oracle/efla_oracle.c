@@ -1,0 +1,176 @@
+/*
+ * EFLA oracle -- TEST INFRASTRUCTURE ONLY.
+ *
+ * A plain, slow, sequential fp64 implementation of the Error-Free Linear
+ * Attention token mixer, used to check the CUDA path.  Only the tests, the
+ * smoke entry and the CPU-baseline leg of the benchmark may load it; the
+ * product path never does.  It shares no code, header or constant with the
+ * CUDA library.
+ *
+ * What it computes, per (sequence, head), token by token:
+ *
+ *   lam_t   = ||k_t||^2
+ *       ["Exact Flow Linear Attention" (gist.science), Metodologia 2:
+ *        the rank-1 dynamics matrix A_t = k_t k_t^T has A_t^n = lam_t^{n-1} A_t]
+ *   alpha_t = (1 - exp(-beta_t lam_t)) / lam_t, evaluated as
+ *             -expm1(-beta_t lam_t) / lam_t; alpha_t = beta_t when lam_t == 0
+ *       [same page, Metodologia 3; "Error-Free Linear Attention is a Free
+ *        Lunch" (howistudyai), Step 1.  The lam -> 0 value is the limit of the
+ *        formula, which the howistudyai page describes in Step 5 as small keys
+ *        behaving like the delta rule.]
+ *   S_t     = (I - alpha_t k_t k_t^T) S_{t-1} + alpha_t k_t v_t^T
+ *       [gist.science, Metodologia 3; howistudyai, Step 2]
+ *   o_t     = S_t^T q_t   (the state AFTER token t's update)
+ *       [howistudyai, Step 3 and "Putting it all together (pipeline)"]
+ *
+ * The update is evaluated in the factored form
+ *   x = S_{t-1}^T k_t;   S_t = S_{t-1} + alpha_t k_t (v_t - x)^T,
+ * which is the same matrix as (I - alpha k k^T) S + alpha k v^T by
+ * distributivity: (I - a k k^T) S + a k v^T = S - a k (k^T S) + a k v^T.
+ * A literal d x d form of the same update is in oracle/literal.py and the
+ * tests check that the two agree.
+ *
+ * Layouts (all row-major, fp64):
+ *   q, k  [B, T, H, dk];  v [B, T, H, dv];  beta [B, T, H]
+ *   S0, S_T [N, H, dk, dv]  (dv contiguous), S0 may be NULL (zeros)
+ *   o     [B, T, H, dv]
+ *   cu_seqlens [N+1] int64 or NULL.  When given, B must be 1 and sequence n
+ *   covers tokens cu_seqlens[n] .. cu_seqlens[n+1]-1 of the packed T axis;
+ *   sequences are independent and each starts from its own S0[n].
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+double efla_oracle_alpha(double beta, double lam)
+{
+    if (lam > 0.0)
+        return -expm1(-beta * lam) / lam;
+    return beta;
+}
+
+/* One token of one head: updates S (dk x dv) in place and writes o (dv). */
+static void oracle_token(const double *q, const double *k, const double *v, double beta,
+                         double *S, double *o, int dk, int dv, double *x)
+{
+    double lam = 0.0;
+    for (int i = 0; i < dk; ++i)
+        lam += k[i] * k[i];
+    const double a = efla_oracle_alpha(beta, lam);
+
+    for (int j = 0; j < dv; ++j)
+        x[j] = 0.0;
+    for (int i = 0; i < dk; ++i)
+        for (int j = 0; j < dv; ++j)
+            x[j] += k[i] * S[(size_t)i * dv + j];
+
+    for (int i = 0; i < dk; ++i)
+        for (int j = 0; j < dv; ++j)
+            S[(size_t)i * dv + j] += a * k[i] * (v[j] - x[j]);
+
+    for (int j = 0; j < dv; ++j)
+        o[j] = 0.0;
+    for (int i = 0; i < dk; ++i)
+        for (int j = 0; j < dv; ++j)
+            o[j] += q[i] * S[(size_t)i * dv + j];
+}
+
+/* Returns 0 on success, -1 on bad arguments, -2 on allocation failure. */
+int efla_oracle_fwd(const double *q, const double *k, const double *v, const double *beta,
+                    const double *S0, const int64_t *cu_seqlens, double *o, double *S_T,
+                    int B, int T, int H, int dk, int dv, int N, int nthreads)
+{
+    if (B < 0 || T < 0 || H <= 0 || dk <= 0 || dv <= 0 || N < 0)
+        return -1;
+    if (cu_seqlens) {
+        if (B != 1)
+            return -1;
+        if (cu_seqlens[0] != 0 || cu_seqlens[N] != T)
+            return -1;
+        for (int n = 0; n < N; ++n)
+            if (cu_seqlens[n + 1] < cu_seqlens[n])
+                return -1;
+    } else if (N != B) {
+        return -1;
+    }
+    const long units = (long)N * H;
+    int failed = 0;
+#ifdef _OPENMP
+    if (nthreads > 0)
+        omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : failed)
+#endif
+    for (long u = 0; u < units; ++u) {
+        const int n = (int)(u / H), h = (int)(u % H);
+        double *S = (double *)malloc(sizeof(double) * (size_t)dk * dv);
+        double *x = (double *)malloc(sizeof(double) * (size_t)dv);
+        if (!S || !x) {
+            free(S);
+            free(x);
+            failed |= 1;
+            continue;
+        }
+        const double *s0 = S0 ? S0 + ((size_t)n * H + h) * dk * dv : NULL;
+        for (size_t e = 0; e < (size_t)dk * dv; ++e)
+            S[e] = s0 ? s0[e] : 0.0;
+        long t0, t1, b;
+        if (cu_seqlens) {
+            b = 0;
+            t0 = cu_seqlens[n];
+            t1 = cu_seqlens[n + 1];
+        } else {
+            b = n;
+            t0 = 0;
+            t1 = T;
+        }
+        for (long t = t0; t < t1; ++t) {
+            const size_t row = ((size_t)b * T + t) * H + h;
+            oracle_token(q + row * dk, k + row * dk, v + row * dv, beta[row], S, o + row * dv,
+                         dk, dv, x);
+        }
+        if (S_T)
+            memcpy(S_T + ((size_t)n * H + h) * dk * dv, S, sizeof(double) * (size_t)dk * dv);
+        free(S);
+        free(x);
+    }
+    return failed ? -2 : 0;
+}
+
+/* One decode step for B*H independent heads; S [B, H, dk, dv] updated in place. */
+int efla_oracle_decode(const double *q, const double *k, const double *v, const double *beta,
+                       double *S, double *o, int B, int H, int dk, int dv, int nthreads)
+{
+    if (B < 0 || H <= 0 || dk <= 0 || dv <= 0)
+        return -1;
+    const long units = (long)B * H;
+    int failed = 0;
+#ifdef _OPENMP
+    if (nthreads > 0)
+        omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(static) reduction(| : failed)
+#endif
+    for (long u = 0; u < units; ++u) {
+        double *x = (double *)malloc(sizeof(double) * (size_t)dv);
+        if (!x) {
+            failed |= 1;
+            continue;
+        }
+        oracle_token(q + u * dk, k + u * dk, v + u * dv, beta[u], S + u * (size_t)dk * dv,
+                     o + u * dv, dk, dv, x);
+        free(x);
+    }
+    return failed ? -2 : 0;
+}
+
+int efla_oracle_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
