@@ -1,0 +1,192 @@
+"""Python binding of libefla.so -- the GB300 (sm_103a) EFLA token mixer.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI declared in ``include/efla.h``.  PyTorch provides
+device memory and streams.  If the shared library is missing, importing
+works but every call raises ``RuntimeError`` -- there is no fallback path.
+
+    o, S_T = fwd_chunked(q, k, v, beta, S0=None, cu_seqlens=None)
+    o      = decode_step(q, k, v, beta, S)        # S updated in place
+
+Semantics (per head): lambda = ||k||^2, alpha = (1 - e^{-beta*lambda})/lambda,
+S <- (I - alpha k k^T) S + alpha k v^T, o = S^T q with the updated S.
+["Exact Flow Linear Attention" (gist.science), Metodologia 3;
+ "Error-Free Linear Attention is a Free Lunch" (howistudyai), Steps 1-3.]
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Tuple
+
+import torch
+
+__all__ = ["EflaError", "lib_path", "load", "fwd_chunked", "fwd_recurrent", "decode_step",
+           "device_status", "abi_version", "STATUS"]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+lib_path = os.path.join(_PKG, "libefla.so")
+
+STATUS = {0: "EFLA_OK", 1: "EFLA_ERR_INVALID_ARG", 2: "EFLA_ERR_UNSUPPORTED", 3: "EFLA_ERR_CUDA",
+          4: "EFLA_ERR_DEVICE_TIMEOUT"}
+BF16, F32 = 0, 1
+
+_lock = threading.Lock()
+_lib = None
+
+
+class EflaError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"{STATUS.get(code, code)}: {msg}")
+        self.code = code
+
+
+def load():
+    """Load libefla.so (built by ``__graft_entry__.build()``); raise if absent."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(lib_path):
+            raise RuntimeError(f"{lib_path} is not built; run `python -c 'import __graft_entry__ as g; "
+                               f"g.build()'` (there is no non-CUDA fallback)")
+        L = ctypes.CDLL(lib_path)
+        vp, ip = ctypes.c_void_p, ctypes.c_int
+        L.efla_fwd_chunked.restype = ip
+        L.efla_fwd_chunked.argtypes = [vp] * 8 + [ip] * 9 + [vp]
+        L.efla_fwd_recurrent.restype = ip
+        L.efla_fwd_recurrent.argtypes = [vp] * 8 + [ip] * 8 + [vp]
+        L.efla_decode_step.restype = ip
+        L.efla_decode_step.argtypes = [vp] * 6 + [ip] * 6 + [vp]
+        L.efla_device_status.restype = ip
+        L.efla_device_status.argtypes = [vp]
+        L.efla_status_string.restype = ctypes.c_char_p
+        L.efla_status_string.argtypes = [ip]
+        L.efla_last_error.restype = ctypes.c_char_p
+        L.efla_last_error.argtypes = []
+        L.efla_abi_version.restype = ip
+        L.efla_abi_version.argtypes = []
+        _lib = L
+        return L
+
+
+def abi_version() -> int:
+    return load().efla_abi_version()
+
+
+def _check(code: int):
+    if code != 0:
+        raise EflaError(code, load().efla_last_error().decode())
+
+
+def _dt(t: torch.dtype) -> int:
+    if t == torch.bfloat16:
+        return BF16
+    if t == torch.float32:
+        return F32
+    raise EflaError(1, f"unsupported dtype {t}")
+
+
+def _p(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t: Optional[torch.Tensor], name: str):
+    if t is None:
+        return
+    if not t.is_cuda:
+        raise EflaError(1, f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise EflaError(1, f"{name} must be contiguous")
+
+
+def _fwd(entry, q, k, v, beta, S0, cu_seqlens, o, S_T, o_dtype, chunk, stream, return_state):
+    L = load()
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (beta, "beta"), (S0, "S0"), (cu_seqlens, "cu_seqlens"),
+                 (o, "o"), (S_T if isinstance(S_T, torch.Tensor) else None, "S_T")):
+        _need(t, n)
+    if q.dim() != 4 or k.shape != q.shape or v.shape[:3] != q.shape[:3] or beta.shape != q.shape[:3]:
+        raise EflaError(1, f"shape mismatch q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)} "
+                           f"beta{tuple(beta.shape)}")
+    if q.dtype != k.dtype or q.dtype != v.dtype or beta.dtype != torch.float32:
+        raise EflaError(1, "q, k, v must share a dtype and beta must be float32")
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if cu_seqlens is not None:
+        if cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1:
+            raise EflaError(1, "cu_seqlens must be a 1-D int32 tensor")
+        N = cu_seqlens.shape[0] - 1
+    else:
+        N = B
+    if S0 is not None and (S0.dtype != torch.float32 or tuple(S0.shape) != (N, H, dk, dv)):
+        raise EflaError(1, f"S0 must be float32 [{N},{H},{dk},{dv}]")
+    if o is None:
+        o = torch.empty((B, T, H, dv), dtype=o_dtype, device=q.device)
+    elif tuple(o.shape) != (B, T, H, dv):
+        raise EflaError(1, "o has the wrong shape")
+    if S_T is None and return_state:
+        S_T = torch.empty((N, H, dk, dv), dtype=torch.float32, device=q.device)
+    elif isinstance(S_T, torch.Tensor) and (S_T.dtype != torch.float32 or tuple(S_T.shape) != (N, H, dk, dv)):
+        raise EflaError(1, f"S_T must be float32 [{N},{H},{dk},{dv}]")
+    st = S_T if isinstance(S_T, torch.Tensor) else None
+    args = [_p(q), _p(k), _p(v), _p(beta), _p(S0), _p(cu_seqlens), _p(o), _p(st), B, T, H, dk, dv, N,
+            _dt(q.dtype), _dt(o.dtype)]
+    if entry == "chunked":
+        _check(L.efla_fwd_chunked(*args, int(chunk), _stream(stream)))
+    else:
+        _check(L.efla_fwd_recurrent(*args, _stream(stream)))
+    return o, st
+
+
+def fwd_chunked(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor,
+                S0: Optional[torch.Tensor] = None, cu_seqlens: Optional[torch.Tensor] = None, *,
+                o: Optional[torch.Tensor] = None, S_T: Optional[torch.Tensor] = None,
+                o_dtype: torch.dtype = torch.float32, chunk: int = 64, stream=None,
+                return_state: bool = True) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """EFLA forward, chunkwise.  Layouts as in ``efla_fwd_chunked`` (include/efla.h).
+
+    q, k [B,T,H,dk], v [B,T,H,dv] (bf16 or fp32); beta [B,T,H] fp32; S0 [N,H,dk,dv] fp32;
+    cu_seqlens [N+1] int32 (then B == 1).  Returns (o [B,T,H,dv] in ``o_dtype``,
+    S_T [N,H,dk,dv] fp32 or None when ``return_state`` is False).
+    """
+    return _fwd("chunked", q, k, v, beta, S0, cu_seqlens, o, S_T, o_dtype, chunk, stream, return_state)
+
+
+def fwd_recurrent(q, k, v, beta, S0=None, cu_seqlens=None, *, o=None, S_T=None,
+                  o_dtype: torch.dtype = torch.float32, stream=None, return_state: bool = True):
+    """Token-by-token fp32 evaluation on CUDA cores (``efla_fwd_recurrent``)."""
+    return _fwd("recurrent", q, k, v, beta, S0, cu_seqlens, o, S_T, o_dtype, 0, stream, return_state)
+
+
+def decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor, S: torch.Tensor, *,
+                o: Optional[torch.Tensor] = None, o_dtype: torch.dtype = torch.float32,
+                stream=None) -> torch.Tensor:
+    """One token per sequence; S [B,H,dk,dv] fp32 is updated in place.  Returns o [B,H,dv]."""
+    L = load()
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (beta, "beta"), (S, "S"), (o, "o")):
+        _need(t, n)
+    if q.dim() != 3 or k.shape != q.shape or v.shape[:2] != q.shape[:2] or beta.shape != q.shape[:2]:
+        raise EflaError(1, "shape mismatch")
+    B, H, dk = q.shape
+    dv = v.shape[-1]
+    if S.dtype != torch.float32 or tuple(S.shape) != (B, H, dk, dv):
+        raise EflaError(1, f"S must be float32 [{B},{H},{dk},{dv}]")
+    if q.dtype != k.dtype or q.dtype != v.dtype or beta.dtype != torch.float32:
+        raise EflaError(1, "q, k, v must share a dtype and beta must be float32")
+    if o is None:
+        o = torch.empty((B, H, dv), dtype=o_dtype, device=q.device)
+    _check(L.efla_decode_step(_p(q), _p(k), _p(v), _p(beta), _p(S), _p(o), B, H, dk, dv,
+                              _dt(q.dtype), _dt(o.dtype), _stream(stream)))
+    return o
+
+
+def device_status(stream=None) -> int:
+    """Read and clear the library's device status word (synchronises ``stream``)."""
+    return load().efla_device_status(_stream(stream))

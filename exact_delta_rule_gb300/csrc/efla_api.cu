@@ -1,0 +1,208 @@
+// C-ABI entry points of libefla.so: argument validation, dispatch to the
+// kernels, status reporting.  Declarations and the contract are in efla.h.
+#include <stdarg.h>
+#include <stdio.h>
+
+#include <string>
+
+#include "internal.cuh"
+
+namespace efla {
+namespace {
+
+__device__ int g_device_status = 0;
+
+thread_local std::string g_last_error;
+
+efla_status fail(efla_status s, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return s;
+}
+
+efla_status cuda_fail(cudaError_t e, const char *what) {
+    return fail(EFLA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool supported_dim(int d) { return d == 32 || d == 64 || d == 128; }
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+size_t dsize(efla_dtype t) { return t == EFLA_BF16 ? 2 : 4; }
+
+struct Range {
+    const char *name;
+    uintptr_t lo, hi;
+};
+bool overlap(const Range &a, const Range &b) {
+    return a.lo < a.hi && b.lo < b.hi && a.lo < b.hi && b.lo < a.hi;
+}
+
+efla_status check_dims_common(int d_k, int d_v, efla_dtype in_dtype, efla_dtype o_dtype) {
+    if (d_k <= 0 || d_v <= 0) return fail(EFLA_ERR_INVALID_ARG, "d_k=%d d_v=%d must be positive", d_k, d_v);
+    if (!supported_dim(d_k) || !supported_dim(d_v))
+        return fail(EFLA_ERR_UNSUPPORTED, "d_k=%d d_v=%d: supported head sizes are 32, 64, 128", d_k, d_v);
+    if ((in_dtype != EFLA_BF16 && in_dtype != EFLA_F32) || (o_dtype != EFLA_BF16 && o_dtype != EFLA_F32))
+        return fail(EFLA_ERR_INVALID_ARG, "unknown dtype (in=%d, o=%d)", (int)in_dtype, (int)o_dtype);
+    return EFLA_OK;
+}
+
+efla_status validate_fwd(const FwdArgs &a, bool chunked) {
+    if (a.B < 0 || a.T < 0 || a.H <= 0 || a.N < 0)
+        return fail(EFLA_ERR_INVALID_ARG, "bad sizes B=%d T=%d H=%d N=%d", a.B, a.T, a.H, a.N);
+    efla_status s = check_dims_common(a.dk, a.dv, a.in_dtype, a.o_dtype);
+    if (s != EFLA_OK) return s;
+    if (chunked && a.chunk != 64)
+        return fail(EFLA_ERR_UNSUPPORTED, "chunk=%d: supported chunk length is 64", a.chunk);
+    if (a.cu_seqlens) {
+        if (a.B != 1) return fail(EFLA_ERR_INVALID_ARG, "cu_seqlens given with B=%d (must be 1)", a.B);
+    } else if (a.N != a.B) {
+        return fail(EFLA_ERR_INVALID_ARG, "N=%d must equal B=%d when cu_seqlens is NULL", a.N, a.B);
+    }
+    const long long tokens = (long long)a.B * a.T;
+    if (tokens * a.H > (1LL << 31) - 1)
+        return fail(EFLA_ERR_UNSUPPORTED, "B*T*H=%lld exceeds 2^31-1 token-heads", tokens * a.H);
+    if (a.cu_seqlens && a.N > (1 << 30)) return fail(EFLA_ERR_INVALID_ARG, "N=%d too large", a.N);
+    if (tokens > 0 && (!a.q || !a.k || !a.v || !a.beta || !a.o))
+        return fail(EFLA_ERR_INVALID_ARG, "q, k, v, beta and o must be non-NULL when B*T > 0");
+    const void *ptrs[] = {a.q, a.k, a.v, a.beta, a.S0, a.cu_seqlens, a.o, a.S_T};
+    const char *names[] = {"q", "k", "v", "beta", "S0", "cu_seqlens", "o", "S_T"};
+    for (int i = 0; i < 8; ++i)
+        if (ptrs[i] && !aligned16(ptrs[i]))
+            return fail(EFLA_ERR_INVALID_ARG, "%s=%p is not 16-byte aligned", names[i], ptrs[i]);
+    const size_t th = (size_t)tokens * a.H;
+    const size_t st = (size_t)a.N * a.H * a.dk * a.dv * 4;
+    auto R = [](const char *n, const void *p, size_t bytes) {
+        uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+        return Range{n, lo, p ? lo + bytes : lo};
+    };
+    const Range in[] = {R("q", a.q, th * a.dk * dsize(a.in_dtype)), R("k", a.k, th * a.dk * dsize(a.in_dtype)),
+                        R("v", a.v, th * a.dv * dsize(a.in_dtype)), R("beta", a.beta, th * 4),
+                        R("S0", a.S0, st), R("cu_seqlens", a.cu_seqlens, a.cu_seqlens ? (size_t)(a.N + 1) * 4 : 0)};
+    const Range out[] = {R("o", a.o, th * a.dv * dsize(a.o_dtype)), R("S_T", a.S_T, st)};
+    for (const Range &w : out)
+        for (const Range &r : in) {
+            if (w.name[0] == 'S' && r.name[0] == 'S' && w.lo == r.lo) continue;  // S0 == S_T allowed
+            if (overlap(w, r)) return fail(EFLA_ERR_INVALID_ARG, "output %s overlaps input %s", w.name, r.name);
+        }
+    if (overlap(out[0], out[1])) return fail(EFLA_ERR_INVALID_ARG, "o overlaps S_T");
+    return EFLA_OK;
+}
+
+efla_status run_fwd(const FwdArgs &a, bool chunked) {
+    efla_status s = validate_fwd(a, chunked);
+    if (s != EFLA_OK) return s;
+    cudaError_t e;
+    if (chunked && a.in_dtype == EFLA_BF16 && a.dk == 128 && a.dv == 128) {
+        const char *why = nullptr;
+        e = launch_chunk_tc(a, &why);
+        if (e != cudaSuccess) return cuda_fail(e, why ? why : "tcgen05 chunk kernel launch");
+    } else {
+        e = launch_recurrent(a);
+        if (e != cudaSuccess) return cuda_fail(e, "recurrent kernel launch");
+    }
+    g_last_error.clear();
+    return EFLA_OK;
+}
+
+}  // namespace
+
+int *device_status_ptr() {
+    static int *ptr = nullptr;  // one device in this process; set-up is idempotent
+    if (!ptr) {
+        int *p = nullptr;
+        if (cudaGetSymbolAddress(reinterpret_cast<void **>(&p), g_device_status) == cudaSuccess) ptr = p;
+    }
+    return ptr;
+}
+
+}  // namespace efla
+
+using namespace efla;
+
+extern "C" {
+
+efla_status efla_fwd_chunked(const void *q, const void *k, const void *v, const float *beta, const float *S0,
+                             const int32_t *cu_seqlens, void *o, float *S_T, int B, int T, int H, int d_k,
+                             int d_v, int N, efla_dtype in_dtype, efla_dtype o_dtype, int chunk,
+                             efla_stream_t stream) {
+    FwdArgs a{q, k, v, beta, S0, cu_seqlens, o, S_T, B, T, H, d_k, d_v, N, in_dtype, o_dtype,
+              chunk == 0 ? 64 : chunk, reinterpret_cast<cudaStream_t>(stream)};
+    return run_fwd(a, true);
+}
+
+efla_status efla_fwd_recurrent(const void *q, const void *k, const void *v, const float *beta,
+                               const float *S0, const int32_t *cu_seqlens, void *o, float *S_T, int B,
+                               int T, int H, int d_k, int d_v, int N, efla_dtype in_dtype, efla_dtype o_dtype,
+                               efla_stream_t stream) {
+    FwdArgs a{q, k, v, beta, S0, cu_seqlens, o, S_T, B, T, H, d_k, d_v, N, in_dtype, o_dtype,
+              0, reinterpret_cast<cudaStream_t>(stream)};
+    return run_fwd(a, false);
+}
+
+efla_status efla_decode_step(const void *q, const void *k, const void *v, const float *beta, float *S, void *o,
+                             int B, int H, int d_k, int d_v, efla_dtype in_dtype, efla_dtype o_dtype,
+                             efla_stream_t stream) {
+    if (B < 0 || H <= 0) return fail(EFLA_ERR_INVALID_ARG, "bad sizes B=%d H=%d", B, H);
+    efla_status s = check_dims_common(d_k, d_v, in_dtype, o_dtype);
+    if (s != EFLA_OK) return s;
+    if ((long long)B * H > (1LL << 31) - 1) return fail(EFLA_ERR_UNSUPPORTED, "B*H too large");
+    if (B > 0 && (!q || !k || !v || !beta || !S || !o))
+        return fail(EFLA_ERR_INVALID_ARG, "q, k, v, beta, S and o must be non-NULL when B > 0");
+    const void *ptrs[] = {q, k, v, beta, S, o};
+    const char *names[] = {"q", "k", "v", "beta", "S", "o"};
+    for (int i = 0; i < 6; ++i)
+        if (ptrs[i] && !aligned16(ptrs[i]))
+            return fail(EFLA_ERR_INVALID_ARG, "%s=%p is not 16-byte aligned", names[i], ptrs[i]);
+    const size_t u = (size_t)B * H;
+    auto rng = [](const void *p, size_t n) {
+        return Range{"", reinterpret_cast<uintptr_t>(p), reinterpret_cast<uintptr_t>(p) + n};
+    };
+    const Range rS = rng(S, u * d_k * d_v * 4), ro = rng(o, u * d_v * dsize(o_dtype));
+    const Range ins[] = {rng(q, u * d_k * dsize(in_dtype)), rng(k, u * d_k * dsize(in_dtype)),
+                         rng(v, u * d_v * dsize(in_dtype)), rng(beta, u * 4)};
+    for (const Range &r : ins)
+        if (overlap(rS, r) || overlap(ro, r)) return fail(EFLA_ERR_INVALID_ARG, "an output overlaps an input");
+    if (overlap(rS, ro)) return fail(EFLA_ERR_INVALID_ARG, "o overlaps S");
+    DecodeArgs a{q, k, v, beta, S, o, B, H, d_k, d_v, in_dtype, o_dtype, reinterpret_cast<cudaStream_t>(stream)};
+    cudaError_t e = launch_decode(a);
+    if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
+    g_last_error.clear();
+    return EFLA_OK;
+}
+
+efla_status efla_device_status(efla_stream_t stream) {
+    int *p = device_status_ptr();
+    if (!p) return fail(EFLA_ERR_CUDA, "cannot resolve the device status word");
+    int h = 0;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(&h, p, sizeof(int), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(p, 0, sizeof(int), st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the device status word");
+    if (h != EFLA_OK) {
+        g_last_error = "a bounded in-kernel wait expired";
+        return static_cast<efla_status>(h);
+    }
+    return EFLA_OK;
+}
+
+const char *efla_status_string(efla_status s) {
+    switch (s) {
+        case EFLA_OK: return "EFLA_OK";
+        case EFLA_ERR_INVALID_ARG: return "EFLA_ERR_INVALID_ARG: invalid argument";
+        case EFLA_ERR_UNSUPPORTED: return "EFLA_ERR_UNSUPPORTED: valid but unsupported configuration";
+        case EFLA_ERR_CUDA: return "EFLA_ERR_CUDA: CUDA call or kernel launch failed";
+        case EFLA_ERR_DEVICE_TIMEOUT: return "EFLA_ERR_DEVICE_TIMEOUT: a bounded in-kernel wait expired";
+    }
+    return "unknown efla_status";
+}
+
+const char *efla_last_error(void) { return g_last_error.c_str(); }
+
+int efla_abi_version(void) { return EFLA_ABI_VERSION; }
+
+}  // extern "C"

@@ -1,0 +1,59 @@
+// Internal declarations shared by the translation units of libefla.so.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "efla.h"
+
+namespace efla {
+
+// Library-owned device status word (EFLA_OK or EFLA_ERR_DEVICE_TIMEOUT).
+// Defined in efla_api.cu; kernels in other units reach it through a pointer
+// obtained with cudaGetSymbolAddress, passed as a kernel argument.
+int *device_status_ptr();
+
+struct FwdArgs {
+    const void *q, *k, *v;
+    const float *beta;
+    const float *S0;
+    const int32_t *cu_seqlens;
+    void *o;
+    float *S_T;
+    int B, T, H, dk, dv, N;
+    efla_dtype in_dtype, o_dtype;
+    int chunk;
+    cudaStream_t stream;
+};
+
+struct DecodeArgs {
+    const void *q, *k, *v;
+    const float *beta;
+    float *S;
+    void *o;
+    int B, H, dk, dv;
+    efla_dtype in_dtype, o_dtype;
+    cudaStream_t stream;
+};
+
+// Launchers return a cudaError_t from the launch (cudaSuccess if nothing launched).
+cudaError_t launch_recurrent(const FwdArgs &a);
+cudaError_t launch_decode(const DecodeArgs &a);
+// tcgen05 chunk kernel: bf16 inputs, d_k = d_v = 128, chunk 64.
+cudaError_t launch_chunk_tc(const FwdArgs &a, const char **why);
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);
+}
+
+// alpha = (1 - e^{-beta*lam}) / lam, evaluated as -expm1(-beta*lam)/lam; beta at lam == 0.
+__device__ __forceinline__ float efla_alpha(float beta, float lam) {
+    return lam > 0.f ? -expm1f(-beta * lam) / lam : beta;
+}
+
+}  // namespace efla

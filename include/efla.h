@@ -1,0 +1,146 @@
+/*
+ * efla.h -- C ABI of libefla.so, the GB300 (sm_103a) implementation of the
+ * Error-Free Linear Attention (EFLA) token mixer.
+ *
+ * The operation (per head; notation of the pages that describe the method):
+ *
+ *   lambda_t = ||k_t||^2
+ *   alpha_t  = (1 - exp(-beta_t lambda_t)) / lambda_t      (beta_t when lambda_t == 0)
+ *   S_t      = (I - alpha_t k_t k_t^T) S_{t-1} + alpha_t k_t v_t^T
+ *   o_t      = S_t^T q_t                                     (reads the UPDATED state)
+ *
+ *   ["Exact Flow Linear Attention: Exact Solution from Continuous-Time Dynamics"
+ *    (gist.science summary), Metodologia 2-3;
+ *    "Error-Free Linear Attention is a Free Lunch: Exact Solution from
+ *    Continuous-Time Dynamics" (howistudyai explainer), Steps 1-3 and
+ *    "Putting it all together (pipeline)".]
+ *
+ * No scaling of q and no normalisation of q or k is applied: the key norm is
+ * the gate's input (howistudyai, "Key Norms as Dynamic Gates").
+ *
+ * Conventions shared by every entry point
+ *   - All tensor arguments are DEVICE pointers to contiguous row-major arrays
+ *     owned by the caller.  The library allocates no device memory per call.
+ *   - Every call is asynchronous on `stream` (NULL = legacy default stream)
+ *     and never synchronises the host.
+ *   - Arguments are validated on the host before anything is launched.  A
+ *     rejected call returns EFLA_ERR_INVALID_ARG or EFLA_ERR_UNSUPPORTED and
+ *     launches nothing.  Launch failures return EFLA_ERR_CUDA.
+ *   - Kernels that wait on other warps bound every wait; if a bound expires
+ *     the kernel abandons its work, records EFLA_ERR_DEVICE_TIMEOUT in a
+ *     library-owned device status word and returns.  efla_device_status()
+ *     reads and clears that word.
+ *   - Pointers must be 16-byte aligned.  Outputs must not alias inputs, except
+ *     that S0 == S_T is allowed (each unit reads its S0 before writing S_T).
+ *   - efla_last_error() gives a human-readable reason for the most recent
+ *     failing call on the calling host thread.
+ */
+#ifndef EFLA_H
+#define EFLA_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define EFLA_ABI_VERSION 1
+
+typedef enum {
+    EFLA_OK = 0,
+    EFLA_ERR_INVALID_ARG = 1,     /* null/misaligned pointer, bad size, bad cu_seqlens shape */
+    EFLA_ERR_UNSUPPORTED = 2,     /* valid but not implemented (e.g. d_k not in {32,64,128}) */
+    EFLA_ERR_CUDA = 3,            /* a CUDA runtime/driver call or a launch failed */
+    EFLA_ERR_DEVICE_TIMEOUT = 4   /* a bounded in-kernel wait expired (device status word) */
+} efla_status;
+
+typedef enum {
+    EFLA_BF16 = 0,
+    EFLA_F32 = 1
+} efla_dtype;
+
+/* Same object as cudaStream_t; kept opaque so that this header needs no CUDA header. */
+typedef struct CUstream_st *efla_stream_t;
+
+/*
+ * efla_fwd_chunked -- EFLA forward over whole sequences, chunkwise (WY/UT form).
+ *
+ * Defined by: the update rule and read-out above, evaluated in chunks of
+ * `chunk` tokens with the WY/UT representation of the products of rank-1
+ * updates ("Exact Flow Linear Attention" (gist.science), Metodologia 3;
+ * "Error-Free Linear Attention is a Free Lunch" (howistudyai), Step 4).
+ * The result equals the token-by-token recurrence up to rounding.
+ *
+ *   q, k     [B, T, H, d_k]  in_dtype
+ *   v        [B, T, H, d_v]  in_dtype
+ *   beta     [B, T, H]       fp32, the per-token step size beta_t (any finite value)
+ *   S0       [N, H, d_k, d_v] fp32 (d_v contiguous) initial states, or NULL for zeros
+ *   cu_seqlens [N+1] int32 DEVICE array, or NULL.
+ *            NULL: N must equal B; sequence b is row b, length T.
+ *            non-NULL: B must be 1; sequence n covers packed tokens
+ *            cu_seqlens[n] .. cu_seqlens[n+1]-1 of T; cu_seqlens[0] = 0,
+ *            cu_seqlens[N] = T, non-decreasing (the caller guarantees this;
+ *            it is not read on the host).  Sequences are independent.
+ *   o        [B, T, H, d_v]  o_dtype (EFLA_F32 or EFLA_BF16); every token row written
+ *   S_T      [N, H, d_k, d_v] fp32 final states, or NULL (not written)
+ *   chunk    chunk length; 64 (0 selects 64)
+ *
+ * State and all accumulation are fp32.  Supported: d_k, d_v in {32, 64, 128}.
+ * bf16 inputs with d_k = d_v = 128 run on the tcgen05 tensor-core chunk
+ * kernel; other supported shapes and fp32 inputs run on a CUDA-core fp32
+ * kernel.  T = 0 or N = 0 is valid (S_T = S0 or zeros is written).
+ */
+efla_status efla_fwd_chunked(const void *q, const void *k, const void *v, const float *beta,
+                             const float *S0, const int32_t *cu_seqlens, void *o, float *S_T,
+                             int B, int T, int H, int d_k, int d_v, int N,
+                             efla_dtype in_dtype, efla_dtype o_dtype, int chunk,
+                             efla_stream_t stream);
+
+/*
+ * efla_fwd_recurrent -- the same forward, evaluated token by token on CUDA
+ * cores in fp32 (howistudyai, "Putting it all together (pipeline)": for each
+ * token compute lambda and alpha, update S, emit o).  Same arguments and
+ * layouts as efla_fwd_chunked without `chunk`.  Used for fp32 inputs and as an
+ * independent GPU evaluation of the recurrence.
+ */
+efla_status efla_fwd_recurrent(const void *q, const void *k, const void *v, const float *beta,
+                               const float *S0, const int32_t *cu_seqlens, void *o, float *S_T,
+                               int B, int T, int H, int d_k, int d_v, int N,
+                               efla_dtype in_dtype, efla_dtype o_dtype, efla_stream_t stream);
+
+/*
+ * efla_decode_step -- one token per sequence, state updated IN PLACE.
+ *
+ * Defined by: one application of the update rule and read-out above
+ * ("Exact Flow Linear Attention" (gist.science), Metodologia 3;
+ *  "Error-Free Linear Attention is a Free Lunch" (howistudyai), Steps 1-3).
+ * Evaluated in one pass over S using o = S^T q + (q.k) u with
+ * u = alpha (v - S^T k), which equals S_t^T q after S_t = S + k u^T.
+ *
+ *   q, k  [B, H, d_k] in_dtype;  v [B, H, d_v] in_dtype;  beta [B, H] fp32
+ *   S     [B, H, d_k, d_v] fp32, read and overwritten with the new state
+ *   o     [B, H, d_v] o_dtype
+ * Supported: d_k, d_v in {32, 64, 128}.
+ */
+efla_status efla_decode_step(const void *q, const void *k, const void *v, const float *beta,
+                             float *S, void *o, int B, int H, int d_k, int d_v,
+                             efla_dtype in_dtype, efla_dtype o_dtype, efla_stream_t stream);
+
+/* Reads the library's device status word on `stream` (synchronising that
+ * stream), resets it to EFLA_OK and returns what it held. */
+efla_status efla_device_status(efla_stream_t stream);
+
+/* Static description of a status code; never NULL. */
+const char *efla_status_string(efla_status status);
+
+/* Reason for the most recent failing call on this host thread ("" if none). */
+const char *efla_last_error(void);
+
+/* EFLA_ABI_VERSION of the loaded library. */
+int efla_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EFLA_H */

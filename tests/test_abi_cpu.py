@@ -1,0 +1,144 @@
+"""C-ABI checks that need no GPU: the library loads, exports every symbol the
+header declares, and rejects bad arguments on the host before any launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "efla.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from exact_delta_rule_gb300 import build
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(efla_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("efla_fwd_chunked", "efla_fwd_recurrent", "efla_decode_step", "efla_device_status",
+              "efla_status_string", "efla_last_error", "efla_abi_version"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in efla.h but not exported"
+
+
+def test_abi_version_matches_header(lib):
+    m = re.search(r"#define\s+EFLA_ABI_VERSION\s+(\d+)", open(HEADER).read())
+    lib.efla_abi_version.restype = ctypes.c_int
+    assert lib.efla_abi_version() == int(m.group(1))
+
+
+def test_status_strings(lib):
+    lib.efla_status_string.restype = ctypes.c_char_p
+    lib.efla_status_string.argtypes = [ctypes.c_int]
+    for code, name in enumerate(["EFLA_OK", "EFLA_ERR_INVALID_ARG", "EFLA_ERR_UNSUPPORTED", "EFLA_ERR_CUDA",
+                                 "EFLA_ERR_DEVICE_TIMEOUT"]):
+        assert lib.efla_status_string(code).decode().startswith(name)
+    assert lib.efla_status_string(99)
+
+
+# Fake, never-dereferenced device addresses: validation rejects before any CUDA call.
+Q, K, V, BETA, O, S0, ST, CU = (0x10000000 * (i + 1) for i in range(8))
+
+
+def _fwd(lib, **kw):
+    a = dict(q=Q, k=K, v=V, beta=BETA, S0=None, cu=None, o=O, S_T=None, B=2, T=64, H=4, dk=128, dv=128, N=2,
+             ind=0, od=1, chunk=64, stream=None)
+    a.update(kw)
+    vp, ip = ctypes.c_void_p, ctypes.c_int
+    f = lib.efla_fwd_chunked
+    f.restype = ip
+    f.argtypes = [vp] * 8 + [ip] * 9 + [vp]
+    return f(a["q"], a["k"], a["v"], a["beta"], a["S0"], a["cu"], a["o"], a["S_T"], a["B"], a["T"], a["H"],
+             a["dk"], a["dv"], a["N"], a["ind"], a["od"], a["chunk"], a["stream"])
+
+
+def _last(lib):
+    lib.efla_last_error.restype = ctypes.c_char_p
+    return lib.efla_last_error().decode()
+
+
+INVALID, UNSUPPORTED = 1, 2
+
+
+@pytest.mark.parametrize("kw,code,msg", [
+    (dict(B=-1), INVALID, "bad sizes"),
+    (dict(H=0), INVALID, "bad sizes"),
+    (dict(dk=0), INVALID, "positive"),
+    (dict(dk=48), UNSUPPORTED, "supported head sizes"),
+    (dict(dv=256), UNSUPPORTED, "supported head sizes"),
+    (dict(chunk=32), UNSUPPORTED, "chunk"),
+    (dict(ind=7), INVALID, "dtype"),
+    (dict(N=3), INVALID, "must equal B"),
+    (dict(cu=CU, B=2), INVALID, "must be 1"),
+    (dict(q=None), INVALID, "non-NULL"),
+    (dict(beta=None), INVALID, "non-NULL"),
+    (dict(k=K + 8), INVALID, "aligned"),
+    (dict(S0=S0 + 4), INVALID, "aligned"),
+    (dict(o=Q + 1024), INVALID, "overlaps"),
+    (dict(S_T=O + 64), INVALID, "overlaps"),
+    (dict(T=1 << 30), UNSUPPORTED, "exceeds"),
+])
+def test_fwd_rejects(lib, kw, code, msg):
+    assert _fwd(lib, **kw) == code
+    assert msg in _last(lib)
+
+
+def test_fwd_recurrent_rejects(lib):
+    vp, ip = ctypes.c_void_p, ctypes.c_int
+    f = lib.efla_fwd_recurrent
+    f.restype = ip
+    f.argtypes = [vp] * 8 + [ip] * 8 + [vp]
+    assert f(Q, K, V, BETA, None, None, O, None, 2, 64, 4, 128, 96, 2, 0, 1, None) == UNSUPPORTED
+    assert f(None, K, V, BETA, None, None, O, None, 2, 64, 4, 128, 128, 2, 0, 1, None) == INVALID
+
+
+def _dec(lib, **kw):
+    a = dict(q=Q, k=K, v=V, beta=BETA, S=S0, o=O, B=4, H=2, dk=128, dv=128, ind=0, od=1, stream=None)
+    a.update(kw)
+    vp, ip = ctypes.c_void_p, ctypes.c_int
+    f = lib.efla_decode_step
+    f.restype = ip
+    f.argtypes = [vp] * 6 + [ip] * 6 + [vp]
+    return f(a["q"], a["k"], a["v"], a["beta"], a["S"], a["o"], a["B"], a["H"], a["dk"], a["dv"], a["ind"],
+             a["od"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(B=-2), INVALID), (dict(H=0), INVALID), (dict(dk=16), UNSUPPORTED), (dict(dv=100), UNSUPPORTED),
+    (dict(S=None), INVALID), (dict(S=S0 + 8), INVALID), (dict(o=S0 + 4096), INVALID), (dict(od=5), INVALID),
+])
+def test_decode_rejects(lib, kw, code):
+    assert _dec(lib, **kw) == code
+    assert _last(lib)
+
+
+def test_product_package_does_not_touch_the_oracle():
+    pkg = os.path.join(ROOT, "exact_delta_rule_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"\boracle\b", text), f"{f} mentions the oracle"
+                assert "efla_oracle" not in text
+
+
+def test_binding_raises_without_library(tmp_path, monkeypatch):
+    import exact_delta_rule_gb300 as efla
+    monkeypatch.setattr(efla, "lib_path", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(efla, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        efla.load()
