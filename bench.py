@@ -1,0 +1,411 @@
+#!/usr/bin/env python
+"""Benchmark of the EFLA chunked forward (and decode step) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one efla_fwd_chunked call over the language-model-layer workload
+(B=8, H=16, T=2048, d_k=d_v=128, bf16 q/k/v, fp32 beta, S0 = 0, fp32 o and
+S_T, chunk 64) with inputs resident in HBM.  L2 is flushed (a 512 MiB write)
+before every timed step; each step is bracketed by CUDA events on the
+launching stream.  Prints ONE JSON line on rank 0.
+
+Under torchrun (N > 1) every rank runs an independent replica of the workload
+(the (sequence, head) units are independent, no collective is needed); value =
+tokens of all ranks / max-over-ranks time.
+
+--impl reference times the fp64 CPU oracle on the host cores (rank 0 only) on
+a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "EFLA chunked fwd tokens/s & TFLOP/s (H16 d128 T2048), % roofline; decode GB/s"
+WORKLOAD = "lm"
+CHUNK = 64
+
+
+def flops_per_token_head(dk: int, dv: int, C: int = CHUNK) -> float:
+    """Algorithmic flop count per token-head: 6 d_k d_v (state products) +
+    3 C d_k + 2 C d_v (intra-chunk products) + C^2/3 (triangular inverse)."""
+    return 6 * dk * dv + 3 * C * dk + 2 * C * dv + C * C / 3.0
+
+
+def fwd_bytes(B, T, H, dk, dv, N, in_bytes=2, o_bytes=4, s0=False, s_t=True) -> int:
+    """Algorithmic bytes: every input read once, every output written once."""
+    th = B * T * H
+    b = th * (2 * dk * in_bytes + dv * in_bytes + 4 + dv * o_bytes)
+    st = N * H * dk * dv * 4
+    return b + (st if s0 else 0) + (st if s_t else 0)
+
+
+def decode_bytes(B, H, dk, dv, in_bytes=2, o_bytes=4) -> int:
+    u = B * H
+    return u * ((2 * dk + dv) * in_bytes + 4 + dv * o_bytes + 2 * dk * dv * 4)
+
+
+def read_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"], "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+
+
+def profile_traffic(kernel_tag: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current source of the kernel (else None)."""
+    path = os.path.join(ROOT, "profiles", f"{kernel_tag}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_b = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    m_s = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+    m_f = re.search(r"source_file:\s*(\S+)", text)
+    if not (m_b and m_s and m_f):
+        return None
+    src = os.path.join(ROOT, m_f.group(1))
+    if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest() != m_s.group(1):
+        return None
+    return float(m_b.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"efla_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[3]) if v.lower() == "active"})
+        loaded = [r for r in rows if r[2] > 200.0] or rows
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "power_w_max": max(r[2] for r in rows), "samples": len(rows), "reasons": reasons}
+
+
+def dist_init():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def oracle_sample(inp, units, threads):
+    """Time the fp64 oracle on a list of (b, h) units of a fixed-length workload."""
+    import oracle
+    q, k, v, beta = inp["q"], inp["k"], inp["v"], inp["beta"]
+    bs = sorted({b for b, _ in units})
+    hs = sorted({h for _, h in units})
+    # contiguous fp64 copies of the sampled rows/heads (not timed)
+    sub = [x[bs][:, :, hs].double().numpy() for x in (q, k, v)]
+    sb = beta[bs][:, :, hs].double().numpy()
+    t0 = time.perf_counter()
+    oracle.fwd(sub[0], sub[1], sub[2], sb, None, threads=threads)
+    dt = time.perf_counter() - t0
+    return dt, len(bs) * len(hs) * q.shape[1]
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    import oracle
+    import workloads
+    cfg = workloads.FWD_WORKLOADS[WORKLOAD]
+    inp = workloads.make_fwd_inputs(cfg)
+    cores = os.cpu_count() or 1
+    oracle.build()
+    # each step: 2 batch rows x 8 heads = 16 (b, h) units = 32768 token-heads
+    units = [(b, h) for b in (0, 1) for h in range(8)]
+    for _ in range(args.warmup):
+        oracle_sample(inp, units[:cores] if len(units) > cores else units, cores)
+    times, toks = [], 0
+    for _ in range(args.steps):
+        dt, n = oracle_sample(inp, units, cores)
+        times.append(dt)
+        toks += n
+    total = sum(times)
+    value = toks / total / cfg.H  # tokens/s: a token is one position of all H heads
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{WORKLOAD}: EFLA forward B8 H16 T2048 d128 (sample: 16 (b,h) units per step)",
+                   "sample_units_per_step": len(units)},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": "16 (batch row, head) units x 2048 tokens per step, fp64 C oracle, "
+                                   "OpenMP over units"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, world, rank, local):
+    import torch
+
+    import exact_delta_rule_gb300 as efla
+    import workloads
+    from exact_delta_rule_gb300 import build as libbuild
+
+    libbuild.build()
+    efla.load()
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    cfg = workloads.FWD_WORKLOADS[WORKLOAD]
+    inp = workloads.make_fwd_inputs(cfg)
+    B, T, H, dk, dv, N = inp["B"], inp["T"], inp["H"], cfg.dk, cfg.dv, inp["N"]
+    q, k, v, beta = (inp[x].to(dev) for x in ("q", "k", "v", "beta"))
+    o = torch.empty((B, T, H, dv), dtype=torch.float32, device=dev)
+    S_T = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        efla.fwd_chunked(q, k, v, beta, None, None, o=o, S_T=S_T, chunk=CHUNK, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if efla.device_status() != 0:
+        raise RuntimeError("device status word set during warm-up")
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for i in range(args.steps):
+            flush.fill_(float(i))
+            evs[i][0].record(stream)
+            step()
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    per_step = [a.elapsed_time(b) / 1e3 for a, b in evs]
+    t_local = sum(per_step)
+    t_max = max_over_ranks(t_local, world)
+    tokens = B * T * H  # token-heads per step
+    value = world * tokens * args.steps / t_max / H  # tokens/s (a token = one position of all H heads)
+    ms_per_step = 1e3 * t_max / args.steps
+
+    peaks = read_peaks()
+    nbytes = fwd_bytes(B, T, H, dk, dv, N)
+    avg = t_local / args.steps
+    achieved_gbs = nbytes / avg / 1e9
+    flops = flops_per_token_head(dk, dv) * tokens
+    traffic = profile_traffic("chunk_tc_lm")
+
+    # ---- end to end through host buffers (pinned), copies inside the timed region
+    hq, hk, hv, hb = (x.cpu().pin_memory() for x in (inp["q"], inp["k"], inp["v"], inp["beta"]))
+    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    hs = torch.empty(S_T.shape, dtype=S_T.dtype).pin_memory()
+    dq, dk_, dv_, db = (torch.empty_like(x) for x in (q, k, v, beta))
+    e_steps = max(3, min(args.steps, 10))
+
+    def e2e_step():
+        dq.copy_(hq, non_blocking=True)
+        dk_.copy_(hk, non_blocking=True)
+        dv_.copy_(hv, non_blocking=True)
+        db.copy_(hb, non_blocking=True)
+        efla.fwd_chunked(dq, dk_, dv_, db, None, None, o=o, S_T=S_T, chunk=CHUNK, stream=stream)
+        ho.copy_(o, non_blocking=True)
+        hs.copy_(S_T, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t_e2e = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hb))
+    d2h = ho.numel() * ho.element_size() + hs.numel() * hs.element_size()
+
+    # ---- decode step (secondary figure): B256 H32 d128, CUDA graph of chained steps
+    dec = decode_figures(efla, dev, stream)
+
+    # ---- CPU baseline: the oracle on a bounded sample of the same workload
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(inp)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16",
+            "precision": "bf16 inputs; tensor-core operands split into bf16 hi+lo; fp32 state, accumulation and o",
+            "data": "synthetic",
+            "config": {"workload": "lm: EFLA chunked forward B=8 H=16 T=2048 d_k=d_v=128, bf16 q,k,v, fp32 beta, "
+                                   "S0=0, o fp32, S_T fp32, chunk 64",
+                       "B": B, "T": T, "H": H, "d_k": dk, "d_v": dv, "chunk": CHUNK,
+                       "l2": "flushed (512 MiB write) before every timed step",
+                       "parallelism": f"replicas x{world}"},
+            "token_heads_per_s": world * tokens * args.steps / t_max,
+            "tflops": flops / avg / 1e12,
+            "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": traffic,
+                         "algorithmic_bytes_per_launch": nbytes,
+                         "peak_source": f"{peaks['source']} hbm_gbs (copy burst)",
+                         "kernel": "efla chunk kernel (one launch per step)",
+                         "t_roof_us": 1e6 * max(nbytes / (peaks["hbm_gbs"] * 1e9),
+                                                flops / (peaks["bf16_tflops"] * 1e12))},
+            "e2e": {"value": world * tokens * e_steps / t_e2e / H, "unit": "tokens/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e_steps},
+            "gpu_launches": args.steps,
+            "clocks": clk.summary(),
+            "decode": dec,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def decode_figures(efla, dev, stream):
+    import torch
+
+    import workloads
+    cfg = workloads.DECODE
+    S = workloads.make_decode_state(cfg).to(dev)
+    pool = 8
+    steps = [workloads.make_decode_step(i, cfg) for i in range(pool)]
+    ins = [[s[x].to(dev) for x in ("q", "k", "v", "beta")] for s in steps]
+    o = torch.empty((cfg.B, cfg.H, cfg.dv), dtype=torch.float32, device=dev)
+    n_graph = 100
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        for i in range(3):
+            efla.decode_step(*ins[i % pool], S, o=o, stream=side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        for i in range(n_graph):
+            efla.decode_step(*ins[i % pool], S, o=o, stream=side)
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 5
+    e0.record()
+    for _ in range(reps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    t = e0.elapsed_time(e1) / 1e3 / (reps * n_graph)
+    nbytes = decode_bytes(cfg.B, cfg.H, cfg.dk, cfg.dv)
+    peaks = read_peaks()
+    return {"workload": "decode: B=256 H=32 d=128 bf16 q,k,v, fp32 S in place, o fp32; CUDA graph of 100 "
+                        "chained steps (inputs cycled from 8 seeded steps); S (512 MiB) exceeds L2",
+            "us_per_step": 1e6 * t, "GB/s": nbytes / t / 1e9, "bytes_per_step": nbytes,
+            "frac_hbm": nbytes / t / 1e9 / peaks["hbm_gbs"], "gpu_launches": reps * n_graph}
+
+
+def cpu_baseline(inp):
+    import oracle
+    oracle.build()
+    cores = os.cpu_count() or 1
+    units = [(b, h) for b in range(8) for h in range(16)]
+    dt, th = oracle_sample(inp, units, cores)
+    return {"value": th / dt / 16, "unit": "tokens/s", "token_heads_per_s": th / dt,
+            "cores": cores, "kind": "oracle",
+            "sample": f"all {len(units)} (batch row, head) units x 2048 tokens of one lm step, fp64 C oracle, "
+                      f"OpenMP over units", "seconds": dt}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world, rank, local = dist_init()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
