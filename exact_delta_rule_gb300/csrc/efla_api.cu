@@ -91,9 +91,11 @@ efla_status validate_fwd(const FwdArgs &a, bool chunked) {
     return EFLA_OK;
 }
 
-efla_status run_fwd(const FwdArgs &a, bool chunked) {
+efla_status run_fwd(FwdArgs a, bool chunked) {
     efla_status s = validate_fwd(a, chunked);
     if (s != EFLA_OK) return s;
+    a.status = device_status_ptr();
+    if (!a.status) return fail(EFLA_ERR_CUDA, "cannot resolve the device status word");
     cudaError_t e;
     if (chunked && a.in_dtype == EFLA_BF16 && a.dk == 128 && a.dv == 128) {
         const char *why = nullptr;

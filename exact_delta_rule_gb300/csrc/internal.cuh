@@ -25,6 +25,7 @@ struct FwdArgs {
     efla_dtype in_dtype, o_dtype;
     int chunk;
     cudaStream_t stream;
+    int *status;  // library device status word
 };
 
 struct DecodeArgs {

@@ -136,6 +136,10 @@ __global__ void __launch_bounds__(128) recurrent_kernel(FwdArgs a) {
         b = 0;
         t0 = a.cu_seqlens[n];
         t1 = a.cu_seqlens[n + 1];
+        if (t0 < 0 || t1 < t0 || t1 > a.T) {  // malformed bounds: flag and touch nothing
+            if (lane == 0) atomicExch(a.status, (int)EFLA_ERR_INVALID_ARG);
+            return;
+        }
     } else {
         b = n;
         t0 = 0;
