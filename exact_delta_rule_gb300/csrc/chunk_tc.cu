@@ -5,12 +5,12 @@
 // "Error-Free Linear Attention is a Free Lunch" (howistudyai), Steps 1-4) is
 // evaluated in chunks of C = 64 tokens with the WY/UT representation of the
 // product of the chunk's rank-1 updates.  For one chunk with start state S
-// (d_k x d_v, fp32), keys K, queries Q, values V (C x d), and per-row
+// (d_k x d_v, fp32), keys K, queries Q, values V (C x d), and per row
 //   lambda_t = ||k_t||^2,  n_t = sqrt(lambda_t),  gamma_t = 1 - e^{-beta_t lambda_t}
-//   (gamma_t = alpha_t lambda_t; computed as -expm1(-beta_t lambda_t)):
+//   (gamma_t = alpha_t lambda_t, computed as -expm1(-beta_t lambda_t)):
 //
 //   A~  = strictly-lower( gamma_t (k_t . k_s) / (n_t n_s) )        (C x C)
-//   T~  = (I + A~)^{-1}                                            (forward substitution)
+//   T~  = (I + A~)^{-1}                                            (blocked forward substitution)
 //   T'  = T~ diag(gamma / n)
 //   U^  = T' (V - K S)            u_t = U^_t / n_t   (= the rank-1 write u_t of token t)
 //   O   = Q S + (Q K^T o M) u     (M lower-triangular INCLUDING the diagonal:
@@ -30,17 +30,23 @@
 // sequence; T~ is computed in fp32 on the CUDA cores.
 //
 // Orientation: everything that involves the state is computed transposed, so
-// that the state's d_v index is the MMA row (TMEM lane) and every operand is
-// written by the thread that owns that lane:
+// that the state's d_v index is the MMA row (TMEM lane) and the operands S^T,
+// (V - X)^T and u^T are written into TMEM by the thread that owns the lane and
+// read from there by the tensor core:
 //   [X^T | O1^T] = S^T [K ; Q]^T     (M = d_v = 128, N = 2C = 128, K = d_k = 128)
-//   U^T          = (V - X)^T T'^T    (M = 128, N = C, K = C)
+//   U^^T         = (V - X)^T T'^T    (M = 128, N = C, K = C)
 //   O^T         += u^T P^T,  P = Q K^T o M   (M = 128, N = C, K = C)
 //   S^T         += u^T K             (M = 128, N = d_k = 128, K = C; K as MN-major operand)
-// plus G = [K ; Q] K^T (M = 2C = 128, N = C, K = d_k) for the chunk-local Gram terms.
+// and G = [K ; Q] K^T (M = 2C = 128, N = C, K = d_k) gives the chunk's Gram terms.
 //
-// One CTA of 128 threads (one warpgroup) per (sequence, head); thread j owns
-// TMEM lane j.  K and Q tiles arrive by TMA (128B swizzle) double-buffered, the
-// next chunk's load in flight while the current chunk is processed.
+// One CTA of two warpgroups per (sequence, head):
+//   state warpgroup (threads 0-127): thread j owns TMEM lane j (column j of S);
+//     runs the per-chunk dependency chain above and writes o with TMA stores.
+//   prep warpgroup (threads 128-255): loads K, Q, V by TMA (two stages), forms
+//     the Gram products, the gate terms, T' and P for the NEXT chunk while the
+//     state warpgroup works on the current one.
+// Every wait is bounded; on expiry the CTA records EFLA_ERR_DEVICE_TIMEOUT and
+// leaves.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -56,36 +62,43 @@ constexpr int C = 64;
 constexpr int D = 128;
 
 // Shared memory map (bytes from a 1024-byte aligned base).
-constexpr uint32_t OFF_KQ = 0;             // 2 stages x [2 col blocks][128 rows][64] bf16; rows 0-63 K, 64-127 Q
-constexpr uint32_t KQ_STAGE = 32768;
-constexpr uint32_t OFF_ST_HI = 65536;      // S^T hi  [2][128 j][64 i]
-constexpr uint32_t OFF_ST_LO = 98304;      // S^T lo
-constexpr uint32_t OFF_RU_HI = 131072;     // (V - X)^T, then u^T, hi  [128 j][64 t]
-constexpr uint32_t OFF_RU_LO = 147456;
-constexpr uint32_t OFF_TP_HI = 163840;     // T' hi [64 t][64 s]
-constexpr uint32_t OFF_TP_LO = 172032;
-constexpr uint32_t OFF_P_HI = 180224;      // P hi [64 t][64 s]
-constexpr uint32_t OFF_P_LO = 188416;
-constexpr uint32_t OFF_AT = 196608;        // fp32 A~ rows split by column parity: [2][64 t][32]
-constexpr uint32_t OFF_ROW = 212992;       // fp32 beta[64], gamma[64], inv_n[64], gn[64]
-constexpr uint32_t OFF_BAR = 214016;       // mbarriers: tma[2], mma
-constexpr uint32_t OFF_MISC = 214048;      // tmem base (u32), abort flag (i32)
-constexpr uint32_t SMEM_ALLOC = 214064 + 1024;
+constexpr uint32_t STAGE_BYTES = 49152;    // [K;Q] [2 cb][128 rows][64] (32 KB) + V [2 cb][64 rows][64] (16 KB)
+constexpr uint32_t OFF_STAGE = 0;          // 2 stages
+constexpr uint32_t OFF_V = 32768;          // within a stage
+constexpr uint32_t OFF_TP = 98304;         // 2 buffers x {hi 8 KB, lo 8 KB}: T' [64 t][64 s]
+constexpr uint32_t OFF_P = 131072;         // 2 buffers x {hi, lo}: P [64 t][64 s]
+constexpr uint32_t OFF_OST = 163840;       // o staging for the TMA store, 32 KB
+constexpr uint32_t OFF_AT = 196608;        // fp32 [64][65]: A~, then T~ in place
+constexpr uint32_t AT_LD = 65;
+constexpr uint32_t OFF_ROW = OFF_AT + 64 * AT_LD * 4;  // fp32: invn[2][64], gn[2][64], beta[64], gam[64]
+constexpr uint32_t ROW_BYTES = 6 * 64 * 4;
+constexpr uint32_t OFF_BAR = OFF_ROW + ROW_BYTES;       // mbarriers (struct Bars)
+constexpr uint32_t OFF_MISC = OFF_BAR + 64;             // tmem base (u32), abort flag (i32)
+constexpr uint32_t SMEM_USED = OFF_MISC + 16;
+constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;       // + alignment slack for the 1024-byte base
+static_assert(OFF_TP == 2 * STAGE_BYTES && OFF_P == OFF_TP + 32768 && OFF_OST == OFF_P + 32768 &&
+                  OFF_AT == OFF_OST + 32768,
+              "shared memory regions must not overlap");
+static_assert(SMEM_ALLOC <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
 
-// TMEM columns (fp32, lane = row of the MMA result)
-constexpr uint32_t TM_S = 0;    // S^T            128 columns
-constexpr uint32_t TM_X = 128;  // X^T = (K S)^T   64 columns
-constexpr uint32_t TM_O = 192;  // O^T             64 columns
-constexpr uint32_t TM_U = 256;  // U^^T            64 columns
-constexpr uint32_t TM_G = 320;  // [K;Q] K^T       64 columns
+// TMEM columns (32-bit; lane = row of the MMA result)
+constexpr uint32_t TM_S = 0;    // S^T fp32                        128 columns
+constexpr uint32_t TM_SA = 128; // S^T as bf16 operand: hi 64, lo 64 columns
+constexpr uint32_t TM_X = 256;  // X^T fp32 (64), then (V-X)^T bf16 hi 32 + lo 32
+constexpr uint32_t TM_O = 320;  // O^T fp32                         64 columns
+constexpr uint32_t TM_U = 384;  // U^^T fp32 (64), then u^T bf16 hi 32 + lo 32
+constexpr uint32_t TM_G = 448;  // [K;Q] K^T fp32                   64 columns
 constexpr uint32_t TM_COLS = 512;
 
 constexpr uint64_t WAIT_NS = 2000000000ull;  // 2 s bound on any wait
 
+constexpr int BAR_STATE = 1, BAR_PREP = 2;  // named barriers (128 threads each)
+
 struct TcParams {
     CUtensorMap map_q;
     CUtensorMap map_k;
-    const __nv_bfloat16 *v;
+    CUtensorMap map_v;
+    CUtensorMap map_o;
     const float *beta;
     const float *S0;
     const int32_t *cu_seqlens;
@@ -95,32 +108,57 @@ struct TcParams {
     int B, T, H, N;
 };
 
-__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
-    const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(a));
-    const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(b));
-    return lo | (hi << 16);
+struct Bars {
+    uint64_t tma_full[2];
+    uint64_t g_done;
+    uint64_t state_mma;
+    uint64_t prep_ready[2];
+    uint64_t chunk_done[2];
+};
+static_assert(sizeof(Bars) <= 64, "mbarrier block exceeds its slot");
+
+// Bounded wait that also gives up when the other warpgroup has aborted.
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > WAIT_NS) {
+            *abort_flag = 1;
+            return false;
+        }
+    }
 }
 
-// Splits x into bf16 hi + lo (x ~= hi + lo to ~2^-17 relative).
-__device__ __forceinline__ void split_bf16(float x, float &hi, float &lo) {
-    hi = __bfloat162float(__float2bfloat16_rn(x));
-    lo = x - hi;
+__device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
 }
 
-// Writes 64 fp32 values of one row as bf16 hi/lo into two 128B-swizzled tiles
-// (row `row`, columns col0..col0+63; blocks of 64 columns `block` bytes apart).
-__device__ __forceinline__ void store_row_split(uint8_t *hi_tile, uint8_t *lo_tile, int row, int col0,
-                                                uint32_t block, const float *x) {
+// Splits pairs x[2c], x[2c+1] into packed bf16 hi and lo words (x ~= hi + lo).
+template <int NP>
+__device__ __forceinline__ void split_pack(const float *x, uint32_t *hi, uint32_t *lo) {
+#pragma unroll
+    for (int c = 0; c < NP; ++c) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(x[2 * c], x[2 * c + 1]);
+        const float2 hf = __bfloat1622float2(h);
+        hi[c] = *reinterpret_cast<uint32_t *>(&h);
+        lo[c] = bf16x2_bits(x[2 * c] - hf.x, x[2 * c + 1] - hf.y);
+    }
+}
+
+// Writes 64 fp32 values of one row as bf16 hi/lo into two 128B-swizzled tiles.
+__device__ __forceinline__ void store_row_split(uint8_t *hi_tile, uint8_t *lo_tile, int row, const float *x) {
 #pragma unroll
     for (int c = 0; c < 64; c += 8) {
-        float h[8], l[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) split_bf16(x[c + e], h[e], l[e]);
-        const uint32_t off = swz_offset(row, col0 + c, block);
-        *reinterpret_cast<uint4 *>(hi_tile + off) =
-            make_uint4(pack_bf16(h[0], h[1]), pack_bf16(h[2], h[3]), pack_bf16(h[4], h[5]), pack_bf16(h[6], h[7]));
-        *reinterpret_cast<uint4 *>(lo_tile + off) =
-            make_uint4(pack_bf16(l[0], l[1]), pack_bf16(l[2], l[3]), pack_bf16(l[4], l[5]), pack_bf16(l[6], l[7]));
+        uint32_t h[4], l[4];
+        split_pack<4>(x + c, h, l);
+        const uint32_t off = swz_offset(row, c, 8192);
+        *reinterpret_cast<uint4 *>(hi_tile + off) = make_uint4(h[0], h[1], h[2], h[3]);
+        *reinterpret_cast<uint4 *>(lo_tile + off) = make_uint4(l[0], l[1], l[2], l[3]);
     }
 }
 
@@ -136,28 +174,102 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&r)[64]) {
     }
 }
 
-// All threads: CTA barrier with the tcgen05 ordering fences around it.
-__device__ __forceinline__ void cta_sync_tc() {
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
+__device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t (&u)[32]) {
+    tmem_st32(taddr, reinterpret_cast<const float(&)[32]>(u));
+}
+
+// T~ = (I + A~)^{-1} in place in At (fp32, row stride AT_LD), with 128 threads.
+// Diagonal 16x16 blocks by column substitution, then the blocks below them row
+// block by row block: T~_IJ = -T~_II sum_{M=J}^{I-1} A~_IM T~_MJ.
+__device__ __forceinline__ void invert_unit_lower(float *At, int pt) {
+    const int lane = pt & 31, pw = pt >> 5;
+    {  // diagonal block pw, column `lane` (lanes 0-15)
+        const int B0 = pw * 16, c = lane & 15;
+        float col[16];
+#pragma unroll
+        for (int s = 0; s < 16; ++s) col[s] = (s == c) ? 1.f : 0.f;
+#pragma unroll
+        for (int t = 1; t < 16; ++t) {
+            float acc = 0.f;
+            const float *row = At + (B0 + t) * AT_LD + B0;
+#pragma unroll
+            for (int s = 0; s < t; ++s) acc = fmaf(row[s], col[s], acc);
+            if (t > c) col[t] = -acc;
+        }
+        __syncwarp();
+        if (lane < 16) {
+#pragma unroll
+            for (int s = 0; s < 16; ++s) At[(B0 + s) * AT_LD + B0 + c] = col[s];
+        }
+    }
+    named_bar(BAR_PREP, 128);
+#pragma unroll 1
+    for (int I = 1; I < 4; ++I) {
+        const int cid = pt >> 1, h = pt & 1;
+        const bool active = cid < 16 * I;
+        const int J = cid >> 4, c = cid & 15;
+        float y[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) y[r] = 0.f;
+        if (active) {
+#pragma unroll 1
+            for (int M = J; M < I; ++M) {
+                float tcol[16];
+#pragma unroll
+                for (int k = 0; k < 16; ++k) tcol[k] = At[(16 * M + k) * AT_LD + 16 * J + c];
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    const float *arow = At + (16 * I + 8 * h + r) * AT_LD + 16 * M;
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) y[r] = fmaf(arow[k], tcol[k], y[r]);
+                }
+            }
+        }
+        // the full column of Y is split between this thread (rows 8h..8h+7) and its partner
+        float yo[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) yo[r] = __shfl_xor_sync(0xffffffffu, y[r], 1);
+        float z[8];
+        if (active) {
+            const float *y0 = h ? yo : y;  // rows 0..7
+            const float *y1 = h ? y : yo;  // rows 8..15
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                const int R = 8 * h + r;
+                const float *trow = At + (16 * I + R) * AT_LD + 16 * I;
+                float acc = 0.f;
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    if (k <= R) acc = fmaf(trow[k], y0[k], acc);
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    if (8 + k <= R) acc = fmaf(trow[8 + k], y1[k], acc);
+                z[r] = -acc;
+            }
+        }
+        named_bar(BAR_PREP, 128);
+        if (active) {
+#pragma unroll
+            for (int r = 0; r < 8; ++r) At[(16 * I + 8 * h + r) * AT_LD + 16 * J + c] = z[r];
+        }
+        named_bar(BAR_PREP, 128);
+    }
 }
 
 template <bool OUT_BF16>
-__global__ void __launch_bounds__(128, 1) chunk_tc_kernel(const __grid_constant__ TcParams p) {
+__global__ void __launch_bounds__(256, 1) chunk_tc_kernel(const __grid_constant__ TcParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    float *row_beta = reinterpret_cast<float *>(sm + OFF_ROW);
-    float *row_gam = row_beta + 64;
-    float *row_invn = row_beta + 128;
-    float *row_gn = row_beta + 192;
+    float *row_invn = reinterpret_cast<float *>(sm + OFF_ROW);  // [2][64]
+    float *row_gn = row_invn + 128;                             // [2][64]
+    float *row_beta = row_invn + 256;                           // [64] (prep only)
+    float *row_gam = row_invn + 320;                            // [64] (prep only)
     float *At = reinterpret_cast<float *>(sm + OFF_AT);
-    uint64_t *bar_tma = reinterpret_cast<uint64_t *>(sm + OFF_BAR);
-    uint64_t *bar_mma = bar_tma + 2;
+    Bars *bars = reinterpret_cast<Bars *>(sm + OFF_BAR);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + OFF_MISC + 4);
 
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tid = threadIdx.x, warp = tid >> 5;
     const int n = blockIdx.x / p.H, h = blockIdx.x % p.H;
     long b, bos, eos;
     if (p.cu_seqlens) {
@@ -165,7 +277,7 @@ __global__ void __launch_bounds__(128, 1) chunk_tc_kernel(const __grid_constant_
         bos = p.cu_seqlens[n];
         eos = p.cu_seqlens[n + 1];
         if (bos < 0 || eos < bos || eos > p.T) {  // malformed bounds: flag and touch nothing
-            if (threadIdx.x == 0) atomicExch(p.status, (int)EFLA_ERR_INVALID_ARG);
+            if (tid == 0) atomicExch(p.status, (int)EFLA_ERR_INVALID_ARG);
             return;
         }
     } else {
@@ -175,18 +287,23 @@ __global__ void __launch_bounds__(128, 1) chunk_tc_kernel(const __grid_constant_
     }
     const int nchunks = eos > bos ? (int)((eos - bos + C - 1) / C) : 0;
     const size_t sbase = ((size_t)n * p.H + h) * D * D;
-    const int j = tid;  // d_v index owned by this thread (TMEM lane)
 
     if (nchunks == 0) {  // empty sequence: S_T = S0
-        if (p.S_T)
-            for (int i = 0; i < D; ++i) p.S_T[sbase + (size_t)i * D + j] = p.S0 ? p.S0[sbase + (size_t)i * D + j] : 0.f;
+        if (p.S_T && tid < D)
+            for (int i = 0; i < D; ++i)
+                p.S_T[sbase + (size_t)i * D + tid] = p.S0 ? p.S0[sbase + (size_t)i * D + tid] : 0.f;
         return;
     }
 
     if (tid == 0) {
-        mbar_init(&bar_tma[0], 1);
-        mbar_init(&bar_tma[1], 1);
-        mbar_init(bar_mma, 1);
+        mbar_init(&bars->tma_full[0], 1);
+        mbar_init(&bars->tma_full[1], 1);
+        mbar_init(&bars->g_done, 1);
+        mbar_init(&bars->state_mma, 1);
+        mbar_init(&bars->prep_ready[0], 1);
+        mbar_init(&bars->prep_ready[1], 1);
+        mbar_init(&bars->chunk_done[0], 1);
+        mbar_init(&bars->chunk_done[1], 1);
         fence_mbar_init();
         *abort_flag = 0;
     }
@@ -194,298 +311,351 @@ __global__ void __launch_bounds__(128, 1) chunk_tc_kernel(const __grid_constant_
         tmem_alloc(tmem_slot, TM_COLS);
         tmem_relinquish();
     }
-    cta_sync_tc();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
     const uint32_t s_sm = smem_u32(sm);
+    const bool varlen = p.cu_seqlens != nullptr;
 
-    auto issue_tma = [&](int c) {
-        const int stage = c & 1;
-        uint8_t *dst = sm + OFF_KQ + stage * KQ_STAGE;
-        const int tok = (int)(bos + (long)c * C);
-        mbar_arrive_expect_tx(&bar_tma[stage], KQ_STAGE);
-        for (int cb = 0; cb < 2; ++cb) {
-            tma_load_4d(dst + cb * 16384, &p.map_k, &bar_tma[stage], cb * 64, h, tok, (int)b);
-            tma_load_4d(dst + cb * 16384 + 8192, &p.map_q, &bar_tma[stage], cb * 64, h, tok, (int)b);
-        }
-    };
-    if (tid == 0) {
-        prefetch_tensormap(&p.map_q);
-        prefetch_tensormap(&p.map_k);
-        issue_tma(0);
-    }
-
-    // Initial state -> TMEM (S^T: lane j holds column j of S).
-    {
-        float r[32];
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-                r[i] = p.S0 ? p.S0[sbase + (size_t)(g * 32 + i) * D + j] : 0.f;
-            tmem_st32(lane_base + TM_S + g * 32, r);
-        }
-        tmem_st_wait();
-    }
-
-    uint32_t mma_phase = 0;
-    bool ok = true;
-    int aborted_at = 0;
-    auto wait_mma = [&]() {
-        if (!mbar_wait(bar_mma, mma_phase, WAIT_NS)) ok = false;
-        mma_phase ^= 1;
-        tc_fence_after();
-    };
-
-    for (int c = 0; c < nchunks; ++c) {
-        const int stage = c & 1;
-        const long tok0 = bos + (long)c * C;
-        const int valid = (int)min((long)C, eos - tok0);
-        uint8_t *KQ = sm + OFF_KQ + stage * KQ_STAGE;
-        const uint32_t kq_s = s_sm + OFF_KQ + stage * KQ_STAGE;
-
-        // (a) values of this chunk for column j (kept as packed bf16 pairs), and the step sizes
-        uint32_t vpk[C / 2];
-        {
-            const unsigned short *vv = reinterpret_cast<const unsigned short *>(p.v);
-#pragma unroll
-            for (int t = 0; t < C; t += 2) {
-                const size_t row = ((size_t)b * p.T + (size_t)(tok0 + t)) * p.H + h;
-                const uint32_t lo = t < valid ? vv[row * D + j] : 0u;
-                const uint32_t hi = t + 1 < valid ? vv[(row + p.H) * D + j] : 0u;
-                vpk[t / 2] = lo | (hi << 16);
+    if (tid >= 128) {
+        // =============================== prep warpgroup ===============================
+        const int pt = tid - 128;
+        const uint32_t lane_base = tmem + ((uint32_t)((warp - 4) * 32) << 16);
+        auto issue_tma = [&](int c) {
+            const int st = c & 1;
+            uint8_t *dst = sm + OFF_STAGE + st * STAGE_BYTES;
+            const int tok = (int)(bos + (long)c * C);
+            mbar_arrive_expect_tx(&bars->tma_full[st], STAGE_BYTES);
+            for (int cb = 0; cb < 2; ++cb) {
+                tma_load_4d(dst + cb * 16384, &p.map_k, &bars->tma_full[st], cb * 64, h, tok, (int)b);
+                tma_load_4d(dst + cb * 16384 + 8192, &p.map_q, &bars->tma_full[st], cb * 64, h, tok, (int)b);
+                tma_load_4d(dst + OFF_V + cb * 8192, &p.map_v, &bars->tma_full[st], cb * 64, h, tok, (int)b);
             }
+        };
+        if (pt == 0) {
+            prefetch_tensormap(&p.map_q);
+            prefetch_tensormap(&p.map_k);
+            prefetch_tensormap(&p.map_v);
+            issue_tma(0);
         }
-        if (tid < C) {
-            const size_t row = ((size_t)b * p.T + (size_t)(tok0 + tid)) * p.H + h;
-            row_beta[tid] = tid < valid ? p.beta[row] : 0.f;
-        }
+        int issued = 1, landed = 0;  // chunks whose TMA was issued / seen complete
+        for (int c = 0; c < nchunks; ++c) {
+            const int st = c & 1, buf = c & 1;
+            const long tok0 = bos + (long)c * C;
+            const int valid = (int)min((long)C, eos - tok0);
+            uint8_t *KQ = sm + OFF_STAGE + st * STAGE_BYTES;
+            const uint32_t kq_s = s_sm + OFF_STAGE + st * STAGE_BYTES;
 
-        // (b) K and Q tiles
-        if (!mbar_wait(&bar_tma[stage], (c >> 1) & 1, WAIT_NS)) ok = false;
-        // (c) rows past the end of the sequence are zeroed (they may hold the next sequence)
-        if (valid < C) {
-            const int rows = C - valid;
-            for (int e = tid; e < 4 * rows * 8; e += 128) {
-                const int ch = e & 7, r = (e >> 3) % rows, part = (e >> 3) / rows;  // part: 0-1 K cb, 2-3 Q cb
-                const int R = valid + r + ((part >> 1) ? 64 : 0), cb = part & 1;
-                *reinterpret_cast<uint4 *>(KQ + cb * 16384 + (R >> 3) * 1024 + (R & 7) * 128 + ch * 16) =
-                    make_uint4(0, 0, 0, 0);
-            }
-            fence_proxy_async_smem();
-        }
-        if (!ok) *abort_flag = 1;
-        cta_sync_tc();
-        if (*abort_flag) {
-            aborted_at = c - 1;
-            break;
-        }
-
-        // (d) next chunk's TMA; Gram MMA G = [K;Q] K^T
-        if (tid == 0) {
-            if (c + 1 < nchunks) issue_tma(c + 1);
-            const uint32_t idesc = idesc_bf16_f32(128, 64, 0, 0);
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-                mma_bf16(tmem + TM_G, smem_desc(kq_s + off, 16, 1024), smem_desc(kq_s + off, 16, 1024), idesc,
-                         ks > 0);
-            }
-            mma_commit(bar_mma);
-        }
-        wait_mma();
-
-        // (e) per-row gate terms, A~ and P
-        {
-            float g[64];
-            tmem_ld64(lane_base + TM_G, g);
-            if (tid < C) {  // raw K K^T row t, parity-split
-#pragma unroll
-                for (int s = 0; s < 64; ++s) At[(s & 1) * 2048 + tid * 32 + (s >> 1)] = g[s];
-            }
-            __syncthreads();
-            if (tid < C) {
-                const int t = tid;
-                const float lam = At[(t & 1) * 2048 + t * 32 + (t >> 1)];
-                const float nrm = sqrtf(lam);
-                const float invn = lam > 0.f ? 1.f / nrm : 0.f;
-                const float gam = lam > 0.f ? -expm1f(-row_beta[t] * lam) : 0.f;
-                row_gam[t] = gam;
-                row_invn[t] = invn;
-                row_gn[t] = gam * invn;
-            }
-            __syncthreads();
-            if (tid < C) {
-                const int t = tid;
-                const float rs = row_gam[t] * row_invn[t];
-#pragma unroll
-                for (int s = 0; s < 64; ++s) {
-                    float* a = &At[(s & 1) * 2048 + t * 32 + (s >> 1)];
-                    *a = s < t ? rs * row_invn[s] * *a : 0.f;
+            if (pt < C) row_beta[pt] = pt < valid ? p.beta[((size_t)b * p.T + (size_t)(tok0 + pt)) * p.H + h] : 0.f;
+            bool ok = wait_bar(&bars->tma_full[st], (c >> 1) & 1, abort_flag);
+            if (ok && valid < C) {  // rows past the end of the sequence are zeroed (they may hold the next one)
+                const int rows = C - valid;
+                for (int e = pt; e < 4 * rows * 8; e += 128) {
+                    const int ch = e & 7, r = (e >> 3) % rows, part = (e >> 3) / rows;
+                    const int R = valid + r + ((part >> 1) ? 64 : 0), cb = part & 1;
+                    *reinterpret_cast<uint4 *>(KQ + cb * 16384 + (R >> 3) * 1024 + (R & 7) * 128 + ch * 16) =
+                        make_uint4(0, 0, 0, 0);
                 }
-            } else {
-                const int t = tid - C;
-#pragma unroll
-                for (int s = 0; s < 64; ++s) g[s] = s <= t ? g[s] : 0.f;
-                store_row_split(sm + OFF_P_HI, sm + OFF_P_LO, t, 0, 8192, g);
+                fence_proxy_async_smem();
             }
-        }
-        __syncthreads();
-
-        // (f) T~ = (I + A~)^{-1}: thread (column cc, parity pp) holds T~[2m+pp][cc]
-        {
-            const int cc = (lane & 15) + 16 * warp;
-            const int pp = lane >> 4;
-            const float *Ap = At + pp * 2048;
-            float col[32];
-#pragma unroll
-            for (int m = 0; m < 32; ++m) col[m] = (2 * m + pp == cc) ? 1.f : 0.f;
-#pragma unroll
-            for (int t = 1; t < C; ++t) {
-                const int mt = (t + 1) / 2;
-                float acc = 0.f;
-                const float *row = Ap + t * 32;
-#pragma unroll
-                for (int m = 0; m < mt; ++m) acc = fmaf(row[m], col[m], acc);
-                const float tot = acc + __shfl_xor_sync(0xffffffffu, acc, 16);
-                if ((t & 1) == pp && t > cc) col[t >> 1] = -tot;
+            if (named_bar_any(BAR_PREP, 128, !ok || *abort_flag)) {
+                *abort_flag = 1;
+                break;
             }
-            // T' = T~ diag(gamma/n): scale column cc, write bf16 hi/lo into the B operand [t][s]
-            const float gs = row_gn[cc];
-#pragma unroll
-            for (int m = 0; m < 32; ++m) {
-                float hi, lo;
-                split_bf16(col[m] * gs, hi, lo);
-                const uint32_t off = swz_offset(2 * m + pp, cc, 8192);
-                *reinterpret_cast<__nv_bfloat16 *>(sm + OFF_TP_HI + off) = __float2bfloat16_rn(hi);
-                *reinterpret_cast<__nv_bfloat16 *>(sm + OFF_TP_LO + off) = __float2bfloat16_rn(lo);
-            }
-        }
+            landed = c + 1;
 
-        // (g) S^T -> bf16 hi/lo operand
-        {
-            float s64[64];
-            tmem_ld64(lane_base + TM_S, s64);
-            store_row_split(sm + OFF_ST_HI, sm + OFF_ST_LO, j, 0, 16384, s64);
-            tmem_ld64(lane_base + TM_S + 64, s64);
-            store_row_split(sm + OFF_ST_HI, sm + OFF_ST_LO, j, 64, 16384, s64);
-        }
-        fence_proxy_async_smem();
-        cta_sync_tc();
-
-        // (h) [X^T | O1^T] = S^T [K;Q]^T
-        if (tid == 0) {
-            const uint32_t idesc = idesc_bf16_f32(128, 128, 0, 0);
-#pragma unroll
-            for (int part = 0; part < 2; ++part) {
-                const uint32_t a_s = s_sm + (part ? OFF_ST_LO : OFF_ST_HI);
+            // Gram products G = [K;Q] K^T
+            if (pt == 0) {
+                tc_fence_after();
+                const uint32_t idesc = idesc_bf16_f32(128, 64, 0, 0);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-                    mma_bf16(tmem + TM_X, smem_desc(a_s + off, 16, 1024), smem_desc(kq_s + off, 16, 1024), idesc,
-                             (part | ks) != 0);
+                    mma_bf16(tmem + TM_G, smem_desc(kq_s + off, 16, 1024), smem_desc(kq_s + off, 16, 1024), idesc,
+                             ks > 0);
+                }
+                mma_commit(&bars->g_done);
+            }
+            ok = wait_bar(&bars->g_done, c & 1, abort_flag);
+            tc_fence_after();
+            {
+                float g[64];
+                tmem_ld64(lane_base + TM_G, g);
+                if (pt < C) {
+#pragma unroll
+                    for (int s = 0; s < 64; ++s) At[pt * AT_LD + s] = g[s];
+                } else {  // P = Q K^T with the inclusive causal mask
+                    const int t = pt - C;
+#pragma unroll
+                    for (int s = 0; s < 64; ++s) g[s] = s <= t ? g[s] : 0.f;
+                    store_row_split(sm + OFF_P + buf * 16384, sm + OFF_P + buf * 16384 + 8192, t, g);
                 }
             }
-            mma_commit(bar_mma);
-        }
-        wait_mma();
-
-        // (i) R^T = V^T - X^T  -> operand; U^^T = R^T T'^T
-        {
-            float x[64];
-            tmem_ld64(lane_base + TM_X, x);
-#pragma unroll
-            for (int t = 0; t < C; t += 2) {
-                x[t] = __uint_as_float(vpk[t / 2] << 16) - x[t];
-                x[t + 1] = __uint_as_float(vpk[t / 2] & 0xffff0000u) - x[t + 1];
+            named_bar(BAR_PREP, 128);
+            if (pt < C) {
+                const int t = pt;
+                const float lam = At[t * AT_LD + t];
+                const bool live = t < valid && lam > 0.f;
+                const float invn = live ? rsqrtf(lam) : 0.f;
+                const float gam = live ? -expm1f(-row_beta[t] * lam) : 0.f;
+                row_gam[t] = gam;
+                row_invn[buf * 64 + t] = invn;
+                row_gn[buf * 64 + t] = gam * invn;
             }
-            store_row_split(sm + OFF_RU_HI, sm + OFF_RU_LO, j, 0, 16384, x);
+            named_bar(BAR_PREP, 128);
+            if (pt < C) {  // A~ row t
+                const int t = pt;
+                const float rs = row_gam[t] * row_invn[buf * 64 + t];
+#pragma unroll
+                for (int s = 0; s < 64; ++s) {
+                    float *a = &At[t * AT_LD + s];
+                    *a = s < t ? rs * row_invn[buf * 64 + s] * *a : 0.f;
+                }
+            }
+            named_bar(BAR_PREP, 128);
+            invert_unit_lower(At, pt);
+            {  // T' = T~ diag(gamma/n), lower triangle, as bf16 hi/lo [t][s]
+                const int t = pt >> 1, s0 = (pt & 1) * 32;
+                uint8_t *hi = sm + OFF_TP + buf * 16384, *lo = hi + 8192;
+#pragma unroll
+                for (int c8 = 0; c8 < 32; c8 += 8) {
+                    float x[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int s = s0 + c8 + e;
+                        x[e] = s <= t ? At[t * AT_LD + s] * row_gn[buf * 64 + s] : 0.f;
+                    }
+                    uint32_t hh[4], ll[4];
+                    split_pack<4>(x, hh, ll);
+                    const uint32_t off = swz_offset(t, s0 + c8, 8192);
+                    *reinterpret_cast<uint4 *>(hi + off) = make_uint4(hh[0], hh[1], hh[2], hh[3]);
+                    *reinterpret_cast<uint4 *>(lo + off) = make_uint4(ll[0], ll[1], ll[2], ll[3]);
+                }
+            }
+            fence_proxy_async_smem();
+            named_bar(BAR_PREP, 128);
+            if (pt == 0) mbar_arrive(&bars->prep_ready[buf]);
+            // the stage and the T'/P buffers of chunk c-1 are free once its state MMAs completed
+            if (c >= 1) ok = wait_bar(&bars->chunk_done[(c - 1) & 1], ((c - 1) >> 1) & 1, abort_flag) && ok;
+            if (named_bar_any(BAR_PREP, 128, !ok || *abort_flag)) {
+                *abort_flag = 1;
+                break;
+            }
+            if (c + 1 < nchunks) {
+                if (pt == 0) issue_tma(c + 1);
+                issued = c + 2;
+            }
         }
-        fence_proxy_async_smem();
-        cta_sync_tc();
-        if (tid == 0) {
-            const uint32_t idesc = idesc_bf16_f32(128, 64, 0, 0);
-            const uint32_t A_[3] = {OFF_RU_HI, OFF_RU_HI, OFF_RU_LO};
-            const uint32_t B_[3] = {OFF_TP_HI, OFF_TP_LO, OFF_TP_HI};
-#pragma unroll
-            for (int part = 0; part < 3; ++part)
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16(tmem + TM_U, smem_desc(s_sm + A_[part] + ks * 32, 16, 1024),
-                             smem_desc(s_sm + B_[part] + ks * 32, 16, 1024), idesc, (part | ks) != 0);
-            mma_commit(bar_mma);
-        }
-        wait_mma();
-
-        // (j) u^T = U^^T diag(1/n) -> operand; O^T += u^T P^T; S^T += u^T K
-        {
-            float u[64];
-            tmem_ld64(lane_base + TM_U, u);
-#pragma unroll
-            for (int t = 0; t < C; ++t) u[t] *= row_invn[t];
-            store_row_split(sm + OFF_RU_HI, sm + OFF_RU_LO, j, 0, 16384, u);
-        }
-        fence_proxy_async_smem();
-        cta_sync_tc();
-        if (tid == 0) {
-            const uint32_t idesc_o = idesc_bf16_f32(128, 64, 0, 0);
-            const uint32_t A_[3] = {OFF_RU_HI, OFF_RU_HI, OFF_RU_LO};
-            const uint32_t B_[3] = {OFF_P_HI, OFF_P_LO, OFF_P_HI};
-#pragma unroll
-            for (int part = 0; part < 3; ++part)
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16(tmem + TM_O, smem_desc(s_sm + A_[part] + ks * 32, 16, 1024),
-                             smem_desc(s_sm + B_[part] + ks * 32, 16, 1024), idesc_o, 1);
-            const uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 1);
-#pragma unroll
-            for (int part = 0; part < 2; ++part)
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16(tmem + TM_S, smem_desc(s_sm + (part ? OFF_RU_LO : OFF_RU_HI) + ks * 32, 16, 1024),
-                             smem_desc(kq_s + ks * 2048, 16384, 1024), idesc_s, 1);
-            mma_commit(bar_mma);
-        }
-        wait_mma();
-
-        // (k) outputs of this chunk
-        {
-            float ov[64];
-            tmem_ld64(lane_base + TM_O, ov);
-#pragma unroll
-            for (int t = 0; t < C; ++t) {
-                if (t < valid) {
-                    const size_t row = ((size_t)b * p.T + (size_t)(tok0 + t)) * p.H + h;
-                    if (OUT_BF16)
-                        static_cast<__nv_bfloat16 *>(p.o)[row * D + j] = __float2bfloat16_rn(ov[t]);
-                    else
-                        static_cast<float *>(p.o)[row * D + j] = ov[t];
+        if (pt == 0) {  // after an abort, let TMA loads still in flight land (bounded)
+            for (int cc = landed; cc < issued; ++cc) {
+                const uint64_t t0 = globaltimer_ns();
+                while (!mbar_try_wait(&bars->tma_full[cc & 1], (cc >> 1) & 1) &&
+                       globaltimer_ns() - t0 < WAIT_NS / 4) {
                 }
             }
         }
-        if (!ok) *abort_flag = 1;
-        cta_sync_tc();
-        if (*abort_flag) {
-            aborted_at = c;
-            break;
+    } else {
+        // =============================== state warpgroup ===============================
+        const int j = tid;
+        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+        {  // initial state -> TMEM (S^T: lane j holds column j of S)
+            float r[32];
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) r[i] = p.S0 ? p.S0[sbase + (size_t)(g * 32 + i) * D + j] : 0.f;
+                tmem_st32(lane_base + TM_S + g * 32, r);
+            }
+            tmem_st_wait();
+        }
+        uint32_t mma_phase = 0;
+        for (int c = 0; c < nchunks; ++c) {
+            const int st = c & 1, buf = c & 1;
+            const long tok0 = bos + (long)c * C;
+            const int valid = (int)min((long)C, eos - tok0);
+            const uint32_t kq_s = s_sm + OFF_STAGE + st * STAGE_BYTES;
+            const uint8_t *Vt = sm + OFF_STAGE + st * STAGE_BYTES + OFF_V;
+
+            bool ok = wait_bar(&bars->prep_ready[buf], (c >> 1) & 1, abort_flag);
+            // S^T -> bf16 hi/lo operand in TMEM
+            {
+                float s[32];
+                uint32_t hi[32], lo[32];
+#pragma unroll
+                for (int g = 0; g < 4; g += 2) {
+                    tmem_ld32(lane_base + TM_S + g * 32, s);
+                    tmem_ld_wait();
+                    split_pack<16>(s, hi, lo);
+                    tmem_ld32(lane_base + TM_S + g * 32 + 32, s);
+                    tmem_ld_wait();
+                    split_pack<16>(s, hi + 16, lo + 16);
+                    tmem_st32u(lane_base + TM_SA + g * 16, hi);
+                    tmem_st32u(lane_base + TM_SA + 64 + g * 16, lo);
+                }
+                tmem_st_wait();
+            }
+            if (j == 0) bulk_wait_read0();  // the o staging of chunk c-1 has been read
+            tc_fence_before();
+            if (named_bar_any(BAR_STATE, 128, !ok || *abort_flag)) {
+                *abort_flag = 1;
+                break;
+            }
+            if (j == 0) {  // [X^T | O1^T] = S^T [K;Q]^T
+                tc_fence_after();
+                const uint32_t idesc = idesc_bf16_f32(128, 128, 0, 0);
+#pragma unroll
+                for (int part = 0; part < 2; ++part)
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+                        mma_bf16_ts(tmem + TM_X, tmem + TM_SA + part * 64 + ks * 8, smem_desc(kq_s + off, 16, 1024),
+                                    idesc, (part | ks) != 0);
+                    }
+                mma_commit(&bars->state_mma);
+            }
+            ok = wait_bar(&bars->state_mma, mma_phase, abort_flag);
+            mma_phase ^= 1;
+            tc_fence_after();
+            // (V - X)^T -> bf16 hi/lo operand in TMEM
+            {
+                float x[64];
+                tmem_ld64(lane_base + TM_X, x);
+#pragma unroll
+                for (int t = 0; t < C; ++t) {
+                    const float vv =
+                        __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(Vt + swz_offset(t, j, 8192)));
+                    x[t] = t < valid ? vv - x[t] : 0.f;
+                }
+                uint32_t hi[32], lo[32];
+                split_pack<32>(x, hi, lo);
+                tmem_st32u(lane_base + TM_X, hi);
+                tmem_st32u(lane_base + TM_X + 32, lo);
+                tmem_st_wait();
+            }
+            tc_fence_before();
+            if (named_bar_any(BAR_STATE, 128, !ok || *abort_flag)) {
+                *abort_flag = 1;
+                break;
+            }
+            if (j == 0) {  // U^^T = (V-X)^T T'^T
+                tc_fence_after();
+                const uint32_t idesc = idesc_bf16_f32(128, 64, 0, 0);
+                const uint32_t tp = s_sm + OFF_TP + buf * 16384;
+#pragma unroll
+                for (int part = 0; part < 3; ++part) {
+                    const uint32_t a_col = TM_X + (part == 2 ? 32 : 0);
+                    const uint32_t b_s = tp + (part == 1 ? 8192 : 0);
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_bf16_ts(tmem + TM_U, tmem + a_col + ks * 8, smem_desc(b_s + ks * 32, 16, 1024), idesc,
+                                    (part | ks) != 0);
+                }
+                mma_commit(&bars->state_mma);
+            }
+            ok = wait_bar(&bars->state_mma, mma_phase, abort_flag);
+            mma_phase ^= 1;
+            tc_fence_after();
+            // u^T = U^^T diag(1/n) -> bf16 hi/lo operand in TMEM
+            {
+                float u[64];
+                tmem_ld64(lane_base + TM_U, u);
+                const float *invn = row_invn + buf * 64;
+#pragma unroll
+                for (int t = 0; t < C; ++t) u[t] *= invn[t];
+                uint32_t hi[32], lo[32];
+                split_pack<32>(u, hi, lo);
+                tmem_st32u(lane_base + TM_U, hi);
+                tmem_st32u(lane_base + TM_U + 32, lo);
+                tmem_st_wait();
+            }
+            tc_fence_before();
+            if (named_bar_any(BAR_STATE, 128, !ok || *abort_flag)) {
+                *abort_flag = 1;
+                break;
+            }
+            if (j == 0) {  // O^T += u^T P^T ;  S^T += u^T K
+                tc_fence_after();
+                const uint32_t idesc_o = idesc_bf16_f32(128, 64, 0, 0);
+                const uint32_t pb = s_sm + OFF_P + buf * 16384;
+#pragma unroll
+                for (int part = 0; part < 3; ++part) {
+                    const uint32_t a_col = TM_U + (part == 2 ? 32 : 0);
+                    const uint32_t b_s = pb + (part == 1 ? 8192 : 0);
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_bf16_ts(tmem + TM_O, tmem + a_col + ks * 8, smem_desc(b_s + ks * 32, 16, 1024), idesc_o, 1);
+                }
+                const uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 1);
+#pragma unroll
+                for (int part = 0; part < 2; ++part)
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_bf16_ts(tmem + TM_S, tmem + TM_U + part * 32 + ks * 8,
+                                    smem_desc(kq_s + ks * 2048, 16384, 1024), idesc_s, 1);
+                mma_commit(&bars->state_mma);
+                mma_commit(&bars->chunk_done[c & 1]);
+            }
+            ok = wait_bar(&bars->state_mma, mma_phase, abort_flag);
+            mma_phase ^= 1;
+            tc_fence_after();
+            // outputs of this chunk
+            {
+                float ov[64];
+                tmem_ld64(lane_base + TM_O, ov);
+                const bool direct = varlen && valid < C;
+                if (!direct) {
+                    if (OUT_BF16) {
+                        __nv_bfloat16 *stg =
+                            reinterpret_cast<__nv_bfloat16 *>(sm + OFF_OST) + (j >> 6) * 4096 + (j & 63);
+#pragma unroll
+                        for (int t = 0; t < C; ++t) stg[t * 64] = __float2bfloat16_rn(ov[t]);
+                    } else {
+                        float *stg = reinterpret_cast<float *>(sm + OFF_OST) + (j >> 5) * 2048 + (j & 31);
+#pragma unroll
+                        for (int t = 0; t < C; ++t) stg[t * 32] = ov[t];
+                    }
+                    fence_proxy_async_smem();
+                } else {
+#pragma unroll
+                    for (int t = 0; t < C; ++t) {
+                        if (t < valid) {
+                            const size_t row = ((size_t)b * p.T + (size_t)(tok0 + t)) * p.H + h;
+                            if (OUT_BF16)
+                                static_cast<__nv_bfloat16 *>(p.o)[row * D + j] = __float2bfloat16_rn(ov[t]);
+                            else
+                                static_cast<float *>(p.o)[row * D + j] = ov[t];
+                        }
+                    }
+                }
+                tc_fence_before();
+                if (named_bar_any(BAR_STATE, 128, !ok || *abort_flag)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                if (!direct && j == 0) {
+                    const int nb = OUT_BF16 ? 2 : 4, bw = OUT_BF16 ? 64 : 32;
+                    for (int bx = 0; bx < nb; ++bx)
+                        tma_store_4d(&p.map_o, sm + OFF_OST + bx * 8192, bx * bw, h, (int)tok0, (int)b);
+                    bulk_commit();
+                }
+            }
+        }
+        if (j == 0) bulk_wait0();
+        if (!*abort_flag && p.S_T) {
+            float s64[64];
+            tmem_ld64(lane_base + TM_S, s64);
+#pragma unroll
+            for (int i = 0; i < 64; ++i) p.S_T[sbase + (size_t)i * D + j] = s64[i];
+            tmem_ld64(lane_base + TM_S + 64, s64);
+#pragma unroll
+            for (int i = 0; i < 64; ++i) p.S_T[sbase + (size_t)(64 + i) * D + j] = s64[i];
         }
     }
 
-    if (*abort_flag) {
-        if (tid == 0) atomicExch(p.status, (int)EFLA_ERR_DEVICE_TIMEOUT);
-        // let the most recently issued TMA land before the CTA exits (bounded)
-        const int last = min(aborted_at + 1, nchunks - 1);
-        mbar_wait(&bar_tma[last & 1], (last >> 1) & 1, WAIT_NS / 4);
-    } else if (p.S_T) {
-        float s64[64];
-        tmem_ld64(lane_base + TM_S, s64);
-#pragma unroll
-        for (int i = 0; i < 64; ++i) p.S_T[sbase + (size_t)i * D + j] = s64[i];
-        tmem_ld64(lane_base + TM_S + 64, s64);
-#pragma unroll
-        for (int i = 0; i < 64; ++i) p.S_T[sbase + (size_t)(64 + i) * D + j] = s64[i];
-    }
-    cta_sync_tc();
+    if (*abort_flag && tid == 0) atomicExch(p.status, (int)EFLA_ERR_DEVICE_TIMEOUT);
+    tc_fence_before();
+    __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, TM_COLS);
 }
 
@@ -503,16 +673,18 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// 4-D map over a [B, T, H, 128] bf16 tensor: box of 64 features x 1 head x 64 tokens.
-bool make_map(CUtensorMap *m, const void *ptr, int B, int T, int H) {
+// 4-D map over a [B, T, H, 128] tensor: box of `box_x` features x 1 head x 64 tokens.
+bool make_map(CUtensorMap *m, const void *ptr, int B, int T, int H, bool f32, int box_x, bool swizzle) {
     auto fn = encode_fn();
     if (!fn) return false;
+    const cuuint64_t es_b = f32 ? 4 : 2;
     cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
-    cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2, (cuuint64_t)T * H * D * 2};
-    cuuint32_t box[4] = {64, 1, (cuuint32_t)C, 1};
+    cuuint64_t strides[3] = {(cuuint64_t)D * es_b, (cuuint64_t)H * D * es_b, (cuuint64_t)T * H * D * es_b};
+    cuuint32_t box[4] = {(cuuint32_t)box_x, 1, (cuuint32_t)C, 1};
     cuuint32_t es[4] = {1, 1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims, strides, box, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    return fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr),
+              dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -522,13 +694,13 @@ cudaError_t launch_typed(const TcParams &p, unsigned grid, cudaStream_t stream) 
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 64 && !attr_done[dev]) {
+    if (dev >= 64 || !attr_done[dev]) {
         e = cudaFuncSetAttribute(chunk_tc_kernel<OUT_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)SMEM_ALLOC);
         if (e != cudaSuccess) return e;
-        attr_done[dev] = true;
+        if (dev < 64) attr_done[dev] = true;
     }
-    chunk_tc_kernel<OUT_BF16><<<grid, 128, SMEM_ALLOC, stream>>>(p);
+    chunk_tc_kernel<OUT_BF16><<<grid, 256, SMEM_ALLOC, stream>>>(p);
     return cudaGetLastError();
 }
 
@@ -538,30 +710,29 @@ cudaError_t launch_chunk_tc(const FwdArgs &a, const char **why) {
     if (a.N == 0) return cudaSuccess;
     TcParams p;
     memset(&p, 0, sizeof p);
+    const bool o_bf16 = a.o_dtype == EFLA_BF16;
     if ((long long)a.B * a.T > 0) {
-        if (!make_map(&p.map_q, a.q, a.B, a.T, a.H) || !make_map(&p.map_k, a.k, a.B, a.T, a.H)) {
-            *why = "cuTensorMapEncodeTiled failed for q/k";
+        if (!make_map(&p.map_q, a.q, a.B, a.T, a.H, false, 64, true) ||
+            !make_map(&p.map_k, a.k, a.B, a.T, a.H, false, 64, true) ||
+            !make_map(&p.map_v, a.v, a.B, a.T, a.H, false, 64, true) ||
+            !make_map(&p.map_o, a.o, a.B, a.T, a.H, !o_bf16, o_bf16 ? 64 : 32, false)) {
+            *why = "cuTensorMapEncodeTiled failed";
             return cudaErrorInvalidValue;
         }
     }
-    p.v = static_cast<const __nv_bfloat16 *>(a.v);
     p.beta = a.beta;
     p.S0 = a.S0;
     p.cu_seqlens = a.cu_seqlens;
     p.o = a.o;
     p.S_T = a.S_T;
-    p.status = device_status_ptr();
+    p.status = a.status;
     p.B = a.B;
     p.T = a.T;
     p.H = a.H;
     p.N = a.N;
-    if (!p.status) {
-        *why = "device status word unavailable";
-        return cudaErrorInvalidSymbol;
-    }
     *why = "tcgen05 chunk kernel launch";
     const unsigned grid = (unsigned)((long)a.N * a.H);
-    return a.o_dtype == EFLA_BF16 ? launch_typed<true>(p, grid, a.stream) : launch_typed<false>(p, grid, a.stream);
+    return o_bf16 ? launch_typed<true>(p, grid, a.stream) : launch_typed<false>(p, grid, a.stream);
 }
 
 }  // namespace efla
