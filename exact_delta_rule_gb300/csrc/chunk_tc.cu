@@ -70,11 +70,13 @@ constexpr uint32_t OFF_P = 131072;         // 2 buffers x {hi, lo}: P [64 t][64 
 constexpr uint32_t OFF_OST = 163840;       // o staging for the TMA store, 32 KB
 constexpr uint32_t OFF_AT = 196608;        // fp32 [64][65]: A~, then T~ in place
 constexpr uint32_t AT_LD = 65;
-constexpr uint32_t OFF_ROW = OFF_AT + 64 * AT_LD * 4;  // fp32: invn[2][64], gn[2][64], beta[64], gam[64]
+constexpr uint32_t OFF_ROW = OFF_AT + 64 * AT_LD * 4;  // fp32: invn[2][64], gn[2][64], beta[64]
 constexpr uint32_t ROW_BYTES = 6 * 64 * 4;
 constexpr uint32_t OFF_BAR = OFF_ROW + ROW_BYTES;       // mbarriers (struct Bars)
-constexpr uint32_t OFF_MISC = OFF_BAR + 64;             // tmem base (u32), abort flag (i32)
-constexpr uint32_t SMEM_USED = OFF_MISC + 16;
+constexpr uint32_t OFF_MISC = OFF_BAR + 128;            // tmem base (u32), abort flag (i32)
+constexpr uint32_t OFF_SCR = OFF_MISC + 16;             // fp32 scratch of the triangular inverse
+constexpr uint32_t SCR_FLOATS = 32 * 33;
+constexpr uint32_t SMEM_USED = OFF_SCR + SCR_FLOATS * 4;
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;       // + alignment slack for the 1024-byte base
 static_assert(OFF_TP == 2 * STAGE_BYTES && OFF_P == OFF_TP + 32768 && OFF_OST == OFF_P + 32768 &&
                   OFF_AT == OFF_OST + 32768,
@@ -109,13 +111,16 @@ struct TcParams {
 };
 
 struct Bars {
-    uint64_t tma_full[2];
-    uint64_t g_done;
-    uint64_t state_mma;
-    uint64_t prep_ready[2];
-    uint64_t chunk_done[2];
+    uint64_t tma_full[2];    // K, Q, V of a stage landed
+    uint64_t g_done;         // Gram MMA of the prep warpgroup
+    uint64_t x_done;         // X^T = S^T K^T
+    uint64_t u_done;         // U^^T
+    uint64_t s_done;         // S^T += u^T K
+    uint64_t o_done;         // O^T of the chunk complete
+    uint64_t prep_ready[2];  // T', P, gate terms and the zeroed tail of a chunk written
+    uint64_t chunk_done[2];  // every MMA of a chunk complete: its stage and buffers are free
 };
-static_assert(sizeof(Bars) <= 64, "mbarrier block exceeds its slot");
+static_assert(sizeof(Bars) <= 128, "mbarrier block exceeds its slot");
 
 // Bounded wait that also gives up when the other warpgroup has aborted.
 __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
@@ -178,79 +183,103 @@ __device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t (&u)[3
     tmem_st32(taddr, reinterpret_cast<const float(&)[32]>(u));
 }
 
-// T~ = (I + A~)^{-1} in place in At (fp32, row stride AT_LD), with 128 threads.
-// Diagonal 16x16 blocks by column substitution, then the blocks below them row
-// block by row block: T~_IJ = -T~_II sum_{M=J}^{I-1} A~_IM T~_MJ.
-__device__ __forceinline__ void invert_unit_lower(float *At, int pt) {
+// T~ = (I + A~)^{-1} in place in At (fp32, row stride AT_LD), by the 128
+// threads of the prep warpgroup, with a scratch Y of SCR_FLOATS floats.  Each
+// step applies [[L1, 0], [B, L2]]^{-1} = [[L1^{-1}, 0], [-L2^{-1} B L1^{-1}, L2^{-1}]]
+// for unit lower-triangular L1, L2:
+//   1. the four diagonal 16x16 blocks by column substitution (warp w: block w;
+//      the two half-warps split each column's rows by parity);
+//   2. blocks (1,0) and (3,2) of 16:  T~_IJ = -T~_II (A~_IJ T~_JJ);
+//   3. the lower-left 32x32 block:    T~_21 = -T~_22 (A~_21 T~_11)  (32x32 blocks).
+// Steps 2 and 3 are register-tiled fp32 products.
+__device__ __forceinline__ void invert_unit_lower(float *At, float *Y, int pt) {
     const int lane = pt & 31, pw = pt >> 5;
-    {  // diagonal block pw, column `lane` (lanes 0-15)
-        const int B0 = pw * 16, c = lane & 15;
-        float col[16];
+    {
+        const int B0 = pw * 16, c = lane & 15, par = lane >> 4;
+        float col[8];  // col[m] = T~[B0 + 2m + par][B0 + c]
 #pragma unroll
-        for (int s = 0; s < 16; ++s) col[s] = (s == c) ? 1.f : 0.f;
+        for (int m = 0; m < 8; ++m) col[m] = (2 * m + par == c) ? 1.f : 0.f;
 #pragma unroll
         for (int t = 1; t < 16; ++t) {
+            const float *row = At + (B0 + t) * AT_LD + B0 + par;
             float acc = 0.f;
-            const float *row = At + (B0 + t) * AT_LD + B0;
 #pragma unroll
-            for (int s = 0; s < t; ++s) acc = fmaf(row[s], col[s], acc);
-            if (t > c) col[t] = -acc;
+            for (int m = 0; m < (t + 1) / 2; ++m) acc = fmaf(row[2 * m], col[m], acc);  // A~[t][t] = 0
+            const float tot = acc + __shfl_xor_sync(0xffffffffu, acc, 16);
+            if ((t & 1) == par && t > c) col[t >> 1] = -tot;
         }
         __syncwarp();
-        if (lane < 16) {
 #pragma unroll
-            for (int s = 0; s < 16; ++s) At[(B0 + s) * AT_LD + B0 + c] = col[s];
-        }
+        for (int m = 0; m < 8; ++m) At[(B0 + 2 * m + par) * AT_LD + B0 + c] = col[m];
     }
     named_bar(BAR_PREP, 128);
-#pragma unroll 1
-    for (int I = 1; I < 4; ++I) {
-        const int cid = pt >> 1, h = pt & 1;
-        const bool active = cid < 16 * I;
-        const int J = cid >> 4, c = cid & 15;
-        float y[8];
+    {
+        const int q = pt >> 6, tt = pt & 63;
+        const int I = 2 * q + 1, J = 2 * q;
+        const int r = tt >> 2, c0 = (tt & 3) * 4;
+        float *yq = Y + q * (16 * 17);
+        float y[4] = {0.f, 0.f, 0.f, 0.f};
+        const float *arow = At + (16 * I + r) * AT_LD + 16 * J;
 #pragma unroll
-        for (int r = 0; r < 8; ++r) y[r] = 0.f;
-        if (active) {
-#pragma unroll 1
-            for (int M = J; M < I; ++M) {
-                float tcol[16];
+        for (int k = 0; k < 16; ++k) {
+            const float a = arow[k];
+            const float *brow = At + (16 * J + k) * AT_LD + 16 * J + c0;
 #pragma unroll
-                for (int k = 0; k < 16; ++k) tcol[k] = At[(16 * M + k) * AT_LD + 16 * J + c];
+            for (int i = 0; i < 4; ++i) y[i] = fmaf(a, brow[i], y[i]);
+        }
 #pragma unroll
-                for (int r = 0; r < 8; ++r) {
-                    const float *arow = At + (16 * I + 8 * h + r) * AT_LD + 16 * M;
+        for (int i = 0; i < 4; ++i) yq[r * 17 + c0 + i] = y[i];
+        named_bar(BAR_PREP, 128);
+        float z[4] = {0.f, 0.f, 0.f, 0.f};
+        const float *trow = At + (16 * I + r) * AT_LD + 16 * I;  // T~_II row r (zeros above the diagonal)
 #pragma unroll
-                    for (int k = 0; k < 16; ++k) y[r] = fmaf(arow[k], tcol[k], y[r]);
-                }
+        for (int k = 0; k < 16; ++k) {
+            const float tv = trow[k];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) z[i] = fmaf(tv, yq[k * 17 + c0 + i], z[i]);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) At[(16 * I + r) * AT_LD + 16 * J + c0 + i] = -z[i];
+        named_bar(BAR_PREP, 128);
+    }
+    {
+        const int r0 = 2 * (pt >> 3), c0 = 4 * (pt & 7);
+        float x0[4] = {0.f, 0.f, 0.f, 0.f}, x1[4] = {0.f, 0.f, 0.f, 0.f};
+        const float *a0 = At + (32 + r0) * AT_LD, *a1 = a0 + AT_LD;
+#pragma unroll 8
+        for (int k = 0; k < 32; ++k) {
+            const float va0 = a0[k], va1 = a1[k];
+            const float *brow = At + k * AT_LD + c0;  // T~_11 (rows/cols 0..31)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float bv = brow[i];
+                x0[i] = fmaf(va0, bv, x0[i]);
+                x1[i] = fmaf(va1, bv, x1[i]);
             }
         }
-        // the full column of Y is split between this thread (rows 8h..8h+7) and its partner
-        float yo[8];
 #pragma unroll
-        for (int r = 0; r < 8; ++r) yo[r] = __shfl_xor_sync(0xffffffffu, y[r], 1);
-        float z[8];
-        if (active) {
-            const float *y0 = h ? yo : y;  // rows 0..7
-            const float *y1 = h ? y : yo;  // rows 8..15
-#pragma unroll
-            for (int r = 0; r < 8; ++r) {
-                const int R = 8 * h + r;
-                const float *trow = At + (16 * I + R) * AT_LD + 16 * I;
-                float acc = 0.f;
-#pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    if (k <= R) acc = fmaf(trow[k], y0[k], acc);
-#pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    if (8 + k <= R) acc = fmaf(trow[8 + k], y1[k], acc);
-                z[r] = -acc;
-            }
+        for (int i = 0; i < 4; ++i) {
+            Y[r0 * 33 + c0 + i] = x0[i];
+            Y[(r0 + 1) * 33 + c0 + i] = x1[i];
         }
         named_bar(BAR_PREP, 128);
-        if (active) {
+        float z0[4] = {0.f, 0.f, 0.f, 0.f}, z1[4] = {0.f, 0.f, 0.f, 0.f};
+        const float *t0 = At + (32 + r0) * AT_LD + 32, *t1 = t0 + AT_LD;  // T~_22 rows
+#pragma unroll 8
+        for (int k = 0; k < 32; ++k) {
+            const float tv0 = t0[k], tv1 = t1[k];
+            const float *xrow = Y + k * 33 + c0;
 #pragma unroll
-            for (int r = 0; r < 8; ++r) At[(16 * I + 8 * h + r) * AT_LD + 16 * J + c] = z[r];
+            for (int i = 0; i < 4; ++i) {
+                const float xv = xrow[i];
+                z0[i] = fmaf(tv0, xv, z0[i]);
+                z1[i] = fmaf(tv1, xv, z1[i]);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            At[(32 + r0) * AT_LD + c0 + i] = -z0[i];
+            At[(33 + r0) * AT_LD + c0 + i] = -z1[i];
         }
         named_bar(BAR_PREP, 128);
     }
@@ -263,7 +292,7 @@ __global__ void __launch_bounds__(256, 1) chunk_tc_kernel(const __grid_constant_
     float *row_invn = reinterpret_cast<float *>(sm + OFF_ROW);  // [2][64]
     float *row_gn = row_invn + 128;                             // [2][64]
     float *row_beta = row_invn + 256;                           // [64] (prep only)
-    float *row_gam = row_invn + 320;                            // [64] (prep only)
+    float *scr = reinterpret_cast<float *>(sm + OFF_SCR);
     float *At = reinterpret_cast<float *>(sm + OFF_AT);
     Bars *bars = reinterpret_cast<Bars *>(sm + OFF_BAR);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + OFF_MISC);
@@ -299,7 +328,10 @@ __global__ void __launch_bounds__(256, 1) chunk_tc_kernel(const __grid_constant_
         mbar_init(&bars->tma_full[0], 1);
         mbar_init(&bars->tma_full[1], 1);
         mbar_init(&bars->g_done, 1);
-        mbar_init(&bars->state_mma, 1);
+        mbar_init(&bars->x_done, 1);
+        mbar_init(&bars->u_done, 1);
+        mbar_init(&bars->s_done, 1);
+        mbar_init(&bars->o_done, 1);
         mbar_init(&bars->prep_ready[0], 1);
         mbar_init(&bars->prep_ready[1], 1);
         mbar_init(&bars->chunk_done[0], 1);
@@ -382,39 +414,30 @@ __global__ void __launch_bounds__(256, 1) chunk_tc_kernel(const __grid_constant_
             {
                 float g[64];
                 tmem_ld64(lane_base + TM_G, g);
-                if (pt < C) {
+                if (pt < C) {  // K K^T row t -> gate terms, then A~ row t
+                    const int t = pt;
+                    float lam = 0.f;
 #pragma unroll
-                    for (int s = 0; s < 64; ++s) At[pt * AT_LD + s] = g[s];
+                    for (int s = 0; s < 64; ++s) lam = (s == t) ? g[s] : lam;
+                    const bool live = t < valid && lam > 0.f;
+                    const float invn = live ? rsqrtf(lam) : 0.f;
+                    const float gam = live ? -expm1f(-row_beta[t] * lam) : 0.f;
+                    row_invn[buf * 64 + t] = invn;
+                    row_gn[buf * 64 + t] = gam * invn;
+                    named_bar(BAR_PREP, 128);
+                    const float rs = gam * invn;
+#pragma unroll
+                    for (int s = 0; s < 64; ++s) At[t * AT_LD + s] = s < t ? rs * row_invn[buf * 64 + s] * g[s] : 0.f;
                 } else {  // P = Q K^T with the inclusive causal mask
                     const int t = pt - C;
 #pragma unroll
                     for (int s = 0; s < 64; ++s) g[s] = s <= t ? g[s] : 0.f;
                     store_row_split(sm + OFF_P + buf * 16384, sm + OFF_P + buf * 16384 + 8192, t, g);
+                    named_bar(BAR_PREP, 128);
                 }
             }
             named_bar(BAR_PREP, 128);
-            if (pt < C) {
-                const int t = pt;
-                const float lam = At[t * AT_LD + t];
-                const bool live = t < valid && lam > 0.f;
-                const float invn = live ? rsqrtf(lam) : 0.f;
-                const float gam = live ? -expm1f(-row_beta[t] * lam) : 0.f;
-                row_gam[t] = gam;
-                row_invn[buf * 64 + t] = invn;
-                row_gn[buf * 64 + t] = gam * invn;
-            }
-            named_bar(BAR_PREP, 128);
-            if (pt < C) {  // A~ row t
-                const int t = pt;
-                const float rs = row_gam[t] * row_invn[buf * 64 + t];
-#pragma unroll
-                for (int s = 0; s < 64; ++s) {
-                    float *a = &At[t * AT_LD + s];
-                    *a = s < t ? rs * row_invn[buf * 64 + s] * *a : 0.f;
-                }
-            }
-            named_bar(BAR_PREP, 128);
-            invert_unit_lower(At, pt);
+            invert_unit_lower(At, scr, pt);
             {  // T' = T~ diag(gamma/n), lower triangle, as bf16 hi/lo [t][s]
                 const int t = pt >> 1, s0 = (pt & 1) * 32;
                 uint8_t *hi = sm + OFF_TP + buf * 16384, *lo = hi + 8192;
@@ -457,6 +480,10 @@ __global__ void __launch_bounds__(256, 1) chunk_tc_kernel(const __grid_constant_
         }
     } else {
         // =============================== state warpgroup ===============================
+        // Per chunk c, the dependency chain through the state is
+        //   S -> X = K S -> V - X -> U^ -> u -> S + K^T u;
+        // the outputs O = Q S + P u are formed beside it (O1 after X, O2 after the
+        // state update) and written out while the next chunk's X is computed.
         const int j = tid;
         const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
         {  // initial state -> TMEM (S^T: lane j holds column j of S)
@@ -469,7 +496,46 @@ __global__ void __launch_bounds__(256, 1) chunk_tc_kernel(const __grid_constant_
             }
             tmem_st_wait();
         }
-        uint32_t mma_phase = 0;
+        // O^T of chunk cc -> staging (TMA store issued by thread 0 after the next barrier)
+        // or, for a partial chunk of a packed batch, straight to global memory.
+        auto epilogue_load = [&](int cc) -> bool {
+            const long t0c = bos + (long)cc * C;
+            const int vc = (int)min((long)C, eos - t0c);
+            const bool direct = varlen && vc < C;
+            float ov[64];
+            tmem_ld64(lane_base + TM_O, ov);
+            if (!direct) {
+                if (OUT_BF16) {
+                    __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(sm + OFF_OST) + (j >> 6) * 4096 + (j & 63);
+#pragma unroll
+                    for (int t = 0; t < C; ++t) stg[t * 64] = __float2bfloat16_rn(ov[t]);
+                } else {
+                    float *stg = reinterpret_cast<float *>(sm + OFF_OST) + (j >> 5) * 2048 + (j & 31);
+#pragma unroll
+                    for (int t = 0; t < C; ++t) stg[t * 32] = ov[t];
+                }
+                fence_proxy_async_smem();
+            } else {
+#pragma unroll
+                for (int t = 0; t < C; ++t) {
+                    if (t < vc) {
+                        const size_t row = ((size_t)b * p.T + (size_t)(t0c + t)) * p.H + h;
+                        if (OUT_BF16)
+                            static_cast<__nv_bfloat16 *>(p.o)[row * D + j] = __float2bfloat16_rn(ov[t]);
+                        else
+                            static_cast<float *>(p.o)[row * D + j] = ov[t];
+                    }
+                }
+            }
+            return direct;
+        };
+        auto epilogue_store = [&](int cc) {  // thread 0, after the barrier
+            const int nb = OUT_BF16 ? 2 : 4, bw = OUT_BF16 ? 64 : 32;
+            const int t0c = (int)(bos + (long)cc * C);
+            for (int bx = 0; bx < nb; ++bx) tma_store_4d(&p.map_o, sm + OFF_OST + bx * 8192, bx * bw, h, t0c, (int)b);
+            bulk_commit();
+        };
+        bool aborted = false;
         for (int c = 0; c < nchunks; ++c) {
             const int st = c & 1, buf = c & 1;
             const long tok0 = bos + (long)c * C;
@@ -495,15 +561,15 @@ __global__ void __launch_bounds__(256, 1) chunk_tc_kernel(const __grid_constant_
                 }
                 tmem_st_wait();
             }
-            if (j == 0) bulk_wait_read0();  // the o staging of chunk c-1 has been read
+            if (j == 0) bulk_wait_read0();  // the staging buffer is free again
             tc_fence_before();
             if (named_bar_any(BAR_STATE, 128, !ok || *abort_flag)) {
-                *abort_flag = 1;
+                aborted = true;
                 break;
             }
-            if (j == 0) {  // [X^T | O1^T] = S^T [K;Q]^T
+            if (j == 0) {  // X^T = S^T K^T
                 tc_fence_after();
-                const uint32_t idesc = idesc_bf16_f32(128, 128, 0, 0);
+                const uint32_t idesc = idesc_bf16_f32(128, 64, 0, 0);
 #pragma unroll
                 for (int part = 0; part < 2; ++part)
 #pragma unroll
@@ -512,10 +578,34 @@ __global__ void __launch_bounds__(256, 1) chunk_tc_kernel(const __grid_constant_
                         mma_bf16_ts(tmem + TM_X, tmem + TM_SA + part * 64 + ks * 8, smem_desc(kq_s + off, 16, 1024),
                                     idesc, (part | ks) != 0);
                     }
-                mma_commit(&bars->state_mma);
+                mma_commit(&bars->x_done);
             }
-            ok = wait_bar(&bars->state_mma, mma_phase, abort_flag);
-            mma_phase ^= 1;
+            // outputs of chunk c-1 leave while X is computed
+            bool direct_prev = true;
+            if (c > 0) {
+                ok = wait_bar(&bars->o_done, (c - 1) & 1, abort_flag) && ok;
+                tc_fence_after();
+                direct_prev = epilogue_load(c - 1);
+            }
+            tc_fence_before();
+            if (named_bar_any(BAR_STATE, 128, !ok || *abort_flag)) {
+                aborted = true;
+                break;
+            }
+            if (j == 0) {
+                if (!direct_prev) epilogue_store(c - 1);
+                tc_fence_after();
+                const uint32_t idesc = idesc_bf16_f32(128, 64, 0, 0);  // O1^T = S^T Q^T
+#pragma unroll
+                for (int part = 0; part < 2; ++part)
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32 + 8192;
+                        mma_bf16_ts(tmem + TM_O, tmem + TM_SA + part * 64 + ks * 8, smem_desc(kq_s + off, 16, 1024),
+                                    idesc, (part | ks) != 0);
+                    }
+            }
+            ok = wait_bar(&bars->x_done, c & 1, abort_flag);
             tc_fence_after();
             // (V - X)^T -> bf16 hi/lo operand in TMEM
             {
@@ -535,7 +625,7 @@ __global__ void __launch_bounds__(256, 1) chunk_tc_kernel(const __grid_constant_
             }
             tc_fence_before();
             if (named_bar_any(BAR_STATE, 128, !ok || *abort_flag)) {
-                *abort_flag = 1;
+                aborted = true;
                 break;
             }
             if (j == 0) {  // U^^T = (V-X)^T T'^T
@@ -551,10 +641,9 @@ __global__ void __launch_bounds__(256, 1) chunk_tc_kernel(const __grid_constant_
                         mma_bf16_ts(tmem + TM_U, tmem + a_col + ks * 8, smem_desc(b_s + ks * 32, 16, 1024), idesc,
                                     (part | ks) != 0);
                 }
-                mma_commit(&bars->state_mma);
+                mma_commit(&bars->u_done);
             }
-            ok = wait_bar(&bars->state_mma, mma_phase, abort_flag);
-            mma_phase ^= 1;
+            ok = wait_bar(&bars->u_done, c & 1, abort_flag);
             tc_fence_after();
             // u^T = U^^T diag(1/n) -> bf16 hi/lo operand in TMEM
             {
@@ -571,11 +660,19 @@ __global__ void __launch_bounds__(256, 1) chunk_tc_kernel(const __grid_constant_
             }
             tc_fence_before();
             if (named_bar_any(BAR_STATE, 128, !ok || *abort_flag)) {
-                *abort_flag = 1;
+                aborted = true;
                 break;
             }
-            if (j == 0) {  // O^T += u^T P^T ;  S^T += u^T K
+            if (j == 0) {  // S^T += u^T K  (the chain), then O^T += u^T P^T
                 tc_fence_after();
+                const uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 1);
+#pragma unroll
+                for (int part = 0; part < 2; ++part)
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_bf16_ts(tmem + TM_S, tmem + TM_U + part * 32 + ks * 8,
+                                    smem_desc(kq_s + ks * 2048, 16384, 1024), idesc_s, 1);
+                mma_commit(&bars->s_done);
                 const uint32_t idesc_o = idesc_bf16_f32(128, 64, 0, 0);
                 const uint32_t pb = s_sm + OFF_P + buf * 16384;
 #pragma unroll
@@ -586,63 +683,25 @@ __global__ void __launch_bounds__(256, 1) chunk_tc_kernel(const __grid_constant_
                     for (int ks = 0; ks < 4; ++ks)
                         mma_bf16_ts(tmem + TM_O, tmem + a_col + ks * 8, smem_desc(b_s + ks * 32, 16, 1024), idesc_o, 1);
                 }
-                const uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 1);
-#pragma unroll
-                for (int part = 0; part < 2; ++part)
-#pragma unroll
-                    for (int ks = 0; ks < 4; ++ks)
-                        mma_bf16_ts(tmem + TM_S, tmem + TM_U + part * 32 + ks * 8,
-                                    smem_desc(kq_s + ks * 2048, 16384, 1024), idesc_s, 1);
-                mma_commit(&bars->state_mma);
+                mma_commit(&bars->o_done);
                 mma_commit(&bars->chunk_done[c & 1]);
             }
-            ok = wait_bar(&bars->state_mma, mma_phase, abort_flag);
-            mma_phase ^= 1;
+            if (!wait_bar(&bars->s_done, c & 1, abort_flag)) *abort_flag = 1;
             tc_fence_after();
-            // outputs of this chunk
-            {
-                float ov[64];
-                tmem_ld64(lane_base + TM_O, ov);
-                const bool direct = varlen && valid < C;
-                if (!direct) {
-                    if (OUT_BF16) {
-                        __nv_bfloat16 *stg =
-                            reinterpret_cast<__nv_bfloat16 *>(sm + OFF_OST) + (j >> 6) * 4096 + (j & 63);
-#pragma unroll
-                        for (int t = 0; t < C; ++t) stg[t * 64] = __float2bfloat16_rn(ov[t]);
-                    } else {
-                        float *stg = reinterpret_cast<float *>(sm + OFF_OST) + (j >> 5) * 2048 + (j & 31);
-#pragma unroll
-                        for (int t = 0; t < C; ++t) stg[t * 32] = ov[t];
-                    }
-                    fence_proxy_async_smem();
-                } else {
-#pragma unroll
-                    for (int t = 0; t < C; ++t) {
-                        if (t < valid) {
-                            const size_t row = ((size_t)b * p.T + (size_t)(tok0 + t)) * p.H + h;
-                            if (OUT_BF16)
-                                static_cast<__nv_bfloat16 *>(p.o)[row * D + j] = __float2bfloat16_rn(ov[t]);
-                            else
-                                static_cast<float *>(p.o)[row * D + j] = ov[t];
-                        }
-                    }
-                }
-                tc_fence_before();
-                if (named_bar_any(BAR_STATE, 128, !ok || *abort_flag)) {
-                    *abort_flag = 1;
-                    break;
-                }
-                if (!direct && j == 0) {
-                    const int nb = OUT_BF16 ? 2 : 4, bw = OUT_BF16 ? 64 : 32;
-                    for (int bx = 0; bx < nb; ++bx)
-                        tma_store_4d(&p.map_o, sm + OFF_OST + bx * 8192, bx * bw, h, (int)tok0, (int)b);
-                    bulk_commit();
-                }
-            }
+        }
+        // outputs of the last chunk
+        bool ok = !aborted && wait_bar(&bars->o_done, (nchunks - 1) & 1, abort_flag);
+        tc_fence_after();
+        if (j == 0) bulk_wait_read0();
+        if (!named_bar_any(BAR_STATE, 128, !ok || *abort_flag)) {
+            const bool direct = epilogue_load(nchunks - 1);
+            tc_fence_before();
+            named_bar(BAR_STATE, 128);
+            if (j == 0 && !direct) epilogue_store(nchunks - 1);
         }
         if (j == 0) bulk_wait0();
         if (!*abort_flag && p.S_T) {
+            tc_fence_after();
             float s64[64];
             tmem_ld64(lane_base + TM_S, s64);
 #pragma unroll
