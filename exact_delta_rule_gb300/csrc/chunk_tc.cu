@@ -67,13 +67,13 @@ constexpr uint32_t OFF_STAGE = 0;          // 2 stages
 constexpr uint32_t OFF_V = 32768;          // within a stage
 constexpr uint32_t OFF_TP = 98304;         // 2 buffers x {hi 8 KB, lo 8 KB}: T' [64 t][64 s]
 constexpr uint32_t OFF_P = 131072;         // 2 buffers x {hi, lo}: P [64 t][64 s]
-constexpr uint32_t OFF_OST = 163840;       // o staging for the TMA store, 32 KB
+constexpr uint32_t OFF_OST = 163840;       // o staging for the TMA stores: 4 warps x [64 t][32], 32 KB
 constexpr uint32_t OFF_AT = 196608;        // fp32 [64][65]: A~, then T~ in place
 constexpr uint32_t AT_LD = 65;
 constexpr uint32_t OFF_ROW = OFF_AT + 64 * AT_LD * 4;  // fp32: invn[2][64], gn[2][64], beta[64]
 constexpr uint32_t ROW_BYTES = 6 * 64 * 4;
 constexpr uint32_t OFF_BAR = OFF_ROW + ROW_BYTES;       // mbarriers (struct Bars)
-constexpr uint32_t OFF_MISC = OFF_BAR + 128;            // tmem base (u32), abort flag (i32)
+constexpr uint32_t OFF_MISC = OFF_BAR + 192;            // tmem base (u32), abort flag (i32)
 constexpr uint32_t OFF_SCR = OFF_MISC + 16;             // fp32 scratch of the triangular inverse
 constexpr uint32_t SCR_FLOATS = 32 * 33;
 constexpr uint32_t SMEM_USED = OFF_SCR + SCR_FLOATS * 4;
@@ -94,7 +94,7 @@ constexpr uint32_t TM_COLS = 512;
 
 constexpr uint64_t WAIT_NS = 2000000000ull;  // 2 s bound on any wait
 
-constexpr int BAR_STATE = 1, BAR_PREP = 2;  // named barriers (128 threads each)
+constexpr int BAR_PREP = 2;  // named barrier of the prep warpgroup (128 threads)
 
 struct TcParams {
     CUtensorMap map_q;
@@ -119,17 +119,20 @@ struct Bars {
     uint64_t o_done;         // O^T of the chunk complete
     uint64_t prep_ready[2];  // T', P, gate terms and the zeroed tail of a chunk written
     uint64_t chunk_done[2];  // every MMA of a chunk complete: its stage and buffers are free
+    uint64_t sa_ready;       // state warpgroup wrote S^T hi/lo        (128 arrivals)
+    uint64_t o_free;         // state warpgroup read O^T of the chunk  (128 arrivals)
+    uint64_t r_ready;        // state warpgroup wrote (V - X)^T hi/lo  (128 arrivals)
+    uint64_t u_ready;        // state warpgroup wrote u^T hi/lo        (128 arrivals)
+    uint64_t drain[2];       // all MMAs of the MMA thread / of the prep thread complete
 };
-static_assert(sizeof(Bars) <= 128, "mbarrier block exceeds its slot");
+static_assert(sizeof(Bars) <= 192, "mbarrier block exceeds its slot");
 
 // Bounded wait that also gives up when the other warpgroup has aborted.
 __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
-#pragma unroll 1
-        for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, 20000)) return true;  // sleeps instead of spinning
         if (*abort_flag) return false;
         if (globaltimer_ns() - t0 > WAIT_NS) {
             *abort_flag = 1;
@@ -138,20 +141,19 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatil
     }
 }
 
-__device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t *>(&v);
-}
-
-// Splits pairs x[2c], x[2c+1] into packed bf16 hi and lo words (x ~= hi + lo).
+// Splits pairs x[2c], x[2c+1] into packed bf16 hi and lo words with
+// x = hi + lo + e, |e| < 2^-14 |x|: hi is x truncated to bf16 (its upper 16
+// bits), lo is the exact fp32 remainder x - hi truncated the same way.  Bit
+// operations only (one byte permute per packed pair).
 template <int NP>
 __device__ __forceinline__ void split_pack(const float *x, uint32_t *hi, uint32_t *lo) {
 #pragma unroll
     for (int c = 0; c < NP; ++c) {
-        __nv_bfloat162 h = __floats2bfloat162_rn(x[2 * c], x[2 * c + 1]);
-        const float2 hf = __bfloat1622float2(h);
-        hi[c] = *reinterpret_cast<uint32_t *>(&h);
-        lo[c] = bf16x2_bits(x[2 * c] - hf.x, x[2 * c + 1] - hf.y);
+        const uint32_t b0 = __float_as_uint(x[2 * c]), b1 = __float_as_uint(x[2 * c + 1]);
+        hi[c] = __byte_perm(b0, b1, 0x7632);
+        const float r0 = x[2 * c] - __uint_as_float(b0 & 0xffff0000u);
+        const float r1 = x[2 * c + 1] - __uint_as_float(b1 & 0xffff0000u);
+        lo[c] = __byte_perm(__float_as_uint(r0), __float_as_uint(r1), 0x7632);
     }
 }
 
@@ -286,7 +288,7 @@ __device__ __forceinline__ void invert_unit_lower(float *At, float *Y, int pt) {
 }
 
 template <bool OUT_BF16>
-__global__ void __launch_bounds__(256, 1) chunk_tc_kernel(const __grid_constant__ TcParams p) {
+__global__ void __launch_bounds__(288, 1) chunk_tc_kernel(const __grid_constant__ TcParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float *row_invn = reinterpret_cast<float *>(sm + OFF_ROW);  // [2][64]
@@ -336,6 +338,12 @@ __global__ void __launch_bounds__(256, 1) chunk_tc_kernel(const __grid_constant_
         mbar_init(&bars->prep_ready[1], 1);
         mbar_init(&bars->chunk_done[0], 1);
         mbar_init(&bars->chunk_done[1], 1);
+        mbar_init(&bars->sa_ready, 128);
+        mbar_init(&bars->o_free, 128);
+        mbar_init(&bars->r_ready, 128);
+        mbar_init(&bars->u_ready, 128);
+        mbar_init(&bars->drain[0], 1);
+        mbar_init(&bars->drain[1], 1);
         fence_mbar_init();
         *abort_flag = 0;
     }
@@ -348,9 +356,8 @@ __global__ void __launch_bounds__(256, 1) chunk_tc_kernel(const __grid_constant_
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint32_t s_sm = smem_u32(sm);
-    const bool varlen = p.cu_seqlens != nullptr;
 
-    if (tid >= 128) {
+    if (tid >= 128 && tid < 256) {
         // =============================== prep warpgroup ===============================
         const int pt = tid - 128;
         const uint32_t lane_base = tmem + ((uint32_t)((warp - 4) * 32) << 16);
@@ -414,6 +421,7 @@ __global__ void __launch_bounds__(256, 1) chunk_tc_kernel(const __grid_constant_
             {
                 float g[64];
                 tmem_ld64(lane_base + TM_G, g);
+                // [gate: G row loaded]
                 if (pt < C) {  // K K^T row t -> gate terms, then A~ row t
                     const int t = pt;
                     float lam = 0.f;
@@ -424,10 +432,21 @@ __global__ void __launch_bounds__(256, 1) chunk_tc_kernel(const __grid_constant_
                     const float gam = live ? -expm1f(-row_beta[t] * lam) : 0.f;
                     row_invn[buf * 64 + t] = invn;
                     row_gn[buf * 64 + t] = gam * invn;
+                    // [gate: terms computed]
                     named_bar(BAR_PREP, 128);
+                    // [gate: barrier passed]
                     const float rs = gam * invn;
+                    float iv[64];  // all scales first: the stores below may alias them for the compiler
 #pragma unroll
-                    for (int s = 0; s < 64; ++s) At[t * AT_LD + s] = s < t ? rs * row_invn[buf * 64 + s] * g[s] : 0.f;
+                    for (int s4 = 0; s4 < 16; ++s4) {
+                        const float4 f = reinterpret_cast<const float4 *>(row_invn + buf * 64)[s4];
+                        iv[4 * s4] = f.x;
+                        iv[4 * s4 + 1] = f.y;
+                        iv[4 * s4 + 2] = f.z;
+                        iv[4 * s4 + 3] = f.w;
+                    }
+#pragma unroll
+                    for (int s = 0; s < 64; ++s) At[t * AT_LD + s] = s < t ? rs * iv[s] * g[s] : 0.f;
                 } else {  // P = Q K^T with the inclusive causal mask
                     const int t = pt - C;
 #pragma unroll
@@ -470,6 +489,12 @@ __global__ void __launch_bounds__(256, 1) chunk_tc_kernel(const __grid_constant_
                 issued = c + 2;
             }
         }
+        if (pt == 0) {  // every Gram MMA has completed before TMEM is released (bounded)
+            mma_commit(&bars->drain[1]);
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait_sleep(&bars->drain[1], 0, 20000) && globaltimer_ns() - t0 < WAIT_NS) {
+            }
+        }
         if (pt == 0) {  // after an abort, let TMA loads still in flight land (bounded)
             for (int cc = landed; cc < issued; ++cc) {
                 const uint64_t t0 = globaltimer_ns();
@@ -478,13 +503,14 @@ __global__ void __launch_bounds__(256, 1) chunk_tc_kernel(const __grid_constant_
                 }
             }
         }
-    } else {
+    } else if (tid < 128) {
         // =============================== state warpgroup ===============================
         // Per chunk c, the dependency chain through the state is
         //   S -> X = K S -> V - X -> U^ -> u -> S + K^T u;
-        // the outputs O = Q S + P u are formed beside it (O1 after X, O2 after the
-        // state update) and written out while the next chunk's X is computed.
-        const int j = tid;
+        // this warpgroup forms the operands of each link in TMEM and the MMA warp
+        // issues the products.  The outputs O = Q S + P u are formed beside the
+        // chain and written out while the next chunk's X is computed.
+        const int j = tid, lane = tid & 31;
         const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
         {  // initial state -> TMEM (S^T: lane j holds column j of S)
             float r[32];
@@ -496,25 +522,37 @@ __global__ void __launch_bounds__(256, 1) chunk_tc_kernel(const __grid_constant_
             }
             tmem_st_wait();
         }
-        // O^T of chunk cc -> staging (TMA store issued by thread 0 after the next barrier)
-        // or, for a partial chunk of a packed batch, straight to global memory.
-        auto epilogue_load = [&](int cc) -> bool {
+        // O^T of chunk cc (fp32 in TMEM) -> o.  Each warp stages its own 32 columns
+        // ([64 t][32] in its 8 KB slice of the staging buffer) and its lane 0 sends
+        // them with one TMA store, so no cross-warp synchronisation is needed.  A
+        // partial chunk of a packed batch is written with plain stores instead (a
+        // TMA box would spill into the next sequence).
+        auto epilogue = [&](int cc) {
             const long t0c = bos + (long)cc * C;
             const int vc = (int)min((long)C, eos - t0c);
-            const bool direct = varlen && vc < C;
             float ov[64];
             tmem_ld64(lane_base + TM_O, ov);
-            if (!direct) {
+            tc_fence_before();
+            mbar_arrive(&bars->o_free);
+            if (p.cu_seqlens == nullptr || vc == C) {
+                uint8_t *slice = sm + OFF_OST + warp * 8192;
+                if (lane == 0) bulk_wait_read0();  // this warp's previous store has read its slice
+                __syncwarp();
                 if (OUT_BF16) {
-                    __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(sm + OFF_OST) + (j >> 6) * 4096 + (j & 63);
+                    __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(slice) + lane;
 #pragma unroll
-                    for (int t = 0; t < C; ++t) stg[t * 64] = __float2bfloat16_rn(ov[t]);
+                    for (int t = 0; t < C; ++t) stg[t * 32] = __float2bfloat16_rn(ov[t]);
                 } else {
-                    float *stg = reinterpret_cast<float *>(sm + OFF_OST) + (j >> 5) * 2048 + (j & 31);
+                    float *stg = reinterpret_cast<float *>(slice) + lane;
 #pragma unroll
                     for (int t = 0; t < C; ++t) stg[t * 32] = ov[t];
                 }
                 fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_4d(&p.map_o, slice, warp * 32, h, (int)t0c, (int)b);
+                    bulk_commit();
+                }
             } else {
 #pragma unroll
                 for (int t = 0; t < C; ++t) {
@@ -527,23 +565,17 @@ __global__ void __launch_bounds__(256, 1) chunk_tc_kernel(const __grid_constant_
                     }
                 }
             }
-            return direct;
         };
-        auto epilogue_store = [&](int cc) {  // thread 0, after the barrier
-            const int nb = OUT_BF16 ? 2 : 4, bw = OUT_BF16 ? 64 : 32;
-            const int t0c = (int)(bos + (long)cc * C);
-            for (int bx = 0; bx < nb; ++bx) tma_store_4d(&p.map_o, sm + OFF_OST + bx * 8192, bx * bw, h, t0c, (int)b);
-            bulk_commit();
-        };
-        bool aborted = false;
-        for (int c = 0; c < nchunks; ++c) {
+        bool ok = true;
+        for (int c = 0; c < nchunks && ok; ++c) {
             const int st = c & 1, buf = c & 1;
             const long tok0 = bos + (long)c * C;
             const int valid = (int)min((long)C, eos - tok0);
-            const uint32_t kq_s = s_sm + OFF_STAGE + st * STAGE_BYTES;
             const uint8_t *Vt = sm + OFF_STAGE + st * STAGE_BYTES + OFF_V;
 
-            bool ok = wait_bar(&bars->prep_ready[buf], (c >> 1) & 1, abort_flag);
+            ok = wait_bar(&bars->prep_ready[buf], (c >> 1) & 1, abort_flag);
+            if (c > 0) ok = ok && wait_bar(&bars->s_done, (c - 1) & 1, abort_flag);
+            tc_fence_after();
             // S^T -> bf16 hi/lo operand in TMEM
             {
                 float s[32];
@@ -561,51 +593,15 @@ __global__ void __launch_bounds__(256, 1) chunk_tc_kernel(const __grid_constant_
                 }
                 tmem_st_wait();
             }
-            if (j == 0) bulk_wait_read0();  // the staging buffer is free again
             tc_fence_before();
-            if (named_bar_any(BAR_STATE, 128, !ok || *abort_flag)) {
-                aborted = true;
-                break;
-            }
-            if (j == 0) {  // X^T = S^T K^T
-                tc_fence_after();
-                const uint32_t idesc = idesc_bf16_f32(128, 64, 0, 0);
-#pragma unroll
-                for (int part = 0; part < 2; ++part)
-#pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
-                        const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-                        mma_bf16_ts(tmem + TM_X, tmem + TM_SA + part * 64 + ks * 8, smem_desc(kq_s + off, 16, 1024),
-                                    idesc, (part | ks) != 0);
-                    }
-                mma_commit(&bars->x_done);
-            }
+            mbar_arrive(&bars->sa_ready);
             // outputs of chunk c-1 leave while X is computed
-            bool direct_prev = true;
             if (c > 0) {
-                ok = wait_bar(&bars->o_done, (c - 1) & 1, abort_flag) && ok;
+                ok = ok && wait_bar(&bars->o_done, (c - 1) & 1, abort_flag);
                 tc_fence_after();
-                direct_prev = epilogue_load(c - 1);
+                epilogue(c - 1);
             }
-            tc_fence_before();
-            if (named_bar_any(BAR_STATE, 128, !ok || *abort_flag)) {
-                aborted = true;
-                break;
-            }
-            if (j == 0) {
-                if (!direct_prev) epilogue_store(c - 1);
-                tc_fence_after();
-                const uint32_t idesc = idesc_bf16_f32(128, 64, 0, 0);  // O1^T = S^T Q^T
-#pragma unroll
-                for (int part = 0; part < 2; ++part)
-#pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
-                        const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32 + 8192;
-                        mma_bf16_ts(tmem + TM_O, tmem + TM_SA + part * 64 + ks * 8, smem_desc(kq_s + off, 16, 1024),
-                                    idesc, (part | ks) != 0);
-                    }
-            }
-            ok = wait_bar(&bars->x_done, c & 1, abort_flag);
+            ok = ok && wait_bar(&bars->x_done, c & 1, abort_flag);
             tc_fence_after();
             // (V - X)^T -> bf16 hi/lo operand in TMEM
             {
@@ -624,26 +620,8 @@ __global__ void __launch_bounds__(256, 1) chunk_tc_kernel(const __grid_constant_
                 tmem_st_wait();
             }
             tc_fence_before();
-            if (named_bar_any(BAR_STATE, 128, !ok || *abort_flag)) {
-                aborted = true;
-                break;
-            }
-            if (j == 0) {  // U^^T = (V-X)^T T'^T
-                tc_fence_after();
-                const uint32_t idesc = idesc_bf16_f32(128, 64, 0, 0);
-                const uint32_t tp = s_sm + OFF_TP + buf * 16384;
-#pragma unroll
-                for (int part = 0; part < 3; ++part) {
-                    const uint32_t a_col = TM_X + (part == 2 ? 32 : 0);
-                    const uint32_t b_s = tp + (part == 1 ? 8192 : 0);
-#pragma unroll
-                    for (int ks = 0; ks < 4; ++ks)
-                        mma_bf16_ts(tmem + TM_U, tmem + a_col + ks * 8, smem_desc(b_s + ks * 32, 16, 1024), idesc,
-                                    (part | ks) != 0);
-                }
-                mma_commit(&bars->u_done);
-            }
-            ok = wait_bar(&bars->u_done, c & 1, abort_flag);
+            mbar_arrive(&bars->r_ready);
+            ok = ok && wait_bar(&bars->u_done, c & 1, abort_flag);
             tc_fence_after();
             // u^T = U^^T diag(1/n) -> bf16 hi/lo operand in TMEM
             {
@@ -659,12 +637,80 @@ __global__ void __launch_bounds__(256, 1) chunk_tc_kernel(const __grid_constant_
                 tmem_st_wait();
             }
             tc_fence_before();
-            if (named_bar_any(BAR_STATE, 128, !ok || *abort_flag)) {
-                aborted = true;
-                break;
+            mbar_arrive(&bars->u_ready);
+        }
+        // outputs of the last chunk, then the final state
+        ok = ok && wait_bar(&bars->o_done, (nchunks - 1) & 1, abort_flag) &&
+             wait_bar(&bars->s_done, (nchunks - 1) & 1, abort_flag);
+        if (!ok) *abort_flag = 1;
+        if (ok) {
+            tc_fence_after();
+            epilogue(nchunks - 1);
+            if (p.S_T) {
+                float s64[64];
+                tmem_ld64(lane_base + TM_S, s64);
+#pragma unroll
+                for (int i = 0; i < 64; ++i) p.S_T[sbase + (size_t)i * D + j] = s64[i];
+                tmem_ld64(lane_base + TM_S + 64, s64);
+#pragma unroll
+                for (int i = 0; i < 64; ++i) p.S_T[sbase + (size_t)(64 + i) * D + j] = s64[i];
             }
-            if (j == 0) {  // S^T += u^T K  (the chain), then O^T += u^T P^T
-                tc_fence_after();
+        }
+        if (lane == 0) bulk_wait0();  // TMA stores have completed before the CTA leaves
+    } else if (tid == 256) {
+        // ================================ MMA warp (one thread) ================================
+        bool ok = true;
+        for (int c = 0; c < nchunks && ok; ++c) {
+            const int st = c & 1, buf = c & 1;
+            const uint32_t kq_s = s_sm + OFF_STAGE + st * STAGE_BYTES;
+            ok = wait_bar(&bars->prep_ready[buf], (c >> 1) & 1, abort_flag) &&
+                 wait_bar(&bars->sa_ready, c & 1, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            {  // X^T = S^T K^T
+                const uint32_t idesc = idesc_bf16_f32(128, 64, 0, 0);
+#pragma unroll
+                for (int part = 0; part < 2; ++part)
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+                        mma_bf16_ts(tmem + TM_X, tmem + TM_SA + part * 64 + ks * 8, smem_desc(kq_s + off, 16, 1024),
+                                    idesc, (part | ks) != 0);
+                    }
+                mma_commit(&bars->x_done);
+            }
+            if (c > 0 && !(ok = wait_bar(&bars->o_free, (c - 1) & 1, abort_flag))) break;
+            tc_fence_after();
+            {  // O1^T = S^T Q^T
+                const uint32_t idesc = idesc_bf16_f32(128, 64, 0, 0);
+#pragma unroll
+                for (int part = 0; part < 2; ++part)
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32 + 8192;
+                        mma_bf16_ts(tmem + TM_O, tmem + TM_SA + part * 64 + ks * 8, smem_desc(kq_s + off, 16, 1024),
+                                    idesc, (part | ks) != 0);
+                    }
+            }
+            if (!(ok = wait_bar(&bars->r_ready, c & 1, abort_flag))) break;
+            tc_fence_after();
+            {  // U^^T = (V-X)^T T'^T
+                const uint32_t idesc = idesc_bf16_f32(128, 64, 0, 0);
+                const uint32_t tp = s_sm + OFF_TP + buf * 16384;
+#pragma unroll
+                for (int part = 0; part < 3; ++part) {
+                    const uint32_t a_col = TM_X + (part == 2 ? 32 : 0);
+                    const uint32_t b_s = tp + (part == 1 ? 8192 : 0);
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_bf16_ts(tmem + TM_U, tmem + a_col + ks * 8, smem_desc(b_s + ks * 32, 16, 1024), idesc,
+                                    (part | ks) != 0);
+                }
+                mma_commit(&bars->u_done);
+            }
+            if (!(ok = wait_bar(&bars->u_ready, c & 1, abort_flag))) break;
+            tc_fence_after();
+            {  // S^T += u^T K  (the chain), then O^T += u^T P^T
                 const uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 1);
 #pragma unroll
                 for (int part = 0; part < 2; ++part)
@@ -686,29 +732,12 @@ __global__ void __launch_bounds__(256, 1) chunk_tc_kernel(const __grid_constant_
                 mma_commit(&bars->o_done);
                 mma_commit(&bars->chunk_done[c & 1]);
             }
-            if (!wait_bar(&bars->s_done, c & 1, abort_flag)) *abort_flag = 1;
-            tc_fence_after();
         }
-        // outputs of the last chunk
-        bool ok = !aborted && wait_bar(&bars->o_done, (nchunks - 1) & 1, abort_flag);
-        tc_fence_after();
-        if (j == 0) bulk_wait_read0();
-        if (!named_bar_any(BAR_STATE, 128, !ok || *abort_flag)) {
-            const bool direct = epilogue_load(nchunks - 1);
-            tc_fence_before();
-            named_bar(BAR_STATE, 128);
-            if (j == 0 && !direct) epilogue_store(nchunks - 1);
-        }
-        if (j == 0) bulk_wait0();
-        if (!*abort_flag && p.S_T) {
-            tc_fence_after();
-            float s64[64];
-            tmem_ld64(lane_base + TM_S, s64);
-#pragma unroll
-            for (int i = 0; i < 64; ++i) p.S_T[sbase + (size_t)i * D + j] = s64[i];
-            tmem_ld64(lane_base + TM_S + 64, s64);
-#pragma unroll
-            for (int i = 0; i < 64; ++i) p.S_T[sbase + (size_t)(64 + i) * D + j] = s64[i];
+        if (!ok) *abort_flag = 1;
+        // every MMA this thread issued has completed before TMEM is released (bounded)
+        mma_commit(&bars->drain[0]);
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait_sleep(&bars->drain[0], 0, 20000) && globaltimer_ns() - t0 < WAIT_NS) {
         }
     }
 
@@ -759,7 +788,7 @@ cudaError_t launch_typed(const TcParams &p, unsigned grid, cudaStream_t stream) 
         if (e != cudaSuccess) return e;
         if (dev < 64) attr_done[dev] = true;
     }
-    chunk_tc_kernel<OUT_BF16><<<grid, 256, SMEM_ALLOC, stream>>>(p);
+    chunk_tc_kernel<OUT_BF16><<<grid, 288, SMEM_ALLOC, stream>>>(p);
     return cudaGetLastError();
 }
 
@@ -774,7 +803,7 @@ cudaError_t launch_chunk_tc(const FwdArgs &a, const char **why) {
         if (!make_map(&p.map_q, a.q, a.B, a.T, a.H, false, 64, true) ||
             !make_map(&p.map_k, a.k, a.B, a.T, a.H, false, 64, true) ||
             !make_map(&p.map_v, a.v, a.B, a.T, a.H, false, 64, true) ||
-            !make_map(&p.map_o, a.o, a.B, a.T, a.H, !o_bf16, o_bf16 ? 64 : 32, false)) {
+            !make_map(&p.map_o, a.o, a.B, a.T, a.H, !o_bf16, 32, false)) {
             *why = "cuTensorMapEncodeTiled failed";
             return cudaErrorInvalidValue;
         }
