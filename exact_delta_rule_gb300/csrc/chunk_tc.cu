@@ -13,6 +13,7 @@
 //   T~  = (I + A~)^{-1}                                            (blocked forward substitution)
 //   T'  = T~ diag(gamma / n)
 //   U^  = T' (V - K S)            u_t = U^_t / n_t   (= the rank-1 write u_t of token t)
+//   so u = T'' (K S - V) with T'' = -diag(1/n) T~ diag(gamma / n).
 //   O   = Q S + (Q K^T o M) u     (M lower-triangular INCLUDING the diagonal:
 //                                  o_t reads the state after token t's update)
 //   S  <- S + K^T u
@@ -33,8 +34,9 @@
 // that the state's d_v index is the MMA row (TMEM lane) and the operands S^T,
 // (V - X)^T and u^T are written into TMEM by the thread that owns the lane and
 // read from there by the tensor core:
-//   [X^T | O1^T] = S^T [K ; Q]^T     (M = d_v = 128, N = 2C = 128, K = d_k = 128)
-//   U^^T         = (V - X)^T T'^T    (M = 128, N = C, K = C)
+//   D^T  = V^T (-I) + S^T K^T = (K S - V)^T   (M = d_v = 128, N = C, K = C and d_k)
+//   O1^T = S^T Q^T                            (M = 128, N = C, K = d_k)
+//   u^T  = D^T T''^T,  T'' = -diag(1/n) T'    (M = 128, N = C, K = C)
 //   O^T         += u^T P^T,  P = Q K^T o M   (M = 128, N = C, K = C)
 //   S^T         += u^T K             (M = 128, N = d_k = 128, K = C; K as MN-major operand)
 // and G = [K ; Q] K^T (M = 2C = 128, N = C, K = d_k) gives the chunk's Gram terms.
@@ -73,10 +75,11 @@ constexpr uint32_t AT_LD = 65;
 constexpr uint32_t OFF_ROW = OFF_AT + 64 * AT_LD * 4;  // fp32: invn[2][64], gn[2][64], beta[64]
 constexpr uint32_t ROW_BYTES = 6 * 64 * 4;
 constexpr uint32_t OFF_BAR = OFF_ROW + ROW_BYTES;       // mbarriers (struct Bars)
-constexpr uint32_t OFF_MISC = OFF_BAR + 192;            // tmem base (u32), abort flag (i32)
+constexpr uint32_t OFF_MISC = OFF_BAR + 224;            // tmem base (u32), abort flag (i32)
 constexpr uint32_t OFF_SCR = OFF_MISC + 16;             // fp32 scratch of the triangular inverse
 constexpr uint32_t SCR_FLOATS = 32 * 33;
-constexpr uint32_t SMEM_USED = OFF_SCR + SCR_FLOATS * 4;
+constexpr uint32_t OFF_NEGI = (OFF_SCR + SCR_FLOATS * 4 + 1023) & ~1023u;  // -I, 64x64 bf16 (K-major, swizzled)
+constexpr uint32_t SMEM_USED = OFF_NEGI + 8192;
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;       // + alignment slack for the 1024-byte base
 static_assert(OFF_TP == 2 * STAGE_BYTES && OFF_P == OFF_TP + 32768 && OFF_OST == OFF_P + 32768 &&
                   OFF_AT == OFF_OST + 32768,
@@ -124,8 +127,9 @@ struct Bars {
     uint64_t r_ready;        // state warpgroup wrote (V - X)^T hi/lo  (128 arrivals)
     uint64_t u_ready;        // state warpgroup wrote u^T hi/lo        (128 arrivals)
     uint64_t drain[2];       // all MMAs of the MMA thread / of the prep thread complete
+    uint64_t s_free[2];      // the state update of a chunk complete: its K/Q/V stage is free
 };
-static_assert(sizeof(Bars) <= 192, "mbarrier block exceeds its slot");
+static_assert(sizeof(Bars) <= 224, "mbarrier block exceeds its slot");
 
 // Bounded wait that also gives up when the other warpgroup has aborted.
 __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
@@ -288,7 +292,7 @@ __device__ __forceinline__ void invert_unit_lower(float *At, float *Y, int pt) {
 }
 
 template <bool OUT_BF16>
-__global__ void __launch_bounds__(288, 1) chunk_tc_kernel(const __grid_constant__ TcParams p) {
+__global__ void __launch_bounds__(320, 1) chunk_tc_kernel(const __grid_constant__ TcParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float *row_invn = reinterpret_cast<float *>(sm + OFF_ROW);  // [2][64]
@@ -344,12 +348,32 @@ __global__ void __launch_bounds__(288, 1) chunk_tc_kernel(const __grid_constant_
         mbar_init(&bars->u_ready, 128);
         mbar_init(&bars->drain[0], 1);
         mbar_init(&bars->drain[1], 1);
+        mbar_init(&bars->s_free[0], 1);
+        mbar_init(&bars->s_free[1], 1);
         fence_mbar_init();
         *abort_flag = 0;
     }
     if (warp == 0) {
         tmem_alloc(tmem_slot, TM_COLS);
         tmem_relinquish();
+    }
+    if (tid >= 128 && tid < 192) {  // -I as a K-major bf16 operand: row t holds -1 in column t
+        const int t = tid - 128;
+        uint8_t *negi = sm + OFF_NEGI;
+#pragma unroll
+        for (int c8 = 0; c8 < 64; c8 += 8) {
+            uint4 w = make_uint4(0, 0, 0, 0);
+            if (t >= c8 && t < c8 + 8) {
+                const uint32_t m1 = 0xBF80u << (16 * ((t - c8) & 1));  // bf16(-1) in the low or high half
+                const int word = (t - c8) >> 1;
+                if (word == 0) w.x = m1;
+                if (word == 1) w.y = m1;
+                if (word == 2) w.z = m1;
+                if (word == 3) w.w = m1;
+            }
+            *reinterpret_cast<uint4 *>(negi + swz_offset(t, c8, 8192)) = w;
+        }
+        fence_proxy_async_smem();
     }
     tc_fence_before();
     __syncthreads();
@@ -361,30 +385,32 @@ __global__ void __launch_bounds__(288, 1) chunk_tc_kernel(const __grid_constant_
         // =============================== prep warpgroup ===============================
         const int pt = tid - 128;
         const uint32_t lane_base = tmem + ((uint32_t)((warp - 4) * 32) << 16);
-        auto issue_tma = [&](int c) {
-            const int st = c & 1;
-            uint8_t *dst = sm + OFF_STAGE + st * STAGE_BYTES;
-            const int tok = (int)(bos + (long)c * C);
-            mbar_arrive_expect_tx(&bars->tma_full[st], STAGE_BYTES);
-            for (int cb = 0; cb < 2; ++cb) {
-                tma_load_4d(dst + cb * 16384, &p.map_k, &bars->tma_full[st], cb * 64, h, tok, (int)b);
-                tma_load_4d(dst + cb * 16384 + 8192, &p.map_q, &bars->tma_full[st], cb * 64, h, tok, (int)b);
-                tma_load_4d(dst + OFF_V + cb * 8192, &p.map_v, &bars->tma_full[st], cb * 64, h, tok, (int)b);
+        int g_issued = 0;  // chunks whose Gram MMA was issued (thread pt == 0)
+        auto issue_gram = [&](int c) {
+            const uint32_t kq = s_sm + OFF_STAGE + (c & 1) * STAGE_BYTES;
+            const uint32_t idesc = idesc_bf16_f32(128, 64, 0, 0);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+                mma_bf16(tmem + TM_G, smem_desc(kq + off, 16, 1024), smem_desc(kq + off, 16, 1024), idesc, ks > 0);
+            }
+            mma_commit(&bars->g_done);
+            g_issued = c + 1;
+        };
+        // Thread pt == 0, during chunk c: start the Gram MMA of chunk c+1 as soon as its tile
+        // has landed (full chunks only: a partial chunk's tail is zeroed first).  Non-blocking.
+        auto prefetch_gram = [&](int c) {
+            if (c + 1 >= nchunks || g_issued != c + 1 || eos - (bos + (long)(c + 1) * C) < C) return;
+            if (mbar_try_wait(&bars->tma_full[(c + 1) & 1], ((c + 1) >> 1) & 1)) {
+                tc_fence_after();
+                issue_gram(c + 1);
             }
         };
-        if (pt == 0) {
-            prefetch_tensormap(&p.map_q);
-            prefetch_tensormap(&p.map_k);
-            prefetch_tensormap(&p.map_v);
-            issue_tma(0);
-        }
-        int issued = 1, landed = 0;  // chunks whose TMA was issued / seen complete
         for (int c = 0; c < nchunks; ++c) {
             const int st = c & 1, buf = c & 1;
             const long tok0 = bos + (long)c * C;
             const int valid = (int)min((long)C, eos - tok0);
             uint8_t *KQ = sm + OFF_STAGE + st * STAGE_BYTES;
-            const uint32_t kq_s = s_sm + OFF_STAGE + st * STAGE_BYTES;
 
             if (pt < C) row_beta[pt] = pt < valid ? p.beta[((size_t)b * p.T + (size_t)(tok0 + pt)) * p.H + h] : 0.f;
             bool ok = wait_bar(&bars->tma_full[st], (c >> 1) & 1, abort_flag);
@@ -402,25 +428,20 @@ __global__ void __launch_bounds__(288, 1) chunk_tc_kernel(const __grid_constant_
                 *abort_flag = 1;
                 break;
             }
-            landed = c + 1;
 
-            // Gram products G = [K;Q] K^T
-            if (pt == 0) {
+            // Gram products G = [K;Q] K^T (unless already started during the previous chunk)
+            if (pt == 0 && g_issued == c) {
                 tc_fence_after();
-                const uint32_t idesc = idesc_bf16_f32(128, 64, 0, 0);
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-                    mma_bf16(tmem + TM_G, smem_desc(kq_s + off, 16, 1024), smem_desc(kq_s + off, 16, 1024), idesc,
-                             ks > 0);
-                }
-                mma_commit(&bars->g_done);
+                issue_gram(c);
             }
             ok = wait_bar(&bars->g_done, c & 1, abort_flag);
+            // the T''/P buffers of this chunk were last read by chunk c-2's MMAs
+            if (c >= 2) ok = wait_bar(&bars->chunk_done[c & 1], ((c - 2) >> 1) & 1, abort_flag) && ok;
             tc_fence_after();
             {
                 float g[64];
                 tmem_ld64(lane_base + TM_G, g);
+                tc_fence_before();  // the next Gram MMA may overwrite TM_G once every row is read
                 // [gate: G row loaded]
                 if (pt < C) {  // K K^T row t -> gate terms, then A~ row t
                     const int t = pt;
@@ -456,17 +477,20 @@ __global__ void __launch_bounds__(288, 1) chunk_tc_kernel(const __grid_constant_
                 }
             }
             named_bar(BAR_PREP, 128);
+            if (pt == 0) prefetch_gram(c);
             invert_unit_lower(At, scr, pt);
-            {  // T' = T~ diag(gamma/n), lower triangle, as bf16 hi/lo [t][s]
+            if (pt == 0) prefetch_gram(c);
+            {  // T'' = -diag(1/n) T~ diag(gamma/n), lower triangle, as bf16 hi/lo [t][s]
                 const int t = pt >> 1, s0 = (pt & 1) * 32;
                 uint8_t *hi = sm + OFF_TP + buf * 16384, *lo = hi + 8192;
+                const float rsc = -row_invn[buf * 64 + t];
 #pragma unroll
                 for (int c8 = 0; c8 < 32; c8 += 8) {
                     float x[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
                         const int s = s0 + c8 + e;
-                        x[e] = s <= t ? At[t * AT_LD + s] * row_gn[buf * 64 + s] : 0.f;
+                        x[e] = s <= t ? rsc * At[t * AT_LD + s] * row_gn[buf * 64 + s] : 0.f;
                     }
                     uint32_t hh[4], ll[4];
                     split_pack<4>(x, hh, ll);
@@ -478,29 +502,16 @@ __global__ void __launch_bounds__(288, 1) chunk_tc_kernel(const __grid_constant_
             fence_proxy_async_smem();
             named_bar(BAR_PREP, 128);
             if (pt == 0) mbar_arrive(&bars->prep_ready[buf]);
-            // the stage and the T'/P buffers of chunk c-1 are free once its state MMAs completed
-            if (c >= 1) ok = wait_bar(&bars->chunk_done[(c - 1) & 1], ((c - 1) >> 1) & 1, abort_flag) && ok;
+            if (pt == 0) prefetch_gram(c);
             if (named_bar_any(BAR_PREP, 128, !ok || *abort_flag)) {
                 *abort_flag = 1;
                 break;
-            }
-            if (c + 1 < nchunks) {
-                if (pt == 0) issue_tma(c + 1);
-                issued = c + 2;
             }
         }
         if (pt == 0) {  // every Gram MMA has completed before TMEM is released (bounded)
             mma_commit(&bars->drain[1]);
             const uint64_t t0 = globaltimer_ns();
             while (!mbar_try_wait_sleep(&bars->drain[1], 0, 20000) && globaltimer_ns() - t0 < WAIT_NS) {
-            }
-        }
-        if (pt == 0) {  // after an abort, let TMA loads still in flight land (bounded)
-            for (int cc = landed; cc < issued; ++cc) {
-                const uint64_t t0 = globaltimer_ns();
-                while (!mbar_try_wait(&bars->tma_full[cc & 1], (cc >> 1) & 1) &&
-                       globaltimer_ns() - t0 < WAIT_NS / 4) {
-                }
             }
         }
     } else if (tid < 128) {
@@ -568,11 +579,9 @@ __global__ void __launch_bounds__(288, 1) chunk_tc_kernel(const __grid_constant_
         };
         bool ok = true;
         for (int c = 0; c < nchunks && ok; ++c) {
-            const int st = c & 1, buf = c & 1;
+            const int buf = c & 1;
             const long tok0 = bos + (long)c * C;
             const int valid = (int)min((long)C, eos - tok0);
-            const uint8_t *Vt = sm + OFF_STAGE + st * STAGE_BYTES + OFF_V;
-
             ok = wait_bar(&bars->prep_ready[buf], (c >> 1) & 1, abort_flag);
             if (c > 0) ok = ok && wait_bar(&bars->s_done, (c - 1) & 1, abort_flag);
             tc_fence_after();
@@ -603,16 +612,12 @@ __global__ void __launch_bounds__(288, 1) chunk_tc_kernel(const __grid_constant_
             }
             ok = ok && wait_bar(&bars->x_done, c & 1, abort_flag);
             tc_fence_after();
-            // (V - X)^T -> bf16 hi/lo operand in TMEM
+            // D^T = (K S - V)^T -> bf16 hi/lo operand in TMEM (rows past the sequence end are zero)
             {
                 float x[64];
                 tmem_ld64(lane_base + TM_X, x);
 #pragma unroll
-                for (int t = 0; t < C; ++t) {
-                    const float vv =
-                        __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(Vt + swz_offset(t, j, 8192)));
-                    x[t] = t < valid ? vv - x[t] : 0.f;
-                }
+                for (int t = 0; t < C; ++t) x[t] = t < valid ? x[t] : 0.f;
                 uint32_t hi[32], lo[32];
                 split_pack<32>(x, hi, lo);
                 tmem_st32u(lane_base + TM_X, hi);
@@ -623,13 +628,10 @@ __global__ void __launch_bounds__(288, 1) chunk_tc_kernel(const __grid_constant_
             mbar_arrive(&bars->r_ready);
             ok = ok && wait_bar(&bars->u_done, c & 1, abort_flag);
             tc_fence_after();
-            // u^T = U^^T diag(1/n) -> bf16 hi/lo operand in TMEM
+            // u^T -> bf16 hi/lo operand in TMEM
             {
                 float u[64];
                 tmem_ld64(lane_base + TM_U, u);
-                const float *invn = row_invn + buf * 64;
-#pragma unroll
-                for (int t = 0; t < C; ++t) u[t] *= invn[t];
                 uint32_t hi[32], lo[32];
                 split_pack<32>(u, hi, lo);
                 tmem_st32u(lane_base + TM_U, hi);
@@ -657,17 +659,53 @@ __global__ void __launch_bounds__(288, 1) chunk_tc_kernel(const __grid_constant_
             }
         }
         if (lane == 0) bulk_wait0();  // TMA stores have completed before the CTA leaves
+    } else if (tid == 288) {
+        // ============================ TMA producer (one thread) ============================
+        // Chunk c goes into stage c % 2 once the state update of chunk c-2 (the last
+        // reader of that stage) has completed.
+        prefetch_tensormap(&p.map_q);
+        prefetch_tensormap(&p.map_k);
+        prefetch_tensormap(&p.map_v);
+        int issued = 0;
+        for (int c = 0; c < nchunks; ++c) {
+            if (c >= 2 && !wait_bar(&bars->s_free[c & 1], ((c - 2) >> 1) & 1, abort_flag)) break;
+            const int st = c & 1;
+            uint8_t *dst = sm + OFF_STAGE + st * STAGE_BYTES;
+            const int tok = (int)(bos + (long)c * C);
+            mbar_arrive_expect_tx(&bars->tma_full[st], STAGE_BYTES);
+            for (int cb = 0; cb < 2; ++cb) {
+                tma_load_4d(dst + cb * 16384, &p.map_k, &bars->tma_full[st], cb * 64, h, tok, (int)b);
+                tma_load_4d(dst + cb * 16384 + 8192, &p.map_q, &bars->tma_full[st], cb * 64, h, tok, (int)b);
+                tma_load_4d(dst + OFF_V + cb * 8192, &p.map_v, &bars->tma_full[st], cb * 64, h, tok, (int)b);
+            }
+            issued = c + 1;
+        }
+        // the last loads have landed before the CTA can leave (bounded; matters after an abort)
+        for (int cc = max(0, issued - 2); cc < issued; ++cc) {
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait_sleep(&bars->tma_full[cc & 1], (cc >> 1) & 1, 20000) &&
+                   globaltimer_ns() - t0 < WAIT_NS) {
+            }
+        }
     } else if (tid == 256) {
         // ================================ MMA warp (one thread) ================================
         bool ok = true;
         for (int c = 0; c < nchunks && ok; ++c) {
             const int st = c & 1, buf = c & 1;
             const uint32_t kq_s = s_sm + OFF_STAGE + st * STAGE_BYTES;
-            ok = wait_bar(&bars->prep_ready[buf], (c >> 1) & 1, abort_flag) &&
-                 wait_bar(&bars->sa_ready, c & 1, abort_flag);
-            if (!ok) break;
+            if (!(ok = wait_bar(&bars->prep_ready[buf], (c >> 1) & 1, abort_flag))) break;
             tc_fence_after();
-            {  // X^T = S^T K^T
+            {  // D^T = V^T (-I): V^T is the stage's V tile read as an MN-major operand
+                const uint32_t idesc = idesc_bf16_f32(128, 64, 1, 0);
+                const uint32_t v_s = kq_s + OFF_V, ni = s_sm + OFF_NEGI;
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_bf16(tmem + TM_X, smem_desc(v_s + ks * 2048, 8192, 1024), smem_desc(ni + ks * 32, 16, 1024),
+                             idesc, ks > 0);
+            }
+            if (!(ok = wait_bar(&bars->sa_ready, c & 1, abort_flag))) break;
+            tc_fence_after();
+            {  // D^T += S^T K^T
                 const uint32_t idesc = idesc_bf16_f32(128, 64, 0, 0);
 #pragma unroll
                 for (int part = 0; part < 2; ++part)
@@ -675,7 +713,7 @@ __global__ void __launch_bounds__(288, 1) chunk_tc_kernel(const __grid_constant_
                     for (int ks = 0; ks < 8; ++ks) {
                         const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
                         mma_bf16_ts(tmem + TM_X, tmem + TM_SA + part * 64 + ks * 8, smem_desc(kq_s + off, 16, 1024),
-                                    idesc, (part | ks) != 0);
+                                    idesc, 1);
                     }
                 mma_commit(&bars->x_done);
             }
@@ -694,7 +732,7 @@ __global__ void __launch_bounds__(288, 1) chunk_tc_kernel(const __grid_constant_
             }
             if (!(ok = wait_bar(&bars->r_ready, c & 1, abort_flag))) break;
             tc_fence_after();
-            {  // U^^T = (V-X)^T T'^T
+            {  // u^T = D^T T''^T
                 const uint32_t idesc = idesc_bf16_f32(128, 64, 0, 0);
                 const uint32_t tp = s_sm + OFF_TP + buf * 16384;
 #pragma unroll
@@ -719,6 +757,7 @@ __global__ void __launch_bounds__(288, 1) chunk_tc_kernel(const __grid_constant_
                         mma_bf16_ts(tmem + TM_S, tmem + TM_U + part * 32 + ks * 8,
                                     smem_desc(kq_s + ks * 2048, 16384, 1024), idesc_s, 1);
                 mma_commit(&bars->s_done);
+                mma_commit(&bars->s_free[c & 1]);
                 const uint32_t idesc_o = idesc_bf16_f32(128, 64, 0, 0);
                 const uint32_t pb = s_sm + OFF_P + buf * 16384;
 #pragma unroll
@@ -788,7 +827,7 @@ cudaError_t launch_typed(const TcParams &p, unsigned grid, cudaStream_t stream) 
         if (e != cudaSuccess) return e;
         if (dev < 64) attr_done[dev] = true;
     }
-    chunk_tc_kernel<OUT_BF16><<<grid, 288, SMEM_ALLOC, stream>>>(p);
+    chunk_tc_kernel<OUT_BF16><<<grid, 320, SMEM_ALLOC, stream>>>(p);
     return cudaGetLastError();
 }
 
