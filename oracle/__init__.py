@@ -69,10 +69,10 @@ def _load():
             lp = ctypes.POINTER(ctypes.c_int64)
             lib.efla_oracle_alpha.restype = ctypes.c_double
             lib.efla_oracle_alpha.argtypes = [ctypes.c_double, ctypes.c_double]
-            lib.efla_oracle_fwd.restype = ctypes.c_int
-            lib.efla_oracle_fwd.argtypes = [dp, dp, dp, dp, dp, lp, dp, dp] + [ctypes.c_int] * 7
-            lib.efla_oracle_decode.restype = ctypes.c_int
-            lib.efla_oracle_decode.argtypes = [dp, dp, dp, dp, dp, dp] + [ctypes.c_int] * 5
+            lib.efla_oracle_fwd_mode.restype = ctypes.c_int
+            lib.efla_oracle_fwd_mode.argtypes = [dp, dp, dp, dp, dp, lp, dp, dp] + [ctypes.c_int] * 8
+            lib.efla_oracle_decode_mode.restype = ctypes.c_int
+            lib.efla_oracle_decode_mode.argtypes = [dp, dp, dp, dp, dp, dp] + [ctypes.c_int] * 6
             lib.efla_oracle_max_threads.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -101,8 +101,11 @@ def max_threads() -> int:
     return _load().efla_oracle_max_threads()
 
 
-def fwd(q, k, v, beta, S0=None, cu_seqlens=None, *, threads: int = 0):
-    """Sequential fp64 EFLA forward.
+_UPDATES = {"exact": 0, "euler": 1}
+
+
+def fwd(q, k, v, beta, S0=None, cu_seqlens=None, *, threads: int = 0, update: str = "exact"):
+    """Sequential fp64 EFLA forward (``update="euler"``: the DeltaNet step, alpha = beta).
 
     q, k: [B, T, H, dk]; v: [B, T, H, dv]; beta: [B, T, H]; S0: [N, H, dk, dv] or None;
     cu_seqlens: [N+1] or None (then N = B).  Inputs of any float dtype are
@@ -122,15 +125,15 @@ def fwd(q, k, v, beta, S0=None, cu_seqlens=None, *, threads: int = 0):
         N = B
     o = np.zeros((B, T, H, dv), dtype=np.float64)
     S_T = np.zeros((N, H, dk, dv), dtype=np.float64)
-    rc = _load().efla_oracle_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(S0),
-                                 _ptr(cu, ctypes.c_int64), _ptr(o), _ptr(S_T),
-                                 B, T, H, dk, dv, N, int(threads))
+    rc = _load().efla_oracle_fwd_mode(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(S0),
+                                      _ptr(cu, ctypes.c_int64), _ptr(o), _ptr(S_T),
+                                      B, T, H, dk, dv, N, int(threads), _UPDATES[update])
     if rc != 0:
         raise ValueError(f"efla_oracle_fwd failed with code {rc}")
     return o, S_T
 
 
-def decode_step(q, k, v, beta, S, *, threads: int = 0):
+def decode_step(q, k, v, beta, S, *, threads: int = 0, update: str = "exact"):
     """One fp64 decode step.  q,k: [B,H,dk]; v: [B,H,dv]; beta: [B,H]; S: [B,H,dk,dv].
 
     Returns (o [B,H,dv], S_new [B,H,dk,dv]); the input S is not modified.
@@ -140,8 +143,8 @@ def decode_step(q, k, v, beta, S, *, threads: int = 0):
     B, H, dk = q.shape
     dv = v.shape[-1]
     o = np.zeros((B, H, dv), dtype=np.float64)
-    rc = _load().efla_oracle_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(S), _ptr(o),
-                                    B, H, dk, dv, int(threads))
+    rc = _load().efla_oracle_decode_mode(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(S), _ptr(o),
+                                         B, H, dk, dv, int(threads), _UPDATES[update])
     if rc != 0:
         raise ValueError(f"efla_oracle_decode failed with code {rc}")
     return o, S

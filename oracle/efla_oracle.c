@@ -23,6 +23,11 @@
  *   o_t     = S_t^T q_t   (the state AFTER token t's update)
  *       [howistudyai, Step 3 and "Putting it all together (pipeline)"]
  *
+ * With `euler` set, the gate is alpha_t = beta_t: the explicit-Euler (delta rule,
+ * DeltaNet) step S_t = (I - beta_t k_t k_t^T) S_{t-1} + beta_t k_t v_t^T that the
+ * pages compare EFLA against [howistudyai, "Delta Rule (Linear Attention as
+ * Online Learning)"; gist.science, "Enunciato del Problema"].
+ *
  * The update is evaluated in the factored form
  *   x = S_{t-1}^T k_t;   S_t = S_{t-1} + alpha_t k_t (v_t - x)^T,
  * which is the same matrix as (I - alpha k k^T) S + alpha k v^T by
@@ -55,12 +60,12 @@ double efla_oracle_alpha(double beta, double lam)
 
 /* One token of one head: updates S (dk x dv) in place and writes o (dv). */
 static void oracle_token(const double *q, const double *k, const double *v, double beta,
-                         double *S, double *o, int dk, int dv, double *x)
+                         double *S, double *o, int dk, int dv, double *x, int euler)
 {
     double lam = 0.0;
     for (int i = 0; i < dk; ++i)
         lam += k[i] * k[i];
-    const double a = efla_oracle_alpha(beta, lam);
+    const double a = euler ? beta : efla_oracle_alpha(beta, lam);
 
     for (int j = 0; j < dv; ++j)
         x[j] = 0.0;
@@ -80,9 +85,9 @@ static void oracle_token(const double *q, const double *k, const double *v, doub
 }
 
 /* Returns 0 on success, -1 on bad arguments, -2 on allocation failure. */
-int efla_oracle_fwd(const double *q, const double *k, const double *v, const double *beta,
-                    const double *S0, const int64_t *cu_seqlens, double *o, double *S_T,
-                    int B, int T, int H, int dk, int dv, int N, int nthreads)
+int efla_oracle_fwd_mode(const double *q, const double *k, const double *v, const double *beta,
+                         const double *S0, const int64_t *cu_seqlens, double *o, double *S_T,
+                         int B, int T, int H, int dk, int dv, int N, int nthreads, int euler)
 {
     if (B < 0 || T < 0 || H <= 0 || dk <= 0 || dv <= 0 || N < 0)
         return -1;
@@ -130,7 +135,7 @@ int efla_oracle_fwd(const double *q, const double *k, const double *v, const dou
         for (long t = t0; t < t1; ++t) {
             const size_t row = ((size_t)b * T + t) * H + h;
             oracle_token(q + row * dk, k + row * dk, v + row * dv, beta[row], S, o + row * dv,
-                         dk, dv, x);
+                         dk, dv, x, euler);
         }
         if (S_T)
             memcpy(S_T + ((size_t)n * H + h) * dk * dv, S, sizeof(double) * (size_t)dk * dv);
@@ -140,9 +145,16 @@ int efla_oracle_fwd(const double *q, const double *k, const double *v, const dou
     return failed ? -2 : 0;
 }
 
+int efla_oracle_fwd(const double *q, const double *k, const double *v, const double *beta,
+                    const double *S0, const int64_t *cu_seqlens, double *o, double *S_T,
+                    int B, int T, int H, int dk, int dv, int N, int nthreads)
+{
+    return efla_oracle_fwd_mode(q, k, v, beta, S0, cu_seqlens, o, S_T, B, T, H, dk, dv, N, nthreads, 0);
+}
+
 /* One decode step for B*H independent heads; S [B, H, dk, dv] updated in place. */
-int efla_oracle_decode(const double *q, const double *k, const double *v, const double *beta,
-                       double *S, double *o, int B, int H, int dk, int dv, int nthreads)
+int efla_oracle_decode_mode(const double *q, const double *k, const double *v, const double *beta,
+                            double *S, double *o, int B, int H, int dk, int dv, int nthreads, int euler)
 {
     if (B < 0 || H <= 0 || dk <= 0 || dv <= 0)
         return -1;
@@ -160,10 +172,16 @@ int efla_oracle_decode(const double *q, const double *k, const double *v, const 
             continue;
         }
         oracle_token(q + u * dk, k + u * dk, v + u * dv, beta[u], S + u * (size_t)dk * dv,
-                     o + u * dv, dk, dv, x);
+                     o + u * dv, dk, dv, x, euler);
         free(x);
     }
     return failed ? -2 : 0;
+}
+
+int efla_oracle_decode(const double *q, const double *k, const double *v, const double *beta,
+                       double *S, double *o, int B, int H, int dk, int dv, int nthreads)
+{
+    return efla_oracle_decode_mode(q, k, v, beta, S, o, B, H, dk, dv, nthreads, 0);
 }
 
 int efla_oracle_max_threads(void)

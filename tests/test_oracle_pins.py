@@ -348,3 +348,29 @@ def test_oracle_rejects_bad_bounds():
         oracle.fwd(q, q, q, np.zeros((1, 4, 1)), None, np.array([0, 3, 2, 4]))
     with pytest.raises(ValueError):
         oracle.fwd(q, q, q, np.zeros((1, 4, 1)), None, np.array([0, 3]))
+
+
+# ------------------------------------------------------------- Euler (DeltaNet) mode
+def test_euler_mode_matches_literal_deltanet():
+    """update="euler" is the delta-rule step S <- (I - beta k k^T) S + beta k v^T
+    (howistudyai, "Delta Rule"), checked against the literal matrix form."""
+    q, k, v, beta, S0 = _head(60, 29, 6, 5)
+    o, S = oracle.fwd(q[None, :, None], k[None, :, None], v[None, :, None], beta[None, :, None],
+                      S0[None, None], update="euler")
+    o_l, S_l = literal.run_literal(literal.deltanet_step_literal, S0, q, k, v, beta)
+    np.testing.assert_allclose(o[0, :, 0], o_l, rtol=0, atol=1e-11 * (1 + np.abs(o_l).max()))
+    np.testing.assert_allclose(S[0, 0], S_l, rtol=0, atol=1e-11 * (1 + np.abs(S_l).max()))
+    o_d, S_d = oracle.decode_step(q[0][None, None], k[0][None, None], v[0][None, None],
+                                  np.array([[beta[0]]]), S0[None, None], update="euler")
+    o_l1, S_l1 = literal.deltanet_step_literal(S0, q[0], k[0], v[0], beta[0])
+    np.testing.assert_allclose(S_d[0, 0], S_l1, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(o_d[0, 0], o_l1, rtol=0, atol=1e-12)
+
+
+def test_euler_and_exact_differ_for_large_keys():
+    """The two updates are different methods: with beta*lambda ~ 4 they disagree."""
+    q, k, v, beta, S0 = _head(61, 10, 4, 3, key_scale=2.0)
+    _, S_e = _fwd1(S0, q, k, v, beta)
+    _, S_d = oracle.fwd(q[None, :, None], k[None, :, None], v[None, :, None], beta[None, :, None],
+                        S0[None, None], update="euler")
+    assert np.abs(S_e - S_d[0, 0]).max() > 0.1
