@@ -301,6 +301,22 @@ def run_ours(args, world, rank, local):
     # ---- decode step (secondary figure): B256 H32 d128, CUDA graph of chained steps
     dec = decode_figures(efla, dev, stream)
 
+    # ---- the same forward with the delta-rule (DeltaNet) gate, L2-normalised keys
+    kn = (k.float() / k.float().norm(dim=-1, keepdim=True).clamp_min(1e-6)).to(k.dtype)
+    t_dn = time_steps(lambda: efla.fwd_chunked(q, kn, v, beta, None, None, o=o, S_T=S_T, chunk=CHUNK,
+                                               stream=stream, update="euler"), args.steps, flush, stream)
+    deltanet = {"workload": "lm shape, delta-rule gate alpha = beta, unit-norm keys",
+                "ms_per_step": 1e3 * t_dn, "tokens_per_s": tokens / H / t_dn,
+                "efla_time_over_deltanet_time": avg / t_dn}
+
+    # ---- prep kernel: lambda, alpha, alpha*k, alpha*v for every token-head of the lm workload
+    t_pr = time_steps(lambda: efla.prep(k, beta, v, lam=True, alpha=True, ak=True, av=True, stream=stream),
+                      args.steps, flush, stream)
+    pr_bytes = tokens * (2 * dk * 2 + 2 * dv * 2 + 12)
+    prep_fig = {"workload": "lm: 262144 token-head rows, bf16 k, v in, lambda/alpha fp32 and alpha*k, alpha*v bf16 out",
+                "us_per_call": 1e6 * t_pr, "GB/s": pr_bytes / t_pr / 1e9, "bytes_per_call": pr_bytes,
+                "frac_hbm": pr_bytes / t_pr / 1e9 / peaks["hbm_gbs"]}
+
     # ---- CPU baseline: the oracle on a bounded sample of the same workload
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -332,9 +348,29 @@ def run_ours(args, world, rank, local):
             "gpu_launches": args.steps,
             "clocks": clk.summary(),
             "decode": dec,
+            "deltanet": deltanet,
+            "prep": prep_fig,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
+
+
+def time_steps(fn, steps, flush, stream):
+    """Average seconds of `fn` over `steps` calls, L2 flushed before each, CUDA events."""
+    import torch
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    total = 0.0
+    for i in range(steps):
+        flush.fill_(float(i))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        b.synchronize()
+        total += a.elapsed_time(b) / 1e3
+    return total / steps
 
 
 def decode_figures(efla, dev, stream):

@@ -22,12 +22,13 @@ from typing import Optional, Tuple
 
 import torch
 
-__all__ = ["EflaError", "lib_path", "load", "fwd_chunked", "fwd_recurrent", "decode_step",
-           "device_status", "abi_version", "STATUS"]
+__all__ = ["EflaError", "lib_path", "load", "fwd_chunked", "fwd_recurrent", "decode_step", "prep",
+           "device_status", "abi_version", "STATUS", "UPDATES"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 lib_path = os.path.join(_PKG, "libefla.so")
 
+UPDATES = {"exact": 0, "euler": 1}
 STATUS = {0: "EFLA_OK", 1: "EFLA_ERR_INVALID_ARG", 2: "EFLA_ERR_UNSUPPORTED", 3: "EFLA_ERR_CUDA",
           4: "EFLA_ERR_DEVICE_TIMEOUT"}
 BF16, F32 = 0, 1
@@ -59,6 +60,14 @@ def load():
         L.efla_fwd_recurrent.argtypes = [vp] * 8 + [ip] * 8 + [vp]
         L.efla_decode_step.restype = ip
         L.efla_decode_step.argtypes = [vp] * 6 + [ip] * 6 + [vp]
+        L.efla_fwd_chunked_ex.restype = ip
+        L.efla_fwd_chunked_ex.argtypes = [vp] * 8 + [ip] * 10 + [vp]
+        L.efla_fwd_recurrent_ex.restype = ip
+        L.efla_fwd_recurrent_ex.argtypes = [vp] * 8 + [ip] * 9 + [vp]
+        L.efla_decode_step_ex.restype = ip
+        L.efla_decode_step_ex.argtypes = [vp] * 6 + [ip] * 7 + [vp]
+        L.efla_prep.restype = ip
+        L.efla_prep.argtypes = [vp] * 7 + [ctypes.c_longlong] + [ip] * 4 + [vp]
         L.efla_device_status.restype = ip
         L.efla_device_status.argtypes = [vp]
         L.efla_status_string.restype = ctypes.c_char_p
@@ -107,7 +116,7 @@ def _need(t: Optional[torch.Tensor], name: str):
         raise EflaError(1, f"{name} must be contiguous")
 
 
-def _fwd(entry, q, k, v, beta, S0, cu_seqlens, o, S_T, o_dtype, chunk, stream, return_state):
+def _fwd(entry, q, k, v, beta, S0, cu_seqlens, o, S_T, o_dtype, chunk, stream, return_state, update="exact"):
     L = load()
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (beta, "beta"), (S0, "S0"), (cu_seqlens, "cu_seqlens"),
                  (o, "o"), (S_T if isinstance(S_T, torch.Tensor) else None, "S_T")):
@@ -138,10 +147,12 @@ def _fwd(entry, q, k, v, beta, S0, cu_seqlens, o, S_T, o_dtype, chunk, stream, r
     st = S_T if isinstance(S_T, torch.Tensor) else None
     args = [_p(q), _p(k), _p(v), _p(beta), _p(S0), _p(cu_seqlens), _p(o), _p(st), B, T, H, dk, dv, N,
             _dt(q.dtype), _dt(o.dtype)]
+    if update not in UPDATES:
+        raise EflaError(1, f"unknown update rule {update!r}")
     if entry == "chunked":
-        _check(L.efla_fwd_chunked(*args, int(chunk), _stream(stream)))
+        _check(L.efla_fwd_chunked_ex(*args, int(chunk), UPDATES[update], _stream(stream)))
     else:
-        _check(L.efla_fwd_recurrent(*args, _stream(stream)))
+        _check(L.efla_fwd_recurrent_ex(*args, UPDATES[update], _stream(stream)))
     return o, st
 
 
@@ -149,25 +160,27 @@ def fwd_chunked(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.T
                 S0: Optional[torch.Tensor] = None, cu_seqlens: Optional[torch.Tensor] = None, *,
                 o: Optional[torch.Tensor] = None, S_T: Optional[torch.Tensor] = None,
                 o_dtype: torch.dtype = torch.float32, chunk: int = 64, stream=None,
-                return_state: bool = True) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+                return_state: bool = True, update: str = "exact") -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
     """EFLA forward, chunkwise.  Layouts as in ``efla_fwd_chunked`` (include/efla.h).
 
     q, k [B,T,H,dk], v [B,T,H,dv] (bf16 or fp32); beta [B,T,H] fp32; S0 [N,H,dk,dv] fp32;
     cu_seqlens [N+1] int32 (then B == 1).  Returns (o [B,T,H,dv] in ``o_dtype``,
-    S_T [N,H,dk,dv] fp32 or None when ``return_state`` is False).
+    S_T [N,H,dk,dv] fp32 or None when ``return_state`` is False).  ``update="euler"`` runs
+    the delta-rule (DeltaNet) gate alpha = beta through the same kernels.
     """
-    return _fwd("chunked", q, k, v, beta, S0, cu_seqlens, o, S_T, o_dtype, chunk, stream, return_state)
+    return _fwd("chunked", q, k, v, beta, S0, cu_seqlens, o, S_T, o_dtype, chunk, stream, return_state, update)
 
 
 def fwd_recurrent(q, k, v, beta, S0=None, cu_seqlens=None, *, o=None, S_T=None,
-                  o_dtype: torch.dtype = torch.float32, stream=None, return_state: bool = True):
+                  o_dtype: torch.dtype = torch.float32, stream=None, return_state: bool = True,
+                  update: str = "exact"):
     """Token-by-token fp32 evaluation on CUDA cores (``efla_fwd_recurrent``)."""
-    return _fwd("recurrent", q, k, v, beta, S0, cu_seqlens, o, S_T, o_dtype, 0, stream, return_state)
+    return _fwd("recurrent", q, k, v, beta, S0, cu_seqlens, o, S_T, o_dtype, 0, stream, return_state, update)
 
 
 def decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor, S: torch.Tensor, *,
                 o: Optional[torch.Tensor] = None, o_dtype: torch.dtype = torch.float32,
-                stream=None) -> torch.Tensor:
+                stream=None, update: str = "exact") -> torch.Tensor:
     """One token per sequence; S [B,H,dk,dv] fp32 is updated in place.  Returns o [B,H,dv]."""
     L = load()
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (beta, "beta"), (S, "S"), (o, "o")):
@@ -182,9 +195,47 @@ def decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.T
         raise EflaError(1, "q, k, v must share a dtype and beta must be float32")
     if o is None:
         o = torch.empty((B, H, dv), dtype=o_dtype, device=q.device)
-    _check(L.efla_decode_step(_p(q), _p(k), _p(v), _p(beta), _p(S), _p(o), B, H, dk, dv,
-                              _dt(q.dtype), _dt(o.dtype), _stream(stream)))
+    if update not in UPDATES:
+        raise EflaError(1, f"unknown update rule {update!r}")
+    _check(L.efla_decode_step_ex(_p(q), _p(k), _p(v), _p(beta), _p(S), _p(o), B, H, dk, dv,
+                                 _dt(q.dtype), _dt(o.dtype), UPDATES[update], _stream(stream)))
     return o
+
+
+def prep(k: torch.Tensor, beta: torch.Tensor, v: Optional[torch.Tensor] = None, *, lam: bool = True,
+         alpha: bool = True, ak: bool = False, av: bool = False, update: str = "exact", stream=None) -> dict:
+    """Per-token lambda = ||k||^2, gate alpha, and optionally alpha*k, alpha*v (``efla_prep``).
+
+    k [..., d_k], v [..., d_v] (bf16 or fp32), beta [...] fp32 with matching leading
+    dimensions.  Returns a dict with the requested outputs, shaped like beta
+    (lam, alpha) or like k / v (ak, av).
+    """
+    L = load()
+    for t, n in ((k, "k"), (beta, "beta"), (v, "v")):
+        _need(t, n)
+    if beta.dtype != torch.float32 or tuple(beta.shape) != tuple(k.shape[:-1]):
+        raise EflaError(1, "beta must be float32 with k's leading shape")
+    if av and v is None:
+        raise EflaError(1, "av requested without v")
+    if v is not None and (v.dtype != k.dtype or tuple(v.shape[:-1]) != tuple(k.shape[:-1])):
+        raise EflaError(1, "v must match k's dtype and leading shape")
+    if update not in UPDATES:
+        raise EflaError(1, f"unknown update rule {update!r}")
+    n = beta.numel()
+    dk = k.shape[-1]
+    dv = v.shape[-1] if v is not None else dk
+    out = {}
+    if lam:
+        out["lam"] = torch.empty_like(beta)
+    if alpha:
+        out["alpha"] = torch.empty_like(beta)
+    if ak:
+        out["ak"] = torch.empty_like(k)
+    if av:
+        out["av"] = torch.empty_like(v)
+    _check(L.efla_prep(_p(k), _p(v), _p(beta), _p(out.get("lam")), _p(out.get("alpha")), _p(out.get("ak")),
+                       _p(out.get("av")), n, dk, dv, _dt(k.dtype), UPDATES[update], _stream(stream)))
+    return out
 
 
 def device_status(stream=None) -> int:

@@ -111,6 +111,7 @@ struct TcParams {
     float *S_T;
     int *status;
     int B, T, H, N;
+    int euler;  // 1: delta-rule gate (gamma = beta * lambda)
 };
 
 struct Bars {
@@ -450,7 +451,7 @@ __global__ void __launch_bounds__(320, 1) chunk_tc_kernel(const __grid_constant_
                     for (int s = 0; s < 64; ++s) lam = (s == t) ? g[s] : lam;
                     const bool live = t < valid && lam > 0.f;
                     const float invn = live ? rsqrtf(lam) : 0.f;
-                    const float gam = live ? -expm1f(-row_beta[t] * lam) : 0.f;
+                    const float gam = !live ? 0.f : p.euler ? row_beta[t] * lam : -expm1f(-row_beta[t] * lam);
                     row_invn[buf * 64 + t] = invn;
                     row_gn[buf * 64 + t] = gam * invn;
                     // [gate: terms computed]
@@ -857,6 +858,7 @@ cudaError_t launch_chunk_tc(const FwdArgs &a, const char **why) {
     p.T = a.T;
     p.H = a.H;
     p.N = a.N;
+    p.euler = a.euler;
     *why = "tcgen05 chunk kernel launch";
     const unsigned grid = (unsigned)((long)a.N * a.H);
     return o_bf16 ? launch_typed<true>(p, grid, a.stream) : launch_typed<false>(p, grid, a.stream);

@@ -126,27 +126,48 @@ using namespace efla;
 
 extern "C" {
 
+static bool update_ok(efla_update u) { return u == EFLA_UPDATE_EXACT || u == EFLA_UPDATE_EULER; }
+
+efla_status efla_fwd_chunked_ex(const void *q, const void *k, const void *v, const float *beta, const float *S0,
+                                const int32_t *cu_seqlens, void *o, float *S_T, int B, int T, int H, int d_k,
+                                int d_v, int N, efla_dtype in_dtype, efla_dtype o_dtype, int chunk,
+                                efla_update update, efla_stream_t stream) {
+    if (!update_ok(update)) return fail(EFLA_ERR_INVALID_ARG, "unknown update rule %d", (int)update);
+    FwdArgs a{q, k, v, beta, S0, cu_seqlens, o, S_T, B, T, H, d_k, d_v, N, in_dtype, o_dtype,
+              chunk == 0 ? 64 : chunk, reinterpret_cast<cudaStream_t>(stream), nullptr, (int)update};
+    return run_fwd(a, true);
+}
+
 efla_status efla_fwd_chunked(const void *q, const void *k, const void *v, const float *beta, const float *S0,
                              const int32_t *cu_seqlens, void *o, float *S_T, int B, int T, int H, int d_k,
                              int d_v, int N, efla_dtype in_dtype, efla_dtype o_dtype, int chunk,
                              efla_stream_t stream) {
+    return efla_fwd_chunked_ex(q, k, v, beta, S0, cu_seqlens, o, S_T, B, T, H, d_k, d_v, N, in_dtype, o_dtype,
+                               chunk, EFLA_UPDATE_EXACT, stream);
+}
+
+efla_status efla_fwd_recurrent_ex(const void *q, const void *k, const void *v, const float *beta,
+                                  const float *S0, const int32_t *cu_seqlens, void *o, float *S_T, int B,
+                                  int T, int H, int d_k, int d_v, int N, efla_dtype in_dtype,
+                                  efla_dtype o_dtype, efla_update update, efla_stream_t stream) {
+    if (!update_ok(update)) return fail(EFLA_ERR_INVALID_ARG, "unknown update rule %d", (int)update);
     FwdArgs a{q, k, v, beta, S0, cu_seqlens, o, S_T, B, T, H, d_k, d_v, N, in_dtype, o_dtype,
-              chunk == 0 ? 64 : chunk, reinterpret_cast<cudaStream_t>(stream)};
-    return run_fwd(a, true);
+              0, reinterpret_cast<cudaStream_t>(stream), nullptr, (int)update};
+    return run_fwd(a, false);
 }
 
 efla_status efla_fwd_recurrent(const void *q, const void *k, const void *v, const float *beta,
                                const float *S0, const int32_t *cu_seqlens, void *o, float *S_T, int B,
                                int T, int H, int d_k, int d_v, int N, efla_dtype in_dtype, efla_dtype o_dtype,
                                efla_stream_t stream) {
-    FwdArgs a{q, k, v, beta, S0, cu_seqlens, o, S_T, B, T, H, d_k, d_v, N, in_dtype, o_dtype,
-              0, reinterpret_cast<cudaStream_t>(stream)};
-    return run_fwd(a, false);
+    return efla_fwd_recurrent_ex(q, k, v, beta, S0, cu_seqlens, o, S_T, B, T, H, d_k, d_v, N, in_dtype, o_dtype,
+                                 EFLA_UPDATE_EXACT, stream);
 }
 
-efla_status efla_decode_step(const void *q, const void *k, const void *v, const float *beta, float *S, void *o,
-                             int B, int H, int d_k, int d_v, efla_dtype in_dtype, efla_dtype o_dtype,
-                             efla_stream_t stream) {
+efla_status efla_decode_step_ex(const void *q, const void *k, const void *v, const float *beta, float *S,
+                                void *o, int B, int H, int d_k, int d_v, efla_dtype in_dtype,
+                                efla_dtype o_dtype, efla_update update, efla_stream_t stream) {
+    if (!update_ok(update)) return fail(EFLA_ERR_INVALID_ARG, "unknown update rule %d", (int)update);
     if (B < 0 || H <= 0) return fail(EFLA_ERR_INVALID_ARG, "bad sizes B=%d H=%d", B, H);
     efla_status s = check_dims_common(d_k, d_v, in_dtype, o_dtype);
     if (s != EFLA_OK) return s;
@@ -168,9 +189,53 @@ efla_status efla_decode_step(const void *q, const void *k, const void *v, const 
     for (const Range &r : ins)
         if (overlap(rS, r) || overlap(ro, r)) return fail(EFLA_ERR_INVALID_ARG, "an output overlaps an input");
     if (overlap(rS, ro)) return fail(EFLA_ERR_INVALID_ARG, "o overlaps S");
-    DecodeArgs a{q, k, v, beta, S, o, B, H, d_k, d_v, in_dtype, o_dtype, reinterpret_cast<cudaStream_t>(stream)};
+    DecodeArgs a{q, k, v, beta, S, o, B, H, d_k, d_v, in_dtype, o_dtype, reinterpret_cast<cudaStream_t>(stream),
+                 (int)update};
     cudaError_t e = launch_decode(a);
     if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
+    g_last_error.clear();
+    return EFLA_OK;
+}
+
+efla_status efla_decode_step(const void *q, const void *k, const void *v, const float *beta, float *S, void *o,
+                             int B, int H, int d_k, int d_v, efla_dtype in_dtype, efla_dtype o_dtype,
+                             efla_stream_t stream) {
+    return efla_decode_step_ex(q, k, v, beta, S, o, B, H, d_k, d_v, in_dtype, o_dtype, EFLA_UPDATE_EXACT, stream);
+}
+
+efla_status efla_prep(const void *k, const void *v, const float *beta, float *lam, float *alpha, void *ak, void *av,
+                      long long n, int d_k, int d_v, efla_dtype dtype, efla_update update, efla_stream_t stream) {
+    if (!update_ok(update)) return fail(EFLA_ERR_INVALID_ARG, "unknown update rule %d", (int)update);
+    if (n < 0) return fail(EFLA_ERR_INVALID_ARG, "n=%lld must be >= 0", n);
+    efla_status s = check_dims_common(d_k, d_v, dtype, dtype);
+    if (s != EFLA_OK) return s;
+    if (n > (1LL << 40)) return fail(EFLA_ERR_UNSUPPORTED, "n=%lld too large", n);
+    if (n > 0 && (!k || !beta)) return fail(EFLA_ERR_INVALID_ARG, "k and beta must be non-NULL when n > 0");
+    if (n > 0 && av && !v) return fail(EFLA_ERR_INVALID_ARG, "v must be non-NULL when av is requested");
+    const void *ptrs[] = {k, v, beta, lam, alpha, ak, av};
+    const char *names[] = {"k", "v", "beta", "lam", "alpha", "ak", "av"};
+    for (int i = 0; i < 7; ++i)
+        if (ptrs[i] && !aligned16(ptrs[i]))
+            return fail(EFLA_ERR_INVALID_ARG, "%s=%p is not 16-byte aligned", names[i], ptrs[i]);
+    auto R = [](const char *nm, const void *p, size_t bytes) {
+        uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+        return Range{nm, lo, p ? lo + bytes : lo};
+    };
+    const size_t un = (size_t)n;
+    const Range in[] = {R("k", k, un * d_k * dsize(dtype)), R("v", av ? v : nullptr, un * d_v * dsize(dtype)),
+                        R("beta", beta, un * 4)};
+    const Range out[] = {R("lam", lam, un * 4), R("alpha", alpha, un * 4), R("ak", ak, un * d_k * dsize(dtype)),
+                         R("av", av, un * d_v * dsize(dtype))};
+    for (int i = 0; i < 4; ++i) {
+        for (const Range &r : in)
+            if (overlap(out[i], r)) return fail(EFLA_ERR_INVALID_ARG, "output %s overlaps input %s", out[i].name, r.name);
+        for (int j = i + 1; j < 4; ++j)
+            if (overlap(out[i], out[j])) return fail(EFLA_ERR_INVALID_ARG, "outputs %s and %s overlap", out[i].name, out[j].name);
+    }
+    PrepArgs a{k, av ? v : nullptr, beta, lam, alpha, ak, av, n, d_k, d_v, dtype, (int)update,
+               reinterpret_cast<cudaStream_t>(stream)};
+    cudaError_t e = launch_prep(a);
+    if (e != cudaSuccess) return cuda_fail(e, "prep kernel launch");
     g_last_error.clear();
     return EFLA_OK;
 }

@@ -26,6 +26,7 @@ struct FwdArgs {
     int chunk;
     cudaStream_t stream;
     int *status;  // library device status word
+    int euler;    // 1: delta-rule gate alpha = beta instead of the exact gate
 };
 
 struct DecodeArgs {
@@ -36,11 +37,25 @@ struct DecodeArgs {
     int B, H, dk, dv;
     efla_dtype in_dtype, o_dtype;
     cudaStream_t stream;
+    int euler;
+};
+
+struct PrepArgs {
+    const void *k, *v;
+    const float *beta;
+    float *lam, *alpha;
+    void *ak, *av;
+    long long n;
+    int dk, dv;
+    efla_dtype dtype;
+    int euler;
+    cudaStream_t stream;
 };
 
 // Launchers return a cudaError_t from the launch (cudaSuccess if nothing launched).
 cudaError_t launch_recurrent(const FwdArgs &a);
 cudaError_t launch_decode(const DecodeArgs &a);
+cudaError_t launch_prep(const PrepArgs &a);
 // tcgen05 chunk kernel: bf16 inputs, d_k = d_v = 128, chunk 64.
 cudaError_t launch_chunk_tc(const FwdArgs &a, const char **why);
 
@@ -53,7 +68,9 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
 }
 
 // alpha = (1 - e^{-beta*lam}) / lam, evaluated as -expm1(-beta*lam)/lam; beta at lam == 0.
-__device__ __forceinline__ float efla_alpha(float beta, float lam) {
+// With `euler` the delta-rule gate alpha = beta.
+__device__ __forceinline__ float efla_alpha(float beta, float lam, int euler) {
+    if (euler) return beta;
     return lam > 0.f ? -expm1f(-beta * lam) / lam : beta;
 }
 

@@ -27,7 +27,7 @@ __global__ void __launch_bounds__(256) decode_kernel(const TIn *__restrict__ q,
                                                      const TIn *__restrict__ v,
                                                      const float *__restrict__ beta,
                                                      float *__restrict__ S,
-                                                     TOut *__restrict__ o) {
+                                                     TOut *__restrict__ o, int euler) {
     constexpr int CG = DV / 4;
     constexpr int RG = 256 / CG;
     constexpr int ROWS = DK / RG;
@@ -64,7 +64,7 @@ __global__ void __launch_bounds__(256) decode_kernel(const TIn *__restrict__ q,
             qk += __shfl_xor_sync(0xffffffffu, qk, off);
         }
         if (tid == 0) {
-            scal[0] = efla_alpha(beta[unit], lam);
+            scal[0] = efla_alpha(beta[unit], lam, euler);
             scal[1] = qk;
         }
     }
@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(128) recurrent_kernel(FwdArgs a) {
             qk += __shfl_xor_sync(0xffffffffu, qk, off);
         }
         __syncwarp();
-        const float alpha = efla_alpha(a.beta[row], lam);
+        const float alpha = efla_alpha(a.beta[row], lam, a.euler);
         float x = 0.f, y = 0.f;
 #pragma unroll
         for (int i = 0; i < DK; ++i) {
@@ -195,7 +195,7 @@ template <int DK, int DV, typename TIn, typename TOut>
 cudaError_t decode_launch(const DecodeArgs &a) {
     decode_kernel<DK, DV, TIn, TOut><<<a.B * a.H, 256, 0, a.stream>>>(
         static_cast<const TIn *>(a.q), static_cast<const TIn *>(a.k),
-        static_cast<const TIn *>(a.v), a.beta, a.S, static_cast<TOut *>(a.o));
+        static_cast<const TIn *>(a.v), a.beta, a.S, static_cast<TOut *>(a.o), a.euler);
     return cudaGetLastError();
 }
 

@@ -44,7 +44,7 @@
 extern "C" {
 #endif
 
-#define EFLA_ABI_VERSION 1
+#define EFLA_ABI_VERSION 2
 
 typedef enum {
     EFLA_OK = 0,
@@ -58,6 +58,18 @@ typedef enum {
     EFLA_BF16 = 0,
     EFLA_F32 = 1
 } efla_dtype;
+
+/* The gate of the rank-1 update.
+ *   EFLA_UPDATE_EXACT: alpha = (1 - exp(-beta lambda)) / lambda, the exact solution of
+ *     the zero-order-hold ODE over the token window (the method itself).
+ *   EFLA_UPDATE_EULER: alpha = beta, the explicit-Euler (delta rule, DeltaNet) step
+ *     that the pages compare EFLA against ("Error-Free Linear Attention is a Free
+ *     Lunch" (howistudyai), "Delta Rule (Linear Attention as Online Learning)").
+ *     Same kernels, same layouts; provided for side-by-side measurement. */
+typedef enum {
+    EFLA_UPDATE_EXACT = 0,
+    EFLA_UPDATE_EULER = 1
+} efla_update;
 
 /* Same object as cudaStream_t; kept opaque so that this header needs no CUDA header. */
 typedef struct CUstream_st *efla_stream_t;
@@ -125,6 +137,46 @@ efla_status efla_fwd_recurrent(const void *q, const void *k, const void *v, cons
 efla_status efla_decode_step(const void *q, const void *k, const void *v, const float *beta,
                              float *S, void *o, int B, int H, int d_k, int d_v,
                              efla_dtype in_dtype, efla_dtype o_dtype, efla_stream_t stream);
+
+/*
+ * The three calls above with an explicit update rule (efla_update); the
+ * versions without the suffix use EFLA_UPDATE_EXACT.  An unknown rule returns
+ * EFLA_ERR_INVALID_ARG.
+ */
+efla_status efla_fwd_chunked_ex(const void *q, const void *k, const void *v, const float *beta,
+                                const float *S0, const int32_t *cu_seqlens, void *o, float *S_T,
+                                int B, int T, int H, int d_k, int d_v, int N,
+                                efla_dtype in_dtype, efla_dtype o_dtype, int chunk,
+                                efla_update update, efla_stream_t stream);
+efla_status efla_fwd_recurrent_ex(const void *q, const void *k, const void *v, const float *beta,
+                                  const float *S0, const int32_t *cu_seqlens, void *o, float *S_T,
+                                  int B, int T, int H, int d_k, int d_v, int N,
+                                  efla_dtype in_dtype, efla_dtype o_dtype, efla_update update,
+                                  efla_stream_t stream);
+efla_status efla_decode_step_ex(const void *q, const void *k, const void *v, const float *beta,
+                                float *S, void *o, int B, int H, int d_k, int d_v,
+                                efla_dtype in_dtype, efla_dtype o_dtype, efla_update update,
+                                efla_stream_t stream);
+
+/*
+ * efla_prep -- the per-token quantities of the update, for n token-head rows.
+ *
+ * Defined by: lambda = ||k||^2 ("Exact Flow Linear Attention" (gist.science),
+ * Metodologia 2) and the gate alpha (efla_update; exact: (1 - exp(-beta lambda))
+ * / lambda, beta at lambda = 0; Metodologia 3 and howistudyai Step 1), and the
+ * two gate-scaled factors of the rank-1 write alpha k v^T.
+ *
+ *   k     [n, d_k] dtype; v [n, d_v] dtype (may be NULL unless av is requested)
+ *   beta  [n] fp32
+ *   lam   [n] fp32 out, or NULL      alpha [n] fp32 out, or NULL
+ *   ak    [n, d_k] dtype out = alpha k, or NULL
+ *   av    [n, d_v] dtype out = alpha v, or NULL
+ * A [B, T, H, d] activation tensor is n = B*T*H rows.  Supported d_k, d_v in
+ * {32, 64, 128}; dtype EFLA_BF16 or EFLA_F32 (fp32 arithmetic either way).
+ */
+efla_status efla_prep(const void *k, const void *v, const float *beta, float *lam, float *alpha,
+                      void *ak, void *av, long long n, int d_k, int d_v, efla_dtype dtype,
+                      efla_update update, efla_stream_t stream);
 
 /* Reads the library's device status word on `stream` (synchronising that
  * stream), resets it to EFLA_OK and returns what it held. */

@@ -142,3 +142,37 @@ def test_binding_raises_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(efla, "_lib", None)
     with pytest.raises(RuntimeError, match="not built"):
         efla.load()
+
+
+def test_update_rule_validated(lib):
+    vp, ip = ctypes.c_void_p, ctypes.c_int
+    f = lib.efla_fwd_chunked_ex
+    f.restype = ip
+    f.argtypes = [vp] * 8 + [ip] * 10 + [vp]
+    assert f(Q, K, V, BETA, None, None, O, None, 2, 64, 4, 128, 128, 2, 0, 1, 64, 7, None) == INVALID
+    assert "update" in _last(lib)
+    g = lib.efla_decode_step_ex
+    g.restype = ip
+    g.argtypes = [vp] * 6 + [ip] * 7 + [vp]
+    assert g(Q, K, V, BETA, S0, O, 4, 2, 128, 128, 0, 1, 3, None) == INVALID
+
+
+def _prep(lib, **kw):
+    a = dict(k=K, v=V, beta=BETA, lam=O, alpha=ST, ak=S0, av=CU, n=1000, dk=128, dv=128, dt=0, upd=0)
+    a.update(kw)
+    vp, ip = ctypes.c_void_p, ctypes.c_int
+    f = lib.efla_prep
+    f.restype = ip
+    f.argtypes = [vp] * 7 + [ctypes.c_longlong] + [ip] * 4 + [vp]
+    return f(a["k"], a["v"], a["beta"], a["lam"], a["alpha"], a["ak"], a["av"], a["n"], a["dk"], a["dv"],
+             a["dt"], a["upd"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(n=-1), INVALID), (dict(dk=100), UNSUPPORTED), (dict(k=None), INVALID), (dict(v=None), INVALID),
+    (dict(beta=BETA + 8), INVALID), (dict(lam=K + 64), INVALID), (dict(alpha=O + 16), INVALID),
+    (dict(upd=9), INVALID), (dict(dt=4), INVALID),
+])
+def test_prep_rejects(lib, kw, code):
+    assert _prep(lib, **kw) == code
+    assert _last(lib)
