@@ -41,12 +41,13 @@
 //   S^T         += u^T K             (M = 128, N = d_k = 128, K = C; K as MN-major operand)
 // and G = [K ; Q] K^T (M = 2C = 128, N = C, K = d_k) gives the chunk's Gram terms.
 //
-// One CTA of two warpgroups per (sequence, head):
+// One CTA of 448 threads per (sequence, head):
 //   state warpgroup (threads 0-127): thread j owns TMEM lane j (column j of S);
 //     runs the per-chunk dependency chain above and writes o with TMA stores.
-//   prep warpgroup (threads 128-255): loads K, Q, V by TMA (two stages), forms
-//     the Gram products, the gate terms, T' and P for the NEXT chunk while the
-//     state warpgroup works on the current one.
+//   MMA thread (warp 8): issues the state chain's tensor-core products.
+//   TMA producer (warp 9): loads K, Q, V into two stages.
+//   prep warpgroups (warps 4-7 and 10-13): form the Gram products, the gate terms,
+//     T'' and P for the NEXT chunk while the state warpgroup works on the current one.
 // Every wait is bounded; on expiry the CTA records EFLA_ERR_DEVICE_TIMEOUT and
 // leaves.
 #include <cudaTypedefs.h>
@@ -70,14 +71,14 @@ constexpr uint32_t OFF_V = 32768;          // within a stage
 constexpr uint32_t OFF_TP = 98304;         // 2 buffers x {hi 8 KB, lo 8 KB}: T' [64 t][64 s]
 constexpr uint32_t OFF_P = 131072;         // 2 buffers x {hi, lo}: P [64 t][64 s]
 constexpr uint32_t OFF_OST = 163840;       // o staging for the TMA stores: 4 warps x [64 t][32], 32 KB
-constexpr uint32_t OFF_AT = 196608;        // fp32 [64][65]: A~, then T~ in place
-constexpr uint32_t AT_LD = 65;
+constexpr uint32_t OFF_AT = 196608;        // fp32 [64][68]: A~, then T~ in place (rows 16-byte aligned)
+constexpr uint32_t AT_LD = 68;
 constexpr uint32_t OFF_ROW = OFF_AT + 64 * AT_LD * 4;  // fp32: invn[2][64], gn[2][64], beta[64]
 constexpr uint32_t ROW_BYTES = 6 * 64 * 4;
 constexpr uint32_t OFF_BAR = OFF_ROW + ROW_BYTES;       // mbarriers (struct Bars)
 constexpr uint32_t OFF_MISC = OFF_BAR + 224;            // tmem base (u32), abort flag (i32)
 constexpr uint32_t OFF_SCR = OFF_MISC + 16;             // fp32 scratch of the triangular inverse
-constexpr uint32_t SCR_FLOATS = 32 * 33;
+constexpr uint32_t SCR_FLOATS = 32 * 36;
 constexpr uint32_t OFF_NEGI = (OFF_SCR + SCR_FLOATS * 4 + 1023) & ~1023u;  // -I, 64x64 bf16 (K-major, swizzled)
 constexpr uint32_t SMEM_USED = OFF_NEGI + 8192;
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;       // + alignment slack for the 1024-byte base
@@ -97,7 +98,7 @@ constexpr uint32_t TM_COLS = 512;
 
 constexpr uint64_t WAIT_NS = 2000000000ull;  // 2 s bound on any wait
 
-constexpr int BAR_PREP = 2;  // named barrier of the prep warpgroup (128 threads)
+constexpr int BAR_PREP = 2;  // named barrier of the two prep warpgroups (256 threads)
 
 struct TcParams {
     CUtensorMap map_q;
@@ -132,9 +133,10 @@ struct Bars {
 };
 static_assert(sizeof(Bars) <= 224, "mbarrier block exceeds its slot");
 
-// Bounded wait that also gives up when the other warpgroup has aborted.
-__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
-    if (mbar_try_wait(bar, parity)) return true;
+// Bounded wait that also gives up when another role has aborted.  The slow
+// path is out of line: it is reached rarely and the kernel's code must stay
+// small enough for the instruction cache.
+__device__ __noinline__ bool wait_bar_slow(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
     const uint64_t t0 = globaltimer_ns();
     while (true) {
         if (mbar_try_wait_sleep(bar, parity, 20000)) return true;  // sleeps instead of spinning
@@ -144,6 +146,10 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatil
             return false;
         }
     }
+}
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait_bar_slow(bar, parity, abort_flag);
 }
 
 // Splits pairs x[2c], x[2c+1] into packed bf16 hi and lo words with
@@ -159,18 +165,6 @@ __device__ __forceinline__ void split_pack(const float *x, uint32_t *hi, uint32_
         const float r0 = x[2 * c] - __uint_as_float(b0 & 0xffff0000u);
         const float r1 = x[2 * c + 1] - __uint_as_float(b1 & 0xffff0000u);
         lo[c] = __byte_perm(__float_as_uint(r0), __float_as_uint(r1), 0x7632);
-    }
-}
-
-// Writes 64 fp32 values of one row as bf16 hi/lo into two 128B-swizzled tiles.
-__device__ __forceinline__ void store_row_split(uint8_t *hi_tile, uint8_t *lo_tile, int row, const float *x) {
-#pragma unroll
-    for (int c = 0; c < 64; c += 8) {
-        uint32_t h[4], l[4];
-        split_pack<4>(x + c, h, l);
-        const uint32_t off = swz_offset(row, c, 8192);
-        *reinterpret_cast<uint4 *>(hi_tile + off) = make_uint4(h[0], h[1], h[2], h[3]);
-        *reinterpret_cast<uint4 *>(lo_tile + off) = make_uint4(l[0], l[1], l[2], l[3]);
     }
 }
 
@@ -190,110 +184,122 @@ __device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t (&u)[3
     tmem_st32(taddr, reinterpret_cast<const float(&)[32]>(u));
 }
 
-// T~ = (I + A~)^{-1} in place in At (fp32, row stride AT_LD), by the 128
-// threads of the prep warpgroup, with a scratch Y of SCR_FLOATS floats.  Each
-// step applies [[L1, 0], [B, L2]]^{-1} = [[L1^{-1}, 0], [-L2^{-1} B L1^{-1}, L2^{-1}]]
+// T~ = (I + A~)^{-1} in place in At (fp32, row stride AT_LD), by the 256
+// threads of the two prep warpgroups (index pi), with a scratch Y of SCR_FLOATS
+// floats.  Each step applies
+//   [[L1, 0], [B, L2]]^{-1} = [[L1^{-1}, 0], [-L2^{-1} B L1^{-1}, L2^{-1}]]
 // for unit lower-triangular L1, L2:
-//   1. the four diagonal 16x16 blocks by column substitution (warp w: block w;
-//      the two half-warps split each column's rows by parity);
+//   1. the four diagonal 16x16 blocks by column substitution (two warps per
+//      block, eight columns per warp, four lanes per column splitting its rows by
+//      residue mod 4);
 //   2. blocks (1,0) and (3,2) of 16:  T~_IJ = -T~_II (A~_IJ T~_JJ);
 //   3. the lower-left 32x32 block:    T~_21 = -T~_22 (A~_21 T~_11)  (32x32 blocks).
 // Steps 2 and 3 are register-tiled fp32 products.
-__device__ __forceinline__ void invert_unit_lower(float *At, float *Y, int pt) {
-    const int lane = pt & 31, pw = pt >> 5;
+__device__ __forceinline__ void invert_unit_lower(float *At, float *Y, int pi) {
+    const int lane = pi & 31, pw = pi >> 5;
     {
-        const int B0 = pw * 16, c = lane & 15, par = lane >> 4;
-        float col[8];  // col[m] = T~[B0 + 2m + par][B0 + c]
+        const int B0 = (pw >> 1) * 16, c = (lane & 7) + 8 * (pw & 1), r4 = lane >> 3;
+        float col[4];  // col[m] = T~[B0 + 4m + r4][B0 + c]
 #pragma unroll
-        for (int m = 0; m < 8; ++m) col[m] = (2 * m + par == c) ? 1.f : 0.f;
+        for (int m = 0; m < 4; ++m) col[m] = (4 * m + r4 == c) ? 1.f : 0.f;
 #pragma unroll
         for (int t = 1; t < 16; ++t) {
-            const float *row = At + (B0 + t) * AT_LD + B0 + par;
+            const float *row = At + (B0 + t) * AT_LD + B0 + r4;
             float acc = 0.f;
 #pragma unroll
-            for (int m = 0; m < (t + 1) / 2; ++m) acc = fmaf(row[2 * m], col[m], acc);  // A~[t][t] = 0
-            const float tot = acc + __shfl_xor_sync(0xffffffffu, acc, 16);
-            if ((t & 1) == par && t > c) col[t >> 1] = -tot;
+            for (int m = 0; m < (t + 3) / 4; ++m) acc = fmaf(row[4 * m], col[m], acc);  // A~[t][s >= t] = 0
+            float tot = acc + __shfl_xor_sync(0xffffffffu, acc, 8);
+            tot += __shfl_xor_sync(0xffffffffu, tot, 16);
+            if ((t & 3) == r4 && t > c) col[t >> 2] = -tot;
         }
-        __syncwarp();
+        named_bar(BAR_PREP, 256);  // both warps of the block have read A~_BB
 #pragma unroll
-        for (int m = 0; m < 8; ++m) At[(B0 + 2 * m + par) * AT_LD + B0 + c] = col[m];
+        for (int m = 0; m < 4; ++m) At[(B0 + 4 * m + r4) * AT_LD + B0 + c] = col[m];
     }
-    named_bar(BAR_PREP, 128);
+    named_bar(BAR_PREP, 256);
     {
-        const int q = pt >> 6, tt = pt & 63;
+        const int q = pi >> 7, tt = pi & 127;
         const int I = 2 * q + 1, J = 2 * q;
-        const int r = tt >> 2, c0 = (tt & 3) * 4;
-        float *yq = Y + q * (16 * 17);
-        float y[4] = {0.f, 0.f, 0.f, 0.f};
+        const int r = tt >> 3, c0 = (tt & 7) * 2;
+        float *yq = Y + q * (16 * 20);  // [16][20]
+        float y0 = 0.f, y1 = 0.f;
         const float *arow = At + (16 * I + r) * AT_LD + 16 * J;
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            const float a = arow[k];
-            const float *brow = At + (16 * J + k) * AT_LD + 16 * J + c0;
+        for (int k4 = 0; k4 < 16; k4 += 4) {
+            const float4 a = *reinterpret_cast<const float4 *>(arow + k4);
+            const float av[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
-            for (int i = 0; i < 4; ++i) y[i] = fmaf(a, brow[i], y[i]);
+            for (int e = 0; e < 4; ++e) {
+                const float2 bv = *reinterpret_cast<const float2 *>(At + (16 * J + k4 + e) * AT_LD + 16 * J + c0);
+                y0 = fmaf(av[e], bv.x, y0);
+                y1 = fmaf(av[e], bv.y, y1);
+            }
         }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) yq[r * 17 + c0 + i] = y[i];
-        named_bar(BAR_PREP, 128);
-        float z[4] = {0.f, 0.f, 0.f, 0.f};
+        *reinterpret_cast<float2 *>(yq + r * 20 + c0) = make_float2(y0, y1);
+        named_bar(BAR_PREP, 256);
+        float z0 = 0.f, z1 = 0.f;
         const float *trow = At + (16 * I + r) * AT_LD + 16 * I;  // T~_II row r (zeros above the diagonal)
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            const float tv = trow[k];
+        for (int k4 = 0; k4 < 16; k4 += 4) {
+            const float4 tq = *reinterpret_cast<const float4 *>(trow + k4);
+            const float tv[4] = {tq.x, tq.y, tq.z, tq.w};
 #pragma unroll
-            for (int i = 0; i < 4; ++i) z[i] = fmaf(tv, yq[k * 17 + c0 + i], z[i]);
+            for (int e = 0; e < 4; ++e) {
+                const float2 yv = *reinterpret_cast<const float2 *>(yq + (k4 + e) * 20 + c0);
+                z0 = fmaf(tv[e], yv.x, z0);
+                z1 = fmaf(tv[e], yv.y, z1);
+            }
         }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) At[(16 * I + r) * AT_LD + 16 * J + c0 + i] = -z[i];
-        named_bar(BAR_PREP, 128);
+        // nobody reads block (I, J) in this phase: write it at once
+        *reinterpret_cast<float2 *>(At + (16 * I + r) * AT_LD + 16 * J + c0) = make_float2(-z0, -z1);
+        named_bar(BAR_PREP, 256);
     }
     {
-        const int r0 = 2 * (pt >> 3), c0 = 4 * (pt & 7);
-        float x0[4] = {0.f, 0.f, 0.f, 0.f}, x1[4] = {0.f, 0.f, 0.f, 0.f};
+        const int r0 = 2 * (pi >> 4), c0 = 2 * (pi & 15);
+        float x00 = 0.f, x01 = 0.f, x10 = 0.f, x11 = 0.f;
         const float *a0 = At + (32 + r0) * AT_LD, *a1 = a0 + AT_LD;
-#pragma unroll 8
-        for (int k = 0; k < 32; ++k) {
-            const float va0 = a0[k], va1 = a1[k];
-            const float *brow = At + k * AT_LD + c0;  // T~_11 (rows/cols 0..31)
+#pragma unroll 2
+        for (int k4 = 0; k4 < 32; k4 += 4) {
+            const float4 p0 = *reinterpret_cast<const float4 *>(a0 + k4);
+            const float4 p1 = *reinterpret_cast<const float4 *>(a1 + k4);
+            const float va0[4] = {p0.x, p0.y, p0.z, p0.w}, va1[4] = {p1.x, p1.y, p1.z, p1.w};
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float bv = brow[i];
-                x0[i] = fmaf(va0, bv, x0[i]);
-                x1[i] = fmaf(va1, bv, x1[i]);
+            for (int e = 0; e < 4; ++e) {
+                const float2 bv = *reinterpret_cast<const float2 *>(At + (k4 + e) * AT_LD + c0);  // T~_11
+                x00 = fmaf(va0[e], bv.x, x00);
+                x01 = fmaf(va0[e], bv.y, x01);
+                x10 = fmaf(va1[e], bv.x, x10);
+                x11 = fmaf(va1[e], bv.y, x11);
             }
         }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            Y[r0 * 33 + c0 + i] = x0[i];
-            Y[(r0 + 1) * 33 + c0 + i] = x1[i];
-        }
-        named_bar(BAR_PREP, 128);
-        float z0[4] = {0.f, 0.f, 0.f, 0.f}, z1[4] = {0.f, 0.f, 0.f, 0.f};
+        *reinterpret_cast<float2 *>(Y + r0 * 36 + c0) = make_float2(x00, x01);
+        *reinterpret_cast<float2 *>(Y + (r0 + 1) * 36 + c0) = make_float2(x10, x11);
+        named_bar(BAR_PREP, 256);
+        float z00 = 0.f, z01 = 0.f, z10 = 0.f, z11 = 0.f;
         const float *t0 = At + (32 + r0) * AT_LD + 32, *t1 = t0 + AT_LD;  // T~_22 rows
-#pragma unroll 8
-        for (int k = 0; k < 32; ++k) {
-            const float tv0 = t0[k], tv1 = t1[k];
-            const float *xrow = Y + k * 33 + c0;
+#pragma unroll 2
+        for (int k4 = 0; k4 < 32; k4 += 4) {
+            const float4 p0 = *reinterpret_cast<const float4 *>(t0 + k4);
+            const float4 p1 = *reinterpret_cast<const float4 *>(t1 + k4);
+            const float tv0[4] = {p0.x, p0.y, p0.z, p0.w}, tv1[4] = {p1.x, p1.y, p1.z, p1.w};
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float xv = xrow[i];
-                z0[i] = fmaf(tv0, xv, z0[i]);
-                z1[i] = fmaf(tv1, xv, z1[i]);
+            for (int e = 0; e < 4; ++e) {
+                const float2 xv = *reinterpret_cast<const float2 *>(Y + (k4 + e) * 36 + c0);
+                z00 = fmaf(tv0[e], xv.x, z00);
+                z01 = fmaf(tv0[e], xv.y, z01);
+                z10 = fmaf(tv1[e], xv.x, z10);
+                z11 = fmaf(tv1[e], xv.y, z11);
             }
         }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            At[(32 + r0) * AT_LD + c0 + i] = -z0[i];
-            At[(33 + r0) * AT_LD + c0 + i] = -z1[i];
-        }
-        named_bar(BAR_PREP, 128);
+        // nobody reads the lower-left block in this phase: write it at once
+        *reinterpret_cast<float2 *>(At + (32 + r0) * AT_LD + c0) = make_float2(-z00, -z01);
+        *reinterpret_cast<float2 *>(At + (33 + r0) * AT_LD + c0) = make_float2(-z10, -z11);
+        named_bar(BAR_PREP, 256);
     }
 }
 
 template <bool OUT_BF16>
-__global__ void __launch_bounds__(320, 1) chunk_tc_kernel(const __grid_constant__ TcParams p) {
+__global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant__ TcParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float *row_invn = reinterpret_cast<float *>(sm + OFF_ROW);  // [2][64]
@@ -382,15 +388,23 @@ __global__ void __launch_bounds__(320, 1) chunk_tc_kernel(const __grid_constant_
     const uint32_t tmem = *tmem_slot;
     const uint32_t s_sm = smem_u32(sm);
 
-    if (tid >= 128 && tid < 256) {
-        // =============================== prep warpgroup ===============================
-        const int pt = tid - 128;
-        const uint32_t lane_base = tmem + ((uint32_t)((warp - 4) * 32) << 16);
-        int g_issued = 0;  // chunks whose Gram MMA was issued (thread pt == 0)
+    if ((tid >= 128 && tid < 256) || tid >= 320) {
+        // ============================== prep warpgroups ==============================
+        // Warps 4-7 and 10-13 share each chunk's CUDA-core work (256 threads, index pi).
+        // Gram row r (TMEM lane r) is read by one thread of each warpgroup: columns
+        // 0-31 by warps 4-7, columns 32-63 by warps 10-13.
+        const int half = tid >= 320 ? 1 : 0;
+        const int pi = half ? tid - 320 + 128 : tid - 128;
+        const int quarter = warp & 3;  // TMEM lanes this warp may access
+        const int row = quarter * 32 + (tid & 31);
+        const int col0 = half * 32;
+        const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+        const bool leader = pi == 0;  // issues the Gram MMAs
+        int g_issued = 0;             // chunks whose Gram MMA was issued (leader)
         auto issue_gram = [&](int c) {
             const uint32_t kq = s_sm + OFF_STAGE + (c & 1) * STAGE_BYTES;
             const uint32_t idesc = idesc_bf16_f32(128, 64, 0, 0);
-#pragma unroll
+#pragma unroll 1
             for (int ks = 0; ks < 8; ++ks) {
                 const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
                 mma_bf16(tmem + TM_G, smem_desc(kq + off, 16, 1024), smem_desc(kq + off, 16, 1024), idesc, ks > 0);
@@ -398,8 +412,8 @@ __global__ void __launch_bounds__(320, 1) chunk_tc_kernel(const __grid_constant_
             mma_commit(&bars->g_done);
             g_issued = c + 1;
         };
-        // Thread pt == 0, during chunk c: start the Gram MMA of chunk c+1 as soon as its tile
-        // has landed (full chunks only: a partial chunk's tail is zeroed first).  Non-blocking.
+        // Leader, during chunk c: start the Gram MMA of chunk c+1 as soon as its tile has
+        // landed (full chunks only: a partial chunk's tail is zeroed first).  Non-blocking.
         auto prefetch_gram = [&](int c) {
             if (c + 1 >= nchunks || g_issued != c + 1 || eos - (bos + (long)(c + 1) * C) < C) return;
             if (mbar_try_wait(&bars->tma_full[(c + 1) & 1], ((c + 1) >> 1) & 1)) {
@@ -413,11 +427,11 @@ __global__ void __launch_bounds__(320, 1) chunk_tc_kernel(const __grid_constant_
             const int valid = (int)min((long)C, eos - tok0);
             uint8_t *KQ = sm + OFF_STAGE + st * STAGE_BYTES;
 
-            if (pt < C) row_beta[pt] = pt < valid ? p.beta[((size_t)b * p.T + (size_t)(tok0 + pt)) * p.H + h] : 0.f;
+            if (pi < C) row_beta[pi] = pi < valid ? p.beta[((size_t)b * p.T + (size_t)(tok0 + pi)) * p.H + h] : 0.f;
             bool ok = wait_bar(&bars->tma_full[st], (c >> 1) & 1, abort_flag);
             if (ok && valid < C) {  // rows past the end of the sequence are zeroed (they may hold the next one)
                 const int rows = C - valid;
-                for (int e = pt; e < 4 * rows * 8; e += 128) {
+                for (int e = pi; e < 4 * rows * 8; e += 256) {
                     const int ch = e & 7, r = (e >> 3) % rows, part = (e >> 3) / rows;
                     const int R = valid + r + ((part >> 1) ? 64 : 0), cb = part & 1;
                     *reinterpret_cast<uint4 *>(KQ + cb * 16384 + (R >> 3) * 1024 + (R & 7) * 128 + ch * 16) =
@@ -425,13 +439,13 @@ __global__ void __launch_bounds__(320, 1) chunk_tc_kernel(const __grid_constant_
                 }
                 fence_proxy_async_smem();
             }
-            if (named_bar_any(BAR_PREP, 128, !ok || *abort_flag)) {
+            if (named_bar_any(BAR_PREP, 256, !ok || *abort_flag)) {
                 *abort_flag = 1;
                 break;
             }
 
             // Gram products G = [K;Q] K^T (unless already started during the previous chunk)
-            if (pt == 0 && g_issued == c) {
+            if (leader && g_issued == c) {
                 tc_fence_after();
                 issue_gram(c);
             }
@@ -440,58 +454,81 @@ __global__ void __launch_bounds__(320, 1) chunk_tc_kernel(const __grid_constant_
             if (c >= 2) ok = wait_bar(&bars->chunk_done[c & 1], ((c - 2) >> 1) & 1, abort_flag) && ok;
             tc_fence_after();
             {
-                float g[64];
-                tmem_ld64(lane_base + TM_G, g);
+                float g[32];
+                tmem_ld32(lane_base + TM_G + col0, g);
+                tmem_ld_wait();
                 tc_fence_before();  // the next Gram MMA may overwrite TM_G once every row is read
                 // [gate: G row loaded]
-                if (pt < C) {  // K K^T row t -> gate terms, then A~ row t
-                    const int t = pt;
+                if (row < C && (row >> 5) == half) {  // this thread holds K K^T[t][t]: gate terms of row t
+                    const int t = row;
                     float lam = 0.f;
 #pragma unroll
-                    for (int s = 0; s < 64; ++s) lam = (s == t) ? g[s] : lam;
+                    for (int s = 0; s < 32; ++s) lam = (s == (t & 31)) ? g[s] : lam;
                     const bool live = t < valid && lam > 0.f;
                     const float invn = live ? rsqrtf(lam) : 0.f;
                     const float gam = !live ? 0.f : p.euler ? row_beta[t] * lam : -expm1f(-row_beta[t] * lam);
                     row_invn[buf * 64 + t] = invn;
                     row_gn[buf * 64 + t] = gam * invn;
-                    // [gate: terms computed]
-                    named_bar(BAR_PREP, 128);
-                    // [gate: barrier passed]
-                    const float rs = gam * invn;
-                    float iv[64];  // all scales first: the stores below may alias them for the compiler
+                }
+                // [gate: terms computed]
+                named_bar(BAR_PREP, 256);
+                // [gate: barrier passed]
+                if (row < C) {  // A~[t][col0 .. col0+31]
+                    const int t = row;
+                    const float rs = row_gn[buf * 64 + t];  // gamma_t / n_t
+                    float iv[32];  // all scales first: the stores below may alias them for the compiler
 #pragma unroll
-                    for (int s4 = 0; s4 < 16; ++s4) {
-                        const float4 f = reinterpret_cast<const float4 *>(row_invn + buf * 64)[s4];
+                    for (int s4 = 0; s4 < 8; ++s4) {
+                        const float4 f = reinterpret_cast<const float4 *>(row_invn + buf * 64 + col0)[s4];
                         iv[4 * s4] = f.x;
                         iv[4 * s4 + 1] = f.y;
                         iv[4 * s4 + 2] = f.z;
                         iv[4 * s4 + 3] = f.w;
                     }
 #pragma unroll
-                    for (int s = 0; s < 64; ++s) At[t * AT_LD + s] = s < t ? rs * iv[s] * g[s] : 0.f;
-                } else {  // P = Q K^T with the inclusive causal mask
-                    const int t = pt - C;
+                    for (int s4 = 0; s4 < 32; s4 += 4) {
+                        float4 w;
+                        w.x = col0 + s4 + 0 < t ? rs * iv[s4 + 0] * g[s4 + 0] : 0.f;
+                        w.y = col0 + s4 + 1 < t ? rs * iv[s4 + 1] * g[s4 + 1] : 0.f;
+                        w.z = col0 + s4 + 2 < t ? rs * iv[s4 + 2] * g[s4 + 2] : 0.f;
+                        w.w = col0 + s4 + 3 < t ? rs * iv[s4 + 3] * g[s4 + 3] : 0.f;
+                        *reinterpret_cast<float4 *>(At + t * AT_LD + col0 + s4) = w;
+                    }
+                } else {  // P[t][col0 .. col0+31] = Q K^T with the inclusive causal mask
+                    const int t = row - C;
 #pragma unroll
-                    for (int s = 0; s < 64; ++s) g[s] = s <= t ? g[s] : 0.f;
-                    store_row_split(sm + OFF_P + buf * 16384, sm + OFF_P + buf * 16384 + 8192, t, g);
-                    named_bar(BAR_PREP, 128);
+                    for (int s = 0; s < 32; ++s) g[s] = col0 + s <= t ? g[s] : 0.f;
+                    uint8_t *phi = sm + OFF_P + buf * 16384, *plo = phi + 8192;
+#pragma unroll
+                    for (int c8 = 0; c8 < 32; c8 += 8) {
+                        uint32_t hh[4], ll[4];
+                        split_pack<4>(g + c8, hh, ll);
+                        const uint32_t off = swz_offset(t, col0 + c8, 8192);
+                        *reinterpret_cast<uint4 *>(phi + off) = make_uint4(hh[0], hh[1], hh[2], hh[3]);
+                        *reinterpret_cast<uint4 *>(plo + off) = make_uint4(ll[0], ll[1], ll[2], ll[3]);
+                    }
                 }
             }
-            named_bar(BAR_PREP, 128);
-            if (pt == 0) prefetch_gram(c);
-            invert_unit_lower(At, scr, pt);
-            if (pt == 0) prefetch_gram(c);
+            named_bar(BAR_PREP, 256);
+            if (leader) prefetch_gram(c);
+            invert_unit_lower(At, scr, pi);
+            if (leader) prefetch_gram(c);
             {  // T'' = -diag(1/n) T~ diag(gamma/n), lower triangle, as bf16 hi/lo [t][s]
-                const int t = pt >> 1, s0 = (pt & 1) * 32;
+                const int t = pi >> 2, s0 = (pi & 3) * 16;
                 uint8_t *hi = sm + OFF_TP + buf * 16384, *lo = hi + 8192;
                 const float rsc = -row_invn[buf * 64 + t];
 #pragma unroll
-                for (int c8 = 0; c8 < 32; c8 += 8) {
+                for (int c8 = 0; c8 < 16; c8 += 8) {
+                    float tt8[8], gn8[8];
+                    *reinterpret_cast<float4 *>(tt8) = *reinterpret_cast<const float4 *>(At + t * AT_LD + s0 + c8);
+                    *reinterpret_cast<float4 *>(tt8 + 4) = *reinterpret_cast<const float4 *>(At + t * AT_LD + s0 + c8 + 4);
+                    *reinterpret_cast<float4 *>(gn8) = *reinterpret_cast<const float4 *>(row_gn + buf * 64 + s0 + c8);
+                    *reinterpret_cast<float4 *>(gn8 + 4) = *reinterpret_cast<const float4 *>(row_gn + buf * 64 + s0 + c8 + 4);
                     float x[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
                         const int s = s0 + c8 + e;
-                        x[e] = s <= t ? rsc * At[t * AT_LD + s] * row_gn[buf * 64 + s] : 0.f;
+                        x[e] = s <= t ? rsc * tt8[e] * gn8[e] : 0.f;
                     }
                     uint32_t hh[4], ll[4];
                     split_pack<4>(x, hh, ll);
@@ -501,15 +538,15 @@ __global__ void __launch_bounds__(320, 1) chunk_tc_kernel(const __grid_constant_
                 }
             }
             fence_proxy_async_smem();
-            named_bar(BAR_PREP, 128);
-            if (pt == 0) mbar_arrive(&bars->prep_ready[buf]);
-            if (pt == 0) prefetch_gram(c);
-            if (named_bar_any(BAR_PREP, 128, !ok || *abort_flag)) {
+            named_bar(BAR_PREP, 256);
+            if (leader) mbar_arrive(&bars->prep_ready[buf]);
+            if (leader) prefetch_gram(c);
+            if (named_bar_any(BAR_PREP, 256, !ok || *abort_flag)) {
                 *abort_flag = 1;
                 break;
             }
         }
-        if (pt == 0) {  // every Gram MMA has completed before TMEM is released (bounded)
+        if (leader) {  // every Gram MMA has completed before TMEM is released (bounded)
             mma_commit(&bars->drain[1]);
             const uint64_t t0 = globaltimer_ns();
             while (!mbar_try_wait_sleep(&bars->drain[1], 0, 20000) && globaltimer_ns() - t0 < WAIT_NS) {
@@ -526,7 +563,7 @@ __global__ void __launch_bounds__(320, 1) chunk_tc_kernel(const __grid_constant_
         const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
         {  // initial state -> TMEM (S^T: lane j holds column j of S)
             float r[32];
-#pragma unroll
+#pragma unroll 1
             for (int g = 0; g < 4; ++g) {
 #pragma unroll
                 for (int i = 0; i < 32; ++i) r[i] = p.S0 ? p.S0[sbase + (size_t)(g * 32 + i) * D + j] : 0.f;
@@ -542,39 +579,47 @@ __global__ void __launch_bounds__(320, 1) chunk_tc_kernel(const __grid_constant_
         auto epilogue = [&](int cc) {
             const long t0c = bos + (long)cc * C;
             const int vc = (int)min((long)C, eos - t0c);
-            float ov[64];
-            tmem_ld64(lane_base + TM_O, ov);
+            float ov[32], ow[32];
+            tmem_ld32(lane_base + TM_O, ov);
+            tmem_ld32(lane_base + TM_O + 32, ow);
+            tmem_ld_wait();
             tc_fence_before();
             mbar_arrive(&bars->o_free);
-            if (p.cu_seqlens == nullptr || vc == C) {
-                uint8_t *slice = sm + OFF_OST + warp * 8192;
-                if (lane == 0) bulk_wait_read0();  // this warp's previous store has read its slice
-                __syncwarp();
-                if (OUT_BF16) {
-                    __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(slice) + lane;
+            uint8_t *slice = sm + OFF_OST + warp * 8192;
+            if (lane == 0) bulk_wait_read0();  // this warp's previous store has read its slice
+            __syncwarp();
+            if (OUT_BF16) {
+                __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(slice) + lane;
 #pragma unroll
-                    for (int t = 0; t < C; ++t) stg[t * 32] = __float2bfloat16_rn(ov[t]);
-                } else {
-                    float *stg = reinterpret_cast<float *>(slice) + lane;
-#pragma unroll
-                    for (int t = 0; t < C; ++t) stg[t * 32] = ov[t];
+                for (int t = 0; t < 32; ++t) {
+                    stg[t * 32] = __float2bfloat16_rn(ov[t]);
+                    stg[(t + 32) * 32] = __float2bfloat16_rn(ow[t]);
                 }
+            } else {
+                float *stg = reinterpret_cast<float *>(slice) + lane;
+#pragma unroll
+                for (int t = 0; t < 32; ++t) {
+                    stg[t * 32] = ov[t];
+                    stg[(t + 32) * 32] = ow[t];
+                }
+            }
+            if (p.cu_seqlens == nullptr || vc == C) {
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
                     tma_store_4d(&p.map_o, slice, warp * 32, h, (int)t0c, (int)b);
                     bulk_commit();
                 }
-            } else {
-#pragma unroll
-                for (int t = 0; t < C; ++t) {
-                    if (t < vc) {
-                        const size_t row = ((size_t)b * p.T + (size_t)(t0c + t)) * p.H + h;
-                        if (OUT_BF16)
-                            static_cast<__nv_bfloat16 *>(p.o)[row * D + j] = __float2bfloat16_rn(ov[t]);
-                        else
-                            static_cast<float *>(p.o)[row * D + j] = ov[t];
-                    }
+            } else {  // partial chunk of a packed batch: rows past vc belong to the next sequence
+                __syncwarp();
+#pragma unroll 1
+                for (int t = 0; t < vc; ++t) {
+                    const size_t rw = ((size_t)b * p.T + (size_t)(t0c + t)) * p.H + h;
+                    if (OUT_BF16)
+                        static_cast<__nv_bfloat16 *>(p.o)[rw * D + j] =
+                            reinterpret_cast<const __nv_bfloat16 *>(slice)[t * 32 + lane];
+                    else
+                        static_cast<float *>(p.o)[rw * D + j] = reinterpret_cast<const float *>(slice)[t * 32 + lane];
                 }
             }
         };
@@ -590,7 +635,7 @@ __global__ void __launch_bounds__(320, 1) chunk_tc_kernel(const __grid_constant_
             {
                 float s[32];
                 uint32_t hi[32], lo[32];
-#pragma unroll
+#pragma unroll 1
                 for (int g = 0; g < 4; g += 2) {
                     tmem_ld32(lane_base + TM_S + g * 32, s);
                     tmem_ld_wait();
@@ -615,12 +660,16 @@ __global__ void __launch_bounds__(320, 1) chunk_tc_kernel(const __grid_constant_
             tc_fence_after();
             // D^T = (K S - V)^T -> bf16 hi/lo operand in TMEM (rows past the sequence end are zero)
             {
-                float x[64];
-                tmem_ld64(lane_base + TM_X, x);
-#pragma unroll
-                for (int t = 0; t < C; ++t) x[t] = t < valid ? x[t] : 0.f;
                 uint32_t hi[32], lo[32];
-                split_pack<32>(x, hi, lo);
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    float x[32];
+                    tmem_ld32(lane_base + TM_X + hf * 32, x);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) x[t] = hf * 32 + t < valid ? x[t] : 0.f;
+                    split_pack<16>(x, hi + hf * 16, lo + hf * 16);
+                }
                 tmem_st32u(lane_base + TM_X, hi);
                 tmem_st32u(lane_base + TM_X + 32, lo);
                 tmem_st_wait();
@@ -631,10 +680,14 @@ __global__ void __launch_bounds__(320, 1) chunk_tc_kernel(const __grid_constant_
             tc_fence_after();
             // u^T -> bf16 hi/lo operand in TMEM
             {
-                float u[64];
-                tmem_ld64(lane_base + TM_U, u);
                 uint32_t hi[32], lo[32];
-                split_pack<32>(u, hi, lo);
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    float u[32];
+                    tmem_ld32(lane_base + TM_U + hf * 32, u);
+                    tmem_ld_wait();
+                    split_pack<16>(u, hi + hf * 16, lo + hf * 16);
+                }
                 tmem_st32u(lane_base + TM_U, hi);
                 tmem_st32u(lane_base + TM_U + 32, lo);
                 tmem_st_wait();
@@ -650,13 +703,15 @@ __global__ void __launch_bounds__(320, 1) chunk_tc_kernel(const __grid_constant_
             tc_fence_after();
             epilogue(nchunks - 1);
             if (p.S_T) {
-                float s64[64];
-                tmem_ld64(lane_base + TM_S, s64);
+#pragma unroll 1
+                for (int g = 0; g < 4; ++g) {
+                    float s32[32];
+                    tmem_ld32(lane_base + TM_S + g * 32, s32);
+                    tmem_ld_wait();
+                    float *dst = p.S_T + sbase + (size_t)(g * 32) * D + j;
 #pragma unroll
-                for (int i = 0; i < 64; ++i) p.S_T[sbase + (size_t)i * D + j] = s64[i];
-                tmem_ld64(lane_base + TM_S + 64, s64);
-#pragma unroll
-                for (int i = 0; i < 64; ++i) p.S_T[sbase + (size_t)(64 + i) * D + j] = s64[i];
+                    for (int i = 0; i < 32; ++i) dst[(size_t)i * D] = s32[i];
+                }
             }
         }
         if (lane == 0) bulk_wait0();  // TMA stores have completed before the CTA leaves
@@ -699,7 +754,7 @@ __global__ void __launch_bounds__(320, 1) chunk_tc_kernel(const __grid_constant_
             {  // D^T = V^T (-I): V^T is the stage's V tile read as an MN-major operand
                 const uint32_t idesc = idesc_bf16_f32(128, 64, 1, 0);
                 const uint32_t v_s = kq_s + OFF_V, ni = s_sm + OFF_NEGI;
-#pragma unroll
+#pragma unroll 1
                 for (int ks = 0; ks < 4; ++ks)
                     mma_bf16(tmem + TM_X, smem_desc(v_s + ks * 2048, 8192, 1024), smem_desc(ni + ks * 32, 16, 1024),
                              idesc, ks > 0);
@@ -708,9 +763,9 @@ __global__ void __launch_bounds__(320, 1) chunk_tc_kernel(const __grid_constant_
             tc_fence_after();
             {  // D^T += S^T K^T
                 const uint32_t idesc = idesc_bf16_f32(128, 64, 0, 0);
-#pragma unroll
+#pragma unroll 1
                 for (int part = 0; part < 2; ++part)
-#pragma unroll
+#pragma unroll 1
                     for (int ks = 0; ks < 8; ++ks) {
                         const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
                         mma_bf16_ts(tmem + TM_X, tmem + TM_SA + part * 64 + ks * 8, smem_desc(kq_s + off, 16, 1024),
@@ -722,9 +777,9 @@ __global__ void __launch_bounds__(320, 1) chunk_tc_kernel(const __grid_constant_
             tc_fence_after();
             {  // O1^T = S^T Q^T
                 const uint32_t idesc = idesc_bf16_f32(128, 64, 0, 0);
-#pragma unroll
+#pragma unroll 1
                 for (int part = 0; part < 2; ++part)
-#pragma unroll
+#pragma unroll 1
                     for (int ks = 0; ks < 8; ++ks) {
                         const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32 + 8192;
                         mma_bf16_ts(tmem + TM_O, tmem + TM_SA + part * 64 + ks * 8, smem_desc(kq_s + off, 16, 1024),
@@ -736,11 +791,11 @@ __global__ void __launch_bounds__(320, 1) chunk_tc_kernel(const __grid_constant_
             {  // u^T = D^T T''^T
                 const uint32_t idesc = idesc_bf16_f32(128, 64, 0, 0);
                 const uint32_t tp = s_sm + OFF_TP + buf * 16384;
-#pragma unroll
+#pragma unroll 1
                 for (int part = 0; part < 3; ++part) {
                     const uint32_t a_col = TM_X + (part == 2 ? 32 : 0);
                     const uint32_t b_s = tp + (part == 1 ? 8192 : 0);
-#pragma unroll
+#pragma unroll 1
                     for (int ks = 0; ks < 4; ++ks)
                         mma_bf16_ts(tmem + TM_U, tmem + a_col + ks * 8, smem_desc(b_s + ks * 32, 16, 1024), idesc,
                                     (part | ks) != 0);
@@ -751,9 +806,9 @@ __global__ void __launch_bounds__(320, 1) chunk_tc_kernel(const __grid_constant_
             tc_fence_after();
             {  // S^T += u^T K  (the chain), then O^T += u^T P^T
                 const uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 1);
-#pragma unroll
+#pragma unroll 1
                 for (int part = 0; part < 2; ++part)
-#pragma unroll
+#pragma unroll 1
                     for (int ks = 0; ks < 4; ++ks)
                         mma_bf16_ts(tmem + TM_S, tmem + TM_U + part * 32 + ks * 8,
                                     smem_desc(kq_s + ks * 2048, 16384, 1024), idesc_s, 1);
@@ -761,11 +816,11 @@ __global__ void __launch_bounds__(320, 1) chunk_tc_kernel(const __grid_constant_
                 mma_commit(&bars->s_free[c & 1]);
                 const uint32_t idesc_o = idesc_bf16_f32(128, 64, 0, 0);
                 const uint32_t pb = s_sm + OFF_P + buf * 16384;
-#pragma unroll
+#pragma unroll 1
                 for (int part = 0; part < 3; ++part) {
                     const uint32_t a_col = TM_U + (part == 2 ? 32 : 0);
                     const uint32_t b_s = pb + (part == 1 ? 8192 : 0);
-#pragma unroll
+#pragma unroll 1
                     for (int ks = 0; ks < 4; ++ks)
                         mma_bf16_ts(tmem + TM_O, tmem + a_col + ks * 8, smem_desc(b_s + ks * 32, 16, 1024), idesc_o, 1);
                 }
@@ -828,7 +883,7 @@ cudaError_t launch_typed(const TcParams &p, unsigned grid, cudaStream_t stream) 
         if (e != cudaSuccess) return e;
         if (dev < 64) attr_done[dev] = true;
     }
-    chunk_tc_kernel<OUT_BF16><<<grid, 320, SMEM_ALLOC, stream>>>(p);
+    chunk_tc_kernel<OUT_BF16><<<grid, 448, SMEM_ALLOC, stream>>>(p);
     return cudaGetLastError();
 }
 
