@@ -13,7 +13,7 @@
 //   T~  = (I + A~)^{-1}                                            (blocked forward substitution)
 //   T'  = T~ diag(gamma / n)
 //   U^  = T' (V - K S)            u_t = U^_t / n_t   (= the rank-1 write u_t of token t)
-//   so u = T'' (K S - V) with T'' = -diag(1/n) T~ diag(gamma / n).
+//   so u = T'' (V - K S) with T'' = diag(1/n) T~ diag(gamma / n).
 //   O   = Q S + (Q K^T o M) u     (M lower-triangular INCLUDING the diagonal:
 //                                  o_t reads the state after token t's update)
 //   S  <- S + K^T u
@@ -34,9 +34,9 @@
 // that the state's d_v index is the MMA row (TMEM lane) and the operands S^T,
 // (V - X)^T and u^T are written into TMEM by the thread that owns the lane and
 // read from there by the tensor core:
-//   D^T  = V^T (-I) + S^T K^T = (K S - V)^T   (M = d_v = 128, N = C, K = C and d_k)
-//   O1^T = S^T Q^T                            (M = 128, N = C, K = d_k)
-//   u^T  = D^T T''^T,  T'' = -diag(1/n) T'    (M = 128, N = C, K = C)
+//   [X^T | O1^T] = S^T [K; Q]^T               (M = d_v = 128, N = 2C, K = d_k)
+//   u^T  = V^T T''^T + (-X)^T T''^T           (M = 128, N = C, K = C; V^T read from
+//                                              the stage as an MN-major operand)
 //   O^T         += u^T P^T,  P = Q K^T o M   (M = 128, N = C, K = C)
 //   S^T         += u^T K             (M = 128, N = d_k = 128, K = C; K as MN-major operand)
 // and G = [K ; Q] K^T (M = 2C = 128, N = C, K = d_k) gives the chunk's Gram terms.
@@ -45,7 +45,7 @@
 //   state warpgroup (threads 0-127): thread j owns TMEM lane j (column j of S);
 //     runs the per-chunk dependency chain above and writes o with TMA stores.
 //   MMA thread (warp 8): issues the state chain's tensor-core products.
-//   TMA producer (warp 9): loads K, Q, V into two stages.
+//   TMA producer (warp 9): loads K, Q, V into three stages.
 //   prep warpgroups (warps 4-7 and 10-13): form the Gram products, the gate terms,
 //     T'' and P for the NEXT chunk while the state warpgroup works on the current one.
 // Every wait is bounded; on expiry the CTA records EFLA_ERR_DEVICE_TIMEOUT and
@@ -65,35 +65,37 @@ constexpr int C = 64;
 constexpr int D = 128;
 
 // Shared memory map (bytes from a 1024-byte aligned base).
+constexpr int NSTAGE = 3;
 constexpr uint32_t STAGE_BYTES = 49152;    // [K;Q] [2 cb][128 rows][64] (32 KB) + V [2 cb][64 rows][64] (16 KB)
-constexpr uint32_t OFF_STAGE = 0;          // 2 stages
+constexpr uint32_t OFF_STAGE = 0;          // NSTAGE stages
 constexpr uint32_t OFF_V = 32768;          // within a stage
-constexpr uint32_t OFF_TP = 98304;         // 2 buffers x {hi 8 KB, lo 8 KB}: T' [64 t][64 s]
-constexpr uint32_t OFF_P = 131072;         // 2 buffers x {hi, lo}: P [64 t][64 s]
-constexpr uint32_t OFF_OST = 163840;       // o staging for the TMA stores: 4 warps x [64 t][32], 32 KB
-constexpr uint32_t OFF_AT = 196608;        // fp32 [64][68]: A~, then T~ in place (rows 16-byte aligned)
+// Per chunk parity: T'' {hi 8 KB, lo 8 KB} [64 t][64 s], then P {hi, lo} [64 t][64 s].
+// Once a chunk's last product has read them, the 32 KB hold that chunk's o tile
+// on its way to the TMA store (4 warps x [64 t][32] fp32).
+constexpr uint32_t OFF_TPP = NSTAGE * STAGE_BYTES;
+constexpr uint32_t TPP_BYTES = 32768;
+constexpr uint32_t OFF_AT = OFF_TPP + 2 * TPP_BYTES;  // fp32 [64][68]: A~, then T~ in place (rows 16-byte aligned)
 constexpr uint32_t AT_LD = 68;
-constexpr uint32_t OFF_ROW = OFF_AT + 64 * AT_LD * 4;  // fp32: invn[2][64], gn[2][64], beta[64]
-constexpr uint32_t ROW_BYTES = 6 * 64 * 4;
+constexpr uint32_t OFF_ROW = OFF_AT + 64 * AT_LD * 4;  // fp32: invn[64], gn[64], beta[64]
+constexpr uint32_t ROW_BYTES = 3 * 64 * 4;
 constexpr uint32_t OFF_BAR = OFF_ROW + ROW_BYTES;       // mbarriers (struct Bars)
 constexpr uint32_t OFF_MISC = OFF_BAR + 224;            // tmem base (u32), abort flag (i32)
-constexpr uint32_t OFF_SCR = OFF_MISC + 16;             // fp32 scratch of the triangular inverse
-constexpr uint32_t SCR_FLOATS = 32 * 36;
-constexpr uint32_t OFF_NEGI = (OFF_SCR + SCR_FLOATS * 4 + 1023) & ~1023u;  // -I, 64x64 bf16 (K-major, swizzled)
-constexpr uint32_t SMEM_USED = OFF_NEGI + 8192;
+constexpr uint32_t SMEM_USED = OFF_MISC + 16;
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;       // + alignment slack for the 1024-byte base
-static_assert(OFF_TP == 2 * STAGE_BYTES && OFF_P == OFF_TP + 32768 && OFF_OST == OFF_P + 32768 &&
-                  OFF_AT == OFF_OST + 32768,
-              "shared memory regions must not overlap");
+static_assert(OFF_TPP % 1024 == 0 && OFF_AT % 1024 == 0, "operand buffers must be 1024-byte aligned");
 static_assert(SMEM_ALLOC <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
 
 // TMEM columns (32-bit; lane = row of the MMA result)
-constexpr uint32_t TM_S = 0;    // S^T fp32                        128 columns
-constexpr uint32_t TM_SA = 128; // S^T as bf16 operand: hi 64, lo 64 columns
-constexpr uint32_t TM_X = 256;  // X^T fp32 (64), then (V-X)^T bf16 hi 32 + lo 32
-constexpr uint32_t TM_O = 320;  // O^T fp32                         64 columns
-constexpr uint32_t TM_U = 384;  // U^^T fp32 (64), then u^T bf16 hi 32 + lo 32
-constexpr uint32_t TM_G = 448;  // [K;Q] K^T fp32                   64 columns
+// A tcgen05.mma of M = 128 occupies the tensor pipe for about the same time at
+// N = 64 as at N = 128, so products that share their A operand are issued as one
+// instruction over adjacent B rows and adjacent accumulator columns.
+constexpr uint32_t TM_S = 0;    // S^T fp32                                       128 columns
+constexpr uint32_t TM_SA = 128; // S^T as bf16 operand: hi 64, lo 64; then the two
+                                // partial sums of u^T (fp32, 64 + 64)
+constexpr uint32_t TM_X = 256;  // D^T fp32 (64), then D^T bf16 hi 32 + lo 32, then u^T bf16 hi 32 + lo 32
+constexpr uint32_t TM_O = 320;  // O^T fp32 (64); adjacent to TM_X: D^T and O^T share one product
+constexpr uint32_t TM_OB = 384; // second O^T accumulator (the u_hi P_lo term)    64 columns
+constexpr uint32_t TM_G = 448;  // [K;Q] K^T fp32                                  64 columns
 constexpr uint32_t TM_COLS = 512;
 
 constexpr uint64_t WAIT_NS = 2000000000ull;  // 2 s bound on any wait
@@ -116,8 +118,9 @@ struct TcParams {
 };
 
 struct Bars {
-    uint64_t tma_full[2];    // K, Q, V of a stage landed
-    uint64_t g_done;         // Gram MMA of the prep warpgroup
+    uint64_t tma_full[NSTAGE];  // K, Q, V of a stage landed
+    uint64_t g_done;         // Gram MMA of a chunk complete
+    uint64_t g_free;         // the prep warpgroups have read a chunk's Gram products
     uint64_t x_done;         // X^T = S^T K^T
     uint64_t u_done;         // U^^T
     uint64_t s_done;         // S^T += u^T K
@@ -129,7 +132,8 @@ struct Bars {
     uint64_t r_ready;        // state warpgroup wrote (V - X)^T hi/lo  (128 arrivals)
     uint64_t u_ready;        // state warpgroup wrote u^T hi/lo        (128 arrivals)
     uint64_t drain[2];       // all MMAs of the MMA thread / of the prep thread complete
-    uint64_t s_free[2];      // the state update of a chunk complete: its K/Q/V stage is free
+    uint64_t s_free[NSTAGE];  // the state update of a chunk complete: its K/Q/V stage is free
+    uint64_t ost_free[2];     // the TMA stores of a chunk's o tile have read it (4 arrivals)
 };
 static_assert(sizeof(Bars) <= 224, "mbarrier block exceeds its slot");
 
@@ -150,6 +154,13 @@ __device__ __noinline__ bool wait_bar_slow(uint64_t *bar, uint32_t parity, volat
 __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
     if (mbar_try_wait(bar, parity)) return true;
     return wait_bar_slow(bar, parity, abort_flag);
+}
+
+// Hides a loop counter from the optimiser so that the loop stays rolled (the
+// kernel's per-chunk code must fit the instruction cache).
+__device__ __forceinline__ int opaque(int i) {
+    asm volatile("" : "+r"(i));
+    return i;
 }
 
 // Splits pairs x[2c], x[2c+1] into packed bf16 hi and lo words with
@@ -185,8 +196,9 @@ __device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t (&u)[3
 }
 
 // T~ = (I + A~)^{-1} in place in At (fp32, row stride AT_LD), by the 256
-// threads of the two prep warpgroups (index pi), with a scratch Y of SCR_FLOATS
-// floats.  Each step applies
+// threads of the two prep warpgroups (index pi).  The scratch Y of the products
+// lives in the upper-right 32x32 block of At, which the inverse never reads.
+// Each step applies
 //   [[L1, 0], [B, L2]]^{-1} = [[L1^{-1}, 0], [-L2^{-1} B L1^{-1}, L2^{-1}]]
 // for unit lower-triangular L1, L2:
 //   1. the four diagonal 16x16 blocks by column substitution (two warps per
@@ -195,7 +207,8 @@ __device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t (&u)[3
 //   2. blocks (1,0) and (3,2) of 16:  T~_IJ = -T~_II (A~_IJ T~_JJ);
 //   3. the lower-left 32x32 block:    T~_21 = -T~_22 (A~_21 T~_11)  (32x32 blocks).
 // Steps 2 and 3 are register-tiled fp32 products.
-__device__ __forceinline__ void invert_unit_lower(float *At, float *Y, int pi) {
+__device__ __forceinline__ void invert_unit_lower(float *At, int pi) {
+    float *Y = At + 32;  // [32][AT_LD] rows 0-31, columns 32-63
     const int lane = pi & 31, pw = pi >> 5;
     {
         const int B0 = (pw >> 1) * 16, c = (lane & 7) + 8 * (pw & 1), r4 = lane >> 3;
@@ -221,7 +234,7 @@ __device__ __forceinline__ void invert_unit_lower(float *At, float *Y, int pi) {
         const int q = pi >> 7, tt = pi & 127;
         const int I = 2 * q + 1, J = 2 * q;
         const int r = tt >> 3, c0 = (tt & 7) * 2;
-        float *yq = Y + q * (16 * 20);  // [16][20]
+        float *yq = Y + q * (16 * AT_LD);  // [16][AT_LD]
         float y0 = 0.f, y1 = 0.f;
         const float *arow = At + (16 * I + r) * AT_LD + 16 * J;
 #pragma unroll
@@ -235,7 +248,7 @@ __device__ __forceinline__ void invert_unit_lower(float *At, float *Y, int pi) {
                 y1 = fmaf(av[e], bv.y, y1);
             }
         }
-        *reinterpret_cast<float2 *>(yq + r * 20 + c0) = make_float2(y0, y1);
+        *reinterpret_cast<float2 *>(yq + r * AT_LD + c0) = make_float2(y0, y1);
         named_bar(BAR_PREP, 256);
         float z0 = 0.f, z1 = 0.f;
         const float *trow = At + (16 * I + r) * AT_LD + 16 * I;  // T~_II row r (zeros above the diagonal)
@@ -245,7 +258,7 @@ __device__ __forceinline__ void invert_unit_lower(float *At, float *Y, int pi) {
             const float tv[4] = {tq.x, tq.y, tq.z, tq.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const float2 yv = *reinterpret_cast<const float2 *>(yq + (k4 + e) * 20 + c0);
+                const float2 yv = *reinterpret_cast<const float2 *>(yq + (k4 + e) * AT_LD + c0);
                 z0 = fmaf(tv[e], yv.x, z0);
                 z1 = fmaf(tv[e], yv.y, z1);
             }
@@ -272,8 +285,8 @@ __device__ __forceinline__ void invert_unit_lower(float *At, float *Y, int pi) {
                 x11 = fmaf(va1[e], bv.y, x11);
             }
         }
-        *reinterpret_cast<float2 *>(Y + r0 * 36 + c0) = make_float2(x00, x01);
-        *reinterpret_cast<float2 *>(Y + (r0 + 1) * 36 + c0) = make_float2(x10, x11);
+        *reinterpret_cast<float2 *>(Y + r0 * AT_LD + c0) = make_float2(x00, x01);
+        *reinterpret_cast<float2 *>(Y + (r0 + 1) * AT_LD + c0) = make_float2(x10, x11);
         named_bar(BAR_PREP, 256);
         float z00 = 0.f, z01 = 0.f, z10 = 0.f, z11 = 0.f;
         const float *t0 = At + (32 + r0) * AT_LD + 32, *t1 = t0 + AT_LD;  // T~_22 rows
@@ -284,7 +297,7 @@ __device__ __forceinline__ void invert_unit_lower(float *At, float *Y, int pi) {
             const float tv0[4] = {p0.x, p0.y, p0.z, p0.w}, tv1[4] = {p1.x, p1.y, p1.z, p1.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const float2 xv = *reinterpret_cast<const float2 *>(Y + (k4 + e) * 36 + c0);
+                const float2 xv = *reinterpret_cast<const float2 *>(Y + (k4 + e) * AT_LD + c0);
                 z00 = fmaf(tv0[e], xv.x, z00);
                 z01 = fmaf(tv0[e], xv.y, z01);
                 z10 = fmaf(tv1[e], xv.x, z10);
@@ -298,14 +311,25 @@ __device__ __forceinline__ void invert_unit_lower(float *At, float *Y, int pi) {
     }
 }
 
+// G = [K; Q] K^T of chunk c (M = 128, N = C, K = d_k) into TM_G, completion on g_done.
+__device__ __forceinline__ void issue_gram(uint32_t tmem, uint32_t s_sm, int c, Bars *bars) {
+    const uint32_t kq = s_sm + OFF_STAGE + (c % NSTAGE) * STAGE_BYTES;
+    const uint32_t idesc = idesc_bf16_f32(128, 64, 0, 0);
+#pragma unroll 1
+    for (int ks = 0; ks < 8; ks = opaque(ks + 1)) {
+        const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+        mma_bf16(tmem + TM_G, smem_desc(kq + off, 16, 1024), smem_desc(kq + off, 16, 1024), idesc, ks > 0);
+    }
+    mma_commit(&bars->g_done);
+}
+
 template <bool OUT_BF16>
 __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant__ TcParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    float *row_invn = reinterpret_cast<float *>(sm + OFF_ROW);  // [2][64]
-    float *row_gn = row_invn + 128;                             // [2][64]
-    float *row_beta = row_invn + 256;                           // [64] (prep only)
-    float *scr = reinterpret_cast<float *>(sm + OFF_SCR);
+    float *row_invn = reinterpret_cast<float *>(sm + OFF_ROW);  // [64] 1/n_t
+    float *row_gn = row_invn + 64;                              // [64] gamma_t/n_t
+    float *row_beta = row_invn + 128;                           // [64]
     float *At = reinterpret_cast<float *>(sm + OFF_AT);
     Bars *bars = reinterpret_cast<Bars *>(sm + OFF_BAR);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + OFF_MISC);
@@ -338,9 +362,14 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
     }
 
     if (tid == 0) {
-        mbar_init(&bars->tma_full[0], 1);
-        mbar_init(&bars->tma_full[1], 1);
+        for (int i = 0; i < NSTAGE; ++i) {
+            mbar_init(&bars->tma_full[i], 1);
+            mbar_init(&bars->s_free[i], 1);
+        }
+        mbar_init(&bars->ost_free[0], 4);
+        mbar_init(&bars->ost_free[1], 4);
         mbar_init(&bars->g_done, 1);
+        mbar_init(&bars->g_free, 1);
         mbar_init(&bars->x_done, 1);
         mbar_init(&bars->u_done, 1);
         mbar_init(&bars->s_done, 1);
@@ -355,32 +384,12 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
         mbar_init(&bars->u_ready, 128);
         mbar_init(&bars->drain[0], 1);
         mbar_init(&bars->drain[1], 1);
-        mbar_init(&bars->s_free[0], 1);
-        mbar_init(&bars->s_free[1], 1);
         fence_mbar_init();
         *abort_flag = 0;
     }
     if (warp == 0) {
         tmem_alloc(tmem_slot, TM_COLS);
         tmem_relinquish();
-    }
-    if (tid >= 128 && tid < 192) {  // -I as a K-major bf16 operand: row t holds -1 in column t
-        const int t = tid - 128;
-        uint8_t *negi = sm + OFF_NEGI;
-#pragma unroll
-        for (int c8 = 0; c8 < 64; c8 += 8) {
-            uint4 w = make_uint4(0, 0, 0, 0);
-            if (t >= c8 && t < c8 + 8) {
-                const uint32_t m1 = 0xBF80u << (16 * ((t - c8) & 1));  // bf16(-1) in the low or high half
-                const int word = (t - c8) >> 1;
-                if (word == 0) w.x = m1;
-                if (word == 1) w.y = m1;
-                if (word == 2) w.z = m1;
-                if (word == 3) w.w = m1;
-            }
-            *reinterpret_cast<uint4 *>(negi + swz_offset(t, c8, 8192)) = w;
-        }
-        fence_proxy_async_smem();
     }
     tc_fence_before();
     __syncthreads();
@@ -399,36 +408,23 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
         const int row = quarter * 32 + (tid & 31);
         const int col0 = half * 32;
         const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
-        const bool leader = pi == 0;  // issues the Gram MMAs
-        int g_issued = 0;             // chunks whose Gram MMA was issued (leader)
-        auto issue_gram = [&](int c) {
-            const uint32_t kq = s_sm + OFF_STAGE + (c & 1) * STAGE_BYTES;
-            const uint32_t idesc = idesc_bf16_f32(128, 64, 0, 0);
-#pragma unroll 1
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-                mma_bf16(tmem + TM_G, smem_desc(kq + off, 16, 1024), smem_desc(kq + off, 16, 1024), idesc, ks > 0);
-            }
-            mma_commit(&bars->g_done);
-            g_issued = c + 1;
+        const bool leader = pi == 0;  // signals the other roles
+        // beta of the next chunk is loaded a chunk ahead (its latency hides behind the prep)
+        auto load_beta = [&](int cc) {
+            const long t0n = bos + (long)cc * C;
+            return (cc < nchunks && pi < C && t0n + pi < eos)
+                       ? p.beta[((size_t)b * p.T + (size_t)(t0n + pi)) * p.H + h] : 0.f;
         };
-        // Leader, during chunk c: start the Gram MMA of chunk c+1 as soon as its tile has
-        // landed (full chunks only: a partial chunk's tail is zeroed first).  Non-blocking.
-        auto prefetch_gram = [&](int c) {
-            if (c + 1 >= nchunks || g_issued != c + 1 || eos - (bos + (long)(c + 1) * C) < C) return;
-            if (mbar_try_wait(&bars->tma_full[(c + 1) & 1], ((c + 1) >> 1) & 1)) {
-                tc_fence_after();
-                issue_gram(c + 1);
-            }
-        };
+        float beta_next = load_beta(0);
         for (int c = 0; c < nchunks; ++c) {
-            const int st = c & 1, buf = c & 1;
+            const int st = c % NSTAGE, buf = c & 1;
             const long tok0 = bos + (long)c * C;
             const int valid = (int)min((long)C, eos - tok0);
             uint8_t *KQ = sm + OFF_STAGE + st * STAGE_BYTES;
 
-            if (pi < C) row_beta[pi] = pi < valid ? p.beta[((size_t)b * p.T + (size_t)(tok0 + pi)) * p.H + h] : 0.f;
-            bool ok = wait_bar(&bars->tma_full[st], (c >> 1) & 1, abort_flag);
+            if (pi < C) row_beta[pi] = beta_next;
+            beta_next = load_beta(c + 1);
+            bool ok = wait_bar(&bars->tma_full[st], (c / NSTAGE) & 1, abort_flag);
             if (ok && valid < C) {  // rows past the end of the sequence are zeroed (they may hold the next one)
                 const int rows = C - valid;
                 for (int e = pi; e < 4 * rows * 8; e += 256) {
@@ -444,14 +440,19 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
                 break;
             }
 
-            // Gram products G = [K;Q] K^T (unless already started during the previous chunk)
-            if (leader && g_issued == c) {
+            // Gram products G = [K;Q] K^T: issued by the MMA thread ahead of time, except for
+            // a partial chunk, whose tail must be zeroed first
+            if (leader && valid < C) {
                 tc_fence_after();
-                issue_gram(c);
+                issue_gram(tmem, s_sm, c, bars);
             }
             ok = wait_bar(&bars->g_done, c & 1, abort_flag);
-            // the T''/P buffers of this chunk were last read by chunk c-2's MMAs
-            if (c >= 2) ok = wait_bar(&bars->chunk_done[c & 1], ((c - 2) >> 1) & 1, abort_flag) && ok;
+            // the T''/P buffers of this chunk were last read by chunk c-2's MMAs, then
+            // held chunk c-2's o tile until its TMA stores had read it
+            if (c >= 2) {
+                ok = wait_bar(&bars->chunk_done[c & 1], ((c - 2) >> 1) & 1, abort_flag) && ok;
+                ok = wait_bar(&bars->ost_free[c & 1], ((c - 2) >> 1) & 1, abort_flag) && ok;
+            }
             tc_fence_after();
             {
                 float g[32];
@@ -467,19 +468,20 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
                     const bool live = t < valid && lam > 0.f;
                     const float invn = live ? rsqrtf(lam) : 0.f;
                     const float gam = !live ? 0.f : p.euler ? row_beta[t] * lam : -expm1f(-row_beta[t] * lam);
-                    row_invn[buf * 64 + t] = invn;
-                    row_gn[buf * 64 + t] = gam * invn;
+                    row_invn[t] = invn;
+                    row_gn[t] = gam * invn;
                 }
                 // [gate: terms computed]
                 named_bar(BAR_PREP, 256);
                 // [gate: barrier passed]
+                if (leader) mbar_arrive(&bars->g_free);  // every row of G has been read
                 if (row < C) {  // A~[t][col0 .. col0+31]
                     const int t = row;
-                    const float rs = row_gn[buf * 64 + t];  // gamma_t / n_t
+                    const float rs = row_gn[t];  // gamma_t / n_t
                     float iv[32];  // all scales first: the stores below may alias them for the compiler
 #pragma unroll
                     for (int s4 = 0; s4 < 8; ++s4) {
-                        const float4 f = reinterpret_cast<const float4 *>(row_invn + buf * 64 + col0)[s4];
+                        const float4 f = reinterpret_cast<const float4 *>(row_invn + col0)[s4];
                         iv[4 * s4] = f.x;
                         iv[4 * s4 + 1] = f.y;
                         iv[4 * s4 + 2] = f.z;
@@ -498,7 +500,7 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
                     const int t = row - C;
 #pragma unroll
                     for (int s = 0; s < 32; ++s) g[s] = col0 + s <= t ? g[s] : 0.f;
-                    uint8_t *phi = sm + OFF_P + buf * 16384, *plo = phi + 8192;
+                    uint8_t *phi = sm + OFF_TPP + buf * TPP_BYTES + 16384, *plo = phi + 8192;
 #pragma unroll
                     for (int c8 = 0; c8 < 32; c8 += 8) {
                         uint32_t hh[4], ll[4];
@@ -510,20 +512,18 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
                 }
             }
             named_bar(BAR_PREP, 256);
-            if (leader) prefetch_gram(c);
-            invert_unit_lower(At, scr, pi);
-            if (leader) prefetch_gram(c);
-            {  // T'' = -diag(1/n) T~ diag(gamma/n), lower triangle, as bf16 hi/lo [t][s]
+            invert_unit_lower(At, pi);
+            {  // T'' = diag(1/n) T~ diag(gamma/n), lower triangle, as bf16 hi/lo [t][s]
                 const int t = pi >> 2, s0 = (pi & 3) * 16;
-                uint8_t *hi = sm + OFF_TP + buf * 16384, *lo = hi + 8192;
-                const float rsc = -row_invn[buf * 64 + t];
+                uint8_t *hi = sm + OFF_TPP + buf * TPP_BYTES, *lo = hi + 8192;
+                const float rsc = row_invn[t];
 #pragma unroll
                 for (int c8 = 0; c8 < 16; c8 += 8) {
                     float tt8[8], gn8[8];
                     *reinterpret_cast<float4 *>(tt8) = *reinterpret_cast<const float4 *>(At + t * AT_LD + s0 + c8);
                     *reinterpret_cast<float4 *>(tt8 + 4) = *reinterpret_cast<const float4 *>(At + t * AT_LD + s0 + c8 + 4);
-                    *reinterpret_cast<float4 *>(gn8) = *reinterpret_cast<const float4 *>(row_gn + buf * 64 + s0 + c8);
-                    *reinterpret_cast<float4 *>(gn8 + 4) = *reinterpret_cast<const float4 *>(row_gn + buf * 64 + s0 + c8 + 4);
+                    *reinterpret_cast<float4 *>(gn8) = *reinterpret_cast<const float4 *>(row_gn + s0 + c8);
+                    *reinterpret_cast<float4 *>(gn8 + 4) = *reinterpret_cast<const float4 *>(row_gn + s0 + c8 + 4);
                     float x[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
@@ -540,11 +540,7 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
             fence_proxy_async_smem();
             named_bar(BAR_PREP, 256);
             if (leader) mbar_arrive(&bars->prep_ready[buf]);
-            if (leader) prefetch_gram(c);
-            if (named_bar_any(BAR_PREP, 256, !ok || *abort_flag)) {
-                *abort_flag = 1;
-                break;
-            }
+            if (!ok) *abort_flag = 1;  // seen by every prep thread at the next chunk's first barrier
         }
         if (leader) {  // every Gram MMA has completed before TMEM is released (bounded)
             mma_commit(&bars->drain[1]);
@@ -564,7 +560,7 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
         {  // initial state -> TMEM (S^T: lane j holds column j of S)
             float r[32];
 #pragma unroll 1
-            for (int g = 0; g < 4; ++g) {
+            for (int g = 0; g < 4; g = opaque(g + 1)) {
 #pragma unroll
                 for (int i = 0; i < 32; ++i) r[i] = p.S0 ? p.S0[sbase + (size_t)(g * 32 + i) * D + j] : 0.f;
                 tmem_st32(lane_base + TM_S + g * 32, r);
@@ -576,18 +572,38 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
         // them with one TMA store, so no cross-warp synchronisation is needed.  A
         // partial chunk of a packed batch is written with plain stores instead (a
         // TMA box would spill into the next sequence).
+        // The second O accumulator starts every chunk at zero (the first is overwritten
+        // by the chunk's first product).
+        auto clear_ob = [&]() {
+            float z[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) z[i] = 0.f;
+            tmem_st32(lane_base + TM_OB, z);
+            tmem_st32(lane_base + TM_OB + 32, z);
+            tmem_st_wait();
+        };
+        clear_ob();
         auto epilogue = [&](int cc) {
             const long t0c = bos + (long)cc * C;
             const int vc = (int)min((long)C, eos - t0c);
             float ov[32], ow[32];
-            tmem_ld32(lane_base + TM_O, ov);
-            tmem_ld32(lane_base + TM_O + 32, ow);
-            tmem_ld_wait();
+            {
+                float t1[32];
+                tmem_ld32(lane_base + TM_O, ov);
+                tmem_ld32(lane_base + TM_OB, t1);
+                tmem_ld_wait();
+#pragma unroll
+                for (int t = 0; t < 32; ++t) ov[t] += t1[t];
+                tmem_ld32(lane_base + TM_O + 32, ow);
+                tmem_ld32(lane_base + TM_OB + 32, t1);
+                tmem_ld_wait();
+#pragma unroll
+                for (int t = 0; t < 32; ++t) ow[t] += t1[t];
+            }
             tc_fence_before();
-            mbar_arrive(&bars->o_free);
-            uint8_t *slice = sm + OFF_OST + warp * 8192;
-            if (lane == 0) bulk_wait_read0();  // this warp's previous store has read its slice
-            __syncwarp();
+            mbar_arrive(&bars->o_free);  // the next chunk's first product may overwrite O^T
+            // the chunk's T''/P buffers (free once its last product completed) stage the tile
+            uint8_t *slice = sm + OFF_TPP + (cc & 1) * TPP_BYTES + warp * 8192;
             if (OUT_BF16) {
                 __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(slice) + lane;
 #pragma unroll
@@ -609,11 +625,13 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
                 if (lane == 0) {
                     tma_store_4d(&p.map_o, slice, warp * 32, h, (int)t0c, (int)b);
                     bulk_commit();
+                    bulk_wait_read0();  // the slice may be rewritten by the prep two chunks on
+                    mbar_arrive(&bars->ost_free[cc & 1]);
                 }
             } else {  // partial chunk of a packed batch: rows past vc belong to the next sequence
                 __syncwarp();
 #pragma unroll 1
-                for (int t = 0; t < vc; ++t) {
+                for (int t = 0; t < vc; t = opaque(t + 1)) {
                     const size_t rw = ((size_t)b * p.T + (size_t)(t0c + t)) * p.H + h;
                     if (OUT_BF16)
                         static_cast<__nv_bfloat16 *>(p.o)[rw * D + j] =
@@ -621,111 +639,112 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
                     else
                         static_cast<float *>(p.o)[rw * D + j] = reinterpret_cast<const float *>(slice)[t * 32 + lane];
                 }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->ost_free[cc & 1]);
             }
+            clear_ob();  // before this warpgroup's next u_ready, which precedes the next O_b product
         };
+        // One pass per chunk c plus a final pass: the operands of chunk c, and the
+        // outputs of chunk c-1 (one call site keeps the per-chunk code small).
         bool ok = true;
-        for (int c = 0; c < nchunks && ok; ++c) {
-            const int buf = c & 1;
-            const long tok0 = bos + (long)c * C;
-            const int valid = (int)min((long)C, eos - tok0);
-            ok = wait_bar(&bars->prep_ready[buf], (c >> 1) & 1, abort_flag);
-            if (c > 0) ok = ok && wait_bar(&bars->s_done, (c - 1) & 1, abort_flag);
-            tc_fence_after();
-            // S^T -> bf16 hi/lo operand in TMEM
-            {
-                float s[32];
-                uint32_t hi[32], lo[32];
+        for (int c = 0; c <= nchunks && ok; ++c) {
+            const bool live = c < nchunks;
+            if (live) {
+                // The S^T operand needs only the previous state update, not this chunk's prep.
+                if (c > 0) ok = wait_bar(&bars->s_done, (c - 1) & 1, abort_flag);
+                tc_fence_after();
+                // S^T -> bf16 hi/lo operand in TMEM, 32 columns of S^T (16 operand columns) at a time
 #pragma unroll 1
-                for (int g = 0; g < 4; g += 2) {
-                    tmem_ld32(lane_base + TM_S + g * 32, s);
+                for (int g = 0; g < 4; g = opaque(g + 1)) {
+                    float sv[32];
+                    uint32_t hi[16], lo[16];
+                    tmem_ld32(lane_base + TM_S + g * 32, sv);
                     tmem_ld_wait();
-                    split_pack<16>(s, hi, lo);
-                    tmem_ld32(lane_base + TM_S + g * 32 + 32, s);
-                    tmem_ld_wait();
-                    split_pack<16>(s, hi + 16, lo + 16);
-                    tmem_st32u(lane_base + TM_SA + g * 16, hi);
-                    tmem_st32u(lane_base + TM_SA + 64 + g * 16, lo);
+                    split_pack<16>(sv, hi, lo);
+                    tmem_st16u(lane_base + TM_SA + g * 16, hi);
+                    tmem_st16u(lane_base + TM_SA + 64 + g * 16, lo);
                 }
                 tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(&bars->sa_ready);
             }
-            tc_fence_before();
-            mbar_arrive(&bars->sa_ready);
-            // outputs of chunk c-1 leave while X is computed
-            if (c > 0) {
+            if (c > 0) {  // outputs of chunk c-1 leave while X of chunk c is computed
                 ok = ok && wait_bar(&bars->o_done, (c - 1) & 1, abort_flag);
+                if (!ok) break;
                 tc_fence_after();
                 epilogue(c - 1);
             }
+            if (!live) break;
+            const long tok0 = bos + (long)c * C;
+            const int valid = (int)min((long)C, eos - tok0);
             ok = ok && wait_bar(&bars->x_done, c & 1, abort_flag);
             tc_fence_after();
-            // D^T = (K S - V)^T -> bf16 hi/lo operand in TMEM (rows past the sequence end are zero)
+            // (-X)^T = -(K S)^T -> bf16 hi/lo operand in TMEM (rows past the sequence end are zero),
+            // written over X once all of X is in registers
             {
-                uint32_t hi[32], lo[32];
+                float x0[32], x1[32];
+                tmem_ld32(lane_base + TM_X, x0);
+                tmem_ld32(lane_base + TM_X + 32, x1);
+                tmem_ld_wait();
+                uint32_t hi[16], lo[16];
 #pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    float x[32];
-                    tmem_ld32(lane_base + TM_X + hf * 32, x);
-                    tmem_ld_wait();
+                for (int t = 0; t < 32; ++t) x0[t] = t < valid ? -x0[t] : 0.f;
+                split_pack<16>(x0, hi, lo);
+                tmem_st16u(lane_base + TM_X, hi);
+                tmem_st16u(lane_base + TM_X + 32, lo);
 #pragma unroll
-                    for (int t = 0; t < 32; ++t) x[t] = hf * 32 + t < valid ? x[t] : 0.f;
-                    split_pack<16>(x, hi + hf * 16, lo + hf * 16);
-                }
-                tmem_st32u(lane_base + TM_X, hi);
-                tmem_st32u(lane_base + TM_X + 32, lo);
-                tmem_st_wait();
+                for (int t = 0; t < 32; ++t) x1[t] = 32 + t < valid ? -x1[t] : 0.f;
+                split_pack<16>(x1, hi, lo);
+                tmem_st16u(lane_base + TM_X + 16, hi);
+                tmem_st16u(lane_base + TM_X + 48, lo);
             }
+            tmem_st_wait();
             tc_fence_before();
             mbar_arrive(&bars->r_ready);
             ok = ok && wait_bar(&bars->u_done, c & 1, abort_flag);
             tc_fence_after();
-            // u^T -> bf16 hi/lo operand in TMEM
-            {
-                uint32_t hi[32], lo[32];
+            // u^T = U1 + U2 -> bf16 hi/lo operand in TMEM
+#pragma unroll 1
+            for (int hf = 0; hf < 2; hf = opaque(hf + 1)) {
+                float u[32], u2[32];
+                uint32_t hi[16], lo[16];
+                tmem_ld32(lane_base + TM_SA + hf * 32, u);
+                tmem_ld32(lane_base + TM_SA + 64 + hf * 32, u2);
+                tmem_ld_wait();
 #pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    float u[32];
-                    tmem_ld32(lane_base + TM_U + hf * 32, u);
-                    tmem_ld_wait();
-                    split_pack<16>(u, hi + hf * 16, lo + hf * 16);
-                }
-                tmem_st32u(lane_base + TM_U, hi);
-                tmem_st32u(lane_base + TM_U + 32, lo);
-                tmem_st_wait();
+                for (int t = 0; t < 32; ++t) u[t] += u2[t];
+                split_pack<16>(u, hi, lo);
+                tmem_st16u(lane_base + TM_X + hf * 16, hi);
+                tmem_st16u(lane_base + TM_X + 32 + hf * 16, lo);
             }
+            tmem_st_wait();
             tc_fence_before();
             mbar_arrive(&bars->u_ready);
         }
-        // outputs of the last chunk, then the final state
-        ok = ok && wait_bar(&bars->o_done, (nchunks - 1) & 1, abort_flag) &&
-             wait_bar(&bars->s_done, (nchunks - 1) & 1, abort_flag);
         if (!ok) *abort_flag = 1;
-        if (ok) {
-            tc_fence_after();
-            epilogue(nchunks - 1);
-            if (p.S_T) {
+        if (ok && p.S_T) {  // final state (every product has completed: o_done of the last chunk)
 #pragma unroll 1
-                for (int g = 0; g < 4; ++g) {
-                    float s32[32];
-                    tmem_ld32(lane_base + TM_S + g * 32, s32);
-                    tmem_ld_wait();
-                    float *dst = p.S_T + sbase + (size_t)(g * 32) * D + j;
+            for (int g = 0; g < 4; g = opaque(g + 1)) {
+                float s32[32];
+                tmem_ld32(lane_base + TM_S + g * 32, s32);
+                tmem_ld_wait();
+                float *dst = p.S_T + sbase + (size_t)(g * 32) * D + j;
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) dst[(size_t)i * D] = s32[i];
-                }
+                for (int i = 0; i < 32; ++i) dst[(size_t)i * D] = s32[i];
             }
         }
         if (lane == 0) bulk_wait0();  // TMA stores have completed before the CTA leaves
     } else if (tid == 288) {
         // ============================ TMA producer (one thread) ============================
-        // Chunk c goes into stage c % 2 once the state update of chunk c-2 (the last
-        // reader of that stage) has completed.
+        // Chunk c goes into stage c % NSTAGE once the state update of chunk c - NSTAGE
+        // (the last reader of that stage) has completed.
         prefetch_tensormap(&p.map_q);
         prefetch_tensormap(&p.map_k);
         prefetch_tensormap(&p.map_v);
         int issued = 0;
         for (int c = 0; c < nchunks; ++c) {
-            if (c >= 2 && !wait_bar(&bars->s_free[c & 1], ((c - 2) >> 1) & 1, abort_flag)) break;
-            const int st = c & 1;
+            if (c >= NSTAGE && !wait_bar(&bars->s_free[c % NSTAGE], ((c - NSTAGE) / NSTAGE) & 1, abort_flag)) break;
+            const int st = c % NSTAGE;
             uint8_t *dst = sm + OFF_STAGE + st * STAGE_BYTES;
             const int tok = (int)(bos + (long)c * C);
             mbar_arrive_expect_tx(&bars->tma_full[st], STAGE_BYTES);
@@ -737,93 +756,96 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
             issued = c + 1;
         }
         // the last loads have landed before the CTA can leave (bounded; matters after an abort)
-        for (int cc = max(0, issued - 2); cc < issued; ++cc) {
+        for (int cc = max(0, issued - NSTAGE); cc < issued; ++cc) {
             const uint64_t t0 = globaltimer_ns();
-            while (!mbar_try_wait_sleep(&bars->tma_full[cc & 1], (cc >> 1) & 1, 20000) &&
+            while (!mbar_try_wait_sleep(&bars->tma_full[cc % NSTAGE], (cc / NSTAGE) & 1, 20000) &&
                    globaltimer_ns() - t0 < WAIT_NS) {
             }
         }
     } else if (tid == 256) {
         // ================================ MMA warp (one thread) ================================
         bool ok = true;
+        // Gram products of full chunks up to `limit`, each once the prep has read the
+        // previous one (one TM_G buffer) and the chunk's tile has landed.
+        int g_next = 0;
+        auto issue_grams = [&](int limit) {
+            while (ok && g_next <= limit && g_next < nchunks && eos - (bos + (long)g_next * C) >= C) {
+                if (g_next > 0 && !(ok = wait_bar(&bars->g_free, (g_next - 1) & 1, abort_flag))) break;
+                if (!(ok = wait_bar(&bars->tma_full[g_next % NSTAGE], (g_next / NSTAGE) & 1, abort_flag))) break;
+                tc_fence_after();
+                issue_gram(tmem, s_sm, g_next, bars);
+                ++g_next;
+            }
+        };
+        issue_grams(0);
         for (int c = 0; c < nchunks && ok; ++c) {
-            const int st = c & 1, buf = c & 1;
+            const int st = c % NSTAGE, buf = c & 1;
             const uint32_t kq_s = s_sm + OFF_STAGE + st * STAGE_BYTES;
+            const uint32_t tp = s_sm + OFF_TPP + buf * TPP_BYTES, pb = tp + 16384;
             if (!(ok = wait_bar(&bars->prep_ready[buf], (c >> 1) & 1, abort_flag))) break;
             tc_fence_after();
-            {  // D^T = V^T (-I): V^T is the stage's V tile read as an MN-major operand
-                const uint32_t idesc = idesc_bf16_f32(128, 64, 1, 0);
-                const uint32_t v_s = kq_s + OFF_V, ni = s_sm + OFF_NEGI;
-#pragma unroll 1
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16(tmem + TM_X, smem_desc(v_s + ks * 2048, 8192, 1024), smem_desc(ni + ks * 32, 16, 1024),
-                             idesc, ks > 0);
-            }
+            issue_grams(c + 1);
+            if (!ok) break;
             if (!(ok = wait_bar(&bars->sa_ready, c & 1, abort_flag))) break;
+            if (c > 0 && !(ok = wait_bar(&bars->o_free, (c - 1) & 1, abort_flag))) break;
             tc_fence_after();
-            {  // D^T += S^T K^T
-                const uint32_t idesc = idesc_bf16_f32(128, 64, 0, 0);
+            {  // [X^T | O^T] = S^T [K; Q]^T: one N = 128 product over the stage's [K; Q] rows
+                const uint32_t idesc = idesc_bf16_f32(128, 128, 0, 0);
 #pragma unroll 1
-                for (int part = 0; part < 2; ++part)
+                for (int part = 0; part < 2; part = opaque(part + 1))
 #pragma unroll 1
-                    for (int ks = 0; ks < 8; ++ks) {
+                    for (int ks = 0; ks < 8; ks = opaque(ks + 1)) {
                         const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
                         mma_bf16_ts(tmem + TM_X, tmem + TM_SA + part * 64 + ks * 8, smem_desc(kq_s + off, 16, 1024),
-                                    idesc, 1);
+                                    idesc, (part | ks) != 0);
                     }
                 mma_commit(&bars->x_done);
             }
-            if (c > 0 && !(ok = wait_bar(&bars->o_free, (c - 1) & 1, abort_flag))) break;
-            tc_fence_after();
-            {  // O1^T = S^T Q^T
-                const uint32_t idesc = idesc_bf16_f32(128, 64, 0, 0);
+            {  // [U1 | U2] = V^T [T''_hi; T''_lo]^T while the state warpgroup forms -X.  It
+               // overwrites the S^T operand columns, which the products above (issued
+               // earlier, executed in order) have already read.
+                const uint32_t idesc = idesc_bf16_f32(128, 128, 1, 0);
+                const uint32_t v_s = kq_s + OFF_V;
 #pragma unroll 1
-                for (int part = 0; part < 2; ++part)
-#pragma unroll 1
-                    for (int ks = 0; ks < 8; ++ks) {
-                        const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32 + 8192;
-                        mma_bf16_ts(tmem + TM_O, tmem + TM_SA + part * 64 + ks * 8, smem_desc(kq_s + off, 16, 1024),
-                                    idesc, (part | ks) != 0);
-                    }
+                for (int ks = 0; ks < 4; ks = opaque(ks + 1))
+                    mma_bf16(tmem + TM_SA, smem_desc(v_s + ks * 2048, 8192, 1024), smem_desc(tp + ks * 32, 16, 1024),
+                             idesc, ks > 0);
             }
             if (!(ok = wait_bar(&bars->r_ready, c & 1, abort_flag))) break;
             tc_fence_after();
-            {  // u^T = D^T T''^T
-                const uint32_t idesc = idesc_bf16_f32(128, 64, 0, 0);
-                const uint32_t tp = s_sm + OFF_TP + buf * 16384;
+            {  // u^T = [U1 | U2] + (-X)_hi^T [T''_hi; T''_lo]^T + (-X)_lo^T T''_hi^T  (u = U1 + U2)
+                const uint32_t idesc2 = idesc_bf16_f32(128, 128, 0, 0), idesc1 = idesc_bf16_f32(128, 64, 0, 0);
 #pragma unroll 1
-                for (int part = 0; part < 3; ++part) {
-                    const uint32_t a_col = TM_X + (part == 2 ? 32 : 0);
-                    const uint32_t b_s = tp + (part == 1 ? 8192 : 0);
+                for (int ks = 0; ks < 4; ks = opaque(ks + 1))
+                    mma_bf16_ts(tmem + TM_SA, tmem + TM_X + ks * 8, smem_desc(tp + ks * 32, 16, 1024), idesc2, 1);
 #pragma unroll 1
-                    for (int ks = 0; ks < 4; ++ks)
-                        mma_bf16_ts(tmem + TM_U, tmem + a_col + ks * 8, smem_desc(b_s + ks * 32, 16, 1024), idesc,
-                                    (part | ks) != 0);
-                }
+                for (int ks = 0; ks < 4; ks = opaque(ks + 1))
+                    mma_bf16_ts(tmem + TM_SA, tmem + TM_X + 32 + ks * 8, smem_desc(tp + ks * 32, 16, 1024), idesc1, 1);
                 mma_commit(&bars->u_done);
             }
+            // the Gram products two chunks ahead execute while the state warpgroup forms u
+            issue_grams(c + 2);
+            if (!ok) break;
             if (!(ok = wait_bar(&bars->u_ready, c & 1, abort_flag))) break;
             tc_fence_after();
             {  // S^T += u^T K  (the chain), then O^T += u^T P^T
                 const uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 1);
 #pragma unroll 1
-                for (int part = 0; part < 2; ++part)
+                for (int part = 0; part < 2; part = opaque(part + 1))
 #pragma unroll 1
-                    for (int ks = 0; ks < 4; ++ks)
-                        mma_bf16_ts(tmem + TM_S, tmem + TM_U + part * 32 + ks * 8,
+                    for (int ks = 0; ks < 4; ks = opaque(ks + 1))
+                        mma_bf16_ts(tmem + TM_S, tmem + TM_X + part * 32 + ks * 8,
                                     smem_desc(kq_s + ks * 2048, 16384, 1024), idesc_s, 1);
                 mma_commit(&bars->s_done);
-                mma_commit(&bars->s_free[c & 1]);
-                const uint32_t idesc_o = idesc_bf16_f32(128, 64, 0, 0);
-                const uint32_t pb = s_sm + OFF_P + buf * 16384;
+                mma_commit(&bars->s_free[c % NSTAGE]);
+                // [O^T | O_b^T] += u_hi^T [P_hi; P_lo]^T (N = 128), then O^T += u_lo^T P_hi^T
+                const uint32_t idesc_o2 = idesc_bf16_f32(128, 128, 0, 0), idesc_o1 = idesc_bf16_f32(128, 64, 0, 0);
 #pragma unroll 1
-                for (int part = 0; part < 3; ++part) {
-                    const uint32_t a_col = TM_U + (part == 2 ? 32 : 0);
-                    const uint32_t b_s = pb + (part == 1 ? 8192 : 0);
+                for (int ks = 0; ks < 4; ks = opaque(ks + 1))
+                    mma_bf16_ts(tmem + TM_O, tmem + TM_X + ks * 8, smem_desc(pb + ks * 32, 16, 1024), idesc_o2, 1);
 #pragma unroll 1
-                    for (int ks = 0; ks < 4; ++ks)
-                        mma_bf16_ts(tmem + TM_O, tmem + a_col + ks * 8, smem_desc(b_s + ks * 32, 16, 1024), idesc_o, 1);
-                }
+                for (int ks = 0; ks < 4; ks = opaque(ks + 1))
+                    mma_bf16_ts(tmem + TM_O, tmem + TM_X + 32 + ks * 8, smem_desc(pb + ks * 32, 16, 1024), idesc_o1, 1);
                 mma_commit(&bars->o_done);
                 mma_commit(&bars->chunk_done[c & 1]);
             }
