@@ -317,6 +317,9 @@ def run_ours(args, world, rank, local):
                 "us_per_call": 1e6 * t_pr, "GB/s": pr_bytes / t_pr / 1e9, "bytes_per_call": pr_bytes,
                 "frac_hbm": pr_bytes / t_pr / 1e9 / peaks["hbm_gbs"]}
 
+    # ---- multi-token decode: 16 tokens per sequence appended to the B256 H32 state
+    dt_fig = decode_tokens_figure(efla, dev, stream, args.steps, flush, peaks)
+
     # ---- CPU baseline: the oracle on a bounded sample of the same workload
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -350,6 +353,7 @@ def run_ours(args, world, rank, local):
             "decode": dec,
             "deltanet": deltanet,
             "prep": prep_fig,
+            "decode_tokens": dt_fig,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
@@ -411,6 +415,24 @@ def decode_figures(efla, dev, stream):
                         "chained steps (inputs cycled from 8 seeded steps); S (512 MiB) exceeds L2",
             "us_per_step": 1e6 * t, "GB/s": nbytes / t / 1e9, "bytes_per_step": nbytes,
             "frac_hbm": nbytes / t / 1e9 / peaks["hbm_gbs"], "gpu_launches": reps * n_graph}
+
+
+def decode_tokens_figure(efla, dev, stream, steps, flush, peaks, m=16):
+    import workloads
+    cfg = workloads.DECODE
+    S = workloads.make_decode_state(cfg).to(dev)
+    inp = workloads.make_decode_tokens(m, cfg)
+    g = [inp[x].to(dev) for x in ("q", "k", "v", "beta")]
+    import torch
+    o = torch.empty((cfg.B, m, cfg.H, cfg.dv), dtype=torch.float32, device=dev)
+    t = time_steps(lambda: efla.decode_tokens(*g, S, o=o, stream=stream), steps, flush, stream)
+    u = cfg.B * cfg.H
+    nbytes = u * (m * ((2 * cfg.dk + cfg.dv) * 2 + 4 + cfg.dv * 4) + 2 * cfg.dk * cfg.dv * 4)
+    return {"workload": f"decode_tokens: B=256 H=32 d=128, {m} tokens per sequence per call, bf16 q,k,v, "
+                        f"fp32 S in place (read and written once), o fp32",
+            "us_per_call": 1e6 * t, "tokens_per_s": cfg.B * m / t, "GB/s": nbytes / t / 1e9,
+            "bytes_per_call": nbytes, "frac_hbm": nbytes / t / 1e9 / peaks["hbm_gbs"],
+            "gpu_launches": steps}
 
 
 def cpu_baseline(inp):

@@ -7,6 +7,7 @@ works but every call raises ``RuntimeError`` -- there is no fallback path.
 
     o, S_T = fwd_chunked(q, k, v, beta, S0=None, cu_seqlens=None)
     o      = decode_step(q, k, v, beta, S)        # S updated in place
+    o      = decode_tokens(q, k, v, beta, S)      # m tokens per sequence, S in place
 
 Semantics (per head): lambda = ||k||^2, alpha = (1 - e^{-beta*lambda})/lambda,
 S <- (I - alpha k k^T) S + alpha k v^T, o = S^T q with the updated S.
@@ -22,7 +23,7 @@ from typing import Optional, Tuple
 
 import torch
 
-__all__ = ["EflaError", "lib_path", "load", "fwd_chunked", "fwd_recurrent", "decode_step", "prep",
+__all__ = ["EflaError", "lib_path", "load", "fwd_chunked", "fwd_recurrent", "decode_step", "decode_tokens", "prep",
            "device_status", "abi_version", "STATUS", "UPDATES"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -66,6 +67,8 @@ def load():
         L.efla_fwd_recurrent_ex.argtypes = [vp] * 8 + [ip] * 9 + [vp]
         L.efla_decode_step_ex.restype = ip
         L.efla_decode_step_ex.argtypes = [vp] * 6 + [ip] * 7 + [vp]
+        L.efla_decode_tokens.restype = ip
+        L.efla_decode_tokens.argtypes = [vp] * 6 + [ip] * 8 + [vp]
         L.efla_prep.restype = ip
         L.efla_prep.argtypes = [vp] * 7 + [ctypes.c_longlong] + [ip] * 4 + [vp]
         L.efla_device_status.restype = ip
@@ -199,6 +202,36 @@ def decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.T
         raise EflaError(1, f"unknown update rule {update!r}")
     _check(L.efla_decode_step_ex(_p(q), _p(k), _p(v), _p(beta), _p(S), _p(o), B, H, dk, dv,
                                  _dt(q.dtype), _dt(o.dtype), UPDATES[update], _stream(stream)))
+    return o
+
+
+def decode_tokens(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor, S: torch.Tensor, *,
+                  o: Optional[torch.Tensor] = None, o_dtype: torch.dtype = torch.float32,
+                  stream=None, update: str = "exact") -> torch.Tensor:
+    """m tokens per sequence appended to the state; S [B,H,dk,dv] fp32 is updated in place.
+
+    q, k [B,m,H,dk], v [B,m,H,dv] (bf16 or fp32), beta [B,m,H] fp32.  Returns o [B,m,H,dv].
+    Equal to m successive ``decode_step`` calls (``efla_decode_tokens``).
+    """
+    L = load()
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (beta, "beta"), (S, "S"), (o, "o")):
+        _need(t, n)
+    if q.dim() != 4 or k.shape != q.shape or v.shape[:3] != q.shape[:3] or beta.shape != q.shape[:3]:
+        raise EflaError(1, "shape mismatch")
+    B, m, H, dk = q.shape
+    dv = v.shape[-1]
+    if S.dtype != torch.float32 or tuple(S.shape) != (B, H, dk, dv):
+        raise EflaError(1, f"S must be float32 [{B},{H},{dk},{dv}]")
+    if q.dtype != k.dtype or q.dtype != v.dtype or beta.dtype != torch.float32:
+        raise EflaError(1, "q, k, v must share a dtype and beta must be float32")
+    if o is None:
+        o = torch.empty((B, m, H, dv), dtype=o_dtype, device=q.device)
+    elif tuple(o.shape) != (B, m, H, dv):
+        raise EflaError(1, "o has the wrong shape")
+    if update not in UPDATES:
+        raise EflaError(1, f"unknown update rule {update!r}")
+    _check(L.efla_decode_tokens(_p(q), _p(k), _p(v), _p(beta), _p(S), _p(o), B, m, H, dk, dv,
+                                _dt(q.dtype), _dt(o.dtype), UPDATES[update], _stream(stream)))
     return o
 
 

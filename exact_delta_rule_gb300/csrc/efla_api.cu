@@ -203,6 +203,41 @@ efla_status efla_decode_step(const void *q, const void *k, const void *v, const 
     return efla_decode_step_ex(q, k, v, beta, S, o, B, H, d_k, d_v, in_dtype, o_dtype, EFLA_UPDATE_EXACT, stream);
 }
 
+efla_status efla_decode_tokens(const void *q, const void *k, const void *v, const float *beta, float *S, void *o,
+                               int B, int m, int H, int d_k, int d_v, efla_dtype in_dtype, efla_dtype o_dtype,
+                               efla_update update, efla_stream_t stream) {
+    if (!update_ok(update)) return fail(EFLA_ERR_INVALID_ARG, "unknown update rule %d", (int)update);
+    if (B < 0 || m < 0 || H <= 0) return fail(EFLA_ERR_INVALID_ARG, "bad sizes B=%d m=%d H=%d", B, m, H);
+    efla_status s = check_dims_common(d_k, d_v, in_dtype, o_dtype);
+    if (s != EFLA_OK) return s;
+    if ((long long)B * H > (1LL << 31) - 1 || (long long)B * m * H > (1LL << 40))
+        return fail(EFLA_ERR_UNSUPPORTED, "B*H or B*m*H too large");
+    if (B > 0 && !S) return fail(EFLA_ERR_INVALID_ARG, "S must be non-NULL when B > 0");
+    if (B > 0 && m > 0 && (!q || !k || !v || !beta || !o))
+        return fail(EFLA_ERR_INVALID_ARG, "q, k, v, beta and o must be non-NULL when B*m > 0");
+    const void *ptrs[] = {q, k, v, beta, S, o};
+    const char *names[] = {"q", "k", "v", "beta", "S", "o"};
+    for (int i = 0; i < 6; ++i)
+        if (ptrs[i] && !aligned16(ptrs[i]))
+            return fail(EFLA_ERR_INVALID_ARG, "%s=%p is not 16-byte aligned", names[i], ptrs[i]);
+    const size_t u = (size_t)B * H, rows = (size_t)B * m * H;
+    auto rng = [](const void *p, size_t n) {
+        return Range{"", reinterpret_cast<uintptr_t>(p), p ? reinterpret_cast<uintptr_t>(p) + n : 0};
+    };
+    const Range rS = rng(S, u * d_k * d_v * 4), ro = rng(o, rows * d_v * dsize(o_dtype));
+    const Range ins[] = {rng(q, rows * d_k * dsize(in_dtype)), rng(k, rows * d_k * dsize(in_dtype)),
+                         rng(v, rows * d_v * dsize(in_dtype)), rng(beta, rows * 4)};
+    for (const Range &r : ins)
+        if (overlap(rS, r) || overlap(ro, r)) return fail(EFLA_ERR_INVALID_ARG, "an output overlaps an input");
+    if (overlap(rS, ro)) return fail(EFLA_ERR_INVALID_ARG, "o overlaps S");
+    DecodeArgs a{q, k, v, beta, S, o, B, H, d_k, d_v, in_dtype, o_dtype, reinterpret_cast<cudaStream_t>(stream),
+                 (int)update, m};
+    cudaError_t e = launch_decode_tokens(a);
+    if (e != cudaSuccess) return cuda_fail(e, "decode-tokens kernel launch");
+    g_last_error.clear();
+    return EFLA_OK;
+}
+
 efla_status efla_prep(const void *k, const void *v, const float *beta, float *lam, float *alpha, void *ak, void *av,
                       long long n, int d_k, int d_v, efla_dtype dtype, efla_update update, efla_stream_t stream) {
     if (!update_ok(update)) return fail(EFLA_ERR_INVALID_ARG, "unknown update rule %d", (int)update);

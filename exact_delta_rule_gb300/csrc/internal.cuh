@@ -38,6 +38,7 @@ struct DecodeArgs {
     efla_dtype in_dtype, o_dtype;
     cudaStream_t stream;
     int euler;
+    int m = 1;  // tokens per sequence (multi-token decode)
 };
 
 struct PrepArgs {
@@ -55,6 +56,7 @@ struct PrepArgs {
 // Launchers return a cudaError_t from the launch (cudaSuccess if nothing launched).
 cudaError_t launch_recurrent(const FwdArgs &a);
 cudaError_t launch_decode(const DecodeArgs &a);
+cudaError_t launch_decode_tokens(const DecodeArgs &a);
 cudaError_t launch_prep(const PrepArgs &a);
 // tcgen05 chunk kernel: bf16 inputs, d_k = d_v = 128, chunk 64.
 cudaError_t launch_chunk_tc(const FwdArgs &a, const char **why);

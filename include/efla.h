@@ -44,7 +44,7 @@
 extern "C" {
 #endif
 
-#define EFLA_ABI_VERSION 2
+#define EFLA_ABI_VERSION 3
 
 typedef enum {
     EFLA_OK = 0,
@@ -137,6 +137,28 @@ efla_status efla_fwd_recurrent(const void *q, const void *k, const void *v, cons
 efla_status efla_decode_step(const void *q, const void *k, const void *v, const float *beta,
                              float *S, void *o, int B, int H, int d_k, int d_v,
                              efla_dtype in_dtype, efla_dtype o_dtype, efla_stream_t stream);
+
+/*
+ * efla_decode_tokens -- m tokens per sequence appended to a resident state,
+ * S updated IN PLACE (multi-token decode, prefill continuation).
+ *
+ * Defined by: m applications, in token order, of the update rule and read-out
+ * above ("Exact Flow Linear Attention" (gist.science), Metodologia 3;
+ * "Error-Free Linear Attention is a Free Lunch" (howistudyai), Steps 1-3 and
+ * "Putting it all together (pipeline)"); equal to m successive
+ * efla_decode_step calls, with S read and written once.
+ *
+ *   q, k  [B, m, H, d_k] in_dtype;  v [B, m, H, d_v] in_dtype;  beta [B, m, H] fp32
+ *   S     [B, H, d_k, d_v] fp32, read and overwritten with the state after token m
+ *   o     [B, m, H, d_v] o_dtype
+ *   update  EFLA_UPDATE_EXACT or EFLA_UPDATE_EULER
+ * m = 0 or B = 0 is valid and changes nothing.  Supported: d_k, d_v in {32, 64, 128}.
+ * S must not overlap any input or o; o must not overlap any input.
+ */
+efla_status efla_decode_tokens(const void *q, const void *k, const void *v, const float *beta,
+                               float *S, void *o, int B, int m, int H, int d_k, int d_v,
+                               efla_dtype in_dtype, efla_dtype o_dtype, efla_update update,
+                               efla_stream_t stream);
 
 /*
  * The three calls above with an explicit update rule (efla_update); the

@@ -176,3 +176,29 @@ def _prep(lib, **kw):
 def test_prep_rejects(lib, kw, code):
     assert _prep(lib, **kw) == code
     assert _last(lib)
+
+
+def _dect(lib, **kw):
+    a = dict(q=Q, k=K, v=V, beta=BETA, S=S0, o=O, B=4, m=3, H=2, dk=128, dv=128, ind=0, od=1, upd=0)
+    a.update(kw)
+    vp, ip = ctypes.c_void_p, ctypes.c_int
+    f = lib.efla_decode_tokens
+    f.restype = ip
+    f.argtypes = [vp] * 6 + [ip] * 8 + [vp]
+    return f(a["q"], a["k"], a["v"], a["beta"], a["S"], a["o"], a["B"], a["m"], a["H"], a["dk"], a["dv"], a["ind"],
+             a["od"], a["upd"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(m=-1), INVALID), (dict(B=-1), INVALID), (dict(H=0), INVALID), (dict(dk=48), UNSUPPORTED),
+    (dict(S=None), INVALID), (dict(q=None), INVALID), (dict(S=S0 + 8), INVALID), (dict(o=Q + 256), INVALID),
+    (dict(S=O + 64), INVALID), (dict(upd=5), INVALID), (dict(od=3), INVALID),
+])
+def test_decode_tokens_rejects(lib, kw, code):
+    assert _dect(lib, **kw) == code
+    assert _last(lib)
+
+
+def test_decode_tokens_empty_is_ok_without_gpu_work(lib):
+    # m == 0 launches nothing: only S is needed
+    assert _dect(lib, m=0, q=None, k=None, v=None, beta=None, o=None) == 0

@@ -181,3 +181,19 @@ def make_decode_step(step: int, cfg: DecodeWorkload = DECODE, *, B: Optional[int
     beta = torch.sigmoid(torch.randn((B, H), generator=g))
     return {"q": q.to(torch.bfloat16).contiguous(), "k": k.to(torch.bfloat16).contiguous(),
             "v": v.to(torch.bfloat16).contiguous(), "beta": beta.float().contiguous()}
+
+
+def make_decode_tokens(m: int, cfg: DecodeWorkload = DECODE, *, first_step: int = 0, B: Optional[int] = None,
+                       H: Optional[int] = None) -> dict:
+    """Inputs of m consecutive decode steps stacked along a token axis: q, k [B, m, H, d_k],
+    v [B, m, H, d_v] (bf16), beta [B, m, H] (fp32) -- token t is decode step first_step + t."""
+    B_ = cfg.B if B is None else B
+    H_ = cfg.H if H is None else H
+    if m == 0:
+        e = lambda d: torch.empty((B_, 0, H_, d), dtype=torch.bfloat16)
+        return {"q": e(cfg.dk), "k": e(cfg.dk), "v": e(cfg.dv), "beta": torch.empty((B_, 0, H_))}
+    steps = [make_decode_step(first_step + t, cfg, B=B, H=H) for t in range(m)]
+    out = {}
+    for x in ("q", "k", "v", "beta"):
+        out[x] = torch.stack([s[x] for s in steps], dim=1).contiguous()
+    return out
