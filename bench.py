@@ -320,6 +320,9 @@ def run_ours(args, world, rank, local):
     # ---- multi-token decode: 16 tokens per sequence appended to the B256 H32 state
     dt_fig = decode_tokens_figure(efla, dev, stream, args.steps, flush, peaks)
 
+    # ---- the stiff/long configuration: one sequence per head, unsplit and split along time
+    stiff_fig = stiff_figure(efla, dev, stream, max(3, args.steps // 2), flush, peaks)
+
     # ---- CPU baseline: the oracle on a bounded sample of the same workload
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -354,6 +357,7 @@ def run_ours(args, world, rank, local):
             "deltanet": deltanet,
             "prep": prep_fig,
             "decode_tokens": dt_fig,
+            "stiff": stiff_fig,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
@@ -415,6 +419,32 @@ def decode_figures(efla, dev, stream):
                         "chained steps (inputs cycled from 8 seeded steps); S (512 MiB) exceeds L2",
             "us_per_step": 1e6 * t, "GB/s": nbytes / t / 1e9, "bytes_per_step": nbytes,
             "frac_hbm": nbytes / t / 1e9 / peaks["hbm_gbs"], "gpu_launches": reps * n_graph}
+
+
+def stiff_figure(efla, dev, stream, steps, flush, peaks):
+    import torch
+
+    import workloads
+    cfg = workloads.FWD_WORKLOADS["stiff"]
+    inp = workloads.make_fwd_inputs(cfg)
+    g = {x: inp[x].to(dev) for x in ("q", "k", "v", "beta", "S0")}
+    B, T, H, dk, dv = cfg.B, cfg.T, cfg.H, cfg.dk, cfg.dv
+    o = torch.empty((B, T, H, dv), dtype=torch.float32, device=dev)
+    S_T = torch.empty((B, H, dk, dv), dtype=torch.float32, device=dev)
+    need, G = efla.scan_workspace(B, T, H, dk, dv, 0)
+    ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    t_plain = time_steps(lambda: efla.fwd_chunked(g["q"], g["k"], g["v"], g["beta"], g["S0"], o=o, S_T=S_T,
+                                                  stream=stream), steps, flush, stream)
+    t_scan = time_steps(lambda: efla.fwd_chunked_scan(g["q"], g["k"], g["v"], g["beta"], g["S0"], o=o, S_T=S_T,
+                                                      workspace=ws, stream=stream), steps, flush, stream)
+    tokens = B * T
+    nbytes = fwd_bytes(B, T, H, dk, dv, B, s0=True)
+    return {"workload": "stiff: B=1 H=16 T=65536 d=128 bf16, key norms U[0.1,10], beta=sigmoid(N(2,1)), "
+                        "S0~0.1 N(0,1), o fp32, S_T fp32",
+            "ms_unsplit": 1e3 * t_plain, "tokens_per_s_unsplit": tokens / t_plain,
+            "ms_split": 1e3 * t_scan, "tokens_per_s_split": tokens / t_scan, "segments": G,
+            "speedup": t_plain / t_scan, "frac_hbm_split": nbytes / t_scan / 1e9 / peaks["hbm_gbs"],
+            "gpu_launches": 3 * steps + steps}
 
 
 def decode_tokens_figure(efla, dev, stream, steps, flush, peaks, m=16):

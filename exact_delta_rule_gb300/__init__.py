@@ -23,7 +23,8 @@ from typing import Optional, Tuple
 
 import torch
 
-__all__ = ["EflaError", "lib_path", "load", "fwd_chunked", "fwd_recurrent", "decode_step", "decode_tokens", "prep",
+__all__ = ["EflaError", "lib_path", "load", "fwd_chunked", "fwd_chunked_scan", "scan_workspace", "fwd_recurrent",
+           "decode_step", "decode_tokens", "prep",
            "device_status", "abi_version", "STATUS", "UPDATES"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -67,6 +68,10 @@ def load():
         L.efla_fwd_recurrent_ex.argtypes = [vp] * 8 + [ip] * 9 + [vp]
         L.efla_decode_step_ex.restype = ip
         L.efla_decode_step_ex.argtypes = [vp] * 6 + [ip] * 7 + [vp]
+        L.efla_fwd_chunked_scan.restype = ip
+        L.efla_fwd_chunked_scan.argtypes = [vp] * 7 + [ip] * 8 + [vp, ctypes.c_size_t, ip, vp]
+        L.efla_fwd_scan_workspace.restype = ip
+        L.efla_fwd_scan_workspace.argtypes = [ip] * 6 + [ctypes.POINTER(ctypes.c_size_t), ctypes.POINTER(ip)]
         L.efla_decode_tokens.restype = ip
         L.efla_decode_tokens.argtypes = [vp] * 6 + [ip] * 8 + [vp]
         L.efla_prep.restype = ip
@@ -172,6 +177,49 @@ def fwd_chunked(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.T
     the delta-rule (DeltaNet) gate alpha = beta through the same kernels.
     """
     return _fwd("chunked", q, k, v, beta, S0, cu_seqlens, o, S_T, o_dtype, chunk, stream, return_state, update)
+
+
+def scan_workspace(B: int, T: int, H: int, dk: int = 128, dv: int = 128, segments: int = 0) -> Tuple[int, int]:
+    """(workspace bytes, pieces per sequence) of ``fwd_chunked_scan`` (``efla_fwd_scan_workspace``)."""
+    L = load()
+    nb, g = ctypes.c_size_t(0), ctypes.c_int(0)
+    _check(L.efla_fwd_scan_workspace(B, T, H, dk, dv, int(segments), ctypes.byref(nb), ctypes.byref(g)))
+    return nb.value, g.value
+
+
+def fwd_chunked_scan(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor,
+                     S0: Optional[torch.Tensor] = None, *, segments: int = 0,
+                     workspace: Optional[torch.Tensor] = None, o: Optional[torch.Tensor] = None,
+                     S_T: Optional[torch.Tensor] = None, o_dtype: torch.dtype = torch.float32, stream=None,
+                     return_state: bool = True, update: str = "exact") -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """``fwd_chunked`` with each sequence split along time into ``segments`` pieces
+    (``efla_fwd_chunked_scan``): for few long sequences.  ``workspace`` (a CUDA tensor of at
+    least ``scan_workspace(...)[0]`` bytes) is allocated here when not given."""
+    L = load()
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (beta, "beta"), (S0, "S0"), (o, "o"), (workspace, "workspace")):
+        _need(t, n)
+    if q.dim() != 4 or k.shape != q.shape or v.shape[:3] != q.shape[:3] or beta.shape != q.shape[:3]:
+        raise EflaError(1, "shape mismatch")
+    if q.dtype != k.dtype or q.dtype != v.dtype or beta.dtype != torch.float32:
+        raise EflaError(1, "q, k, v must share a dtype and beta must be float32")
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if S0 is not None and (S0.dtype != torch.float32 or tuple(S0.shape) != (B, H, dk, dv)):
+        raise EflaError(1, f"S0 must be float32 [{B},{H},{dk},{dv}]")
+    if o is None:
+        o = torch.empty((B, T, H, dv), dtype=o_dtype, device=q.device)
+    if S_T is None and return_state:
+        S_T = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
+    if update not in UPDATES:
+        raise EflaError(1, f"unknown update rule {update!r}")
+    need, _ = scan_workspace(B, T, H, dk, dv, segments)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(L.efla_fwd_chunked_scan(_p(q), _p(k), _p(v), _p(beta), _p(S0), _p(o), _p(S_T), B, T, H, dk, dv,
+                                   _dt(q.dtype), _dt(o.dtype), int(segments), _p(workspace), nbytes,
+                                   UPDATES[update], _stream(stream)))
+    return o, S_T
 
 
 def fwd_recurrent(q, k, v, beta, S0=None, cu_seqlens=None, *, o=None, S_T=None,

@@ -115,6 +115,13 @@ struct TcParams {
     int *status;
     int B, T, H, N;
     int euler;  // 1: delta-rule gate (gamma = beta * lambda)
+    // Sequences split into segments (seg_len > 0; rows of [B, T] only, no cu_seqlens):
+    //   map launch (maps != nullptr): CTAs (pass, b, g < G-1, h); pass 0 runs segment g from
+    //     S = I with v = 0, pass 1 from S = 0; neither writes o; S_T goes to maps[pass][b][g][h].
+    //   output launch: CTAs (b, g, h) start from s_in[b][g][h]; only g = G-1 writes S_T[b][h].
+    int seg_len, G;
+    const float *s_in;
+    float *maps;
 };
 
 struct Bars {
@@ -336,28 +343,58 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + OFF_MISC + 4);
 
     const int tid = threadIdx.x, warp = tid >> 5;
-    const int n = blockIdx.x / p.H, h = blockIdx.x % p.H;
     long b, bos, eos;
-    if (p.cu_seqlens) {
-        b = 0;
-        bos = p.cu_seqlens[n];
-        eos = p.cu_seqlens[n + 1];
-        if (bos < 0 || eos < bos || eos > p.T) {  // malformed bounds: flag and touch nothing
-            if (tid == 0) atomicExch(p.status, (int)EFLA_ERR_INVALID_ARG);
-            return;
+    int h;
+    int mode = 0;                    // 0: forward; 1: map from S = I, v = 0; 2: map from S = 0
+    const float *s0p = nullptr;      // this CTA's start state (nullptr: zero)
+    float *stp = nullptr;            // where this CTA's final state goes (nullptr: nowhere)
+    if (p.seg_len > 0) {  // a segment of a split sequence
+        int idx = blockIdx.x;
+        const int Gu = p.maps ? p.G - 1 : p.G;
+        if (p.maps) {
+            const int per_pass = p.B * Gu * p.H;
+            mode = 1 + idx / per_pass;
+            idx %= per_pass;
+        }
+        h = idx % p.H;
+        idx /= p.H;
+        const int g = idx % Gu;
+        b = idx / Gu;
+        bos = (long)g * p.seg_len;
+        eos = min((long)p.T, bos + p.seg_len);
+        if (mode == 0) {
+            s0p = p.s_in + (((size_t)b * p.G + g) * p.H + h) * D * D;
+            if (g == p.G - 1 && p.S_T) stp = p.S_T + ((size_t)b * p.H + h) * D * D;
+        } else {
+            stp = p.maps + ((((size_t)(mode - 1) * p.B + b) * Gu + g) * p.H + h) * D * D;
         }
     } else {
-        b = n;
-        bos = 0;
-        eos = p.T;
+        const int n = blockIdx.x / p.H;
+        h = blockIdx.x % p.H;
+        if (p.cu_seqlens) {
+            b = 0;
+            bos = p.cu_seqlens[n];
+            eos = p.cu_seqlens[n + 1];
+            if (bos < 0 || eos < bos || eos > p.T) {  // malformed bounds: flag and touch nothing
+                if (tid == 0) atomicExch(p.status, (int)EFLA_ERR_INVALID_ARG);
+                return;
+            }
+        } else {
+            b = n;
+            bos = 0;
+            eos = p.T;
+        }
+        const size_t sbase = ((size_t)n * p.H + h) * D * D;
+        if (p.S0) s0p = p.S0 + sbase;
+        if (p.S_T) stp = p.S_T + sbase;
     }
+    const bool write_o = mode == 0;
     const int nchunks = eos > bos ? (int)((eos - bos + C - 1) / C) : 0;
-    const size_t sbase = ((size_t)n * p.H + h) * D * D;
 
     if (nchunks == 0) {  // empty sequence: S_T = S0
-        if (p.S_T && tid < D)
+        if (stp && tid < D)
             for (int i = 0; i < D; ++i)
-                p.S_T[sbase + (size_t)i * D + tid] = p.S0 ? p.S0[sbase + (size_t)i * D + tid] : 0.f;
+                stp[(size_t)i * D + tid] = mode == 1 ? (i == tid ? 1.f : 0.f) : s0p ? s0p[(size_t)i * D + tid] : 0.f;
         return;
     }
 
@@ -496,7 +533,7 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
                         w.w = col0 + s4 + 3 < t ? rs * iv[s4 + 3] * g[s4 + 3] : 0.f;
                         *reinterpret_cast<float4 *>(At + t * AT_LD + col0 + s4) = w;
                     }
-                } else {  // P[t][col0 .. col0+31] = Q K^T with the inclusive causal mask
+                } else if (write_o) {  // P[t][col0 .. col0+31] = Q K^T with the inclusive causal mask
                     const int t = row - C;
 #pragma unroll
                     for (int s = 0; s < 32; ++s) g[s] = col0 + s <= t ? g[s] : 0.f;
@@ -562,7 +599,8 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
 #pragma unroll 1
             for (int g = 0; g < 4; g = opaque(g + 1)) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) r[i] = p.S0 ? p.S0[sbase + (size_t)(g * 32 + i) * D + j] : 0.f;
+                for (int i = 0; i < 32; ++i)
+                    r[i] = mode == 1 ? (g * 32 + i == j ? 1.f : 0.f) : s0p ? s0p[(size_t)(g * 32 + i) * D + j] : 0.f;
                 tmem_st32(lane_base + TM_S + g * 32, r);
             }
             tmem_st_wait();
@@ -584,6 +622,12 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
         };
         clear_ob();
         auto epilogue = [&](int cc) {
+            if (!write_o) {  // map modes: nothing to store; release O^T and the staging buffer
+                tc_fence_before();
+                mbar_arrive(&bars->o_free);
+                if (lane == 0) mbar_arrive(&bars->ost_free[cc & 1]);
+                return;
+            }
             const long t0c = bos + (long)cc * C;
             const int vc = (int)min((long)C, eos - t0c);
             float ov[32], ow[32];
@@ -722,13 +766,13 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
             mbar_arrive(&bars->u_ready);
         }
         if (!ok) *abort_flag = 1;
-        if (ok && p.S_T) {  // final state (every product has completed: o_done of the last chunk)
+        if (ok && stp) {  // final state (every product has completed: o_done of the last chunk)
 #pragma unroll 1
             for (int g = 0; g < 4; g = opaque(g + 1)) {
                 float s32[32];
                 tmem_ld32(lane_base + TM_S + g * 32, s32);
                 tmem_ld_wait();
-                float *dst = p.S_T + sbase + (size_t)(g * 32) * D + j;
+                float *dst = stp + (size_t)(g * 32) * D + j;
 #pragma unroll
                 for (int i = 0; i < 32; ++i) dst[(size_t)i * D] = s32[i];
             }
@@ -806,10 +850,12 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
                // earlier, executed in order) have already read.
                 const uint32_t idesc = idesc_bf16_f32(128, 128, 1, 0);
                 const uint32_t v_s = kq_s + OFF_V;
+                if (mode != 1) {  // (the map from S = I takes v = 0)
 #pragma unroll 1
-                for (int ks = 0; ks < 4; ks = opaque(ks + 1))
-                    mma_bf16(tmem + TM_SA, smem_desc(v_s + ks * 2048, 8192, 1024), smem_desc(tp + ks * 32, 16, 1024),
-                             idesc, ks > 0);
+                    for (int ks = 0; ks < 4; ks = opaque(ks + 1))
+                        mma_bf16(tmem + TM_SA, smem_desc(v_s + ks * 2048, 8192, 1024),
+                                 smem_desc(tp + ks * 32, 16, 1024), idesc, ks > 0);
+                }
             }
             if (!(ok = wait_bar(&bars->r_ready, c & 1, abort_flag))) break;
             tc_fence_after();
@@ -817,7 +863,8 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
                 const uint32_t idesc2 = idesc_bf16_f32(128, 128, 0, 0), idesc1 = idesc_bf16_f32(128, 64, 0, 0);
 #pragma unroll 1
                 for (int ks = 0; ks < 4; ks = opaque(ks + 1))
-                    mma_bf16_ts(tmem + TM_SA, tmem + TM_X + ks * 8, smem_desc(tp + ks * 32, 16, 1024), idesc2, 1);
+                    mma_bf16_ts(tmem + TM_SA, tmem + TM_X + ks * 8, smem_desc(tp + ks * 32, 16, 1024), idesc2,
+                                mode != 1 || ks > 0);
 #pragma unroll 1
                 for (int ks = 0; ks < 4; ks = opaque(ks + 1))
                     mma_bf16_ts(tmem + TM_SA, tmem + TM_X + 32 + ks * 8, smem_desc(tp + ks * 32, 16, 1024), idesc1, 1);
@@ -840,12 +887,15 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
                 mma_commit(&bars->s_free[c % NSTAGE]);
                 // [O^T | O_b^T] += u_hi^T [P_hi; P_lo]^T (N = 128), then O^T += u_lo^T P_hi^T
                 const uint32_t idesc_o2 = idesc_bf16_f32(128, 128, 0, 0), idesc_o1 = idesc_bf16_f32(128, 64, 0, 0);
+                if (write_o) {
 #pragma unroll 1
-                for (int ks = 0; ks < 4; ks = opaque(ks + 1))
-                    mma_bf16_ts(tmem + TM_O, tmem + TM_X + ks * 8, smem_desc(pb + ks * 32, 16, 1024), idesc_o2, 1);
+                    for (int ks = 0; ks < 4; ks = opaque(ks + 1))
+                        mma_bf16_ts(tmem + TM_O, tmem + TM_X + ks * 8, smem_desc(pb + ks * 32, 16, 1024), idesc_o2, 1);
 #pragma unroll 1
-                for (int ks = 0; ks < 4; ks = opaque(ks + 1))
-                    mma_bf16_ts(tmem + TM_O, tmem + TM_X + 32 + ks * 8, smem_desc(pb + ks * 32, 16, 1024), idesc_o1, 1);
+                    for (int ks = 0; ks < 4; ks = opaque(ks + 1))
+                        mma_bf16_ts(tmem + TM_O, tmem + TM_X + 32 + ks * 8, smem_desc(pb + ks * 32, 16, 1024),
+                                    idesc_o1, 1);
+                }
                 mma_commit(&bars->o_done);
                 mma_commit(&bars->chunk_done[c & 1]);
             }
@@ -920,7 +970,7 @@ cudaError_t launch_chunk_tc(const FwdArgs &a, const char **why) {
         if (!make_map(&p.map_q, a.q, a.B, a.T, a.H, false, 64, true) ||
             !make_map(&p.map_k, a.k, a.B, a.T, a.H, false, 64, true) ||
             !make_map(&p.map_v, a.v, a.B, a.T, a.H, false, 64, true) ||
-            !make_map(&p.map_o, a.o, a.B, a.T, a.H, !o_bf16, 32, false)) {
+            (a.o && !make_map(&p.map_o, a.o, a.B, a.T, a.H, !o_bf16, 32, false))) {
             *why = "cuTensorMapEncodeTiled failed";
             return cudaErrorInvalidValue;
         }
@@ -936,8 +986,13 @@ cudaError_t launch_chunk_tc(const FwdArgs &a, const char **why) {
     p.H = a.H;
     p.N = a.N;
     p.euler = a.euler;
+    p.seg_len = a.seg_len;
+    p.G = a.G;
+    p.s_in = a.s_in;
+    p.maps = a.maps;
     *why = "tcgen05 chunk kernel launch";
-    const unsigned grid = (unsigned)((long)a.N * a.H);
+    const long units = a.seg_len > 0 ? (a.maps ? 2L * a.B * (a.G - 1) * a.H : (long)a.B * a.G * a.H) : (long)a.N * a.H;
+    const unsigned grid = (unsigned)units;
     return o_bf16 ? launch_typed<true>(p, grid, a.stream) : launch_typed<false>(p, grid, a.stream);
 }
 

@@ -5,6 +5,8 @@
 
 #include <string>
 
+#include <algorithm>
+
 #include "internal.cuh"
 
 namespace efla {
@@ -144,6 +146,101 @@ efla_status efla_fwd_chunked(const void *q, const void *k, const void *v, const 
                              efla_stream_t stream) {
     return efla_fwd_chunked_ex(q, k, v, beta, S0, cu_seqlens, o, S_T, B, T, H, d_k, d_v, N, in_dtype, o_dtype,
                                chunk, EFLA_UPDATE_EXACT, stream);
+}
+
+// Segments of the split forward: G segments of seg_len tokens (a multiple of the chunk)
+// per sequence, every one non-empty.  segments <= 0 picks G = SMs / (B*H).
+static efla_status scan_plan(int B, int T, int H, int segments, int *G_out, int *seg_len) {
+    const int nch = (T + 63) / 64;
+    int G = segments;
+    if (G <= 0) {
+        int dev = 0, sms = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "querying the SM count");
+        G = sms / (B * H > 0 ? B * H : 1);
+    }
+    G = std::max(1, std::min(G, std::max(1, nch)));
+    const int cps = (nch + G - 1) / G;  // chunks per segment
+    *seg_len = std::max(1, cps) * 64;
+    *G_out = nch > 0 ? (nch + cps - 1) / cps : 1;
+    return EFLA_OK;
+}
+
+static size_t scan_bytes(int B, int H, int d_k, int d_v, int G) {
+    return G <= 1 ? 0 : (size_t)(3 * G - 2) * B * H * d_k * d_v * sizeof(float);
+}
+
+efla_status efla_fwd_scan_workspace(int B, int T, int H, int d_k, int d_v, int segments, size_t *bytes,
+                                    int *segments_used) {
+    if (!bytes) return fail(EFLA_ERR_INVALID_ARG, "bytes must be non-NULL");
+    if (B < 0 || T < 0 || H <= 0) return fail(EFLA_ERR_INVALID_ARG, "bad sizes B=%d T=%d H=%d", B, T, H);
+    int G = 1, seg = 64;
+    efla_status s = scan_plan(B, T, H, segments, &G, &seg);
+    if (s != EFLA_OK) return s;
+    *bytes = scan_bytes(B, H, d_k, d_v, G);
+    if (segments_used) *segments_used = G;
+    g_last_error.clear();
+    return EFLA_OK;
+}
+
+efla_status efla_fwd_chunked_scan(const void *q, const void *k, const void *v, const float *beta, const float *S0,
+                                  void *o, float *S_T, int B, int T, int H, int d_k, int d_v, efla_dtype in_dtype,
+                                  efla_dtype o_dtype, int segments, void *workspace, size_t workspace_bytes,
+                                  efla_update update, efla_stream_t stream) {
+    if (!update_ok(update)) return fail(EFLA_ERR_INVALID_ARG, "unknown update rule %d", (int)update);
+    FwdArgs a{q, k, v, beta, S0, nullptr, o, S_T, B, T, H, d_k, d_v, B, in_dtype, o_dtype, 64,
+              reinterpret_cast<cudaStream_t>(stream), nullptr, (int)update};
+    efla_status s = validate_fwd(a, true);
+    if (s != EFLA_OK) return s;
+    const bool tc = in_dtype == EFLA_BF16 && d_k == 128 && d_v == 128;
+    int G = 1, seg = 64;
+    if (tc && (long long)B * T > 0) {
+        s = scan_plan(B, T, H, segments, &G, &seg);
+        if (s != EFLA_OK) return s;
+    }
+    if (G <= 1) return run_fwd(a, true);  // one segment (or a CUDA-core shape): the plain forward
+    const size_t need = scan_bytes(B, H, d_k, d_v, G);
+    if (!workspace || workspace_bytes < need)
+        return fail(EFLA_ERR_INVALID_ARG, "workspace of %zu bytes needed (%zu given)", need,
+                    workspace ? workspace_bytes : (size_t)0);
+    if (!aligned16(workspace)) return fail(EFLA_ERR_INVALID_ARG, "workspace=%p is not 16-byte aligned", workspace);
+    const uintptr_t w0 = reinterpret_cast<uintptr_t>(workspace);
+    const Range ws{"workspace", w0, w0 + need};
+    const size_t th = (size_t)B * T * H, st = (size_t)B * H * d_k * d_v * 4;
+    auto R = [](const char *n, const void *p, size_t bytes) {
+        uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+        return Range{n, lo, p ? lo + bytes : lo};
+    };
+    const Range others[] = {R("q", q, th * d_k * dsize(in_dtype)), R("k", k, th * d_k * dsize(in_dtype)),
+                            R("v", v, th * d_v * dsize(in_dtype)), R("beta", beta, th * 4), R("S0", S0, st),
+                            R("o", o, th * d_v * dsize(o_dtype)), R("S_T", S_T, st)};
+    for (const Range &r : others)
+        if (overlap(ws, r)) return fail(EFLA_ERR_INVALID_ARG, "workspace overlaps %s", r.name);
+    a.status = device_status_ptr();
+    if (!a.status) return fail(EFLA_ERR_CUDA, "cannot resolve the device status word");
+    float *s_in = static_cast<float *>(workspace);
+    float *maps = s_in + (size_t)G * B * H * d_k * d_v;
+    const char *why = nullptr;
+    FwdArgs m = a;  // pass 1: the maps of segments 0..G-2 (no outputs)
+    m.o = nullptr;
+    m.S_T = nullptr;
+    m.S0 = nullptr;
+    m.seg_len = seg;
+    m.G = G;
+    m.maps = maps;
+    cudaError_t e = launch_chunk_tc(m, &why);
+    if (e != cudaSuccess) return cuda_fail(e, why ? why : "segment-map launch");
+    e = launch_scan_combine(S0, maps, s_in, B, G, H, a.stream);
+    if (e != cudaSuccess) return cuda_fail(e, "segment scan launch");
+    FwdArgs f = a;  // pass 2: every segment from its start state, with outputs
+    f.seg_len = seg;
+    f.G = G;
+    f.s_in = s_in;
+    e = launch_chunk_tc(f, &why);
+    if (e != cudaSuccess) return cuda_fail(e, why ? why : "segmented forward launch");
+    g_last_error.clear();
+    return EFLA_OK;
 }
 
 efla_status efla_fwd_recurrent_ex(const void *q, const void *k, const void *v, const float *beta,

@@ -27,6 +27,12 @@ struct FwdArgs {
     cudaStream_t stream;
     int *status;  // library device status word
     int euler;    // 1: delta-rule gate alpha = beta instead of the exact gate
+    // Split sequences (tensor-core path only): segments of seg_len tokens, G per row of
+    // [B, T]; maps != nullptr selects the segment-map launch, else s_in holds the
+    // segments' start states (see the chunk kernel).
+    int seg_len = 0, G = 0;
+    const float *s_in = nullptr;
+    float *maps = nullptr;
 };
 
 struct DecodeArgs {
@@ -57,6 +63,9 @@ struct PrepArgs {
 cudaError_t launch_recurrent(const FwdArgs &a);
 cudaError_t launch_decode(const DecodeArgs &a);
 cudaError_t launch_decode_tokens(const DecodeArgs &a);
+// Start states of the segments of split sequences from the segment maps (scan.cu).
+cudaError_t launch_scan_combine(const float *S0, const float *maps, float *s_in, int B, int G, int H,
+                                cudaStream_t stream);
 cudaError_t launch_prep(const PrepArgs &a);
 // tcgen05 chunk kernel: bf16 inputs, d_k = d_v = 128, chunk 64.
 cudaError_t launch_chunk_tc(const FwdArgs &a, const char **why);

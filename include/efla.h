@@ -38,13 +38,14 @@
 #ifndef EFLA_H
 #define EFLA_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
 extern "C" {
 #endif
 
-#define EFLA_ABI_VERSION 3
+#define EFLA_ABI_VERSION 4
 
 typedef enum {
     EFLA_OK = 0,
@@ -137,6 +138,39 @@ efla_status efla_fwd_recurrent(const void *q, const void *k, const void *v, cons
 efla_status efla_decode_step(const void *q, const void *k, const void *v, const float *beta,
                              float *S, void *o, int B, int H, int d_k, int d_v,
                              efla_dtype in_dtype, efla_dtype o_dtype, efla_stream_t stream);
+
+/*
+ * efla_fwd_chunked_scan -- efla_fwd_chunked for few long sequences, split along time.
+ *
+ * Same operation and layouts as efla_fwd_chunked with cu_seqlens = NULL (N = B).
+ * Over any stretch of tokens the update rule is affine in the start state,
+ * S_out = M S_in + N ("Exact Flow Linear Attention" (gist.science), Metodologia 3,
+ * applied token after token), so each sequence is cut into `segments` pieces at
+ * chunk boundaries and evaluated in three launches: the maps (M, N) of every
+ * piece but the last, all pieces in parallel; the start state of every piece by
+ * a serial scan over the maps; then every piece from its start state, with
+ * outputs.  The result equals the unsplit forward up to rounding; it trades
+ * about three times the arithmetic for `segments` times the parallelism, which
+ * pays when B*H is well below the SM count.
+ *
+ *   segments   pieces per sequence; 0 = SM count / (B*H).  Capped at the chunk count.
+ *   workspace  device scratch owned by the caller, 16-byte aligned, at least the size
+ *              efla_fwd_scan_workspace reports (0 bytes when one piece results);
+ *              must not overlap any argument; its contents on return are unspecified.
+ * Only bf16 inputs with d_k = d_v = 128 are split; other shapes, and a single
+ * piece, run the plain efla_fwd_chunked path (the workspace is then unused).
+ */
+efla_status efla_fwd_chunked_scan(const void *q, const void *k, const void *v, const float *beta,
+                                  const float *S0, void *o, float *S_T, int B, int T, int H,
+                                  int d_k, int d_v, efla_dtype in_dtype, efla_dtype o_dtype,
+                                  int segments, void *workspace, size_t workspace_bytes,
+                                  efla_update update, efla_stream_t stream);
+
+/* Workspace bytes efla_fwd_chunked_scan needs for these sizes, and the number of
+ * pieces it will use (segments_used may be NULL).  segments = 0 queries the
+ * current device's SM count. */
+efla_status efla_fwd_scan_workspace(int B, int T, int H, int d_k, int d_v, int segments,
+                                    size_t *bytes, int *segments_used);
 
 /*
  * efla_decode_tokens -- m tokens per sequence appended to a resident state,

@@ -202,3 +202,40 @@ def test_decode_tokens_rejects(lib, kw, code):
 def test_decode_tokens_empty_is_ok_without_gpu_work(lib):
     # m == 0 launches nothing: only S is needed
     assert _dect(lib, m=0, q=None, k=None, v=None, beta=None, o=None) == 0
+
+
+def test_scan_workspace_query(lib):
+    f = lib.efla_fwd_scan_workspace
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_int] * 6 + [ctypes.POINTER(ctypes.c_size_t), ctypes.POINTER(ctypes.c_int)]
+    nb, g = ctypes.c_size_t(0), ctypes.c_int(0)
+    assert f(1, 65536, 16, 128, 128, 9, ctypes.byref(nb), ctypes.byref(g)) == 0
+    assert g.value == 9 and nb.value == (3 * 9 - 2) * 16 * 128 * 128 * 4
+    assert f(1, 700, 2, 128, 128, 3, ctypes.byref(nb), ctypes.byref(g)) == 0
+    assert g.value == 3  # 11 chunks -> pieces of 4, 4, 3 chunks
+    assert f(2, 100, 2, 128, 128, 50, ctypes.byref(nb), ctypes.byref(g)) == 0
+    assert g.value == 2  # capped at the chunk count
+    assert f(8, 2048, 16, 128, 128, 1, ctypes.byref(nb), ctypes.byref(g)) == 0
+    assert nb.value == 0 and g.value == 1
+    assert f(1, 64, 0, 128, 128, 2, ctypes.byref(nb), ctypes.byref(g)) == INVALID
+
+
+def _scanc(lib, **kw):
+    a = dict(q=Q, k=K, v=V, beta=BETA, S0=None, o=O, S_T=None, B=1, T=700, H=2, dk=128, dv=128, ind=0, od=1,
+             seg=3, ws=CU, wsb=1 << 30, upd=0)
+    a.update(kw)
+    vp, ip = ctypes.c_void_p, ctypes.c_int
+    f = lib.efla_fwd_chunked_scan
+    f.restype = ip
+    f.argtypes = [vp] * 7 + [ip] * 8 + [vp, ctypes.c_size_t, ip, vp]
+    return f(a["q"], a["k"], a["v"], a["beta"], a["S0"], a["o"], a["S_T"], a["B"], a["T"], a["H"], a["dk"],
+             a["dv"], a["ind"], a["od"], a["seg"], a["ws"], a["wsb"], a["upd"], None)
+
+
+@pytest.mark.parametrize("kw,msg", [
+    (dict(ws=None), "workspace"), (dict(wsb=1000), "workspace"), (dict(ws=CU + 8), "aligned"),
+    (dict(ws=O), "overlaps"), (dict(upd=4), "update"), (dict(H=0), "bad sizes"),
+])
+def test_scan_rejects(lib, kw, msg):
+    assert _scanc(lib, **kw) == INVALID
+    assert msg in _last(lib)
