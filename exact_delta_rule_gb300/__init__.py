@@ -23,7 +23,7 @@ from typing import Optional, Tuple
 
 import torch
 
-__all__ = ["EflaError", "lib_path", "load", "fwd_chunked", "fwd_chunked_scan", "scan_workspace", "fwd_recurrent",
+__all__ = ["EflaError", "lib_path", "load", "fwd_chunked", "fwd_chunked_scan", "fwd_chunked_scan_static", "scan_workspace", "fwd_recurrent",
            "decode_step", "decode_tokens", "prep",
            "device_status", "abi_version", "STATUS", "UPDATES"]
 
@@ -70,6 +70,8 @@ def load():
         L.efla_decode_step_ex.argtypes = [vp] * 6 + [ip] * 7 + [vp]
         L.efla_fwd_chunked_scan.restype = ip
         L.efla_fwd_chunked_scan.argtypes = [vp] * 7 + [ip] * 8 + [vp, ctypes.c_size_t, ip, vp]
+        L.efla_fwd_chunked_scan_static.restype = ip
+        L.efla_fwd_chunked_scan_static.argtypes = [vp] * 7 + [ip] * 8 + [ip, vp]
         L.efla_fwd_scan_workspace.restype = ip
         L.efla_fwd_scan_workspace.argtypes = [ip] * 6 + [ctypes.POINTER(ctypes.c_size_t), ctypes.POINTER(ip)]
         L.efla_decode_tokens.restype = ip
@@ -219,6 +221,31 @@ def fwd_chunked_scan(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: to
     _check(L.efla_fwd_chunked_scan(_p(q), _p(k), _p(v), _p(beta), _p(S0), _p(o), _p(S_T), B, T, H, dk, dv,
                                    _dt(q.dtype), _dt(o.dtype), int(segments), _p(workspace), nbytes,
                                    UPDATES[update], _stream(stream)))
+    return o, S_T
+
+
+def fwd_chunked_scan_static(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor,
+                            S0: Optional[torch.Tensor] = None, *, segments: int = 0, o: Optional[torch.Tensor] = None,
+                            S_T: Optional[torch.Tensor] = None, o_dtype: torch.dtype = torch.float32, stream=None,
+                            return_state: bool = True, update: str = "exact"):
+    """``fwd_chunked_scan`` on the library's fixed scratch (``efla_fwd_chunked_scan_static``):
+    no workspace.  Calls that overlap in time race on that scratch."""
+    L = load()
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (beta, "beta"), (S0, "S0"), (o, "o")):
+        _need(t, n)
+    if q.dim() != 4 or k.shape != q.shape or v.shape[:3] != q.shape[:3] or beta.shape != q.shape[:3]:
+        raise EflaError(1, "shape mismatch")
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if o is None:
+        o = torch.empty((B, T, H, dv), dtype=o_dtype, device=q.device)
+    if S_T is None and return_state:
+        S_T = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
+    if update not in UPDATES:
+        raise EflaError(1, f"unknown update rule {update!r}")
+    _check(L.efla_fwd_chunked_scan_static(_p(q), _p(k), _p(v), _p(beta), _p(S0), _p(o), _p(S_T), B, T, H, dk, dv,
+                                          _dt(q.dtype), _dt(o.dtype), int(segments), UPDATES[update],
+                                          _stream(stream)))
     return o, S_T
 
 

@@ -6,6 +6,7 @@
 #include <string>
 
 #include <algorithm>
+#include <mutex>
 
 #include "internal.cuh"
 
@@ -13,6 +14,13 @@ namespace efla {
 namespace {
 
 __device__ int g_device_status = 0;
+
+// Scratch of efla_fwd_chunked_scan_static: a fixed device array, so that call
+// allocates nothing.  32 MiB holds the segment states and maps of any split the
+// automatic segment count picks on a GPU of up to 170 SMs ((3 G - 2) B H pieces of
+// 64 KiB with G <= SMs / (B H)).
+constexpr size_t SCAN_SCRATCH_BYTES = 32ull << 20;
+static __device__ __align__(256) unsigned char g_scan_scratch[SCAN_SCRATCH_BYTES];
 
 thread_local std::string g_last_error;
 
@@ -241,6 +249,44 @@ efla_status efla_fwd_chunked_scan(const void *q, const void *k, const void *v, c
     if (e != cudaSuccess) return cuda_fail(e, why ? why : "segmented forward launch");
     g_last_error.clear();
     return EFLA_OK;
+}
+
+// Device address of the static scratch, resolved once per device.
+static void *scan_scratch_ptr() {
+    static std::mutex mu;
+    static void *ptrs[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!ptrs[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_scan_scratch) == cudaSuccess) ptrs[dev] = p;
+    }
+    return ptrs[dev];
+}
+
+efla_status efla_fwd_chunked_scan_static(const void *q, const void *k, const void *v, const float *beta,
+                                         const float *S0, void *o, float *S_T, int B, int T, int H, int d_k,
+                                         int d_v, efla_dtype in_dtype, efla_dtype o_dtype, int segments,
+                                         efla_update update, efla_stream_t stream) {
+    if (!update_ok(update)) return fail(EFLA_ERR_INVALID_ARG, "unknown update rule %d", (int)update);
+    if (B < 0 || T < 0 || H <= 0) return fail(EFLA_ERR_INVALID_ARG, "bad sizes B=%d T=%d H=%d", B, T, H);
+    size_t need = 0;
+    const bool tc = in_dtype == EFLA_BF16 && d_k == 128 && d_v == 128;
+    if (tc && (long long)B * T > 0) {
+        int G = 1, seg = 64;
+        efla_status s = scan_plan(B, T, H, segments, &G, &seg);
+        if (s != EFLA_OK) return s;
+        need = scan_bytes(B, H, d_k, d_v, G);
+    }
+    if (need > SCAN_SCRATCH_BYTES)
+        return fail(EFLA_ERR_UNSUPPORTED, "this split needs %zu bytes of scratch; the static scratch holds %zu",
+                    need, SCAN_SCRATCH_BYTES);
+    void *ws = nullptr;
+    if (need > 0 && !(ws = scan_scratch_ptr())) return fail(EFLA_ERR_CUDA, "cannot resolve the static scratch");
+    // Nothing in the scratch has to start at zero: every state and map is written before it is read.
+    return efla_fwd_chunked_scan(q, k, v, beta, S0, o, S_T, B, T, H, d_k, d_v, in_dtype, o_dtype, segments, ws,
+                                 need > 0 ? SCAN_SCRATCH_BYTES : 0, update, stream);
 }
 
 efla_status efla_fwd_recurrent_ex(const void *q, const void *k, const void *v, const float *beta,

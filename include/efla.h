@@ -45,7 +45,7 @@
 extern "C" {
 #endif
 
-#define EFLA_ABI_VERSION 4
+#define EFLA_ABI_VERSION 5
 
 typedef enum {
     EFLA_OK = 0,
@@ -171,6 +171,25 @@ efla_status efla_fwd_chunked_scan(const void *q, const void *k, const void *v, c
  * current device's SM count. */
 efla_status efla_fwd_scan_workspace(int B, int T, int H, int d_k, int d_v, int segments,
                                     size_t *bytes, int *segments_used);
+
+/*
+ * efla_fwd_chunked_scan_static -- efla_fwd_chunked_scan with library-owned scratch.
+ *
+ * The pages have no counterpart to this call: it is the same operation as
+ * efla_fwd_chunked_scan (same arguments without workspace/workspace_bytes) for
+ * callers that cannot provide device memory.  The scratch is a fixed 32 MiB device
+ * array inside libefla.so (allocated when the module loads; this call allocates
+ * nothing), enough for any automatic split (segments = 0) on GPUs of up to 170
+ * SMs.  A split that needs more returns EFLA_ERR_UNSUPPORTED before any launch.
+ * Nothing in the scratch has to start at zero, so it is never cleared.
+ * The scratch is shared by every call in the process on the same device: calls
+ * that may overlap in time (other streams, other host threads) race on it and
+ * give wrong results; serialise them, or use efla_fwd_chunked_scan.
+ */
+efla_status efla_fwd_chunked_scan_static(const void *q, const void *k, const void *v, const float *beta,
+                                         const float *S0, void *o, float *S_T, int B, int T, int H,
+                                         int d_k, int d_v, efla_dtype in_dtype, efla_dtype o_dtype,
+                                         int segments, efla_update update, efla_stream_t stream);
 
 /*
  * efla_decode_tokens -- m tokens per sequence appended to a resident state,
