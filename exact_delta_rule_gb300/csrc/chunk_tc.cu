@@ -484,12 +484,8 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
                 issue_gram(tmem, s_sm, c, bars);
             }
             ok = wait_bar(&bars->g_done, c & 1, abort_flag);
-            // the T''/P buffers of this chunk were last read by chunk c-2's MMAs, then
-            // held chunk c-2's o tile until its TMA stores had read it
-            if (c >= 2) {
-                ok = wait_bar(&bars->chunk_done[c & 1], ((c - 2) >> 1) & 1, abort_flag) && ok;
-                ok = wait_bar(&bars->ost_free[c & 1], ((c - 2) >> 1) & 1, abort_flag) && ok;
-            }
+            // the P buffer of this chunk was last read by chunk c-2's products
+            if (c >= 2) ok = wait_bar(&bars->chunk_done[c & 1], ((c - 2) >> 1) & 1, abort_flag) && ok;
             tc_fence_after();
             {
                 float g[32];
@@ -550,6 +546,8 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
             }
             named_bar(BAR_PREP, 256);
             invert_unit_lower(At, pi);
+            // the T'' buffer of this chunk held chunk c-2's o tile until its TMA stores had read it
+            if (c >= 2) ok = wait_bar(&bars->ost_free[c & 1], ((c - 2) >> 1) & 1, abort_flag) && ok;
             {  // T'' = diag(1/n) T~ diag(gamma/n), lower triangle, as bf16 hi/lo [t][s]
                 const int t = pi >> 2, s0 = (pi & 3) * 16;
                 uint8_t *hi = sm + OFF_TPP + buf * TPP_BYTES, *lo = hi + 8192;
@@ -646,45 +644,52 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
             }
             tc_fence_before();
             mbar_arrive(&bars->o_free);  // the next chunk's first product may overwrite O^T
-            // the chunk's T''/P buffers (free once its last product completed) stage the tile
-            uint8_t *slice = sm + OFF_TPP + (cc & 1) * TPP_BYTES + warp * 8192;
-            if (OUT_BF16) {
-                __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(slice) + lane;
+            // The tile leaves in two halves of 32 tokens, staged in the T'' part of the chunk's
+            // T''/P buffers (free once its last product completed): the P part stays free for
+            // the prep of chunk cc + 2 as soon as those products are done.
+            uint8_t *slice = sm + OFF_TPP + (cc & 1) * TPP_BYTES + warp * 4096;
+            auto send_half = [&](const float (&x)[32], int t_off) {
+                if (t_off > 0) {  // the first half's store has read the slice
+                    if (lane == 0) bulk_wait_read0();
+                    __syncwarp();
+                }
+                if (OUT_BF16) {
+                    __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(slice) + lane;
 #pragma unroll
-                for (int t = 0; t < 32; ++t) {
-                    stg[t * 32] = __float2bfloat16_rn(ov[t]);
-                    stg[(t + 32) * 32] = __float2bfloat16_rn(ow[t]);
-                }
-            } else {
-                float *stg = reinterpret_cast<float *>(slice) + lane;
+                    for (int t = 0; t < 32; ++t) stg[t * 32] = __float2bfloat16_rn(x[t]);
+                } else {
+                    float *stg = reinterpret_cast<float *>(slice) + lane;
 #pragma unroll
-                for (int t = 0; t < 32; ++t) {
-                    stg[t * 32] = ov[t];
-                    stg[(t + 32) * 32] = ow[t];
+                    for (int t = 0; t < 32; ++t) stg[t * 32] = x[t];
                 }
-            }
-            if (p.cu_seqlens == nullptr || vc == C) {
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    tma_store_4d(&p.map_o, slice, warp * 32, h, (int)t0c, (int)b);
-                    bulk_commit();
-                    bulk_wait_read0();  // the slice may be rewritten by the prep two chunks on
-                    mbar_arrive(&bars->ost_free[cc & 1]);
-                }
-            } else {  // partial chunk of a packed batch: rows past vc belong to the next sequence
-                __syncwarp();
+                if (p.cu_seqlens == nullptr || vc == C) {
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_4d(&p.map_o, slice, warp * 32, h, (int)(t0c + t_off), (int)b);
+                        bulk_commit();
+                    }
+                } else {  // partial chunk of a packed batch: rows past vc belong to the next sequence
+                    __syncwarp();
+                    const int n = min(32, vc - t_off);
 #pragma unroll 1
-                for (int t = 0; t < vc; t = opaque(t + 1)) {
-                    const size_t rw = ((size_t)b * p.T + (size_t)(t0c + t)) * p.H + h;
-                    if (OUT_BF16)
-                        static_cast<__nv_bfloat16 *>(p.o)[rw * D + j] =
-                            reinterpret_cast<const __nv_bfloat16 *>(slice)[t * 32 + lane];
-                    else
-                        static_cast<float *>(p.o)[rw * D + j] = reinterpret_cast<const float *>(slice)[t * 32 + lane];
+                    for (int t = 0; t < n; t = opaque(t + 1)) {
+                        const size_t rw = ((size_t)b * p.T + (size_t)(t0c + t_off + t)) * p.H + h;
+                        if (OUT_BF16)
+                            static_cast<__nv_bfloat16 *>(p.o)[rw * D + j] =
+                                reinterpret_cast<const __nv_bfloat16 *>(slice)[t * 32 + lane];
+                        else
+                            static_cast<float *>(p.o)[rw * D + j] =
+                                reinterpret_cast<const float *>(slice)[t * 32 + lane];
+                    }
+                    __syncwarp();
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars->ost_free[cc & 1]);
+            };
+            send_half(ov, 0);
+            if (vc > 32) send_half(ow, 32);
+            if (lane == 0) {
+                bulk_wait_read0();  // the slice may be rewritten by the prep two chunks on
+                mbar_arrive(&bars->ost_free[cc & 1]);
             }
             clear_ob();  // before this warpgroup's next u_ready, which precedes the next O_b product
         };
@@ -929,13 +934,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // 4-D map over a [B, T, H, 128] tensor: box of `box_x` features x 1 head x 64 tokens.
-bool make_map(CUtensorMap *m, const void *ptr, int B, int T, int H, bool f32, int box_x, bool swizzle) {
+bool make_map(CUtensorMap *m, const void *ptr, int B, int T, int H, bool f32, int box_x, bool swizzle,
+              int box_t = C) {
     auto fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t es_b = f32 ? 4 : 2;
     cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
     cuuint64_t strides[3] = {(cuuint64_t)D * es_b, (cuuint64_t)H * D * es_b, (cuuint64_t)T * H * D * es_b};
-    cuuint32_t box[4] = {(cuuint32_t)box_x, 1, (cuuint32_t)C, 1};
+    cuuint32_t box[4] = {(cuuint32_t)box_x, 1, (cuuint32_t)box_t, 1};
     cuuint32_t es[4] = {1, 1, 1, 1};
     return fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr),
               dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -970,7 +976,7 @@ cudaError_t launch_chunk_tc(const FwdArgs &a, const char **why) {
         if (!make_map(&p.map_q, a.q, a.B, a.T, a.H, false, 64, true) ||
             !make_map(&p.map_k, a.k, a.B, a.T, a.H, false, 64, true) ||
             !make_map(&p.map_v, a.v, a.B, a.T, a.H, false, 64, true) ||
-            (a.o && !make_map(&p.map_o, a.o, a.B, a.T, a.H, !o_bf16, 32, false))) {
+            (a.o && !make_map(&p.map_o, a.o, a.B, a.T, a.H, !o_bf16, 32, false, 32))) {
             *why = "cuTensorMapEncodeTiled failed";
             return cudaErrorInvalidValue;
         }
