@@ -73,6 +73,11 @@ def _load():
             lib.efla_oracle_fwd_mode.argtypes = [dp, dp, dp, dp, dp, lp, dp, dp] + [ctypes.c_int] * 8
             lib.efla_oracle_decode_mode.restype = ctypes.c_int
             lib.efla_oracle_decode_mode.argtypes = [dp, dp, dp, dp, dp, dp] + [ctypes.c_int] * 6
+            lib.efla_oracle_bwd_mode.restype = ctypes.c_int
+            lib.efla_oracle_bwd_mode.argtypes = [dp] * 12 + [ctypes.c_int] * 7
+            lib.efla_oracle_gate_grad.restype = None
+            lib.efla_oracle_gate_grad.argtypes = [ctypes.c_double, ctypes.c_double, ctypes.c_int,
+                                                  ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)]
             lib.efla_oracle_max_threads.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -148,3 +153,27 @@ def decode_step(q, k, v, beta, S, *, threads: int = 0, update: str = "exact"):
     if rc != 0:
         raise ValueError(f"efla_oracle_decode failed with code {rc}")
     return o, S
+
+
+def gate_grad(beta: float, lam: float, update: str = "exact"):
+    """(d alpha / d beta, d alpha / d lam) of the gate (oracle/efla_oracle.c)."""
+    a, b = ctypes.c_double(0.0), ctypes.c_double(0.0)
+    _load().efla_oracle_gate_grad(float(beta), float(lam), _UPDATES[update], ctypes.byref(a), ctypes.byref(b))
+    return a.value, b.value
+
+
+def bwd(q, k, v, beta, S0, do, dS_T, *, threads: int = 0, update: str = "exact"):
+    """Reverse-mode gradients of ``fwd`` (no cu_seqlens): given do [B,T,H,dv] and dS_T
+    [B,H,dk,dv] (or None), returns dict dq, dk [B,T,H,dk], dv [B,T,H,dv], dbeta [B,T,H],
+    dS0 [B,H,dk,dv] as fp64 numpy arrays."""
+    q, k, v, beta, S0, do, dS_T = (_f64(x) for x in (q, k, v, beta, S0, do, dS_T))
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    out = {"dq": np.zeros((B, T, H, dk)), "dk": np.zeros((B, T, H, dk)), "dv": np.zeros((B, T, H, dv)),
+           "dbeta": np.zeros((B, T, H)), "dS0": np.zeros((B, H, dk, dv))}
+    rc = _load().efla_oracle_bwd_mode(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(S0), _ptr(do), _ptr(dS_T),
+                                      _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]), _ptr(out["dbeta"]),
+                                      _ptr(out["dS0"]), B, T, H, dk, dv, int(threads), _UPDATES[update])
+    if rc != 0:
+        raise RuntimeError(f"efla_oracle_bwd_mode failed ({rc})")
+    return out

@@ -374,3 +374,93 @@ def test_euler_and_exact_differ_for_large_keys():
     _, S_d = oracle.fwd(q[None, :, None], k[None, :, None], v[None, :, None], beta[None, :, None],
                         S0[None, None], update="euler")
     assert np.abs(S_e - S_d[0, 0]).max() > 0.1
+
+
+# ----------------------------------------------------------------- backward
+def _fd_case(seed=3, T=6, H=2, dk=3, dv=2):
+    rng = np.random.default_rng(seed)
+    q = rng.normal(size=(1, T, H, dk))
+    k = rng.normal(size=(1, T, H, dk))
+    k[0, 2, 0] = 0.0                      # lambda = 0: the gate's limit value
+    v = rng.normal(size=(1, T, H, dv))
+    beta = rng.uniform(0.2, 1.5, size=(1, T, H))
+    beta[0, 4, 1] = 1e-5                  # beta*lambda below 1e-3: the gate derivative's series branch
+    S0 = rng.normal(size=(1, H, dk, dv))
+    W = rng.normal(size=(1, T, H, dv))    # L = sum(o * W) + sum(S_T * V)
+    V = rng.normal(size=(1, H, dk, dv))
+    return q, k, v, beta, S0, W, V
+
+
+@pytest.mark.parametrize("update", ["exact", "euler"])
+def test_bwd_matches_finite_differences(update):
+    """Every gradient of L = <o, W> + <S_T, V> against central differences of the forward oracle."""
+    q, k, v, beta, S0, W, V = _fd_case()
+    g = oracle.bwd(q, k, v, beta, S0, W, V, update=update)
+
+    def loss(qq, kk, vv, bb, ss):
+        o, S_T = oracle.fwd(qq, kk, vv, bb, ss, update=update)
+        return float(np.sum(o * W) + np.sum(S_T * V))
+
+    args = [q, k, v, beta, S0]
+    names = ["dq", "dk", "dv", "dbeta", "dS0"]
+    h = 1e-6
+    for ai, name in enumerate(names):
+        base = args[ai]
+        fd = np.zeros_like(base)
+        for idx in np.ndindex(base.shape):
+            if name == "dk" and base[idx] == 0.0 and update == "exact":
+                pass  # k = 0 is inside the domain from both sides: central differences are fine
+            plus = [a.copy() for a in args]
+            minus = [a.copy() for a in args]
+            plus[ai][idx] += h
+            minus[ai][idx] -= h
+            fd[idx] = (loss(*plus) - loss(*minus)) / (2 * h)
+        np.testing.assert_allclose(g[name], fd, rtol=2e-6, atol=2e-7, err_msg=f"{name} ({update})")
+
+
+def test_gate_derivatives_match_finite_differences():
+    h = 1e-7
+    for beta in (0.3, 1.7, -0.4):
+        for lam in (1e-6 / abs(beta), 5e-4 / abs(beta), 2e-3 / abs(beta), 0.5, 5.0, 30.0):
+            dfdb, dfdl = oracle.gate_grad(beta, lam)
+            fb = (oracle.alpha(beta + h, lam) - oracle.alpha(beta - h, lam)) / (2 * h)
+            hl = h * max(lam, 1e-3)
+            fl = (oracle.alpha(beta, lam + hl) - oracle.alpha(beta, lam - hl)) / (2 * hl)
+            assert abs(dfdb - fb) <= 1e-6 * max(1.0, abs(fb)), (beta, lam, dfdb, fb)
+            assert abs(dfdl - fl) <= 2e-5 * max(1.0, abs(fl)), (beta, lam, dfdl, fl)
+        # at lam = 0 the gate is beta and its lam-slope is the limit -beta^2/2
+        dfdb, dfdl = oracle.gate_grad(beta, 0.0)
+        assert dfdb == 1.0 and abs(dfdl + beta * beta / 2) < 1e-15
+        fl = (oracle.alpha(beta, 1e-7) - oracle.alpha(beta, 0.0)) / 1e-7
+        assert abs(dfdl - fl) < 1e-6
+
+
+def test_bwd_zero_step_size_closed_form():
+    """beta = 0: the state never moves, so o_t = S0^T q_t, dq_t = S0 do_t, dS0 = dS_T + sum q_t do_t^T,
+    dv = 0, dk = 0, and dbeta_t = du_t . (v_t - x_t) with du_t = G_t^T k_t, x_t = S0^T k_t and
+    G_t = dS_T + sum_{s >= t} q_s do_s^T (df/dbeta = 1 at beta = 0)."""
+    rng = np.random.default_rng(8)
+    T, dk, dv = 5, 4, 3
+    q, k = rng.normal(size=(1, T, 1, dk)), rng.normal(size=(1, T, 1, dk))
+    v, do = rng.normal(size=(1, T, 1, dv)), rng.normal(size=(1, T, 1, dv))
+    S0, dST = rng.normal(size=(1, 1, dk, dv)), rng.normal(size=(1, 1, dk, dv))
+    g = oracle.bwd(q, k, v, np.zeros((1, T, 1)), S0, do, dST)
+    s0 = S0[0, 0]
+    np.testing.assert_allclose(g["dq"][0, :, 0], do[0, :, 0] @ s0.T, atol=1e-12)
+    np.testing.assert_allclose(g["dS0"][0, 0], dST[0, 0] + np.einsum("ti,tj->ij", q[0, :, 0], do[0, :, 0]),
+                               atol=1e-12)
+    assert np.abs(g["dv"]).max() == 0 and np.abs(g["dk"]).max() == 0
+    for t in range(T):
+        Gt = dST[0, 0] + np.einsum("si,sj->ij", q[0, t:, 0], do[0, t:, 0])
+        du = Gt.T @ k[0, t, 0]
+        x = s0.T @ k[0, t, 0]
+        assert abs(g["dbeta"][0, t, 0] - du @ (v[0, t, 0] - x)) < 1e-12
+
+
+def test_bwd_is_linear_in_output_gradients():
+    q, k, v, beta, S0, W, V = _fd_case(seed=5, T=9, H=2, dk=5, dv=4)
+    g1 = oracle.bwd(q, k, v, beta, S0, W, V)
+    g2 = oracle.bwd(q, k, v, beta, S0, 2.5 * W, None)
+    g3 = oracle.bwd(q, k, v, beta, S0, np.zeros_like(W), 2.5 * V)
+    for name in g1:
+        np.testing.assert_allclose(2.5 * g1[name], g2[name] + g3[name], rtol=1e-12, atol=1e-12)
