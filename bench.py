@@ -320,6 +320,9 @@ def run_ours(args, world, rank, local):
     # ---- multi-token decode: 16 tokens per sequence appended to the B256 H32 state
     dt_fig = decode_tokens_figure(efla, dev, stream, args.steps, flush, peaks)
 
+    # ---- backward pass on the lm shape (dO random, dS_T random)
+    bwd_fig = bwd_figure(efla, dev, stream, q, k, v, beta, flush, peaks)
+
     # ---- the stiff/long configuration: one sequence per head, unsplit and split along time
     stiff_fig = stiff_figure(efla, dev, stream, max(3, args.steps // 2), flush, peaks)
 
@@ -358,6 +361,7 @@ def run_ours(args, world, rank, local):
             "prep": prep_fig,
             "decode_tokens": dt_fig,
             "stiff": stiff_fig,
+            "bwd": bwd_fig,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
@@ -419,6 +423,19 @@ def decode_figures(efla, dev, stream):
                         "chained steps (inputs cycled from 8 seeded steps); S (512 MiB) exceeds L2",
             "us_per_step": 1e6 * t, "GB/s": nbytes / t / 1e9, "bytes_per_step": nbytes,
             "frac_hbm": nbytes / t / 1e9 / peaks["hbm_gbs"], "gpu_launches": reps * n_graph}
+
+
+def bwd_figure(efla, dev, stream, q, k, v, beta, flush, peaks, steps=3):
+    import torch
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    g = torch.Generator(device=dev).manual_seed(7)
+    dO = torch.randn((B, T, H, dv), generator=g, device=dev)
+    dST = torch.randn((B, H, dk, dv), generator=g, device=dev)
+    t = time_steps(lambda: efla.bwd_recurrent(q, k, v, beta, None, dO, dST, stream=stream), steps, flush, stream)
+    return {"workload": "lm shape backward: dq, dk, dv, dbeta, dS0 from random dO and dS_T (fp32 on CUDA cores, "
+                        "one CTA per (b, h), forward sweep + reverse sweep)",
+            "ms_per_call": 1e3 * t, "tokens_per_s": B * T / t, "gpu_launches": steps}
 
 
 def stiff_figure(efla, dev, stream, steps, flush, peaks):

@@ -24,7 +24,7 @@ from typing import Optional, Tuple
 import torch
 
 __all__ = ["EflaError", "lib_path", "load", "fwd_chunked", "fwd_chunked_scan", "fwd_chunked_scan_static", "scan_workspace", "fwd_recurrent",
-           "decode_step", "decode_tokens", "prep",
+           "decode_step", "decode_tokens", "bwd_recurrent", "prep",
            "device_status", "abi_version", "STATUS", "UPDATES"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -74,6 +74,8 @@ def load():
         L.efla_fwd_chunked_scan_static.argtypes = [vp] * 7 + [ip] * 8 + [ip, vp]
         L.efla_fwd_scan_workspace.restype = ip
         L.efla_fwd_scan_workspace.argtypes = [ip] * 6 + [ctypes.POINTER(ctypes.c_size_t), ctypes.POINTER(ip)]
+        L.efla_bwd_recurrent.restype = ip
+        L.efla_bwd_recurrent.argtypes = [vp] * 12 + [ip] * 7 + [vp]
         L.efla_decode_tokens.restype = ip
         L.efla_decode_tokens.argtypes = [vp] * 6 + [ip] * 8 + [vp]
         L.efla_prep.restype = ip
@@ -308,6 +310,35 @@ def decode_tokens(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch
     _check(L.efla_decode_tokens(_p(q), _p(k), _p(v), _p(beta), _p(S), _p(o), B, m, H, dk, dv,
                                 _dt(q.dtype), _dt(o.dtype), UPDATES[update], _stream(stream)))
     return o
+
+
+def bwd_recurrent(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor,
+                  S0: Optional[torch.Tensor], dO: torch.Tensor, dS_T: Optional[torch.Tensor] = None, *,
+                  need_dS0: bool = True, stream=None, update: str = "exact") -> dict:
+    """Gradients of ``fwd_chunked`` (no cu_seqlens) from dO [B,T,H,dv] fp32 and dS_T
+    [B,H,dk,dv] fp32 (or None): returns dq, dk, dv, dbeta and dS0 (fp32), ``efla_bwd_recurrent``."""
+    L = load()
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (beta, "beta"), (S0, "S0"), (dO, "dO"), (dS_T, "dS_T")):
+        _need(t, n)
+    if q.dim() != 4 or k.shape != q.shape or v.shape[:3] != q.shape[:3] or beta.shape != q.shape[:3]:
+        raise EflaError(1, "shape mismatch")
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if dO.dtype != torch.float32 or tuple(dO.shape) != (B, T, H, dv):
+        raise EflaError(1, f"dO must be float32 [{B},{T},{H},{dv}]")
+    for t, n in ((S0, "S0"), (dS_T, "dS_T")):
+        if t is not None and (t.dtype != torch.float32 or tuple(t.shape) != (B, H, dk, dv)):
+            raise EflaError(1, f"{n} must be float32 [{B},{H},{dk},{dv}]")
+    if update not in UPDATES:
+        raise EflaError(1, f"unknown update rule {update!r}")
+    f32 = dict(dtype=torch.float32, device=q.device)
+    out = {"dq": torch.empty((B, T, H, dk), **f32), "dk": torch.empty((B, T, H, dk), **f32),
+           "dv": torch.empty((B, T, H, dv), **f32), "dbeta": torch.empty((B, T, H), **f32),
+           "dS0": torch.empty((B, H, dk, dv), **f32) if need_dS0 else None}
+    _check(L.efla_bwd_recurrent(_p(q), _p(k), _p(v), _p(beta), _p(S0), _p(dO), _p(dS_T), _p(out["dq"]),
+                                _p(out["dk"]), _p(out["dv"]), _p(out["dbeta"]), _p(out["dS0"]), B, T, H, dk, dv,
+                                _dt(q.dtype), UPDATES[update], _stream(stream)))
+    return out
 
 
 def prep(k: torch.Tensor, beta: torch.Tensor, v: Optional[torch.Tensor] = None, *, lam: bool = True,

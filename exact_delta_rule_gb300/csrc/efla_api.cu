@@ -289,6 +289,47 @@ efla_status efla_fwd_chunked_scan_static(const void *q, const void *k, const voi
                                  need > 0 ? SCAN_SCRATCH_BYTES : 0, update, stream);
 }
 
+efla_status efla_bwd_recurrent(const void *q, const void *k, const void *v, const float *beta, const float *S0,
+                               const float *dO, const float *dS_T, float *dq, float *dk, float *dv, float *dbeta,
+                               float *dS0, int B, int T, int H, int d_k, int d_v, efla_dtype in_dtype,
+                               efla_update update, efla_stream_t stream) {
+    if (!update_ok(update)) return fail(EFLA_ERR_INVALID_ARG, "unknown update rule %d", (int)update);
+    if (B < 0 || T < 0 || H <= 0) return fail(EFLA_ERR_INVALID_ARG, "bad sizes B=%d T=%d H=%d", B, T, H);
+    efla_status s = check_dims_common(d_k, d_v, in_dtype, EFLA_F32);
+    if (s != EFLA_OK) return s;
+    const long long rows = (long long)B * T * H;
+    if (rows > (1LL << 31) - 1) return fail(EFLA_ERR_UNSUPPORTED, "B*T*H=%lld exceeds 2^31-1", rows);
+    if (rows > 0 && (!q || !k || !v || !beta || !dO || !dq || !dk || !dv || !dbeta))
+        return fail(EFLA_ERR_INVALID_ARG, "q, k, v, beta, dO, dq, dk, dv and dbeta must be non-NULL when B*T > 0");
+    const void *ptrs[] = {q, k, v, beta, S0, dO, dS_T, dq, dk, dv, dbeta, dS0};
+    const char *names[] = {"q", "k", "v", "beta", "S0", "dO", "dS_T", "dq", "dk", "dv", "dbeta", "dS0"};
+    for (int i = 0; i < 12; ++i)
+        if (ptrs[i] && !aligned16(ptrs[i]))
+            return fail(EFLA_ERR_INVALID_ARG, "%s=%p is not 16-byte aligned", names[i], ptrs[i]);
+    const size_t th = (size_t)rows, st = (size_t)B * H * d_k * d_v * 4;
+    auto R = [](const char *n, const void *p, size_t bytes) {
+        uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+        return Range{n, lo, p ? lo + bytes : lo};
+    };
+    const Range in[] = {R("q", q, th * d_k * dsize(in_dtype)), R("k", k, th * d_k * dsize(in_dtype)),
+                        R("v", v, th * d_v * dsize(in_dtype)), R("beta", beta, th * 4), R("S0", S0, st),
+                        R("dO", dO, th * d_v * 4), R("dS_T", dS_T, st)};
+    const Range out[] = {R("dq", dq, th * d_k * 4), R("dk", dk, th * d_k * 4), R("dv", dv, th * d_v * 4),
+                         R("dbeta", dbeta, th * 4), R("dS0", dS0, st)};
+    for (int i = 0; i < 5; ++i) {
+        for (const Range &r : in)
+            if (overlap(out[i], r)) return fail(EFLA_ERR_INVALID_ARG, "output %s overlaps input %s", out[i].name, r.name);
+        for (int j = i + 1; j < 5; ++j)
+            if (overlap(out[i], out[j])) return fail(EFLA_ERR_INVALID_ARG, "outputs %s and %s overlap", out[i].name, out[j].name);
+    }
+    BwdArgs a{q, k, v, beta, S0, dO, dS_T, dq, dk, dv, dbeta, dS0, B, T, H, d_k, d_v, in_dtype,
+              reinterpret_cast<cudaStream_t>(stream), (int)update};
+    cudaError_t e = launch_bwd(a);
+    if (e != cudaSuccess) return cuda_fail(e, "backward kernel launch");
+    g_last_error.clear();
+    return EFLA_OK;
+}
+
 efla_status efla_fwd_recurrent_ex(const void *q, const void *k, const void *v, const float *beta,
                                   const float *S0, const int32_t *cu_seqlens, void *o, float *S_T, int B,
                                   int T, int H, int d_k, int d_v, int N, efla_dtype in_dtype,

@@ -63,6 +63,18 @@ struct PrepArgs {
 cudaError_t launch_recurrent(const FwdArgs &a);
 cudaError_t launch_decode(const DecodeArgs &a);
 cudaError_t launch_decode_tokens(const DecodeArgs &a);
+// Backward pass (bwd.cu): gradients of the forward over whole rows of [B, T].
+struct BwdArgs {
+    const void *q, *k, *v;
+    const float *beta, *S0, *dO, *dST;
+    float *dq, *dk, *dv, *dbeta, *dS0;
+    int B, T, H, dk_dim, dv_dim;
+    efla_dtype in_dtype;
+    cudaStream_t stream;
+    int euler;
+};
+cudaError_t launch_bwd(const BwdArgs &a);
+
 // Start states of the segments of split sequences from the segment maps (scan.cu).
 cudaError_t launch_scan_combine(const float *S0, const float *maps, float *s_in, int B, int G, int H,
                                 cudaStream_t stream);

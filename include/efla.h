@@ -45,7 +45,7 @@
 extern "C" {
 #endif
 
-#define EFLA_ABI_VERSION 5
+#define EFLA_ABI_VERSION 6
 
 typedef enum {
     EFLA_OK = 0,
@@ -190,6 +190,30 @@ efla_status efla_fwd_chunked_scan_static(const void *q, const void *k, const voi
                                          const float *S0, void *o, float *S_T, int B, int T, int H,
                                          int d_k, int d_v, efla_dtype in_dtype, efla_dtype o_dtype,
                                          int segments, efla_update update, efla_stream_t stream);
+
+/*
+ * efla_bwd_recurrent -- gradients of efla_fwd_chunked (cu_seqlens = NULL, N = B).
+ *
+ * Given dO = dL/do and dS_T = dL/dS_T, returns dq, dk, dv, dbeta and dS0 of any loss L
+ * of the forward's outputs.  The pages give no backward formulas: this is reverse
+ * mode of the update rule and read-out above ("Exact Flow Linear Attention"
+ * (gist.science), Metodologia 3; "Error-Free Linear Attention is a Free Lunch"
+ * (howistudyai), Steps 1-3), evaluated token by token in reverse order in fp32 on CUDA
+ * cores (one CTA per (b, h); a forward sweep first recomputes the states).
+ *
+ *   q, k [B, T, H, d_k], v [B, T, H, d_v] in_dtype;  beta [B, T, H] fp32
+ *   S0, dS_T [B, H, d_k, d_v] fp32 or NULL (zero)
+ *   dO   [B, T, H, d_v] fp32
+ *   dq, dk [B, T, H, d_k], dv [B, T, H, d_v], dbeta [B, T, H] fp32 outputs;
+ *   dS0 [B, H, d_k, d_v] fp32 or NULL (not written)
+ *   update  the gate of the forward (EFLA_UPDATE_EXACT or EFLA_UPDATE_EULER)
+ * Outputs must not overlap inputs or each other.  Supported: d_k, d_v in {32, 64, 128}.
+ */
+efla_status efla_bwd_recurrent(const void *q, const void *k, const void *v, const float *beta,
+                               const float *S0, const float *dO, const float *dS_T, float *dq,
+                               float *dk, float *dv, float *dbeta, float *dS0, int B, int T, int H,
+                               int d_k, int d_v, efla_dtype in_dtype, efla_update update,
+                               efla_stream_t stream);
 
 /*
  * efla_decode_tokens -- m tokens per sequence appended to a resident state,

@@ -239,3 +239,25 @@ def _scanc(lib, **kw):
 def test_scan_rejects(lib, kw, msg):
     assert _scanc(lib, **kw) == INVALID
     assert msg in _last(lib)
+
+
+def _bw(lib, **kw):
+    a = dict(q=Q, k=K, v=V, beta=BETA, S0=None, dO=CU, dST=None, dq=O, dk=ST, dv=S0, db=0x90000000, dS0=None,
+             B=1, T=64, H=2, dk_=128, dv_=128, ind=0, upd=0)
+    a.update(kw)
+    vp, ip = ctypes.c_void_p, ctypes.c_int
+    f = lib.efla_bwd_recurrent
+    f.restype = ip
+    f.argtypes = [vp] * 12 + [ip] * 7 + [vp]
+    return f(a["q"], a["k"], a["v"], a["beta"], a["S0"], a["dO"], a["dST"], a["dq"], a["dk"], a["dv"], a["db"],
+             a["dS0"], a["B"], a["T"], a["H"], a["dk_"], a["dv_"], a["ind"], a["upd"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(T=-1), INVALID), (dict(H=0), INVALID), (dict(dk_=48), UNSUPPORTED), (dict(dq=None), INVALID),
+    (dict(dO=None), INVALID), (dict(dk=O + 256), INVALID), (dict(dq=Q + 1024), INVALID), (dict(upd=3), INVALID),
+    (dict(db=0x90000000 + 4), INVALID), (dict(ind=5), INVALID),
+])
+def test_bwd_rejects(lib, kw, code):
+    assert _bw(lib, **kw) == code
+    assert _last(lib)
