@@ -12,7 +12,7 @@
 //   dbeta = dalpha df/dbeta;  dk += 2 dalpha df/dlambda k;
 // and dS0 = G at the start of the sequence.
 //
-// One CTA of 256 threads per (sequence, head), fp32 on CUDA cores.  S and G live
+// One CTA of 1024 threads per (sequence, head), fp32 on CUDA cores.  S and G live
 // in shared memory (rows padded to DV + 1 floats).  A forward sweep leaves u_t of
 // every token in the dv output (the reverse sweep overwrites it with dv_t after
 // reading it) and S_T in shared memory; the reverse sweep rebuilds
@@ -24,7 +24,7 @@
 namespace efla {
 namespace {
 
-constexpr int NT = 256;
+constexpr int NT = 1024;
 
 // d alpha / d beta and d alpha / d lambda (fp32; series in z = beta*lambda where the
 // difference form cancels).
@@ -56,7 +56,7 @@ __global__ void __launch_bounds__(NT) bwd_kernel(const BwdArgs a) {
     float *qs = G + DK * LD, *ks = qs + DK, *vs = ks + DK, *dos = vs + DV, *us = dos + DV, *dxs = us + DV;
     float *rr = dxs + DV;        // [2][CGR][DK] row partials
     float *rc = rr + 2 * CGR * DK;  // [2][RGC][DV] column partials
-    float *sc = rc + 2 * RGC * DV;  // [8] scalars, [8] warp partials
+    float *sc = rc + 2 * RGC * DV;  // [8] scalars, [NT / 32] warp partials
 
     const TIn *q = static_cast<const TIn *>(a.q), *k = static_cast<const TIn *>(a.k),
               *v = static_cast<const TIn *>(a.v);
@@ -75,17 +75,28 @@ __global__ void __launch_bounds__(NT) bwd_kernel(const BwdArgs a) {
     }
     __syncthreads();
     // ------------------------------------------------------------ forward sweep
+    // (each token's inputs are loaded one token ahead, so their latency is hidden)
+    float kn = 0.f, vn = 0.f, bn = 0.f;
+    auto fetch_f = [&](int t) {
+        const size_t r = rowidx(t);
+        if (tid < DK) kn = to_f32(k[r * DK + tid]);
+        if (tid < DV) vn = to_f32(v[r * DV + tid]);
+        if (tid == 0) bn = a.beta[r];
+    };
+    if (T > 0) fetch_f(0);
     for (int t = 0; t < T; ++t) {
         const size_t r = rowidx(t);
-        if (tid < DK) ks[tid] = to_f32(k[r * DK + tid]);
-        if (tid < DV) vs[tid] = to_f32(v[r * DV + tid]);
+        if (tid < DK) ks[tid] = kn;
+        if (tid < DV) vs[tid] = vn;
+        const float bcur = bn;
         __syncthreads();
+        if (t + 1 < T) fetch_f(t + 1);
         if (wid == 0) {
             float lam = 0.f;
             for (int i = lane; i < DK; i += 32) lam = fmaf(ks[i], ks[i], lam);
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) lam += __shfl_xor_sync(0xffffffffu, lam, off);
-            if (lane == 0) sc[0] = efla_alpha(a.beta[r], lam, a.euler);
+            if (lane == 0) sc[0] = efla_alpha(bcur, lam, a.euler);
         }
         float xp = 0.f;  // x_j over this thread's rows
 #pragma unroll 8
@@ -111,25 +122,42 @@ __global__ void __launch_bounds__(NT) bwd_kernel(const BwdArgs a) {
     }
     __syncthreads();
     // ------------------------------------------------------------ reverse sweep
+    float qn = 0.f, dn = 0.f, un = 0.f;
+    auto fetch_r = [&](int t) {
+        const size_t r = rowidx(t);
+        if (tid < DK) {
+            qn = to_f32(q[r * DK + tid]);
+            kn = to_f32(k[r * DK + tid]);
+        }
+        if (tid < DV) {
+            vn = to_f32(v[r * DV + tid]);
+            dn = a.dO[r * DV + tid];
+            un = a.dv[r * DV + tid];  // u_t, left by this same thread in the forward sweep
+        }
+        if (tid == 0) bn = a.beta[r];
+    };
+    if (T > 0) fetch_r(T - 1);
     for (int t = T - 1; t >= 0; --t) {
         const size_t r = rowidx(t);
         if (tid < DK) {
-            qs[tid] = to_f32(q[r * DK + tid]);
-            ks[tid] = to_f32(k[r * DK + tid]);
+            qs[tid] = qn;
+            ks[tid] = kn;
         }
         if (tid < DV) {
-            vs[tid] = to_f32(v[r * DV + tid]);
-            dos[tid] = a.dO[r * DV + tid];
-            us[tid] = a.dv[r * DV + tid];
+            vs[tid] = vn;
+            dos[tid] = dn;
+            us[tid] = un;
         }
+        const float bcur = bn;
         __syncthreads();
+        if (t > 0) fetch_r(t - 1);
         if (wid == 0) {
             float lam = 0.f;
             for (int i = lane; i < DK; i += 32) lam = fmaf(ks[i], ks[i], lam);
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) lam += __shfl_xor_sync(0xffffffffu, lam, off);
             if (lane == 0) {
-                const float bt = a.beta[r];
+                const float bt = bcur;
                 float dfdb, dfdl;
                 gate_grad(bt, lam, a.euler, dfdb, dfdl);
                 sc[0] = efla_alpha(bt, lam, a.euler);
@@ -218,7 +246,7 @@ __global__ void __launch_bounds__(NT) bwd_kernel(const BwdArgs a) {
 
 template <int DK, int DV>
 constexpr size_t bwd_smem() {
-    return sizeof(float) * (2 * DK * (DV + 1) + 2 * DK + 4 * DV + 2 * (NT / DK) * DK + 2 * (NT / DV) * DV + 16);
+    return sizeof(float) * (2 * DK * (DV + 1) + 2 * DK + 4 * DV + 2 * (NT / DK) * DK + 2 * (NT / DV) * DV + 8 + NT / 32);
 }
 
 template <int DK, int DV, typename TIn>
