@@ -322,8 +322,8 @@ __device__ __forceinline__ void invert_unit_lower(float *At, int pi) {
 __device__ __forceinline__ void issue_gram(uint32_t tmem, uint32_t s_sm, int c, Bars *bars) {
     const uint32_t kq = s_sm + OFF_STAGE + (c % NSTAGE) * STAGE_BYTES;
     const uint32_t idesc = idesc_bf16_f32(128, 64, 0, 0);
-#pragma unroll 1
-    for (int ks = 0; ks < 8; ks = opaque(ks + 1)) {
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
         const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
         mma_bf16(tmem + TM_G, smem_desc(kq + off, 16, 1024), smem_desc(kq + off, 16, 1024), idesc, ks > 0);
     }
@@ -813,6 +813,8 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
         }
     } else if (tid == 256) {
         // ================================ MMA warp (one thread) ================================
+        // Its issue loops are fully unrolled: descriptors fold to constants, which leaves this
+        // thread (sharing its sub-partition with busy warps) fewer instructions per MMA.
         bool ok = true;
         // Gram products of full chunks up to `limit`, each once the prep has read the
         // previous one (one TM_G buffer) and the chunk's tile has landed.
@@ -840,10 +842,10 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
             tc_fence_after();
             {  // [X^T | O^T] = S^T [K; Q]^T: one N = 128 product over the stage's [K; Q] rows
                 const uint32_t idesc = idesc_bf16_f32(128, 128, 0, 0);
-#pragma unroll 1
-                for (int part = 0; part < 2; part = opaque(part + 1))
-#pragma unroll 1
-                    for (int ks = 0; ks < 8; ks = opaque(ks + 1)) {
+#pragma unroll
+                for (int part = 0; part < 2; ++part)
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
                         const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
                         mma_bf16_ts(tmem + TM_X, tmem + TM_SA + part * 64 + ks * 8, smem_desc(kq_s + off, 16, 1024),
                                     idesc, (part | ks) != 0);
@@ -856,8 +858,8 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
                 const uint32_t idesc = idesc_bf16_f32(128, 128, 1, 0);
                 const uint32_t v_s = kq_s + OFF_V;
                 if (mode != 1) {  // (the map from S = I takes v = 0)
-#pragma unroll 1
-                    for (int ks = 0; ks < 4; ks = opaque(ks + 1))
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
                         mma_bf16(tmem + TM_SA, smem_desc(v_s + ks * 2048, 8192, 1024),
                                  smem_desc(tp + ks * 32, 16, 1024), idesc, ks > 0);
                 }
@@ -866,12 +868,12 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
             tc_fence_after();
             {  // u^T = [U1 | U2] + (-X)_hi^T [T''_hi; T''_lo]^T + (-X)_lo^T T''_hi^T  (u = U1 + U2)
                 const uint32_t idesc2 = idesc_bf16_f32(128, 128, 0, 0), idesc1 = idesc_bf16_f32(128, 64, 0, 0);
-#pragma unroll 1
-                for (int ks = 0; ks < 4; ks = opaque(ks + 1))
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
                     mma_bf16_ts(tmem + TM_SA, tmem + TM_X + ks * 8, smem_desc(tp + ks * 32, 16, 1024), idesc2,
                                 mode != 1 || ks > 0);
-#pragma unroll 1
-                for (int ks = 0; ks < 4; ks = opaque(ks + 1))
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
                     mma_bf16_ts(tmem + TM_SA, tmem + TM_X + 32 + ks * 8, smem_desc(tp + ks * 32, 16, 1024), idesc1, 1);
                 mma_commit(&bars->u_done);
             }
@@ -882,10 +884,10 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
             tc_fence_after();
             {  // S^T += u^T K  (the chain), then O^T += u^T P^T
                 const uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 1);
-#pragma unroll 1
-                for (int part = 0; part < 2; part = opaque(part + 1))
-#pragma unroll 1
-                    for (int ks = 0; ks < 4; ks = opaque(ks + 1))
+#pragma unroll
+                for (int part = 0; part < 2; ++part)
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
                         mma_bf16_ts(tmem + TM_S, tmem + TM_X + part * 32 + ks * 8,
                                     smem_desc(kq_s + ks * 2048, 16384, 1024), idesc_s, 1);
                 mma_commit(&bars->s_done);
@@ -893,11 +895,11 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
                 // [O^T | O_b^T] += u_hi^T [P_hi; P_lo]^T (N = 128), then O^T += u_lo^T P_hi^T
                 const uint32_t idesc_o2 = idesc_bf16_f32(128, 128, 0, 0), idesc_o1 = idesc_bf16_f32(128, 64, 0, 0);
                 if (write_o) {
-#pragma unroll 1
-                    for (int ks = 0; ks < 4; ks = opaque(ks + 1))
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
                         mma_bf16_ts(tmem + TM_O, tmem + TM_X + ks * 8, smem_desc(pb + ks * 32, 16, 1024), idesc_o2, 1);
-#pragma unroll 1
-                    for (int ks = 0; ks < 4; ks = opaque(ks + 1))
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
                         mma_bf16_ts(tmem + TM_O, tmem + TM_X + 32 + ks * 8, smem_desc(pb + ks * 32, 16, 1024),
                                     idesc_o1, 1);
                 }
