@@ -12,13 +12,16 @@
 //   dbeta = dalpha df/dbeta;  dk += 2 dalpha df/dlambda k;
 // and dS0 = G at the start of the sequence.
 //
-// One CTA of 1024 threads per (sequence, head), fp32 on CUDA cores.  S and G live
-// in shared memory (rows padded to DV + 1 floats).  A forward sweep leaves u_t of
-// every token in the dv output (the reverse sweep overwrites it with dv_t after
-// reading it) and S_T in shared memory; the reverse sweep rebuilds
-// S_{t-1} = S_t - k_t u_t^T token by token.  Row sums (over d_v) use the mapping
-// thread = (row, column group), column sums (over d_k) thread = (column, row
-// group); both walk shared memory without bank conflicts.
+// One CTA of 1024 threads per (sequence, head), fp32 on CUDA cores.  S and G are
+// held in registers as a 32 x 32 grid of tiles (thread (ti, tj) = (warp, lane)
+// owns rows ti*DK/32.., columns tj*DV/32..), so every per-element update is
+// register arithmetic.  Row sums (over d_v) and column sums (over d_k) go through
+// shared memory once per tile: each thread writes one partial per row (column)
+// of its tile, then DK (DV) threads add the 32 partials of a row (column).
+// A forward sweep recomputes the states and leaves u_t of every token in the dv
+// output (the reverse sweep reads it back before overwriting it with dv_t); the
+// reverse sweep rebuilds S_{t-1} = S_t - k_t u_t^T.  Each token's inputs are
+// loaded one token ahead.
 #include "internal.cuh"
 
 namespace efla {
@@ -46,36 +49,44 @@ __device__ __forceinline__ void gate_grad(float beta, float lam, int euler, floa
     }
 }
 
+template <int DK, int DV>
+struct BwdSmem {
+    static constexpr int RP = 33;                          // row partials [DK][RP] (padded)
+    static constexpr size_t vec = 2 * DK + 4 * DV;         // q, k | v, do, u, dx
+    static constexpr size_t rowp = 2 * (size_t)DK * RP;    // two quantities
+    static constexpr size_t colp = 2 * 32 * (size_t)DV;    // two quantities
+    static constexpr size_t sums = 2 * DK + 2 * DV;
+    static constexpr size_t bytes = sizeof(float) * (vec + rowp + colp + sums + 8 + NT / 32);
+};
+
 template <int DK, int DV, typename TIn>
-__global__ void __launch_bounds__(NT) bwd_kernel(const BwdArgs a) {
-    constexpr int LD = DV + 1;
-    constexpr int CGR = NT / DK, CPR = DV / CGR;  // row mapping: column groups per row, columns each
-    constexpr int RGC = NT / DV, RPC = DK / RGC;  // column mapping: row groups per column, rows each
-    extern __shared__ float smf[];
-    float *S = smf, *G = S + DK * LD;
-    float *qs = G + DK * LD, *ks = qs + DK, *vs = ks + DK, *dos = vs + DV, *us = dos + DV, *dxs = us + DV;
-    float *rr = dxs + DV;        // [2][CGR][DK] row partials
-    float *rc = rr + 2 * CGR * DK;  // [2][RGC][DV] column partials
-    float *sc = rc + 2 * RGC * DV;  // [8] scalars, [NT / 32] warp partials
+__global__ void __launch_bounds__(NT, 1) bwd_kernel(const BwdArgs a) {
+    constexpr int RT = DK / 32, CT = DV / 32;  // tile of S / G per thread
+    using L = BwdSmem<DK, DV>;
+    extern __shared__ __align__(16) float smf[];
+    float *qs = smf, *ks = qs + DK, *vs = ks + DK, *dos = vs + DV, *us = dos + DV, *dxs = us + DV;
+    float *rowp = dxs + DV;                 // [2][DK][RP]
+    float *colp = rowp + L::rowp;           // [2][32][DV]
+    float *rsum = colp + L::colp;           // [2][DK]
+    float *csum = rsum + 2 * DK;            // [2][DV]
+    float *sc = csum + 2 * DV;              // [8] scalars, [NT/32] warp partials
 
     const TIn *q = static_cast<const TIn *>(a.q), *k = static_cast<const TIn *>(a.k),
               *v = static_cast<const TIn *>(a.v);
     const int unit = blockIdx.x, b = unit / a.H, h = unit % a.H;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    const int ri = tid % DK, cg = tid / DK;   // row mapping
-    const int cj = tid % DV, rg = tid / DV;   // column mapping
+    const int ti = wid, tj = lane, r0 = ti * RT, c0 = tj * CT;
     const size_t mat = (size_t)DK * DV;
     const int T = a.T;
     auto rowidx = [&](int t) { return ((size_t)b * T + t) * a.H + h; };
 
-    // S = S0
-    for (int e = tid; e < DK * DV; e += NT) {
-        const int i = e / DV, j = e % DV;
-        S[i * LD + j] = a.S0 ? a.S0[(size_t)unit * mat + e] : 0.f;
-    }
-    __syncthreads();
+    float S[RT][CT], G[RT][CT];
+#pragma unroll
+    for (int r = 0; r < RT; ++r)
+#pragma unroll
+        for (int c = 0; c < CT; ++c) S[r][c] = a.S0 ? a.S0[(size_t)unit * mat + (size_t)(r0 + r) * DV + c0 + c] : 0.f;
+
     // ------------------------------------------------------------ forward sweep
-    // (each token's inputs are loaded one token ahead, so their latency is hidden)
     float kn = 0.f, vn = 0.f, bn = 0.f;
     auto fetch_f = [&](int t) {
         const size_t r = rowidx(t);
@@ -86,10 +97,11 @@ __global__ void __launch_bounds__(NT) bwd_kernel(const BwdArgs a) {
     if (T > 0) fetch_f(0);
     for (int t = 0; t < T; ++t) {
         const size_t r = rowidx(t);
+        __syncthreads();  // the previous token's update has read k and u
         if (tid < DK) ks[tid] = kn;
         if (tid < DV) vs[tid] = vn;
         const float bcur = bn;
-        __syncthreads();
+        __syncthreads();  // this token's k, v visible
         if (t + 1 < T) fetch_f(t + 1);
         if (wid == 0) {
             float lam = 0.f;
@@ -98,29 +110,34 @@ __global__ void __launch_bounds__(NT) bwd_kernel(const BwdArgs a) {
             for (int off = 16; off > 0; off >>= 1) lam += __shfl_xor_sync(0xffffffffu, lam, off);
             if (lane == 0) sc[0] = efla_alpha(bcur, lam, a.euler);
         }
-        float xp = 0.f;  // x_j over this thread's rows
-#pragma unroll 8
-        for (int i = rg * RPC; i < (rg + 1) * RPC; ++i) xp = fmaf(S[i * LD + cj], ks[i], xp);
-        rc[rg * DV + cj] = xp;
+#pragma unroll
+        for (int c = 0; c < CT; ++c) {  // x = S^T k: this tile's column partials
+            float px = 0.f;
+#pragma unroll
+            for (int rr = 0; rr < RT; ++rr) px = fmaf(S[rr][c], ks[r0 + rr], px);
+            colp[ti * DV + c0 + c] = px;
+        }
         __syncthreads();
         if (tid < DV) {
             float x = 0.f;
-#pragma unroll
-            for (int g = 0; g < RGC; ++g) x += rc[g * DV + tid];
+#pragma unroll 8
+            for (int tt = 0; tt < 32; ++tt) x += colp[tt * DV + tid];
             const float u = sc[0] * (vs[tid] - x);
             us[tid] = u;
-            a.dv[r * DV + tid] = u;  // kept for the reverse sweep
+            a.dv[r * DV + tid] = u;  // kept for the reverse sweep (read back by this thread)
         }
-        __syncthreads();
-        for (int i = rg * RPC; i < (rg + 1) * RPC; ++i) S[i * LD + cj] = fmaf(ks[i], us[cj], S[i * LD + cj]);
-        __syncthreads();
+        __syncthreads();  // u visible
+#pragma unroll
+        for (int rr = 0; rr < RT; ++rr)
+#pragma unroll
+            for (int c = 0; c < CT; ++c) S[rr][c] = fmaf(ks[r0 + rr], us[c0 + c], S[rr][c]);
     }
     // G = dS_T
-    for (int e = tid; e < DK * DV; e += NT) {
-        const int i = e / DV, j = e % DV;
-        G[i * LD + j] = a.dST ? a.dST[(size_t)unit * mat + e] : 0.f;
-    }
-    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < RT; ++r)
+#pragma unroll
+        for (int c = 0; c < CT; ++c) G[r][c] = a.dST ? a.dST[(size_t)unit * mat + (size_t)(r0 + r) * DV + c0 + c] : 0.f;
+
     // ------------------------------------------------------------ reverse sweep
     float qn = 0.f, dn = 0.f, un = 0.f;
     auto fetch_r = [&](int t) {
@@ -132,13 +149,14 @@ __global__ void __launch_bounds__(NT) bwd_kernel(const BwdArgs a) {
         if (tid < DV) {
             vn = to_f32(v[r * DV + tid]);
             dn = a.dO[r * DV + tid];
-            un = a.dv[r * DV + tid];  // u_t, left by this same thread in the forward sweep
+            un = a.dv[r * DV + tid];  // u_t, written by this same thread in the forward sweep
         }
         if (tid == 0) bn = a.beta[r];
     };
     if (T > 0) fetch_r(T - 1);
     for (int t = T - 1; t >= 0; --t) {
         const size_t r = rowidx(t);
+        __syncthreads();  // the previous token is done with every shared array
         if (tid < DK) {
             qs[tid] = qn;
             ks[tid] = kn;
@@ -149,7 +167,7 @@ __global__ void __launch_bounds__(NT) bwd_kernel(const BwdArgs a) {
             us[tid] = un;
         }
         const float bcur = bn;
-        __syncthreads();
+        __syncthreads();  // this token's vectors visible
         if (t > 0) fetch_r(t - 1);
         if (wid == 0) {
             float lam = 0.f;
@@ -157,101 +175,116 @@ __global__ void __launch_bounds__(NT) bwd_kernel(const BwdArgs a) {
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) lam += __shfl_xor_sync(0xffffffffu, lam, off);
             if (lane == 0) {
-                const float bt = bcur;
                 float dfdb, dfdl;
-                gate_grad(bt, lam, a.euler, dfdb, dfdl);
-                sc[0] = efla_alpha(bt, lam, a.euler);
+                gate_grad(bcur, lam, a.euler, dfdb, dfdl);
+                sc[0] = efla_alpha(bcur, lam, a.euler);
                 sc[1] = dfdb;
                 sc[2] = dfdl;
             }
         }
-        {  // rows: dq = S_t do; G += q do^T; dk1 = G u; S_{t-1} = S_t - k u^T
-            const float qi = qs[ri], ki = ks[ri];
-            float dq = 0.f, dk1 = 0.f;
-#pragma unroll 8
-            for (int j = cg * CPR; j < (cg + 1) * CPR; ++j) {
-                const float s = S[ri * LD + j], dj = dos[j], uj = us[j];
-                const float g = fmaf(qi, dj, G[ri * LD + j]);
-                dq = fmaf(s, dj, dq);
-                dk1 = fmaf(g, uj, dk1);
-                S[ri * LD + j] = fmaf(-ki, uj, s);
-                G[ri * LD + j] = g;
+        // rows: dq = S_t do; G += q do^T; dk1 = G u; S_{t-1} = S_t - k u^T;
+        // then columns: du = G^T k; x = S_{t-1}^T k
+        {
+            float pdq[RT], pdk[RT];
+#pragma unroll
+            for (int rr = 0; rr < RT; ++rr) {
+                const float qi = qs[r0 + rr], ki = ks[r0 + rr];
+                float dq = 0.f, dk1 = 0.f;
+#pragma unroll
+                for (int c = 0; c < CT; ++c) {
+                    const float dj = dos[c0 + c], uj = us[c0 + c];
+                    const float g = fmaf(qi, dj, G[rr][c]);
+                    dq = fmaf(S[rr][c], dj, dq);
+                    dk1 = fmaf(g, uj, dk1);
+                    S[rr][c] = fmaf(-ki, uj, S[rr][c]);
+                    G[rr][c] = g;
+                }
+                pdq[rr] = dq;
+                pdk[rr] = dk1;
             }
-            rr[cg * DK + ri] = dq;
-            rr[CGR * DK + cg * DK + ri] = dk1;
+#pragma unroll
+            for (int rr = 0; rr < RT; ++rr) {
+                rowp[(r0 + rr) * L::RP + tj] = pdq[rr];
+                rowp[(DK + r0 + rr) * L::RP + tj] = pdk[rr];
+            }
+#pragma unroll
+            for (int c = 0; c < CT; ++c) {
+                float du = 0.f, x = 0.f;
+#pragma unroll
+                for (int rr = 0; rr < RT; ++rr) {
+                    du = fmaf(G[rr][c], ks[r0 + rr], du);
+                    x = fmaf(S[rr][c], ks[r0 + rr], x);
+                }
+                colp[ti * DV + c0 + c] = du;
+                colp[(32 + ti) * DV + c0 + c] = x;
+            }
         }
         __syncthreads();
-        {  // columns: du = G^T k; x = S_{t-1}^T k
-            float du = 0.f, x = 0.f;
+        if (tid < 2 * DV) {  // column sums: du, x
+            const int qn2 = tid / DV, j = tid % DV;
+            float s = 0.f;
 #pragma unroll 8
-            for (int i = rg * RPC; i < (rg + 1) * RPC; ++i) {
-                du = fmaf(G[i * LD + cj], ks[i], du);
-                x = fmaf(S[i * LD + cj], ks[i], x);
-            }
-            rc[rg * DV + cj] = du;
-            rc[RGC * DV + rg * DV + cj] = x;
+            for (int tt = 0; tt < 32; ++tt) s += colp[(qn2 * 32 + tt) * DV + j];
+            csum[qn2 * DV + j] = s;
+        }
+        if (tid < 2 * DK) {  // row sums: dq, dk1
+            const float *pp = rowp + tid * L::RP;
+            float s = 0.f;
+#pragma unroll 8
+            for (int j = 0; j < 32; ++j) s += pp[j];
+            rsum[tid] = s;
         }
         __syncthreads();
         float dap = 0.f;
         if (tid < DV) {
-            float du = 0.f, x = 0.f;
-#pragma unroll
-            for (int g = 0; g < RGC; ++g) {
-                du += rc[g * DV + tid];
-                x += rc[RGC * DV + g * DV + tid];
-            }
-            const float al = sc[0];
+            const float du = csum[tid], x = csum[DV + tid], al = sc[0];
             a.dv[r * DV + tid] = al * du;
             dxs[tid] = -al * du;
             dap = du * (vs[tid] - x);
         }
+        if (tid < DK) a.dq[r * DK + tid] = rsum[tid];
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) dap += __shfl_xor_sync(0xffffffffu, dap, off);
         if (lane == 0) sc[8 + wid] = dap;
+        __syncthreads();  // dx visible
+        {  // rows: dk2 = S_{t-1} dx;  G += k dx^T
+#pragma unroll
+            for (int rr = 0; rr < RT; ++rr) {
+                const float ki = ks[r0 + rr];
+                float acc = 0.f;
+#pragma unroll
+                for (int c = 0; c < CT; ++c) {
+                    const float dx = dxs[c0 + c];
+                    acc = fmaf(S[rr][c], dx, acc);
+                    G[rr][c] = fmaf(ki, dx, G[rr][c]);
+                }
+                rowp[(r0 + rr) * L::RP + tj] = acc;
+            }
+        }
         __syncthreads();
-        {  // rows: dk2 = S_{t-1} dx; G += k dx^T
-            const float ki = ks[ri];
+        if (tid < DK) {
+            float da = 0.f;
+#pragma unroll
+            for (int w = 0; w < (DV + 31) / 32; ++w) da += sc[8 + w];  // only warps holding columns contribute
+            const float *pp = rowp + tid * L::RP;
             float dk2 = 0.f;
 #pragma unroll 8
-            for (int j = cg * CPR; j < (cg + 1) * CPR; ++j) {
-                const float dx = dxs[j];
-                dk2 = fmaf(S[ri * LD + j], dx, dk2);
-                G[ri * LD + j] = fmaf(ki, dx, G[ri * LD + j]);
-            }
-            rr[CGR * DK + cg * DK + ri] += dk2;
+            for (int j = 0; j < 32; ++j) dk2 += pp[j];
+            a.dk[r * DK + tid] = fmaf(2.f * da * sc[2], ks[tid], rsum[DK + tid] + dk2);
+            if (tid == 0) a.dbeta[r] = da * sc[1];
         }
-        __syncthreads();
-        float da = 0.f;
-#pragma unroll
-        for (int w = 0; w < NT / 32; ++w) da += sc[8 + w];
-        if (tid < DK) {
-            float dq = 0.f, dk = 0.f;
-#pragma unroll
-            for (int g = 0; g < CGR; ++g) {
-                dq += rr[g * DK + tid];
-                dk += rr[CGR * DK + g * DK + tid];
-            }
-            a.dq[r * DK + tid] = dq;
-            a.dk[r * DK + tid] = fmaf(2.f * da * sc[2], ks[tid], dk);
-        }
-        if (tid == 0) a.dbeta[r] = da * sc[1];
-        __syncthreads();
     }
-    if (a.dS0)
-        for (int e = tid; e < DK * DV; e += NT) {
-            const int i = e / DV, j = e % DV;
-            a.dS0[(size_t)unit * mat + e] = G[i * LD + j];
-        }
-}
-
-template <int DK, int DV>
-constexpr size_t bwd_smem() {
-    return sizeof(float) * (2 * DK * (DV + 1) + 2 * DK + 4 * DV + 2 * (NT / DK) * DK + 2 * (NT / DV) * DV + 8 + NT / 32);
+    if (a.dS0) {
+#pragma unroll
+        for (int rr = 0; rr < RT; ++rr)
+#pragma unroll
+            for (int c = 0; c < CT; ++c) a.dS0[(size_t)unit * mat + (size_t)(r0 + rr) * DV + c0 + c] = G[rr][c];
+    }
 }
 
 template <int DK, int DV, typename TIn>
 cudaError_t bwd_launch(const BwdArgs &a) {
-    constexpr size_t smem = bwd_smem<DK, DV>();
+    constexpr size_t smem = BwdSmem<DK, DV>::bytes;
     static bool attr[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
