@@ -186,22 +186,6 @@ __device__ __forceinline__ void split_pack(const float *x, uint32_t *hi, uint32_
     }
 }
 
-__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&r)[64]) {
-    float a[32], b[32];
-    tmem_ld32(taddr, a);
-    tmem_ld32(taddr + 32, b);
-    tmem_ld_wait();
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        r[i] = a[i];
-        r[32 + i] = b[i];
-    }
-}
-
-__device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t (&u)[32]) {
-    tmem_st32(taddr, reinterpret_cast<const float(&)[32]>(u));
-}
-
 // T~ = (I + A~)^{-1} in place in At (fp32, row stride AT_LD), by the 256
 // threads of the two prep warpgroups (index pi).  The scratch Y of the products
 // lives in the upper-right 32x32 block of At, which the inverse never reads.
