@@ -76,8 +76,8 @@ constexpr uint32_t OFF_TPP = NSTAGE * STAGE_BYTES;
 constexpr uint32_t TPP_BYTES = 32768;
 constexpr uint32_t OFF_AT = OFF_TPP + 2 * TPP_BYTES;  // fp32 [64][68]: A~, then T~ in place (rows 16-byte aligned)
 constexpr uint32_t AT_LD = 68;
-constexpr uint32_t OFF_ROW = OFF_AT + 64 * AT_LD * 4;  // fp32: invn[64], gn[64], beta[64]
-constexpr uint32_t ROW_BYTES = 3 * 64 * 4;
+constexpr uint32_t OFF_ROW = OFF_AT + 64 * AT_LD * 4;  // fp32: invn[64], gn[64]
+constexpr uint32_t ROW_BYTES = 2 * 64 * 4;
 constexpr uint32_t OFF_BAR = OFF_ROW + ROW_BYTES;       // mbarriers (struct Bars)
 constexpr uint32_t OFF_MISC = OFF_BAR + 224;            // tmem base (u32), abort flag (i32)
 constexpr uint32_t SMEM_USED = OFF_MISC + 16;
@@ -133,14 +133,14 @@ struct Bars {
     uint64_t s_done;         // S^T += u^T K
     uint64_t o_done;         // O^T of the chunk complete
     uint64_t prep_ready[2];  // T', P, gate terms and the zeroed tail of a chunk written
-    uint64_t chunk_done[2];  // every MMA of a chunk complete: its stage and buffers are free
     uint64_t sa_ready;       // state warpgroup wrote S^T hi/lo        (128 arrivals)
     uint64_t o_free;         // state warpgroup read O^T of the chunk  (128 arrivals)
     uint64_t r_ready;        // state warpgroup wrote (V - X)^T hi/lo  (128 arrivals)
     uint64_t u_ready;        // state warpgroup wrote u^T hi/lo        (128 arrivals)
     uint64_t drain[2];       // all MMAs of the MMA thread / of the prep thread complete
     uint64_t s_free[NSTAGE];  // the state update of a chunk complete: its K/Q/V stage is free
-    uint64_t ost_free[2];     // the TMA stores of a chunk's o tile have read it (4 arrivals)
+    uint64_t ost_free[2];     // a chunk's T''/P buffer is free: its last products and the TMA
+                              // stores of its o tile have read it (4 arrivals)
 };
 static_assert(sizeof(Bars) <= 224, "mbarrier block exceeds its slot");
 
@@ -192,33 +192,38 @@ __device__ __forceinline__ void split_pack(const float *x, uint32_t *hi, uint32_
 // Each step applies
 //   [[L1, 0], [B, L2]]^{-1} = [[L1^{-1}, 0], [-L2^{-1} B L1^{-1}, L2^{-1}]]
 // for unit lower-triangular L1, L2:
-//   1. the four diagonal 16x16 blocks by column substitution (two warps per
-//      block, eight columns per warp, four lanes per column splitting its rows by
-//      residue mod 4);
+//   1. the four diagonal 16x16 blocks by column substitution: warps 0 and 1 of the
+//      prep, two blocks per warp, one lane per column holding the whole column in
+//      registers (no shuffles; the other warps wait at the barrier);
 //   2. blocks (1,0) and (3,2) of 16:  T~_IJ = -T~_II (A~_IJ T~_JJ);
 //   3. the lower-left 32x32 block:    T~_21 = -T~_22 (A~_21 T~_11)  (32x32 blocks).
 // Steps 2 and 3 are register-tiled fp32 products.
 __device__ __forceinline__ void invert_unit_lower(float *At, int pi) {
     float *Y = At + 32;  // [32][AT_LD] rows 0-31, columns 32-63
     const int lane = pi & 31, pw = pi >> 5;
-    {
-        const int B0 = (pw >> 1) * 16, c = (lane & 7) + 8 * (pw & 1), r4 = lane >> 3;
-        float col[4];  // col[m] = T~[B0 + 4m + r4][B0 + c]
+    if (pw < 2) {
+        const int B0 = 16 * (2 * pw + (lane >> 4)), c = lane & 15;
+        float col[16];  // col[s] = T~[B0 + s][B0 + c]
 #pragma unroll
-        for (int m = 0; m < 4; ++m) col[m] = (4 * m + r4 == c) ? 1.f : 0.f;
+        for (int s = 0; s < 16; ++s) col[s] = s == c ? 1.f : 0.f;
 #pragma unroll
         for (int t = 1; t < 16; ++t) {
-            const float *row = At + (B0 + t) * AT_LD + B0 + r4;
+            const float *row = At + (B0 + t) * AT_LD + B0;
+            asm volatile("" : "+l"(row));  // keeps each step's loads in that step (register pressure)
             float acc = 0.f;
 #pragma unroll
-            for (int m = 0; m < (t + 3) / 4; ++m) acc = fmaf(row[4 * m], col[m], acc);  // A~[t][s >= t] = 0
-            float tot = acc + __shfl_xor_sync(0xffffffffu, acc, 8);
-            tot += __shfl_xor_sync(0xffffffffu, tot, 16);
-            if ((t & 3) == r4 && t > c) col[t >> 2] = -tot;
+            for (int s4 = 0; s4 < t; s4 += 4) {  // A~[t][s] for s < t; col[s] = 0 for s < c
+                const float4 a = *reinterpret_cast<const float4 *>(row + s4);
+                acc = fmaf(a.x, col[s4], acc);
+                if (s4 + 1 < t) acc = fmaf(a.y, col[s4 + 1], acc);
+                if (s4 + 2 < t) acc = fmaf(a.z, col[s4 + 2], acc);
+                if (s4 + 3 < t) acc = fmaf(a.w, col[s4 + 3], acc);
+            }
+            col[t] = t > c ? -acc : col[t];
         }
-        named_bar(BAR_PREP, 256);  // both warps of the block have read A~_BB
+        __syncwarp();  // both blocks of this warp have been read
 #pragma unroll
-        for (int m = 0; m < 4; ++m) At[(B0 + 4 * m + r4) * AT_LD + B0 + c] = col[m];
+        for (int s = 0; s < 16; ++s) At[(B0 + s) * AT_LD + B0 + c] = col[s];
     }
     named_bar(BAR_PREP, 256);
     {
@@ -320,7 +325,6 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float *row_invn = reinterpret_cast<float *>(sm + OFF_ROW);  // [64] 1/n_t
     float *row_gn = row_invn + 64;                              // [64] gamma_t/n_t
-    float *row_beta = row_invn + 128;                           // [64]
     float *At = reinterpret_cast<float *>(sm + OFF_AT);
     Bars *bars = reinterpret_cast<Bars *>(sm + OFF_BAR);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + OFF_MISC);
@@ -397,8 +401,6 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
         mbar_init(&bars->o_done, 1);
         mbar_init(&bars->prep_ready[0], 1);
         mbar_init(&bars->prep_ready[1], 1);
-        mbar_init(&bars->chunk_done[0], 1);
-        mbar_init(&bars->chunk_done[1], 1);
         mbar_init(&bars->sa_ready, 128);
         mbar_init(&bars->o_free, 128);
         mbar_init(&bars->r_ready, 128);
@@ -430,11 +432,13 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
         const int col0 = half * 32;
         const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
         const bool leader = pi == 0;  // signals the other roles
-        // beta of the next chunk is loaded a chunk ahead (its latency hides behind the prep)
+        // The thread that reads the Gram diagonal of row t computes that row's gate terms;
+        // it loads beta_t itself, a chunk ahead (its latency hides behind the prep).
+        const bool gate_thr = row < C && (row >> 5) == half;
         auto load_beta = [&](int cc) {
             const long t0n = bos + (long)cc * C;
-            return (cc < nchunks && pi < C && t0n + pi < eos)
-                       ? p.beta[((size_t)b * p.T + (size_t)(t0n + pi)) * p.H + h] : 0.f;
+            return (cc < nchunks && gate_thr && t0n + row < eos)
+                       ? p.beta[((size_t)b * p.T + (size_t)(t0n + row)) * p.H + h] : 0.f;
         };
         float beta_next = load_beta(0);
         for (int c = 0; c < nchunks; ++c) {
@@ -443,33 +447,38 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
             const int valid = (int)min((long)C, eos - tok0);
             uint8_t *KQ = sm + OFF_STAGE + st * STAGE_BYTES;
 
-            if (pi < C) row_beta[pi] = beta_next;
+            const float beta_t = beta_next;
             beta_next = load_beta(c + 1);
-            bool ok = wait_bar(&bars->tma_full[st], (c / NSTAGE) & 1, abort_flag);
-            if (ok && valid < C) {  // rows past the end of the sequence are zeroed (they may hold the next one)
-                const int rows = C - valid;
-                for (int e = pi; e < 4 * rows * 8; e += 256) {
-                    const int ch = e & 7, r = (e >> 3) % rows, part = (e >> 3) / rows;
-                    const int R = valid + r + ((part >> 1) ? 64 : 0), cb = part & 1;
-                    *reinterpret_cast<uint4 *>(KQ + cb * 16384 + (R >> 3) * 1024 + (R & 7) * 128 + ch * 16) =
-                        make_uint4(0, 0, 0, 0);
+            bool ok = true;
+            // Gram products G = [K;Q] K^T: the MMA thread issues a full chunk's once its stage
+            // has landed (the prep reads nothing else of the stage); a partial chunk's tail is
+            // zeroed here first (those rows may hold the next sequence) and its product issued
+            // by the prep
+            if (valid < C) {
+                ok = wait_bar(&bars->tma_full[st], (c / NSTAGE) & 1, abort_flag);
+                if (ok) {
+                    const int rows = C - valid;
+                    for (int e = pi; e < 4 * rows * 8; e += 256) {
+                        const int ch = e & 7, r = (e >> 3) % rows, part = (e >> 3) / rows;
+                        const int R = valid + r + ((part >> 1) ? 64 : 0), cb = part & 1;
+                        *reinterpret_cast<uint4 *>(KQ + cb * 16384 + (R >> 3) * 1024 + (R & 7) * 128 + ch * 16) =
+                            make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
                 }
-                fence_proxy_async_smem();
-            }
-            if (named_bar_any(BAR_PREP, 256, !ok || *abort_flag)) {
-                *abort_flag = 1;
-                break;
-            }
-
-            // Gram products G = [K;Q] K^T: issued by the MMA thread ahead of time, except for
-            // a partial chunk, whose tail must be zeroed first
-            if (leader && valid < C) {
-                tc_fence_after();
-                issue_gram(tmem, s_sm, c, bars);
+                if (named_bar_any(BAR_PREP, 256, !ok || *abort_flag)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                if (leader) {
+                    tc_fence_after();
+                    issue_gram(tmem, s_sm, c, bars);
+                }
             }
             ok = wait_bar(&bars->g_done, c & 1, abort_flag);
-            // the P buffer of this chunk was last read by chunk c-2's products
-            if (c >= 2) ok = wait_bar(&bars->chunk_done[c & 1], ((c - 2) >> 1) & 1, abort_flag) && ok;
+            // This chunk's T''/P buffer was last read by chunk c-2's products (P) and o stores
+            // (T'' part); the state warpgroup releases it after both.
+            if (c >= 2) ok = wait_bar(&bars->ost_free[c & 1], ((c - 2) >> 1) & 1, abort_flag) && ok;
             tc_fence_after();
             {
                 float g[32];
@@ -484,12 +493,15 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
                     for (int s = 0; s < 32; ++s) lam = (s == (t & 31)) ? g[s] : lam;
                     const bool live = t < valid && lam > 0.f;
                     const float invn = live ? rsqrtf(lam) : 0.f;
-                    const float gam = !live ? 0.f : p.euler ? row_beta[t] * lam : -expm1f(-row_beta[t] * lam);
+                    const float gam = !live ? 0.f : p.euler ? beta_t * lam : -expm1f(-beta_t * lam);
                     row_invn[t] = invn;
                     row_gn[t] = gam * invn;
                 }
                 // [gate: terms computed]
-                named_bar(BAR_PREP, 256);
+                if (named_bar_any(BAR_PREP, 256, !ok || *abort_flag)) {  // also spreads an abort
+                    *abort_flag = 1;
+                    break;
+                }
                 // [gate: barrier passed]
                 if (leader) mbar_arrive(&bars->g_free);  // every row of G has been read
                 if (row < C) {  // A~[t][col0 .. col0+31]
@@ -530,8 +542,6 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
             }
             named_bar(BAR_PREP, 256);
             invert_unit_lower(At, pi);
-            // the T'' buffer of this chunk held chunk c-2's o tile until its TMA stores had read it
-            if (c >= 2) ok = wait_bar(&bars->ost_free[c & 1], ((c - 2) >> 1) & 1, abort_flag) && ok;
             {  // T'' = diag(1/n) T~ diag(gamma/n), lower triangle, as bf16 hi/lo [t][s]
                 const int t = pi >> 2, s0 = (pi & 3) * 16;
                 uint8_t *hi = sm + OFF_TPP + buf * TPP_BYTES, *lo = hi + 8192;
@@ -559,7 +569,7 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
             fence_proxy_async_smem();
             named_bar(BAR_PREP, 256);
             if (leader) mbar_arrive(&bars->prep_ready[buf]);
-            if (!ok) *abort_flag = 1;  // seen by every prep thread at the next chunk's first barrier
+            if (!ok) *abort_flag = 1;  // seen by every prep thread at the next chunk's gate barrier
         }
         if (leader) {  // every Gram MMA has completed before TMEM is released (bounded)
             mma_commit(&bars->drain[1]);
@@ -817,10 +827,11 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
             const int st = c % NSTAGE, buf = c & 1;
             const uint32_t kq_s = s_sm + OFF_STAGE + st * STAGE_BYTES;
             const uint32_t tp = s_sm + OFF_TPP + buf * TPP_BYTES, pb = tp + 16384;
-            if (!(ok = wait_bar(&bars->prep_ready[buf], (c >> 1) & 1, abort_flag))) break;
-            tc_fence_after();
-            issue_grams(c + 1);
-            if (!ok) break;
+            // X needs the stage and the state only; a partial chunk also needs its zeroed tail,
+            // which its prep writes before prep_ready
+            const bool partial = eos - (bos + (long)c * C) < C;
+            if (!(ok = wait_bar(partial ? &bars->prep_ready[buf] : &bars->tma_full[st],
+                                partial ? (c >> 1) & 1 : (c / NSTAGE) & 1, abort_flag))) break;
             if (!(ok = wait_bar(&bars->sa_ready, c & 1, abort_flag))) break;
             if (c > 0 && !(ok = wait_bar(&bars->o_free, (c - 1) & 1, abort_flag))) break;
             tc_fence_after();
@@ -836,6 +847,11 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
                     }
                 mma_commit(&bars->x_done);
             }
+            // the rest of the chunk needs its prep (T'', P)
+            if (!(ok = wait_bar(&bars->prep_ready[buf], (c >> 1) & 1, abort_flag))) break;
+            tc_fence_after();
+            issue_grams(c + 1);
+            if (!ok) break;
             {  // [U1 | U2] = V^T [T''_hi; T''_lo]^T while the state warpgroup forms -X.  It
                // overwrites the S^T operand columns, which the products above (issued
                // earlier, executed in order) have already read.
@@ -888,7 +904,6 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
                                     idesc_o1, 1);
                 }
                 mma_commit(&bars->o_done);
-                mma_commit(&bars->chunk_done[c & 1]);
             }
         }
         if (!ok) *abort_flag = 1;
