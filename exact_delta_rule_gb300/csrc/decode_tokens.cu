@@ -16,47 +16,54 @@
 // is a short forward substitution over the block, and the state update is the
 // rank-block S_0 + K^T U.  S is read from HBM once per call and written once.
 //
-// One CTA of 256 threads per (b, h); thread (half, j) holds rows
-// half*DK/2 .. +DK/2-1 of column j of S in registers.  Blocks of MB = 16 tokens;
-// K and Q of a block are staged transposed in shared memory ([d][t], read as
-// broadcasts), the Gram terms k_t.k_i and q_t.k_i are formed once per block.
+// One CTA of 256 threads per (b, h).  Thread (rg, cl) holds rows rg*RW .. +RW-1 and the
+// two adjacent columns 2cl, 2cl+1 of S in registers, so each broadcast load of a K^T or Q^T
+// row feeds two columns.  Blocks of MB = 16 tokens; K and Q of a block are staged transposed
+// in shared memory ([d][t], read as broadcasts), the Gram terms k_t.k_i and q_t.k_i are
+// formed once per block, and the partial sums of X and Y of every row group are added in a
+// shared-memory pass (no atomics).
 #include "internal.cuh"
 
 namespace efla {
 namespace {
 
 constexpr int MB = 16;  // tokens per block
+constexpr int KS = MB + 4;  // row stride of the staged K^T, Q^T: rows stay 16-byte aligned and the
+                            // transposing stores (consecutive d, one t) spread over 8 banks
+constexpr int NT = 256;
+constexpr int CW = 2;   // columns of S per thread
+constexpr size_t PART_BYTES = 2 * (size_t)NT * CW * MB * sizeof(float);  // [2][NRG][MB][DV] (64 KB)
 
 template <int DK, int DV, typename TIn, typename TOut>
 __global__ void __launch_bounds__(256, 2) decode_tokens_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k,
                                                             const TIn *__restrict__ v, const float *__restrict__ beta,
                                                             float *__restrict__ S, TOut *__restrict__ o, int m, int H,
                                                             int euler) {
-    constexpr int NT = 256;
-    constexpr int CPT = DV >= 128 ? 1 : 128 / DV;   // columns per thread-half (1 for DV = 128)
-    constexpr int HALVES = 2;
-    static_assert(DV * CPT == 128, "thread layout assumes DV * CPT == 128");
-    constexpr int RPT = DK / HALVES;                 // rows of S per thread
+    constexpr int NCL = DV / CW;   // column lanes per row group
+    constexpr int NRG = NT / NCL;  // row groups
+    constexpr int RW = DK / NRG;   // rows of S per thread
+    static_assert(NCL * NRG == NT && RW * NRG == DK && RW >= 1, "thread layout");
+    static_assert(2 * NRG * MB * DV * sizeof(float) == PART_BYTES, "partial-sum buffer size");
 
-    __shared__ __align__(16) float kT[DK][MB], qT[DK][MB];
-    __shared__ float vs[MB][DV];       // v of the block, then u in place (same thread, same (t, j))
+    __shared__ __align__(16) float kT[DK][KS], qT[DK][KS];
+    __shared__ __align__(16) float vs[MB][DV];  // v of the block, then u in place (same thread, same (t, j))
     __shared__ float gkk[MB][MB + 1], gqk[MB][MB + 1];
     __shared__ float al[MB], bs[MB];
-    __shared__ float red[2][MB][DV];   // partial X and Y of the other row-slices (starts at zero)
+    extern __shared__ __align__(16) float part[];  // [X, Y][row group][t][j]; group 0 then holds the sums
 
     const int unit = blockIdx.x;  // b * H + h
     const int b = unit / H, h = unit % H;
     const int tid = threadIdx.x;
-    const int half = tid / 128, l = tid % 128;
-    const int j = l % DV, csub = l / DV;           // column, and which of the CPT row-slices (DV < 128)
-    // thread (half, l) holds rows [row0, row0 + RPT/CPT) of column j
-    constexpr int R = RPT / CPT;
-    const int row0 = half * RPT + csub * R;
+    const int cl = tid % NCL, rg = tid / NCL;
+    const int c0 = cl * CW, r0 = rg * RW;
     float *Su = S + (size_t)unit * DK * DV;
-    for (int e = tid; e < 2 * MB * DV; e += NT) (&red[0][0][0])[e] = 0.f;
-    float s[R];
+    float s[RW][CW];
 #pragma unroll
-    for (int r = 0; r < R; ++r) s[r] = Su[(size_t)(row0 + r) * DV + j];
+    for (int r = 0; r < RW; ++r) {
+        const float2 x = *reinterpret_cast<const float2 *>(Su + (size_t)(r0 + r) * DV + c0);
+        s[r][0] = x.x;
+        s[r][1] = x.y;
+    }
 
     for (int t0 = 0; t0 < m; t0 += MB) {
         const int mb = min(MB, m - t0);
@@ -90,63 +97,94 @@ __global__ void __launch_bounds__(256, 2) decode_tokens_kernel(const TIn *__rest
         }
         if (tid < MB) bs[tid] = br;
         __syncthreads();
-        // Gram terms: thread (t, i) for t, i < MB
+        // Gram terms k_t.k_i, q_t.k_i: thread (t, i4, dq) forms i = 4 i4 .. 4 i4 + 3 over the
+        // quarter dq of d (rotated by 2 dq rows so that the four quarters hit different banks),
+        // and the four quarters are added across lanes
         {
-            const int t = tid / MB, i = tid % MB;
-            float a = 0.f, c = 0.f;
-#pragma unroll 8
-            for (int d = 0; d < DK; ++d) {
-                const float ki = kT[d][i];
-                a = fmaf(kT[d][t], ki, a);
-                c = fmaf(qT[d][t], ki, c);
+            static_assert(MB == 16 && NT == 256, "Gram thread layout");
+            const int t = tid >> 4, i4 = (tid >> 2) & 3, dq = tid & 3;
+            constexpr int DQ = DK / 4;
+            float a[4] = {0.f, 0.f, 0.f, 0.f}, c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+            for (int dd = 0; dd < DQ; ++dd) {
+                const int d = dq * DQ + ((dd + 2 * dq) & (DQ - 1));
+                const float kt = kT[d][t], qt = qT[d][t];
+                const float4 ki = *reinterpret_cast<const float4 *>(&kT[d][4 * i4]);
+                const float kv[4] = {ki.x, ki.y, ki.z, ki.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    a[e] = fmaf(kt, kv[e], a[e]);
+                    c[e] = fmaf(qt, kv[e], c[e]);
+                }
             }
-            gkk[t][i] = a;
-            gqk[t][i] = c;
-            if (t == i) al[t] = t < mb ? efla_alpha(bs[t], a, euler) : 0.f;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                a[e] += __shfl_xor_sync(0xffffffffu, a[e], 1);
+                a[e] += __shfl_xor_sync(0xffffffffu, a[e], 2);
+                c[e] += __shfl_xor_sync(0xffffffffu, c[e], 1);
+                c[e] += __shfl_xor_sync(0xffffffffu, c[e], 2);
+            }
+            if (dq == 0) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    gkk[t][4 * i4 + e] = a[e];
+                    gqk[t][4 * i4 + e] = c[e];
+                }
+                if ((t >> 2) == i4) {
+                    const int e = t & 3;
+                    const float lam = e == 0 ? a[0] : e == 1 ? a[1] : e == 2 ? a[2] : a[3];
+                    al[t] = t < mb ? efla_alpha(bs[t], lam, euler) : 0.f;
+                }
+            }
         }
-        // X = S_0^T K^T, Y = S_0^T Q^T over this thread's rows
-        float xp[MB], yp[MB];
+        // X = S_0^T K^T, then Y = S_0^T Q^T, over this thread's rows: partial sums per row group
 #pragma unroll
-        for (int t = 0; t < MB; ++t) xp[t] = yp[t] = 0.f;
+        for (int pass = 0; pass < 2; ++pass) {
+            const float(*src)[KS] = pass == 0 ? kT : qT;
+            float acc[MB][CW];
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const float sv = s[r];
-            const float4 *kr = reinterpret_cast<const float4 *>(kT[row0 + r]);
-            const float4 *qr = reinterpret_cast<const float4 *>(qT[row0 + r]);
+            for (int t = 0; t < MB; ++t) acc[t][0] = acc[t][1] = 0.f;
 #pragma unroll
-            for (int t4 = 0; t4 < MB / 4; ++t4) {
-                const float4 a = kr[t4], c = qr[t4];
-                xp[4 * t4] = fmaf(sv, a.x, xp[4 * t4]);
-                xp[4 * t4 + 1] = fmaf(sv, a.y, xp[4 * t4 + 1]);
-                xp[4 * t4 + 2] = fmaf(sv, a.z, xp[4 * t4 + 2]);
-                xp[4 * t4 + 3] = fmaf(sv, a.w, xp[4 * t4 + 3]);
-                yp[4 * t4] = fmaf(sv, c.x, yp[4 * t4]);
-                yp[4 * t4 + 1] = fmaf(sv, c.y, yp[4 * t4 + 1]);
-                yp[4 * t4 + 2] = fmaf(sv, c.z, yp[4 * t4 + 2]);
-                yp[4 * t4 + 3] = fmaf(sv, c.w, yp[4 * t4 + 3]);
+            for (int r = 0; r < RW; ++r) {
+                const float4 *row = reinterpret_cast<const float4 *>(src[r0 + r]);
+#pragma unroll
+                for (int t4 = 0; t4 < MB / 4; ++t4) {
+                    const float4 a = row[t4];
+                    const float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        acc[4 * t4 + e][0] = fmaf(s[r][0], av[e], acc[4 * t4 + e][0]);
+                        acc[4 * t4 + e][1] = fmaf(s[r][1], av[e], acc[4 * t4 + e][1]);
+                    }
+                }
             }
-        }
-        // partial sums of all but the first row-slice go through shared memory
-        if (half == 1 || csub > 0) {
+            float *dst = part + ((size_t)(pass * NRG + rg) * MB) * DV + c0;
 #pragma unroll
-            for (int t = 0; t < MB; ++t) {
-                atomicAdd(&red[0][t][j], xp[t]);
-                atomicAdd(&red[1][t][j], yp[t]);
-            }
+            for (int t = 0; t < MB; ++t)
+                *reinterpret_cast<float2 *>(dst + t * DV) = make_float2(acc[t][0], acc[t][1]);
         }
         __syncthreads();
-        if (half == 0 && csub == 0) {  // one thread per column: the forward substitution
+        // sums over the row groups into group 0 (each entry owned by one thread)
+        for (int e = tid; e < 2 * MB * DV; e += NT) {
+            const int pass = e / (MB * DV), rest = e % (MB * DV);
+            float *p0 = part + (size_t)pass * NRG * MB * DV + rest;
+            float acc = p0[0];
+#pragma unroll
+            for (int g = 1; g < NRG; ++g) acc += p0[(size_t)g * MB * DV];
+            p0[0] = acc;
+        }
+        __syncthreads();
+        if (tid < DV) {  // one thread per column: the forward substitution
+            const int j = tid;
+            const float *X = part, *Y = part + (size_t)NRG * MB * DV;
             float u[MB];
 #pragma unroll
             for (int t = 0; t < MB; ++t) {
-                const float x = xp[t] + red[0][t][j], y = yp[t] + red[1][t][j];
-                red[0][t][j] = 0.f;  // cleared for the next block
-                red[1][t][j] = 0.f;
-                float acc = vs[t][j] - x;
+                float acc = vs[t][j] - X[t * DV + j];
 #pragma unroll
                 for (int i = 0; i < t; ++i) acc = fmaf(-gkk[t][i], u[i], acc);
                 u[t] = al[t] * acc;
-                float ov = y;
+                float ov = Y[t * DV + j];
 #pragma unroll
                 for (int i = 0; i <= t; ++i) ov = fmaf(gqk[t][i], u[i], ov);
                 vs[t][j] = u[t];
@@ -155,31 +193,49 @@ __global__ void __launch_bounds__(256, 2) decode_tokens_kernel(const TIn *__rest
         }
         __syncthreads();
         // S_0 + K^T U over this thread's rows (u of tokens past mb is zero)
-        float uc[MB];
+        float uc[MB][CW];
 #pragma unroll
-        for (int t = 0; t < MB; ++t) uc[t] = vs[t][j];
+        for (int t = 0; t < MB; ++t) {
+            const float2 x = *reinterpret_cast<const float2 *>(&vs[t][c0]);
+            uc[t][0] = x.x;
+            uc[t][1] = x.y;
+        }
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const float4 *kr = reinterpret_cast<const float4 *>(kT[row0 + r]);
-            float acc = s[r];
+        for (int r = 0; r < RW; ++r) {
+            const float4 *row = reinterpret_cast<const float4 *>(kT[r0 + r]);
+            float a0 = s[r][0], a1 = s[r][1];
 #pragma unroll
             for (int t4 = 0; t4 < MB / 4; ++t4) {
-                const float4 a = kr[t4];
-                acc = fmaf(a.x, uc[4 * t4], acc);
-                acc = fmaf(a.y, uc[4 * t4 + 1], acc);
-                acc = fmaf(a.z, uc[4 * t4 + 2], acc);
-                acc = fmaf(a.w, uc[4 * t4 + 3], acc);
+                const float4 a = row[t4];
+                const float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    a0 = fmaf(av[e], uc[4 * t4 + e][0], a0);
+                    a1 = fmaf(av[e], uc[4 * t4 + e][1], a1);
+                }
             }
-            s[r] = acc;
+            s[r][0] = a0;
+            s[r][1] = a1;
         }
     }
 #pragma unroll
-    for (int r = 0; r < R; ++r) Su[(size_t)(row0 + r) * DV + j] = s[r];
+    for (int r = 0; r < RW; ++r)
+        *reinterpret_cast<float2 *>(Su + (size_t)(r0 + r) * DV + c0) = make_float2(s[r][0], s[r][1]);
 }
 
 template <int DK, int DV, typename TIn, typename TOut>
 cudaError_t tokens_launch(const DecodeArgs &a) {
-    decode_tokens_kernel<DK, DV, TIn, TOut><<<a.B * a.H, 256, 0, a.stream>>>(
+    static bool attr[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 64 || !attr[dev]) {
+        e = cudaFuncSetAttribute(decode_tokens_kernel<DK, DV, TIn, TOut>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)PART_BYTES);
+        if (e != cudaSuccess) return e;
+        if (dev < 64) attr[dev] = true;
+    }
+    decode_tokens_kernel<DK, DV, TIn, TOut><<<a.B * a.H, NT, PART_BYTES, a.stream>>>(
         static_cast<const TIn *>(a.q), static_cast<const TIn *>(a.k), static_cast<const TIn *>(a.v), a.beta, a.S,
         static_cast<TOut *>(a.o), a.m, a.H, a.euler);
     return cudaGetLastError();

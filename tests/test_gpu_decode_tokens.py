@@ -31,7 +31,7 @@ def _case(dk, dv, m, B=3, H=5, seed=91):
 
 
 @pytest.mark.parametrize("dk,dv", [(128, 128), (64, 64), (32, 128), (128, 32)])
-@pytest.mark.parametrize("m", [1, 5, 16])
+@pytest.mark.parametrize("m", [1, 5, 16, 37])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_decode_tokens_small(efla, dk, dv, m, dtype):
     cfg, S0, inp = _case(dk, dv, m)
