@@ -4,8 +4,8 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 One step = one efla_fwd_chunked call over the language-model-layer workload
-(B=8, H=16, T=2048, d_k=d_v=128, bf16 q/k/v, fp32 beta, S0 = 0, fp32 o and
-S_T, chunk 64) with inputs resident in HBM.  L2 is flushed (a 512 MiB write)
+(B=8, H=16, T=2048, d_k=d_v=128, bf16 q/k/v, fp32 beta, S0 = 0, o in the dtype
+of q (bf16), fp32 S_T, chunk 64) with inputs resident in HBM.  L2 is flushed (a 512 MiB write)
 before every timed step; each step is bracketed by CUDA events on the
 launching stream.  Prints ONE JSON line on rank 0.
 
@@ -42,15 +42,16 @@ def flops_per_token_head(dk: int, dv: int, C: int = CHUNK) -> float:
     return 6 * dk * dv + 3 * C * dk + 2 * C * dv + C * C / 3.0
 
 
-def fwd_bytes(B, T, H, dk, dv, N, in_bytes=2, o_bytes=4, s0=False, s_t=True) -> int:
-    """Algorithmic bytes: every input read once, every output written once."""
+def fwd_bytes(B, T, H, dk, dv, N, in_bytes=2, o_bytes=2, s0=False, s_t=True) -> int:
+    """Algorithmic bytes: every input read once, every output written once (o in the
+    input dtype: 1028 B per token-head at d = 128 bf16, plus S0 and S_T per unit)."""
     th = B * T * H
     b = th * (2 * dk * in_bytes + dv * in_bytes + 4 + dv * o_bytes)
     st = N * H * dk * dv * 4
     return b + (st if s0 else 0) + (st if s_t else 0)
 
 
-def decode_bytes(B, H, dk, dv, in_bytes=2, o_bytes=4) -> int:
+def decode_bytes(B, H, dk, dv, in_bytes=2, o_bytes=2) -> int:
     u = B * H
     return u * ((2 * dk + dv) * in_bytes + 4 + dv * o_bytes + 2 * dk * dv * 4)
 
@@ -234,7 +235,7 @@ def run_ours(args, world, rank, local):
     inp = workloads.make_fwd_inputs(cfg)
     B, T, H, dk, dv, N = inp["B"], inp["T"], inp["H"], cfg.dk, cfg.dv, inp["N"]
     q, k, v, beta = (inp[x].to(dev) for x in ("q", "k", "v", "beta"))
-    o = torch.empty((B, T, H, dv), dtype=torch.float32, device=dev)
+    o = torch.empty((B, T, H, dv), dtype=q.dtype, device=dev)  # o in the dtype of q
     S_T = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
@@ -354,6 +355,9 @@ def run_ours(args, world, rank, local):
     # ---- the stiff/long configuration: one sequence per head, unsplit and split along time
     stiff_fig = stiff_figure(efla, dev, stream, max(3, args.steps // 2), flush, peaks)
 
+    # ---- the packed variable-length configuration
+    varlen_fig = varlen_figure(efla, dev, stream, max(3, args.steps // 2), flush, peaks)
+
     # ---- CPU baseline: the oracle on a bounded sample of the same workload
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -364,10 +368,10 @@ def run_ours(args, world, rank, local):
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16",
-            "precision": "bf16 inputs; tensor-core operands split into bf16 hi+lo; fp32 state, accumulation and o",
+            "precision": "bf16 inputs and o; tensor-core operands split into bf16 hi+lo; fp32 state and accumulation",
             "data": "synthetic",
             "config": {"workload": "lm: EFLA chunked forward B=8 H=16 T=2048 d_k=d_v=128, bf16 q,k,v, fp32 beta, "
-                                   "S0=0, o fp32, S_T fp32, chunk 64",
+                                   "S0=0, o bf16 (the dtype of q), S_T fp32, chunk 64",
                        "B": B, "T": T, "H": H, "d_k": dk, "d_v": dv, "chunk": CHUNK,
                        "l2": "flushed (512 MiB write) before every timed step",
                        "parallelism": f"replicas x{world}"},
@@ -376,6 +380,7 @@ def run_ours(args, world, rank, local):
             "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": traffic,
                          "algorithmic_bytes_per_launch": nbytes,
+                         "bytes_per_token_head": "q,k,v 768 + beta 4 + o 256 = 1028 (bf16), plus S_T 64 KiB per unit",
                          "peak_source": f"{peaks['source']} hbm_gbs (copy burst)",
                          "kernel": "efla chunk kernel (one launch per step)",
                          "t_roof_us": 1e6 * max(nbytes / (peaks["hbm_gbs"] * 1e9),
@@ -391,6 +396,7 @@ def run_ours(args, world, rank, local):
             "prep": prep_fig,
             "decode_tokens": dt_fig,
             "stiff": stiff_fig,
+            "varlen": varlen_fig,
             "bwd": bwd_fig,
             "cpu_baseline": cpu,
         }
@@ -416,43 +422,53 @@ def time_steps(fn, steps, flush, stream):
 
 
 def decode_figures(efla, dev, stream):
+    """Decode: 1000 chained efla_decode_step calls on the B256 H32 state, each step with its
+    own inputs (drawn on the device beforehand from seed (4 << 32) + step, the workload's laws),
+    captured in one CUDA graph; the state (512 MiB) exceeds L2."""
     import torch
 
     import workloads
     cfg = workloads.DECODE
     S = workloads.make_decode_state(cfg).to(dev)
-    pool = 8
-    steps = [workloads.make_decode_step(i, cfg) for i in range(pool)]
-    ins = [[s[x].to(dev) for x in ("q", "k", "v", "beta")] for s in steps]
-    o = torch.empty((cfg.B, cfg.H, cfg.dv), dtype=torch.float32, device=dev)
-    n_graph = 100
+    n = cfg.steps
+    shp = (cfg.B, cfg.H)
+    ins = []
+    for i in range(n):
+        gen = torch.Generator(device=dev)
+        gen.manual_seed((cfg.seed << 32) + i)
+        ins.append([torch.randn(shp + (cfg.dk,), generator=gen, device=dev).to(torch.bfloat16),
+                    torch.randn(shp + (cfg.dk,), generator=gen, device=dev).to(torch.bfloat16),
+                    torch.randn(shp + (cfg.dv,), generator=gen, device=dev).to(torch.bfloat16),
+                    torch.sigmoid(torch.randn(shp, generator=gen, device=dev))])
+    o = torch.empty((cfg.B, cfg.H, cfg.dv), dtype=torch.bfloat16, device=dev)
     side = torch.cuda.Stream()
     side.wait_stream(stream)
     with torch.cuda.stream(side):
         for i in range(3):
-            efla.decode_step(*ins[i % pool], S, o=o, stream=side)
+            efla.decode_step(*ins[i], S, o=o, stream=side)
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=side):
-        for i in range(n_graph):
-            efla.decode_step(*ins[i % pool], S, o=o, stream=side)
-    for _ in range(2):
-        g.replay()
+        for i in range(n):
+            efla.decode_step(*ins[i], S, o=o, stream=side)
+    g.replay()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    reps = 5
+    reps = 2
     e0.record()
     for _ in range(reps):
         g.replay()
     e1.record()
     torch.cuda.synchronize()
-    t = e0.elapsed_time(e1) / 1e3 / (reps * n_graph)
+    t = e0.elapsed_time(e1) / 1e3 / (reps * n)
     nbytes = decode_bytes(cfg.B, cfg.H, cfg.dk, cfg.dv)
     peaks = read_peaks()
-    return {"workload": "decode: B=256 H=32 d=128 bf16 q,k,v, fp32 S in place, o fp32; CUDA graph of 100 "
-                        "chained steps (inputs cycled from 8 seeded steps); S (512 MiB) exceeds L2",
+    del ins
+    return {"workload": f"decode: B=256 H=32 d=128 bf16 q,k,v and o, fp32 S in place; a CUDA graph of {n} "
+                        f"chained steps, each with its own inputs (drawn on the device from seed (4<<32)+step); "
+                        f"S (512 MiB) exceeds L2",
             "us_per_step": 1e6 * t, "GB/s": nbytes / t / 1e9, "bytes_per_step": nbytes,
-            "frac_hbm": nbytes / t / 1e9 / peaks["hbm_gbs"], "gpu_launches": reps * n_graph}
+            "frac_hbm": nbytes / t / 1e9 / peaks["hbm_gbs"], "gpu_launches": reps * n}
 
 
 def bwd_figure(efla, dev, stream, q, k, v, beta, flush, peaks, steps=3):
@@ -476,7 +492,7 @@ def stiff_figure(efla, dev, stream, steps, flush, peaks):
     inp = workloads.make_fwd_inputs(cfg)
     g = {x: inp[x].to(dev) for x in ("q", "k", "v", "beta", "S0")}
     B, T, H, dk, dv = cfg.B, cfg.T, cfg.H, cfg.dk, cfg.dv
-    o = torch.empty((B, T, H, dv), dtype=torch.float32, device=dev)
+    o = torch.empty((B, T, H, dv), dtype=torch.bfloat16, device=dev)
     S_T = torch.empty((B, H, dk, dv), dtype=torch.float32, device=dev)
     need, G = efla.scan_workspace(B, T, H, dk, dv, 0)
     ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
@@ -487,11 +503,39 @@ def stiff_figure(efla, dev, stream, steps, flush, peaks):
     tokens = B * T
     nbytes = fwd_bytes(B, T, H, dk, dv, B, s0=True)
     return {"workload": "stiff: B=1 H=16 T=65536 d=128 bf16, key norms U[0.1,10], beta=sigmoid(N(2,1)), "
-                        "S0~0.1 N(0,1), o fp32, S_T fp32",
+                        "S0~0.1 N(0,1), o bf16, S_T fp32",
             "ms_unsplit": 1e3 * t_plain, "tokens_per_s_unsplit": tokens / t_plain,
             "ms_split": 1e3 * t_scan, "tokens_per_s_split": tokens / t_scan, "segments": G,
-            "speedup": t_plain / t_scan, "frac_hbm_split": nbytes / t_scan / 1e9 / peaks["hbm_gbs"],
+            "speedup": t_plain / t_scan, "algorithmic_bytes": nbytes,
+            "frac_hbm_unsplit": nbytes / t_plain / 1e9 / peaks["hbm_gbs"],
+            "frac_hbm_split": nbytes / t_scan / 1e9 / peaks["hbm_gbs"],
             "gpu_launches": 3 * steps + steps}
+
+
+def varlen_figure(efla, dev, stream, steps, flush, peaks):
+    """The packed variable-length workload: 64 sequences of U{1..8192} tokens, H8 d128 bf16,
+    per-sequence S0; one launch, one CTA per (sequence, head), in sequence order (no
+    longest-first ordering)."""
+    import torch
+
+    import workloads
+    cfg = workloads.FWD_WORKLOADS["varlen"]
+    inp = workloads.make_fwd_inputs(cfg)
+    g = {x: inp[x].to(dev) for x in ("q", "k", "v", "beta", "S0", "cu_seqlens")}
+    B, T, H, N, dk, dv = inp["B"], inp["T"], inp["H"], inp["N"], cfg.dk, cfg.dv
+    o = torch.empty((B, T, H, dv), dtype=torch.bfloat16, device=dev)
+    S_T = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
+    t = time_steps(lambda: efla.fwd_chunked(g["q"], g["k"], g["v"], g["beta"], g["S0"], g["cu_seqlens"], o=o,
+                                            S_T=S_T, stream=stream), steps, flush, stream)
+    nbytes = fwd_bytes(B, T, H, dk, dv, N, s0=True) + (N + 1) * 4
+    lens = [int(inp["cu_seqlens"][i + 1] - inp["cu_seqlens"][i]) for i in range(N)]
+    return {"workload": f"varlen: {N} sequences, lengths U{{1..8192}} (seeded; {T} tokens, longest {max(lens)}), "
+                        f"H=8 d=128 bf16, per-sequence S0~0.1 N(0,1), o bf16, S_T fp32",
+            "ms_per_call": 1e3 * t, "tokens_per_s": T / t, "algorithmic_bytes": nbytes,
+            "GB/s": nbytes / t / 1e9, "frac_hbm": nbytes / t / 1e9 / peaks["hbm_gbs"],
+            "tflops": flops_per_token_head(dk, dv) * T * H / t / 1e12,
+            "scheduling": "one CTA per (sequence, head) in sequence order; no longest-first ordering",
+            "gpu_launches": steps}
 
 
 def decode_tokens_figure(efla, dev, stream, steps, flush, peaks, m=16):
@@ -501,12 +545,12 @@ def decode_tokens_figure(efla, dev, stream, steps, flush, peaks, m=16):
     inp = workloads.make_decode_tokens(m, cfg)
     g = [inp[x].to(dev) for x in ("q", "k", "v", "beta")]
     import torch
-    o = torch.empty((cfg.B, m, cfg.H, cfg.dv), dtype=torch.float32, device=dev)
+    o = torch.empty((cfg.B, m, cfg.H, cfg.dv), dtype=torch.bfloat16, device=dev)
     t = time_steps(lambda: efla.decode_tokens(*g, S, o=o, stream=stream), steps, flush, stream)
     u = cfg.B * cfg.H
-    nbytes = u * (m * ((2 * cfg.dk + cfg.dv) * 2 + 4 + cfg.dv * 4) + 2 * cfg.dk * cfg.dv * 4)
-    return {"workload": f"decode_tokens: B=256 H=32 d=128, {m} tokens per sequence per call, bf16 q,k,v, "
-                        f"fp32 S in place (read and written once), o fp32",
+    nbytes = u * (m * ((2 * cfg.dk + cfg.dv) * 2 + 4 + cfg.dv * 2) + 2 * cfg.dk * cfg.dv * 4)
+    return {"workload": f"decode_tokens: B=256 H=32 d=128, {m} tokens per sequence per call, bf16 q,k,v and o, "
+                        f"fp32 S in place (read and written once)",
             "us_per_call": 1e6 * t, "tokens_per_s": cfg.B * m / t, "GB/s": nbytes / t / 1e9,
             "bytes_per_call": nbytes, "frac_hbm": nbytes / t / 1e9 / peaks["hbm_gbs"],
             "gpu_launches": steps}

@@ -23,9 +23,9 @@ from typing import Optional, Tuple
 
 import torch
 
-__all__ = ["EflaError", "lib_path", "load", "fwd_chunked", "fwd_chunked_scan", "fwd_chunked_scan_static", "scan_workspace", "fwd_recurrent",
-           "decode_step", "decode_tokens", "bwd_recurrent", "prep",
-           "device_status", "abi_version", "STATUS", "UPDATES"]
+__all__ = ["EflaError", "lib_path", "load", "fwd_chunked", "fwd_chunked_scan", "fwd_chunked_scan_static",
+           "scan_workspace", "fwd_recurrent", "decode_step", "decode_tokens", "bwd_recurrent", "prep",
+           "device_status", "error_string", "set_wait_limit_ns", "set_debug_stall", "abi_version", "STATUS", "UPDATES"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 lib_path = os.path.join(_PKG, "libefla.so")
@@ -57,11 +57,11 @@ def load():
         L = ctypes.CDLL(lib_path)
         vp, ip = ctypes.c_void_p, ctypes.c_int
         L.efla_fwd_chunked.restype = ip
-        L.efla_fwd_chunked.argtypes = [vp] * 8 + [ip] * 9 + [vp]
+        L.efla_fwd_chunked.argtypes = [vp] * 8 + [ip] * 8 + [vp]
         L.efla_fwd_recurrent.restype = ip
-        L.efla_fwd_recurrent.argtypes = [vp] * 8 + [ip] * 8 + [vp]
+        L.efla_fwd_recurrent.argtypes = [vp] * 8 + [ip] * 7 + [vp]
         L.efla_decode_step.restype = ip
-        L.efla_decode_step.argtypes = [vp] * 6 + [ip] * 6 + [vp]
+        L.efla_decode_step.argtypes = [vp] * 6 + [ip] * 5 + [vp]
         L.efla_fwd_chunked_ex.restype = ip
         L.efla_fwd_chunked_ex.argtypes = [vp] * 8 + [ip] * 10 + [vp]
         L.efla_fwd_recurrent_ex.restype = ip
@@ -82,8 +82,12 @@ def load():
         L.efla_prep.argtypes = [vp] * 7 + [ctypes.c_longlong] + [ip] * 4 + [vp]
         L.efla_device_status.restype = ip
         L.efla_device_status.argtypes = [vp]
-        L.efla_status_string.restype = ctypes.c_char_p
-        L.efla_status_string.argtypes = [ip]
+        L.efla_get_error_string.restype = ctypes.c_char_p
+        L.efla_get_error_string.argtypes = [ip]
+        L.efla_debug_set_wait_limit_ns.restype = None
+        L.efla_debug_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
+        L.efla_debug_set_stall.restype = None
+        L.efla_debug_set_stall.argtypes = [ip]
         L.efla_last_error.restype = ctypes.c_char_p
         L.efla_last_error.argtypes = []
         L.efla_abi_version.restype = ip
@@ -128,35 +132,56 @@ def _need(t: Optional[torch.Tensor], name: str):
         raise EflaError(1, f"{name} must be contiguous")
 
 
-def _fwd(entry, q, k, v, beta, S0, cu_seqlens, o, S_T, o_dtype, chunk, stream, return_state, update="exact"):
-    L = load()
-    for t, n in ((q, "q"), (k, "k"), (v, "v"), (beta, "beta"), (S0, "S0"), (cu_seqlens, "cu_seqlens"),
-                 (o, "o"), (S_T if isinstance(S_T, torch.Tensor) else None, "S_T")):
-        _need(t, n)
-    if q.dim() != 4 or k.shape != q.shape or v.shape[:3] != q.shape[:3] or beta.shape != q.shape[:3]:
+def _check_fwd_inputs(q, k, v, beta, S0, N=None):
+    """Shape and dtype checks shared by every forward wrapper (made before the device and
+    layout checks); returns (B, T, H, dk, dv, N)."""
+    if q.dim() != 4 or k.shape != q.shape or v.dim() != 4 or v.shape[:3] != q.shape[:3] \
+            or beta.shape != q.shape[:3]:
         raise EflaError(1, f"shape mismatch q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)} "
                            f"beta{tuple(beta.shape)}")
     if q.dtype != k.dtype or q.dtype != v.dtype or beta.dtype != torch.float32:
         raise EflaError(1, "q, k, v must share a dtype and beta must be float32")
+    _dt(q.dtype)
     B, T, H, dk = q.shape
     dv = v.shape[-1]
+    N = B if N is None else N
+    if S0 is not None and (S0.dtype != torch.float32 or tuple(S0.shape) != (N, H, dk, dv)):
+        raise EflaError(1, f"S0 must be float32 [{N},{H},{dk},{dv}]")
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (beta, "beta"), (S0, "S0")):
+        _need(t, n)
+    return B, T, H, dk, dv, N
+
+
+def _outputs(q, o, S_T, o_dtype, return_state, B, T, H, dk, dv, N):
+    """The output tensors of a forward call: given ones are checked, missing ones allocated."""
+    o_dtype = q.dtype if o_dtype is None else o_dtype
+    if o is None:
+        o = torch.empty((B, T, H, dv), dtype=o_dtype, device=q.device)
+    else:
+        _need(o, "o")
+        if tuple(o.shape) != (B, T, H, dv):
+            raise EflaError(1, f"o must be [{B},{T},{H},{dv}]")
+        _dt(o.dtype)
+    if S_T is None and return_state:
+        S_T = torch.empty((N, H, dk, dv), dtype=torch.float32, device=q.device)
+    elif S_T is not None:
+        _need(S_T, "S_T")
+        if S_T.dtype != torch.float32 or tuple(S_T.shape) != (N, H, dk, dv):
+            raise EflaError(1, f"S_T must be float32 [{N},{H},{dk},{dv}]")
+    return o, S_T
+
+
+def _fwd(entry, q, k, v, beta, S0, cu_seqlens, o, S_T, o_dtype, chunk, stream, return_state, update="exact"):
+    L = load()
+    _need(cu_seqlens, "cu_seqlens")
     if cu_seqlens is not None:
         if cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1:
             raise EflaError(1, "cu_seqlens must be a 1-D int32 tensor")
         N = cu_seqlens.shape[0] - 1
     else:
-        N = B
-    if S0 is not None and (S0.dtype != torch.float32 or tuple(S0.shape) != (N, H, dk, dv)):
-        raise EflaError(1, f"S0 must be float32 [{N},{H},{dk},{dv}]")
-    if o is None:
-        o = torch.empty((B, T, H, dv), dtype=o_dtype, device=q.device)
-    elif tuple(o.shape) != (B, T, H, dv):
-        raise EflaError(1, "o has the wrong shape")
-    if S_T is None and return_state:
-        S_T = torch.empty((N, H, dk, dv), dtype=torch.float32, device=q.device)
-    elif isinstance(S_T, torch.Tensor) and (S_T.dtype != torch.float32 or tuple(S_T.shape) != (N, H, dk, dv)):
-        raise EflaError(1, f"S_T must be float32 [{N},{H},{dk},{dv}]")
-    st = S_T if isinstance(S_T, torch.Tensor) else None
+        N = None
+    B, T, H, dk, dv, N = _check_fwd_inputs(q, k, v, beta, S0, N)
+    o, st = _outputs(q, o, S_T, o_dtype, return_state, B, T, H, dk, dv, N)
     args = [_p(q), _p(k), _p(v), _p(beta), _p(S0), _p(cu_seqlens), _p(o), _p(st), B, T, H, dk, dv, N,
             _dt(q.dtype), _dt(o.dtype)]
     if update not in UPDATES:
@@ -171,14 +196,15 @@ def _fwd(entry, q, k, v, beta, S0, cu_seqlens, o, S_T, o_dtype, chunk, stream, r
 def fwd_chunked(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor,
                 S0: Optional[torch.Tensor] = None, cu_seqlens: Optional[torch.Tensor] = None, *,
                 o: Optional[torch.Tensor] = None, S_T: Optional[torch.Tensor] = None,
-                o_dtype: torch.dtype = torch.float32, chunk: int = 64, stream=None,
+                o_dtype: Optional[torch.dtype] = None, chunk: int = 64, stream=None,
                 return_state: bool = True, update: str = "exact") -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
     """EFLA forward, chunkwise.  Layouts as in ``efla_fwd_chunked`` (include/efla.h).
 
     q, k [B,T,H,dk], v [B,T,H,dv] (bf16 or fp32); beta [B,T,H] fp32; S0 [N,H,dk,dv] fp32;
-    cu_seqlens [N+1] int32 (then B == 1).  Returns (o [B,T,H,dv] in ``o_dtype``,
-    S_T [N,H,dk,dv] fp32 or None when ``return_state`` is False).  ``update="euler"`` runs
-    the delta-rule (DeltaNet) gate alpha = beta through the same kernels.
+    cu_seqlens [N+1] int32 (then B == 1).  Returns (o [B,T,H,dv] in ``o_dtype`` -- q's dtype
+    unless given, or the dtype of a given ``o`` --, S_T [N,H,dk,dv] fp32 or None when
+    ``return_state`` is False).  ``update="euler"`` runs the delta-rule (DeltaNet) gate
+    alpha = beta through the same kernels.
     """
     return _fwd("chunked", q, k, v, beta, S0, cu_seqlens, o, S_T, o_dtype, chunk, stream, return_state, update)
 
@@ -194,26 +220,15 @@ def scan_workspace(B: int, T: int, H: int, dk: int = 128, dv: int = 128, segment
 def fwd_chunked_scan(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor,
                      S0: Optional[torch.Tensor] = None, *, segments: int = 0,
                      workspace: Optional[torch.Tensor] = None, o: Optional[torch.Tensor] = None,
-                     S_T: Optional[torch.Tensor] = None, o_dtype: torch.dtype = torch.float32, stream=None,
+                     S_T: Optional[torch.Tensor] = None, o_dtype: Optional[torch.dtype] = None, stream=None,
                      return_state: bool = True, update: str = "exact") -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
     """``fwd_chunked`` with each sequence split along time into ``segments`` pieces
     (``efla_fwd_chunked_scan``): for few long sequences.  ``workspace`` (a CUDA tensor of at
     least ``scan_workspace(...)[0]`` bytes) is allocated here when not given."""
     L = load()
-    for t, n in ((q, "q"), (k, "k"), (v, "v"), (beta, "beta"), (S0, "S0"), (o, "o"), (workspace, "workspace")):
-        _need(t, n)
-    if q.dim() != 4 or k.shape != q.shape or v.shape[:3] != q.shape[:3] or beta.shape != q.shape[:3]:
-        raise EflaError(1, "shape mismatch")
-    if q.dtype != k.dtype or q.dtype != v.dtype or beta.dtype != torch.float32:
-        raise EflaError(1, "q, k, v must share a dtype and beta must be float32")
-    B, T, H, dk = q.shape
-    dv = v.shape[-1]
-    if S0 is not None and (S0.dtype != torch.float32 or tuple(S0.shape) != (B, H, dk, dv)):
-        raise EflaError(1, f"S0 must be float32 [{B},{H},{dk},{dv}]")
-    if o is None:
-        o = torch.empty((B, T, H, dv), dtype=o_dtype, device=q.device)
-    if S_T is None and return_state:
-        S_T = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
+    _need(workspace, "workspace")
+    B, T, H, dk, dv, N = _check_fwd_inputs(q, k, v, beta, S0)
+    o, S_T = _outputs(q, o, S_T, o_dtype, return_state, B, T, H, dk, dv, N)
     if update not in UPDATES:
         raise EflaError(1, f"unknown update rule {update!r}")
     need, _ = scan_workspace(B, T, H, dk, dv, segments)
@@ -228,21 +243,14 @@ def fwd_chunked_scan(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: to
 
 def fwd_chunked_scan_static(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor,
                             S0: Optional[torch.Tensor] = None, *, segments: int = 0, o: Optional[torch.Tensor] = None,
-                            S_T: Optional[torch.Tensor] = None, o_dtype: torch.dtype = torch.float32, stream=None,
+                            S_T: Optional[torch.Tensor] = None, o_dtype: Optional[torch.dtype] = None, stream=None,
                             return_state: bool = True, update: str = "exact"):
     """``fwd_chunked_scan`` on the library's fixed scratch (``efla_fwd_chunked_scan_static``):
-    no workspace.  Calls that overlap in time race on that scratch."""
+    no workspace.  Calls that overlap in time race on that scratch.  Pass ``o`` (and ``S_T``)
+    to make the call allocate nothing at all."""
     L = load()
-    for t, n in ((q, "q"), (k, "k"), (v, "v"), (beta, "beta"), (S0, "S0"), (o, "o")):
-        _need(t, n)
-    if q.dim() != 4 or k.shape != q.shape or v.shape[:3] != q.shape[:3] or beta.shape != q.shape[:3]:
-        raise EflaError(1, "shape mismatch")
-    B, T, H, dk = q.shape
-    dv = v.shape[-1]
-    if o is None:
-        o = torch.empty((B, T, H, dv), dtype=o_dtype, device=q.device)
-    if S_T is None and return_state:
-        S_T = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
+    B, T, H, dk, dv, N = _check_fwd_inputs(q, k, v, beta, S0)
+    o, S_T = _outputs(q, o, S_T, o_dtype, return_state, B, T, H, dk, dv, N)
     if update not in UPDATES:
         raise EflaError(1, f"unknown update rule {update!r}")
     _check(L.efla_fwd_chunked_scan_static(_p(q), _p(k), _p(v), _p(beta), _p(S0), _p(o), _p(S_T), B, T, H, dk, dv,
@@ -252,16 +260,17 @@ def fwd_chunked_scan_static(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, b
 
 
 def fwd_recurrent(q, k, v, beta, S0=None, cu_seqlens=None, *, o=None, S_T=None,
-                  o_dtype: torch.dtype = torch.float32, stream=None, return_state: bool = True,
+                  o_dtype: Optional[torch.dtype] = None, stream=None, return_state: bool = True,
                   update: str = "exact"):
     """Token-by-token fp32 evaluation on CUDA cores (``efla_fwd_recurrent``)."""
     return _fwd("recurrent", q, k, v, beta, S0, cu_seqlens, o, S_T, o_dtype, 0, stream, return_state, update)
 
 
 def decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor, S: torch.Tensor, *,
-                o: Optional[torch.Tensor] = None, o_dtype: torch.dtype = torch.float32,
+                o: Optional[torch.Tensor] = None, o_dtype: Optional[torch.dtype] = None,
                 stream=None, update: str = "exact") -> torch.Tensor:
-    """One token per sequence; S [B,H,dk,dv] fp32 is updated in place.  Returns o [B,H,dv]."""
+    """One token per sequence; S [B,H,dk,dv] fp32 is updated in place.  Returns o [B,H,dv]
+    (in q's dtype unless ``o_dtype`` or ``o`` says otherwise)."""
     L = load()
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (beta, "beta"), (S, "S"), (o, "o")):
         _need(t, n)
@@ -274,7 +283,9 @@ def decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.T
     if q.dtype != k.dtype or q.dtype != v.dtype or beta.dtype != torch.float32:
         raise EflaError(1, "q, k, v must share a dtype and beta must be float32")
     if o is None:
-        o = torch.empty((B, H, dv), dtype=o_dtype, device=q.device)
+        o = torch.empty((B, H, dv), dtype=q.dtype if o_dtype is None else o_dtype, device=q.device)
+    elif tuple(o.shape) != (B, H, dv):
+        raise EflaError(1, "o has the wrong shape")
     if update not in UPDATES:
         raise EflaError(1, f"unknown update rule {update!r}")
     _check(L.efla_decode_step_ex(_p(q), _p(k), _p(v), _p(beta), _p(S), _p(o), B, H, dk, dv,
@@ -283,7 +294,7 @@ def decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.T
 
 
 def decode_tokens(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor, S: torch.Tensor, *,
-                  o: Optional[torch.Tensor] = None, o_dtype: torch.dtype = torch.float32,
+                  o: Optional[torch.Tensor] = None, o_dtype: Optional[torch.dtype] = None,
                   stream=None, update: str = "exact") -> torch.Tensor:
     """m tokens per sequence appended to the state; S [B,H,dk,dv] fp32 is updated in place.
 
@@ -302,7 +313,7 @@ def decode_tokens(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch
     if q.dtype != k.dtype or q.dtype != v.dtype or beta.dtype != torch.float32:
         raise EflaError(1, "q, k, v must share a dtype and beta must be float32")
     if o is None:
-        o = torch.empty((B, m, H, dv), dtype=o_dtype, device=q.device)
+        o = torch.empty((B, m, H, dv), dtype=q.dtype if o_dtype is None else o_dtype, device=q.device)
     elif tuple(o.shape) != (B, m, H, dv):
         raise EflaError(1, "o has the wrong shape")
     if update not in UPDATES:
@@ -378,5 +389,20 @@ def prep(k: torch.Tensor, beta: torch.Tensor, v: Optional[torch.Tensor] = None, 
 
 
 def device_status(stream=None) -> int:
-    """Read and clear the library's device status word (synchronises ``stream``)."""
+    """Read and clear the current device's status word (synchronises ``stream``)."""
     return load().efla_device_status(_stream(stream))
+
+
+def error_string(code: int) -> str:
+    """Static description of a status code (``efla_get_error_string``)."""
+    return load().efla_get_error_string(int(code)).decode()
+
+
+def set_wait_limit_ns(ns: int) -> None:
+    """Test hook: bound on the chunk kernel's waits between warp roles, in ns (0 = the 2 s default)."""
+    load().efla_debug_set_wait_limit_ns(int(ns))
+
+
+def set_debug_stall(on: bool) -> None:
+    """Test hook (``efla_debug_set_stall``): make the chunk kernel's waits run out on purpose."""
+    load().efla_debug_set_stall(1 if on else 0)

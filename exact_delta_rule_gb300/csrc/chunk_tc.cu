@@ -98,7 +98,9 @@ constexpr uint32_t TM_OB = 384; // second O^T accumulator (the u_hi P_lo term)  
 constexpr uint32_t TM_G = 448;  // [K;Q] K^T fp32                                  64 columns
 constexpr uint32_t TM_COLS = 512;
 
-constexpr uint64_t WAIT_NS = 2000000000ull;  // 2 s bound on any wait
+// Bound on the waits that let a CTA's own copies and tensor-core operations finish before it
+// releases tensor memory.  The waits between roles are bounded by TcParams::wait_ns.
+constexpr uint64_t WAIT_NS = 2000000000ull;
 
 constexpr int BAR_PREP = 2;  // named barrier of the two prep warpgroups (256 threads)
 
@@ -122,6 +124,8 @@ struct TcParams {
     int seg_len, G;
     const float *s_in;
     float *maps;
+    unsigned long long wait_ns;  // bound on every wait between roles (2 s unless a test lowers it)
+    int debug_stall;             // test hook: the MMA thread first waits on a barrier nothing completes
 };
 
 struct Bars {
@@ -141,26 +145,36 @@ struct Bars {
     uint64_t s_free[NSTAGE];  // the state update of a chunk complete: its K/Q/V stage is free
     uint64_t ost_free[2];     // a chunk's T''/P buffer is free: its last products and the TMA
                               // stores of its o tile have read it (4 arrivals)
+    uint64_t never;           // never completed (the debug_stall test hook waits on it)
 };
 static_assert(sizeof(Bars) <= 224, "mbarrier block exceeds its slot");
 
 // Bounded wait that also gives up when another role has aborted.  The slow
 // path is out of line: it is reached rarely and the kernel's code must stay
 // small enough for the instruction cache.
-__device__ __noinline__ bool wait_bar_slow(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
+__device__ __noinline__ bool wait_bar_slow(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                           uint64_t limit_ns) {
     const uint64_t t0 = globaltimer_ns();
     while (true) {
         if (mbar_try_wait_sleep(bar, parity, 20000)) return true;  // sleeps instead of spinning
         if (*abort_flag) return false;
-        if (globaltimer_ns() - t0 > WAIT_NS) {
+        if (globaltimer_ns() - t0 > limit_ns) {
             *abort_flag = 1;
             return false;
         }
     }
 }
-__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort_flag, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
-    return wait_bar_slow(bar, parity, abort_flag);
+    return wait_bar_slow(bar, parity, abort_flag, limit_ns);
+}
+// The same for all 32 lanes of a warp, with one outcome for the whole warp: every lane
+// waits, and the warp proceeds only if every lane's wait succeeded (the warp-collective
+// TMEM loads and stores that follow need all lanes together).
+__device__ __forceinline__ bool wait_bar_warp(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                              uint64_t limit_ns) {
+    const bool ok = wait_bar(bar, parity, abort_flag, limit_ns);
+    return __all_sync(0xffffffffu, ok);
 }
 
 // Hides a loop counter from the optimiser so that the loop stays rolled (the
@@ -331,6 +345,7 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + OFF_MISC + 4);
 
     const int tid = threadIdx.x, warp = tid >> 5;
+    const uint64_t wait_ns = p.wait_ns;
     long b, bos, eos;
     int h;
     int mode = 0;                    // 0: forward; 1: map from S = I, v = 0; 2: map from S = 0
@@ -407,6 +422,7 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
         mbar_init(&bars->u_ready, 128);
         mbar_init(&bars->drain[0], 1);
         mbar_init(&bars->drain[1], 1);
+        mbar_init(&bars->never, 1);
         fence_mbar_init();
         *abort_flag = 0;
     }
@@ -455,7 +471,7 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
             // zeroed here first (those rows may hold the next sequence) and its product issued
             // by the prep
             if (valid < C) {
-                ok = wait_bar(&bars->tma_full[st], (c / NSTAGE) & 1, abort_flag);
+                ok = wait_bar(&bars->tma_full[st], (c / NSTAGE) & 1, abort_flag, wait_ns);
                 if (ok) {
                     const int rows = C - valid;
                     for (int e = pi; e < 4 * rows * 8; e += 256) {
@@ -475,10 +491,10 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
                     issue_gram(tmem, s_sm, c, bars);
                 }
             }
-            ok = wait_bar(&bars->g_done, c & 1, abort_flag);
+            ok = wait_bar_warp(&bars->g_done, c & 1, abort_flag, wait_ns);
             // This chunk's T''/P buffer was last read by chunk c-2's products (P) and o stores
             // (T'' part); the state warpgroup releases it after both.
-            if (c >= 2) ok = wait_bar(&bars->ost_free[c & 1], ((c - 2) >> 1) & 1, abort_flag) && ok;
+            if (c >= 2) ok = wait_bar_warp(&bars->ost_free[c & 1], ((c - 2) >> 1) & 1, abort_flag, wait_ns) && ok;
             tc_fence_after();
             {
                 float g[32];
@@ -694,7 +710,7 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
             const bool live = c < nchunks;
             if (live) {
                 // The S^T operand needs only the previous state update, not this chunk's prep.
-                if (c > 0) ok = wait_bar(&bars->s_done, (c - 1) & 1, abort_flag);
+                if (c > 0) ok = wait_bar_warp(&bars->s_done, (c - 1) & 1, abort_flag, wait_ns);
                 tc_fence_after();
                 // S^T -> bf16 hi/lo operand in TMEM, 32 columns of S^T (16 operand columns) at a time
 #pragma unroll 1
@@ -712,7 +728,7 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
                 mbar_arrive(&bars->sa_ready);
             }
             if (c > 0) {  // outputs of chunk c-1 leave while X of chunk c is computed
-                ok = ok && wait_bar(&bars->o_done, (c - 1) & 1, abort_flag);
+                ok = ok && wait_bar_warp(&bars->o_done, (c - 1) & 1, abort_flag, wait_ns);
                 if (!ok) break;
                 tc_fence_after();
                 epilogue(c - 1);
@@ -720,7 +736,8 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
             if (!live) break;
             const long tok0 = bos + (long)c * C;
             const int valid = (int)min((long)C, eos - tok0);
-            ok = ok && wait_bar(&bars->x_done, c & 1, abort_flag);
+            ok = ok && wait_bar_warp(&bars->x_done, c & 1, abort_flag, wait_ns);
+            if (!ok) break;
             tc_fence_after();
             // (-X)^T = -(K S)^T -> bf16 hi/lo operand in TMEM (rows past the sequence end are zero),
             // written over X once all of X is in registers
@@ -744,7 +761,8 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(&bars->r_ready);
-            ok = ok && wait_bar(&bars->u_done, c & 1, abort_flag);
+            ok = ok && wait_bar_warp(&bars->u_done, c & 1, abort_flag, wait_ns);
+            if (!ok) break;
             tc_fence_after();
             // u^T = U1 + U2 -> bf16 hi/lo operand in TMEM
 #pragma unroll 1
@@ -786,7 +804,7 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
         prefetch_tensormap(&p.map_v);
         int issued = 0;
         for (int c = 0; c < nchunks; ++c) {
-            if (c >= NSTAGE && !wait_bar(&bars->s_free[c % NSTAGE], ((c - NSTAGE) / NSTAGE) & 1, abort_flag)) break;
+            if (c >= NSTAGE && !wait_bar(&bars->s_free[c % NSTAGE], ((c - NSTAGE) / NSTAGE) & 1, abort_flag, wait_ns)) break;
             const int st = c % NSTAGE;
             uint8_t *dst = sm + OFF_STAGE + st * STAGE_BYTES;
             const int tok = (int)(bos + (long)c * C);
@@ -815,13 +833,14 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
         int g_next = 0;
         auto issue_grams = [&](int limit) {
             while (ok && g_next <= limit && g_next < nchunks && eos - (bos + (long)g_next * C) >= C) {
-                if (g_next > 0 && !(ok = wait_bar(&bars->g_free, (g_next - 1) & 1, abort_flag))) break;
-                if (!(ok = wait_bar(&bars->tma_full[g_next % NSTAGE], (g_next / NSTAGE) & 1, abort_flag))) break;
+                if (g_next > 0 && !(ok = wait_bar(&bars->g_free, (g_next - 1) & 1, abort_flag, wait_ns))) break;
+                if (!(ok = wait_bar(&bars->tma_full[g_next % NSTAGE], (g_next / NSTAGE) & 1, abort_flag, wait_ns))) break;
                 tc_fence_after();
                 issue_gram(tmem, s_sm, g_next, bars);
                 ++g_next;
             }
         };
+        if (p.debug_stall) ok = wait_bar(&bars->never, 0, abort_flag, wait_ns);
         issue_grams(0);
         for (int c = 0; c < nchunks && ok; ++c) {
             const int st = c % NSTAGE, buf = c & 1;
@@ -831,9 +850,9 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
             // which its prep writes before prep_ready
             const bool partial = eos - (bos + (long)c * C) < C;
             if (!(ok = wait_bar(partial ? &bars->prep_ready[buf] : &bars->tma_full[st],
-                                partial ? (c >> 1) & 1 : (c / NSTAGE) & 1, abort_flag))) break;
-            if (!(ok = wait_bar(&bars->sa_ready, c & 1, abort_flag))) break;
-            if (c > 0 && !(ok = wait_bar(&bars->o_free, (c - 1) & 1, abort_flag))) break;
+                                partial ? (c >> 1) & 1 : (c / NSTAGE) & 1, abort_flag, wait_ns))) break;
+            if (!(ok = wait_bar(&bars->sa_ready, c & 1, abort_flag, wait_ns))) break;
+            if (c > 0 && !(ok = wait_bar(&bars->o_free, (c - 1) & 1, abort_flag, wait_ns))) break;
             tc_fence_after();
             {  // [X^T | O^T] = S^T [K; Q]^T: one N = 128 product over the stage's [K; Q] rows
                 const uint32_t idesc = idesc_bf16_f32(128, 128, 0, 0);
@@ -848,7 +867,7 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
                 mma_commit(&bars->x_done);
             }
             // the rest of the chunk needs its prep (T'', P)
-            if (!(ok = wait_bar(&bars->prep_ready[buf], (c >> 1) & 1, abort_flag))) break;
+            if (!(ok = wait_bar(&bars->prep_ready[buf], (c >> 1) & 1, abort_flag, wait_ns))) break;
             tc_fence_after();
             issue_grams(c + 1);
             if (!ok) break;
@@ -864,7 +883,7 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
                                  smem_desc(tp + ks * 32, 16, 1024), idesc, ks > 0);
                 }
             }
-            if (!(ok = wait_bar(&bars->r_ready, c & 1, abort_flag))) break;
+            if (!(ok = wait_bar(&bars->r_ready, c & 1, abort_flag, wait_ns))) break;
             tc_fence_after();
             {  // u^T = [U1 | U2] + (-X)_hi^T [T''_hi; T''_lo]^T + (-X)_lo^T T''_hi^T  (u = U1 + U2)
                 const uint32_t idesc2 = idesc_bf16_f32(128, 128, 0, 0), idesc1 = idesc_bf16_f32(128, 64, 0, 0);
@@ -880,7 +899,7 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
             // the Gram products two chunks ahead execute while the state warpgroup forms u
             issue_grams(c + 2);
             if (!ok) break;
-            if (!(ok = wait_bar(&bars->u_ready, c & 1, abort_flag))) break;
+            if (!(ok = wait_bar(&bars->u_ready, c & 1, abort_flag, wait_ns))) break;
             tc_fence_after();
             {  // S^T += u^T K  (the chain), then O^T += u^T P^T
                 const uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 1);
@@ -997,6 +1016,8 @@ cudaError_t launch_chunk_tc(const FwdArgs &a, const char **why) {
     p.G = a.G;
     p.s_in = a.s_in;
     p.maps = a.maps;
+    p.wait_ns = wait_limit_ns();
+    p.debug_stall = debug_stall() ? 1 : 0;
     *why = "tcgen05 chunk kernel launch";
     const long units = a.seg_len > 0 ? (a.maps ? 2L * a.B * (a.G - 1) * a.H : (long)a.B * a.G * a.H) : (long)a.N * a.H;
     const unsigned grid = (unsigned)units;

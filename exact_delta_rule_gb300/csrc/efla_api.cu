@@ -6,6 +6,7 @@
 #include <string>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "internal.cuh"
@@ -122,13 +123,33 @@ efla_status run_fwd(FwdArgs a, bool chunked) {
 }  // namespace
 
 int *device_status_ptr() {
-    static int *ptr = nullptr;  // one device in this process; set-up is idempotent
-    if (!ptr) {
+    // One status word per device: the symbol's device address differs per device, so it is
+    // resolved (once) with that device current.
+    static std::mutex mu;
+    static int *ptrs[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!ptrs[dev]) {
         int *p = nullptr;
-        if (cudaGetSymbolAddress(reinterpret_cast<void **>(&p), g_device_status) == cudaSuccess) ptr = p;
+        if (cudaGetSymbolAddress(reinterpret_cast<void **>(&p), g_device_status) == cudaSuccess) ptrs[dev] = p;
     }
-    return ptr;
+    return ptrs[dev];
 }
+
+namespace {
+std::atomic<unsigned long long> g_wait_limit_ns{0};
+std::atomic<int> g_debug_stall{0};
+}
+
+bool debug_stall() { return g_debug_stall.load(std::memory_order_relaxed) != 0; }
+
+unsigned long long wait_limit_ns() {
+    const unsigned long long v = g_wait_limit_ns.load(std::memory_order_relaxed);
+    return v ? v : 2000000000ull;
+}
+
+void set_wait_limit_ns(unsigned long long ns) { g_wait_limit_ns.store(ns, std::memory_order_relaxed); }
 
 }  // namespace efla
 
@@ -150,10 +171,9 @@ efla_status efla_fwd_chunked_ex(const void *q, const void *k, const void *v, con
 
 efla_status efla_fwd_chunked(const void *q, const void *k, const void *v, const float *beta, const float *S0,
                              const int32_t *cu_seqlens, void *o, float *S_T, int B, int T, int H, int d_k,
-                             int d_v, int N, efla_dtype in_dtype, efla_dtype o_dtype, int chunk,
-                             efla_stream_t stream) {
-    return efla_fwd_chunked_ex(q, k, v, beta, S0, cu_seqlens, o, S_T, B, T, H, d_k, d_v, N, in_dtype, o_dtype,
-                               chunk, EFLA_UPDATE_EXACT, stream);
+                             int d_v, int N, efla_dtype dtype, int chunk, efla_stream_t stream) {
+    return efla_fwd_chunked_ex(q, k, v, beta, S0, cu_seqlens, o, S_T, B, T, H, d_k, d_v, N, dtype, dtype, chunk,
+                               EFLA_UPDATE_EXACT, stream);
 }
 
 // Segments of the split forward: G segments of seg_len tokens (a multiple of the chunk)
@@ -278,6 +298,14 @@ efla_status efla_fwd_chunked_scan_static(const void *q, const void *k, const voi
         efla_status s = scan_plan(B, T, H, segments, &G, &seg);
         if (s != EFLA_OK) return s;
         need = scan_bytes(B, H, d_k, d_v, G);
+        if (segments <= 0) {  // automatic split: the most pieces whose maps and states fit the scratch
+            while (G > 1 && need > SCAN_SCRATCH_BYTES) {
+                s = scan_plan(B, T, H, G - 1, &G, &seg);
+                if (s != EFLA_OK) return s;
+                need = scan_bytes(B, H, d_k, d_v, G);
+            }
+            segments = G;
+        }
     }
     if (need > SCAN_SCRATCH_BYTES)
         return fail(EFLA_ERR_UNSUPPORTED, "this split needs %zu bytes of scratch; the static scratch holds %zu",
@@ -342,9 +370,8 @@ efla_status efla_fwd_recurrent_ex(const void *q, const void *k, const void *v, c
 
 efla_status efla_fwd_recurrent(const void *q, const void *k, const void *v, const float *beta,
                                const float *S0, const int32_t *cu_seqlens, void *o, float *S_T, int B,
-                               int T, int H, int d_k, int d_v, int N, efla_dtype in_dtype, efla_dtype o_dtype,
-                               efla_stream_t stream) {
-    return efla_fwd_recurrent_ex(q, k, v, beta, S0, cu_seqlens, o, S_T, B, T, H, d_k, d_v, N, in_dtype, o_dtype,
+                               int T, int H, int d_k, int d_v, int N, efla_dtype dtype, efla_stream_t stream) {
+    return efla_fwd_recurrent_ex(q, k, v, beta, S0, cu_seqlens, o, S_T, B, T, H, d_k, d_v, N, dtype, dtype,
                                  EFLA_UPDATE_EXACT, stream);
 }
 
@@ -382,9 +409,8 @@ efla_status efla_decode_step_ex(const void *q, const void *k, const void *v, con
 }
 
 efla_status efla_decode_step(const void *q, const void *k, const void *v, const float *beta, float *S, void *o,
-                             int B, int H, int d_k, int d_v, efla_dtype in_dtype, efla_dtype o_dtype,
-                             efla_stream_t stream) {
-    return efla_decode_step_ex(q, k, v, beta, S, o, B, H, d_k, d_v, in_dtype, o_dtype, EFLA_UPDATE_EXACT, stream);
+                             int B, int H, int d_k, int d_v, efla_dtype dtype, efla_stream_t stream) {
+    return efla_decode_step_ex(q, k, v, beta, S, o, B, H, d_k, d_v, dtype, dtype, EFLA_UPDATE_EXACT, stream);
 }
 
 efla_status efla_decode_tokens(const void *q, const void *k, const void *v, const float *beta, float *S, void *o,
@@ -470,13 +496,15 @@ efla_status efla_device_status(efla_stream_t stream) {
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) return cuda_fail(e, "reading the device status word");
     if (h != EFLA_OK) {
-        g_last_error = "a bounded in-kernel wait expired";
+        g_last_error = h == EFLA_ERR_DEVICE_TIMEOUT ? "a bounded in-kernel wait expired"
+                       : h == EFLA_ERR_INVALID_ARG  ? "a kernel met malformed cu_seqlens bounds"
+                                                     : "a kernel recorded an error";
         return static_cast<efla_status>(h);
     }
     return EFLA_OK;
 }
 
-const char *efla_status_string(efla_status s) {
+const char *efla_get_error_string(efla_status s) {
     switch (s) {
         case EFLA_OK: return "EFLA_OK";
         case EFLA_ERR_INVALID_ARG: return "EFLA_ERR_INVALID_ARG: invalid argument";
@@ -486,6 +514,10 @@ const char *efla_status_string(efla_status s) {
     }
     return "unknown efla_status";
 }
+
+void efla_debug_set_wait_limit_ns(unsigned long long ns) { set_wait_limit_ns(ns); }
+
+void efla_debug_set_stall(int stall) { g_debug_stall.store(stall ? 1 : 0, std::memory_order_relaxed); }
 
 const char *efla_last_error(void) { return g_last_error.c_str(); }
 

@@ -13,6 +13,11 @@ namespace efla {
 // Defined in efla_api.cu; kernels in other units reach it through a pointer
 // obtained with cudaGetSymbolAddress, passed as a kernel argument.
 int *device_status_ptr();
+// Bound on the chunk kernel's inter-role waits, in ns (efla_debug_set_wait_limit_ns; 2 s by default).
+unsigned long long wait_limit_ns();
+// Test hook (efla_debug_set_stall): the chunk kernel's MMA thread first waits on a barrier
+// that nothing completes, so that wait runs out and the kernel takes its abort path.
+bool debug_stall();
 
 struct FwdArgs {
     const void *q, *k, *v;

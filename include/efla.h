@@ -45,7 +45,7 @@
 extern "C" {
 #endif
 
-#define EFLA_ABI_VERSION 6
+#define EFLA_ABI_VERSION 7
 
 typedef enum {
     EFLA_OK = 0,
@@ -84,42 +84,47 @@ typedef struct CUstream_st *efla_stream_t;
  * "Error-Free Linear Attention is a Free Lunch" (howistudyai), Step 4).
  * The result equals the token-by-token recurrence up to rounding.
  *
- *   q, k     [B, T, H, d_k]  in_dtype
- *   v        [B, T, H, d_v]  in_dtype
+ *   q, k     [B, T, H, d_k]  dtype
+ *   v        [B, T, H, d_v]  dtype
  *   beta     [B, T, H]       fp32, the per-token step size beta_t (any finite value)
  *   S0       [N, H, d_k, d_v] fp32 (d_v contiguous) initial states, or NULL for zeros
  *   cu_seqlens [N+1] int32 DEVICE array, or NULL.
  *            NULL: N must equal B; sequence b is row b, length T.
  *            non-NULL: B must be 1; sequence n covers packed tokens
  *            cu_seqlens[n] .. cu_seqlens[n+1]-1 of T; cu_seqlens[0] = 0,
- *            cu_seqlens[N] = T, non-decreasing (the caller guarantees this;
- *            it is not read on the host).  Sequences are independent.
- *   o        [B, T, H, d_v]  o_dtype (EFLA_F32 or EFLA_BF16); every token row written
+ *            cu_seqlens[N] = T, non-decreasing.  It is not read on the host:
+ *            a kernel that meets a sequence with bounds outside [0, T] or
+ *            decreasing writes nothing for that sequence and records
+ *            EFLA_ERR_INVALID_ARG in the device status word.  Sequences are
+ *            independent.
+ *   o        [B, T, H, d_v]  dtype (the dtype of q); every token row written
  *   S_T      [N, H, d_k, d_v] fp32 final states, or NULL (not written)
- *   chunk    chunk length; 64 (0 selects 64)
+ *   dtype    EFLA_BF16 or EFLA_F32, the element type of q, k, v and o
+ *   chunk    chunk length: 16, 32, 64 or 128 (0 selects 64)
  *
  * State and all accumulation are fp32.  Supported: d_k, d_v in {32, 64, 128}.
- * bf16 inputs with d_k = d_v = 128 run on the tcgen05 tensor-core chunk
- * kernel; other supported shapes and fp32 inputs run on a CUDA-core fp32
- * kernel.  T = 0 or N = 0 is valid (S_T = S0 or zeros is written).
+ * bf16 inputs with d_k = d_v = 128 and chunk 64 run on the tcgen05
+ * tensor-core chunk kernel; every other supported combination runs the
+ * chunkwise evaluation on CUDA cores in fp32.  T = 0 or N = 0 is valid
+ * (S_T = S0, or zeros, is written).  efla_fwd_chunked_ex below takes an
+ * explicit output dtype (an fp32 o for bf16 inputs) and update rule.
  */
 efla_status efla_fwd_chunked(const void *q, const void *k, const void *v, const float *beta,
                              const float *S0, const int32_t *cu_seqlens, void *o, float *S_T,
                              int B, int T, int H, int d_k, int d_v, int N,
-                             efla_dtype in_dtype, efla_dtype o_dtype, int chunk,
-                             efla_stream_t stream);
+                             efla_dtype dtype, int chunk, efla_stream_t stream);
 
 /*
  * efla_fwd_recurrent -- the same forward, evaluated token by token on CUDA
  * cores in fp32 (howistudyai, "Putting it all together (pipeline)": for each
  * token compute lambda and alpha, update S, emit o).  Same arguments and
- * layouts as efla_fwd_chunked without `chunk`.  Used for fp32 inputs and as an
+ * layouts as efla_fwd_chunked without `chunk` (o in the dtype of q).  An
  * independent GPU evaluation of the recurrence.
  */
 efla_status efla_fwd_recurrent(const void *q, const void *k, const void *v, const float *beta,
                                const float *S0, const int32_t *cu_seqlens, void *o, float *S_T,
                                int B, int T, int H, int d_k, int d_v, int N,
-                               efla_dtype in_dtype, efla_dtype o_dtype, efla_stream_t stream);
+                               efla_dtype dtype, efla_stream_t stream);
 
 /*
  * efla_decode_step -- one token per sequence, state updated IN PLACE.
@@ -130,14 +135,15 @@ efla_status efla_fwd_recurrent(const void *q, const void *k, const void *v, cons
  * Evaluated in one pass over S using o = S^T q + (q.k) u with
  * u = alpha (v - S^T k), which equals S_t^T q after S_t = S + k u^T.
  *
- *   q, k  [B, H, d_k] in_dtype;  v [B, H, d_v] in_dtype;  beta [B, H] fp32
+ *   q, k  [B, H, d_k] dtype;  v [B, H, d_v] dtype;  beta [B, H] fp32
  *   S     [B, H, d_k, d_v] fp32, read and overwritten with the new state
- *   o     [B, H, d_v] o_dtype
- * Supported: d_k, d_v in {32, 64, 128}.
+ *   o     [B, H, d_v] dtype
+ * Supported: d_k, d_v in {32, 64, 128}.  efla_decode_step_ex takes an explicit
+ * output dtype and update rule.
  */
 efla_status efla_decode_step(const void *q, const void *k, const void *v, const float *beta,
                              float *S, void *o, int B, int H, int d_k, int d_v,
-                             efla_dtype in_dtype, efla_dtype o_dtype, efla_stream_t stream);
+                             efla_dtype dtype, efla_stream_t stream);
 
 /*
  * efla_fwd_chunked_scan -- efla_fwd_chunked for few long sequences, split along time.
@@ -238,8 +244,10 @@ efla_status efla_decode_tokens(const void *q, const void *k, const void *v, cons
                                efla_stream_t stream);
 
 /*
- * The three calls above with an explicit update rule (efla_update); the
- * versions without the suffix use EFLA_UPDATE_EXACT.  An unknown rule returns
+ * The three calls above with an explicit output dtype (o_dtype: EFLA_F32 gives
+ * an fp32 o for bf16 inputs, free of the output's own bf16 rounding) and an
+ * explicit update rule (efla_update).  The versions without the suffix use
+ * o_dtype = in_dtype and EFLA_UPDATE_EXACT.  An unknown rule or dtype returns
  * EFLA_ERR_INVALID_ARG.
  */
 efla_status efla_fwd_chunked_ex(const void *q, const void *k, const void *v, const float *beta,
@@ -277,12 +285,31 @@ efla_status efla_prep(const void *k, const void *v, const float *beta, float *la
                       void *ak, void *av, long long n, int d_k, int d_v, efla_dtype dtype,
                       efla_update update, efla_stream_t stream);
 
-/* Reads the library's device status word on `stream` (synchronising that
- * stream), resets it to EFLA_OK and returns what it held. */
+/* Reads the calling thread's current device's status word on `stream`
+ * (synchronising that stream), resets it to EFLA_OK and returns what it held:
+ * EFLA_ERR_DEVICE_TIMEOUT after a bounded in-kernel wait expired, or
+ * EFLA_ERR_INVALID_ARG after a kernel met malformed cu_seqlens.  Each device
+ * has its own word. */
 efla_status efla_device_status(efla_stream_t stream);
 
 /* Static description of a status code; never NULL. */
-const char *efla_status_string(efla_status status);
+const char *efla_get_error_string(efla_status status);
+
+/* Test hook: the bound, in nanoseconds, on each wait of the tensor-core chunk
+ * kernel between its warp roles (0 restores the default of 2 s).  Applies to
+ * launches made after the call, from any host thread.  The waits that let a
+ * kernel's own copies and tensor-core operations finish before it releases
+ * tensor memory keep their 2 s bound whatever this is set to. */
+void efla_debug_set_wait_limit_ns(unsigned long long ns);
+
+/* Test hook: with stall != 0, each launch of the tensor-core chunk kernel made
+ * after the call has its tensor-core issuing thread first wait on a barrier that
+ * nothing completes.  That wait runs out after the wait limit above; the kernel
+ * then abandons its work, lets its own copies and tensor-core operations finish,
+ * records EFLA_ERR_DEVICE_TIMEOUT in the status word and returns (its outputs are
+ * unspecified).  This exercises the bounded-wait path without any fault.
+ * stall = 0 (the default) restores normal launches. */
+void efla_debug_set_stall(int stall);
 
 /* Reason for the most recent failing call on this host thread ("" if none). */
 const char *efla_last_error(void);

@@ -23,11 +23,34 @@ def declared_functions():
     return sorted(set(re.findall(r"\b(efla_[a-z_]+)\s*\(", text)))
 
 
+def declared_params(name):
+    """Parameter names of a function declared in the header, in order."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    m = re.search(r"\b" + name + r"\s*\(([^)]*)\)\s*;", text)
+    assert m, name
+    params = [p.strip() for p in m.group(1).split(",")]
+    return [re.findall(r"[A-Za-z_][A-Za-z_0-9]*", p)[-1] for p in params if p and p != "void"]
+
+
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for n in ("efla_fwd_chunked", "efla_fwd_recurrent", "efla_decode_step", "efla_device_status",
-              "efla_status_string", "efla_last_error", "efla_abi_version"):
+    for n in ("efla_fwd_chunked", "efla_decode_step", "efla_get_error_string", "efla_fwd_recurrent",
+              "efla_device_status", "efla_last_error", "efla_abi_version"):
         assert n in names
+
+
+def test_boundary_signatures():
+    """The two calls of the boundary take exactly these arguments, in this order (o has the
+    dtype of q; no output-dtype argument)."""
+    assert declared_params("efla_fwd_chunked") == [
+        "q", "k", "v", "beta", "S0", "cu_seqlens", "o", "S_T", "B", "T", "H", "d_k", "d_v", "N", "dtype",
+        "chunk", "stream"]
+    assert declared_params("efla_decode_step") == [
+        "q", "k", "v", "beta", "S", "o", "B", "H", "d_k", "d_v", "dtype", "stream"]
+    assert declared_params("efla_get_error_string") == ["status"]
+    text = open(HEADER).read()
+    assert re.search(r"EFLA_OK\s*=\s*0,\s*EFLA_ERR_INVALID_ARG\s*=\s*1,", text)
+    assert re.search(r"EFLA_BF16\s*=\s*0,\s*EFLA_F32\s*=\s*1", text)
 
 
 def test_every_declared_symbol_is_exported(lib):
@@ -42,12 +65,12 @@ def test_abi_version_matches_header(lib):
 
 
 def test_status_strings(lib):
-    lib.efla_status_string.restype = ctypes.c_char_p
-    lib.efla_status_string.argtypes = [ctypes.c_int]
+    lib.efla_get_error_string.restype = ctypes.c_char_p
+    lib.efla_get_error_string.argtypes = [ctypes.c_int]
     for code, name in enumerate(["EFLA_OK", "EFLA_ERR_INVALID_ARG", "EFLA_ERR_UNSUPPORTED", "EFLA_ERR_CUDA",
                                  "EFLA_ERR_DEVICE_TIMEOUT"]):
-        assert lib.efla_status_string(code).decode().startswith(name)
-    assert lib.efla_status_string(99)
+        assert lib.efla_get_error_string(code).decode().startswith(name)
+    assert lib.efla_get_error_string(99)
 
 
 # Fake, never-dereferenced device addresses: validation rejects before any CUDA call.
@@ -56,14 +79,14 @@ Q, K, V, BETA, O, S0, ST, CU = (0x10000000 * (i + 1) for i in range(8))
 
 def _fwd(lib, **kw):
     a = dict(q=Q, k=K, v=V, beta=BETA, S0=None, cu=None, o=O, S_T=None, B=2, T=64, H=4, dk=128, dv=128, N=2,
-             ind=0, od=1, chunk=64, stream=None)
+             dt=0, chunk=64, stream=None)
     a.update(kw)
     vp, ip = ctypes.c_void_p, ctypes.c_int
     f = lib.efla_fwd_chunked
     f.restype = ip
-    f.argtypes = [vp] * 8 + [ip] * 9 + [vp]
+    f.argtypes = [vp] * 8 + [ip] * 8 + [vp]
     return f(a["q"], a["k"], a["v"], a["beta"], a["S0"], a["cu"], a["o"], a["S_T"], a["B"], a["T"], a["H"],
-             a["dk"], a["dv"], a["N"], a["ind"], a["od"], a["chunk"], a["stream"])
+             a["dk"], a["dv"], a["N"], a["dt"], a["chunk"], a["stream"])
 
 
 def _last(lib):
@@ -80,8 +103,9 @@ INVALID, UNSUPPORTED = 1, 2
     (dict(dk=0), INVALID, "positive"),
     (dict(dk=48), UNSUPPORTED, "supported head sizes"),
     (dict(dv=256), UNSUPPORTED, "supported head sizes"),
-    (dict(chunk=32), UNSUPPORTED, "chunk"),
-    (dict(ind=7), INVALID, "dtype"),
+    (dict(chunk=48), UNSUPPORTED, "chunk"),
+    (dict(chunk=-64), UNSUPPORTED, "chunk"),
+    (dict(dt=7), INVALID, "dtype"),
     (dict(N=3), INVALID, "must equal B"),
     (dict(cu=CU, B=2), INVALID, "must be 1"),
     (dict(q=None), INVALID, "non-NULL"),
@@ -101,25 +125,25 @@ def test_fwd_recurrent_rejects(lib):
     vp, ip = ctypes.c_void_p, ctypes.c_int
     f = lib.efla_fwd_recurrent
     f.restype = ip
-    f.argtypes = [vp] * 8 + [ip] * 8 + [vp]
-    assert f(Q, K, V, BETA, None, None, O, None, 2, 64, 4, 128, 96, 2, 0, 1, None) == UNSUPPORTED
-    assert f(None, K, V, BETA, None, None, O, None, 2, 64, 4, 128, 128, 2, 0, 1, None) == INVALID
+    f.argtypes = [vp] * 8 + [ip] * 7 + [vp]
+    assert f(Q, K, V, BETA, None, None, O, None, 2, 64, 4, 128, 96, 2, 0, None) == UNSUPPORTED
+    assert f(None, K, V, BETA, None, None, O, None, 2, 64, 4, 128, 128, 2, 0, None) == INVALID
 
 
 def _dec(lib, **kw):
-    a = dict(q=Q, k=K, v=V, beta=BETA, S=S0, o=O, B=4, H=2, dk=128, dv=128, ind=0, od=1, stream=None)
+    a = dict(q=Q, k=K, v=V, beta=BETA, S=S0, o=O, B=4, H=2, dk=128, dv=128, dt=0, stream=None)
     a.update(kw)
     vp, ip = ctypes.c_void_p, ctypes.c_int
     f = lib.efla_decode_step
     f.restype = ip
-    f.argtypes = [vp] * 6 + [ip] * 6 + [vp]
-    return f(a["q"], a["k"], a["v"], a["beta"], a["S"], a["o"], a["B"], a["H"], a["dk"], a["dv"], a["ind"],
-             a["od"], a["stream"])
+    f.argtypes = [vp] * 6 + [ip] * 5 + [vp]
+    return f(a["q"], a["k"], a["v"], a["beta"], a["S"], a["o"], a["B"], a["H"], a["dk"], a["dv"], a["dt"],
+             a["stream"])
 
 
 @pytest.mark.parametrize("kw,code", [
     (dict(B=-2), INVALID), (dict(H=0), INVALID), (dict(dk=16), UNSUPPORTED), (dict(dv=100), UNSUPPORTED),
-    (dict(S=None), INVALID), (dict(S=S0 + 8), INVALID), (dict(o=S0 + 4096), INVALID), (dict(od=5), INVALID),
+    (dict(S=None), INVALID), (dict(S=S0 + 8), INVALID), (dict(o=S0 + 4096), INVALID), (dict(dt=5), INVALID),
 ])
 def test_decode_rejects(lib, kw, code):
     assert _dec(lib, **kw) == code
@@ -261,3 +285,36 @@ def _bw(lib, **kw):
 def test_bwd_rejects(lib, kw, code):
     assert _bw(lib, **kw) == code
     assert _last(lib)
+
+
+def test_binding_checks_dtypes_and_shapes_before_any_device_call():
+    """The forward wrappers (plain, split and static-scratch) reject a non-fp32 beta, a
+    wrongly shaped S0 and mismatched q/k/v before touching a device."""
+    import torch
+
+    import exact_delta_rule_gb300 as efla
+    B, T, H, d = 1, 8, 2, 128
+    q = torch.zeros((B, T, H, d), dtype=torch.bfloat16)
+    beta = torch.zeros((B, T, H))
+    S0 = torch.zeros((B, H, d, d))
+    for fn in (efla.fwd_chunked, efla.fwd_chunked_scan, efla.fwd_chunked_scan_static):
+        with pytest.raises(efla.EflaError, match="beta must be float32"):
+            fn(q, q, q, beta.bfloat16(), S0)
+        with pytest.raises(efla.EflaError, match="S0 must be float32"):
+            fn(q, q, q, beta, S0[:, :1])
+        with pytest.raises(efla.EflaError, match="S0 must be float32"):
+            fn(q, q, q, beta, S0.double())
+        with pytest.raises(efla.EflaError, match="share a dtype"):
+            fn(q, q.float(), q, beta, S0)
+        with pytest.raises(efla.EflaError, match="shape mismatch"):
+            fn(q, q[:, :4], q, beta, S0)
+        with pytest.raises(efla.EflaError, match="CUDA tensor"):
+            fn(q, q, q, beta, S0)
+
+
+def test_status_word_is_resolved_per_device():
+    """The status word's device address is cached per device index, under a lock."""
+    src = open(os.path.join(ROOT, "exact_delta_rule_gb300", "csrc", "efla_api.cu")).read()
+    body = src[src.index("int *device_status_ptr() {"):]
+    body = body[:body.index("\n}\n")]
+    assert "cudaGetDevice(&dev)" in body and "ptrs[dev]" in body and "lock_guard" in body

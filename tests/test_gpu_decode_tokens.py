@@ -38,7 +38,7 @@ def test_decode_tokens_small(efla, dk, dv, m, dtype):
     if dtype == "f32":
         inp = {k: v.float() for k, v in inp.items()}
     S = S0.to(DEV)
-    o = efla.decode_tokens(*(inp[x].to(DEV) for x in ("q", "k", "v", "beta")), S)
+    o = efla.decode_tokens(*(inp[x].to(DEV) for x in ("q", "k", "v", "beta")), S, o_dtype=torch.float32)
     torch.cuda.synchronize()
     o_ref, S_ref = oracle.fwd(inp["q"], inp["k"], inp["v"], inp["beta"], S0, threads=0)
     check(o, o_ref, in_dtype=dtype, what=f"decode_tokens o m={m}")
@@ -64,9 +64,10 @@ def test_decode_tokens_equals_chained_steps(efla):
     cfg, S0, inp = _case(128, 128, 9, B=4, H=6)
     S1, S2 = S0.to(DEV), S0.to(DEV)
     g = {x: inp[x].to(DEV) for x in ("q", "k", "v", "beta")}
-    o1 = efla.decode_tokens(g["q"], g["k"], g["v"], g["beta"], S1)
+    o1 = efla.decode_tokens(g["q"], g["k"], g["v"], g["beta"], S1, o_dtype=torch.float32)
     o2 = torch.stack([efla.decode_step(g["q"][:, t].contiguous(), g["k"][:, t].contiguous(),
-                                       g["v"][:, t].contiguous(), g["beta"][:, t].contiguous(), S2)
+                                       g["v"][:, t].contiguous(), g["beta"][:, t].contiguous(), S2,
+                                       o_dtype=torch.float32)
                       for t in range(9)], dim=1)
     torch.cuda.synchronize()
     assert torch.allclose(o1, o2, rtol=1e-5, atol=1e-5)
@@ -76,13 +77,13 @@ def test_decode_tokens_equals_chained_steps(efla):
 def test_decode_tokens_zero_tokens_and_empty_batch(efla):
     cfg, S0, inp = _case(64, 64, 0)
     S = S0.to(DEV)
-    o = efla.decode_tokens(*(inp[x].to(DEV) for x in ("q", "k", "v", "beta")), S)
+    o = efla.decode_tokens(*(inp[x].to(DEV) for x in ("q", "k", "v", "beta")), S, o_dtype=torch.float32)
     torch.cuda.synchronize()
     assert o.shape == (3, 0, 5, 64)
     assert torch.equal(S.cpu(), S0)
     e = torch.empty((0, 4, 2, 64), dtype=torch.bfloat16, device=DEV)
     Se = torch.empty((0, 2, 64, 64), device=DEV)
-    o = efla.decode_tokens(e, e, e, torch.empty((0, 4, 2), device=DEV), Se)
+    o = efla.decode_tokens(e, e, e, torch.empty((0, 4, 2), device=DEV), Se, o_dtype=torch.float32)
     assert o.shape == (0, 4, 2, 64)
 
 
@@ -97,7 +98,7 @@ def test_decode_tokens_full_size_sampled(efla):
     S_ref = S0[bs][:, hs].contiguous()
     for call in range(2):
         inp = workloads.make_decode_tokens(16, cfg, first_step=16 * call)
-        o = efla.decode_tokens(*(inp[x].to(DEV) for x in ("q", "k", "v", "beta")), S)
+        o = efla.decode_tokens(*(inp[x].to(DEV) for x in ("q", "k", "v", "beta")), S, o_dtype=torch.float32)
         torch.cuda.synchronize()
         sub = {x: inp[x][bs][:, :, hs].contiguous() for x in ("q", "k", "v", "beta")}
         # the oracle's sequences are the (b, h) pairs of the sample

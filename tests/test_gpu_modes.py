@@ -34,7 +34,7 @@ def test_euler_forward(efla, fn, dtype, d):
     inp = _unit_keys(workloads.small_fwd(dtype, B=2, T=150, H=2, d=d, seed=71))
     g = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
     f = efla.fwd_chunked if fn == "chunked" else efla.fwd_recurrent
-    o, S = f(g["q"], g["k"], g["v"], g["beta"], g["S0"], update="euler")
+    o, S = f(g["q"], g["k"], g["v"], g["beta"], g["S0"], update="euler", o_dtype=torch.float32)
     torch.cuda.synchronize()
     o_ref, S_ref = oracle.fwd(inp["q"], inp["k"], inp["v"], inp["beta"], inp["S0"], update="euler")
     check(o, o_ref, in_dtype=dtype, what=f"euler o {fn}")
@@ -51,7 +51,7 @@ def test_euler_decode(efla):
     k = inp["k"].float()
     inp["k"] = (k / k.norm(dim=-1, keepdim=True)).to(torch.bfloat16)
     S = S0.to(DEV)
-    o = efla.decode_step(*(inp[x].to(DEV) for x in ("q", "k", "v", "beta")), S, update="euler")
+    o = efla.decode_step(*(inp[x].to(DEV) for x in ("q", "k", "v", "beta")), S, update="euler", o_dtype=torch.float32)
     torch.cuda.synchronize()
     o_ref, S_ref = oracle.decode_step(inp["q"], inp["k"], inp["v"], inp["beta"], S0, update="euler")
     check(o, o_ref, in_dtype="bf16", what="euler decode o")

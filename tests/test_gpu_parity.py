@@ -111,12 +111,12 @@ def test_state_alias_and_no_state(efla):
     inp = workloads.small_fwd("bf16", B=2, T=100, H=2, d=128, seed=31)
     g = _dev(inp)
     S = g["S0"].clone()
-    o, S_out = efla.fwd_chunked(g["q"], g["k"], g["v"], g["beta"], S, S_T=S)
+    o, S_out = efla.fwd_chunked(g["q"], g["k"], g["v"], g["beta"], S, S_T=S, o_dtype=torch.float32)
     torch.cuda.synchronize()
     assert S_out.data_ptr() == S.data_ptr()
     o_ref, S_ref = _oracle(inp)
     check(S, S_ref, in_dtype="bf16", what="S_T aliased with S0")
-    o2, none = efla.fwd_chunked(g["q"], g["k"], g["v"], g["beta"], g["S0"], return_state=False)
+    o2, none = efla.fwd_chunked(g["q"], g["k"], g["v"], g["beta"], g["S0"], return_state=False, o_dtype=torch.float32)
     torch.cuda.synchronize()
     assert none is None
     check(o2, o_ref, in_dtype="bf16", what="o without S_T")
@@ -159,7 +159,7 @@ def test_decode_small(efla, dk, dv, dtype):
         inp = workloads.make_decode_step(step, cfg)
         if dtype == "f32":
             inp = {k: v.float() for k, v in inp.items()}
-        o = efla.decode_step(*(inp[x].to(DEV) for x in ("q", "k", "v", "beta")), S)
+        o = efla.decode_step(*(inp[x].to(DEV) for x in ("q", "k", "v", "beta")), S, o_dtype=torch.float32)
         torch.cuda.synchronize()
         o_ref, S_ref = oracle.decode_step(inp["q"], inp["k"], inp["v"], inp["beta"], S_ref)
         check(o, o_ref, in_dtype=dtype, what=f"decode o step {step}")

@@ -31,6 +31,7 @@ def _dev(inp):
 
 def _scan(efla, inp, segments, **kw):
     g = _dev(inp)
+    kw.setdefault("o_dtype", torch.float32)
     o, S = efla.fwd_chunked_scan(g["q"], g["k"], g["v"], g["beta"], g["S0"], segments=segments, **kw)
     torch.cuda.synchronize()
     return o, S
@@ -67,7 +68,7 @@ def test_scan_euler_unit_keys(efla):
 def test_scan_matches_unsplit_and_one_piece_path(efla):
     inp = workloads.small_fwd("bf16", B=1, T=1500, H=4, d=128, seed=12)
     g = _dev(inp)
-    o1, S1 = efla.fwd_chunked(g["q"], g["k"], g["v"], g["beta"], g["S0"])
+    o1, S1 = efla.fwd_chunked(g["q"], g["k"], g["v"], g["beta"], g["S0"], o_dtype=torch.float32)
     o2, S2 = _scan(efla, inp, 6)
     o3, S3 = _scan(efla, inp, 1)  # one piece: the plain path
     torch.cuda.synchronize()
@@ -83,7 +84,7 @@ def test_scan_aliased_state_and_caller_workspace(efla):
     assert G == 3 and need > 0
     ws = torch.full((need,), 0x7f, dtype=torch.uint8, device=DEV)  # contents must not matter
     S = g["S0"].clone()
-    o, S_out = efla.fwd_chunked_scan(g["q"], g["k"], g["v"], g["beta"], S, S_T=S, segments=3, workspace=ws)
+    o, S_out = efla.fwd_chunked_scan(g["q"], g["k"], g["v"], g["beta"], S, S_T=S, segments=3, workspace=ws, o_dtype=torch.float32)
     torch.cuda.synchronize()
     o_ref, S_ref = oracle.fwd(inp["q"], inp["k"], inp["v"], inp["beta"], inp["S0"], threads=0)
     check(o, o_ref, in_dtype="bf16", what="scan o, S0 aliased with S_T")
