@@ -92,9 +92,8 @@ static_assert(SMEM_ALLOC <= 232448, "exceeds the 227 KB per-CTA shared memory li
 constexpr uint32_t TM_S = 0;    // S^T fp32                                       128 columns
 constexpr uint32_t TM_SA = 128; // S^T as bf16 operand: hi 64, lo 64; then the two
                                 // partial sums of u^T (fp32, 64 + 64)
-constexpr uint32_t TM_X = 256;  // D^T fp32 (64), then D^T bf16 hi 32 + lo 32, then u^T bf16 hi 32 + lo 32
-constexpr uint32_t TM_O = 320;  // O^T fp32 (64); adjacent to TM_X: D^T and O^T share one product
-constexpr uint32_t TM_OB = 384; // second O^T accumulator (the u_hi P_lo term)    64 columns
+constexpr uint32_t TM_X = 256;  // X^T fp32 (64), then (-X)^T bf16 hi 32 + lo 32, then u^T bf16 hi 32 + lo 32
+constexpr uint32_t TM_O = 320;  // O^T fp32 of even chunks (64); odd chunks at TM_O + 64
 constexpr uint32_t TM_G = 448;  // [K;Q] K^T fp32                                  64 columns
 constexpr uint32_t TM_COLS = 512;
 
@@ -135,16 +134,17 @@ struct Bars {
     uint64_t x_done;         // X^T = S^T K^T
     uint64_t u_done;         // U^^T
     uint64_t s_done;         // S^T += u^T K
-    uint64_t o_done;         // O^T of the chunk complete
     uint64_t prep_ready[2];  // T', P, gate terms and the zeroed tail of a chunk written
     uint64_t sa_ready;       // state warpgroup wrote S^T hi/lo        (128 arrivals)
-    uint64_t o_free;         // state warpgroup read O^T of the chunk  (128 arrivals)
     uint64_t r_ready;        // state warpgroup wrote (V - X)^T hi/lo  (128 arrivals)
     uint64_t u_ready;        // state warpgroup wrote u^T hi/lo        (128 arrivals)
     uint64_t drain[2];       // all MMAs of the MMA thread / of the prep thread complete
     uint64_t s_free[NSTAGE];  // the state update of a chunk complete: its K/Q/V stage is free
-    uint64_t ost_free[2];     // a chunk's T''/P buffer is free: its last products and the TMA
-                              // stores of its o tile have read it (4 arrivals)
+    // Per chunk parity b (chunk c uses O^T buffer c & 1 and T''/P buffer c & 1):
+    uint64_t o_done[2];       // the chunk's O^T products complete (its P part is free again)
+    uint64_t o_free[2];       // the state warpgroup has read the chunk's O^T  (128 arrivals)
+    uint64_t stg_free[2];     // the TMA stores of the chunk's o tile have read their staging,
+                              // the T'' part of its buffer (4 arrivals)
     uint64_t never;           // never completed (the debug_stall test hook waits on it)
 };
 static_assert(sizeof(Bars) <= 224, "mbarrier block exceeds its slot");
@@ -206,38 +206,54 @@ __device__ __forceinline__ void split_pack(const float *x, uint32_t *hi, uint32_
 // Each step applies
 //   [[L1, 0], [B, L2]]^{-1} = [[L1^{-1}, 0], [-L2^{-1} B L1^{-1}, L2^{-1}]]
 // for unit lower-triangular L1, L2:
-//   1. the four diagonal 16x16 blocks by column substitution: warps 0 and 1 of the
-//      prep, two blocks per warp, one lane per column holding the whole column in
+//   1. the eight diagonal 8x8 blocks by column substitution: warps 0 and 1 of the
+//      prep, four blocks per warp, one lane per column holding the whole column in
 //      registers (no shuffles; the other warps wait at the barrier);
-//   2. blocks (1,0) and (3,2) of 16:  T~_IJ = -T~_II (A~_IJ T~_JJ);
-//   3. the lower-left 32x32 block:    T~_21 = -T~_22 (A~_21 T~_11)  (32x32 blocks).
-// Steps 2 and 3 are register-tiled fp32 products.
+//   2. the off-diagonal 8x8 block of each diagonal 16x16 block, one output per thread;
+//   3. blocks (1,0) and (3,2) of 16:  T~_IJ = -T~_II (A~_IJ T~_JJ);
+//   4. the lower-left 32x32 block:    T~_21 = -T~_22 (A~_21 T~_11)  (32x32 blocks).
+// Steps 3 and 4 are register-tiled fp32 products.
 __device__ __forceinline__ void invert_unit_lower(float *At, int pi) {
     float *Y = At + 32;  // [32][AT_LD] rows 0-31, columns 32-63
     const int lane = pi & 31, pw = pi >> 5;
-    if (pw < 2) {
-        const int B0 = 16 * (2 * pw + (lane >> 4)), c = lane & 15;
-        float col[16];  // col[s] = T~[B0 + s][B0 + c]
+    if (pw < 2) {  // 1. the eight diagonal 8x8 blocks, one lane per column
+        const int B0 = 8 * (4 * pw + (lane >> 3)), c = lane & 7;
+        float col[8];  // col[s] = T~[B0 + s][B0 + c]
 #pragma unroll
-        for (int s = 0; s < 16; ++s) col[s] = s == c ? 1.f : 0.f;
+        for (int s = 0; s < 8; ++s) col[s] = s == c ? 1.f : 0.f;
 #pragma unroll
-        for (int t = 1; t < 16; ++t) {
-            const float *row = At + (B0 + t) * AT_LD + B0;
-            asm volatile("" : "+l"(row));  // keeps each step's loads in that step (register pressure)
-            float acc = 0.f;
+        for (int t = 1; t < 8; ++t) {
+            const float4 r0 = *reinterpret_cast<const float4 *>(At + (B0 + t) * AT_LD + B0);
+            const float4 r1 = *reinterpret_cast<const float4 *>(At + (B0 + t) * AT_LD + B0 + 4);
+            const float a[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+            float a0 = 0.f, a1 = 0.f;  // A~[t][s] for s < t; col[s] = 0 for s < c
 #pragma unroll
-            for (int s4 = 0; s4 < t; s4 += 4) {  // A~[t][s] for s < t; col[s] = 0 for s < c
-                const float4 a = *reinterpret_cast<const float4 *>(row + s4);
-                acc = fmaf(a.x, col[s4], acc);
-                if (s4 + 1 < t) acc = fmaf(a.y, col[s4 + 1], acc);
-                if (s4 + 2 < t) acc = fmaf(a.z, col[s4 + 2], acc);
-                if (s4 + 3 < t) acc = fmaf(a.w, col[s4 + 3], acc);
+            for (int s = 0; s < 8; s += 2) {
+                if (s < t) a0 = fmaf(a[s], col[s], a0);
+                if (s + 1 < t) a1 = fmaf(a[s + 1], col[s + 1], a1);
             }
-            col[t] = t > c ? -acc : col[t];
+            col[t] = t > c ? -(a0 + a1) : col[t];
         }
-        __syncwarp();  // both blocks of this warp have been read
+        __syncwarp();  // the four blocks of this warp have been read
 #pragma unroll
-        for (int s = 0; s < 16; ++s) At[(B0 + s) * AT_LD + B0 + c] = col[s];
+        for (int s = 0; s < 8; ++s) At[(B0 + s) * AT_LD + B0 + c] = col[s];
+    }
+    named_bar(BAR_PREP, 256);
+    {  // 2. 8 -> 16 within each diagonal 16x16 block: T~_21 = -T~_22 (A~_21 T~_11), 8x8 blocks;
+       //    one output per thread, the intermediate in the unused upper-right block
+        const int q = pi >> 6, r = (pi >> 3) & 7, cc = pi & 7;
+        const int R0 = 16 * q;
+        const float *arow = At + (R0 + 8 + r) * AT_LD + R0;  // A~_21 row r
+        float y = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) y = fmaf(arow[k], At[(R0 + k) * AT_LD + R0 + cc], y);
+        At[(8 * q + r) * AT_LD + 32 + cc] = y;
+        named_bar(BAR_PREP, 256);
+        const float *trow = At + (R0 + 8 + r) * AT_LD + R0 + 8;  // T~_22 row r
+        float z = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) z = fmaf(trow[k], At[(8 * q + k) * AT_LD + 32 + cc], z);
+        At[(R0 + 8 + r) * AT_LD + R0 + cc] = -z;
     }
     named_bar(BAR_PREP, 256);
     {
@@ -406,22 +422,21 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
             mbar_init(&bars->tma_full[i], 1);
             mbar_init(&bars->s_free[i], 1);
         }
-        mbar_init(&bars->ost_free[0], 4);
-        mbar_init(&bars->ost_free[1], 4);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars->o_done[i], 1);
+            mbar_init(&bars->o_free[i], 128);
+            mbar_init(&bars->stg_free[i], 4);
+            mbar_init(&bars->prep_ready[i], 1);
+            mbar_init(&bars->drain[i], 1);
+        }
         mbar_init(&bars->g_done, 1);
         mbar_init(&bars->g_free, 1);
         mbar_init(&bars->x_done, 1);
         mbar_init(&bars->u_done, 1);
         mbar_init(&bars->s_done, 1);
-        mbar_init(&bars->o_done, 1);
-        mbar_init(&bars->prep_ready[0], 1);
-        mbar_init(&bars->prep_ready[1], 1);
         mbar_init(&bars->sa_ready, 128);
-        mbar_init(&bars->o_free, 128);
         mbar_init(&bars->r_ready, 128);
         mbar_init(&bars->u_ready, 128);
-        mbar_init(&bars->drain[0], 1);
-        mbar_init(&bars->drain[1], 1);
         mbar_init(&bars->never, 1);
         fence_mbar_init();
         *abort_flag = 0;
@@ -492,9 +507,10 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
                 }
             }
             ok = wait_bar_warp(&bars->g_done, c & 1, abort_flag, wait_ns);
-            // This chunk's T''/P buffer was last read by chunk c-2's products (P) and o stores
-            // (T'' part); the state warpgroup releases it after both.
-            if (c >= 2) ok = wait_bar_warp(&bars->ost_free[c & 1], ((c - 2) >> 1) & 1, abort_flag, wait_ns) && ok;
+            // This chunk's T''/P buffer was last read by chunk c-2: its P part by that chunk's
+            // O^T products (o_done), its T'' part by the stores of that chunk's o tile (stg_free,
+            // waited before T'' is written below).
+            if (c >= 2) ok = wait_bar_warp(&bars->o_done[c & 1], ((c - 2) >> 1) & 1, abort_flag, wait_ns) && ok;
             tc_fence_after();
             {
                 float g[32];
@@ -558,6 +574,7 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
             }
             named_bar(BAR_PREP, 256);
             invert_unit_lower(At, pi);
+            if (c >= 2) ok = wait_bar_warp(&bars->stg_free[c & 1], ((c - 2) >> 1) & 1, abort_flag, wait_ns) && ok;
             {  // T'' = diag(1/n) T~ diag(gamma/n), lower triangle, as bf16 hi/lo [t][s]
                 const int t = pi >> 2, s0 = (pi & 3) * 16;
                 uint8_t *hi = sm + OFF_TPP + buf * TPP_BYTES, *lo = hi + 8192;
@@ -598,8 +615,8 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
         // Per chunk c, the dependency chain through the state is
         //   S -> X = K S -> V - X -> U^ -> u -> S + K^T u;
         // this warpgroup forms the operands of each link in TMEM and the MMA warp
-        // issues the products.  The outputs O = Q S + P u are formed beside the
-        // chain and written out while the next chunk's X is computed.
+        // issues the products.  The outputs of chunk c - 1 are read out and sent while the
+        // tensor core updates the state of chunk c (off the chain).
         const int j = tid, lane = tid & 31;
         const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
         {  // initial state -> TMEM (S^T: lane j holds column j of S)
@@ -613,130 +630,119 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
             }
             tmem_st_wait();
         }
-        // O^T of chunk cc (fp32 in TMEM) -> o.  Each warp stages its own 32 columns
-        // ([64 t][32] in its 8 KB slice of the staging buffer) and its lane 0 sends
-        // them with one TMA store, so no cross-warp synchronisation is needed.  A
-        // partial chunk of a packed batch is written with plain stores instead (a
-        // TMA box would spill into the next sequence).
-        // The second O accumulator starts every chunk at zero (the first is overwritten
-        // by the chunk's first product).
-        auto clear_ob = [&]() {
-            float z[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) z[i] = 0.f;
-            tmem_st32(lane_base + TM_OB, z);
-            tmem_st32(lane_base + TM_OB + 32, z);
-            tmem_st_wait();
-        };
-        clear_ob();
+        // O^T of chunk cc (fp32 in TMEM buffer cc & 1) -> o.  Each warp stages its own 32
+        // columns in its 4 KB slice of the T'' part of buffer cc & 1 (free: the chunk's u
+        // products have read T'') and its lane 0 sends them with TMA stores, so no
+        // cross-warp synchronisation is needed.  A bf16 tile (64 tokens x 32 columns) leaves
+        // in one store, an fp32 tile in two halves of 32 tokens.  A partial chunk of a packed
+        // batch is written with plain stores instead (a TMA box would spill into the next
+        // sequence).  The staging is released later (release_staging), once the stores have
+        // read it.
         auto epilogue = [&](int cc) {
-            if (!write_o) {  // map modes: nothing to store; release O^T and the staging buffer
+            const uint32_t ob = TM_O + (uint32_t)(cc & 1) * 64;
+            if (!write_o) {  // map modes: nothing to store
                 tc_fence_before();
-                mbar_arrive(&bars->o_free);
-                if (lane == 0) mbar_arrive(&bars->ost_free[cc & 1]);
+                mbar_arrive(&bars->o_free[cc & 1]);
                 return;
             }
             const long t0c = bos + (long)cc * C;
             const int vc = (int)min((long)C, eos - t0c);
             float ov[32], ow[32];
-            {
-                float t1[32];
-                tmem_ld32(lane_base + TM_O, ov);
-                tmem_ld32(lane_base + TM_OB, t1);
-                tmem_ld_wait();
-#pragma unroll
-                for (int t = 0; t < 32; ++t) ov[t] += t1[t];
-                tmem_ld32(lane_base + TM_O + 32, ow);
-                tmem_ld32(lane_base + TM_OB + 32, t1);
-                tmem_ld_wait();
-#pragma unroll
-                for (int t = 0; t < 32; ++t) ow[t] += t1[t];
-            }
+            tmem_ld32(lane_base + ob, ov);
+            tmem_ld32(lane_base + ob + 32, ow);
+            tmem_ld_wait();
             tc_fence_before();
-            mbar_arrive(&bars->o_free);  // the next chunk's first product may overwrite O^T
-            // The tile leaves in two halves of 32 tokens, staged in the T'' part of the chunk's
-            // T''/P buffers (free once its last product completed): the P part stays free for
-            // the prep of chunk cc + 2 as soon as those products are done.
+            mbar_arrive(&bars->o_free[cc & 1]);  // chunk cc + 2's first product may overwrite this O^T
             uint8_t *slice = sm + OFF_TPP + (cc & 1) * TPP_BYTES + warp * 4096;
-            auto send_half = [&](const float (&x)[32], int t_off) {
-                if (t_off > 0) {  // the first half's store has read the slice
-                    if (lane == 0) bulk_wait_read0();
-                    __syncwarp();
+            const bool full = p.cu_seqlens == nullptr || vc == C;
+            auto store_rows = [&](int t_off, int n) {  // plain stores of staged rows (partial packed chunk)
+#pragma unroll 1
+                for (int t = 0; t < n; t = opaque(t + 1)) {
+                    const size_t rw = ((size_t)b * p.T + (size_t)(t0c + t_off + t)) * p.H + h;
+                    if (OUT_BF16)
+                        static_cast<__nv_bfloat16 *>(p.o)[rw * D + j] =
+                            reinterpret_cast<const __nv_bfloat16 *>(slice)[(t_off + t) * 32 + lane];
+                    else
+                        static_cast<float *>(p.o)[rw * D + j] = reinterpret_cast<const float *>(slice)[t * 32 + lane];
                 }
-                if (OUT_BF16) {
-                    __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(slice) + lane;
+            };
+            if (OUT_BF16) {
+                __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(slice) + lane;
 #pragma unroll
-                    for (int t = 0; t < 32; ++t) stg[t * 32] = __float2bfloat16_rn(x[t]);
-                } else {
-                    float *stg = reinterpret_cast<float *>(slice) + lane;
+                for (int t = 0; t < 32; ++t) stg[t * 32] = __float2bfloat16_rn(ov[t]);
 #pragma unroll
-                    for (int t = 0; t < 32; ++t) stg[t * 32] = x[t];
-                }
-                if (p.cu_seqlens == nullptr || vc == C) {
+                for (int t = 0; t < 32; ++t) stg[(32 + t) * 32] = __float2bfloat16_rn(ow[t]);
+                if (full) {
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_4d(&p.map_o, slice, warp * 32, h, (int)(t0c + t_off), (int)b);
+                        tma_store_4d(&p.map_o, slice, warp * 32, h, (int)t0c, (int)b);
                         bulk_commit();
                     }
-                } else {  // partial chunk of a packed batch: rows past vc belong to the next sequence
+                } else {
                     __syncwarp();
-                    const int n = min(32, vc - t_off);
-#pragma unroll 1
-                    for (int t = 0; t < n; t = opaque(t + 1)) {
-                        const size_t rw = ((size_t)b * p.T + (size_t)(t0c + t_off + t)) * p.H + h;
-                        if (OUT_BF16)
-                            static_cast<__nv_bfloat16 *>(p.o)[rw * D + j] =
-                                reinterpret_cast<const __nv_bfloat16 *>(slice)[t * 32 + lane];
-                        else
-                            static_cast<float *>(p.o)[rw * D + j] =
-                                reinterpret_cast<const float *>(slice)[t * 32 + lane];
+                    store_rows(0, vc);
+                    __syncwarp();
+                }
+            } else {
+                auto send_half = [&](const float (&x)[32], int t_off) {
+                    if (t_off > 0) {  // the first half's store has read the slice
+                        if (lane == 0) bulk_wait_read0();
+                        __syncwarp();
                     }
-                    __syncwarp();
-                }
-            };
-            send_half(ov, 0);
-            if (vc > 32) send_half(ow, 32);
-            if (lane == 0) {
-                bulk_wait_read0();  // the slice may be rewritten by the prep two chunks on
-                mbar_arrive(&bars->ost_free[cc & 1]);
+                    float *stg = reinterpret_cast<float *>(slice) + lane;
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) stg[t * 32] = x[t];
+                    if (full) {
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_4d(&p.map_o, slice, warp * 32, h, (int)(t0c + t_off), (int)b);
+                            bulk_commit();
+                        }
+                    } else {
+                        __syncwarp();
+                        store_rows(t_off, min(32, vc - t_off));
+                        __syncwarp();
+                    }
+                };
+                send_half(ov, 0);
+                if (vc > 32) send_half(ow, 32);
             }
-            clear_ob();  // before this warpgroup's next u_ready, which precedes the next O_b product
         };
-        // One pass per chunk c plus a final pass: the operands of chunk c, and the
-        // outputs of chunk c-1 (one call site keeps the per-chunk code small).
+        // The stores of chunk cc's o tile have read the staging: the prep of chunk cc + 2 may
+        // write its T'' there.
+        auto release_staging = [&](int cc) {
+            if (lane == 0) {
+                bulk_wait_read0();
+                mbar_arrive(&bars->stg_free[cc & 1]);
+            }
+            __syncwarp();
+        };
         bool ok = true;
-        for (int c = 0; c <= nchunks && ok; ++c) {
-            const bool live = c < nchunks;
-            if (live) {
-                // The S^T operand needs only the previous state update, not this chunk's prep.
-                if (c > 0) ok = wait_bar_warp(&bars->s_done, (c - 1) & 1, abort_flag, wait_ns);
-                tc_fence_after();
-                // S^T -> bf16 hi/lo operand in TMEM, 32 columns of S^T (16 operand columns) at a time
+        for (int c = 0; c < nchunks && ok; ++c) {
+            // The S^T operand needs only the previous state update, not this chunk's prep.
+            if (c > 0) ok = wait_bar_warp(&bars->s_done, (c - 1) & 1, abort_flag, wait_ns);
+            if (!ok) break;
+            tc_fence_after();
+            // S^T -> bf16 hi/lo operand in TMEM, 32 columns of S^T (16 operand columns) at a time
 #pragma unroll 1
-                for (int g = 0; g < 4; g = opaque(g + 1)) {
-                    float sv[32];
-                    uint32_t hi[16], lo[16];
-                    tmem_ld32(lane_base + TM_S + g * 32, sv);
-                    tmem_ld_wait();
-                    split_pack<16>(sv, hi, lo);
-                    tmem_st16u(lane_base + TM_SA + g * 16, hi);
-                    tmem_st16u(lane_base + TM_SA + 64 + g * 16, lo);
-                }
-                tmem_st_wait();
-                tc_fence_before();
-                mbar_arrive(&bars->sa_ready);
+            for (int g = 0; g < 4; g = opaque(g + 1)) {
+                float sv[32];
+                uint32_t hi[16], lo[16];
+                tmem_ld32(lane_base + TM_S + g * 32, sv);
+                tmem_ld_wait();
+                split_pack<16>(sv, hi, lo);
+                tmem_st16u(lane_base + TM_SA + g * 16, hi);
+                tmem_st16u(lane_base + TM_SA + 64 + g * 16, lo);
             }
-            if (c > 0) {  // outputs of chunk c-1 leave while X of chunk c is computed
-                ok = ok && wait_bar_warp(&bars->o_done, (c - 1) & 1, abort_flag, wait_ns);
-                if (!ok) break;
-                tc_fence_after();
-                epilogue(c - 1);
-            }
-            if (!live) break;
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(&bars->sa_ready);
+            if (c >= 2) release_staging(c - 2);  // its stores were issued during chunk c - 1
             const long tok0 = bos + (long)c * C;
             const int valid = (int)min((long)C, eos - tok0);
-            ok = ok && wait_bar_warp(&bars->x_done, c & 1, abort_flag, wait_ns);
+            ok = wait_bar_warp(&bars->x_done, c & 1, abort_flag, wait_ns);
             if (!ok) break;
             tc_fence_after();
             // (-X)^T = -(K S)^T -> bf16 hi/lo operand in TMEM (rows past the sequence end are zero),
@@ -761,7 +767,7 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(&bars->r_ready);
-            ok = ok && wait_bar_warp(&bars->u_done, c & 1, abort_flag, wait_ns);
+            ok = wait_bar_warp(&bars->u_done, c & 1, abort_flag, wait_ns);
             if (!ok) break;
             tc_fence_after();
             // u^T = U1 + U2 -> bf16 hi/lo operand in TMEM
@@ -781,9 +787,23 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(&bars->u_ready);
+            // the outputs of the previous chunk leave while the tensor core updates the state
+            if (c >= 1) {
+                ok = wait_bar_warp(&bars->o_done[(c - 1) & 1], ((c - 1) >> 1) & 1, abort_flag, wait_ns);
+                if (!ok) break;
+                tc_fence_after();
+                epilogue(c - 1);
+            }
+        }
+        if (ok && nchunks >= 1) {  // the last chunk's outputs (its o_done also covers the last state update)
+            ok = wait_bar_warp(&bars->o_done[(nchunks - 1) & 1], ((nchunks - 1) >> 1) & 1, abort_flag, wait_ns);
+            if (ok) {
+                tc_fence_after();
+                epilogue(nchunks - 1);
+            }
         }
         if (!ok) *abort_flag = 1;
-        if (ok && stp) {  // final state (every product has completed: o_done of the last chunk)
+        if (ok && stp) {  // final state
 #pragma unroll 1
             for (int g = 0; g < 4; g = opaque(g + 1)) {
                 float s32[32];
@@ -823,25 +843,45 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
                    globaltimer_ns() - t0 < WAIT_NS) {
             }
         }
-    } else if (tid == 256) {
-        // ================================ MMA warp (one thread) ================================
-        // Its issue loops are fully unrolled: descriptors fold to constants, which leaves this
-        // thread (sharing its sub-partition with busy warps) fewer instructions per MMA.
+    } else if (warp == 8) {
+        // =============================== MMA warp ===============================
+        // The whole warp runs this role converged; one elected lane issues each tcgen05
+        // instruction (faster than a lone thread in a divergent branch).  Its issue loops are
+        // fully unrolled, so the descriptors fold to constants.
         bool ok = true;
         // Gram products of full chunks up to `limit`, each once the prep has read the
-        // previous one (one TM_G buffer) and the chunk's tile has landed.
+        // previous one (one TM_G buffer) and the chunk's tile has landed.  With `block`
+        // false it issues only what is ready now and never waits.
         int g_next = 0;
-        auto issue_grams = [&](int limit) {
+        auto issue_grams = [&](int limit, bool block) {
             while (ok && g_next <= limit && g_next < nchunks && eos - (bos + (long)g_next * C) >= C) {
-                if (g_next > 0 && !(ok = wait_bar(&bars->g_free, (g_next - 1) & 1, abort_flag, wait_ns))) break;
-                if (!(ok = wait_bar(&bars->tma_full[g_next % NSTAGE], (g_next / NSTAGE) & 1, abort_flag, wait_ns))) break;
+                if (!block) {
+                    const bool ready = (g_next == 0 || mbar_try_wait(&bars->g_free, (g_next - 1) & 1)) &&
+                                       mbar_try_wait(&bars->tma_full[g_next % NSTAGE], (g_next / NSTAGE) & 1);
+                    if (!__all_sync(0xffffffffu, ready)) break;
+                } else {
+                    if (g_next > 0 && !(ok = wait_bar_warp(&bars->g_free, (g_next - 1) & 1, abort_flag, wait_ns))) break;
+                    if (!(ok = wait_bar_warp(&bars->tma_full[g_next % NSTAGE], (g_next / NSTAGE) & 1, abort_flag,
+                                             wait_ns)))
+                        break;
+                }
                 tc_fence_after();
-                issue_gram(tmem, s_sm, g_next, bars);
+                {
+                    const uint32_t kq = s_sm + OFF_STAGE + (g_next % NSTAGE) * STAGE_BYTES;
+                    const uint32_t idesc = idesc_bf16_f32(128, 64, 0, 0);
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+                        mma_bf16_e(tmem + TM_G, smem_desc(kq + off, 16, 1024), smem_desc(kq + off, 16, 1024), idesc,
+                                   ks > 0);
+                    }
+                    mma_commit_e(&bars->g_done);
+                }
                 ++g_next;
             }
         };
-        if (p.debug_stall) ok = wait_bar(&bars->never, 0, abort_flag, wait_ns);
-        issue_grams(0);
+        if (p.debug_stall) ok = wait_bar_warp(&bars->never, 0, abort_flag, wait_ns);
+        issue_grams(0, true);
         for (int c = 0; c < nchunks && ok; ++c) {
             const int st = c % NSTAGE, buf = c & 1;
             const uint32_t kq_s = s_sm + OFF_STAGE + st * STAGE_BYTES;
@@ -849,27 +889,44 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
             // X needs the stage and the state only; a partial chunk also needs its zeroed tail,
             // which its prep writes before prep_ready
             const bool partial = eos - (bos + (long)c * C) < C;
-            if (!(ok = wait_bar(partial ? &bars->prep_ready[buf] : &bars->tma_full[st],
-                                partial ? (c >> 1) & 1 : (c / NSTAGE) & 1, abort_flag, wait_ns))) break;
-            if (!(ok = wait_bar(&bars->sa_ready, c & 1, abort_flag, wait_ns))) break;
-            if (c > 0 && !(ok = wait_bar(&bars->o_free, (c - 1) & 1, abort_flag, wait_ns))) break;
+            if (!(ok = wait_bar_warp(partial ? &bars->prep_ready[buf] : &bars->tma_full[st],
+                                     partial ? (c >> 1) & 1 : (c / NSTAGE) & 1, abort_flag, wait_ns)))
+                break;
+            if (!(ok = wait_bar_warp(&bars->sa_ready, c & 1, abort_flag, wait_ns))) break;
             tc_fence_after();
-            {  // [X^T | O^T] = S^T [K; Q]^T: one N = 128 product over the stage's [K; Q] rows
-                const uint32_t idesc = idesc_bf16_f32(128, 128, 0, 0);
+            const uint32_t idesc64 = idesc_bf16_f32(128, 64, 0, 0);
+            {  // X^T = S^T K^T (the chain): issued as soon as the S^T operand is written
 #pragma unroll
                 for (int part = 0; part < 2; ++part)
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks) {
                         const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-                        mma_bf16_ts(tmem + TM_X, tmem + TM_SA + part * 64 + ks * 8, smem_desc(kq_s + off, 16, 1024),
-                                    idesc, (part | ks) != 0);
+                        mma_bf16_ts_e(tmem + TM_X, tmem + TM_SA + part * 64 + ks * 8, smem_desc(kq_s + off, 16, 1024),
+                                      idesc64, (part | ks) != 0);
                     }
-                mma_commit(&bars->x_done);
+                mma_commit_e(&bars->x_done);
+            }
+            issue_grams(c + 1, false);  // the next chunk's Gram product, if its inputs are ready
+            // O1^T = S^T Q^T (off the chain) into this chunk's O^T buffer, once chunk c - 2's
+            // outputs have been read out of it
+            const uint32_t ob = TM_O + (uint32_t)(c & 1) * 64;
+            if (write_o) {
+                if (c >= 2 && !(ok = wait_bar_warp(&bars->o_free[c & 1], ((c - 2) >> 1) & 1, abort_flag, wait_ns)))
+                    break;
+                tc_fence_after();
+#pragma unroll
+                for (int part = 0; part < 2; ++part)
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32 + 8192;
+                        mma_bf16_ts_e(tmem + ob, tmem + TM_SA + part * 64 + ks * 8, smem_desc(kq_s + off, 16, 1024),
+                                      idesc64, (part | ks) != 0);
+                    }
             }
             // the rest of the chunk needs its prep (T'', P)
-            if (!(ok = wait_bar(&bars->prep_ready[buf], (c >> 1) & 1, abort_flag, wait_ns))) break;
+            if (!(ok = wait_bar_warp(&bars->prep_ready[buf], (c >> 1) & 1, abort_flag, wait_ns))) break;
             tc_fence_after();
-            issue_grams(c + 1);
+            issue_grams(c + 1, true);
             if (!ok) break;
             {  // [U1 | U2] = V^T [T''_hi; T''_lo]^T while the state warpgroup forms -X.  It
                // overwrites the S^T operand columns, which the products above (issued
@@ -879,27 +936,27 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
                 if (mode != 1) {  // (the map from S = I takes v = 0)
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
-                        mma_bf16(tmem + TM_SA, smem_desc(v_s + ks * 2048, 8192, 1024),
-                                 smem_desc(tp + ks * 32, 16, 1024), idesc, ks > 0);
+                        mma_bf16_e(tmem + TM_SA, smem_desc(v_s + ks * 2048, 8192, 1024),
+                                   smem_desc(tp + ks * 32, 16, 1024), idesc, ks > 0);
                 }
             }
-            if (!(ok = wait_bar(&bars->r_ready, c & 1, abort_flag, wait_ns))) break;
+            if (!(ok = wait_bar_warp(&bars->r_ready, c & 1, abort_flag, wait_ns))) break;
             tc_fence_after();
             {  // u^T = [U1 | U2] + (-X)_hi^T [T''_hi; T''_lo]^T + (-X)_lo^T T''_hi^T  (u = U1 + U2)
-                const uint32_t idesc2 = idesc_bf16_f32(128, 128, 0, 0), idesc1 = idesc_bf16_f32(128, 64, 0, 0);
+                const uint32_t idesc2 = idesc_bf16_f32(128, 128, 0, 0);
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16_ts(tmem + TM_SA, tmem + TM_X + ks * 8, smem_desc(tp + ks * 32, 16, 1024), idesc2,
-                                mode != 1 || ks > 0);
+                    mma_bf16_ts_e(tmem + TM_SA, tmem + TM_X + ks * 8, smem_desc(tp + ks * 32, 16, 1024), idesc2,
+                                  mode != 1 || ks > 0);
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16_ts(tmem + TM_SA, tmem + TM_X + 32 + ks * 8, smem_desc(tp + ks * 32, 16, 1024), idesc1, 1);
-                mma_commit(&bars->u_done);
+                    mma_bf16_ts_e(tmem + TM_SA, tmem + TM_X + 32 + ks * 8, smem_desc(tp + ks * 32, 16, 1024), idesc64,
+                                  1);
+                mma_commit_e(&bars->u_done);
             }
             // the Gram products two chunks ahead execute while the state warpgroup forms u
-            issue_grams(c + 2);
-            if (!ok) break;
-            if (!(ok = wait_bar(&bars->u_ready, c & 1, abort_flag, wait_ns))) break;
+            issue_grams(c + 2, false);
+            if (!(ok = wait_bar_warp(&bars->u_ready, c & 1, abort_flag, wait_ns))) break;
             tc_fence_after();
             {  // S^T += u^T K  (the chain), then O^T += u^T P^T
                 const uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 1);
@@ -907,30 +964,34 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
                 for (int part = 0; part < 2; ++part)
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
-                        mma_bf16_ts(tmem + TM_S, tmem + TM_X + part * 32 + ks * 8,
-                                    smem_desc(kq_s + ks * 2048, 16384, 1024), idesc_s, 1);
-                mma_commit(&bars->s_done);
-                mma_commit(&bars->s_free[c % NSTAGE]);
-                // [O^T | O_b^T] += u_hi^T [P_hi; P_lo]^T (N = 128), then O^T += u_lo^T P_hi^T
-                const uint32_t idesc_o2 = idesc_bf16_f32(128, 128, 0, 0), idesc_o1 = idesc_bf16_f32(128, 64, 0, 0);
+                        mma_bf16_ts_e(tmem + TM_S, tmem + TM_X + part * 32 + ks * 8,
+                                      smem_desc(kq_s + ks * 2048, 16384, 1024), idesc_s, 1);
+                mma_commit_e(&bars->s_done);
+                mma_commit_e(&bars->s_free[c % NSTAGE]);
+                // O^T += u_hi^T P_hi^T + u_hi^T P_lo^T + u_lo^T P_hi^T (N = 64 each)
                 if (write_o) {
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
-                        mma_bf16_ts(tmem + TM_O, tmem + TM_X + ks * 8, smem_desc(pb + ks * 32, 16, 1024), idesc_o2, 1);
+                        mma_bf16_ts_e(tmem + ob, tmem + TM_X + ks * 8, smem_desc(pb + ks * 32, 16, 1024), idesc64, 1);
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
-                        mma_bf16_ts(tmem + TM_O, tmem + TM_X + 32 + ks * 8, smem_desc(pb + ks * 32, 16, 1024),
-                                    idesc_o1, 1);
+                        mma_bf16_ts_e(tmem + ob, tmem + TM_X + ks * 8, smem_desc(pb + 8192 + ks * 32, 16, 1024),
+                                      idesc64, 1);
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_bf16_ts_e(tmem + ob, tmem + TM_X + 32 + ks * 8, smem_desc(pb + ks * 32, 16, 1024),
+                                      idesc64, 1);
                 }
-                mma_commit(&bars->o_done);
+                mma_commit_e(&bars->o_done[c & 1]);
             }
         }
         if (!ok) *abort_flag = 1;
-        // every MMA this thread issued has completed before TMEM is released (bounded)
-        mma_commit(&bars->drain[0]);
+        // every MMA this warp issued has completed before TMEM is released (bounded)
+        mma_commit_e(&bars->drain[0]);
         const uint64_t t0 = globaltimer_ns();
         while (!mbar_try_wait_sleep(&bars->drain[0], 0, 20000) && globaltimer_ns() - t0 < WAIT_NS) {
         }
+        __syncwarp();
     }
 
     if (*abort_flag && tid == 0) atomicExch(p.status, (int)EFLA_ERR_DEVICE_TIMEOUT);
@@ -996,7 +1057,7 @@ cudaError_t launch_chunk_tc(const FwdArgs &a, const char **why) {
         if (!make_map(&p.map_q, a.q, a.B, a.T, a.H, false, 64, true) ||
             !make_map(&p.map_k, a.k, a.B, a.T, a.H, false, 64, true) ||
             !make_map(&p.map_v, a.v, a.B, a.T, a.H, false, 64, true) ||
-            (a.o && !make_map(&p.map_o, a.o, a.B, a.T, a.H, !o_bf16, 32, false, 32))) {
+            (a.o && !make_map(&p.map_o, a.o, a.B, a.T, a.H, !o_bf16, 32, false, o_bf16 ? 64 : 32))) {
             *why = "cuTensorMapEncodeTiled failed";
             return cudaErrorInvalidValue;
         }
