@@ -95,8 +95,9 @@ typedef struct CUstream_st *efla_stream_t;
  *            cu_seqlens[N] = T, non-decreasing.  It is not read on the host:
  *            a kernel that meets a sequence with bounds outside [0, T] or
  *            decreasing writes nothing for that sequence and records
- *            EFLA_ERR_INVALID_ARG in the device status word.  Sequences are
- *            independent.
+ *            EFLA_ERR_INVALID_ARG in the device status word (the outputs of
+ *            sequences whose ranges overlap are then unspecified).  Sequences
+ *            are independent.
  *   o        [B, T, H, d_v]  dtype (the dtype of q); every token row written
  *   S_T      [N, H, d_k, d_v] fp32 final states, or NULL (not written)
  *   dtype    EFLA_BF16 or EFLA_F32, the element type of q, k, v and o
