@@ -65,8 +65,8 @@ efla_status validate_fwd(const FwdArgs &a, bool chunked) {
         return fail(EFLA_ERR_INVALID_ARG, "bad sizes B=%d T=%d H=%d N=%d", a.B, a.T, a.H, a.N);
     efla_status s = check_dims_common(a.dk, a.dv, a.in_dtype, a.o_dtype);
     if (s != EFLA_OK) return s;
-    if (chunked && a.chunk != 64)
-        return fail(EFLA_ERR_UNSUPPORTED, "chunk=%d: supported chunk length is 64", a.chunk);
+    if (chunked && a.chunk != 16 && a.chunk != 32 && a.chunk != 64)
+        return fail(EFLA_ERR_UNSUPPORTED, "chunk=%d: supported chunk lengths are 16, 32 and 64", a.chunk);
     if (a.cu_seqlens) {
         if (a.B != 1) return fail(EFLA_ERR_INVALID_ARG, "cu_seqlens given with B=%d (must be 1)", a.B);
     } else if (a.N != a.B) {
@@ -108,10 +108,13 @@ efla_status run_fwd(FwdArgs a, bool chunked) {
     a.status = device_status_ptr();
     if (!a.status) return fail(EFLA_ERR_CUDA, "cannot resolve the device status word");
     cudaError_t e;
-    if (chunked && a.in_dtype == EFLA_BF16 && a.dk == 128 && a.dv == 128) {
+    if (chunked && a.in_dtype == EFLA_BF16 && a.dk == 128 && a.dv == 128 && a.chunk == 64) {
         const char *why = nullptr;
         e = launch_chunk_tc(a, &why);
         if (e != cudaSuccess) return cuda_fail(e, why ? why : "tcgen05 chunk kernel launch");
+    } else if (chunked) {
+        e = launch_chunk_simt(a);
+        if (e != cudaSuccess) return cuda_fail(e, "chunk kernel launch");
     } else {
         e = launch_recurrent(a);
         if (e != cudaSuccess) return cuda_fail(e, "recurrent kernel launch");

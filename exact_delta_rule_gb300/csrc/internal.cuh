@@ -86,6 +86,8 @@ cudaError_t launch_scan_combine(const float *S0, const float *maps, float *s_in,
 cudaError_t launch_prep(const PrepArgs &a);
 // tcgen05 chunk kernel: bf16 inputs, d_k = d_v = 128, chunk 64.
 cudaError_t launch_chunk_tc(const FwdArgs &a, const char **why);
+// Chunkwise forward on CUDA cores (fp32), every supported head size, chunk 16, 32 or 64.
+cudaError_t launch_chunk_simt(const FwdArgs &a);
 
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }

@@ -101,7 +101,9 @@ typedef struct CUstream_st *efla_stream_t;
  *   o        [B, T, H, d_v]  dtype (the dtype of q); every token row written
  *   S_T      [N, H, d_k, d_v] fp32 final states, or NULL (not written)
  *   dtype    EFLA_BF16 or EFLA_F32, the element type of q, k, v and o
- *   chunk    chunk length: 16, 32, 64 or 128 (0 selects 64)
+ *   chunk    chunk length: 16, 32 or 64 (0 selects 64); 128 returns
+ *            EFLA_ERR_UNSUPPORTED (the chunk's fp32 buffers would not fit one
+ *            CTA's shared memory)
  *
  * State and all accumulation are fp32.  Supported: d_k, d_v in {32, 64, 128}.
  * bf16 inputs with d_k = d_v = 128 and chunk 64 run on the tcgen05

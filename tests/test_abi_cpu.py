@@ -104,6 +104,7 @@ INVALID, UNSUPPORTED = 1, 2
     (dict(dk=48), UNSUPPORTED, "supported head sizes"),
     (dict(dv=256), UNSUPPORTED, "supported head sizes"),
     (dict(chunk=48), UNSUPPORTED, "chunk"),
+    (dict(chunk=128), UNSUPPORTED, "chunk"),
     (dict(chunk=-64), UNSUPPORTED, "chunk"),
     (dict(dt=7), INVALID, "dtype"),
     (dict(N=3), INVALID, "must equal B"),

@@ -54,6 +54,28 @@ def test_fwd_small(efla, fn, dtype, d, T):
     check(S, S_ref, in_dtype=dtype, what=f"S_T {fn} {dtype} d{d} T{T}")
 
 
+@pytest.mark.parametrize("chunk", [16, 32, 64])
+@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("f32", 64), ("bf16", 32), ("f32", 128)])
+def test_fwd_chunk_lengths(efla, chunk, dtype, d):
+    """Every chunk length the boundary accepts (16 and 32 run the CUDA-core chunkwise kernel,
+    64 the tensor-core kernel for bf16 d128), ragged lengths and a packed batch."""
+    inp = workloads.small_fwd(dtype, B=2, T=150, H=2, d=d, seed=300 + chunk + d)
+    g = _dev(inp)
+    o, S = efla.fwd_chunked(g["q"], g["k"], g["v"], g["beta"], g["S0"], chunk=chunk, o_dtype=torch.float32)
+    torch.cuda.synchronize()
+    o_ref, S_ref = _oracle(inp)
+    check(o, o_ref, in_dtype=dtype, what=f"o chunk {chunk}")
+    check(S, S_ref, in_dtype=dtype, what=f"S_T chunk {chunk}")
+    inp = workloads.small_fwd(dtype, H=2, d=d, seed=400 + chunk, lengths=[31, 0, 70, 16, 5])
+    g = _dev(inp)
+    o, S = efla.fwd_chunked(g["q"], g["k"], g["v"], g["beta"], g["S0"], g["cu_seqlens"], chunk=chunk,
+                            o_dtype=torch.float32)
+    torch.cuda.synchronize()
+    o_ref, S_ref = _oracle(inp)
+    check(o, o_ref, in_dtype=dtype, what=f"o varlen chunk {chunk}")
+    check(S, S_ref, in_dtype=dtype, what=f"S_T varlen chunk {chunk}")
+
+
 @pytest.mark.parametrize("fn", ["chunked", "recurrent"])
 def test_fwd_bf16_output(efla, fn):
     inp = workloads.small_fwd("bf16", B=2, T=300, H=2, d=128, seed=7)
