@@ -445,8 +445,10 @@ efla_status efla_decode_tokens(const void *q, const void *k, const void *v, cons
     if (overlap(rS, ro)) return fail(EFLA_ERR_INVALID_ARG, "o overlaps S");
     DecodeArgs a{q, k, v, beta, S, o, B, H, d_k, d_v, in_dtype, o_dtype, reinterpret_cast<cudaStream_t>(stream),
                  (int)update, m};
-    cudaError_t e = launch_decode_tokens(a);
-    if (e != cudaSuccess) return cuda_fail(e, "decode-tokens kernel launch");
+    const char *why = "decode-tokens kernel launch";
+    cudaError_t e = in_dtype == EFLA_BF16 && d_k == 128 && d_v == 128 ? launch_decode_tokens_tc(a, &why)
+                                                                       : launch_decode_tokens(a);
+    if (e != cudaSuccess) return cuda_fail(e, why);
     g_last_error.clear();
     return EFLA_OK;
 }

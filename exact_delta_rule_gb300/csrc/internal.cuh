@@ -68,6 +68,8 @@ struct PrepArgs {
 cudaError_t launch_recurrent(const FwdArgs &a);
 cudaError_t launch_decode(const DecodeArgs &a);
 cudaError_t launch_decode_tokens(const DecodeArgs &a);
+// tcgen05 multi-token decode: bf16 q, k, v, d_k = d_v = 128 (decode_tc.cu).
+cudaError_t launch_decode_tokens_tc(const DecodeArgs &a, const char **why);
 // Backward pass (bwd.cu): gradients of the forward over whole rows of [B, T].
 struct BwdArgs {
     const void *q, *k, *v;

@@ -60,7 +60,12 @@ def test_decode_tokens_bf16_out_and_euler(efla):
 
 
 def test_decode_tokens_equals_chained_steps(efla):
-    """m tokens at once and m single-token steps on the same inputs agree to fp32 rounding."""
+    """m tokens at once and m single-token steps on the same inputs agree.
+
+    With bf16 q, k, v and d = 128 the m tokens go through the tensor-core kernel, whose
+    products split each non-bf16 operand into bf16 hi + lo parts (a residual of at most
+    2^-16 of the operand), so the two paths agree to about 1e-5 of the values' scale
+    rather than to fp32 rounding: relative Frobenius difference <= 1e-4."""
     cfg, S0, inp = _case(128, 128, 9, B=4, H=6)
     S1, S2 = S0.to(DEV), S0.to(DEV)
     g = {x: inp[x].to(DEV) for x in ("q", "k", "v", "beta")}
@@ -70,8 +75,9 @@ def test_decode_tokens_equals_chained_steps(efla):
                                        o_dtype=torch.float32)
                       for t in range(9)], dim=1)
     torch.cuda.synchronize()
-    assert torch.allclose(o1, o2, rtol=1e-5, atol=1e-5)
-    assert torch.allclose(S1, S2, rtol=1e-5, atol=1e-6)
+    for got, want in ((o1, o2), (S1, S2)):
+        rel = (got - want).norm() / want.norm()
+        assert rel <= 1e-4, rel
 
 
 def test_decode_tokens_zero_tokens_and_empty_batch(efla):
