@@ -21,15 +21,20 @@
 //   [X^T | O1^T] = S^T [K; Q]^T        (N = 32, K = d_k)
 //   u^T = V^T T''^T + (-X)^T T''^T     (N = 16, K = 16; V^T read as an MN-major operand)
 //   S^T += u^T K,  O^T = O1^T + u^T P^T,  P = Q K^T o M
-// The block's Gram terms, gate terms, T~ (16x16 forward substitution) and P are formed on CUDA
-// cores in fp32.
+// and the block's Gram terms [K; Q] K^T (N = 16, exact bf16 products summed in fp32; the MMA
+// has M = 128 rows, of which the 32 rows of [K; Q] are kept).  The gate terms, T~ (16x16
+// forward substitution) and the bf16 hi/lo packing of T'' and P are fp32 CUDA-core work.
 //
-// One persistent CTA of 320 threads per SM walks the (b, h) units:
-//   state warpgroup (warps 0-3): thread j owns TMEM lane j (column j of S): moves S between
-//     its shared-memory staging and TMEM, forms the split operands, sends o and the new S.
-//   prep warpgroup (warps 4-7): the block's Gram, gate, T'' and P.
-//   MMA warp (warp 8) and TMA producer (warp 9): the next unit's S (64 KB, a bulk copy into
-//     one of two staging buffers) streams in while the current unit computes.
+// One persistent CTA of 256 threads per SM walks the (b, h) units:
+//   state warpgroup (warps 0-3): thread j owns TMEM lane j (column j of S): moves S between its
+//     shared-memory staging and TMEM, forms the split operands, writes o and the new S into
+//     shared memory for the asynchronous stores.
+//   prep warp (warp 4): the block's gate terms, T'' and P, from the Gram rows in TMEM.
+//   MMA warp (warp 5).
+//   K/Q/V producer (warp 6): the next block's K, Q, V (TMA, two stages) stream in while the
+//     current block computes, so the Gram and prep of the next block run ahead of the state.
+//   state mover (warp 7): per unit, a bulk copy of the new S (64 KB) from the staging buffer to
+//     HBM, then the bulk load of the S two units ahead into the same buffer.
 // Every wait is bounded; on expiry the CTA records EFLA_ERR_DEVICE_TIMEOUT and leaves.
 #include <cudaTypedefs.h>
 
@@ -46,21 +51,27 @@ constexpr int D = 128;
 constexpr int MB = 16;  // tokens per block
 
 // Shared memory map (bytes from a 1024-byte aligned base).
-constexpr uint32_t S_BYTES = 65536;             // S of one unit, fp32 [d_k][d_v]
-constexpr uint32_t OFF_S = 0;                    // 2 staging buffers
-constexpr uint32_t OFF_KQ = 2 * S_BYTES;         // [K; Q]: 2 column blocks x 32 rows x 128 B, 128B swizzle
-constexpr uint32_t OFF_V = OFF_KQ + 8192;        // V: 2 column blocks x 16 rows x 128 B
-constexpr uint32_t OFF_TP = OFF_V + 4096;        // T'' hi, lo: 16 rows x 128 B each (first 32 B used)
-constexpr uint32_t OFF_PP = OFF_TP + 4096;       // P hi, lo
-constexpr uint32_t OFF_G = OFF_PP + 4096;        // fp32 kk[16][17], qk[16][17], then T~ [16][17]
+constexpr uint32_t S_BYTES = 65536;              // S of one unit, fp32 [d_k][d_v]
+constexpr uint32_t OFF_S = 0;                     // 2 staging buffers
+constexpr uint32_t KQ_BYTES = 8192;               // [K; Q]: 2 column blocks x 32 rows x 128 B, 128B swizzle
+constexpr uint32_t V_BYTES = 4096;                // V: 2 column blocks x 16 rows x 128 B
+constexpr uint32_t OFF_KQ = 2 * S_BYTES;          // 2 stages
+constexpr uint32_t OFF_V = OFF_KQ + 2 * KQ_BYTES;  // 2 stages
+constexpr uint32_t OFF_TP = OFF_V + 2 * V_BYTES;  // T'' hi, lo: 16 rows x 128 B each (first 32 B used)
+constexpr uint32_t OFF_PP = OFF_TP + 4096;        // P hi, lo
+constexpr uint32_t OFF_OT = OFF_PP + 4096;        // o tiles: 2 buffers x 8 KB (column blocks of 2 KB: 16 rows x 128 B)
+constexpr uint32_t OFF_G = OFF_OT + 2 * 8192;     // fp32 A~ [16][17], T~ [16][17]
 constexpr uint32_t G_LD = 17;
-constexpr uint32_t OFF_ROW = OFF_G + 3 * 16 * G_LD * 4;  // fp32 invn[16], gn[16]
+constexpr uint32_t OFF_ROW = OFF_G + 2 * 16 * G_LD * 4;  // fp32 invn[16], gn[16]
 constexpr uint32_t OFF_BAR = OFF_ROW + 128;
-constexpr uint32_t OFF_MISC = OFF_BAR + 256;      // tmem base, abort flag
+constexpr uint32_t OFF_MISC = OFF_BAR + 256;  // tmem base, abort flag
 constexpr uint32_t SMEM_USED = OFF_MISC + 16;
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;
 static_assert(OFF_KQ % 1024 == 0 && OFF_V % 1024 == 0 && OFF_TP % 1024 == 0 && OFF_PP % 1024 == 0,
               "operand tiles must be 1024-byte aligned");
+// The Gram MMA reads 128 rows of A from a [K; Q] stage, of which only the first 32 are kept:
+// the rows past them must still lie inside the allocation.
+static_assert(OFF_KQ + KQ_BYTES + 4096 + 16 * 1024 <= SMEM_USED, "Gram operand rows leave shared memory");
 static_assert(SMEM_ALLOC <= 232448, "exceeds the per-CTA shared memory limit");
 
 // TMEM columns
@@ -69,14 +80,18 @@ constexpr uint32_t TM_SA = 128;  // S^T bf16 hi (64) | lo (64)
 constexpr uint32_t TM_X = 256;   // X^T fp32 (16); then (-X)^T hi (8) | lo (8); then u^T hi | lo
 constexpr uint32_t TM_O = 272;   // O^T fp32 (16), adjacent to TM_X: [X | O1] is one N = 32 product
 constexpr uint32_t TM_U = 288;   // u^T fp32 (16)
+constexpr uint32_t TM_G = 304;   // Gram rows: lane t < 16 k_t . k_s, lane 16 + t q_t . k_s (16)
 constexpr uint32_t TM_COLS = 512;
 
-constexpr int THREADS = 320;
-constexpr int BAR_PREP = 2;
+constexpr int THREADS = 256;
+constexpr int TMA_TID = 192;
+constexpr int SMOVE_TID = 224;
+constexpr int BAR_STATE = 1;
 constexpr uint64_t WAIT_NS = 2000000000ull;
 
 struct DtParams {
     CUtensorMap map_q, map_k, map_v;  // [B, m, H, 128] bf16: box 64 x 1 x 16 x 1, 128B swizzle
+    CUtensorMap map_o;                // [B, m, H, 128] in o's dtype: box (128 bytes) x 1 x 16 x 1, no swizzle
     const float *beta;                // [B, m, H]
     float *S;                         // [B, H, 128, 128]
     void *o;                          // [B, m, H, 128]
@@ -87,9 +102,10 @@ struct DtParams {
 };
 
 struct Bars {
-    uint64_t s_full[2], s_empty[2];  // S staging buffer landed / read (128 arrivals)
-    uint64_t kqv_full, kqv_empty;    // K, Q, V of a block landed / no longer read
-    uint64_t prep_ready, tp_free;    // T'', P of a block written / no longer read
+    uint64_t s_full[2], s_out[2];        // S staging buffer landed / holds the unit's new S (128 arrivals)
+    uint64_t kqv_full[2], kqv_empty[2];  // K, Q, V stage landed / no longer read
+    uint64_t g_done, g_free;             // Gram rows in TMEM / read by the prep warp
+    uint64_t prep_ready, tp_free;        // T'', P of a block written / no longer read
     uint64_t sa_ready, x_done, r_ready, u_done, u_ready, s_done, o_done;
     uint64_t drain;
 };
@@ -127,6 +143,19 @@ __device__ __forceinline__ void split_pairs(const float *x, uint32_t *hi, uint32
     }
 }
 
+// 16 fp32 values of row `row` of a 16-row operand tile (128B swizzle) as bf16 hi at `tile`, lo at tile + 2048.
+__device__ __forceinline__ void put_row16(uint8_t *tile, int row, const float (&x)[16]) {
+    uint32_t hh[8], ll[8];
+    split_pairs<8>(x, hh, ll);
+#pragma unroll
+    for (int h8 = 0; h8 < 2; ++h8) {
+        const uint32_t off = swz_offset(row, 8 * h8, 2048);
+        *reinterpret_cast<uint4 *>(tile + off) = make_uint4(hh[4 * h8], hh[4 * h8 + 1], hh[4 * h8 + 2], hh[4 * h8 + 3]);
+        *reinterpret_cast<uint4 *>(tile + 2048 + off) =
+            make_uint4(ll[4 * h8], ll[4 * h8 + 1], ll[4 * h8 + 2], ll[4 * h8 + 3]);
+    }
+}
+
 template <bool OUT_BF16>
 __global__ void __launch_bounds__(THREADS, 1) decode_tc_kernel(const __grid_constant__ DtParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -143,10 +172,12 @@ __global__ void __launch_bounds__(THREADS, 1) decode_tc_kernel(const __grid_cons
     if (tid == 0) {
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars->s_full[i], 1);
-            mbar_init(&bars->s_empty[i], 128);
+            mbar_init(&bars->s_out[i], 128);
+            mbar_init(&bars->kqv_full[i], 1);
+            mbar_init(&bars->kqv_empty[i], 1);
         }
-        mbar_init(&bars->kqv_full, 1);
-        mbar_init(&bars->kqv_empty, 1);
+        mbar_init(&bars->g_done, 1);
+        mbar_init(&bars->g_free, 1);
         mbar_init(&bars->prep_ready, 1);
         mbar_init(&bars->tp_free, 1);
         mbar_init(&bars->sa_ready, 128);
@@ -173,6 +204,8 @@ __global__ void __launch_bounds__(THREADS, 1) decode_tc_kernel(const __grid_cons
 
     if (warp < 4) {
         // =============================== state warpgroup ===============================
+        // A failed wait skips the rest of the block's work but still reaches the block's
+        // closing barrier, which every thread of the warpgroup passes before any leaves.
         const int j = tid;
         bool ok = true;
         int gb = 0;  // blocks processed (all units)
@@ -180,47 +213,47 @@ __global__ void __launch_bounds__(THREADS, 1) decode_tc_kernel(const __grid_cons
         for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++it) {
             const int b = u / p.H, h = u % p.H;
             const int sb = it & 1;
-            const float *stg = reinterpret_cast<const float *>(sm + OFF_S + sb * S_BYTES);
+            float *stg = reinterpret_cast<float *>(sm + OFF_S + sb * S_BYTES);
             for (int blk = 0; blk < nblk && ok; ++blk, ++gb) {
                 const int t0 = blk * MB, mb = min(MB, p.m - t0);
                 if (blk == 0) {  // S^T of the unit from its staging: fp32 into TM_S and split into TM_SA
                     ok = dt_wait_warp(&bars->s_full[sb], (it >> 1) & 1, abort_flag, wait_ns);
-                    if (!ok) break;
+                    if (ok) {
 #pragma unroll 1
-                    for (int g = 0; g < 4; ++g) {
-                        float sv[32];
-                        uint32_t hi[16], lo[16];
+                        for (int g = 0; g < 4; ++g) {
+                            float sv[32];
+                            uint32_t hi[16], lo[16];
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) sv[i] = stg[(g * 32 + i) * D + j];
-                        tmem_st32(lane_base + TM_S + g * 32, sv);
-                        split_pairs<16>(sv, hi, lo);
-                        tmem_st16u(lane_base + TM_SA + g * 16, hi);
-                        tmem_st16u(lane_base + TM_SA + 64 + g * 16, lo);
+                            for (int i = 0; i < 32; ++i) sv[i] = stg[(g * 32 + i) * D + j];
+                            tmem_st32(lane_base + TM_S + g * 32, sv);
+                            split_pairs<16>(sv, hi, lo);
+                            tmem_st16u(lane_base + TM_SA + g * 16, hi);
+                            tmem_st16u(lane_base + TM_SA + 64 + g * 16, lo);
+                        }
+                        tmem_st_wait();
                     }
-                    tmem_st_wait();
-                    mbar_arrive(&bars->s_empty[sb]);  // the staging buffer may take the next S
                 } else {  // S^T after the previous block's update -> split
                     ok = dt_wait_warp(&bars->s_done, (gb - 1) & 1, abort_flag, wait_ns);
-                    if (!ok) break;
-                    tc_fence_after();
+                    if (ok) {
+                        tc_fence_after();
 #pragma unroll 1
-                    for (int g = 0; g < 4; ++g) {
-                        float sv[32];
-                        uint32_t hi[16], lo[16];
-                        tmem_ld32(lane_base + TM_S + g * 32, sv);
-                        tmem_ld_wait();
-                        split_pairs<16>(sv, hi, lo);
-                        tmem_st16u(lane_base + TM_SA + g * 16, hi);
-                        tmem_st16u(lane_base + TM_SA + 64 + g * 16, lo);
+                        for (int g = 0; g < 4; ++g) {
+                            float sv[32];
+                            uint32_t hi[16], lo[16];
+                            tmem_ld32(lane_base + TM_S + g * 32, sv);
+                            tmem_ld_wait();
+                            split_pairs<16>(sv, hi, lo);
+                            tmem_st16u(lane_base + TM_SA + g * 16, hi);
+                            tmem_st16u(lane_base + TM_SA + 64 + g * 16, lo);
+                        }
+                        tmem_st_wait();
                     }
-                    tmem_st_wait();
                 }
                 tc_fence_before();
                 mbar_arrive(&bars->sa_ready);
-                ok = dt_wait_warp(&bars->x_done, gb & 1, abort_flag, wait_ns);
-                if (!ok) break;
-                tc_fence_after();
-                {  // (-X)^T -> bf16 hi | lo (tokens past the block end are zero)
+                ok = ok && dt_wait_warp(&bars->x_done, gb & 1, abort_flag, wait_ns);
+                if (ok) {  // (-X)^T -> bf16 hi | lo (tokens past the block end are zero)
+                    tc_fence_after();
                     float x[16];
                     uint32_t hi[8], lo[8];
                     tmem_ld16(lane_base + TM_X, x);
@@ -231,13 +264,12 @@ __global__ void __launch_bounds__(THREADS, 1) decode_tc_kernel(const __grid_cons
                     tmem_st8u(lane_base + TM_X, hi);
                     tmem_st8u(lane_base + TM_X + 8, lo);
                     tmem_st_wait();
+                    tc_fence_before();
+                    mbar_arrive(&bars->r_ready);
                 }
-                tc_fence_before();
-                mbar_arrive(&bars->r_ready);
-                ok = dt_wait_warp(&bars->u_done, gb & 1, abort_flag, wait_ns);
-                if (!ok) break;
-                tc_fence_after();
-                {  // u^T -> bf16 hi | lo
+                ok = ok && dt_wait_warp(&bars->u_done, gb & 1, abort_flag, wait_ns);
+                if (ok) {  // u^T -> bf16 hi | lo
+                    tc_fence_after();
                     float x[16];
                     uint32_t hi[8], lo[8];
                     tmem_ld16(lane_base + TM_U, x);
@@ -246,153 +278,156 @@ __global__ void __launch_bounds__(THREADS, 1) decode_tc_kernel(const __grid_cons
                     tmem_st8u(lane_base + TM_X, hi);
                     tmem_st8u(lane_base + TM_X + 8, lo);
                     tmem_st_wait();
+                    tc_fence_before();
+                    mbar_arrive(&bars->u_ready);
                 }
-                tc_fence_before();
-                mbar_arrive(&bars->u_ready);
-                ok = dt_wait_warp(&bars->o_done, gb & 1, abort_flag, wait_ns);
-                if (!ok) break;
-                tc_fence_after();
-                {  // o of the block's tokens (column j)
+                ok = ok && dt_wait_warp(&bars->o_done, gb & 1, abort_flag, wait_ns);
+                uint8_t *ot = sm + OFF_OT + (gb & 1) * 8192;
+                if (ok) {  // o of the block's tokens (column j) into o tile gb & 1
+                    tc_fence_after();
                     float ov[16];
                     tmem_ld16(lane_base + TM_O, ov);
                     tmem_ld_wait();
 #pragma unroll
                     for (int t = 0; t < 16; ++t) {
-                        if (t < mb) {
-                            const size_t row = ((size_t)b * p.m + t0 + t) * p.H + h;
-                            if (OUT_BF16)
-                                static_cast<__nv_bfloat16 *>(p.o)[row * D + j] = __float2bfloat16_rn(ov[t]);
-                            else
-                                static_cast<float *>(p.o)[row * D + j] = ov[t];
-                        }
+                        if (OUT_BF16)
+                            *reinterpret_cast<__nv_bfloat16 *>(ot + (j >> 6) * 2048 + t * 128 + (j & 63) * 2) =
+                                __float2bfloat16_rn(ov[t]);
+                        else
+                            *reinterpret_cast<float *>(ot + (j >> 5) * 2048 + t * 128 + (j & 31) * 4) = ov[t];
                     }
+                    fence_proxy_async_smem();
+                }
+                if (named_bar_any(BAR_STATE, 128, !ok)) {
+                    ok = false;
+                    *abort_flag = 1;
+                    break;
+                }
+                if (j == 0) {  // one thread stores the tile; rows past the sequence end fall outside the tensor
+                    constexpr int NCB = OUT_BF16 ? 2 : 4, W = OUT_BF16 ? 64 : 32;
+                    for (int cb = 0; cb < NCB; ++cb) tma_store_4d(&p.map_o, ot + cb * 2048, cb * W, h, t0, b);
+                    bulk_commit();
+                    // the tile is rewritten two blocks later, after the next closing barrier, which this
+                    // thread reaches only once the copy has read it
+                    bulk_wait_read0();
                 }
             }
             if (!ok) break;
-            {  // the unit's new S (its last block's o_done covers the state update)
-                float *Su = p.S + (size_t)u * D * D;
+            {  // the unit's new S (its last block's o_done covers the state update) into its staging
 #pragma unroll 1
                 for (int g = 0; g < 4; ++g) {
                     float sv[32];
                     tmem_ld32(lane_base + TM_S + g * 32, sv);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) Su[(size_t)(g * 32 + i) * D + j] = sv[i];
+                    for (int i = 0; i < 32; ++i) stg[(g * 32 + i) * D + j] = sv[i];
                 }
+                fence_proxy_async_smem();
+                mbar_arrive(&bars->s_out[sb]);
             }
             tc_fence_before();
         }
+        if (j == 0) bulk_wait0();  // the o stores have completed
         if (!ok) *abort_flag = 1;
-    } else if (warp < 8) {
-        // =============================== prep warpgroup ===============================
-        const int pi = tid - 128;
-        float *kk = reinterpret_cast<float *>(sm + OFF_G), *qk = kk + 16 * G_LD, *Tt = qk + 16 * G_LD;
+    } else if (warp == 4) {
+        // ================================ prep warp ================================
+        const int lane = tid & 31;
+        float *At = reinterpret_cast<float *>(sm + OFF_G), *Tt = At + 16 * G_LD;
         float *invn = reinterpret_cast<float *>(sm + OFF_ROW), *gn = invn + 16;
-        const uint8_t *kq = sm + OFF_KQ;
         bool ok = true;
         int gb = 0;
         for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
             const int b = u / p.H, h = u % p.H;
             for (int blk = 0; blk < nblk && ok; ++blk, ++gb) {
                 const int t0 = blk * MB, mb = min(MB, p.m - t0);
-                if (gb > 0) ok = dt_wait_warp(&bars->tp_free, (gb - 1) & 1, abort_flag, wait_ns);
-                ok = ok && dt_wait_warp(&bars->kqv_full, gb & 1, abort_flag, wait_ns);
-                if (named_bar_any(BAR_PREP, 128, !ok || *abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                {  // Gram terms k_t.k_s and q_t.k_s (t = pi >> 3, s = 2 (pi & 7) + {0, 1}), fp32
-                    const int t = pi >> 3, s = 2 * (pi & 7);
-                    float a0 = 0.f, a1 = 0.f, c0 = 0.f, c1 = 0.f;
-#pragma unroll 4
-                    for (int d8 = 0; d8 < D; d8 += 8) {
-                        // 8 consecutive bf16 of rows t (K), 16 + t (Q), s, s + 1 (K)
-                        const uint4 kt = *reinterpret_cast<const uint4 *>(kq + swz_offset(t, d8, 4096));
-                        const uint4 qt = *reinterpret_cast<const uint4 *>(kq + swz_offset(16 + t, d8, 4096));
-                        const uint4 ks0 = *reinterpret_cast<const uint4 *>(kq + swz_offset(s, d8, 4096));
-                        const uint4 ks1 = *reinterpret_cast<const uint4 *>(kq + swz_offset(s + 1, d8, 4096));
-                        const __nv_bfloat162 *pkt = reinterpret_cast<const __nv_bfloat162 *>(&kt);
-                        const __nv_bfloat162 *pqt = reinterpret_cast<const __nv_bfloat162 *>(&qt);
-                        const __nv_bfloat162 *pk0 = reinterpret_cast<const __nv_bfloat162 *>(&ks0);
-                        const __nv_bfloat162 *pk1 = reinterpret_cast<const __nv_bfloat162 *>(&ks1);
+                // beta of token `lane` (issued before the waits so that its latency overlaps them)
+                const float bt = lane < mb ? p.beta[((size_t)b * p.m + t0 + lane) * p.H + h] : 0.f;
+                if (!(ok = dt_wait_warp(&bars->g_done, gb & 1, abort_flag, wait_ns))) break;
+                tc_fence_after();
+                float row[16];  // lane t < 16: k_t . k_s; lane 16 + t: q_t . k_s
+                tmem_ld16(tmem + TM_G, row);
+                tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->g_free);
+                float lam = 0.f;
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float2 ft = __bfloat1622float2(pkt[e]), fq = __bfloat1622float2(pqt[e]);
-                            const float2 f0 = __bfloat1622float2(pk0[e]), f1 = __bfloat1622float2(pk1[e]);
-                            a0 = fmaf(ft.x, f0.x, fmaf(ft.y, f0.y, a0));
-                            a1 = fmaf(ft.x, f1.x, fmaf(ft.y, f1.y, a1));
-                            c0 = fmaf(fq.x, f0.x, fmaf(fq.y, f0.y, c0));
-                            c1 = fmaf(fq.x, f1.x, fmaf(fq.y, f1.y, c1));
-                        }
-                    }
-                    kk[t * G_LD + s] = a0;
-                    kk[t * G_LD + s + 1] = a1;
-                    qk[t * G_LD + s] = c0;
-                    qk[t * G_LD + s + 1] = c1;
-                }
-                named_bar(BAR_PREP, 128);
-                if (pi < 16) {  // gate terms of token t = pi (zero past the block end and for zero keys)
-                    const int t = pi;
-                    const float lam = kk[t * G_LD + t];
-                    const float bt = t < mb ? p.beta[((size_t)b * p.m + t0 + t) * p.H + h] : 0.f;
-                    const bool live = t < mb && lam > 0.f;
+                for (int s = 0; s < 16; ++s) lam = s == lane ? row[s] : lam;
+                {  // gate terms of token `lane` (zero past the block end and for zero keys)
+                    const bool live = lane < mb && lam > 0.f;
                     const float in = live ? rsqrtf(lam) : 0.f;
                     const float gam = !live ? 0.f : p.euler ? bt * lam : -expm1f(-bt * lam);
-                    invn[t] = in;
-                    gn[t] = gam * in;
+                    if (lane < 16) {
+                        invn[lane] = in;
+                        gn[lane] = gam * in;
+                    }
                 }
-                named_bar(BAR_PREP, 128);
-                if (pi < 16) {  // T~ = (I + A~)^{-1}, one lane per column c, the column in registers
-                    const int c = pi;
+                __syncwarp();
+                if (lane < 16) {  // A~ row t = lane: gamma_t/n_t (k_t . k_s) / n_s, s < t
+                    const float g_t = gn[lane];
+#pragma unroll
+                    for (int s = 0; s < 16; ++s) At[lane * G_LD + s] = s < lane ? g_t * row[s] * invn[s] : 0.f;
+                }
+                __syncwarp();
+                if (lane < 16) {  // T~ = (I + A~)^{-1}, column c = lane, by forward substitution
+                    const int c = lane;
                     float col[16];
 #pragma unroll
                     for (int r = 0; r < 16; ++r) col[r] = r == c ? 1.f : 0.f;
 #pragma unroll
                     for (int t = 1; t < 16; ++t) {
-                        const float rt = gn[t];  // A~[t][s] = gamma_t/n_t * (k_t.k_s) / n_s
                         float acc = 0.f;
 #pragma unroll
-                        for (int s2 = 0; s2 < t; ++s2) acc = fmaf(rt * kk[t * G_LD + s2] * invn[s2], col[s2], acc);
+                        for (int s2 = 0; s2 < t; ++s2) acc = fmaf(At[t * G_LD + s2], col[s2], acc);
                         col[t] = t > c ? -acc : col[t];
                     }
+                    const float gc = gn[c];
 #pragma unroll
-                    for (int r = 0; r < 16; ++r) Tt[r * G_LD + c] = col[r];
+                    for (int r = 0; r < 16; ++r) Tt[r * G_LD + c] = col[r] * gc;
                 }
-                named_bar(BAR_PREP, 128);
-                {  // T'' = diag(1/n) T~ diag(gamma/n) and P = Q K^T o M, bf16 hi/lo, rows t, columns 8h8 .. 8h8+7
-                    const int which = pi >> 5, t = (pi >> 1) & 15, h8 = pi & 1;  // which: 0 T'', 1 P; 64 threads idle
-                    if (which < 2) {
-                        float x[8];
+                if (gb > 0 && !(ok = dt_wait_warp(&bars->tp_free, (gb - 1) & 1, abort_flag, wait_ns))) break;
+                __syncwarp();
+                {  // rows of T'' = diag(1/n) T~ diag(gamma/n) (lanes 0-15) and P = Q K^T o M (lanes 16-31)
+                    const int t = lane & 15;
+                    float x[16];
+                    if (lane < 16) {
+                        const float it = invn[t];
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const int s = 8 * h8 + e;
-                            x[e] = which == 0 ? (s <= t ? invn[t] * Tt[t * G_LD + s] * gn[s] : 0.f)
-                                              : (s <= t ? qk[t * G_LD + s] : 0.f);
-                        }
-                        uint32_t hh[4], ll[4];
-                        split_pairs<4>(x, hh, ll);
-                        uint8_t *dst = sm + (which == 0 ? OFF_TP : OFF_PP);
-                        const uint32_t off = swz_offset(t, 8 * h8, 2048);
-                        *reinterpret_cast<uint4 *>(dst + off) = make_uint4(hh[0], hh[1], hh[2], hh[3]);
-                        *reinterpret_cast<uint4 *>(dst + 2048 + off) = make_uint4(ll[0], ll[1], ll[2], ll[3]);
+                        for (int s = 0; s < 16; ++s) x[s] = s <= t ? it * Tt[t * G_LD + s] : 0.f;
+                    } else {
+#pragma unroll
+                        for (int s = 0; s < 16; ++s) x[s] = s <= t ? row[s] : 0.f;
                     }
+                    put_row16(sm + (lane < 16 ? OFF_TP : OFF_PP), t, x);
                 }
                 fence_proxy_async_smem();
-                named_bar(BAR_PREP, 128);
-                if (pi == 0) mbar_arrive(&bars->prep_ready);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->prep_ready);
             }
         }
         if (!ok) *abort_flag = 1;
-    } else if (warp == 8) {
+    } else if (warp == 5) {
         // =============================== MMA warp ===============================
         bool ok = true;
         int gb = 0;
-        const uint32_t kq_s = s_sm + OFF_KQ, v_s = s_sm + OFF_V, tp = s_sm + OFF_TP, pp = s_sm + OFF_PP;
+        const uint32_t tp = s_sm + OFF_TP, pp = s_sm + OFF_PP;
         const uint32_t id32 = idesc_bf16_f32(128, 32, 0, 0), id16 = idesc_bf16_f32(128, 16, 0, 0);
         const uint32_t id16v = idesc_bf16_f32(128, 16, 1, 0), id128k = idesc_bf16_f32(128, 128, 0, 1);
         for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
             for (int blk = 0; blk < nblk && ok; ++blk, ++gb) {
-                if (!(ok = dt_wait_warp(&bars->kqv_full, gb & 1, abort_flag, wait_ns))) break;
+                const int st = gb & 1;
+                const uint32_t kq_s = s_sm + OFF_KQ + st * KQ_BYTES, v_s = s_sm + OFF_V + st * V_BYTES;
+                if (!(ok = dt_wait_warp(&bars->kqv_full[st], (gb >> 1) & 1, abort_flag, wait_ns))) break;
+                if (gb > 0 && !(ok = dt_wait_warp(&bars->g_free, (gb - 1) & 1, abort_flag, wait_ns))) break;
+                tc_fence_after();
+                // Gram rows [K; Q] K^T (rows 32-127 of the A operand are not used)
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint32_t off = (ks >> 2) * 4096 + (ks & 3) * 32;
+                    mma_bf16_e(tmem + TM_G, smem_desc(kq_s + off, 16, 1024), smem_desc(kq_s + off, 16, 1024), id16,
+                               ks > 0);
+                }
+                mma_commit_e(&bars->g_done);
                 if (!(ok = dt_wait_warp(&bars->sa_ready, gb & 1, abort_flag, wait_ns))) break;
                 tc_fence_after();
                 // [X^T | O1^T] = S^T [K; Q]^T (N = 32 over the 32 rows of [K; Q])
@@ -423,7 +458,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_tc_kernel(const __grid_cons
                 mma_bf16_ts_e(tmem + TM_S, tmem + TM_X, smem_desc(kq_s, 4096, 1024), id128k, 1);
                 mma_bf16_ts_e(tmem + TM_S, tmem + TM_X + 8, smem_desc(kq_s, 4096, 1024), id128k, 1);
                 mma_commit_e(&bars->s_done);
-                mma_commit_e(&bars->kqv_empty);
+                mma_commit_e(&bars->kqv_empty[st]);
                 // O^T += u_hi^T P_hi^T + u_hi^T P_lo^T + u_lo^T P_hi^T
                 mma_bf16_ts_e(tmem + TM_O, tmem + TM_X, smem_desc(pp, 16, 1024), id16, 1);
                 mma_bf16_ts_e(tmem + TM_O, tmem + TM_X, smem_desc(pp + 2048, 16, 1024), id16, 1);
@@ -438,16 +473,43 @@ __global__ void __launch_bounds__(THREADS, 1) decode_tc_kernel(const __grid_cons
         while (!mbar_try_wait_sleep(&bars->drain, 0, 20000) && globaltimer_ns() - t0 < WAIT_NS) {
         }
         __syncwarp();
-    } else if (tid == 288) {
+    } else if (tid == TMA_TID) {
         // ============================ TMA producer (one thread) ============================
         prefetch_tensormap(&p.map_q);
         prefetch_tensormap(&p.map_k);
         prefetch_tensormap(&p.map_v);
         bool ok = true;
-        int gb = 0, s_issued = 0, it = 0, kqv_issued = 0;
+        int gb = 0, kqv_issued = 0;
+        for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+            const int b = u / p.H, h = u % p.H;
+            for (int blk = 0; blk < nblk && ok; ++blk, ++gb) {
+                const int st = gb & 1;
+                if (gb >= 2 && !(ok = dt_wait(&bars->kqv_empty[st], ((gb - 2) >> 1) & 1, abort_flag, wait_ns))) break;
+                mbar_arrive_expect_tx(&bars->kqv_full[st], KQ_BYTES + V_BYTES);
+                const int t0 = blk * MB;
+                uint8_t *kq = sm + OFF_KQ + st * KQ_BYTES, *vv = sm + OFF_V + st * V_BYTES;
+                for (int cb = 0; cb < 2; ++cb) {
+                    tma_load_4d(kq + cb * 4096, &p.map_k, &bars->kqv_full[st], cb * 64, h, t0, b);
+                    tma_load_4d(kq + cb * 4096 + 2048, &p.map_q, &bars->kqv_full[st], cb * 64, h, t0, b);
+                    tma_load_4d(vv + cb * 2048, &p.map_v, &bars->kqv_full[st], cb * 64, h, t0, b);
+                }
+                kqv_issued = gb + 1;
+            }
+        }
+        // every load in flight has landed before the CTA leaves (bounded; matters after an abort)
+        for (int i = max(0, kqv_issued - 2); i < kqv_issued; ++i) {
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait_sleep(&bars->kqv_full[i & 1], (i >> 1) & 1, 20000) &&
+                   globaltimer_ns() - t0 < WAIT_NS) {
+            }
+        }
+        if (!ok) *abort_flag = 1;
+    } else if (tid == SMOVE_TID) {
+        // ============================ state mover (one thread) ============================
+        bool ok = true;
+        int s_issued = 0;
         auto load_s = [&](int unit_i, int idx) {  // S of unit unit_i into staging idx & 1
             const int sb = idx & 1;
-            if (idx >= 2 && !(ok = dt_wait(&bars->s_empty[sb], ((idx - 2) >> 1) & 1, abort_flag, wait_ns))) return;
             mbar_arrive_expect_tx(&bars->s_full[sb], S_BYTES);
             const float *src = p.S + (size_t)unit_i * D * D;
             uint8_t *dst = sm + OFF_S + sb * S_BYTES;
@@ -455,31 +517,24 @@ __global__ void __launch_bounds__(THREADS, 1) decode_tc_kernel(const __grid_cons
             s_issued = idx + 1;
         };
         load_s(blockIdx.x, 0);
+        if ((int)(blockIdx.x + gridDim.x) < units) load_s(blockIdx.x + gridDim.x, 1);
+        int it = 0;
         for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++it) {
-            const int b = u / p.H, h = u % p.H;
-            if (u + (int)gridDim.x < units) load_s(u + gridDim.x, it + 1);  // the next unit's S streams in
-            for (int blk = 0; blk < nblk && ok; ++blk, ++gb) {
-                if (gb > 0 && !(ok = dt_wait(&bars->kqv_empty, (gb - 1) & 1, abort_flag, wait_ns))) break;
-                mbar_arrive_expect_tx(&bars->kqv_full, 12288);
-                const int t0 = blk * MB;
-                for (int cb = 0; cb < 2; ++cb) {
-                    tma_load_4d(sm + OFF_KQ + cb * 4096, &p.map_k, &bars->kqv_full, cb * 64, h, t0, b);
-                    tma_load_4d(sm + OFF_KQ + cb * 4096 + 2048, &p.map_q, &bars->kqv_full, cb * 64, h, t0, b);
-                    tma_load_4d(sm + OFF_V + cb * 2048, &p.map_v, &bars->kqv_full, cb * 64, h, t0, b);
-                }
-                kqv_issued = gb + 1;
-            }
+            const int sb = it & 1;
+            if (!(ok = dt_wait(&bars->s_out[sb], (it >> 1) & 1, abort_flag, wait_ns))) break;
+            uint8_t *src = sm + OFF_S + sb * S_BYTES;
+            float *dst = p.S + (size_t)u * D * D;
+            for (int q = 0; q < 4; ++q) bulk_store(dst + q * 4096, src + q * 16384, 16384);
+            bulk_commit();
+            bulk_wait_read0();  // the buffer is free once the copy has read it
+            const int u2 = u + 2 * (int)gridDim.x;
+            if (u2 < units) load_s(u2, it + 2);
         }
+        bulk_wait0();
         // every load in flight has landed before the CTA leaves (bounded; matters after an abort)
         for (int i = max(0, s_issued - 2); i < s_issued; ++i) {
             const uint64_t t0 = globaltimer_ns();
             while (!mbar_try_wait_sleep(&bars->s_full[i & 1], (i >> 1) & 1, 20000) && globaltimer_ns() - t0 < WAIT_NS) {
-            }
-        }
-        if (kqv_issued > 0) {
-            const uint64_t t0 = globaltimer_ns();
-            while (!mbar_try_wait_sleep(&bars->kqv_full, (kqv_issued - 1) & 1, 20000) &&
-                   globaltimer_ns() - t0 < WAIT_NS) {
             }
         }
         if (!ok) *abort_flag = 1;
@@ -505,16 +560,19 @@ PFN_cuTensorMapEncodeTiled_v12000 dt_encode_fn() {
     return fn;
 }
 
-// [B, m, H, 128] bf16: box of 64 features x 1 head x 16 tokens x 1, 128-byte swizzle.
-bool dt_map(CUtensorMap *mp, const void *ptr, int B, int m, int H) {
+// [B, m, H, 128] of 2-byte (bf16) or 4-byte (fp32) elements: a box of 128 bytes of features x
+// 1 head x 16 tokens x 1; inputs with the 128-byte swizzle of the MMA operands, o unswizzled.
+bool dt_map(CUtensorMap *mp, const void *ptr, int B, int m, int H, bool f32, bool swizzle) {
     auto fn = dt_encode_fn();
     if (!fn) return false;
+    const cuuint64_t es_b = f32 ? 4 : 2;
     cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)m, (cuuint64_t)B};
-    cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2, (cuuint64_t)m * H * D * 2};
-    cuuint32_t box[4] = {64, 1, (cuuint32_t)MB, 1};
+    cuuint64_t strides[3] = {(cuuint64_t)D * es_b, (cuuint64_t)H * D * es_b, (cuuint64_t)m * H * D * es_b};
+    cuuint32_t box[4] = {(cuuint32_t)(128 / es_b), 1, (cuuint32_t)MB, 1};
     cuuint32_t es[4] = {1, 1, 1, 1};
-    return fn(mp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims, strides, box, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    return fn(mp, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr),
+              dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -541,8 +599,9 @@ cudaError_t launch_decode_tokens_tc(const DecodeArgs &a, const char **why) {
     if (a.B == 0 || a.m == 0) return cudaSuccess;
     DtParams p;
     memset(&p, 0, sizeof p);
-    if (!dt_map(&p.map_q, a.q, a.B, a.m, a.H) || !dt_map(&p.map_k, a.k, a.B, a.m, a.H) ||
-        !dt_map(&p.map_v, a.v, a.B, a.m, a.H)) {
+    if (!dt_map(&p.map_q, a.q, a.B, a.m, a.H, false, true) || !dt_map(&p.map_k, a.k, a.B, a.m, a.H, false, true) ||
+        !dt_map(&p.map_v, a.v, a.B, a.m, a.H, false, true) ||
+        !dt_map(&p.map_o, a.o, a.B, a.m, a.H, a.o_dtype != EFLA_BF16, false)) {
         *why = "cuTensorMapEncodeTiled failed";
         return cudaErrorInvalidValue;
     }

@@ -355,3 +355,18 @@ __device__ __forceinline__ void tmem_st8u(uint32_t taddr, const uint32_t (&u)[8]
 
 }  // namespace ptx
 }  // namespace efla
+
+namespace efla {
+namespace ptx {
+
+// Bulk (non-tensor) copy shared -> global, completion through this thread's bulk groups
+// (bulk_commit / bulk_wait_read0 / bulk_wait0).  Both addresses 16-byte aligned, bytes a
+// multiple of 16.
+__device__ __forceinline__ void bulk_store(void *dst, const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(reinterpret_cast<uint64_t>(dst)),
+                 "r"(smem_u32(src)), "r"(bytes)
+                 : "memory");
+}
+
+}  // namespace ptx
+}  // namespace efla
