@@ -239,6 +239,9 @@ def run_ours(args, world, rank, local):
     S_T = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
+    if args.leg != "all":  # one secondary figure alone (profiling runs); no contract line
+        print(json.dumps({args.leg: run_leg(args, efla, dev, stream, flush, q, k, v, beta)}), flush=True)
+        return
 
     def step():
         efla.fwd_chunked(q, k, v, beta, None, None, o=o, S_T=S_T, chunk=CHUNK, stream=stream)
@@ -401,6 +404,19 @@ def run_ours(args, world, rank, local):
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
+
+
+def run_leg(args, efla, dev, stream, flush, q, k, v, beta):
+    peaks = read_peaks()
+    if args.leg == "decode":
+        return decode_figures(efla, dev, stream)
+    if args.leg == "decode_tokens":
+        return decode_tokens_figure(efla, dev, stream, args.steps, flush, peaks)
+    if args.leg == "bwd":
+        return bwd_figure(efla, dev, stream, q, k, v, beta, flush, peaks)
+    if args.leg == "stiff":
+        return stiff_figure(efla, dev, stream, max(3, args.steps // 2), flush, peaks)
+    return varlen_figure(efla, dev, stream, max(3, args.steps // 2), flush, peaks)
 
 
 def time_steps(fn, steps, flush, stream):
@@ -576,6 +592,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--leg", choices=["all", "decode", "decode_tokens", "bwd", "stiff", "varlen"], default="all",
+                    help="run one secondary figure alone and print it (for profiling); 'all' is the bench")
     args = ap.parse_args()
     world, rank, local = dist_init()
     if args.impl == "reference":
