@@ -24,8 +24,8 @@ from typing import Optional, Tuple
 import torch
 
 __all__ = ["EflaError", "lib_path", "load", "fwd_chunked", "fwd_chunked_scan", "fwd_chunked_scan_static",
-           "scan_workspace", "fwd_recurrent", "decode_step", "decode_tokens", "bwd_recurrent", "prep",
-           "device_status", "error_string", "set_wait_limit_ns", "set_debug_stall", "abi_version", "STATUS", "UPDATES"]
+           "scan_workspace", "fwd_recurrent", "decode_step", "decode_tokens", "bwd_recurrent", "bwd_chunked",
+           "bwd_workspace", "prep", "device_status", "error_string", "set_wait_limit_ns", "set_debug_stall", "abi_version", "STATUS", "UPDATES"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 lib_path = os.path.join(_PKG, "libefla.so")
@@ -76,6 +76,10 @@ def load():
         L.efla_fwd_scan_workspace.argtypes = [ip] * 6 + [ctypes.POINTER(ctypes.c_size_t), ctypes.POINTER(ip)]
         L.efla_bwd_recurrent.restype = ip
         L.efla_bwd_recurrent.argtypes = [vp] * 12 + [ip] * 7 + [vp]
+        L.efla_bwd_chunked.restype = ip
+        L.efla_bwd_chunked.argtypes = [vp] * 12 + [ip] * 7 + [vp, ctypes.c_size_t, vp]
+        L.efla_bwd_workspace.restype = ip
+        L.efla_bwd_workspace.argtypes = [ip] * 5 + [ctypes.POINTER(ctypes.c_size_t)]
         L.efla_decode_tokens.restype = ip
         L.efla_decode_tokens.argtypes = [vp] * 6 + [ip] * 8 + [vp]
         L.efla_prep.restype = ip
@@ -323,11 +327,32 @@ def decode_tokens(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch
     return o
 
 
+def bwd_workspace(B: int, T: int, H: int, dk: int = 128, dv: int = 128) -> int:
+    """Workspace bytes of ``bwd_chunked`` (``efla_bwd_workspace``)."""
+    L = load()
+    nb = ctypes.c_size_t(0)
+    _check(L.efla_bwd_workspace(B, T, H, dk, dv, ctypes.byref(nb)))
+    return nb.value
+
+
+def bwd_chunked(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor,
+                S0: Optional[torch.Tensor], dO: torch.Tensor, dS_T: Optional[torch.Tensor] = None, *,
+                need_dS0: bool = True, workspace: Optional[torch.Tensor] = None, stream=None,
+                update: str = "exact") -> dict:
+    """``bwd_recurrent`` evaluated in chunks of 64 tokens (``efla_bwd_chunked``); ``workspace``
+    (a CUDA tensor of at least ``bwd_workspace(...)`` bytes) is allocated here when not given."""
+    return _bwd("chunked", q, k, v, beta, S0, dO, dS_T, need_dS0, workspace, stream, update)
+
+
 def bwd_recurrent(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor,
                   S0: Optional[torch.Tensor], dO: torch.Tensor, dS_T: Optional[torch.Tensor] = None, *,
                   need_dS0: bool = True, stream=None, update: str = "exact") -> dict:
     """Gradients of ``fwd_chunked`` (no cu_seqlens) from dO [B,T,H,dv] fp32 and dS_T
     [B,H,dk,dv] fp32 (or None): returns dq, dk, dv, dbeta and dS0 (fp32), ``efla_bwd_recurrent``."""
+    return _bwd("recurrent", q, k, v, beta, S0, dO, dS_T, need_dS0, None, stream, update)
+
+
+def _bwd(kind, q, k, v, beta, S0, dO, dS_T, need_dS0, workspace, stream, update):
     L = load()
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (beta, "beta"), (S0, "S0"), (dO, "dO"), (dS_T, "dS_T")):
         _need(t, n)
@@ -346,9 +371,16 @@ def bwd_recurrent(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch
     out = {"dq": torch.empty((B, T, H, dk), **f32), "dk": torch.empty((B, T, H, dk), **f32),
            "dv": torch.empty((B, T, H, dv), **f32), "dbeta": torch.empty((B, T, H), **f32),
            "dS0": torch.empty((B, H, dk, dv), **f32) if need_dS0 else None}
-    _check(L.efla_bwd_recurrent(_p(q), _p(k), _p(v), _p(beta), _p(S0), _p(dO), _p(dS_T), _p(out["dq"]),
-                                _p(out["dk"]), _p(out["dv"]), _p(out["dbeta"]), _p(out["dS0"]), B, T, H, dk, dv,
-                                _dt(q.dtype), UPDATES[update], _stream(stream)))
+    args = (_p(q), _p(k), _p(v), _p(beta), _p(S0), _p(dO), _p(dS_T), _p(out["dq"]), _p(out["dk"]), _p(out["dv"]),
+            _p(out["dbeta"]), _p(out["dS0"]), B, T, H, dk, dv, _dt(q.dtype), UPDATES[update])
+    if kind == "recurrent":
+        _check(L.efla_bwd_recurrent(*args, _stream(stream)))
+        return out
+    _need(workspace, "workspace")
+    need = bwd_workspace(B, T, H, dk, dv)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    _check(L.efla_bwd_chunked(*args, _p(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
     return out
 
 

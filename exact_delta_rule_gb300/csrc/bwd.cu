@@ -29,26 +29,6 @@ namespace {
 
 constexpr int NT = 1024;
 
-// d alpha / d beta and d alpha / d lambda (fp32; series in z = beta*lambda where the
-// difference form cancels).
-__device__ __forceinline__ void gate_grad(float beta, float lam, int euler, float &dfdb, float &dfdl) {
-    if (euler) {
-        dfdb = 1.f;
-        dfdl = 0.f;
-        return;
-    }
-    const float z = beta * lam;
-    if (lam > 0.f && fabsf(z) >= 0.1f) {
-        const float e = expf(-z);
-        const float f = -expm1f(-z) / lam;
-        dfdb = e;
-        dfdl = (beta * e - f) / lam;
-    } else {
-        dfdb = lam > 0.f ? expf(-z) : 1.f;
-        dfdl = beta * beta * (-0.5f + z * (1.f / 3.f + z * (-1.f / 8.f + z * (1.f / 30.f - z * (1.f / 144.f)))));
-    }
-}
-
 template <int DK, int DV>
 struct BwdSmem {
     static constexpr int RP = 33;                          // row partials [DK][RP] (padded)

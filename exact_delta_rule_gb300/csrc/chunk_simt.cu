@@ -61,9 +61,14 @@ __global__ void __launch_bounds__(THREADS, 1) chunk_simt_kernel(FwdArgs a) {
 
     for (int e = tid; e < dk * dv; e += THREADS) Ss[e] = a.S0 ? a.S0[sbase + e] : 0.f;
 
+    const int nch = (int)((eos - bos + C - 1) / C);
     for (long t0 = bos; t0 < eos; t0 += C) {
         const int valid = (int)min((long)C, eos - t0);
         __syncthreads();  // the previous chunk is done with every buffer
+        if (a.states) {  // the chunk's start state (chunked backward)
+            float *dst = a.states + ((size_t)blockIdx.x * nch + (t0 - bos) / C) * dk * dv;
+            for (int e = tid; e < dk * dv; e += THREADS) dst[e] = Ss[e];
+        }
         // inputs of the chunk (rows past its end are zero)
         for (int e = tid; e < C * dk; e += THREADS) {
             const int t = e / dk, i = e % dk;
@@ -133,7 +138,7 @@ __global__ void __launch_bounds__(THREADS, 1) chunk_simt_kernel(FwdArgs a) {
             float y = Os[e];
             for (int s = 0; s <= t; ++s) y = fmaf(Ps[t * C + s], Us[s * dv + j], y);
             const size_t row = ((size_t)b * a.T + (size_t)(t0 + t)) * a.H + h;
-            o[row * dv + j] = from_f32<TOut>(y);
+            if (o) o[row * dv + j] = from_f32<TOut>(y);
         }
         for (int e = tid; e < dk * dv; e += THREADS) {
             const int i = e / dv, j = e % dv;

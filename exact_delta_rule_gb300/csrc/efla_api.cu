@@ -361,6 +361,79 @@ efla_status efla_bwd_recurrent(const void *q, const void *k, const void *v, cons
     return EFLA_OK;
 }
 
+efla_status efla_bwd_workspace(int B, int T, int H, int d_k, int d_v, size_t *bytes) {
+    if (!bytes) return fail(EFLA_ERR_INVALID_ARG, "bytes must be non-NULL");
+    if (B < 0 || T < 0 || H <= 0) return fail(EFLA_ERR_INVALID_ARG, "bad sizes B=%d T=%d H=%d", B, T, H);
+    if (d_k != d_v || (d_k != 64 && d_k != 128))
+        return fail(EFLA_ERR_UNSUPPORTED, "the chunked backward supports d_k = d_v in {64, 128} (got %d, %d)", d_k, d_v);
+    const size_t nc = ((size_t)T + 63) / 64;
+    *bytes = 2 * (size_t)B * H * nc * d_k * d_v * sizeof(float);
+    return EFLA_OK;
+}
+
+efla_status efla_bwd_chunked(const void *q, const void *k, const void *v, const float *beta, const float *S0,
+                             const float *dO, const float *dS_T, float *dq, float *dk, float *dv, float *dbeta,
+                             float *dS0, int B, int T, int H, int d_k, int d_v, efla_dtype in_dtype,
+                             efla_update update, void *workspace, size_t workspace_bytes, efla_stream_t stream) {
+    if (!update_ok(update)) return fail(EFLA_ERR_INVALID_ARG, "unknown update rule %d", (int)update);
+    if (B < 0 || T < 0 || H <= 0) return fail(EFLA_ERR_INVALID_ARG, "bad sizes B=%d T=%d H=%d", B, T, H);
+    efla_status s = check_dims_common(d_k, d_v, in_dtype, EFLA_F32);
+    if (s != EFLA_OK) return s;
+    size_t need = 0;
+    if ((s = efla_bwd_workspace(B, T, H, d_k, d_v, &need)) != EFLA_OK) return s;
+    const long long rows = (long long)B * T * H;
+    if (rows > (1LL << 31) - 1) return fail(EFLA_ERR_UNSUPPORTED, "B*T*H=%lld exceeds 2^31-1", rows);
+    if (rows > 0 && (!q || !k || !v || !beta || !dO || !dq || !dk || !dv || !dbeta))
+        return fail(EFLA_ERR_INVALID_ARG, "q, k, v, beta, dO, dq, dk, dv and dbeta must be non-NULL when B*T > 0");
+    if (need > 0 && (!workspace || workspace_bytes < need))
+        return fail(EFLA_ERR_INVALID_ARG, "workspace of %zu bytes needed (got %zu at %p)", need, workspace_bytes,
+                    workspace);
+    const void *ptrs[] = {q, k, v, beta, S0, dO, dS_T, dq, dk, dv, dbeta, dS0, workspace};
+    const char *names[] = {"q", "k", "v", "beta", "S0", "dO", "dS_T", "dq", "dk", "dv", "dbeta", "dS0", "workspace"};
+    for (int i = 0; i < 13; ++i)
+        if (ptrs[i] && !aligned16(ptrs[i]))
+            return fail(EFLA_ERR_INVALID_ARG, "%s=%p is not 16-byte aligned", names[i], ptrs[i]);
+    const size_t th = (size_t)rows, st = (size_t)B * H * d_k * d_v * 4;
+    auto R = [](const char *n, const void *p, size_t bytes) {
+        uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+        return Range{n, lo, p ? lo + bytes : lo};
+    };
+    const Range in[] = {R("q", q, th * d_k * dsize(in_dtype)), R("k", k, th * d_k * dsize(in_dtype)),
+                        R("v", v, th * d_v * dsize(in_dtype)), R("beta", beta, th * 4), R("S0", S0, st),
+                        R("dO", dO, th * d_v * 4), R("dS_T", dS_T, st)};
+    const Range out[] = {R("dq", dq, th * d_k * 4), R("dk", dk, th * d_k * 4), R("dv", dv, th * d_v * 4),
+                         R("dbeta", dbeta, th * 4), R("dS0", dS0, st), R("workspace", workspace, need)};
+    for (int i = 0; i < 6; ++i) {
+        for (const Range &r : in)
+            if (overlap(out[i], r)) return fail(EFLA_ERR_INVALID_ARG, "%s overlaps input %s", out[i].name, r.name);
+        for (int j = i + 1; j < 6; ++j)
+            if (overlap(out[i], out[j])) return fail(EFLA_ERR_INVALID_ARG, "%s and %s overlap", out[i].name, out[j].name);
+    }
+    if ((long long)B * H == 0) {
+        g_last_error.clear();
+        return EFLA_OK;
+    }
+    int *status = device_status_ptr();
+    if (!status) return fail(EFLA_ERR_CUDA, "cannot resolve the device status word");
+    const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    float *states = static_cast<float *>(workspace);
+    float *dse = states + need / (2 * sizeof(float));
+    cudaError_t e;
+    if (T > 0) {  // the forward, keeping the state at the start of every chunk (o and S_T not needed)
+        FwdArgs fa{q, k, v, beta, S0, nullptr, nullptr, nullptr, B, T, H, d_k, d_v, B, in_dtype, in_dtype,
+                   64, cs, status, (int)update};
+        fa.states = states;
+        const char *why = "chunk kernel launch (backward states)";
+        e = in_dtype == EFLA_BF16 && d_k == 128 ? launch_chunk_tc(fa, &why) : launch_chunk_simt(fa);
+        if (e != cudaSuccess) return cuda_fail(e, why);
+    }
+    BwdArgs a{q, k, v, beta, S0, dO, dS_T, dq, dk, dv, dbeta, dS0, B, T, H, d_k, d_v, in_dtype, cs, (int)update};
+    e = launch_bwd_chunked(a, states, dse);
+    if (e != cudaSuccess) return cuda_fail(e, "chunked backward kernel launch");
+    g_last_error.clear();
+    return EFLA_OK;
+}
+
 efla_status efla_fwd_recurrent_ex(const void *q, const void *k, const void *v, const float *beta,
                                   const float *S0, const int32_t *cu_seqlens, void *o, float *S_T, int B,
                                   int T, int H, int d_k, int d_v, int N, efla_dtype in_dtype,

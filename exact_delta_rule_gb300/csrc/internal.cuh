@@ -38,6 +38,9 @@ struct FwdArgs {
     int seg_len = 0, G = 0;
     const float *s_in = nullptr;
     float *maps = nullptr;
+    // Chunked backward: the state at the start of every chunk, [N, H, nchunks, dk, dv] fp32
+    // (rows of [B, T] only; o may then be nullptr).
+    float *states = nullptr;
 };
 
 struct DecodeArgs {
@@ -81,6 +84,10 @@ struct BwdArgs {
     int euler;
 };
 cudaError_t launch_bwd(const BwdArgs &a);
+// Chunked backward (bwd_chunk.cu), chunk 64, rows of [B, T]: the state gradients at the ends of
+// the chunks from `states` (the forward's chunk-start states, filled first by a forward launch
+// with FwdArgs::states), then every chunk's gradients in parallel.  dse: [B, H, nchunks, dk, dv].
+cudaError_t launch_bwd_chunked(const BwdArgs &a, const float *states, float *dse);
 
 // Start states of the segments of split sequences from the segment maps (scan.cu).
 cudaError_t launch_scan_combine(const float *S0, const float *maps, float *s_in, int B, int G, int H,
@@ -97,6 +104,26 @@ template <typename T> __device__ __forceinline__ T from_f32(float x);
 template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
 template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
     return __float2bfloat16_rn(x);
+}
+
+// d alpha / d beta and d alpha / d lambda of alpha = f(beta, lambda) (fp32; a series in
+// z = beta*lambda where the difference form cancels).
+__device__ __forceinline__ void gate_grad(float beta, float lam, int euler, float &dfdb, float &dfdl) {
+    if (euler) {
+        dfdb = 1.f;
+        dfdl = 0.f;
+        return;
+    }
+    const float z = beta * lam;
+    if (lam > 0.f && fabsf(z) >= 0.1f) {
+        const float e = expf(-z);
+        const float f = -expm1f(-z) / lam;
+        dfdb = e;
+        dfdl = (beta * e - f) / lam;
+    } else {
+        dfdb = lam > 0.f ? expf(-z) : 1.f;
+        dfdl = beta * beta * (-0.5f + z * (1.f / 3.f + z * (-1.f / 8.f + z * (1.f / 30.f - z * (1.f / 144.f)))));
+    }
 }
 
 // alpha = (1 - e^{-beta*lam}) / lam, evaluated as -expm1(-beta*lam)/lam; beta at lam == 0.

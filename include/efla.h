@@ -45,7 +45,7 @@
 extern "C" {
 #endif
 
-#define EFLA_ABI_VERSION 7
+#define EFLA_ABI_VERSION 8
 
 typedef enum {
     EFLA_OK = 0,
@@ -223,6 +223,34 @@ efla_status efla_bwd_recurrent(const void *q, const void *k, const void *v, cons
                                float *dk, float *dv, float *dbeta, float *dS0, int B, int T, int H,
                                int d_k, int d_v, efla_dtype in_dtype, efla_update update,
                                efla_stream_t stream);
+
+/*
+ * efla_bwd_chunked -- the gradients of efla_bwd_recurrent, evaluated in chunks of 64 tokens.
+ *
+ * Same arguments, layouts, outputs and rules as efla_bwd_recurrent, plus a workspace.  The
+ * pages give no backward formulas: this is reverse mode of the chunkwise (WY/UT) form of the
+ * forward ("Error-Free Linear Attention is a Free Lunch" (howistudyai), Step 4 "Chunkwise
+ * Parallelism"; "Exact Flow Linear Attention" (gist.science), Metodologia 3).  Three steps
+ * on `stream`: the forward, writing the state at the start of every chunk into the
+ * workspace (the tensor-core chunk kernel for bf16 with d = 128); one CTA per (b, h) that
+ * walks the chunks in reverse for the gradient of each chunk's end state (also into the
+ * workspace); then one CTA per (b, h, chunk), all independent, for every token's gradients
+ * (fp32 on CUDA cores).
+ *
+ *   workspace  device scratch owned by the caller, 16-byte aligned, at least the size
+ *              efla_bwd_workspace reports (2 x B x H x ceil(T/64) x d_k x d_v x 4 bytes);
+ *              it must not overlap any argument.  Too small or NULL: EFLA_ERR_INVALID_ARG.
+ * Supported: d_k = d_v in {64, 128} (other sizes: EFLA_ERR_UNSUPPORTED, use
+ * efla_bwd_recurrent).
+ */
+efla_status efla_bwd_chunked(const void *q, const void *k, const void *v, const float *beta,
+                             const float *S0, const float *dO, const float *dS_T, float *dq,
+                             float *dk, float *dv, float *dbeta, float *dS0, int B, int T, int H,
+                             int d_k, int d_v, efla_dtype in_dtype, efla_update update,
+                             void *workspace, size_t workspace_bytes, efla_stream_t stream);
+
+/* Workspace bytes efla_bwd_chunked needs for these sizes (into *bytes). */
+efla_status efla_bwd_workspace(int B, int T, int H, int d_k, int d_v, size_t *bytes);
 
 /*
  * efla_decode_tokens -- m tokens per sequence appended to a resident state,

@@ -1,8 +1,12 @@
-"""GPU parity of the backward pass (efla_bwd_recurrent) against the fp64 reverse-mode oracle.
+"""GPU parity of the backward passes (efla_bwd_recurrent, efla_bwd_chunked) against the fp64
+reverse-mode oracle.
 
-Tolerance: the kernel evaluates every gradient in fp32 on CUDA cores from exactly
+Tolerance: the kernels evaluate every gradient in fp32 on CUDA cores from exactly
 representable inputs (the oracle sees the same values upcast), so the bar is the fp32
-one used for the forward, relative Frobenius error <= 1e-4 per gradient tensor."""
+one used for the forward, relative Frobenius error <= 1e-4 per gradient tensor.  The chunked
+path takes its chunk-start states from the forward kernels (for bf16 with d = 128 the
+tensor-core kernel, whose split-bf16 products leave about 1e-5 of relative error in them);
+the same bar holds."""
 import numpy as np
 import pytest
 import torch
@@ -47,14 +51,18 @@ def _case(dtype, B, T, H, dk, dv, seed, s0=True, dst=True):
     return dict(q=q.contiguous(), k=k.contiguous(), v=v.contiguous(), beta=beta, S0=S0, dO=dO, dST=dST)
 
 
-def _check(efla, c, update="exact"):
+def _check(efla, c, update="exact", kind="recurrent"):
     d = {x: (y.to(DEV) if y is not None else None) for x, y in c.items()}
-    got = efla.bwd_recurrent(d["q"], d["k"], d["v"], d["beta"], d["S0"], d["dO"], d["dST"], update=update)
+    fn = efla.bwd_recurrent if kind == "recurrent" else efla.bwd_chunked
+    got = fn(d["q"], d["k"], d["v"], d["beta"], d["S0"], d["dO"], d["dST"], update=update)
     torch.cuda.synchronize()
     ref = oracle.bwd(c["q"], c["k"], c["v"], c["beta"], c["S0"], c["dO"], c["dST"], update=update)
     for name in ("dq", "dk", "dv", "dbeta", "dS0"):
         r = _rel(got[name], ref[name])
         assert r <= REL, f"{name}: rel-fro {r:.3e}"
+
+
+KINDS = ["recurrent", "chunked"]
 
 
 @pytest.mark.parametrize("dk,dv", [(32, 32), (64, 64), (128, 128), (64, 32), (32, 128)])
@@ -63,37 +71,79 @@ def test_bwd_small(efla, dk, dv, dtype):
     _check(efla, _case(dtype, 2, 37, 2, dk, dv, seed=dk + dv))
 
 
-def test_bwd_no_state_no_state_gradient(efla):
-    _check(efla, _case("bf16", 1, 64, 3, 128, 128, seed=4, s0=False, dst=False))
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("T", [37, 64, 200])
+def test_bwd_chunked_small(efla, d, dtype, T):
+    """One partial chunk, one full chunk, and several chunks with a ragged tail."""
+    _check(efla, _case(dtype, 2, T, 2, d, d, seed=d + T), kind="chunked")
 
 
-def test_bwd_zero_keys_and_zero_steps(efla):
-    c = _case("f32", 1, 40, 2, 64, 64, seed=6)
+@pytest.mark.parametrize("kind", KINDS)
+def test_bwd_no_state_no_state_gradient(efla, kind):
+    _check(efla, _case("bf16", 1, 64, 3, 128, 128, seed=4, s0=False, dst=False), kind=kind)
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_bwd_zero_keys_and_zero_steps(efla, kind):
+    c = _case("f32", 1, 140, 2, 64, 64, seed=6)
     c["k"][:, 3::7] = 0
     c["beta"][:, 5::6] = 0
     c["beta"][:, 2::9] = 1e-4  # beta*lambda in the gate derivative's series range
-    _check(efla, c)
+    _check(efla, c, kind=kind)
 
 
-def test_bwd_delta_rule_gate(efla):
-    c = _case("f32", 2, 50, 2, 64, 64, seed=7)
+@pytest.mark.parametrize("kind", KINDS)
+def test_bwd_delta_rule_gate(efla, kind):
+    c = _case("f32", 2, 150, 2, 64, 64, seed=7)
     c["k"] = torch.nn.functional.normalize(c["k"], dim=-1).contiguous()
-    _check(efla, c, update="euler")
+    _check(efla, c, update="euler", kind=kind)
 
 
-def test_bwd_longer_sequence_lm_law(efla):
+@pytest.mark.parametrize("kind", KINDS)
+def test_bwd_longer_sequence_lm_law(efla, kind):
     inp = workloads.small_fwd("bf16", B=1, T=384, H=2, d=128, seed=19)
     g = torch.Generator().manual_seed(20)
     c = dict(q=inp["q"], k=inp["k"], v=inp["v"], beta=inp["beta"], S0=inp["S0"],
              dO=torch.randn((1, 384, 2, 128), generator=g), dST=torch.randn((1, 2, 128, 128), generator=g))
-    _check(efla, c)
+    _check(efla, c, kind=kind)
     assert efla.device_status() == 0
 
 
-def test_bwd_empty(efla):
+def test_bwd_chunked_stiff_keys(efla):
+    """Key norms U[0.1, 10] and beta = sigmoid(N(2, 1)), as in the long-sequence workload."""
+    g = torch.Generator().manual_seed(23)
+    c = _case("bf16", 1, 256, 2, 128, 128, seed=22)
+    kd = torch.nn.functional.normalize(torch.randn((1, 256, 2, 128), generator=g), dim=-1)
+    c["k"] = (kd * (0.1 + 9.9 * torch.rand((1, 256, 2, 1), generator=g))).to(torch.bfloat16).contiguous()
+    c["beta"] = torch.sigmoid(2.0 + torch.randn((1, 256, 2), generator=g))
+    _check(efla, c, kind="chunked")
+
+
+def test_bwd_chunked_equals_recurrent_lm_heads(efla):
+    """B=8 H=16 T=2048 d=128 (the language-model-layer shape): the two backward paths agree on
+    every head to rel-Frobenius <= 1e-4 (two fp32 evaluations of the same gradients)."""
+    inp = workloads.make_fwd_inputs(workloads.FWD_WORKLOADS["lm"])
+    g = torch.Generator().manual_seed(31)
+    q, k, v, beta = (inp[x].to(DEV) for x in ("q", "k", "v", "beta"))
+    B, T, H, d = q.shape
+    dO = torch.randn((B, T, H, d), generator=g).to(DEV)
+    dST = torch.randn((B, H, d, d), generator=g).to(DEV)
+    a = efla.bwd_chunked(q, k, v, beta, None, dO, dST)
+    b = efla.bwd_recurrent(q, k, v, beta, None, dO, dST)
+    torch.cuda.synchronize()
+    for name in ("dq", "dk", "dv", "dbeta", "dS0"):
+        r = ((a[name] - b[name]).norm() / b[name].norm()).item()
+        assert r <= REL, f"{name}: rel-fro {r:.3e}"
+    assert efla.device_status() == 0
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_bwd_empty(efla, kind):
+    fn = efla.bwd_recurrent if kind == "recurrent" else efla.bwd_chunked
     e = torch.empty((2, 0, 2, 64), device=DEV)
     S0 = torch.randn((2, 2, 64, 64), device=DEV)
     dST = torch.randn((2, 2, 64, 64), device=DEV)
-    out = efla.bwd_recurrent(e, e, e, torch.empty((2, 0, 2), device=DEV), S0, e, dST)
+    out = fn(e, e, e, torch.empty((2, 0, 2), device=DEV), S0, e, dST)
     torch.cuda.synchronize()
     assert torch.equal(out["dS0"], dST)
