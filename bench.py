@@ -494,10 +494,24 @@ def bwd_figure(efla, dev, stream, q, k, v, beta, flush, peaks, steps=3):
     g = torch.Generator(device=dev).manual_seed(7)
     dO = torch.randn((B, T, H, dv), generator=g, device=dev)
     dST = torch.randn((B, H, dk, dv), generator=g, device=dev)
-    t = time_steps(lambda: efla.bwd_recurrent(q, k, v, beta, None, dO, dST, stream=stream), steps, flush, stream)
-    return {"workload": "lm shape backward: dq, dk, dv, dbeta, dS0 from random dO and dS_T (fp32 on CUDA cores, "
-                        "one CTA per (b, h), forward sweep + reverse sweep)",
-            "ms_per_call": 1e3 * t, "tokens_per_s": B * T / t, "gpu_launches": steps}
+    ws = torch.empty(efla.bwd_workspace(B, T, H, dk, dv), dtype=torch.uint8, device=dev)
+    t = time_steps(lambda: efla.bwd_chunked(q, k, v, beta, None, dO, dST, workspace=ws, stream=stream), steps,
+                   flush, stream)
+    t_rec = time_steps(lambda: efla.bwd_recurrent(q, k, v, beta, None, dO, dST, stream=stream), 1, flush, stream)
+    th = B * T * H
+    # each input read once and each output written once: q, k, v bf16 + beta + dO fp32 in; dq, dk, dv fp32 +
+    # dbeta out; dS_T in and dS0 out per (b, h)
+    nbytes = th * ((dk + dk + dv) * 2 + 4 + dv * 4 + (dk + dk + dv) * 4 + 4) + 2 * B * H * dk * dv * 4
+    ws_bytes = ws.numel()
+    return {"workload": "lm shape backward (B=8 H=16 T=2048 d=128, bf16 q,k,v): dq, dk, dv, dbeta, dS0 (fp32) "
+                        "from random dO and dS_T (fp32), chunks of 64",
+            "ms_per_call": 1e3 * t, "tokens_per_s": B * T / t, "algorithmic_bytes": nbytes,
+            "GB/s": nbytes / t / 1e9, "frac_hbm": nbytes / t / 1e9 / peaks["hbm_gbs"],
+            "workspace_bytes": ws_bytes,
+            "path": "forward on the tensor cores writing every chunk-start state (workspace), reverse pass over "
+                    "chunks for the end-state gradients (one CTA per (b, h)), per-chunk gradients (one CTA per "
+                    "(b, h, chunk)), fp32 on CUDA cores",
+            "ms_recurrent": 1e3 * t_rec, "gpu_launches": 3 * steps + 1}
 
 
 def stiff_figure(efla, dev, stream, steps, flush, peaks):

@@ -288,6 +288,45 @@ def test_bwd_rejects(lib, kw, code):
     assert _last(lib)
 
 
+def _bwc(lib, ws=0xA0000000, ws_bytes=None, **kw):
+    a = dict(q=Q, k=K, v=V, beta=BETA, S0=None, dO=CU, dST=None, dq=O, dk=ST, dv=S0, db=0x90000000, dS0=None,
+             B=1, T=64, H=2, dk_=128, dv_=128, ind=0, upd=0)
+    a.update(kw)
+    vp, ip = ctypes.c_void_p, ctypes.c_int
+    f = lib.efla_bwd_chunked
+    f.restype = ip
+    f.argtypes = [vp] * 12 + [ip] * 7 + [vp, ctypes.c_size_t, vp]
+    need = 2 * a["B"] * a["H"] * ((max(a["T"], 0) + 63) // 64) * a["dk_"] * a["dv_"] * 4
+    return f(a["q"], a["k"], a["v"], a["beta"], a["S0"], a["dO"], a["dST"], a["dq"], a["dk"], a["dv"], a["db"],
+             a["dS0"], a["B"], a["T"], a["H"], a["dk_"], a["dv_"], a["ind"], a["upd"], ws,
+             need if ws_bytes is None else ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(T=-1), INVALID), (dict(H=0), INVALID), (dict(dk_=64, dv_=128), UNSUPPORTED),
+    (dict(dk_=32, dv_=32), UNSUPPORTED), (dict(dq=None), INVALID), (dict(upd=3), INVALID),
+    (dict(ws=None), INVALID), (dict(ws_bytes=1024), INVALID), (dict(ws=0xA0000000 + 8), INVALID),
+    (dict(ws=Q), INVALID),
+])
+def test_bwd_chunked_rejects(lib, kw, code):
+    """efla_bwd_chunked validates sizes, the supported shapes (d_k = d_v in {64, 128}) and its
+    workspace (present, large enough, aligned, overlapping no argument) before any launch."""
+    assert _bwc(lib, **kw) == code
+    assert _last(lib)
+
+
+def test_bwd_workspace_size(lib):
+    f = lib.efla_bwd_workspace
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_int] * 5 + [ctypes.POINTER(ctypes.c_size_t)]
+    n = ctypes.c_size_t(0)
+    assert f(8, 2048, 16, 128, 128, ctypes.byref(n)) == 0
+    assert n.value == 2 * 8 * 16 * 32 * 128 * 128 * 4
+    assert f(1, 65, 1, 64, 64, ctypes.byref(n)) == 0 and n.value == 2 * 2 * 64 * 64 * 4
+    assert f(1, 64, 1, 32, 32, ctypes.byref(n)) == UNSUPPORTED
+    assert f(1, 64, 1, 128, 128, None) == INVALID
+
+
 def test_binding_checks_dtypes_and_shapes_before_any_device_call():
     """The forward wrappers (plain, split and static-scratch) reject a non-fp32 beta, a
     wrongly shaped S0 and mismatched q/k/v before touching a device."""
