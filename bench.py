@@ -564,7 +564,7 @@ def varlen_figure(efla, dev, stream, steps, flush, peaks):
             "ms_per_call": 1e3 * t, "tokens_per_s": T / t, "algorithmic_bytes": nbytes,
             "GB/s": nbytes / t / 1e9, "frac_hbm": nbytes / t / 1e9 / peaks["hbm_gbs"],
             "tflops": flops_per_token_head(dk, dv) * T * H / t / 1e12,
-            "scheduling": "one CTA per (sequence, head) in sequence order; no longest-first ordering",
+            "scheduling": "one CTA per (sequence, head), longest sequence first (each CTA ranks the lengths)",
             "gpu_launches": steps}
 
 

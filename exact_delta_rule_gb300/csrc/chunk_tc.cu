@@ -80,7 +80,7 @@ constexpr uint32_t AT_LD = 68;
 constexpr uint32_t OFF_ROW = OFF_AT + 64 * AT_LD * 4;  // fp32: invn[64], gn[64]
 constexpr uint32_t ROW_BYTES = 2 * 64 * 4;
 constexpr uint32_t OFF_BAR = OFF_ROW + ROW_BYTES;       // mbarriers (struct Bars)
-constexpr uint32_t OFF_MISC = OFF_BAR + 224;            // tmem base (u32), abort flag (i32)
+constexpr uint32_t OFF_MISC = OFF_BAR + 224;            // tmem base (u32), abort flag (i32), sequence slot (i32)
 constexpr uint32_t SMEM_USED = OFF_MISC + 16;
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;       // + alignment slack for the 1024-byte base
 static_assert(OFF_TPP % 1024 == 0 && OFF_AT % 1024 == 0, "operand buffers must be 1024-byte aligned");
@@ -102,7 +102,10 @@ constexpr uint32_t TM_COLS = 512;
 // releases tensor memory.  The waits between roles are bounded by TcParams::wait_ns.
 constexpr uint64_t WAIT_NS = 2000000000ull;
 
-constexpr int BAR_PREP = 2;  // named barrier of the two prep warpgroups (256 threads)
+constexpr int BAR_PREP = 2;
+// Packed batches of at most this many sequences are run longest first (each CTA ranks the
+// sequence lengths itself: N^2 / threads comparisons).
+constexpr int LONGEST_FIRST_MAX_N = 128;  // named barrier of the two prep warpgroups (256 threads)
 
 struct TcParams {
     CUtensorMap map_q;
@@ -253,8 +256,26 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
             stp = p.maps + ((((size_t)(mode - 1) * p.B + b) * Gu + g) * p.H + h) * D * D;
         }
     } else {
-        const int n = blockIdx.x / p.H;
+        int n = blockIdx.x / p.H;
         h = blockIdx.x % p.H;
+        if (p.cu_seqlens && p.N <= LONGEST_FIRST_MAX_N) {
+            // Longest first: the CTAs of group r (blockIdx / H = r, dispatched roughly in that
+            // order) run the r-th longest sequence (ties by index), so the long sequences start
+            // early and the short ones fill the tail.  The ranks are a permutation of 0..N-1.
+            int *len = reinterpret_cast<int *>(sm + OFF_AT);  // free until the prep starts
+            int *slot = reinterpret_cast<int *>(sm + OFF_MISC + 8);
+            if (tid < p.N) len[tid] = p.cu_seqlens[tid + 1] - p.cu_seqlens[tid];
+            __syncthreads();
+            if (tid < p.N) {
+                const int li = len[tid];
+                int rank = 0;
+                for (int j = 0; j < p.N; ++j) rank += (len[j] > li) || (len[j] == li && j < tid);
+                if (rank == n) *slot = tid;
+            }
+            __syncthreads();
+            n = *slot;
+            __syncthreads();  // every thread has read the slot before the scratch is reused
+        }
         if (p.cu_seqlens) {
             b = 0;
             bos = p.cu_seqlens[n];
