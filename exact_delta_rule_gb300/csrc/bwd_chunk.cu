@@ -617,26 +617,30 @@ static_assert(state_smem_floats<128>() * sizeof(float) <= 232448, "state kernel 
 static_assert(grad_smem_floats<128>() * sizeof(float) <= 232448, "gradient kernel shared memory");
 
 template <typename TIn, int D>
-cudaError_t launch_d(const BwdArgs &a, const float *states, float *dse) {
+cudaError_t launch_d(const BwdArgs &a, const float *states, float *dse, bool state_pass) {
     const int nc = (a.T + C - 1) / C;
     const size_t s1 = state_smem_floats<D>() * sizeof(float), s2 = grad_smem_floats<D>() * sizeof(float);
     cudaError_t e = cudaFuncSetAttribute(bwd_state_kernel<TIn, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(bwd_grad_kernel<TIn, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s2);
     if (e != cudaSuccess) return e;
-    bwd_state_kernel<TIn, D><<<(unsigned)((long)a.B * a.H), NT, s1, a.stream>>>(a, dse);
-    if ((e = cudaGetLastError()) != cudaSuccess || nc == 0) return e;
+    if (state_pass) {
+        bwd_state_kernel<TIn, D><<<(unsigned)((long)a.B * a.H), NT, s1, a.stream>>>(a, dse);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    if (nc == 0) return cudaSuccess;
     bwd_grad_kernel<TIn, D><<<(unsigned)((long)a.B * a.H * nc), NT, s2, a.stream>>>(a, states, dse);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_bwd_chunked(const BwdArgs &a, const float *states, float *dse) {
+cudaError_t launch_bwd_chunked(const BwdArgs &a, const float *states, float *dse, bool state_pass) {
     if ((long long)a.B * a.H == 0) return cudaSuccess;
     const bool bf = a.in_dtype == EFLA_BF16;
-    if (a.dk_dim == 64) return bf ? launch_d<__nv_bfloat16, 64>(a, states, dse) : launch_d<float, 64>(a, states, dse);
-    return bf ? launch_d<__nv_bfloat16, 128>(a, states, dse) : launch_d<float, 128>(a, states, dse);
+    if (a.dk_dim == 64)
+        return bf ? launch_d<__nv_bfloat16, 64>(a, states, dse, state_pass) : launch_d<float, 64>(a, states, dse, state_pass);
+    return bf ? launch_d<__nv_bfloat16, 128>(a, states, dse, state_pass) : launch_d<float, 128>(a, states, dse, state_pass);
 }
 
 }  // namespace efla

@@ -367,7 +367,8 @@ efla_status efla_bwd_workspace(int B, int T, int H, int d_k, int d_v, size_t *by
     if (d_k != d_v || (d_k != 64 && d_k != 128))
         return fail(EFLA_ERR_UNSUPPORTED, "the chunked backward supports d_k = d_v in {64, 128} (got %d, %d)", d_k, d_v);
     const size_t nc = ((size_t)T + 63) / 64;
-    *bytes = 2 * (size_t)B * H * nc * d_k * d_v * sizeof(float);
+    // chunk-start states and end-state gradients (fp32), then dO as bf16 hi and lo
+    *bytes = 2 * (size_t)B * H * nc * d_k * d_v * sizeof(float) + 2 * (size_t)B * T * H * d_v * 2;
     return EFLA_OK;
 }
 
@@ -416,8 +417,10 @@ efla_status efla_bwd_chunked(const void *q, const void *k, const void *v, const 
     int *status = device_status_ptr();
     if (!status) return fail(EFLA_ERR_CUDA, "cannot resolve the device status word");
     const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    const size_t state_floats = (size_t)B * H * (((size_t)T + 63) / 64) * d_k * d_v;
     float *states = static_cast<float *>(workspace);
-    float *dse = states + need / (2 * sizeof(float));
+    float *dse = states + state_floats;
+    void *do_split = dse + state_floats;
     cudaError_t e;
     if (T > 0) {  // the forward, keeping the state at the start of every chunk (o and S_T not needed)
         FwdArgs fa{q, k, v, beta, S0, nullptr, nullptr, nullptr, B, T, H, d_k, d_v, B, in_dtype, in_dtype,
@@ -428,7 +431,13 @@ efla_status efla_bwd_chunked(const void *q, const void *k, const void *v, const 
         if (e != cudaSuccess) return cuda_fail(e, why);
     }
     BwdArgs a{q, k, v, beta, S0, dO, dS_T, dq, dk, dv, dbeta, dS0, B, T, H, d_k, d_v, in_dtype, cs, (int)update};
-    e = launch_bwd_chunked(a, states, dse);
+    const bool tc = in_dtype == EFLA_BF16 && d_k == 128 && T > 0;  // the state pass on the tensor cores
+    if (tc) {
+        const char *why = "tcgen05 state-gradient kernel launch";
+        e = launch_bwd_state_tc(a, dse, do_split, &why);
+        if (e != cudaSuccess) return cuda_fail(e, why);
+    }
+    e = launch_bwd_chunked(a, states, dse, !tc);
     if (e != cudaSuccess) return cuda_fail(e, "chunked backward kernel launch");
     g_last_error.clear();
     return EFLA_OK;

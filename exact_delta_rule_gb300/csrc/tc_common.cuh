@@ -1,0 +1,66 @@
+// Helpers shared by the tcgen05 kernels: bounded mbarrier waits that also give up when
+// another role of the CTA has aborted, a loop-counter barrier for the optimiser, and the
+// bf16 hi/lo operand split.
+#pragma once
+
+#include "ptx.cuh"
+
+namespace efla {
+namespace tc {
+namespace {  // internal to each kernel's translation unit
+using namespace ptx;
+
+// Bounded wait that also gives up when another role has aborted.  The slow
+// path is out of line: it is reached rarely and the kernel's code must stay
+// small enough for the instruction cache.
+__device__ __noinline__ bool wait_bar_slow(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                           uint64_t limit_ns) {
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait_sleep(bar, parity, 20000)) return true;  // sleeps instead of spinning
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > limit_ns) {
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort_flag, uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait_bar_slow(bar, parity, abort_flag, limit_ns);
+}
+// The same for all 32 lanes of a warp, with one outcome for the whole warp: every lane
+// waits, and the warp proceeds only if every lane's wait succeeded (the warp-collective
+// TMEM loads and stores that follow need all lanes together).
+__device__ __forceinline__ bool wait_bar_warp(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                              uint64_t limit_ns) {
+    const bool ok = wait_bar(bar, parity, abort_flag, limit_ns);
+    return __all_sync(0xffffffffu, ok);
+}
+
+// Hides a loop counter from the optimiser so that the loop stays rolled (the
+// kernel's per-chunk code must fit the instruction cache).
+__device__ __forceinline__ int opaque(int i) {
+    asm volatile("" : "+r"(i));
+    return i;
+}
+
+// Splits pairs x[2c], x[2c+1] into packed bf16 hi and lo words with
+// x = hi + lo + e, |e| < 2^-14 |x|: hi is x truncated to bf16 (its upper 16
+// bits), lo is the exact fp32 remainder x - hi truncated the same way.  Bit
+// operations only (one byte permute per packed pair).
+template <int NP>
+__device__ __forceinline__ void split_pack(const float *x, uint32_t *hi, uint32_t *lo) {
+#pragma unroll
+    for (int c = 0; c < NP; ++c) {
+        const uint32_t b0 = __float_as_uint(x[2 * c]), b1 = __float_as_uint(x[2 * c + 1]);
+        hi[c] = __byte_perm(b0, b1, 0x7632);
+        const float r0 = x[2 * c] - __uint_as_float(b0 & 0xffff0000u);
+        const float r1 = x[2 * c + 1] - __uint_as_float(b1 & 0xffff0000u);
+        lo[c] = __byte_perm(__float_as_uint(r0), __float_as_uint(r1), 0x7632);
+    }
+}
+
+}  // namespace
+}  // namespace tc
+}  // namespace efla
