@@ -15,7 +15,8 @@
 //   dR^T = G^T T''                   (N = 64; T'' as an MN-major operand)
 //   dS^T += dO^T Q - dR^T K          (N = 128; Q and K as MN-major operands)
 // dO (fp32) enters as bf16 hi and lo arrays written by a pre-pass (split_do_kernel) and loaded
-// by TMA like the other inputs.
+// by TMA like the other inputs.  G and dR (= dv) of every token are written out for the
+// per-chunk gradient kernel, which then forms neither.
 //
 // One CTA of 448 threads per (b, h), the forward kernel's roles:
 //   state warpgroup (warps 0-3): dS^T -> bf16 hi/lo operand (and dS' to HBM), G^T -> hi/lo,
@@ -77,6 +78,7 @@ struct BtParams {
     const float *dST;                            // [B, H, 128, 128] or nullptr (zero)
     float *dse;                                  // [B, H, nchunks, 128, 128]: dS' of every chunk
     float *dS0;                                  // [B, H, 128, 128] or nullptr
+    float *g_out, *dr_out;                       // [B, T, H, 128] fp32: G and dR (= dv) of every token
     int *status;
     int B, T, H;
     int euler;
@@ -109,30 +111,39 @@ __global__ void __launch_bounds__(256) split_do_kernel(const float4 *__restrict_
     }
 }
 
-// A 64-column fp32 block of TMEM at lane_base + src (tokens 0-31, 32-63), negated or not, as
-// bf16 hi (columns 0-31) and lo (columns 32-63) at lane_base + TM_X.  Both halves are in
-// registers before anything is written (src may be TM_X).
-template <bool NEGATE>
-__device__ __forceinline__ void split64(uint32_t lane_base, uint32_t src) {
-    float x0[32], x1[32];
+// A 64-column fp32 block of TMEM at lane_base + src (tokens 0-31 into x0, 32-63 into x1),
+// times `sign`, as bf16 hi (columns 0-31) and lo (columns 32-63) at lane_base + TM_X.  Both
+// halves are in registers before anything is written (src may be TM_X); x0 and x1 keep the
+// values (before the sign) for the caller.
+__device__ __forceinline__ void split64(uint32_t lane_base, uint32_t src, float sign, float (&x0)[32], float (&x1)[32]) {
     tmem_ld32(lane_base + src, x0);
     tmem_ld32(lane_base + src + 32, x1);
     tmem_ld_wait();
     uint32_t hi[16], lo[16];
-    if (NEGATE) {
+    float y[32];
 #pragma unroll
-        for (int t = 0; t < 32; ++t) {
-            x0[t] = -x0[t];
-            x1[t] = -x1[t];
-        }
-    }
-    split_pack<16>(x0, hi, lo);
+    for (int t = 0; t < 32; ++t) y[t] = sign * x0[t];
+    split_pack<16>(y, hi, lo);
     tmem_st16u(lane_base + TM_X, hi);
     tmem_st16u(lane_base + TM_X + 32, lo);
-    split_pack<16>(x1, hi, lo);
+#pragma unroll
+    for (int t = 0; t < 32; ++t) y[t] = sign * x1[t];
+    split_pack<16>(y, hi, lo);
     tmem_st16u(lane_base + TM_X + 16, hi);
     tmem_st16u(lane_base + TM_X + 48, lo);
     tmem_st_wait();
+}
+
+// Column j of a chunk's [64 tokens][128] block of a [B, T, H, 128] fp32 tensor from registers
+// (tokens past `valid` not written); consecutive threads write consecutive columns.
+__device__ __forceinline__ void store_cols(float *base, size_t row_stride, int valid, const float (&x0)[32],
+                                           const float (&x1)[32]) {
+#pragma unroll
+    for (int t = 0; t < 32; ++t)
+        if (t < valid) base[(size_t)t * row_stride] = x0[t];
+#pragma unroll
+    for (int t = 0; t < 32; ++t)
+        if (32 + t < valid) base[(size_t)(32 + t) * row_stride] = x1[t];
 }
 
 __global__ void __launch_bounds__(448, 1) bwd_tc_kernel(const __grid_constant__ BtParams p) {
@@ -320,16 +331,13 @@ __global__ void __launch_bounds__(448, 1) bwd_tc_kernel(const __grid_constant__ 
             if (it > 0) ok = wait_bar_warp(&bars->s_done, (it - 1) & 1, abort_flag, wait_ns);
             if (!ok) break;
             tc_fence_after();
-            // dS' of this chunk (the gradient of its end state) to HBM, and dS^T -> bf16 hi/lo operand
-            float *dst = p.dse + ((size_t)blockIdx.x * nchunks + chunk_of(it)) * D * D + j;
+            // dS^T -> bf16 hi/lo operand
 #pragma unroll 1
             for (int g = 0; g < 4; g = opaque(g + 1)) {
                 float sv[32];
                 uint32_t hi[16], lo[16];
                 tmem_ld32(lane_base + TM_S + g * 32, sv);
                 tmem_ld_wait();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) dst[(size_t)(g * 32 + i) * D] = sv[i];
                 split_pack<16>(sv, hi, lo);
                 tmem_st16u(lane_base + TM_SA + g * 16, hi);
                 tmem_st16u(lane_base + TM_SA + 64 + g * 16, lo);
@@ -337,18 +345,36 @@ __global__ void __launch_bounds__(448, 1) bwd_tc_kernel(const __grid_constant__ 
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(&bars->sa_ready);
+            {  // dS' of this chunk (the gradient of its end state) to HBM while the tensor core forms
+               // G^T; TM_S changes again only after r_ready, which this warpgroup arrives at later
+                float *dst = p.dse + ((size_t)blockIdx.x * nchunks + chunk_of(it)) * D * D + j;
+#pragma unroll 1
+                for (int g = 0; g < 4; g = opaque(g + 1)) {
+                    float sv[32];
+                    tmem_ld32(lane_base + TM_S + g * 32, sv);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) dst[(size_t)(g * 32 + i) * D] = sv[i];
+                }
+            }
             ok = wait_bar_warp(&bars->x_done, it & 1, abort_flag, wait_ns);
             if (!ok) break;
             tc_fence_after();
-            split64<false>(lane_base, TM_X);  // G^T
+            const int c = chunk_of(it), valid = min(C, p.T - c * C);
+            const size_t row0 = ((size_t)b * p.T + (size_t)c * C) * p.H + h;
+            float x0[32], x1[32];
+            split64(lane_base, TM_X, 1.f, x0, x1);  // G^T
             tc_fence_before();
             mbar_arrive(&bars->r_ready);
+            // G for the per-chunk gradient kernel, sent while the tensor core forms dR
+            store_cols(p.g_out + row0 * D + j, (size_t)p.H * D, valid, x0, x1);
             ok = wait_bar_warp(&bars->u_done, it & 1, abort_flag, wait_ns);
             if (!ok) break;
             tc_fence_after();
-            split64<true>(lane_base, TM_SA);  // -dR^T
+            split64(lane_base, TM_SA, -1.f, x0, x1);  // -dR^T
             tc_fence_before();
             mbar_arrive(&bars->u_ready);
+            store_cols(p.dr_out + row0 * D + j, (size_t)p.H * D, valid, x0, x1);  // dv = dR
         }
         if (ok) {  // dS0: the gradient of the first chunk's start state
             ok = wait_bar_warp(&bars->s_done, (nchunks - 1) & 1, abort_flag, wait_ns);
@@ -460,15 +486,6 @@ __global__ void __launch_bounds__(448, 1) bwd_tc_kernel(const __grid_constant__ 
                 }
                 mma_commit_e(&bars->x_done);
             }
-            {  // dS^T += dO^T Q (off the chain: the state warpgroup has read this chunk's dS')
-                const uint32_t idesc = idesc_bf16_f32(128, 128, 1, 1);
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {
-                    const uint64_t bq = smem_desc(kq_s + 8192 + ks * 2048, 16384, 1024);
-                    mma_bf16_e(tmem + TM_S, smem_desc(doh + ks * 2048, 8192, 1024), bq, idesc, 1);
-                    mma_bf16_e(tmem + TM_S, smem_desc(dol + ks * 2048, 8192, 1024), bq, idesc, 1);
-                }
-            }
             if (!(ok = wait_bar_warp(&bars->r_ready, it & 1, abort_flag, wait_ns))) break;
             tc_fence_after();
             {  // dR^T = G^T T'' (T'' read as an MN-major operand, K = s), into TM_SA
@@ -482,6 +499,16 @@ __global__ void __launch_bounds__(448, 1) bwd_tc_kernel(const __grid_constant__ 
                 }
                 mma_commit_e(&bars->u_done);
                 mma_commit_e(&bars->tpp_free[buf]);
+            }
+            {  // dS^T += dO^T Q (after r_ready, so after the state warpgroup has sent this chunk's dS';
+               // behind dR in the pipe, off the chain)
+                const uint32_t idesc = idesc_bf16_f32(128, 128, 1, 1);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                    const uint64_t bq = smem_desc(kq_s + 8192 + ks * 2048, 16384, 1024);
+                    mma_bf16_e(tmem + TM_S, smem_desc(doh + ks * 2048, 8192, 1024), bq, idesc, 1);
+                    mma_bf16_e(tmem + TM_S, smem_desc(dol + ks * 2048, 8192, 1024), bq, idesc, 1);
+                }
             }
             issue_grams(it + 2, false);
             if (!(ok = wait_bar_warp(&bars->u_ready, it & 1, abort_flag, wait_ns))) break;
@@ -543,8 +570,9 @@ bool bt_map(CUtensorMap *m, const void *ptr, int B, int T, int H) {
 }  // namespace
 
 // State gradients of the chunked backward on the tensor cores: bf16 q, k, d_k = d_v = 128,
-// T > 0.  do_split: 2 x B*T*H*128 bf16 of scratch (dO hi, then lo).
-cudaError_t launch_bwd_state_tc(const BwdArgs &a, float *dse, void *do_split, const char **why) {
+// T > 0.  do_split: 2 x B*T*H*128 bf16 of scratch (dO hi, then lo); g_out: B*T*H*128 fp32
+// (G of every token); dv receives dR.
+cudaError_t launch_bwd_state_tc(const BwdArgs &a, float *dse, void *do_split, float *g_out, const char **why) {
     const size_t n = (size_t)a.B * a.T * a.H * D;
     __nv_bfloat16 *hi = static_cast<__nv_bfloat16 *>(do_split), *lo = hi + n;
     int dev = 0, sms = 0;
@@ -573,6 +601,8 @@ cudaError_t launch_bwd_state_tc(const BwdArgs &a, float *dse, void *do_split, co
     p.dST = a.dST;
     p.dse = dse;
     p.dS0 = a.dS0;
+    p.g_out = g_out;
+    p.dr_out = a.dv;
     p.status = device_status_ptr();
     p.B = a.B;
     p.T = a.T;

@@ -85,13 +85,14 @@ struct BwdArgs {
 };
 cudaError_t launch_bwd(const BwdArgs &a);
 // Chunked backward (bwd_chunk.cu), chunk 64, rows of [B, T]: the state gradients at the ends of
-// the chunks (unless state_pass is false: dse already holds them), then every chunk's gradients
-// in parallel from `states` (the forward's chunk-start states, filled first by a forward launch
-// with FwdArgs::states).  dse: [B, H, nchunks, dk, dv].
-cudaError_t launch_bwd_chunked(const BwdArgs &a, const float *states, float *dse, bool state_pass = true);
+// the chunks, then every chunk's gradients in parallel from `states` (the forward's chunk-start
+// states, filled first by a forward launch with FwdArgs::states).  dse: [B, H, nchunks, dk, dv].
+// With g_in, the tensor-core state pass has already filled dse, G (g_in) and dv.
+cudaError_t launch_bwd_chunked(const BwdArgs &a, const float *states, float *dse, const float *g_in = nullptr);
 // The same state pass on the tensor cores (bwd_tc.cu): bf16 q, k, d_k = d_v = 128, T > 0;
-// do_split is scratch for dO as bf16 hi and lo (2 x B*T*H*128 bf16).
-cudaError_t launch_bwd_state_tc(const BwdArgs &a, float *dse, void *do_split, const char **why);
+// do_split is scratch for dO as bf16 hi and lo (2 x B*T*H*128 bf16); it also writes G of every
+// token into g_out (B*T*H*128 fp32) and dR into dv, for launch_bwd_chunked with g_in = g_out.
+cudaError_t launch_bwd_state_tc(const BwdArgs &a, float *dse, void *do_split, float *g_out, const char **why);
 
 // Start states of the segments of split sequences from the segment maps (scan.cu).
 cudaError_t launch_scan_combine(const float *S0, const float *maps, float *s_in, int B, int G, int H,

@@ -240,7 +240,7 @@ efla_status efla_bwd_recurrent(const void *q, const void *k, const void *v, cons
  *
  *   workspace  device scratch owned by the caller, 16-byte aligned, at least the size
  *              efla_bwd_workspace reports (2 x B x H x ceil(T/64) x d_k x d_v x 4 bytes
- *              + 2 x B x T x H x d_v x 2 bytes);
+ *              + B x T x H x d_v x 8 bytes);
  *              it must not overlap any argument.  Too small or NULL: EFLA_ERR_INVALID_ARG.
  * Supported: d_k = d_v in {64, 128} (other sizes: EFLA_ERR_UNSUPPORTED, use
  * efla_bwd_recurrent).

@@ -297,7 +297,7 @@ def _bwc(lib, ws=0xA0000000, ws_bytes=None, **kw):
     f.restype = ip
     f.argtypes = [vp] * 12 + [ip] * 7 + [vp, ctypes.c_size_t, vp]
     need = 2 * a["B"] * a["H"] * ((max(a["T"], 0) + 63) // 64) * a["dk_"] * a["dv_"] * 4 + \
-        2 * a["B"] * max(a["T"], 0) * a["H"] * a["dv_"] * 2
+        2 * a["B"] * max(a["T"], 0) * a["H"] * a["dv_"] * 2 + a["B"] * max(a["T"], 0) * a["H"] * a["dv_"] * 4
     return f(a["q"], a["k"], a["v"], a["beta"], a["S0"], a["dO"], a["dST"], a["dq"], a["dk"], a["dv"], a["db"],
              a["dS0"], a["B"], a["T"], a["H"], a["dk_"], a["dv_"], a["ind"], a["upd"], ws,
              need if ws_bytes is None else ws_bytes, None)
@@ -322,8 +322,8 @@ def test_bwd_workspace_size(lib):
     f.argtypes = [ctypes.c_int] * 5 + [ctypes.POINTER(ctypes.c_size_t)]
     n = ctypes.c_size_t(0)
     assert f(8, 2048, 16, 128, 128, ctypes.byref(n)) == 0
-    assert n.value == 2 * 8 * 16 * 32 * 128 * 128 * 4 + 2 * 8 * 2048 * 16 * 128 * 2
-    assert f(1, 65, 1, 64, 64, ctypes.byref(n)) == 0 and n.value == 2 * 2 * 64 * 64 * 4 + 2 * 65 * 64 * 2
+    assert n.value == 2 * 8 * 16 * 32 * 128 * 128 * 4 + 2 * 8 * 2048 * 16 * 128 * 2 + 8 * 2048 * 16 * 128 * 4
+    assert f(1, 65, 1, 64, 64, ctypes.byref(n)) == 0 and n.value == 2 * 2 * 64 * 64 * 4 + 2 * 65 * 64 * 2 + 65 * 64 * 4
     assert f(1, 64, 1, 32, 32, ctypes.byref(n)) == UNSUPPORTED
     assert f(1, 64, 1, 128, 128, None) == INVALID
 
