@@ -508,10 +508,10 @@ def bwd_figure(efla, dev, stream, q, k, v, beta, flush, peaks, steps=3):
             "ms_per_call": 1e3 * t, "tokens_per_s": B * T / t, "algorithmic_bytes": nbytes,
             "GB/s": nbytes / t / 1e9, "frac_hbm": nbytes / t / 1e9 / peaks["hbm_gbs"],
             "workspace_bytes": ws_bytes,
-            "path": "forward on the tensor cores writing every chunk-start state (workspace), reverse pass over "
-                    "chunks for the end-state gradients (one CTA per (b, h)), per-chunk gradients (one CTA per "
-                    "(b, h, chunk)), fp32 on CUDA cores",
-            "ms_recurrent": 1e3 * t_rec, "gpu_launches": 3 * steps + 1}
+            "path": "forward on the tensor cores writing every chunk-start state (workspace); reverse pass over "
+                    "chunks for the end-state gradients on the tensor cores (one CTA per (b, h)), also writing G "
+                    "and dv; per-chunk gradients (one CTA per (b, h, chunk)) fp32 on CUDA cores",
+            "ms_recurrent": 1e3 * t_rec, "gpu_launches": 4 * steps + 1}
 
 
 def stiff_figure(efla, dev, stream, steps, flush, peaks):
