@@ -93,6 +93,23 @@ def test_bwd_zero_keys_and_zero_steps(efla, kind):
     _check(efla, c, kind=kind)
 
 
+def test_bwd_chunked_tensor_core_path_zero_keys_zero_steps_and_euler(efla):
+    """bf16 with d = 128 takes the tensor-core state pass and the gradient kernel's hand-over
+    of G and dR: zero keys, beta = 0, the gate derivative's series branch, a ragged tail and
+    the delta-rule gate, against the oracle."""
+    c = _case("bf16", 1, 150, 2, 128, 128, seed=8)
+    k = c["k"].clone()
+    k[:, 3::7] = 0
+    c["k"] = k.contiguous()
+    c["beta"][:, 5::6] = 0
+    c["beta"][:, 2::9] = 1e-4
+    _check(efla, c, kind="chunked")
+    e = _case("bf16", 2, 100, 2, 128, 128, seed=9)
+    e["k"] = torch.nn.functional.normalize(e["k"].float(), dim=-1).to(torch.bfloat16).contiguous()
+    _check(efla, e, update="euler", kind="chunked")
+    assert efla.device_status() == 0
+
+
 @pytest.mark.parametrize("kind", KINDS)
 def test_bwd_delta_rule_gate(efla, kind):
     c = _case("f32", 2, 150, 2, 64, 64, seed=7)
