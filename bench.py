@@ -510,7 +510,7 @@ def bwd_figure(efla, dev, stream, q, k, v, beta, flush, peaks, steps=3):
             "workspace_bytes": ws_bytes,
             "path": "forward on the tensor cores writing every chunk-start state (workspace); reverse pass over "
                     "chunks for the end-state gradients on the tensor cores (one CTA per (b, h)), also writing G "
-                    "and dv; per-chunk gradients (one CTA per (b, h, chunk)) fp32 on CUDA cores",
+                    "and dv; per-chunk gradients (one CTA per (b, h, chunk)) on the tensor cores",
             "ms_recurrent": 1e3 * t_rec, "gpu_launches": 4 * steps + 1}
 
 

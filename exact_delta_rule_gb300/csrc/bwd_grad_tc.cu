@@ -1,0 +1,587 @@
+// Per-chunk gradients of the chunked backward on the sm_103a tensor cores (tcgen05 + TMEM):
+// bf16 q, k, v with d_k = d_v = 128, chunks of 64, after the tensor-core state pass.
+//
+// Reverse mode of the chunkwise forward ["Error-Free Linear Attention is a Free Lunch"
+// (howistudyai), Step 4; "Exact Flow Linear Attention" (gist.science), Metodologia 3].  For a
+// chunk with start state S, end-state gradient dS', and G, dR (= dv) from the state pass, with
+// L = strictly-lower(K K^T) and T'' = T diag(alpha) the forward's:
+//   R  = V - K S,  U = T'' R
+//   dY = G - L^T dR,  Z = R - L U,  dalpha_t = sum_j dY[t][j] Z[t][j]
+//   dP = (dO U^T) o M_incl,  dL = -strictly-lower(dR U^T)
+//   dq = dO S^T + dP K
+//   dk = -dR S^T + U dS'^T + dP^T Q + (dL + dL^T) K + 2 dalpha (dalpha/dlambda) k
+//   dbeta = dalpha (dalpha/dbeta)
+// All products run on the tensor core in the transposed orientation (TMEM lane = feature),
+// every operand that is not an exact bf16 input split into bf16 hi + lo (fp32 accumulation):
+//   P0  Gram K K^T (TMEM); gate terms, A~, blocked inverse; T'' and -L as bf16 hi/lo tiles
+//   P1  X^T = S^T K^T;  [dQ^T | dK^T] = S [dO; -dR]^T            (S: a swizzled bf16 tile)
+//   P2  R^T = V^T - X^T (TMEM);  U^T = R^T T''^T
+//   P3  Z^T = R^T + U^T (-L)^T;  dY^T = G^T + dR^T (-L)
+//       [dP; -dR U^T] = [dO; -dR] U^T;  dK^T += dS' U^T          (dS': the same tile, reloaded)
+//   P4  dalpha (lane reduction of dY^T o Z^T); dP and dL + dL^T as bf16 hi/lo tiles
+//   P5  dQ^T += K^T dP^T;  dK^T += Q^T dP + K^T (dL + dL^T)
+//   P6  dq, dk (+ 2 dalpha dalpha/dlambda k), dbeta to HBM
+// One CTA of 256 threads per (b, h, chunk); thread 0 issues the products, all threads take
+// part in every other step, the two warpgroups each on half of a chunk's 64 tokens.  Every
+// wait is bounded; on expiry the CTA records EFLA_ERR_DEVICE_TIMEOUT and leaves.
+#include <cudaTypedefs.h>
+
+#include "internal.cuh"
+#include "ptx.cuh"
+#include "tc_common.cuh"
+#include "tri_inverse.cuh"
+
+namespace efla {
+namespace {
+using namespace ptx;
+using namespace tc;
+
+constexpr int C = 64;
+constexpr int D = 128;
+constexpr int NT = 256;
+
+// Shared memory map (bytes from a 1024-byte aligned base).  Operand tiles are bf16 with the
+// 128-byte swizzle in column blocks of 64 elements; "hi | lo" pairs are the two split parts.
+constexpr uint32_t OFF_KQ = 0;        // [K; Q]: 2 column blocks x 128 rows (K 0-63, Q 64-127), 32 KB
+constexpr uint32_t OFF_DOR = 32768;   // [dO; -dR] hi | lo: 2 column blocks x 128 rows each, 64 KB
+constexpr uint32_t OFF_SS = 98304;    // S, later dS', hi | lo: 2 column blocks x 128 rows each, 64 KB
+constexpr uint32_t OFF_W = 163840;    // T'' hi | lo [64][64] (16 KB); later dP hi | lo
+constexpr uint32_t OFF_L = 180224;    // -L hi | lo [64][64] (16 KB); later dL + dL^T hi | lo
+constexpr uint32_t OFF_UT = 196608;   // U^T hi | lo [128][64] (32 KB); before: fp32 A~ [64][68]; after: fp32 dL [64][65]
+constexpr uint32_t OFF_ROW = 229376;  // fp32 per token: beta, invn, gn, alpha, dadb, dadl, dalpha
+constexpr uint32_t OFF_BAR = OFF_ROW + 7 * C * 4;
+constexpr uint32_t OFF_MISC = OFF_BAR + 64;  // tmem base, abort flag
+constexpr uint32_t SMEM_USED = OFF_MISC + 16;
+constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;
+constexpr int AT_LD = 68;
+constexpr int DL_LD = 65;
+constexpr uint32_t LO_128 = 32768;  // lo part after hi in the 128 x 128 tiles
+constexpr uint32_t LO_UT = 16384;   // ... in the U^T tile
+constexpr uint32_t LO_64 = 8192;    // ... in the 64 x 64 tiles
+static_assert(OFF_DOR % 1024 == 0 && OFF_SS % 1024 == 0 && OFF_W % 1024 == 0 && OFF_L % 1024 == 0 &&
+                  OFF_UT % 1024 == 0,
+              "operand tiles must be 1024-byte aligned");
+static_assert(OFF_DOR == OFF_KQ + 32768 && OFF_SS == OFF_DOR + 2 * LO_128 && OFF_W == OFF_SS + 2 * LO_128 &&
+                  OFF_L == OFF_W + 2 * LO_64 && OFF_UT == OFF_L + 2 * LO_64 && OFF_ROW == OFF_UT + 2 * LO_UT,
+              "regions overlap");
+static_assert(C * AT_LD * 4 <= 2 * LO_UT && C * DL_LD * 4 <= 2 * LO_UT, "fp32 scratch exceeds the U^T region");
+static_assert(SMEM_ALLOC <= 232448, "exceeds the per-CTA shared memory limit");
+
+// TMEM columns (fp32 unless split: bf16 pairs, hi in the first 32 columns, lo in the next 32)
+constexpr uint32_t TM_P = 0;     // [dP; -dR U^T] (64)
+constexpr uint32_t TM_X = 128;   // X^T -> R^T -> Z^T (64)
+constexpr uint32_t TM_RS = 192;  // R^T split, later dR^T split (64)
+constexpr uint32_t TM_U = 256;   // Gram -> U^T -> G^T -> dY^T (64)
+constexpr uint32_t TM_US = 320;  // U^T split (64)
+constexpr uint32_t TM_DQ = 384;  // dQ^T (64)
+constexpr uint32_t TM_DK = 448;  // dK^T (64), adjacent to dQ^T: one N = 128 product fills both
+constexpr uint32_t TM_COLS = 512;
+
+constexpr uint64_t DRAIN_NS = 2000000000ull;
+
+struct GtParams {
+    CUtensorMap map_q, map_k, map_doh, map_dol;  // [B, T, H, 128] bf16: box 64 x 1 x 64 x 1, 128B swizzle
+    const __nv_bfloat16 *v;                      // [B, T, H, 128]
+    const float *beta;                           // [B, T, H]
+    const float *states, *dse;                   // [B, H, nchunks, 128, 128]: S and dS' of every chunk
+    const float *g, *dr;                         // [B, T, H, 128]: G and dR (= dv) of every token
+    float *dq, *dk, *dbeta;
+    int *status;
+    int T, H;
+    int euler;
+    unsigned long long wait_ns;
+};
+
+struct Bars {
+    uint64_t tma, g, m, a, b, drain;
+};
+static_assert(sizeof(Bars) <= 64, "mbarrier block exceeds its slot");
+
+// x[0..15] as bf16 hi and lo of row `row`, columns col0 .. col0 + 15 (col0 + 15 < 64) of a
+// swizzled tile (hi at `tile`, lo at tile + lo_off).
+__device__ __forceinline__ void put16(uint8_t *tile, uint32_t lo_off, int row, int col0, const float *x) {
+    uint32_t hh[8], ll[8];
+    split_pack<8>(x, hh, ll);
+#pragma unroll
+    for (int h8 = 0; h8 < 2; ++h8) {
+        const uint32_t off = swz_offset(row, col0 + 8 * h8, 0);
+        *reinterpret_cast<uint4 *>(tile + off) = make_uint4(hh[4 * h8], hh[4 * h8 + 1], hh[4 * h8 + 2], hh[4 * h8 + 3]);
+        *reinterpret_cast<uint4 *>(tile + lo_off + off) =
+            make_uint4(ll[4 * h8], ll[4 * h8 + 1], ll[4 * h8 + 2], ll[4 * h8 + 3]);
+    }
+}
+
+// Four fp32 values as bf16 hi and lo at (row, col .. col + 3) of a swizzled 128-row tile with
+// two column blocks (col a multiple of 4).
+__device__ __forceinline__ void put4(uint8_t *tile, uint32_t lo_off, int row, int col, float4 v) {
+    const float x[4] = {v.x, v.y, v.z, v.w};
+    uint32_t hh[2], ll[2];
+    split_pack<2>(x, hh, ll);
+    const uint32_t off = swz_offset(row, col, 16384);
+    *reinterpret_cast<uint2 *>(tile + off) = make_uint2(hh[0], hh[1]);
+    *reinterpret_cast<uint2 *>(tile + lo_off + off) = make_uint2(ll[0], ll[1]);
+}
+
+// 32 fp32 values (this warpgroup's 32 tokens) as a TMEM A operand: bf16 pairs, hi at
+// base + 16 h, lo at base + 32 + 16 h.
+__device__ __forceinline__ void tsplit32(uint32_t lane_base, uint32_t base, int h, const float (&x)[32]) {
+    uint32_t hh[16], ll[16];
+    split_pack<16>(x, hh, ll);
+    tmem_st16u(lane_base + base + 16 * h, hh);
+    tmem_st16u(lane_base + base + 32 + 16 * h, ll);
+}
+
+// Sum over the 32 lanes of a warp of x[0..31]: lane l returns the sum of x[l] (reduce-scatter
+// by halving, 31 shuffles).
+__device__ __forceinline__ float lane_reduce_scatter(float (&x)[32], int lane) {
+#pragma unroll
+    for (int w = 16; w >= 1; w >>= 1) {
+        const bool up = (lane & w) != 0;
+#pragma unroll
+        for (int i = 0; i < w; ++i) {
+            const float send = up ? x[i] : x[i + w];
+            const float keep = up ? x[i + w] : x[i];
+            x[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+        }
+    }
+    return x[0];
+}
+
+__global__ void __launch_bounds__(NT, 1) bwd_grad_tc_kernel(const __grid_constant__ GtParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float *row_beta = reinterpret_cast<float *>(sm + OFF_ROW), *row_invn = row_beta + C, *row_gn = row_invn + C;
+    float *row_al = row_gn + C, *row_dadb = row_al + C, *row_dadl = row_dadb + C, *row_dal = row_dadl + C;
+    float *At = reinterpret_cast<float *>(sm + OFF_UT);   // A~, then T~ (P0)
+    float *dLs = reinterpret_cast<float *>(sm + OFF_UT);  // dL (P4)
+    Bars *bars = reinterpret_cast<Bars *>(sm + OFF_BAR);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + OFF_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + OFF_MISC + 4);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int nc = (p.T + C - 1) / C;
+    const int unit = blockIdx.x / nc, c = blockIdx.x % nc;
+    const int b = unit / p.H, h = unit % p.H;
+    const int t0 = c * C, valid = min(C, p.T - t0);
+    const size_t row0 = ((size_t)b * p.T + (size_t)t0) * p.H + h;  // token t of the chunk: row0 + t H
+    const uint64_t wait_ns = p.wait_ns;
+    // TMEM: this thread reads and writes lane `ln` (its warp's quarter), columns of token half `hf`
+    const int hf = warp >> 2, ln = (warp & 3) * 32 + lane;
+    const uint32_t s_sm = smem_u32(sm);
+
+    if (tid == 0) {
+        mbar_init(&bars->tma, 1);
+        mbar_init(&bars->g, 1);
+        mbar_init(&bars->m, 1);
+        mbar_init(&bars->a, 1);
+        mbar_init(&bars->b, 1);
+        mbar_init(&bars->drain, 1);
+        fence_mbar_init();
+        *abort_flag = 0;
+    }
+    if (warp == 0) {
+        tmem_alloc(tmem_slot, TM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    int m_uses = 0;
+    bool ok = true;
+    // every thread waits (bounded) on `bar`; one outcome for the CTA
+    auto wait_all = [&](uint64_t *bar, int parity) {
+        const bool mine = ok && wait_bar(bar, parity, abort_flag, wait_ns);
+        ok = __syncthreads_and(mine) != 0;
+        tc_fence_after();
+    };
+    // thread 0 commits the products issued so far to bars->m; everyone waits for them
+    auto sync_m = [&]() {
+        if (tid == 0) mma_commit(&bars->m);
+        wait_all(&bars->m, m_uses & 1);
+        ++m_uses;
+    };
+
+    // ------------------------------ loads ------------------------------
+    if (tid == 0) {
+        prefetch_tensormap(&p.map_q);
+        prefetch_tensormap(&p.map_k);
+        prefetch_tensormap(&p.map_doh);
+        prefetch_tensormap(&p.map_dol);
+        mbar_arrive_expect_tx(&bars->tma, 4 * 16384);
+        for (int cb = 0; cb < 2; ++cb) {
+            tma_load_4d(sm + OFF_KQ + cb * 16384, &p.map_k, &bars->tma, cb * 64, h, t0, b);
+            tma_load_4d(sm + OFF_KQ + cb * 16384 + 8192, &p.map_q, &bars->tma, cb * 64, h, t0, b);
+            tma_load_4d(sm + OFF_DOR + cb * 16384, &p.map_doh, &bars->tma, cb * 64, h, t0, b);
+            tma_load_4d(sm + OFF_DOR + LO_128 + cb * 16384, &p.map_dol, &bars->tma, cb * 64, h, t0, b);
+        }
+    }
+    // V^T of this thread's lane j = ln and token half, kept for P2
+    float vt[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+        const int t = 32 * hf + e;
+        vt[e] = t < valid ? __bfloat162float(p.v[(row0 + (size_t)t * p.H) * D + ln]) : 0.f;
+    }
+    {  // S -> bf16 hi/lo tile (row i, column j); a warp reads one 512-byte row per load
+        const float4 *src = reinterpret_cast<const float4 *>(p.states + (size_t)blockIdx.x * D * D);
+        float4 x[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) x[e] = __ldg(src + e * NT + tid);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) put4(sm + OFF_SS, LO_128, e * 8 + warp, lane * 4, x[e]);
+    }
+    {  // -dR -> rows 64-127 of the [dO; -dR] tile
+        const int jc = lane * 4;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int t = e * 8 + warp;
+            float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (t < valid) x = __ldg(reinterpret_cast<const float4 *>(p.dr + (row0 + (size_t)t * p.H) * D + jc));
+            put4(sm + OFF_DOR, LO_128, C + t, jc, make_float4(-x.x, -x.y, -x.z, -x.w));
+        }
+    }
+    if (tid < C) {
+        row_beta[tid] = tid < valid ? p.beta[row0 + (size_t)tid * p.H] : 0.f;
+        row_dal[tid] = 0.f;
+    }
+    fence_proxy_async_smem();
+    wait_all(&bars->tma, 0);
+
+    do {
+        if (!ok) break;
+        // ------------------------------ P0 / P1 products ------------------------------
+        if (tid == 0) {
+            const uint32_t kq = s_sm + OFF_KQ, ss = s_sm + OFF_SS, dor = s_sm + OFF_DOR;
+            // Gram K K^T (rows 64-127 of the M = 128 product are Q K^T, unused)
+            {
+                const uint32_t idesc = idesc_bf16_f32(128, 64, 0, 0);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+                    mma_bf16(tmem + TM_U, smem_desc(kq + off, 16, 1024), smem_desc(kq + off, 16, 1024), idesc, ks > 0);
+                }
+                mma_commit(&bars->g);
+            }
+            {  // X^T = S^T K^T: S^T read as an MN-major A (M = j), K = i
+                const uint32_t idesc = idesc_bf16_f32(128, 64, 1, 0);
+#pragma unroll
+                for (int part = 0; part < 2; ++part)
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint32_t boff = (ks >> 2) * 16384 + (ks & 3) * 32;
+                        mma_bf16(tmem + TM_X, smem_desc(ss + part * LO_128 + ks * 2048, 16384, 1024),
+                                 smem_desc(kq + boff, 16, 1024), idesc, (part | ks) != 0);
+                    }
+            }
+            {  // [dQ^T | dK^T] = S [dO; -dR]^T: one N = 128 product, K = j
+                const uint32_t idesc = idesc_bf16_f32(128, 128, 0, 0);
+#pragma unroll
+                for (int pr = 0; pr < 3; ++pr) {  // S hi x hi, S hi x lo, S lo x hi
+                    const uint32_t a_lo = pr == 2 ? LO_128 : 0, b_lo = pr == 1 ? LO_128 : 0;
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+                        mma_bf16(tmem + TM_DQ, smem_desc(ss + a_lo + off, 16, 1024), smem_desc(dor + b_lo + off, 16, 1024),
+                                 idesc, (pr | ks) != 0);
+                    }
+                }
+            }
+            mma_commit(&bars->m);
+        }
+        // ------------------------------ P0: gate terms, -L, T'' ------------------------------
+        wait_all(&bars->g, 0);
+        if (!ok) break;
+        if (ln < C) {  // row t = ln of K K^T, this half's 32 columns (warps 0, 1, 4, 5)
+            const int t = ln, col0 = 32 * hf;
+            float g[32];
+            tmem_ld32(lane_base + TM_U + col0, g);
+            tmem_ld_wait();
+            if ((t >> 5) == hf) {  // the diagonal element is in this half: gate terms of row t
+                float lam = 0.f;
+#pragma unroll
+                for (int s = 0; s < 32; ++s) lam = (s == (t & 31)) ? g[s] : lam;
+                const float bt = row_beta[t];
+                const bool live = t < valid && lam > 0.f;
+                const float in = live ? rsqrtf(lam) : 0.f;
+                const float gam = !live ? 0.f : p.euler ? bt * lam : -expm1f(-bt * lam);
+                float db = 0.f, dl = 0.f;
+                if (t < valid) gate_grad(bt, lam, p.euler, db, dl);
+                row_invn[t] = in;
+                row_gn[t] = gam * in;
+                row_al[t] = t < valid ? efla_alpha(bt, lam, p.euler) : 0.f;
+                row_dadb[t] = db;
+                row_dadl[t] = dl;
+            }
+            float x[32];
+#pragma unroll
+            for (int s = 0; s < 32; ++s) x[s] = col0 + s < t ? -g[s] : 0.f;  // -L
+            put16(sm + OFF_L, LO_64, t, col0, x);
+            put16(sm + OFF_L, LO_64, t, col0 + 16, x + 16);
+#pragma unroll
+            for (int s = 0; s < 32; s += 4)
+                *reinterpret_cast<float4 *>(At + t * AT_LD + col0 + s) = make_float4(g[s], g[s + 1], g[s + 2], g[s + 3]);
+        }
+        __syncthreads();
+        for (int e = tid; e < C * C; e += NT) {  // A~ = strictly-lower(gamma_t k^_t . k^_s), in place
+            const int t = e / C, s = e % C;
+            At[t * AT_LD + s] = s < t ? row_gn[t] * At[t * AT_LD + s] * row_invn[s] : 0.f;
+        }
+        __syncthreads();
+        invert_unit_lower<1, AT_LD>(At, tid);  // T~; ends with a barrier over all 256 threads
+        {  // T'' = diag(1/n) T~ diag(gamma/n); a zero key's row keeps u_t = alpha_t r_t
+            const int t = tid >> 2, s0 = (tid & 3) * 16;
+            float x[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const int s = s0 + e;
+                x[e] = s < t    ? row_invn[t] * At[t * AT_LD + s] * row_gn[s]
+                       : s == t ? (row_invn[t] > 0.f ? row_gn[t] * row_invn[t] : row_al[t])
+                                : 0.f;
+            }
+            put16(sm + OFF_W, LO_64, t, s0, x);
+        }
+        // ------------------------------ P2: R^T, U^T ------------------------------
+        wait_all(&bars->m, 0);  // X^T and S [dO; -dR]^T complete: the S tile is free again
+        m_uses = 1;
+        if (!ok) break;
+        float gt[32], drt[32];  // G^T and dR^T of this lane and token half, for P3
+        {
+            const float4 *src = reinterpret_cast<const float4 *>(p.dse + (size_t)blockIdx.x * D * D);
+            float4 x[16];  // dS', in flight while R^T is formed
+#pragma unroll
+            for (int e = 0; e < 16; ++e) x[e] = __ldg(src + e * NT + tid);
+            float r[32];
+            tmem_ld32(lane_base + TM_X + 32 * hf, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) r[e] = vt[e] - r[e];
+            tmem_st32(lane_base + TM_X + 32 * hf, r);
+            tsplit32(lane_base, TM_RS, hf, r);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                const int t = 32 * hf + e;
+                const size_t o = (row0 + (size_t)t * p.H) * D + ln;
+                gt[e] = t < valid ? __ldg(p.g + o) : 0.f;
+                drt[e] = t < valid ? __ldg(p.dr + o) : 0.f;
+            }
+#pragma unroll
+            for (int e = 0; e < 16; ++e) put4(sm + OFF_SS, LO_128, e * 8 + warp, lane * 4, x[e]);
+        }
+        tmem_st_wait();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {  // U^T = R^T T''^T: A = R^T split (TMEM), B[t][s] = T''[t][s] (K-major)
+            tc_fence_after();
+            const uint32_t w = s_sm + OFF_W, idesc = idesc_bf16_f32(128, 64, 0, 0);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+                const uint64_t bh = smem_desc(w + ks * 32, 16, 1024), bl = smem_desc(w + LO_64 + ks * 32, 16, 1024);
+                mma_bf16_ts(tmem + TM_U, tmem + TM_RS + ks * 8, bh, idesc, ks > 0);
+                mma_bf16_ts(tmem + TM_U, tmem + TM_RS + ks * 8, bl, idesc, 1);
+                mma_bf16_ts(tmem + TM_U, tmem + TM_RS + 32 + ks * 8, bh, idesc, 1);
+            }
+        }
+        sync_m();
+        if (!ok) break;
+        // ------------------------------ P3 ------------------------------
+        {
+            float u[32];
+            tmem_ld32(lane_base + TM_U + 32 * hf, u);
+            tmem_ld_wait();
+            tsplit32(lane_base, TM_US, hf, u);
+            put16(sm + OFF_UT, LO_UT, ln, 32 * hf, u);
+            put16(sm + OFF_UT, LO_UT, ln, 32 * hf + 16, u + 16);
+            tmem_st32(lane_base + TM_U + 32 * hf, gt);  // G^T over U^T (read above)
+            tsplit32(lane_base, TM_RS, hf, drt);        // dR^T split over R^T's (its product is complete)
+        }
+        tmem_st_wait();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            tc_fence_after();
+            const uint32_t l = s_sm + OFF_L, ut = s_sm + OFF_UT, ss = s_sm + OFF_SS, dor = s_sm + OFF_DOR;
+            {  // Z^T += U^T (-L)^T: A = U^T split (TMEM), B[t][s] = -L[t][s] (K-major)
+                const uint32_t idesc = idesc_bf16_f32(128, 64, 0, 0);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                    const uint64_t bh = smem_desc(l + ks * 32, 16, 1024), bl = smem_desc(l + LO_64 + ks * 32, 16, 1024);
+                    mma_bf16_ts(tmem + TM_X, tmem + TM_US + ks * 8, bh, idesc, 1);
+                    mma_bf16_ts(tmem + TM_X, tmem + TM_US + ks * 8, bl, idesc, 1);
+                    mma_bf16_ts(tmem + TM_X, tmem + TM_US + 32 + ks * 8, bh, idesc, 1);
+                }
+            }
+            {  // dY^T += dR^T (-L): A = dR^T split (TMEM), B[t][s] = -L[s][t] (MN-major)
+                const uint32_t idesc = idesc_bf16_f32(128, 64, 0, 1);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                    const uint64_t bh = smem_desc(l + ks * 2048, 8192, 1024), bl = smem_desc(l + LO_64 + ks * 2048, 8192, 1024);
+                    mma_bf16_ts(tmem + TM_U, tmem + TM_RS + ks * 8, bh, idesc, 1);
+                    mma_bf16_ts(tmem + TM_U, tmem + TM_RS + ks * 8, bl, idesc, 1);
+                    mma_bf16_ts(tmem + TM_U, tmem + TM_RS + 32 + ks * 8, bh, idesc, 1);
+                }
+            }
+            mma_commit(&bars->a);
+            {  // [dP; -dR U^T] = [dO; -dR] U^T, and dK^T += dS' U^T: B[t][j] = U^T[j][t] (MN-major), K = j
+                const uint32_t idesc = idesc_bf16_f32(128, 64, 0, 1);
+#pragma unroll
+                for (int pr = 0; pr < 3; ++pr) {  // hi x hi, hi x lo, lo x hi
+                    const uint32_t a_lo = pr == 2 ? LO_128 : 0, b_lo = pr == 1 ? LO_UT : 0;
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint32_t aoff = a_lo + (ks >> 2) * 16384 + (ks & 3) * 32;
+                        const uint64_t bd = smem_desc(ut + b_lo + ks * 2048, 8192, 1024);
+                        mma_bf16(tmem + TM_P, smem_desc(dor + aoff, 16, 1024), bd, idesc, (pr | ks) != 0);
+                        mma_bf16(tmem + TM_DK, smem_desc(ss + aoff, 16, 1024), bd, idesc, 1);
+                    }
+                }
+            }
+            mma_commit(&bars->b);
+        }
+        // ------------------------------ P4 ------------------------------
+        wait_all(&bars->a, 0);
+        if (!ok) break;
+        {  // dalpha_t: sum over j of dY^T[j][t] Z^T[j][t]; this warp's 32 lanes, then across warps
+            float y[32], z[32];
+            tmem_ld32(lane_base + TM_U + 32 * hf, y);
+            tmem_ld32(lane_base + TM_X + 32 * hf, z);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) y[e] *= z[e];
+            atomicAdd(&row_dal[32 * hf + lane], lane_reduce_scatter(y, lane));
+        }
+        wait_all(&bars->b, 0);
+        if (!ok) break;
+        {
+            float x[32];
+            tmem_ld32(lane_base + TM_P + 32 * hf, x);
+            tmem_ld_wait();
+            if (ln < C) {  // dP = (dO U^T) o M_incl, row t
+                const int t = ln;
+#pragma unroll
+                for (int s = 0; s < 32; ++s) x[s] = 32 * hf + s <= t ? x[s] : 0.f;
+                put16(sm + OFF_W, LO_64, t, 32 * hf, x);
+                put16(sm + OFF_W, LO_64, t, 32 * hf + 16, x + 16);
+            } else {  // dL = strictly-lower(-dR U^T), row t
+                const int t = ln - C;
+#pragma unroll
+                for (int s = 0; s < 32; ++s) dLs[t * DL_LD + 32 * hf + s] = 32 * hf + s < t ? x[s] : 0.f;
+            }
+        }
+        __syncthreads();
+        {  // dL + dL^T
+            const int t = tid >> 2, s0 = (tid & 3) * 16;
+            float x[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) x[e] = dLs[t * DL_LD + s0 + e] + dLs[(s0 + e) * DL_LD + t];
+            put16(sm + OFF_L, LO_64, t, s0, x);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        // ------------------------------ P5 ------------------------------
+        if (tid == 0) {
+            tc_fence_after();
+            const uint32_t kq = s_sm + OFF_KQ, w = s_sm + OFF_W, l = s_sm + OFF_L;
+            const uint32_t id_kn = idesc_bf16_f32(128, 64, 1, 0), id_mn = idesc_bf16_f32(128, 64, 1, 1);
+#pragma unroll
+            for (int part = 0; part < 2; ++part)
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                    const uint64_t kt = smem_desc(kq + ks * 2048, 16384, 1024);         // K^T (M = i, K = s)
+                    const uint64_t qt = smem_desc(kq + 8192 + ks * 2048, 16384, 1024);  // Q^T
+                    const uint32_t lo = part * LO_64;
+                    mma_bf16(tmem + TM_DQ, kt, smem_desc(w + lo + ks * 32, 16, 1024), id_kn, 1);       // dP[t][s]
+                    mma_bf16(tmem + TM_DK, qt, smem_desc(w + lo + ks * 2048, 8192, 1024), id_mn, 1);   // dP[s][t]
+                    mma_bf16(tmem + TM_DK, kt, smem_desc(l + lo + ks * 32, 16, 1024), id_kn, 1);       // (dL + dL^T)[t][s]
+                }
+        }
+        sync_m();
+        if (!ok) break;
+        // ------------------------------ P6 ------------------------------
+        {
+            float dq[32], dk[32];
+            tmem_ld32(lane_base + TM_DQ + 32 * hf, dq);
+            tmem_ld32(lane_base + TM_DK + 32 * hf, dk);
+            tmem_ld_wait();
+            const int i = ln;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                const int t = 32 * hf + e;
+                if (t < valid) {
+                    const size_t o = (row0 + (size_t)t * p.H) * D + i;
+                    const float kv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
+                        sm + OFF_KQ + swz_offset(t, i, 16384)));
+                    p.dq[o] = dq[e];
+                    p.dk[o] = fmaf(2.f * row_dal[t] * row_dadl[t], kv, dk[e]);
+                }
+            }
+            if (tid < valid) p.dbeta[row0 + (size_t)tid * p.H] = row_dal[tid] * row_dadb[tid];
+        }
+    } while (0);
+
+    if (tid == 0) {  // every product and load issued has completed before TMEM and the CTA go (bounded)
+        mma_commit(&bars->drain);
+        const uint64_t ts = globaltimer_ns();
+        while (!mbar_try_wait_sleep(&bars->drain, 0, 20000) && globaltimer_ns() - ts < DRAIN_NS) {
+        }
+        while (!mbar_try_wait_sleep(&bars->tma, 0, 20000) && globaltimer_ns() - ts < DRAIN_NS) {
+        }
+        if (!ok || *abort_flag) atomicExch(p.status, (int)EFLA_ERR_DEVICE_TIMEOUT);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, TM_COLS);
+}
+
+}  // namespace
+
+// Per-chunk gradients on the tensor cores: bf16 q, k, v, d_k = d_v = 128, T > 0, after
+// launch_bwd_state_tc (dse, G in g, dR in a.dv, dO split in do_split).
+cudaError_t launch_bwd_grad_tc(const BwdArgs &a, const float *states, const float *dse, const void *do_split,
+                               const float *g, const char **why) {
+    const long grid = (long)a.B * a.H * ((a.T + C - 1) / C);
+    if (grid == 0) return cudaSuccess;
+    const size_t n = (size_t)a.B * a.T * a.H * D;
+    const __nv_bfloat16 *hi = static_cast<const __nv_bfloat16 *>(do_split), *lo = hi + n;
+    GtParams p;
+    memset(&p, 0, sizeof p);
+    if (!bwd_row_map(&p.map_q, a.q, a.B, a.T, a.H) || !bwd_row_map(&p.map_k, a.k, a.B, a.T, a.H) ||
+        !bwd_row_map(&p.map_doh, hi, a.B, a.T, a.H) || !bwd_row_map(&p.map_dol, lo, a.B, a.T, a.H)) {
+        *why = "cuTensorMapEncodeTiled failed";
+        return cudaErrorInvalidValue;
+    }
+    p.v = static_cast<const __nv_bfloat16 *>(a.v);
+    p.beta = a.beta;
+    p.states = states;
+    p.dse = dse;
+    p.g = g;
+    p.dr = a.dv;
+    p.dq = a.dq;
+    p.dk = a.dk;
+    p.dbeta = a.dbeta;
+    p.status = device_status_ptr();
+    p.T = a.T;
+    p.H = a.H;
+    p.euler = a.euler;
+    p.wait_ns = wait_limit_ns();
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    static bool attr_done[64] = {};
+    if (e == cudaSuccess && (dev >= 64 || !attr_done[dev])) {
+        e = cudaFuncSetAttribute(bwd_grad_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_ALLOC);
+        if (e == cudaSuccess && dev < 64) attr_done[dev] = true;
+    }
+    if (e != cudaSuccess) {
+        *why = "setting the gradient kernel's shared memory";
+        return e;
+    }
+    *why = "tcgen05 gradient kernel launch";
+    bwd_grad_tc_kernel<<<(unsigned)grid, NT, SMEM_ALLOC, a.stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace efla

@@ -554,8 +554,11 @@ PFN_cuTensorMapEncodeTiled_v12000 bt_encode_fn() {
     return fn;
 }
 
-// [B, T, H, 128] bf16: box of 64 features x 1 head x 64 tokens x 1, 128-byte swizzle.
-bool bt_map(CUtensorMap *m, const void *ptr, int B, int T, int H) {
+}  // namespace
+
+// [B, T, H, 128] bf16: box of 64 features x 1 head x 64 tokens x 1, 128-byte swizzle (the
+// backward kernels' operand tiles).
+bool bwd_row_map(CUtensorMap *m, const void *ptr, int B, int T, int H) {
     auto fn = bt_encode_fn();
     if (!fn) return false;
     cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
@@ -567,7 +570,6 @@ bool bt_map(CUtensorMap *m, const void *ptr, int B, int T, int H) {
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-}  // namespace
 
 // State gradients of the chunked backward on the tensor cores: bf16 q, k, d_k = d_v = 128,
 // T > 0.  do_split: 2 x B*T*H*128 bf16 of scratch (dO hi, then lo); g_out: B*T*H*128 fp32
@@ -592,8 +594,8 @@ cudaError_t launch_bwd_state_tc(const BwdArgs &a, float *dse, void *do_split, fl
     }
     BtParams p;
     memset(&p, 0, sizeof p);
-    if (!bt_map(&p.map_q, a.q, a.B, a.T, a.H) || !bt_map(&p.map_k, a.k, a.B, a.T, a.H) ||
-        !bt_map(&p.map_doh, hi, a.B, a.T, a.H) || !bt_map(&p.map_dol, lo, a.B, a.T, a.H)) {
+    if (!bwd_row_map(&p.map_q, a.q, a.B, a.T, a.H) || !bwd_row_map(&p.map_k, a.k, a.B, a.T, a.H) ||
+        !bwd_row_map(&p.map_doh, hi, a.B, a.T, a.H) || !bwd_row_map(&p.map_dol, lo, a.B, a.T, a.H)) {
         *why = "cuTensorMapEncodeTiled failed";
         return cudaErrorInvalidValue;
     }

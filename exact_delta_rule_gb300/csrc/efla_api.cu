@@ -437,10 +437,12 @@ efla_status efla_bwd_chunked(const void *q, const void *k, const void *v, const 
     if (tc) {
         const char *why = "tcgen05 state-gradient kernel launch";
         e = launch_bwd_state_tc(a, dse, do_split, g_tok, &why);
+        if (e == cudaSuccess) e = launch_bwd_grad_tc(a, states, dse, do_split, g_tok, &why);
         if (e != cudaSuccess) return cuda_fail(e, why);
+    } else {
+        e = launch_bwd_chunked(a, states, dse);
+        if (e != cudaSuccess) return cuda_fail(e, "chunked backward kernel launch");
     }
-    e = launch_bwd_chunked(a, states, dse, tc ? g_tok : nullptr);
-    if (e != cudaSuccess) return cuda_fail(e, "chunked backward kernel launch");
     g_last_error.clear();
     return EFLA_OK;
 }

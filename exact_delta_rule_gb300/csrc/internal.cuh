@@ -1,6 +1,7 @@
 // Internal declarations shared by the translation units of libefla.so.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -93,6 +94,13 @@ cudaError_t launch_bwd_chunked(const BwdArgs &a, const float *states, float *dse
 // do_split is scratch for dO as bf16 hi and lo (2 x B*T*H*128 bf16); it also writes G of every
 // token into g_out (B*T*H*128 fp32) and dR into dv, for launch_bwd_chunked with g_in = g_out.
 cudaError_t launch_bwd_state_tc(const BwdArgs &a, float *dse, void *do_split, float *g_out, const char **why);
+// Per-chunk gradients on the tensor cores (bwd_grad_tc.cu) after launch_bwd_state_tc: reads the
+// forward's chunk-start states, dse, do_split, G (g) and dR (a.dv); writes dq, dk, dbeta.
+cudaError_t launch_bwd_grad_tc(const BwdArgs &a, const float *states, const float *dse, const void *do_split,
+                               const float *g, const char **why);
+// [B, T, H, 128] bf16 tensor map of the backward kernels: box 64 features x 1 head x 64 tokens
+// x 1, 128-byte swizzle (bwd_tc.cu).
+bool bwd_row_map(CUtensorMap *m, const void *ptr, int B, int T, int H);
 
 // Start states of the segments of split sequences from the segment maps (scan.cu).
 cudaError_t launch_scan_combine(const float *S0, const float *maps, float *s_in, int B, int G, int H,
