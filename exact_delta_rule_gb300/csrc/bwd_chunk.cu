@@ -332,11 +332,8 @@ constexpr size_t grad_smem_floats() {
     return 2 * (size_t)C * (D + 4) + 3 * (size_t)C * LC + 6 * C + 2 * (size_t)D * LJ + 6 * (size_t)C * LJ;
 }
 
-// GIVEN: G and dR (= dv) of every token were written by the tensor-core state pass (g_in and
-// a.dv); the kernel then reads them instead of forming them.
-template <typename TIn, int D, bool GIVEN>
-__global__ void __launch_bounds__(NT, 1) bwd_grad_kernel(BwdArgs a, const float *states, const float *dse,
-                                                         const float *g_in) {
+template <typename TIn, int D>
+__global__ void __launch_bounds__(NT, 1) bwd_grad_kernel(BwdArgs a, const float *states, const float *dse) {
     extern __shared__ __align__(16) float sm[];
     constexpr int LK = D + 4;
     constexpr int TI = D / 16;  // columns of dQ / dK per thread
@@ -411,13 +408,6 @@ __global__ void __launch_bounds__(NT, 1) bwd_grad_kernel(BwdArgs a, const float 
             eb.fetch(dSe + j0, D, D);
             vb.fetch(v + row0 * D + j0, stride, valid);
             ob.fetch(a.dO + row0 * D + j0, stride, valid);
-            if constexpr (GIVEN) {
-                Block<float, C, J> gb, rb;
-                gb.fetch(g_in + row0 * D + j0, stride, valid);
-                rb.fetch(a.dv + row0 * D + j0, stride, valid);
-                gb.put(Gs, LJ);
-                rb.put(dRs, LJ);
-            }
             sb.put(Ssl, LJ);
             eb.put(dSsl, LJ);
             vb.put(Vsl, LJ);
@@ -436,16 +426,14 @@ __global__ void __launch_bounds__(NT, 1) bwd_grad_kernel(BwdArgs a, const float 
                     const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
 #pragma unroll
                     for (int n = 0; n < 8; ++n) x[n] = fmaf(kv[ii], sv[n], x[n]);
-                    if constexpr (!GIVEN) {
-                        const float4 d0 = ld4(dSsl + (i + ii) * LJ + jq), d1 = ld4(dSsl + (i + ii) * LJ + jq + 4);
-                        const float dv8[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+                    const float4 d0 = ld4(dSsl + (i + ii) * LJ + jq), d1 = ld4(dSsl + (i + ii) * LJ + jq + 4);
+                    const float dv8[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
 #pragma unroll
-                        for (int n = 0; n < 8; ++n) g[n] = fmaf(kv[ii], dv8[n], g[n]);
-                    }
+                    for (int n = 0; n < 8; ++n) g[n] = fmaf(kv[ii], dv8[n], g[n]);
                 }
             }
 #pragma unroll 1
-            for (int s = ts; s < (GIVEN ? 0 : valid); ++s) {  // P[s][ts] is zero for s < ts
+            for (int s = ts; s < valid; ++s) {  // P[s][ts] is zero for s < ts
                 const float pv = Pm[s * LC + ts];
                 const float4 o0 = ld4(dOsl + s * LJ + jq), o1 = ld4(dOsl + s * LJ + jq + 4);
                 const float ov[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
@@ -455,10 +443,8 @@ __global__ void __launch_bounds__(NT, 1) bwd_grad_kernel(BwdArgs a, const float 
             const float4 v0 = ld4(Vsl + ts * LJ + jq), v1 = ld4(Vsl + ts * LJ + jq + 4);
             st4(Rs + ts * LJ + jq, make_float4(v0.x - x[0], v0.y - x[1], v0.z - x[2], v0.w - x[3]));
             st4(Rs + ts * LJ + jq + 4, make_float4(v1.x - x[4], v1.y - x[5], v1.z - x[6], v1.w - x[7]));
-            if constexpr (!GIVEN) {
-                st4(Gs + ts * LJ + jq, make_float4(g[0], g[1], g[2], g[3]));
-                st4(Gs + ts * LJ + jq + 4, make_float4(g[4], g[5], g[6], g[7]));
-            }
+            st4(Gs + ts * LJ + jq, make_float4(g[0], g[1], g[2], g[3]));
+            st4(Gs + ts * LJ + jq + 4, make_float4(g[4], g[5], g[6], g[7]));
         }
         __syncthreads();
         {  // U = W R (W lower) and dR = W^T G (W^T upper)
@@ -472,7 +458,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_grad_kernel(BwdArgs a, const float 
                 for (int n = 0; n < 8; ++n) u[n] = fmaf(wv, av[n], u[n]);
             }
 #pragma unroll 1
-            for (int s = ts; s < (GIVEN ? 0 : C); ++s) {
+            for (int s = ts; s < C; ++s) {
                 const float wv = W[s * LC + ts];
                 const float4 a0 = ld4(Gs + s * LJ + jq), a1 = ld4(Gs + s * LJ + jq + 4);
                 const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
@@ -481,11 +467,9 @@ __global__ void __launch_bounds__(NT, 1) bwd_grad_kernel(BwdArgs a, const float 
             }
             st4(Us + ts * LJ + jq, make_float4(u[0], u[1], u[2], u[3]));
             st4(Us + ts * LJ + jq + 4, make_float4(u[4], u[5], u[6], u[7]));
-            if constexpr (!GIVEN) {
-                st4(dRs + ts * LJ + jq, make_float4(r[0], r[1], r[2], r[3]));
-                st4(dRs + ts * LJ + jq + 4, make_float4(r[4], r[5], r[6], r[7]));
-            }
-            if (!GIVEN && ts < valid) {  // dv = dR
+            st4(dRs + ts * LJ + jq, make_float4(r[0], r[1], r[2], r[3]));
+            st4(dRs + ts * LJ + jq + 4, make_float4(r[4], r[5], r[6], r[7]));
+            if (ts < valid) {  // dv = dR
                 float *dvp = a.dv + (((size_t)b * a.T + (size_t)(t0 + ts)) * a.H + h) * D + j0 + jq;
                 st4(dvp, make_float4(r[0], r[1], r[2], r[3]));
                 st4(dvp + 4, make_float4(r[4], r[5], r[6], r[7]));
@@ -632,35 +616,28 @@ static_assert(state_smem_floats<128>() * sizeof(float) <= 232448, "state kernel 
 static_assert(grad_smem_floats<128>() * sizeof(float) <= 232448, "gradient kernel shared memory");
 
 template <typename TIn, int D>
-cudaError_t launch_d(const BwdArgs &a, const float *states, float *dse, const float *g_in) {
+cudaError_t launch_d(const BwdArgs &a, const float *states, float *dse) {
     const int nc = (a.T + C - 1) / C;
     const size_t s1 = state_smem_floats<D>() * sizeof(float), s2 = grad_smem_floats<D>() * sizeof(float);
     cudaError_t e = cudaFuncSetAttribute(bwd_state_kernel<TIn, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(bwd_grad_kernel<TIn, D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s2);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(bwd_grad_kernel<TIn, D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s2);
+        e = cudaFuncSetAttribute(bwd_grad_kernel<TIn, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s2);
     if (e != cudaSuccess) return e;
-    if (!g_in) {
-        bwd_state_kernel<TIn, D><<<(unsigned)((long)a.B * a.H), NT, s1, a.stream>>>(a, dse);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    }
+    bwd_state_kernel<TIn, D><<<(unsigned)((long)a.B * a.H), NT, s1, a.stream>>>(a, dse);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (nc == 0) return cudaSuccess;
-    if (g_in)
-        bwd_grad_kernel<TIn, D, true><<<(unsigned)((long)a.B * a.H * nc), NT, s2, a.stream>>>(a, states, dse, g_in);
-    else
-        bwd_grad_kernel<TIn, D, false><<<(unsigned)((long)a.B * a.H * nc), NT, s2, a.stream>>>(a, states, dse, nullptr);
+    bwd_grad_kernel<TIn, D><<<(unsigned)((long)a.B * a.H * nc), NT, s2, a.stream>>>(a, states, dse);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_bwd_chunked(const BwdArgs &a, const float *states, float *dse, const float *g_in) {
+cudaError_t launch_bwd_chunked(const BwdArgs &a, const float *states, float *dse) {
     if ((long long)a.B * a.H == 0) return cudaSuccess;
     const bool bf = a.in_dtype == EFLA_BF16;
     if (a.dk_dim == 64)
-        return bf ? launch_d<__nv_bfloat16, 64>(a, states, dse, g_in) : launch_d<float, 64>(a, states, dse, g_in);
-    return bf ? launch_d<__nv_bfloat16, 128>(a, states, dse, g_in) : launch_d<float, 128>(a, states, dse, g_in);
+        return bf ? launch_d<__nv_bfloat16, 64>(a, states, dse) : launch_d<float, 64>(a, states, dse);
+    return bf ? launch_d<__nv_bfloat16, 128>(a, states, dse) : launch_d<float, 128>(a, states, dse);
 }
 
 }  // namespace efla

@@ -9,7 +9,7 @@
 //   dY = G - L^T dR,  Z = R - L U,  dalpha_t = sum_j dY[t][j] Z[t][j]
 //   dP = (dO U^T) o M_incl,  dL = -strictly-lower(dR U^T)
 //   dq = dO S^T + dP K
-//   dk = -dR S^T + U dS'^T + dP^T Q + (dL + dL^T) K + 2 dalpha (dalpha/dlambda) k
+//   dk = -dR S^T + U dS'^T + dP^T Q + (dL + dL^T + diag(2 dalpha dalpha/dlambda)) K
 //   dbeta = dalpha (dalpha/dbeta)
 // All products run on the tensor core in the transposed orientation (TMEM lane = feature),
 // every operand that is not an exact bf16 input split into bf16 hi + lo (fp32 accumulation):
@@ -18,13 +18,20 @@
 //   P2  R^T = V^T - X^T (TMEM);  U^T = R^T T''^T
 //   P3  Z^T = R^T + U^T (-L)^T;  dY^T = G^T + dR^T (-L)
 //       [dP; -dR U^T] = [dO; -dR] U^T;  dK^T += dS' U^T          (dS': the same tile, reloaded)
-//   P4  dalpha (lane reduction of dY^T o Z^T); dP and dL + dL^T as bf16 hi/lo tiles
-//   P5  dQ^T += K^T dP^T;  dK^T += Q^T dP + K^T (dL + dL^T)
-//   P6  dq, dk (+ 2 dalpha dalpha/dlambda k), dbeta to HBM
-// One CTA of 256 threads per (b, h, chunk); thread 0 issues the products, all threads take
-// part in every other step, the two warpgroups each on half of a chunk's 64 tokens.  Every
-// wait is bounded; on expiry the CTA records EFLA_ERR_DEVICE_TIMEOUT and leaves.
+//   P4  dalpha (lane reduction of dY^T o Z^T); dP and E = dL + dL^T + diag(2 dalpha dalpha/dlambda)
+//       as bf16 hi/lo tiles
+//   P5  dQ^T += K^T dP^T;  dK^T += Q^T dP + K^T E
+//   P6  dq, dk, dbeta to HBM
+// Persistent CTAs of 288 threads walk the (b, h, chunk) items with a stride of the grid:
+//   warps 0-7 (CUDA cores): every step above that is not a product, the two warpgroups each on
+//     half of a chunk's 64 tokens; they meet at named barrier 1 only and hand operands to the
+//     tensor core through mbarriers;
+//   warp 8 (one lane): TMA loads of K, Q, dO, bulk copies of the S and dS' tiles (written in this
+//     layout by the forward and the state pass), every tcgen05.mma and commit.
+// Every wait is bounded; on expiry the CTA records EFLA_ERR_DEVICE_TIMEOUT and leaves.
 #include <cudaTypedefs.h>
+
+#include <algorithm>
 
 #include "internal.cuh"
 #include "ptx.cuh"
@@ -38,7 +45,9 @@ using namespace tc;
 
 constexpr int C = 64;
 constexpr int D = 128;
-constexpr int NT = 256;
+constexpr int NW = 256;         // CUDA-core threads (warps 0-7)
+constexpr int NTH = NW + 32;    // and the MMA / TMA warp
+constexpr int BAR_W = 1;        // named barrier of the CUDA-core warps
 
 // Shared memory map (bytes from a 1024-byte aligned base).  Operand tiles are bf16 with the
 // 128-byte swizzle in column blocks of 64 elements; "hi | lo" pairs are the two split parts.
@@ -50,7 +59,7 @@ constexpr uint32_t OFF_L = 180224;    // -L hi | lo [64][64] (16 KB); later dL +
 constexpr uint32_t OFF_UT = 196608;   // U^T hi | lo [128][64] (32 KB); before: fp32 A~ [64][68]; after: fp32 dL [64][65]
 constexpr uint32_t OFF_ROW = 229376;  // fp32 per token: beta, invn, gn, alpha, dadb, dadl, dalpha
 constexpr uint32_t OFF_BAR = OFF_ROW + 7 * C * 4;
-constexpr uint32_t OFF_MISC = OFF_BAR + 64;  // tmem base, abort flag
+constexpr uint32_t OFF_MISC = OFF_BAR + 128;  // tmem base, abort flag
 constexpr uint32_t SMEM_USED = OFF_MISC + 16;
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;
 constexpr int AT_LD = 68;
@@ -83,19 +92,24 @@ struct GtParams {
     CUtensorMap map_q, map_k, map_doh, map_dol;  // [B, T, H, 128] bf16: box 64 x 1 x 64 x 1, 128B swizzle
     const __nv_bfloat16 *v;                      // [B, T, H, 128]
     const float *beta;                           // [B, T, H]
-    const float *states, *dse;                   // [B, H, nchunks, 128, 128]: S and dS' of every chunk
+    const uint8_t *states, *dse;                 // [B, H, nchunks] x 64 KB: S and dS' of every chunk as
+                                                 // bf16 hi/lo operand tiles (put_col_split_tile)
     const float *g, *dr;                         // [B, T, H, 128]: G and dR (= dv) of every token
     float *dq, *dk, *dbeta;
     int *status;
-    int T, H;
+    int T, H, items;                             // items = B H nchunks
     int euler;
     unsigned long long wait_ns;
 };
 
 struct Bars {
-    uint64_t tma, g, m, a, b, drain;
+    uint64_t tma;                          // K, Q, dO of the item landed
+    uint64_t s_full, d_full;               // the S tile / the dS' tile landed (bulk copies)
+    uint64_t g, m1, u, a, b, m2;           // products complete (tcgen05.commit)
+    uint64_t w_s, w_u, w_p3, w_p5, w_free; // operands written / TMEM read by the CUDA-core warps (8 arrivals)
+    uint64_t drain;
 };
-static_assert(sizeof(Bars) <= 64, "mbarrier block exceeds its slot");
+static_assert(sizeof(Bars) <= 128, "mbarrier block exceeds its slot");
 
 // x[0..15] as bf16 hi and lo of row `row`, columns col0 .. col0 + 15 (col0 + 15 < 64) of a
 // swizzled tile (hi at `tile`, lo at tile + lo_off).
@@ -147,34 +161,49 @@ __device__ __forceinline__ float lane_reduce_scatter(float (&x)[32], int lane) {
     return x[0];
 }
 
-__global__ void __launch_bounds__(NT, 1) bwd_grad_tc_kernel(const __grid_constant__ GtParams p) {
+
+// One work item: chunk c of unit (b, h); token t of the chunk is row row0 + t H of [B, T, H].
+struct Item {
+    int b, h, t0, valid;
+    size_t row0;
+};
+__device__ __forceinline__ Item item_of(const GtParams &p, int w, int nc) {
+    Item it;
+    const int unit = w / nc, c = w - unit * nc;
+    it.b = unit / p.H;
+    it.h = unit - it.b * p.H;
+    it.t0 = c * C;
+    it.valid = min(C, p.T - it.t0);
+    it.row0 = ((size_t)it.b * p.T + (size_t)it.t0) * p.H + it.h;
+    return it;
+}
+
+__global__ void __launch_bounds__(NTH, 1) bwd_grad_tc_kernel(const __grid_constant__ GtParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    float *row_beta = reinterpret_cast<float *>(sm + OFF_ROW), *row_invn = row_beta + C, *row_gn = row_invn + C;
-    float *row_al = row_gn + C, *row_dadb = row_al + C, *row_dadl = row_dadb + C, *row_dal = row_dadl + C;
-    float *At = reinterpret_cast<float *>(sm + OFF_UT);   // A~, then T~ (P0)
-    float *dLs = reinterpret_cast<float *>(sm + OFF_UT);  // dL (P4)
     Bars *bars = reinterpret_cast<Bars *>(sm + OFF_BAR);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + OFF_MISC + 4);
-
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nc = (p.T + C - 1) / C;
-    const int unit = blockIdx.x / nc, c = blockIdx.x % nc;
-    const int b = unit / p.H, h = unit % p.H;
-    const int t0 = c * C, valid = min(C, p.T - t0);
-    const size_t row0 = ((size_t)b * p.T + (size_t)t0) * p.H + h;  // token t of the chunk: row0 + t H
     const uint64_t wait_ns = p.wait_ns;
-    // TMEM: this thread reads and writes lane `ln` (its warp's quarter), columns of token half `hf`
-    const int hf = warp >> 2, ln = (warp & 3) * 32 + lane;
     const uint32_t s_sm = smem_u32(sm);
 
     if (tid == 0) {
         mbar_init(&bars->tma, 1);
+        mbar_init(&bars->s_full, 1);
+        mbar_init(&bars->d_full, 1);
         mbar_init(&bars->g, 1);
-        mbar_init(&bars->m, 1);
+        mbar_init(&bars->m1, 1);
+        mbar_init(&bars->u, 1);
         mbar_init(&bars->a, 1);
         mbar_init(&bars->b, 1);
+        mbar_init(&bars->m2, 1);
+        mbar_init(&bars->w_s, 8);
+        mbar_init(&bars->w_u, 8);
+        mbar_init(&bars->w_p3, 8);
+        mbar_init(&bars->w_p5, 8);
+        mbar_init(&bars->w_free, 8);
         mbar_init(&bars->drain, 1);
         fence_mbar_init();
         *abort_flag = 0;
@@ -187,364 +216,416 @@ __global__ void __launch_bounds__(NT, 1) bwd_grad_tc_kernel(const __grid_constan
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-    int m_uses = 0;
-    bool ok = true;
-    // every thread waits (bounded) on `bar`; one outcome for the CTA
-    auto wait_all = [&](uint64_t *bar, int parity) {
-        const bool mine = ok && wait_bar(bar, parity, abort_flag, wait_ns);
-        ok = __syncthreads_and(mine) != 0;
-        tc_fence_after();
-    };
-    // thread 0 commits the products issued so far to bars->m; everyone waits for them
-    auto sync_m = [&]() {
-        if (tid == 0) mma_commit(&bars->m);
-        wait_all(&bars->m, m_uses & 1);
-        ++m_uses;
-    };
 
-    // ------------------------------ loads ------------------------------
-    if (tid == 0) {
-        prefetch_tensormap(&p.map_q);
-        prefetch_tensormap(&p.map_k);
-        prefetch_tensormap(&p.map_doh);
-        prefetch_tensormap(&p.map_dol);
-        mbar_arrive_expect_tx(&bars->tma, 4 * 16384);
-        for (int cb = 0; cb < 2; ++cb) {
-            tma_load_4d(sm + OFF_KQ + cb * 16384, &p.map_k, &bars->tma, cb * 64, h, t0, b);
-            tma_load_4d(sm + OFF_KQ + cb * 16384 + 8192, &p.map_q, &bars->tma, cb * 64, h, t0, b);
-            tma_load_4d(sm + OFF_DOR + cb * 16384, &p.map_doh, &bars->tma, cb * 64, h, t0, b);
-            tma_load_4d(sm + OFF_DOR + LO_128 + cb * 16384, &p.map_dol, &bars->tma, cb * 64, h, t0, b);
+    if (warp == 8) {
+        // ============================ MMA / TMA warp ============================
+        const bool leader = lane == 0;
+        const uint32_t kq = s_sm + OFF_KQ, dor = s_sm + OFF_DOR, ss = s_sm + OFF_SS;
+        const uint32_t wt = s_sm + OFF_W, l = s_sm + OFF_L, ut = s_sm + OFF_UT;
+        if (leader) {
+            prefetch_tensormap(&p.map_q);
+            prefetch_tensormap(&p.map_k);
+            prefetch_tensormap(&p.map_doh);
+            prefetch_tensormap(&p.map_dol);
         }
-    }
-    // V^T of this thread's lane j = ln and token half, kept for P2
-    float vt[32];
-#pragma unroll
-    for (int e = 0; e < 32; ++e) {
-        const int t = 32 * hf + e;
-        vt[e] = t < valid ? __bfloat162float(p.v[(row0 + (size_t)t * p.H) * D + ln]) : 0.f;
-    }
-    {  // S -> bf16 hi/lo tile (row i, column j); a warp reads one 512-byte row per load
-        const float4 *src = reinterpret_cast<const float4 *>(p.states + (size_t)blockIdx.x * D * D);
-        float4 x[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) x[e] = __ldg(src + e * NT + tid);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) put4(sm + OFF_SS, LO_128, e * 8 + warp, lane * 4, x[e]);
-    }
-    {  // -dR -> rows 64-127 of the [dO; -dR] tile
-        const int jc = lane * 4;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const int t = e * 8 + warp;
-            float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (t < valid) x = __ldg(reinterpret_cast<const float4 *>(p.dr + (row0 + (size_t)t * p.H) * D + jc));
-            put4(sm + OFF_DOR, LO_128, C + t, jc, make_float4(-x.x, -x.y, -x.z, -x.w));
+        bool ok = true;
+        int it = 0, tma_pending = -1, s_pending = -1, d_pending = -1;
+        auto load_tile = [&](uint64_t *bar, const uint8_t *src) {  // one 64 KB operand tile into the S tile
+            if (leader) {
+                mbar_arrive_expect_tx(bar, 65536);
+                bulk_load(sm + OFF_SS, src, 65536, bar);
+            }
+            __syncwarp();
+        };
+        if (blockIdx.x < p.items) {
+            load_tile(&bars->s_full, p.states + (size_t)blockIdx.x * 65536);
+            s_pending = 0;
         }
-    }
-    if (tid < C) {
-        row_beta[tid] = tid < valid ? p.beta[row0 + (size_t)tid * p.H] : 0.f;
-        row_dal[tid] = 0.f;
-    }
-    fence_proxy_async_smem();
-    wait_all(&bars->tma, 0);
-
-    do {
-        if (!ok) break;
-        // ------------------------------ P0 / P1 products ------------------------------
-        if (tid == 0) {
-            const uint32_t kq = s_sm + OFF_KQ, ss = s_sm + OFF_SS, dor = s_sm + OFF_DOR;
-            // Gram K K^T (rows 64-127 of the M = 128 product are Q K^T, unused)
-            {
+        auto wait = [&](uint64_t *bar, int parity) {
+            ok = ok && wait_bar_warp(bar, parity, abort_flag, wait_ns);
+            tc_fence_after();
+            return ok;
+        };
+        for (int w = blockIdx.x; w < p.items; w += gridDim.x, ++it) {
+            const int ph = it & 1;
+            const Item I = item_of(p, w, nc);
+            // the previous item's last products are complete: [K; Q], dO, T''/dP, -L/E are free
+            if (it > 0 && !wait(&bars->m2, ph ^ 1)) break;
+            if (leader) {
+                mbar_arrive_expect_tx(&bars->tma, 4 * 16384);
+                for (int cb = 0; cb < 2; ++cb) {
+                    tma_load_4d(sm + OFF_KQ + cb * 16384, &p.map_k, &bars->tma, cb * 64, I.h, I.t0, I.b);
+                    tma_load_4d(sm + OFF_KQ + cb * 16384 + 8192, &p.map_q, &bars->tma, cb * 64, I.h, I.t0, I.b);
+                    tma_load_4d(sm + OFF_DOR + cb * 16384, &p.map_doh, &bars->tma, cb * 64, I.h, I.t0, I.b);
+                    tma_load_4d(sm + OFF_DOR + LO_128 + cb * 16384, &p.map_dol, &bars->tma, cb * 64, I.h, I.t0, I.b);
+                }
+            }
+            tma_pending = ph;
+            __syncwarp();
+            if (!wait(&bars->tma, ph)) break;
+            tma_pending = -1;
+            if (leader) {  // Gram K K^T (rows 64-127 of the M = 128 product are Q K^T, unused)
                 const uint32_t idesc = idesc_bf16_f32(128, 64, 0, 0);
-#pragma unroll
+#pragma unroll 1
                 for (int ks = 0; ks < 8; ++ks) {
                     const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
                     mma_bf16(tmem + TM_U, smem_desc(kq + off, 16, 1024), smem_desc(kq + off, 16, 1024), idesc, ks > 0);
                 }
                 mma_commit(&bars->g);
             }
-            {  // X^T = S^T K^T: S^T read as an MN-major A (M = j), K = i
-                const uint32_t idesc = idesc_bf16_f32(128, 64, 1, 0);
-#pragma unroll
-                for (int part = 0; part < 2; ++part)
-#pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
-                        const uint32_t boff = (ks >> 2) * 16384 + (ks & 3) * 32;
-                        mma_bf16(tmem + TM_X, smem_desc(ss + part * LO_128 + ks * 2048, 16384, 1024),
-                                 smem_desc(kq + boff, 16, 1024), idesc, (part | ks) != 0);
-                    }
-            }
-            {  // [dQ^T | dK^T] = S [dO; -dR]^T: one N = 128 product, K = j
-                const uint32_t idesc = idesc_bf16_f32(128, 128, 0, 0);
-#pragma unroll
-                for (int pr = 0; pr < 3; ++pr) {  // S hi x hi, S hi x lo, S lo x hi
-                    const uint32_t a_lo = pr == 2 ? LO_128 : 0, b_lo = pr == 1 ? LO_128 : 0;
-#pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
-                        const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-                        mma_bf16(tmem + TM_DQ, smem_desc(ss + a_lo + off, 16, 1024), smem_desc(dor + b_lo + off, 16, 1024),
-                                 idesc, (pr | ks) != 0);
+            __syncwarp();
+            // the S tile and -dR rows are written; the previous item's dQ^T and dK^T are read out
+            if (!wait(&bars->w_s, ph)) break;
+            if (it > 0 && !wait(&bars->w_free, ph ^ 1)) break;
+            if (!wait(&bars->s_full, ph)) break;
+            s_pending = -1;
+            if (leader) {
+                {  // X^T = S^T K^T: S^T read as an MN-major A (M = j), K = i
+                    const uint32_t idesc = idesc_bf16_f32(128, 64, 1, 0);
+#pragma unroll 1
+                    for (int part = 0; part < 2; ++part)
+#pragma unroll 1
+                        for (int ks = 0; ks < 8; ++ks) {
+                            const uint32_t boff = (ks >> 2) * 16384 + (ks & 3) * 32;
+                            mma_bf16(tmem + TM_X, smem_desc(ss + part * LO_128 + ks * 2048, 16384, 1024),
+                                     smem_desc(kq + boff, 16, 1024), idesc, (part | ks) != 0);
+                        }
+                }
+                {  // [dQ^T | dK^T] = S [dO; -dR]^T: one N = 128 product, K = j
+                    const uint32_t idesc = idesc_bf16_f32(128, 128, 0, 0);
+#pragma unroll 1
+                    for (int pr = 0; pr < 3; ++pr) {  // S hi x hi, S hi x lo, S lo x hi
+                        const uint32_t a_lo = pr == 2 ? LO_128 : 0, b_lo = pr == 1 ? LO_128 : 0;
+#pragma unroll 1
+                        for (int ks = 0; ks < 8; ++ks) {
+                            const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+                            mma_bf16(tmem + TM_DQ, smem_desc(ss + a_lo + off, 16, 1024),
+                                     smem_desc(dor + b_lo + off, 16, 1024), idesc, (pr | ks) != 0);
+                        }
                     }
                 }
+                mma_commit(&bars->m1);
             }
-            mma_commit(&bars->m);
-        }
-        // ------------------------------ P0: gate terms, -L, T'' ------------------------------
-        wait_all(&bars->g, 0);
-        if (!ok) break;
-        if (ln < C) {  // row t = ln of K K^T, this half's 32 columns (warps 0, 1, 4, 5)
-            const int t = ln, col0 = 32 * hf;
-            float g[32];
-            tmem_ld32(lane_base + TM_U + col0, g);
-            tmem_ld_wait();
-            if ((t >> 5) == hf) {  // the diagonal element is in this half: gate terms of row t
-                float lam = 0.f;
-#pragma unroll
-                for (int s = 0; s < 32; ++s) lam = (s == (t & 31)) ? g[s] : lam;
-                const float bt = row_beta[t];
-                const bool live = t < valid && lam > 0.f;
-                const float in = live ? rsqrtf(lam) : 0.f;
-                const float gam = !live ? 0.f : p.euler ? bt * lam : -expm1f(-bt * lam);
-                float db = 0.f, dl = 0.f;
-                if (t < valid) gate_grad(bt, lam, p.euler, db, dl);
-                row_invn[t] = in;
-                row_gn[t] = gam * in;
-                row_al[t] = t < valid ? efla_alpha(bt, lam, p.euler) : 0.f;
-                row_dadb[t] = db;
-                row_dadl[t] = dl;
-            }
-            float x[32];
-#pragma unroll
-            for (int s = 0; s < 32; ++s) x[s] = col0 + s < t ? -g[s] : 0.f;  // -L
-            put16(sm + OFF_L, LO_64, t, col0, x);
-            put16(sm + OFF_L, LO_64, t, col0 + 16, x + 16);
-#pragma unroll
-            for (int s = 0; s < 32; s += 4)
-                *reinterpret_cast<float4 *>(At + t * AT_LD + col0 + s) = make_float4(g[s], g[s + 1], g[s + 2], g[s + 3]);
-        }
-        __syncthreads();
-        for (int e = tid; e < C * C; e += NT) {  // A~ = strictly-lower(gamma_t k^_t . k^_s), in place
-            const int t = e / C, s = e % C;
-            At[t * AT_LD + s] = s < t ? row_gn[t] * At[t * AT_LD + s] * row_invn[s] : 0.f;
-        }
-        __syncthreads();
-        invert_unit_lower<1, AT_LD>(At, tid);  // T~; ends with a barrier over all 256 threads
-        {  // T'' = diag(1/n) T~ diag(gamma/n); a zero key's row keeps u_t = alpha_t r_t
-            const int t = tid >> 2, s0 = (tid & 3) * 16;
-            float x[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                const int s = s0 + e;
-                x[e] = s < t    ? row_invn[t] * At[t * AT_LD + s] * row_gn[s]
-                       : s == t ? (row_invn[t] > 0.f ? row_gn[t] * row_invn[t] : row_al[t])
-                                : 0.f;
-            }
-            put16(sm + OFF_W, LO_64, t, s0, x);
-        }
-        // ------------------------------ P2: R^T, U^T ------------------------------
-        wait_all(&bars->m, 0);  // X^T and S [dO; -dR]^T complete: the S tile is free again
-        m_uses = 1;
-        if (!ok) break;
-        float gt[32], drt[32];  // G^T and dR^T of this lane and token half, for P3
-        {
-            const float4 *src = reinterpret_cast<const float4 *>(p.dse + (size_t)blockIdx.x * D * D);
-            float4 x[16];  // dS', in flight while R^T is formed
-#pragma unroll
-            for (int e = 0; e < 16; ++e) x[e] = __ldg(src + e * NT + tid);
-            float r[32];
-            tmem_ld32(lane_base + TM_X + 32 * hf, r);
-            tmem_ld_wait();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) r[e] = vt[e] - r[e];
-            tmem_st32(lane_base + TM_X + 32 * hf, r);
-            tsplit32(lane_base, TM_RS, hf, r);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                const int t = 32 * hf + e;
-                const size_t o = (row0 + (size_t)t * p.H) * D + ln;
-                gt[e] = t < valid ? __ldg(p.g + o) : 0.f;
-                drt[e] = t < valid ? __ldg(p.dr + o) : 0.f;
-            }
-#pragma unroll
-            for (int e = 0; e < 16; ++e) put4(sm + OFF_SS, LO_128, e * 8 + warp, lane * 4, x[e]);
-        }
-        tmem_st_wait();
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        if (tid == 0) {  // U^T = R^T T''^T: A = R^T split (TMEM), B[t][s] = T''[t][s] (K-major)
-            tc_fence_after();
-            const uint32_t w = s_sm + OFF_W, idesc = idesc_bf16_f32(128, 64, 0, 0);
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-                const uint64_t bh = smem_desc(w + ks * 32, 16, 1024), bl = smem_desc(w + LO_64 + ks * 32, 16, 1024);
-                mma_bf16_ts(tmem + TM_U, tmem + TM_RS + ks * 8, bh, idesc, ks > 0);
-                mma_bf16_ts(tmem + TM_U, tmem + TM_RS + ks * 8, bl, idesc, 1);
-                mma_bf16_ts(tmem + TM_U, tmem + TM_RS + 32 + ks * 8, bh, idesc, 1);
-            }
-        }
-        sync_m();
-        if (!ok) break;
-        // ------------------------------ P3 ------------------------------
-        {
-            float u[32];
-            tmem_ld32(lane_base + TM_U + 32 * hf, u);
-            tmem_ld_wait();
-            tsplit32(lane_base, TM_US, hf, u);
-            put16(sm + OFF_UT, LO_UT, ln, 32 * hf, u);
-            put16(sm + OFF_UT, LO_UT, ln, 32 * hf + 16, u + 16);
-            tmem_st32(lane_base + TM_U + 32 * hf, gt);  // G^T over U^T (read above)
-            tsplit32(lane_base, TM_RS, hf, drt);        // dR^T split over R^T's (its product is complete)
-        }
-        tmem_st_wait();
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        if (tid == 0) {
-            tc_fence_after();
-            const uint32_t l = s_sm + OFF_L, ut = s_sm + OFF_UT, ss = s_sm + OFF_SS, dor = s_sm + OFF_DOR;
-            {  // Z^T += U^T (-L)^T: A = U^T split (TMEM), B[t][s] = -L[t][s] (K-major)
+            __syncwarp();
+            if (!wait(&bars->m1, ph)) break;  // the S tile is read: dS' replaces it
+            load_tile(&bars->d_full, p.dse + (size_t)w * 65536);
+            d_pending = ph;
+            if (!wait(&bars->w_u, ph)) break;  // T'' tile and R^T split written
+            if (leader) {  // U^T = R^T T''^T: A = R^T split (TMEM), B[t][s] = T''[t][s] (K-major)
                 const uint32_t idesc = idesc_bf16_f32(128, 64, 0, 0);
-#pragma unroll
+#pragma unroll 1
                 for (int ks = 0; ks < 4; ++ks) {
-                    const uint64_t bh = smem_desc(l + ks * 32, 16, 1024), bl = smem_desc(l + LO_64 + ks * 32, 16, 1024);
-                    mma_bf16_ts(tmem + TM_X, tmem + TM_US + ks * 8, bh, idesc, 1);
-                    mma_bf16_ts(tmem + TM_X, tmem + TM_US + ks * 8, bl, idesc, 1);
-                    mma_bf16_ts(tmem + TM_X, tmem + TM_US + 32 + ks * 8, bh, idesc, 1);
-                }
-            }
-            {  // dY^T += dR^T (-L): A = dR^T split (TMEM), B[t][s] = -L[s][t] (MN-major)
-                const uint32_t idesc = idesc_bf16_f32(128, 64, 0, 1);
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {
-                    const uint64_t bh = smem_desc(l + ks * 2048, 8192, 1024), bl = smem_desc(l + LO_64 + ks * 2048, 8192, 1024);
-                    mma_bf16_ts(tmem + TM_U, tmem + TM_RS + ks * 8, bh, idesc, 1);
+                    const uint64_t bh = smem_desc(wt + ks * 32, 16, 1024), bl = smem_desc(wt + LO_64 + ks * 32, 16, 1024);
+                    mma_bf16_ts(tmem + TM_U, tmem + TM_RS + ks * 8, bh, idesc, ks > 0);
                     mma_bf16_ts(tmem + TM_U, tmem + TM_RS + ks * 8, bl, idesc, 1);
                     mma_bf16_ts(tmem + TM_U, tmem + TM_RS + 32 + ks * 8, bh, idesc, 1);
                 }
+                mma_commit(&bars->u);
             }
-            mma_commit(&bars->a);
-            {  // [dP; -dR U^T] = [dO; -dR] U^T, and dK^T += dS' U^T: B[t][j] = U^T[j][t] (MN-major), K = j
-                const uint32_t idesc = idesc_bf16_f32(128, 64, 0, 1);
+            __syncwarp();
+            if (!wait(&bars->w_p3, ph)) break;  // U^T split and tile, G^T, dR^T split written
+            if (!wait(&bars->d_full, ph)) break;
+            d_pending = -1;
+            if (leader) {
+                {  // Z^T += U^T (-L)^T: A = U^T split (TMEM), B[t][s] = -L[t][s] (K-major)
+                    const uint32_t idesc = idesc_bf16_f32(128, 64, 0, 0);
+#pragma unroll 1
+                    for (int ks = 0; ks < 4; ++ks) {
+                        const uint64_t bh = smem_desc(l + ks * 32, 16, 1024), bl = smem_desc(l + LO_64 + ks * 32, 16, 1024);
+                        mma_bf16_ts(tmem + TM_X, tmem + TM_US + ks * 8, bh, idesc, 1);
+                        mma_bf16_ts(tmem + TM_X, tmem + TM_US + ks * 8, bl, idesc, 1);
+                        mma_bf16_ts(tmem + TM_X, tmem + TM_US + 32 + ks * 8, bh, idesc, 1);
+                    }
+                }
+                {  // dY^T += dR^T (-L): A = dR^T split (TMEM), B[t][s] = -L[s][t] (MN-major)
+                    const uint32_t idesc = idesc_bf16_f32(128, 64, 0, 1);
+#pragma unroll 1
+                    for (int ks = 0; ks < 4; ++ks) {
+                        const uint64_t bh = smem_desc(l + ks * 2048, 8192, 1024), bl = smem_desc(l + LO_64 + ks * 2048, 8192, 1024);
+                        mma_bf16_ts(tmem + TM_U, tmem + TM_RS + ks * 8, bh, idesc, 1);
+                        mma_bf16_ts(tmem + TM_U, tmem + TM_RS + ks * 8, bl, idesc, 1);
+                        mma_bf16_ts(tmem + TM_U, tmem + TM_RS + 32 + ks * 8, bh, idesc, 1);
+                    }
+                }
+                mma_commit(&bars->a);
+                {  // [dP; -dR U^T] = [dO; -dR] U^T and dK^T += dS' U^T: B[t][j] = U^T[j][t] (MN-major), K = j
+                    const uint32_t idesc = idesc_bf16_f32(128, 64, 0, 1);
+#pragma unroll 1
+                    for (int pr = 0; pr < 3; ++pr) {  // hi x hi, hi x lo, lo x hi
+                        const uint32_t a_lo = pr == 2 ? LO_128 : 0, b_lo = pr == 1 ? LO_UT : 0;
+#pragma unroll 1
+                        for (int ks = 0; ks < 8; ++ks) {
+                            const uint32_t aoff = a_lo + (ks >> 2) * 16384 + (ks & 3) * 32;
+                            const uint64_t bd = smem_desc(ut + b_lo + ks * 2048, 8192, 1024);
+                            mma_bf16(tmem + TM_P, smem_desc(dor + aoff, 16, 1024), bd, idesc, (pr | ks) != 0);
+                            mma_bf16(tmem + TM_DK, smem_desc(ss + aoff, 16, 1024), bd, idesc, 1);
+                        }
+                    }
+                }
+                mma_commit(&bars->b);
+            }
+            __syncwarp();
+            if (w + (int)gridDim.x < p.items) {  // the dS' tile is read: the next item's S replaces it
+                if (!wait(&bars->b, ph)) break;
+                load_tile(&bars->s_full, p.states + (size_t)(w + gridDim.x) * 65536);
+                s_pending = ph ^ 1;
+            }
+            if (!wait(&bars->w_p5, ph)) break;  // dP and E tiles written
+            if (leader) {  // dQ^T += K^T dP^T;  dK^T += Q^T dP + K^T E
+                const uint32_t id_kn = idesc_bf16_f32(128, 64, 1, 0), id_mn = idesc_bf16_f32(128, 64, 1, 1);
+#pragma unroll 1
+                for (int part = 0; part < 2; ++part)
+#pragma unroll 1
+                    for (int ks = 0; ks < 4; ++ks) {
+                        const uint64_t kt = smem_desc(kq + ks * 2048, 16384, 1024);         // K^T (M = i, K = s)
+                        const uint64_t qt = smem_desc(kq + 8192 + ks * 2048, 16384, 1024);  // Q^T
+                        const uint32_t lo = part * LO_64;
+                        mma_bf16(tmem + TM_DQ, kt, smem_desc(wt + lo + ks * 32, 16, 1024), id_kn, 1);      // dP[t][s]
+                        mma_bf16(tmem + TM_DK, qt, smem_desc(wt + lo + ks * 2048, 8192, 1024), id_mn, 1);  // dP[s][t]
+                        mma_bf16(tmem + TM_DK, kt, smem_desc(l + lo + ks * 32, 16, 1024), id_kn, 1);       // E[t][s]
+                    }
+                mma_commit(&bars->m2);
+            }
+            __syncwarp();
+        }
+        if (!ok) *abort_flag = 1;
+        if (leader) {  // every product and load issued has completed before TMEM and the CTA go (bounded)
+            mma_commit(&bars->drain);
+            const uint64_t ts = globaltimer_ns();
+            while (!mbar_try_wait_sleep(&bars->drain, 0, 20000) && globaltimer_ns() - ts < DRAIN_NS) {
+            }
+            while (tma_pending >= 0 && !mbar_try_wait_sleep(&bars->tma, tma_pending, 20000) &&
+                   globaltimer_ns() - ts < DRAIN_NS) {
+            }
+            while (s_pending >= 0 && !mbar_try_wait_sleep(&bars->s_full, s_pending, 20000) &&
+                   globaltimer_ns() - ts < DRAIN_NS) {
+            }
+            while (d_pending >= 0 && !mbar_try_wait_sleep(&bars->d_full, d_pending, 20000) &&
+                   globaltimer_ns() - ts < DRAIN_NS) {
+            }
+        }
+        __syncwarp();
+    } else {
+        // ============================ CUDA-core warps ============================
+        float *row_invn = reinterpret_cast<float *>(sm + OFF_ROW), *row_gn = row_invn + C, *row_al = row_gn + C;
+        float *row_dadb = row_al + C, *row_dadl = row_dadb + C, *row_dal = row_dadl + C;
+        float *At = reinterpret_cast<float *>(sm + OFF_UT);   // A~, then T~ (P0)
+        float *dLs = reinterpret_cast<float *>(sm + OFF_UT);  // dL (P4)
+        // TMEM: this thread reads and writes lane `ln` (its warp's quarter), the columns of token half `hf`
+        const int hf = warp >> 2, ln = (warp & 3) * 32 + lane;
+        const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        const bool gate_thr = ln < C && (ln >> 5) == hf;  // holds K K^T[t][t] for t = ln
+        bool ok = true;
+        int it = 0;
+        auto wait = [&](uint64_t *bar, int parity) {
+            ok = ok && wait_bar_warp(bar, parity, abort_flag, wait_ns);
+            tc_fence_after();
+        };
+        // operands of this warp written (generic and TMEM stores): one arrival per warp
+        auto hand_over = [&](uint64_t *bar) {
+            tmem_st_wait();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar);
+        };
+        for (int w = blockIdx.x; w < p.items; w += gridDim.x, ++it) {
+            const int ph = it & 1;
+            const Item I = item_of(p, w, nc);
+            const int valid = I.valid;
+            const size_t row0 = I.row0;
+            // ------------------------------ -dR rows ------------------------------
+            const float bt = gate_thr && ln < valid ? p.beta[row0 + (size_t)ln * p.H] : 0.f;
+            if (ok) {
+                const int jc = lane * 4;
+                float4 y[8];  // -dR -> rows 64-127 of the [dO; -dR] tile (loads as for V^T)
 #pragma unroll
-                for (int pr = 0; pr < 3; ++pr) {  // hi x hi, hi x lo, lo x hi
-                    const uint32_t a_lo = pr == 2 ? LO_128 : 0, b_lo = pr == 1 ? LO_UT : 0;
+                for (int e = 0; e < 8; ++e)
+                    y[e] = __ldcg(reinterpret_cast<const float4 *>(p.dr + (row0 + (size_t)min(e * 8 + warp, valid - 1) * p.H) * D + jc));
 #pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
-                        const uint32_t aoff = a_lo + (ks >> 2) * 16384 + (ks & 3) * 32;
-                        const uint64_t bd = smem_desc(ut + b_lo + ks * 2048, 8192, 1024);
-                        mma_bf16(tmem + TM_P, smem_desc(dor + aoff, 16, 1024), bd, idesc, (pr | ks) != 0);
-                        mma_bf16(tmem + TM_DK, smem_desc(ss + aoff, 16, 1024), bd, idesc, 1);
+                for (int e = 0; e < 8; ++e) {
+                    const bool in = e * 8 + warp < valid;
+                    put4(sm + OFF_DOR, LO_128, C + e * 8 + warp, jc,
+                         in ? make_float4(-y[e].x, -y[e].y, -y[e].z, -y[e].w) : make_float4(0.f, 0.f, 0.f, 0.f));
+                }
+            }
+            if (tid < C) row_dal[tid] = 0.f;  // (read by this thread only, in the previous item's dbeta)
+            hand_over(&bars->w_s);
+            // ------------------------------ P0: gate terms, -L, T'' ------------------------------
+            wait(&bars->g, ph);
+            if (ok && ln < C) {  // row t = ln of K K^T, this half's 32 columns (warps 0, 1, 4, 5)
+                const int t = ln, col0 = 32 * hf;
+                float g[32];
+                tmem_ld32(lane_base + TM_U + col0, g);
+                tmem_ld_wait();
+                if (gate_thr) {
+                    float lam = 0.f;
+#pragma unroll
+                    for (int s = 0; s < 32; ++s) lam = (s == (t & 31)) ? g[s] : lam;
+                    const bool live = t < valid && lam > 0.f;
+                    const float in = live ? rsqrtf(lam) : 0.f;
+                    const float gam = !live ? 0.f : p.euler ? bt * lam : -expm1f(-bt * lam);
+                    float db = 0.f, dl = 0.f;
+                    if (t < valid) gate_grad(bt, lam, p.euler, db, dl);
+                    row_invn[t] = in;
+                    row_gn[t] = gam * in;
+                    row_al[t] = t < valid ? efla_alpha(bt, lam, p.euler) : 0.f;
+                    row_dadb[t] = db;
+                    row_dadl[t] = dl;
+                }
+                float x[32];
+#pragma unroll
+                for (int s = 0; s < 32; ++s) x[s] = col0 + s < t ? -g[s] : 0.f;  // -L
+                put16(sm + OFF_L, LO_64, t, col0, x);
+                put16(sm + OFF_L, LO_64, t, col0 + 16, x + 16);
+#pragma unroll
+                for (int s = 0; s < 32; s += 4)
+                    *reinterpret_cast<float4 *>(At + t * AT_LD + col0 + s) = make_float4(g[s], g[s + 1], g[s + 2], g[s + 3]);
+            }
+            if (named_bar_any(BAR_W, NW, !ok)) break;  // every CUDA-core warp leaves together
+            for (int e = tid; e < C * C; e += NW) {  // A~ = strictly-lower(gamma_t k^_t . k^_s), in place
+                const int t = e / C, s = e % C;
+                At[t * AT_LD + s] = s < t ? row_gn[t] * At[t * AT_LD + s] * row_invn[s] : 0.f;
+            }
+            named_bar(BAR_W, NW);
+            invert_unit_lower<BAR_W, AT_LD>(At, tid);  // T~; ends with a barrier over the CUDA-core warps
+            {  // T'' = diag(1/n) T~ diag(gamma/n); a zero key's row keeps u_t = alpha_t r_t
+                const int t = tid >> 2, s0 = (tid & 3) * 16;
+                float x[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const int s = s0 + e;
+                    x[e] = s < t    ? row_invn[t] * At[t * AT_LD + s] * row_gn[s]
+                           : s == t ? (row_invn[t] > 0.f ? row_gn[t] * row_invn[t] : row_al[t])
+                                    : 0.f;
+                }
+                put16(sm + OFF_W, LO_64, t, s0, x);
+            }
+            // ------------------------------ P2: R^T, dS' ------------------------------
+            wait(&bars->m1, ph);  // X^T complete
+            if (ok) {
+                // V^T: rows past the chunk's end load its last row (always in bounds) and are zeroed
+                // after, so that all 32 loads are unconditional and in flight together
+                const __nv_bfloat16 *vc = p.v + row0 * D + ln;
+                __nv_bfloat16 vr[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) vr[e] = __ldcg(vc + (size_t)min(32 * hf + e, valid - 1) * p.H * D);
+                float r[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) r[e] = 32 * hf + e < valid ? __bfloat162float(vr[e]) : 0.f;
+                float xt[32];
+                tmem_ld32(lane_base + TM_X + 32 * hf, xt);
+                tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) r[e] -= xt[e];  // R^T = V^T - X^T
+                tmem_st32(lane_base + TM_X + 32 * hf, r);
+                tsplit32(lane_base, TM_RS, hf, r);
+            }
+            hand_over(&bars->w_u);
+            // ------------------------------ P3 operands ------------------------------
+            wait(&bars->u, ph);
+            if (ok) {
+                float gt[32], drt[32];  // G^T and dR^T of this lane and token half (loads as for V^T)
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const size_t o = (row0 + (size_t)min(32 * hf + e, valid - 1) * p.H) * D + ln;
+                    gt[e] = __ldcg(p.g + o);
+                    drt[e] = __ldcg(p.dr + o);
+                }
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    gt[e] = 32 * hf + e < valid ? gt[e] : 0.f;
+                    drt[e] = 32 * hf + e < valid ? drt[e] : 0.f;
+                }
+                float u[32];
+                tmem_ld32(lane_base + TM_U + 32 * hf, u);
+                tmem_ld_wait();
+                tsplit32(lane_base, TM_US, hf, u);
+                put16(sm + OFF_UT, LO_UT, ln, 32 * hf, u);
+                put16(sm + OFF_UT, LO_UT, ln, 32 * hf + 16, u + 16);
+                tmem_st32(lane_base + TM_U + 32 * hf, gt);  // G^T over U^T (read above)
+                tsplit32(lane_base, TM_RS, hf, drt);        // dR^T split over R^T's (its product is complete)
+            }
+            hand_over(&bars->w_p3);
+            // ------------------------------ P4 ------------------------------
+            wait(&bars->a, ph);
+            if (ok) {  // dalpha_t: sum over j of dY^T[j][t] Z^T[j][t]; this warp's 32 lanes, then across warps
+                float y[32], z[32];
+                tmem_ld32(lane_base + TM_U + 32 * hf, y);
+                tmem_ld32(lane_base + TM_X + 32 * hf, z);
+                tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) y[e] *= z[e];
+                atomicAdd(&row_dal[32 * hf + lane], lane_reduce_scatter(y, lane));
+            }
+            wait(&bars->b, ph);
+            if (ok) {
+                float x[32];
+                tmem_ld32(lane_base + TM_P + 32 * hf, x);
+                tmem_ld_wait();
+                if (ln < C) {  // dP = (dO U^T) o M_incl, row t
+                    const int t = ln;
+#pragma unroll
+                    for (int s = 0; s < 32; ++s) x[s] = 32 * hf + s <= t ? x[s] : 0.f;
+                    put16(sm + OFF_W, LO_64, t, 32 * hf, x);
+                    put16(sm + OFF_W, LO_64, t, 32 * hf + 16, x + 16);
+                } else {  // dL = strictly-lower(-dR U^T), row t
+                    const int t = ln - C;
+#pragma unroll
+                    for (int s = 0; s < 32; ++s) dLs[t * DL_LD + 32 * hf + s] = 32 * hf + s < t ? x[s] : 0.f;
+                }
+            }
+            if (named_bar_any(BAR_W, NW, !ok)) break;
+            {  // E = dL + dL^T + diag(2 dalpha dalpha/dlambda): the gate's share of dk rides on K^T E
+                const int t = tid >> 2, s0 = (tid & 3) * 16;
+                const float dg = 2.f * row_dal[t] * row_dadl[t];
+                float x[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    x[e] = dLs[t * DL_LD + s0 + e] + dLs[(s0 + e) * DL_LD + t] + (s0 + e == t ? dg : 0.f);
+                put16(sm + OFF_L, LO_64, t, s0, x);
+            }
+            if (tid < valid) p.dbeta[row0 + (size_t)tid * p.H] = row_dal[tid] * row_dadb[tid];
+            hand_over(&bars->w_p5);
+            // ------------------------------ P6 ------------------------------
+            wait(&bars->m2, ph);
+            if (ok) {
+                float dq[32], dk[32];
+                tmem_ld32(lane_base + TM_DQ + 32 * hf, dq);
+                tmem_ld32(lane_base + TM_DK + 32 * hf, dk);
+                tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->w_free);  // dQ^T and dK^T are in registers
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const int t = 32 * hf + e;
+                    if (t < valid) {
+                        const size_t o = (row0 + (size_t)t * p.H) * D + ln;
+                        p.dq[o] = dq[e];
+                        p.dk[o] = dk[e];
                     }
                 }
             }
-            mma_commit(&bars->b);
         }
-        // ------------------------------ P4 ------------------------------
-        wait_all(&bars->a, 0);
-        if (!ok) break;
-        {  // dalpha_t: sum over j of dY^T[j][t] Z^T[j][t]; this warp's 32 lanes, then across warps
-            float y[32], z[32];
-            tmem_ld32(lane_base + TM_U + 32 * hf, y);
-            tmem_ld32(lane_base + TM_X + 32 * hf, z);
-            tmem_ld_wait();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) y[e] *= z[e];
-            atomicAdd(&row_dal[32 * hf + lane], lane_reduce_scatter(y, lane));
-        }
-        wait_all(&bars->b, 0);
-        if (!ok) break;
-        {
-            float x[32];
-            tmem_ld32(lane_base + TM_P + 32 * hf, x);
-            tmem_ld_wait();
-            if (ln < C) {  // dP = (dO U^T) o M_incl, row t
-                const int t = ln;
-#pragma unroll
-                for (int s = 0; s < 32; ++s) x[s] = 32 * hf + s <= t ? x[s] : 0.f;
-                put16(sm + OFF_W, LO_64, t, 32 * hf, x);
-                put16(sm + OFF_W, LO_64, t, 32 * hf + 16, x + 16);
-            } else {  // dL = strictly-lower(-dR U^T), row t
-                const int t = ln - C;
-#pragma unroll
-                for (int s = 0; s < 32; ++s) dLs[t * DL_LD + 32 * hf + s] = 32 * hf + s < t ? x[s] : 0.f;
-            }
-        }
-        __syncthreads();
-        {  // dL + dL^T
-            const int t = tid >> 2, s0 = (tid & 3) * 16;
-            float x[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) x[e] = dLs[t * DL_LD + s0 + e] + dLs[(s0 + e) * DL_LD + t];
-            put16(sm + OFF_L, LO_64, t, s0, x);
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        // ------------------------------ P5 ------------------------------
-        if (tid == 0) {
-            tc_fence_after();
-            const uint32_t kq = s_sm + OFF_KQ, w = s_sm + OFF_W, l = s_sm + OFF_L;
-            const uint32_t id_kn = idesc_bf16_f32(128, 64, 1, 0), id_mn = idesc_bf16_f32(128, 64, 1, 1);
-#pragma unroll
-            for (int part = 0; part < 2; ++part)
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {
-                    const uint64_t kt = smem_desc(kq + ks * 2048, 16384, 1024);         // K^T (M = i, K = s)
-                    const uint64_t qt = smem_desc(kq + 8192 + ks * 2048, 16384, 1024);  // Q^T
-                    const uint32_t lo = part * LO_64;
-                    mma_bf16(tmem + TM_DQ, kt, smem_desc(w + lo + ks * 32, 16, 1024), id_kn, 1);       // dP[t][s]
-                    mma_bf16(tmem + TM_DK, qt, smem_desc(w + lo + ks * 2048, 8192, 1024), id_mn, 1);   // dP[s][t]
-                    mma_bf16(tmem + TM_DK, kt, smem_desc(l + lo + ks * 32, 16, 1024), id_kn, 1);       // (dL + dL^T)[t][s]
-                }
-        }
-        sync_m();
-        if (!ok) break;
-        // ------------------------------ P6 ------------------------------
-        {
-            float dq[32], dk[32];
-            tmem_ld32(lane_base + TM_DQ + 32 * hf, dq);
-            tmem_ld32(lane_base + TM_DK + 32 * hf, dk);
-            tmem_ld_wait();
-            const int i = ln;
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                const int t = 32 * hf + e;
-                if (t < valid) {
-                    const size_t o = (row0 + (size_t)t * p.H) * D + i;
-                    const float kv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
-                        sm + OFF_KQ + swz_offset(t, i, 16384)));
-                    p.dq[o] = dq[e];
-                    p.dk[o] = fmaf(2.f * row_dal[t] * row_dadl[t], kv, dk[e]);
-                }
-            }
-            if (tid < valid) p.dbeta[row0 + (size_t)tid * p.H] = row_dal[tid] * row_dadb[tid];
-        }
-    } while (0);
-
-    if (tid == 0) {  // every product and load issued has completed before TMEM and the CTA go (bounded)
-        mma_commit(&bars->drain);
-        const uint64_t ts = globaltimer_ns();
-        while (!mbar_try_wait_sleep(&bars->drain, 0, 20000) && globaltimer_ns() - ts < DRAIN_NS) {
-        }
-        while (!mbar_try_wait_sleep(&bars->tma, 0, 20000) && globaltimer_ns() - ts < DRAIN_NS) {
-        }
-        if (!ok || *abort_flag) atomicExch(p.status, (int)EFLA_ERR_DEVICE_TIMEOUT);
+        if (!ok) *abort_flag = 1;
     }
+
     tc_fence_before();
     __syncthreads();
+    if (tid == 0 && *abort_flag) atomicExch(p.status, (int)EFLA_ERR_DEVICE_TIMEOUT);
     if (warp == 0) tmem_dealloc(tmem, TM_COLS);
 }
 
 }  // namespace
 
 // Per-chunk gradients on the tensor cores: bf16 q, k, v, d_k = d_v = 128, T > 0, after
-// launch_bwd_state_tc (dse, G in g, dR in a.dv, dO split in do_split).
+// launch_bwd_state_tc (dse, G in g, dR in a.dv, dO split in do_split).  Persistent: one CTA per
+// SM at most, each walking items blockIdx.x, blockIdx.x + gridDim.x, ...
 cudaError_t launch_bwd_grad_tc(const BwdArgs &a, const float *states, const float *dse, const void *do_split,
                                const float *g, const char **why) {
-    const long grid = (long)a.B * a.H * ((a.T + C - 1) / C);
-    if (grid == 0) return cudaSuccess;
+    const long items = (long)a.B * a.H * ((a.T + C - 1) / C);
+    if (items == 0) return cudaSuccess;
     const size_t n = (size_t)a.B * a.T * a.H * D;
     const __nv_bfloat16 *hi = static_cast<const __nv_bfloat16 *>(do_split), *lo = hi + n;
     GtParams p;
@@ -556,8 +637,8 @@ cudaError_t launch_bwd_grad_tc(const BwdArgs &a, const float *states, const floa
     }
     p.v = static_cast<const __nv_bfloat16 *>(a.v);
     p.beta = a.beta;
-    p.states = states;
-    p.dse = dse;
+    p.states = reinterpret_cast<const uint8_t *>(states);
+    p.dse = reinterpret_cast<const uint8_t *>(dse);
     p.g = g;
     p.dr = a.dv;
     p.dq = a.dq;
@@ -566,21 +647,27 @@ cudaError_t launch_bwd_grad_tc(const BwdArgs &a, const float *states, const floa
     p.status = device_status_ptr();
     p.T = a.T;
     p.H = a.H;
+    p.items = (int)items;
     p.euler = a.euler;
     p.wait_ns = wait_limit_ns();
-    int dev = 0;
+    int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
-    static bool attr_done[64] = {};
-    if (e == cudaSuccess && (dev >= 64 || !attr_done[dev])) {
-        e = cudaFuncSetAttribute(bwd_grad_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_ALLOC);
-        if (e == cudaSuccess && dev < 64) attr_done[dev] = true;
-    }
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) {
-        *why = "setting the gradient kernel's shared memory";
+        *why = "querying the SM count";
         return e;
     }
+    static bool attr_done[64] = {};
+    if (dev >= 64 || !attr_done[dev]) {
+        e = cudaFuncSetAttribute(bwd_grad_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_ALLOC);
+        if (e != cudaSuccess) {
+            *why = "setting the gradient kernel's shared memory";
+            return e;
+        }
+        if (dev < 64) attr_done[dev] = true;
+    }
     *why = "tcgen05 gradient kernel launch";
-    bwd_grad_tc_kernel<<<(unsigned)grid, NT, SMEM_ALLOC, a.stream>>>(p);
+    bwd_grad_tc_kernel<<<(unsigned)std::min<long>(items, sms), NTH, SMEM_ALLOC, a.stream>>>(p);
     return cudaGetLastError();
 }
 

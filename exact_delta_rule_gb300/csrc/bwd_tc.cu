@@ -76,7 +76,8 @@ struct BtParams {
     CUtensorMap map_q, map_k, map_doh, map_dol;  // [B, T, H, 128] bf16: box 64 x 1 x 64 x 1, 128B swizzle
     const float *beta;                           // [B, T, H]
     const float *dST;                            // [B, H, 128, 128] or nullptr (zero)
-    float *dse;                                  // [B, H, nchunks, 128, 128]: dS' of every chunk
+    float *dse;                                  // [B, H, nchunks] x 64 KB: dS' of every chunk as bf16 hi/lo
+                                                 // operand tiles (put_col_split_tile)
     float *dS0;                                  // [B, H, 128, 128] or nullptr
     float *g_out, *dr_out;                       // [B, T, H, 128] fp32: G and dR (= dv) of every token
     int *status;
@@ -347,14 +348,13 @@ __global__ void __launch_bounds__(448, 1) bwd_tc_kernel(const __grid_constant__ 
             mbar_arrive(&bars->sa_ready);
             {  // dS' of this chunk (the gradient of its end state) to HBM while the tensor core forms
                // G^T; TM_S changes again only after r_ready, which this warpgroup arrives at later
-                float *dst = p.dse + ((size_t)blockIdx.x * nchunks + chunk_of(it)) * D * D + j;
+                uint8_t *dst = reinterpret_cast<uint8_t *>(p.dse + ((size_t)blockIdx.x * nchunks + chunk_of(it)) * D * D);
 #pragma unroll 1
                 for (int g = 0; g < 4; g = opaque(g + 1)) {
                     float sv[32];
                     tmem_ld32(lane_base + TM_S + g * 32, sv);
                     tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) dst[(size_t)(g * 32 + i) * D] = sv[i];
+                    put_col_split_tile(dst, g * 32, j, sv);
                 }
             }
             ok = wait_bar_warp(&bars->x_done, it & 1, abort_flag, wait_ns);

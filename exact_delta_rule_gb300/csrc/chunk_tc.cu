@@ -129,7 +129,8 @@ struct TcParams {
     int seg_len, G;
     const float *s_in;
     float *maps;
-    float *states;               // chunk-start states [N, H, nchunks, 128, 128] (rows of [B, T]) or nullptr
+    float *states;               // chunk-start states [N, H, nchunks] x 64 KB (rows of [B, T]) or nullptr: S as
+                                 // bf16 hi/lo operand tiles (put_col_split_tile) for the tensor-core backward
     unsigned long long wait_ns;  // bound on every wait between roles (2 s unless a test lowers it)
     int debug_stall;             // test hook: the MMA thread first waits on a barrier nothing completes
 };
@@ -563,18 +564,17 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
             if (!ok) break;
             tc_fence_after();
             // S^T -> bf16 hi/lo operand in TMEM, 32 columns of S^T (16 operand columns) at a time;
-            // with `states`, also the chunk's start state S (column j from this thread)
-            float *st_c = p.states ? p.states + ((size_t)blockIdx.x * nchunks + c) * D * D + j : nullptr;
+            // with `states`, also the chunk's start state S (column j from this thread) as a bf16
+            // hi/lo operand tile of the backward
+            uint8_t *st_c = p.states ? reinterpret_cast<uint8_t *>(p.states + ((size_t)blockIdx.x * nchunks + c) * D * D)
+                                     : nullptr;
 #pragma unroll 1
             for (int g = 0; g < 4; g = opaque(g + 1)) {
                 float sv[32];
                 uint32_t hi[16], lo[16];
                 tmem_ld32(lane_base + TM_S + g * 32, sv);
                 tmem_ld_wait();
-                if (st_c) {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) st_c[(size_t)(g * 32 + i) * D] = sv[i];
-                }
+                if (st_c) put_col_split_tile(st_c, g * 32, j, sv);
                 split_pack<16>(sv, hi, lo);
                 tmem_st16u(lane_base + TM_SA + g * 16, hi);
                 tmem_st16u(lane_base + TM_SA + 64 + g * 16, lo);

@@ -39,8 +39,9 @@ struct FwdArgs {
     int seg_len = 0, G = 0;
     const float *s_in = nullptr;
     float *maps = nullptr;
-    // Chunked backward: the state at the start of every chunk, [N, H, nchunks, dk, dv] fp32
-    // (rows of [B, T] only; o may then be nullptr).
+    // Chunked backward: the state at the start of every chunk, [N, H, nchunks] x dk x dv x 4 bytes
+    // (rows of [B, T] only; o may then be nullptr): fp32 row-major from the CUDA-core chunk
+    // kernel, bf16 hi/lo operand tiles (tc::put_col_split_tile) from the tensor-core one.
     float *states = nullptr;
 };
 
@@ -88,14 +89,15 @@ cudaError_t launch_bwd(const BwdArgs &a);
 // Chunked backward (bwd_chunk.cu), chunk 64, rows of [B, T]: the state gradients at the ends of
 // the chunks, then every chunk's gradients in parallel from `states` (the forward's chunk-start
 // states, filled first by a forward launch with FwdArgs::states).  dse: [B, H, nchunks, dk, dv].
-// With g_in, the tensor-core state pass has already filled dse, G (g_in) and dv.
-cudaError_t launch_bwd_chunked(const BwdArgs &a, const float *states, float *dse, const float *g_in = nullptr);
+cudaError_t launch_bwd_chunked(const BwdArgs &a, const float *states, float *dse);
 // The same state pass on the tensor cores (bwd_tc.cu): bf16 q, k, d_k = d_v = 128, T > 0;
 // do_split is scratch for dO as bf16 hi and lo (2 x B*T*H*128 bf16); it also writes G of every
-// token into g_out (B*T*H*128 fp32) and dR into dv, for launch_bwd_chunked with g_in = g_out.
+// token into g_out (B*T*H*128 fp32), dR into dv, and dse as bf16 hi/lo operand tiles, for
+// launch_bwd_grad_tc.
 cudaError_t launch_bwd_state_tc(const BwdArgs &a, float *dse, void *do_split, float *g_out, const char **why);
 // Per-chunk gradients on the tensor cores (bwd_grad_tc.cu) after launch_bwd_state_tc: reads the
-// forward's chunk-start states, dse, do_split, G (g) and dR (a.dv); writes dq, dk, dbeta.
+// forward's chunk-start states and dse (both as bf16 hi/lo operand tiles), do_split, G (g) and dR
+// (a.dv); writes dq, dk, dbeta.
 cudaError_t launch_bwd_grad_tc(const BwdArgs &a, const float *states, const float *dse, const void *do_split,
                                const float *g, const char **why);
 // [B, T, H, 128] bf16 tensor map of the backward kernels: box 64 features x 1 head x 64 tokens

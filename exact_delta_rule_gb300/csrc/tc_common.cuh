@@ -61,6 +61,25 @@ __device__ __forceinline__ void split_pack(const float *x, uint32_t *hi, uint32_
     }
 }
 
+// Rows row0 .. row0 + 31 of column j (this lane) of a 128 x 128 fp32 matrix, x[i] = M[row0 + i][j],
+// into the operand-tile layout the backward kernels load whole: bf16 hi (truncated) in the first
+// 32 KB and lo (the remainder, truncated) in the next, each as 2 column blocks of [128 rows][64]
+// with the 128-byte swizzle.  Lanes j and j ^ 1 of a warp (consecutive columns) pair up: each
+// shuffle hands one half to the partner, the even lane stores the hi word, the odd lane the lo
+// word.  All 32 lanes take part.
+__device__ __forceinline__ void put_col_split_tile(uint8_t *tile, int row0, int j, const float (&x)[32]) {
+    const bool odd = (j & 1) != 0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const uint32_t b = __float_as_uint(x[i]);
+        const uint32_t h16 = b >> 16;
+        const uint32_t l16 = __float_as_uint(x[i] - __uint_as_float(b & 0xffff0000u)) >> 16;
+        const uint32_t recv = __shfl_xor_sync(0xffffffffu, odd ? h16 : l16, 1);
+        const uint32_t word = odd ? (recv | (l16 << 16)) : (h16 | (recv << 16));
+        *reinterpret_cast<uint32_t *>(tile + swz_offset(row0 + i, j & ~1, 16384) + (odd ? 32768u : 0u)) = word;
+    }
+}
+
 }  // namespace
 }  // namespace tc
 }  // namespace efla
