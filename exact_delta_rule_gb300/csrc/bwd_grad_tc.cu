@@ -16,9 +16,9 @@
 //   P0  Gram K K^T (TMEM); gate terms, A~, blocked inverse; T'' and -L as bf16 hi/lo tiles
 //   P1  X^T = S^T K^T;  [dQ^T | dK^T] = S [dO; -dR]^T            (S: a swizzled bf16 tile)
 //   P2  R^T = V^T - X^T (TMEM);  U^T = R^T T''^T
-//   P3  Z^T = R^T + U^T (-L)^T;  dY^T = G^T + dR^T (-L)
+//   P3  Z^T = R^T + U^T (-L)^T;  -dY^T = -G^T + (-dR)^T (-L)        ((-dR)^T read from the tile)
 //       [dP; -dR U^T] = [dO; -dR] U^T;  dK^T += dS' U^T          (dS': the same tile, reloaded)
-//   P4  dalpha (lane reduction of dY^T o Z^T); dP and E = dL + dL^T + diag(2 dalpha dalpha/dlambda)
+//   P4  dalpha (lane reduction of -dY^T o Z^T); dP and E = dL + dL^T + diag(2 dalpha dalpha/dlambda)
 //       as bf16 hi/lo tiles
 //   P5  dQ^T += K^T dP^T;  dK^T += Q^T dP + K^T E
 //   P6  dq, dk, dbeta to HBM
@@ -26,8 +26,9 @@
 //   warps 0-7 (CUDA cores): every step above that is not a product, the two warpgroups each on
 //     half of a chunk's 64 tokens; they meet at named barrier 1 only and hand operands to the
 //     tensor core through mbarriers;
-//   warp 8 (one lane): TMA loads of K, Q, dO, bulk copies of the S and dS' tiles (written in this
-//     layout by the forward and the state pass), every tcgen05.mma and commit.
+//   warp 8 (one lane): TMA loads of K, Q, dO and -dR (the last two as bf16 hi/lo arrays), bulk
+//     copies of the S and dS' tiles (written in this layout by the forward and the state pass),
+//     every tcgen05.mma and commit.
 // Every wait is bounded; on expiry the CTA records EFLA_ERR_DEVICE_TIMEOUT and leaves.
 #include <cudaTypedefs.h>
 
@@ -52,11 +53,11 @@ constexpr int BAR_W = 1;        // named barrier of the CUDA-core warps
 // Shared memory map (bytes from a 1024-byte aligned base).  Operand tiles are bf16 with the
 // 128-byte swizzle in column blocks of 64 elements; "hi | lo" pairs are the two split parts.
 constexpr uint32_t OFF_KQ = 0;        // [K; Q]: 2 column blocks x 128 rows (K 0-63, Q 64-127), 32 KB
-constexpr uint32_t OFF_DOR = 32768;   // [dO; -dR] hi | lo: 2 column blocks x 128 rows each, 64 KB
+constexpr uint32_t OFF_DOR = 32768;   // [dO; -dR] hi | lo: 2 column blocks x 128 rows each, 64 KB; later fp32 dL [64][65]
 constexpr uint32_t OFF_SS = 98304;    // S, later dS', hi | lo: 2 column blocks x 128 rows each, 64 KB
 constexpr uint32_t OFF_W = 163840;    // T'' hi | lo [64][64] (16 KB); later dP hi | lo
-constexpr uint32_t OFF_L = 180224;    // -L hi | lo [64][64] (16 KB); later dL + dL^T hi | lo
-constexpr uint32_t OFF_UT = 196608;   // U^T hi | lo [128][64] (32 KB); before: fp32 A~ [64][68]; after: fp32 dL [64][65]
+constexpr uint32_t OFF_L = 180224;    // -L hi | lo [64][64] (16 KB); later E hi | lo
+constexpr uint32_t OFF_UT = 196608;   // U^T hi | lo [128][64] (32 KB); before: fp32 A~ [64][68]
 constexpr uint32_t OFF_ROW = 229376;  // fp32 per token: beta, invn, gn, alpha, dadb, dadl, dalpha
 constexpr uint32_t OFF_BAR = OFF_ROW + 7 * C * 4;
 constexpr uint32_t OFF_MISC = OFF_BAR + 128;  // tmem base, abort flag
@@ -73,14 +74,14 @@ static_assert(OFF_DOR % 1024 == 0 && OFF_SS % 1024 == 0 && OFF_W % 1024 == 0 && 
 static_assert(OFF_DOR == OFF_KQ + 32768 && OFF_SS == OFF_DOR + 2 * LO_128 && OFF_W == OFF_SS + 2 * LO_128 &&
                   OFF_L == OFF_W + 2 * LO_64 && OFF_UT == OFF_L + 2 * LO_64 && OFF_ROW == OFF_UT + 2 * LO_UT,
               "regions overlap");
-static_assert(C * AT_LD * 4 <= 2 * LO_UT && C * DL_LD * 4 <= 2 * LO_UT, "fp32 scratch exceeds the U^T region");
+static_assert(C * AT_LD * 4 <= 2 * LO_UT && C * DL_LD * 4 <= 2 * LO_128, "fp32 scratch exceeds its region");
 static_assert(SMEM_ALLOC <= 232448, "exceeds the per-CTA shared memory limit");
 
 // TMEM columns (fp32 unless split: bf16 pairs, hi in the first 32 columns, lo in the next 32)
 constexpr uint32_t TM_P = 0;     // [dP; -dR U^T] (64)
 constexpr uint32_t TM_X = 128;   // X^T -> R^T -> Z^T (64)
-constexpr uint32_t TM_RS = 192;  // R^T split, later dR^T split (64)
-constexpr uint32_t TM_U = 256;   // Gram -> U^T -> G^T -> dY^T (64)
+constexpr uint32_t TM_RS = 192;  // R^T split (64)
+constexpr uint32_t TM_U = 256;   // Gram -> U^T -> -G^T -> -dY^T (64)
 constexpr uint32_t TM_US = 320;  // U^T split (64)
 constexpr uint32_t TM_DQ = 384;  // dQ^T (64)
 constexpr uint32_t TM_DK = 448;  // dK^T (64), adjacent to dQ^T: one N = 128 product fills both
@@ -89,12 +90,13 @@ constexpr uint32_t TM_COLS = 512;
 constexpr uint64_t DRAIN_NS = 2000000000ull;
 
 struct GtParams {
-    CUtensorMap map_q, map_k, map_doh, map_dol;  // [B, T, H, 128] bf16: box 64 x 1 x 64 x 1, 128B swizzle
+    CUtensorMap map_q, map_k, map_doh, map_dol, map_drh, map_drl;  // [B, T, H, 128] bf16: box 64 x 1 x 64 x 1,
+                                                                   // 128B swizzle (dO, -dR as hi and lo)
     const __nv_bfloat16 *v;                      // [B, T, H, 128]
     const float *beta;                           // [B, T, H]
     const uint8_t *states, *dse;                 // [B, H, nchunks] x 64 KB: S and dS' of every chunk as
                                                  // bf16 hi/lo operand tiles (put_col_split_tile)
-    const float *g, *dr;                         // [B, T, H, 128]: G and dR (= dv) of every token
+    const float *g;                              // [B, T, H, 128]: G of every token
     float *dq, *dk, *dbeta;
     int *status;
     int T, H, items;                             // items = B H nchunks
@@ -103,10 +105,10 @@ struct GtParams {
 };
 
 struct Bars {
-    uint64_t tma;                          // K, Q, dO of the item landed
+    uint64_t tma_kq, tma_dor;              // K, Q / dO, -dR of the item landed (TMA)
     uint64_t s_full, d_full;               // the S tile / the dS' tile landed (bulk copies)
     uint64_t g, m1, u, a, b, m2;           // products complete (tcgen05.commit)
-    uint64_t w_s, w_u, w_p3, w_p5, w_free; // operands written / TMEM read by the CUDA-core warps (8 arrivals)
+    uint64_t w_u, w_p3, w_p5, w_free;      // operands written / TMEM read by the CUDA-core warps (8 arrivals)
     uint64_t drain;
 };
 static_assert(sizeof(Bars) <= 128, "mbarrier block exceeds its slot");
@@ -123,17 +125,6 @@ __device__ __forceinline__ void put16(uint8_t *tile, uint32_t lo_off, int row, i
         *reinterpret_cast<uint4 *>(tile + lo_off + off) =
             make_uint4(ll[4 * h8], ll[4 * h8 + 1], ll[4 * h8 + 2], ll[4 * h8 + 3]);
     }
-}
-
-// Four fp32 values as bf16 hi and lo at (row, col .. col + 3) of a swizzled 128-row tile with
-// two column blocks (col a multiple of 4).
-__device__ __forceinline__ void put4(uint8_t *tile, uint32_t lo_off, int row, int col, float4 v) {
-    const float x[4] = {v.x, v.y, v.z, v.w};
-    uint32_t hh[2], ll[2];
-    split_pack<2>(x, hh, ll);
-    const uint32_t off = swz_offset(row, col, 16384);
-    *reinterpret_cast<uint2 *>(tile + off) = make_uint2(hh[0], hh[1]);
-    *reinterpret_cast<uint2 *>(tile + lo_off + off) = make_uint2(ll[0], ll[1]);
 }
 
 // 32 fp32 values (this warpgroup's 32 tokens) as a TMEM A operand: bf16 pairs, hi at
@@ -190,7 +181,8 @@ __global__ void __launch_bounds__(NTH, 1) bwd_grad_tc_kernel(const __grid_consta
     const uint32_t s_sm = smem_u32(sm);
 
     if (tid == 0) {
-        mbar_init(&bars->tma, 1);
+        mbar_init(&bars->tma_kq, 1);
+        mbar_init(&bars->tma_dor, 1);
         mbar_init(&bars->s_full, 1);
         mbar_init(&bars->d_full, 1);
         mbar_init(&bars->g, 1);
@@ -199,7 +191,6 @@ __global__ void __launch_bounds__(NTH, 1) bwd_grad_tc_kernel(const __grid_consta
         mbar_init(&bars->a, 1);
         mbar_init(&bars->b, 1);
         mbar_init(&bars->m2, 1);
-        mbar_init(&bars->w_s, 8);
         mbar_init(&bars->w_u, 8);
         mbar_init(&bars->w_p3, 8);
         mbar_init(&bars->w_p5, 8);
@@ -227,9 +218,11 @@ __global__ void __launch_bounds__(NTH, 1) bwd_grad_tc_kernel(const __grid_consta
             prefetch_tensormap(&p.map_k);
             prefetch_tensormap(&p.map_doh);
             prefetch_tensormap(&p.map_dol);
+            prefetch_tensormap(&p.map_drh);
+            prefetch_tensormap(&p.map_drl);
         }
         bool ok = true;
-        int it = 0, tma_pending = -1, s_pending = -1, d_pending = -1;
+        int it = 0, kq_pending = -1, dor_pending = -1, s_pending = -1, d_pending = -1;
         auto load_tile = [&](uint64_t *bar, const uint8_t *src) {  // one 64 KB operand tile into the S tile
             if (leader) {
                 mbar_arrive_expect_tx(bar, 65536);
@@ -237,10 +230,22 @@ __global__ void __launch_bounds__(NTH, 1) bwd_grad_tc_kernel(const __grid_consta
             }
             __syncwarp();
         };
-        if (blockIdx.x < p.items) {
-            load_tile(&bars->s_full, p.states + (size_t)blockIdx.x * 65536);
-            s_pending = 0;
-        }
+        // dO and -dR of item w into rows 0-63 / 64-127 of the [dO; -dR] tile (hi and lo)
+        auto load_dor = [&](int w) {
+            if (leader) {
+                const Item I = item_of(p, w, nc);
+                mbar_arrive_expect_tx(&bars->tma_dor, 4 * 16384);
+                for (int cb = 0; cb < 2; ++cb) {
+                    uint8_t *dor_cb = sm + OFF_DOR + cb * 16384;
+                    tma_load_4d(dor_cb, &p.map_doh, &bars->tma_dor, cb * 64, I.h, I.t0, I.b);
+                    tma_load_4d(dor_cb + LO_128, &p.map_dol, &bars->tma_dor, cb * 64, I.h, I.t0, I.b);
+                    tma_load_4d(dor_cb + 8192, &p.map_drh, &bars->tma_dor, cb * 64, I.h, I.t0, I.b);
+                    tma_load_4d(dor_cb + LO_128 + 8192, &p.map_drl, &bars->tma_dor, cb * 64, I.h, I.t0, I.b);
+                }
+            }
+            __syncwarp();
+        };
+
         auto wait = [&](uint64_t *bar, int parity) {
             ok = ok && wait_bar_warp(bar, parity, abort_flag, wait_ns);
             tc_fence_after();
@@ -249,21 +254,23 @@ __global__ void __launch_bounds__(NTH, 1) bwd_grad_tc_kernel(const __grid_consta
         for (int w = blockIdx.x; w < p.items; w += gridDim.x, ++it) {
             const int ph = it & 1;
             const Item I = item_of(p, w, nc);
-            // the previous item's last products are complete: [K; Q], dO, T''/dP, -L/E are free
+            // the previous item's last products are complete: every operand tile is free
             if (it > 0 && !wait(&bars->m2, ph ^ 1)) break;
             if (leader) {
-                mbar_arrive_expect_tx(&bars->tma, 4 * 16384);
+                mbar_arrive_expect_tx(&bars->tma_kq, 2 * 16384);
                 for (int cb = 0; cb < 2; ++cb) {
-                    tma_load_4d(sm + OFF_KQ + cb * 16384, &p.map_k, &bars->tma, cb * 64, I.h, I.t0, I.b);
-                    tma_load_4d(sm + OFF_KQ + cb * 16384 + 8192, &p.map_q, &bars->tma, cb * 64, I.h, I.t0, I.b);
-                    tma_load_4d(sm + OFF_DOR + cb * 16384, &p.map_doh, &bars->tma, cb * 64, I.h, I.t0, I.b);
-                    tma_load_4d(sm + OFF_DOR + LO_128 + cb * 16384, &p.map_dol, &bars->tma, cb * 64, I.h, I.t0, I.b);
+                    tma_load_4d(sm + OFF_KQ + cb * 16384, &p.map_k, &bars->tma_kq, cb * 64, I.h, I.t0, I.b);
+                    tma_load_4d(sm + OFF_KQ + cb * 16384 + 8192, &p.map_q, &bars->tma_kq, cb * 64, I.h, I.t0, I.b);
                 }
             }
-            tma_pending = ph;
+            kq_pending = ph;
             __syncwarp();
-            if (!wait(&bars->tma, ph)) break;
-            tma_pending = -1;
+            load_tile(&bars->s_full, p.states + (size_t)w * 65536);  // queued behind K and Q: the Gram needs only those
+            s_pending = ph;
+            load_dor(w);
+            dor_pending = ph;
+            if (!wait(&bars->tma_kq, ph)) break;
+            kq_pending = -1;
             if (leader) {  // Gram K K^T (rows 64-127 of the M = 128 product are Q K^T, unused)
                 const uint32_t idesc = idesc_bf16_f32(128, 64, 0, 0);
 #pragma unroll 1
@@ -274,23 +281,24 @@ __global__ void __launch_bounds__(NTH, 1) bwd_grad_tc_kernel(const __grid_consta
                 mma_commit(&bars->g);
             }
             __syncwarp();
-            // the S tile and -dR rows are written; the previous item's dQ^T and dK^T are read out
-            if (!wait(&bars->w_s, ph)) break;
-            if (it > 0 && !wait(&bars->w_free, ph ^ 1)) break;
             if (!wait(&bars->s_full, ph)) break;
             s_pending = -1;
+            if (leader) {  // X^T = S^T K^T: S^T read as an MN-major A (M = j), K = i
+                const uint32_t idesc = idesc_bf16_f32(128, 64, 1, 0);
+#pragma unroll 1
+                for (int part = 0; part < 2; ++part)
+#pragma unroll 1
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint32_t boff = (ks >> 2) * 16384 + (ks & 3) * 32;
+                        mma_bf16(tmem + TM_X, smem_desc(ss + part * LO_128 + ks * 2048, 16384, 1024),
+                                 smem_desc(kq + boff, 16, 1024), idesc, (part | ks) != 0);
+                    }
+            }
+            __syncwarp();
+            if (!wait(&bars->tma_dor, ph)) break;
+            dor_pending = -1;
+            if (it > 0 && !wait(&bars->w_free, ph ^ 1)) break;  // the previous dQ^T and dK^T are read out
             if (leader) {
-                {  // X^T = S^T K^T: S^T read as an MN-major A (M = j), K = i
-                    const uint32_t idesc = idesc_bf16_f32(128, 64, 1, 0);
-#pragma unroll 1
-                    for (int part = 0; part < 2; ++part)
-#pragma unroll 1
-                        for (int ks = 0; ks < 8; ++ks) {
-                            const uint32_t boff = (ks >> 2) * 16384 + (ks & 3) * 32;
-                            mma_bf16(tmem + TM_X, smem_desc(ss + part * LO_128 + ks * 2048, 16384, 1024),
-                                     smem_desc(kq + boff, 16, 1024), idesc, (part | ks) != 0);
-                        }
-                }
                 {  // [dQ^T | dK^T] = S [dO; -dR]^T: one N = 128 product, K = j
                     const uint32_t idesc = idesc_bf16_f32(128, 128, 0, 0);
 #pragma unroll 1
@@ -323,7 +331,7 @@ __global__ void __launch_bounds__(NTH, 1) bwd_grad_tc_kernel(const __grid_consta
                 mma_commit(&bars->u);
             }
             __syncwarp();
-            if (!wait(&bars->w_p3, ph)) break;  // U^T split and tile, G^T, dR^T split written
+            if (!wait(&bars->w_p3, ph)) break;  // U^T split and tile, -G^T written
             if (!wait(&bars->d_full, ph)) break;
             d_pending = -1;
             if (leader) {
@@ -337,39 +345,45 @@ __global__ void __launch_bounds__(NTH, 1) bwd_grad_tc_kernel(const __grid_consta
                         mma_bf16_ts(tmem + TM_X, tmem + TM_US + 32 + ks * 8, bh, idesc, 1);
                     }
                 }
-                {  // dY^T += dR^T (-L): A = dR^T split (TMEM), B[t][s] = -L[s][t] (MN-major)
-                    const uint32_t idesc = idesc_bf16_f32(128, 64, 0, 1);
+                {  // -dY^T += (-dR)^T (-L): A[j][s] = -dR[s][j] (rows 64-127 of the [dO; -dR] tile, MN-major),
+                   // B[t][s] = -L[s][t] (MN-major)
+                    const uint32_t idesc = idesc_bf16_f32(128, 64, 1, 1);
 #pragma unroll 1
                     for (int ks = 0; ks < 4; ++ks) {
+                        const uint64_t ah = smem_desc(dor + 8192 + ks * 2048, 16384, 1024);
+                        const uint64_t al = smem_desc(dor + LO_128 + 8192 + ks * 2048, 16384, 1024);
                         const uint64_t bh = smem_desc(l + ks * 2048, 8192, 1024), bl = smem_desc(l + LO_64 + ks * 2048, 8192, 1024);
-                        mma_bf16_ts(tmem + TM_U, tmem + TM_RS + ks * 8, bh, idesc, 1);
-                        mma_bf16_ts(tmem + TM_U, tmem + TM_RS + ks * 8, bl, idesc, 1);
-                        mma_bf16_ts(tmem + TM_U, tmem + TM_RS + 32 + ks * 8, bh, idesc, 1);
+                        mma_bf16(tmem + TM_U, ah, bh, idesc, 1);
+                        mma_bf16(tmem + TM_U, ah, bl, idesc, 1);
+                        mma_bf16(tmem + TM_U, al, bh, idesc, 1);
                     }
                 }
                 mma_commit(&bars->a);
-                {  // [dP; -dR U^T] = [dO; -dR] U^T and dK^T += dS' U^T: B[t][j] = U^T[j][t] (MN-major), K = j
-                    const uint32_t idesc = idesc_bf16_f32(128, 64, 0, 1);
+                // [dP; -dR U^T] = [dO; -dR] U^T, then dK^T += dS' U^T: B[t][j] = U^T[j][t] (MN-major), K = j
+                const uint32_t idesc = idesc_bf16_f32(128, 64, 0, 1);
 #pragma unroll 1
-                    for (int pr = 0; pr < 3; ++pr) {  // hi x hi, hi x lo, lo x hi
-                        const uint32_t a_lo = pr == 2 ? LO_128 : 0, b_lo = pr == 1 ? LO_UT : 0;
+                for (int pr = 0; pr < 3; ++pr) {  // hi x hi, hi x lo, lo x hi
+                    const uint32_t a_lo = pr == 2 ? LO_128 : 0, b_lo = pr == 1 ? LO_UT : 0;
 #pragma unroll 1
-                        for (int ks = 0; ks < 8; ++ks) {
-                            const uint32_t aoff = a_lo + (ks >> 2) * 16384 + (ks & 3) * 32;
-                            const uint64_t bd = smem_desc(ut + b_lo + ks * 2048, 8192, 1024);
-                            mma_bf16(tmem + TM_P, smem_desc(dor + aoff, 16, 1024), bd, idesc, (pr | ks) != 0);
-                            mma_bf16(tmem + TM_DK, smem_desc(ss + aoff, 16, 1024), bd, idesc, 1);
-                        }
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint32_t aoff = a_lo + (ks >> 2) * 16384 + (ks & 3) * 32;
+                        mma_bf16(tmem + TM_P, smem_desc(dor + aoff, 16, 1024), smem_desc(ut + b_lo + ks * 2048, 8192, 1024),
+                                 idesc, (pr | ks) != 0);
                     }
                 }
                 mma_commit(&bars->b);
+#pragma unroll 1
+                for (int pr = 0; pr < 3; ++pr) {
+                    const uint32_t a_lo = pr == 2 ? LO_128 : 0, b_lo = pr == 1 ? LO_UT : 0;
+#pragma unroll 1
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint32_t aoff = a_lo + (ks >> 2) * 16384 + (ks & 3) * 32;
+                        mma_bf16(tmem + TM_DK, smem_desc(ss + aoff, 16, 1024), smem_desc(ut + b_lo + ks * 2048, 8192, 1024),
+                                 idesc, 1);
+                    }
+                }
             }
             __syncwarp();
-            if (w + (int)gridDim.x < p.items) {  // the dS' tile is read: the next item's S replaces it
-                if (!wait(&bars->b, ph)) break;
-                load_tile(&bars->s_full, p.states + (size_t)(w + gridDim.x) * 65536);
-                s_pending = ph ^ 1;
-            }
             if (!wait(&bars->w_p5, ph)) break;  // dP and E tiles written
             if (leader) {  // dQ^T += K^T dP^T;  dK^T += Q^T dP + K^T E
                 const uint32_t id_kn = idesc_bf16_f32(128, 64, 1, 0), id_mn = idesc_bf16_f32(128, 64, 1, 1);
@@ -394,7 +408,10 @@ __global__ void __launch_bounds__(NTH, 1) bwd_grad_tc_kernel(const __grid_consta
             const uint64_t ts = globaltimer_ns();
             while (!mbar_try_wait_sleep(&bars->drain, 0, 20000) && globaltimer_ns() - ts < DRAIN_NS) {
             }
-            while (tma_pending >= 0 && !mbar_try_wait_sleep(&bars->tma, tma_pending, 20000) &&
+            while (kq_pending >= 0 && !mbar_try_wait_sleep(&bars->tma_kq, kq_pending, 20000) &&
+                   globaltimer_ns() - ts < DRAIN_NS) {
+            }
+            while (dor_pending >= 0 && !mbar_try_wait_sleep(&bars->tma_dor, dor_pending, 20000) &&
                    globaltimer_ns() - ts < DRAIN_NS) {
             }
             while (s_pending >= 0 && !mbar_try_wait_sleep(&bars->s_full, s_pending, 20000) &&
@@ -410,7 +427,7 @@ __global__ void __launch_bounds__(NTH, 1) bwd_grad_tc_kernel(const __grid_consta
         float *row_invn = reinterpret_cast<float *>(sm + OFF_ROW), *row_gn = row_invn + C, *row_al = row_gn + C;
         float *row_dadb = row_al + C, *row_dadl = row_dadb + C, *row_dal = row_dadl + C;
         float *At = reinterpret_cast<float *>(sm + OFF_UT);   // A~, then T~ (P0)
-        float *dLs = reinterpret_cast<float *>(sm + OFF_UT);  // dL (P4)
+        float *dLs = reinterpret_cast<float *>(sm + OFF_DOR);  // dL (P4)
         // TMEM: this thread reads and writes lane `ln` (its warp's quarter), the columns of token half `hf`
         const int hf = warp >> 2, ln = (warp & 3) * 32 + lane;
         const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
@@ -434,23 +451,8 @@ __global__ void __launch_bounds__(NTH, 1) bwd_grad_tc_kernel(const __grid_consta
             const Item I = item_of(p, w, nc);
             const int valid = I.valid;
             const size_t row0 = I.row0;
-            // ------------------------------ -dR rows ------------------------------
             const float bt = gate_thr && ln < valid ? p.beta[row0 + (size_t)ln * p.H] : 0.f;
-            if (ok) {
-                const int jc = lane * 4;
-                float4 y[8];  // -dR -> rows 64-127 of the [dO; -dR] tile (loads as for V^T)
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    y[e] = __ldcg(reinterpret_cast<const float4 *>(p.dr + (row0 + (size_t)min(e * 8 + warp, valid - 1) * p.H) * D + jc));
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const bool in = e * 8 + warp < valid;
-                    put4(sm + OFF_DOR, LO_128, C + e * 8 + warp, jc,
-                         in ? make_float4(-y[e].x, -y[e].y, -y[e].z, -y[e].w) : make_float4(0.f, 0.f, 0.f, 0.f));
-                }
-            }
             if (tid < C) row_dal[tid] = 0.f;  // (read by this thread only, in the previous item's dbeta)
-            hand_over(&bars->w_s);
             // ------------------------------ P0: gate terms, -L, T'' ------------------------------
             wait(&bars->g, ph);
             if (ok && ln < C) {  // row t = ln of K K^T, this half's 32 columns (warps 0, 1, 4, 5)
@@ -502,6 +504,7 @@ __global__ void __launch_bounds__(NTH, 1) bwd_grad_tc_kernel(const __grid_consta
                 put16(sm + OFF_W, LO_64, t, s0, x);
             }
             // ------------------------------ P2: R^T, dS' ------------------------------
+            float gt[32];
             wait(&bars->m1, ph);  // X^T complete
             if (ok) {
                 // V^T: rows past the chunk's end load its last row (always in bounds) and are zeroed
@@ -510,6 +513,9 @@ __global__ void __launch_bounds__(NTH, 1) bwd_grad_tc_kernel(const __grid_consta
                 __nv_bfloat16 vr[32];
 #pragma unroll
                 for (int e = 0; e < 32; ++e) vr[e] = __ldcg(vc + (size_t)min(32 * hf + e, valid - 1) * p.H * D);
+                // -G^T of this lane and token half (loads as for V^T), kept for P3
+#pragma unroll
+                for (int e = 0; e < 32; ++e) gt[e] = __ldcg(p.g + (row0 + (size_t)min(32 * hf + e, valid - 1) * p.H) * D + ln);
                 float r[32];
 #pragma unroll
                 for (int e = 0; e < 32; ++e) r[e] = 32 * hf + e < valid ? __bfloat162float(vr[e]) : 0.f;
@@ -525,26 +531,15 @@ __global__ void __launch_bounds__(NTH, 1) bwd_grad_tc_kernel(const __grid_consta
             // ------------------------------ P3 operands ------------------------------
             wait(&bars->u, ph);
             if (ok) {
-                float gt[32], drt[32];  // G^T and dR^T of this lane and token half (loads as for V^T)
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const size_t o = (row0 + (size_t)min(32 * hf + e, valid - 1) * p.H) * D + ln;
-                    gt[e] = __ldcg(p.g + o);
-                    drt[e] = __ldcg(p.dr + o);
-                }
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    gt[e] = 32 * hf + e < valid ? gt[e] : 0.f;
-                    drt[e] = 32 * hf + e < valid ? drt[e] : 0.f;
-                }
+                for (int e = 0; e < 32; ++e) gt[e] = 32 * hf + e < valid ? -gt[e] : 0.f;
                 float u[32];
                 tmem_ld32(lane_base + TM_U + 32 * hf, u);
                 tmem_ld_wait();
                 tsplit32(lane_base, TM_US, hf, u);
                 put16(sm + OFF_UT, LO_UT, ln, 32 * hf, u);
                 put16(sm + OFF_UT, LO_UT, ln, 32 * hf + 16, u + 16);
-                tmem_st32(lane_base + TM_U + 32 * hf, gt);  // G^T over U^T (read above)
-                tsplit32(lane_base, TM_RS, hf, drt);        // dR^T split over R^T's (its product is complete)
+                tmem_st32(lane_base + TM_U + 32 * hf, gt);  // -G^T over U^T (read above)
             }
             hand_over(&bars->w_p3);
             // ------------------------------ P4 ------------------------------
@@ -555,7 +550,7 @@ __global__ void __launch_bounds__(NTH, 1) bwd_grad_tc_kernel(const __grid_consta
                 tmem_ld32(lane_base + TM_X + 32 * hf, z);
                 tmem_ld_wait();
 #pragma unroll
-                for (int e = 0; e < 32; ++e) y[e] *= z[e];
+                for (int e = 0; e < 32; ++e) y[e] *= -z[e];  // TM_U holds -dY^T
                 atomicAdd(&row_dal[32 * hf + lane], lane_reduce_scatter(y, lane));
             }
             wait(&bars->b, ph);
@@ -620,18 +615,20 @@ __global__ void __launch_bounds__(NTH, 1) bwd_grad_tc_kernel(const __grid_consta
 }  // namespace
 
 // Per-chunk gradients on the tensor cores: bf16 q, k, v, d_k = d_v = 128, T > 0, after
-// launch_bwd_state_tc (dse, G in g, dR in a.dv, dO split in do_split).  Persistent: one CTA per
+// launch_bwd_state_tc (dse, G in g, -dR split in dr_split, dO split in do_split).  Persistent: one CTA per
 // SM at most, each walking items blockIdx.x, blockIdx.x + gridDim.x, ...
 cudaError_t launch_bwd_grad_tc(const BwdArgs &a, const float *states, const float *dse, const void *do_split,
-                               const float *g, const char **why) {
+                               const float *g, const void *dr_split, const char **why) {
     const long items = (long)a.B * a.H * ((a.T + C - 1) / C);
     if (items == 0) return cudaSuccess;
     const size_t n = (size_t)a.B * a.T * a.H * D;
     const __nv_bfloat16 *hi = static_cast<const __nv_bfloat16 *>(do_split), *lo = hi + n;
+    const __nv_bfloat16 *rhi = static_cast<const __nv_bfloat16 *>(dr_split), *rlo = rhi + n;
     GtParams p;
     memset(&p, 0, sizeof p);
     if (!bwd_row_map(&p.map_q, a.q, a.B, a.T, a.H) || !bwd_row_map(&p.map_k, a.k, a.B, a.T, a.H) ||
-        !bwd_row_map(&p.map_doh, hi, a.B, a.T, a.H) || !bwd_row_map(&p.map_dol, lo, a.B, a.T, a.H)) {
+        !bwd_row_map(&p.map_doh, hi, a.B, a.T, a.H) || !bwd_row_map(&p.map_dol, lo, a.B, a.T, a.H) ||
+        !bwd_row_map(&p.map_drh, rhi, a.B, a.T, a.H) || !bwd_row_map(&p.map_drl, rlo, a.B, a.T, a.H)) {
         *why = "cuTensorMapEncodeTiled failed";
         return cudaErrorInvalidValue;
     }
@@ -640,7 +637,6 @@ cudaError_t launch_bwd_grad_tc(const BwdArgs &a, const float *states, const floa
     p.states = reinterpret_cast<const uint8_t *>(states);
     p.dse = reinterpret_cast<const uint8_t *>(dse);
     p.g = g;
-    p.dr = a.dv;
     p.dq = a.dq;
     p.dk = a.dk;
     p.dbeta = a.dbeta;

@@ -80,6 +80,7 @@ struct BtParams {
                                                  // operand tiles (put_col_split_tile)
     float *dS0;                                  // [B, H, 128, 128] or nullptr
     float *g_out, *dr_out;                       // [B, T, H, 128] fp32: G and dR (= dv) of every token
+    __nv_bfloat16 *drs_hi, *drs_lo;              // [B, T, H, 128]: -dR as bf16 hi and lo
     int *status;
     int B, T, H;
     int euler;
@@ -375,6 +376,9 @@ __global__ void __launch_bounds__(448, 1) bwd_tc_kernel(const __grid_constant__ 
             tc_fence_before();
             mbar_arrive(&bars->u_ready);
             store_cols(p.dr_out + row0 * D + j, (size_t)p.H * D, valid, x0, x1);  // dv = dR
+            // -dR as bf16 hi/lo for the per-chunk gradient kernel
+            put_col_split_rows(p.drs_hi + row0 * D, p.drs_lo + row0 * D, (size_t)p.H * D, valid, 0, j, -1.f, x0);
+            put_col_split_rows(p.drs_hi + row0 * D, p.drs_lo + row0 * D, (size_t)p.H * D, valid, 32, j, -1.f, x1);
         }
         if (ok) {  // dS0: the gradient of the first chunk's start state
             ok = wait_bar_warp(&bars->s_done, (nchunks - 1) & 1, abort_flag, wait_ns);
@@ -574,7 +578,8 @@ bool bwd_row_map(CUtensorMap *m, const void *ptr, int B, int T, int H) {
 // State gradients of the chunked backward on the tensor cores: bf16 q, k, d_k = d_v = 128,
 // T > 0.  do_split: 2 x B*T*H*128 bf16 of scratch (dO hi, then lo); g_out: B*T*H*128 fp32
 // (G of every token); dv receives dR.
-cudaError_t launch_bwd_state_tc(const BwdArgs &a, float *dse, void *do_split, float *g_out, const char **why) {
+cudaError_t launch_bwd_state_tc(const BwdArgs &a, float *dse, void *do_split, float *g_out, void *dr_split,
+                                const char **why) {
     const size_t n = (size_t)a.B * a.T * a.H * D;
     __nv_bfloat16 *hi = static_cast<__nv_bfloat16 *>(do_split), *lo = hi + n;
     int dev = 0, sms = 0;
@@ -605,6 +610,8 @@ cudaError_t launch_bwd_state_tc(const BwdArgs &a, float *dse, void *do_split, fl
     p.dS0 = a.dS0;
     p.g_out = g_out;
     p.dr_out = a.dv;
+    p.drs_hi = static_cast<__nv_bfloat16 *>(dr_split);
+    p.drs_lo = p.drs_hi + n;
     p.status = device_status_ptr();
     p.B = a.B;
     p.T = a.T;

@@ -80,6 +80,26 @@ __device__ __forceinline__ void put_col_split_tile(uint8_t *tile, int row0, int 
     }
 }
 
+// Tokens t0 .. t0 + 31 (x) of column j (this lane) of a [token][128] block, times `sign`, as
+// bf16 hi and lo (the split above) into two arrays of that shape whose token rows are `stride`
+// elements apart (hi and lo point at token 0, column 0); tokens at or past `valid` are not
+// written.  Lanes j and j ^ 1 pair up as in put_col_split_tile: the even lane stores the hi
+// word, the odd lane the lo word.
+__device__ __forceinline__ void put_col_split_rows(__nv_bfloat16 *hi, __nv_bfloat16 *lo, size_t stride, int valid,
+                                                   int t0, int j, float sign, const float (&x)[32]) {
+    const bool odd = (j & 1) != 0;
+    uint32_t *dst = reinterpret_cast<uint32_t *>(odd ? lo + (j - 1) : hi + j);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const float v = sign * x[i];
+        const uint32_t b = __float_as_uint(v);
+        const uint32_t h16 = b >> 16;
+        const uint32_t l16 = __float_as_uint(v - __uint_as_float(b & 0xffff0000u)) >> 16;
+        const uint32_t recv = __shfl_xor_sync(0xffffffffu, odd ? h16 : l16, 1);
+        if (t0 + i < valid) dst[(size_t)(t0 + i) * stride / 2] = odd ? (recv | (l16 << 16)) : (h16 | (recv << 16));
+    }
+}
+
 }  // namespace
 }  // namespace tc
 }  // namespace efla

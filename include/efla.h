@@ -45,7 +45,7 @@
 extern "C" {
 #endif
 
-#define EFLA_ABI_VERSION 8
+#define EFLA_ABI_VERSION 9
 
 typedef enum {
     EFLA_OK = 0,
@@ -233,14 +233,15 @@ efla_status efla_bwd_recurrent(const void *q, const void *k, const void *v, cons
  * Parallelism"; "Exact Flow Linear Attention" (gist.science), Metodologia 3).  Three steps
  * on `stream`: the forward, writing the state at the start of every chunk into the
  * workspace; one CTA per (b, h) that walks the chunks in reverse for the gradient of each
- * chunk's end state (also into the workspace); then one CTA per (b, h, chunk), all
+ * chunk's end state (also into the workspace); then the (b, h, chunk) items, all
  * independent, for every token's gradients (fp32 on CUDA cores).  For bf16 inputs with
- * d = 128 the first two steps run on the tensor cores (split-bf16 operands, fp32
- * accumulation), after a pass that writes dO as bf16 hi and lo parts into the workspace.
+ * d = 128 all three steps run on the tensor cores (split-bf16 operands, fp32 accumulation;
+ * the last on persistent CTAs), after a pass that writes dO as bf16 hi and lo parts into the
+ * workspace; the second also writes G and -dR (bf16 hi and lo) of every token there.
  *
  *   workspace  device scratch owned by the caller, 16-byte aligned, at least the size
  *              efla_bwd_workspace reports (2 x B x H x ceil(T/64) x d_k x d_v x 4 bytes
- *              + B x T x H x d_v x 8 bytes);
+ *              + B x T x H x d_v x 12 bytes);
  *              it must not overlap any argument.  Too small or NULL: EFLA_ERR_INVALID_ARG.
  * Supported: d_k = d_v in {64, 128} (other sizes: EFLA_ERR_UNSUPPORTED, use
  * efla_bwd_recurrent).
