@@ -13,7 +13,8 @@
 //   dbeta = dalpha (dalpha/dbeta)
 // All products run on the tensor core in the transposed orientation (TMEM lane = feature),
 // every operand that is not an exact bf16 input split into bf16 hi + lo (fp32 accumulation):
-//   P0  Gram K K^T (TMEM); gate terms, A~, blocked inverse; T'' and -L as bf16 hi/lo tiles
+//   P0  Gram K K^T (TMEM); gate terms; -L as a bf16 hi/lo tile (T'' is the forward's, loaded whole;
+//       a zero key's diagonal entry, 0 there, is set to alpha_t here)
 //   P1  X^T = S^T K^T;  [dQ^T | dK^T] = S [dO; -dR]^T            (S: a swizzled bf16 tile)
 //   P2  R^T = V^T - X^T (TMEM);  U^T = R^T T''^T
 //   P3  Z^T = R^T + U^T (-L)^T;  -dY^T = -G^T + (-dR)^T (-L)        ((-dR)^T read from the tile)
@@ -37,7 +38,6 @@
 #include "internal.cuh"
 #include "ptx.cuh"
 #include "tc_common.cuh"
-#include "tri_inverse.cuh"
 
 namespace efla {
 namespace {
@@ -55,15 +55,14 @@ constexpr int BAR_W = 1;        // named barrier of the CUDA-core warps
 constexpr uint32_t OFF_KQ = 0;        // [K; Q]: 2 column blocks x 128 rows (K 0-63, Q 64-127), 32 KB
 constexpr uint32_t OFF_DOR = 32768;   // [dO; -dR] hi | lo: 2 column blocks x 128 rows each, 64 KB; later fp32 dL [64][65]
 constexpr uint32_t OFF_SS = 98304;    // S, later dS', hi | lo: 2 column blocks x 128 rows each, 64 KB
-constexpr uint32_t OFF_W = 163840;    // T'' hi | lo [64][64] (16 KB); later dP hi | lo
+constexpr uint32_t OFF_W = 163840;    // T'' hi | lo [64][64] (16 KB, the forward's); later dP hi | lo
 constexpr uint32_t OFF_L = 180224;    // -L hi | lo [64][64] (16 KB); later E hi | lo
-constexpr uint32_t OFF_UT = 196608;   // U^T hi | lo [128][64] (32 KB); before: fp32 A~ [64][68]
-constexpr uint32_t OFF_ROW = 229376;  // fp32 per token: beta, invn, gn, alpha, dadb, dadl, dalpha
-constexpr uint32_t OFF_BAR = OFF_ROW + 7 * C * 4;
-constexpr uint32_t OFF_MISC = OFF_BAR + 128;  // tmem base, abort flag
+constexpr uint32_t OFF_UT = 196608;   // U^T hi | lo [128][64] (32 KB)
+constexpr uint32_t OFF_ROW = 229376;  // fp32 per token: dalpha/dbeta, dalpha/dlambda, dalpha
+constexpr uint32_t OFF_BAR = OFF_ROW + 3 * C * 4;
+constexpr uint32_t OFF_MISC = OFF_BAR + 256;  // tmem base, abort flag
 constexpr uint32_t SMEM_USED = OFF_MISC + 16;
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;
-constexpr int AT_LD = 68;
 constexpr int DL_LD = 65;
 constexpr uint32_t LO_128 = 32768;  // lo part after hi in the 128 x 128 tiles
 constexpr uint32_t LO_UT = 16384;   // ... in the U^T tile
@@ -74,7 +73,7 @@ static_assert(OFF_DOR % 1024 == 0 && OFF_SS % 1024 == 0 && OFF_W % 1024 == 0 && 
 static_assert(OFF_DOR == OFF_KQ + 32768 && OFF_SS == OFF_DOR + 2 * LO_128 && OFF_W == OFF_SS + 2 * LO_128 &&
                   OFF_L == OFF_W + 2 * LO_64 && OFF_UT == OFF_L + 2 * LO_64 && OFF_ROW == OFF_UT + 2 * LO_UT,
               "regions overlap");
-static_assert(C * AT_LD * 4 <= 2 * LO_UT && C * DL_LD * 4 <= 2 * LO_128, "fp32 scratch exceeds its region");
+static_assert(C * DL_LD * 4 <= 2 * LO_128, "fp32 scratch exceeds its region");
 static_assert(SMEM_ALLOC <= 232448, "exceeds the per-CTA shared memory limit");
 
 // TMEM columns (fp32 unless split: bf16 pairs, hi in the first 32 columns, lo in the next 32)
@@ -96,6 +95,7 @@ struct GtParams {
     const float *beta;                           // [B, T, H]
     const uint8_t *states, *dse;                 // [B, H, nchunks] x 64 KB: S and dS' of every chunk as
                                                  // bf16 hi/lo operand tiles (put_col_split_tile)
+    const uint8_t *tpp;                          // [B, H, nchunks] x 16 KB: the forward's T'' tiles
     const float *g;                              // [B, T, H, 128]: G of every token
     float *dq, *dk, *dbeta;
     int *status;
@@ -106,12 +106,12 @@ struct GtParams {
 
 struct Bars {
     uint64_t tma_kq, tma_dor;              // K, Q / dO, -dR of the item landed (TMA)
-    uint64_t s_full, d_full;               // the S tile / the dS' tile landed (bulk copies)
-    uint64_t g, m1, u, a, b, m2;           // products complete (tcgen05.commit)
+    uint64_t s_full, d_full, t_full;       // the S / dS' / T'' tile landed (bulk copies)
+    uint64_t g, m1a, m1b, u, a, b, m2;     // products complete (tcgen05.commit)
     uint64_t w_u, w_p3, w_p5, w_free;      // operands written / TMEM read by the CUDA-core warps (8 arrivals)
     uint64_t drain;
 };
-static_assert(sizeof(Bars) <= 128, "mbarrier block exceeds its slot");
+static_assert(sizeof(Bars) <= 256, "mbarrier block exceeds its slot");
 
 // x[0..15] as bf16 hi and lo of row `row`, columns col0 .. col0 + 15 (col0 + 15 < 64) of a
 // swizzled tile (hi at `tile`, lo at tile + lo_off).
@@ -185,8 +185,10 @@ __global__ void __launch_bounds__(NTH, 1) bwd_grad_tc_kernel(const __grid_consta
         mbar_init(&bars->tma_dor, 1);
         mbar_init(&bars->s_full, 1);
         mbar_init(&bars->d_full, 1);
+        mbar_init(&bars->t_full, 1);
         mbar_init(&bars->g, 1);
-        mbar_init(&bars->m1, 1);
+        mbar_init(&bars->m1a, 1);
+        mbar_init(&bars->m1b, 1);
         mbar_init(&bars->u, 1);
         mbar_init(&bars->a, 1);
         mbar_init(&bars->b, 1);
@@ -222,11 +224,11 @@ __global__ void __launch_bounds__(NTH, 1) bwd_grad_tc_kernel(const __grid_consta
             prefetch_tensormap(&p.map_drl);
         }
         bool ok = true;
-        int it = 0, kq_pending = -1, dor_pending = -1, s_pending = -1, d_pending = -1;
-        auto load_tile = [&](uint64_t *bar, const uint8_t *src) {  // one 64 KB operand tile into the S tile
+        int it = 0, kq_pending = -1, dor_pending = -1, s_pending = -1, d_pending = -1, t_pending = -1;
+        auto load_tile = [&](uint64_t *bar, uint32_t off, const uint8_t *src, uint32_t bytes) {  // a whole operand tile
             if (leader) {
-                mbar_arrive_expect_tx(bar, 65536);
-                bulk_load(sm + OFF_SS, src, 65536, bar);
+                mbar_arrive_expect_tx(bar, bytes);
+                bulk_load(sm + off, src, bytes, bar);
             }
             __syncwarp();
         };
@@ -265,8 +267,11 @@ __global__ void __launch_bounds__(NTH, 1) bwd_grad_tc_kernel(const __grid_consta
             }
             kq_pending = ph;
             __syncwarp();
-            load_tile(&bars->s_full, p.states + (size_t)w * 65536);  // queued behind K and Q: the Gram needs only those
+            // queued behind K and Q (the Gram needs only those), in the order of their first use
+            load_tile(&bars->s_full, OFF_SS, p.states + (size_t)w * 65536, 65536);
             s_pending = ph;
+            load_tile(&bars->t_full, OFF_W, p.tpp + (size_t)w * 16384, 16384);
+            t_pending = ph;
             load_dor(w);
             dor_pending = ph;
             if (!wait(&bars->tma_kq, ph)) break;
@@ -293,6 +298,7 @@ __global__ void __launch_bounds__(NTH, 1) bwd_grad_tc_kernel(const __grid_consta
                         mma_bf16(tmem + TM_X, smem_desc(ss + part * LO_128 + ks * 2048, 16384, 1024),
                                  smem_desc(kq + boff, 16, 1024), idesc, (part | ks) != 0);
                     }
+                mma_commit(&bars->m1a);
             }
             __syncwarp();
             if (!wait(&bars->tma_dor, ph)) break;
@@ -312,13 +318,13 @@ __global__ void __launch_bounds__(NTH, 1) bwd_grad_tc_kernel(const __grid_consta
                         }
                     }
                 }
-                mma_commit(&bars->m1);
+                mma_commit(&bars->m1b);
             }
             __syncwarp();
-            if (!wait(&bars->m1, ph)) break;  // the S tile is read: dS' replaces it
-            load_tile(&bars->d_full, p.dse + (size_t)w * 65536);
+            if (!wait(&bars->m1b, ph)) break;  // the S tile is read: dS' replaces it
+            load_tile(&bars->d_full, OFF_SS, p.dse + (size_t)w * 65536, 65536);
             d_pending = ph;
-            if (!wait(&bars->w_u, ph)) break;  // T'' tile and R^T split written
+            if (!wait(&bars->w_u, ph)) break;  // R^T split written, zero keys' T'' entries set (after t_full)
             if (leader) {  // U^T = R^T T''^T: A = R^T split (TMEM), B[t][s] = T''[t][s] (K-major)
                 const uint32_t idesc = idesc_bf16_f32(128, 64, 0, 0);
 #pragma unroll 1
@@ -420,13 +426,14 @@ __global__ void __launch_bounds__(NTH, 1) bwd_grad_tc_kernel(const __grid_consta
             while (d_pending >= 0 && !mbar_try_wait_sleep(&bars->d_full, d_pending, 20000) &&
                    globaltimer_ns() - ts < DRAIN_NS) {
             }
+            while (t_pending >= 0 && !mbar_try_wait_sleep(&bars->t_full, t_pending, 20000) &&
+                   globaltimer_ns() - ts < DRAIN_NS) {
+            }
         }
         __syncwarp();
     } else {
         // ============================ CUDA-core warps ============================
-        float *row_invn = reinterpret_cast<float *>(sm + OFF_ROW), *row_gn = row_invn + C, *row_al = row_gn + C;
-        float *row_dadb = row_al + C, *row_dadl = row_dadb + C, *row_dal = row_dadl + C;
-        float *At = reinterpret_cast<float *>(sm + OFF_UT);   // A~, then T~ (P0)
+        float *row_dadb = reinterpret_cast<float *>(sm + OFF_ROW), *row_dadl = row_dadb + C, *row_dal = row_dadl + C;
         float *dLs = reinterpret_cast<float *>(sm + OFF_DOR);  // dL (P4)
         // TMEM: this thread reads and writes lane `ln` (its warp's quarter), the columns of token half `hf`
         const int hf = warp >> 2, ln = (warp & 3) * 32 + lane;
@@ -453,8 +460,10 @@ __global__ void __launch_bounds__(NTH, 1) bwd_grad_tc_kernel(const __grid_consta
             const size_t row0 = I.row0;
             const float bt = gate_thr && ln < valid ? p.beta[row0 + (size_t)ln * p.H] : 0.f;
             if (tid < C) row_dal[tid] = 0.f;  // (read by this thread only, in the previous item's dbeta)
-            // ------------------------------ P0: gate terms, -L, T'' ------------------------------
+            // ------------------------------ P0: gate terms, -L ------------------------------
             wait(&bars->g, ph);
+            bool zero_key = false;  // this gate thread's key is zero: T''[t][t] = alpha_t (the forward has 0)
+            float alpha = 0.f;
             if (ok && ln < C) {  // row t = ln of K K^T, this half's 32 columns (warps 0, 1, 4, 5)
                 const int t = ln, col0 = 32 * hf;
                 float g[32];
@@ -464,48 +473,30 @@ __global__ void __launch_bounds__(NTH, 1) bwd_grad_tc_kernel(const __grid_consta
                     float lam = 0.f;
 #pragma unroll
                     for (int s = 0; s < 32; ++s) lam = (s == (t & 31)) ? g[s] : lam;
-                    const bool live = t < valid && lam > 0.f;
-                    const float in = live ? rsqrtf(lam) : 0.f;
-                    const float gam = !live ? 0.f : p.euler ? bt * lam : -expm1f(-bt * lam);
                     float db = 0.f, dl = 0.f;
                     if (t < valid) gate_grad(bt, lam, p.euler, db, dl);
-                    row_invn[t] = in;
-                    row_gn[t] = gam * in;
-                    row_al[t] = t < valid ? efla_alpha(bt, lam, p.euler) : 0.f;
                     row_dadb[t] = db;
                     row_dadl[t] = dl;
+                    zero_key = t < valid && !(lam > 0.f);
+                    alpha = efla_alpha(bt, lam, p.euler);
                 }
                 float x[32];
 #pragma unroll
                 for (int s = 0; s < 32; ++s) x[s] = col0 + s < t ? -g[s] : 0.f;  // -L
                 put16(sm + OFF_L, LO_64, t, col0, x);
                 put16(sm + OFF_L, LO_64, t, col0 + 16, x + 16);
-#pragma unroll
-                for (int s = 0; s < 32; s += 4)
-                    *reinterpret_cast<float4 *>(At + t * AT_LD + col0 + s) = make_float4(g[s], g[s + 1], g[s + 2], g[s + 3]);
             }
             if (named_bar_any(BAR_W, NW, !ok)) break;  // every CUDA-core warp leaves together
-            for (int e = tid; e < C * C; e += NW) {  // A~ = strictly-lower(gamma_t k^_t . k^_s), in place
-                const int t = e / C, s = e % C;
-                At[t * AT_LD + s] = s < t ? row_gn[t] * At[t * AT_LD + s] * row_invn[s] : 0.f;
-            }
-            named_bar(BAR_W, NW);
-            invert_unit_lower<BAR_W, AT_LD>(At, tid);  // T~; ends with a barrier over the CUDA-core warps
-            {  // T'' = diag(1/n) T~ diag(gamma/n); a zero key's row keeps u_t = alpha_t r_t
-                const int t = tid >> 2, s0 = (tid & 3) * 16;
-                float x[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int s = s0 + e;
-                    x[e] = s < t    ? row_invn[t] * At[t * AT_LD + s] * row_gn[s]
-                           : s == t ? (row_invn[t] > 0.f ? row_gn[t] * row_invn[t] : row_al[t])
-                                    : 0.f;
-                }
-                put16(sm + OFF_W, LO_64, t, s0, x);
-            }
             // ------------------------------ P2: R^T, dS' ------------------------------
             float gt[32];
-            wait(&bars->m1, ph);  // X^T complete
+            wait(&bars->m1a, ph);    // X^T complete
+            wait(&bars->t_full, ph);  // the forward's T'' landed
+            if (ok && zero_key) {     // u_t = alpha_t r_t for a zero key
+                const uint32_t b = __float_as_uint(alpha), off = swz_offset(ln, ln, 0);
+                const uint32_t lo = __float_as_uint(alpha - __uint_as_float(b & 0xffff0000u));
+                *reinterpret_cast<uint16_t *>(sm + OFF_W + off) = (uint16_t)(b >> 16);
+                *reinterpret_cast<uint16_t *>(sm + OFF_W + LO_64 + off) = (uint16_t)(lo >> 16);
+            }
             if (ok) {
                 // V^T: rows past the chunk's end load its last row (always in bounds) and are zeroed
                 // after, so that all 32 loads are unconditional and in flight together
@@ -615,10 +606,11 @@ __global__ void __launch_bounds__(NTH, 1) bwd_grad_tc_kernel(const __grid_consta
 }  // namespace
 
 // Per-chunk gradients on the tensor cores: bf16 q, k, v, d_k = d_v = 128, T > 0, after
-// launch_bwd_state_tc (dse, G in g, -dR split in dr_split, dO split in do_split).  Persistent: one CTA per
+// launch_bwd_state_tc (dse, G in g, -dR split in dr_split, dO split in do_split) and the forward
+// with chunk-start states and T'' tiles.  Persistent: one CTA per
 // SM at most, each walking items blockIdx.x, blockIdx.x + gridDim.x, ...
-cudaError_t launch_bwd_grad_tc(const BwdArgs &a, const float *states, const float *dse, const void *do_split,
-                               const float *g, const void *dr_split, const char **why) {
+cudaError_t launch_bwd_grad_tc(const BwdArgs &a, const float *states, const float *dse, const uint8_t *tpp,
+                               const void *do_split, const float *g, const void *dr_split, const char **why) {
     const long items = (long)a.B * a.H * ((a.T + C - 1) / C);
     if (items == 0) return cudaSuccess;
     const size_t n = (size_t)a.B * a.T * a.H * D;
@@ -636,6 +628,7 @@ cudaError_t launch_bwd_grad_tc(const BwdArgs &a, const float *states, const floa
     p.beta = a.beta;
     p.states = reinterpret_cast<const uint8_t *>(states);
     p.dse = reinterpret_cast<const uint8_t *>(dse);
+    p.tpp = tpp;
     p.g = g;
     p.dq = a.dq;
     p.dk = a.dk;

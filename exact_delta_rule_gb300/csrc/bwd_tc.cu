@@ -18,11 +18,12 @@
 // by TMA like the other inputs.  G and dR (= dv) of every token are written out for the
 // per-chunk gradient kernel, which then forms neither.
 //
-// One CTA of 448 threads per (b, h), the forward kernel's roles:
+// One CTA of 320 threads per (b, h):
 //   state warpgroup (warps 0-3): dS^T -> bf16 hi/lo operand (and dS' to HBM), G^T -> hi/lo,
 //     -dR^T -> hi/lo;
-//   prep warpgroups (warps 4-7, 10-13): per chunk, from the Gram rows [K; Q] K^T in TMEM, the
-//     gate terms, A~, the blocked inverse, and the bf16 hi/lo tiles of T'' and P;
+//   prep warpgroup (warps 4-7): per chunk, the bf16 hi/lo tile of P from the Gram rows Q K^T in
+//     TMEM (warps 6 and 7, TMEM lanes 64-127), and a bulk copy of the chunk's T'' tile, which the
+//     forward (run first with chunk-start states) formed and wrote out;
 //   MMA warp (warp 8); TMA producer (warp 9): K, Q, dO hi/lo of chunk (reverse index) it into
 //     stage it % 2.
 // Every wait is bounded; on expiry the CTA records EFLA_ERR_DEVICE_TIMEOUT and leaves.
@@ -33,7 +34,6 @@
 #include "internal.cuh"
 #include "ptx.cuh"
 #include "tc_common.cuh"
-#include "tri_inverse.cuh"
 
 namespace efla {
 namespace {
@@ -52,14 +52,11 @@ constexpr uint32_t OFF_DOL = 49152;
 // Per chunk parity: T'' hi, lo, then P hi, lo, each [64][64] bf16 (8 KB).
 constexpr uint32_t OFF_TPP = NSTAGE * STAGE_BYTES;
 constexpr uint32_t TPP_BYTES = 32768;
-constexpr uint32_t OFF_AT = OFF_TPP + 2 * TPP_BYTES;  // fp32 [64][68]: A~, then T~ in place
-constexpr uint32_t AT_LD = 68;
-constexpr uint32_t OFF_ROW = OFF_AT + 64 * AT_LD * 4;  // fp32 invn[64], gn[64]
-constexpr uint32_t OFF_BAR = OFF_ROW + 2 * 64 * 4;
+constexpr uint32_t OFF_BAR = OFF_TPP + 2 * TPP_BYTES;
 constexpr uint32_t OFF_MISC = OFF_BAR + 256;  // tmem base, abort flag
 constexpr uint32_t SMEM_USED = OFF_MISC + 16;
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;
-static_assert(OFF_TPP % 1024 == 0 && OFF_AT % 1024 == 0, "operand buffers must be 1024-byte aligned");
+static_assert(OFF_TPP % 1024 == 0, "operand buffers must be 1024-byte aligned");
 static_assert(SMEM_ALLOC <= 232448, "exceeds the per-CTA shared memory limit");
 
 // TMEM columns
@@ -78,6 +75,7 @@ struct BtParams {
     const float *dST;                            // [B, H, 128, 128] or nullptr (zero)
     float *dse;                                  // [B, H, nchunks] x 64 KB: dS' of every chunk as bf16 hi/lo
                                                  // operand tiles (put_col_split_tile)
+    const uint8_t *tpp;                          // [B, H, nchunks] x 16 KB: the forward's T'' tiles
     float *dS0;                                  // [B, H, 128, 128] or nullptr
     float *g_out, *dr_out;                       // [B, T, H, 128] fp32: G and dR (= dv) of every token
     __nv_bfloat16 *drs_hi, *drs_lo;              // [B, T, H, 128]: -dR as bf16 hi and lo
@@ -91,7 +89,8 @@ struct Bars {
     uint64_t tma_full[NSTAGE];  // K, Q, dO of a stage landed
     uint64_t s_free[NSTAGE];    // the stage's last reader (the state update) complete
     uint64_t g_done, g_free;    // Gram rows in TMEM / read by the prep
-    uint64_t prep_ready[2];     // T'', P and gate terms of a chunk written
+    uint64_t prep_ready[2];     // P of a chunk written and its T'' landed
+    uint64_t t_full[2];         // the forward's T'' of a chunk landed (bulk copy)
     uint64_t tpp_free[2];       // the chunk's T''/P buffer no longer read
     uint64_t x_done, u_done, s_done;
     uint64_t sa_ready, r_ready, u_ready;  // state warpgroup operands written (128 arrivals)
@@ -148,12 +147,9 @@ __device__ __forceinline__ void store_cols(float *base, size_t row_stride, int v
         if (32 + t < valid) base[(size_t)(32 + t) * row_stride] = x1[t];
 }
 
-__global__ void __launch_bounds__(448, 1) bwd_tc_kernel(const __grid_constant__ BtParams p) {
+__global__ void __launch_bounds__(320, 1) bwd_tc_kernel(const __grid_constant__ BtParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    float *row_invn = reinterpret_cast<float *>(sm + OFF_ROW);  // [64] 1/n_t
-    float *row_gn = row_invn + 64;                              // [64] gamma_t/n_t
-    float *At = reinterpret_cast<float *>(sm + OFF_AT);
     Bars *bars = reinterpret_cast<Bars *>(sm + OFF_BAR);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + OFF_MISC + 4);
@@ -173,6 +169,7 @@ __global__ void __launch_bounds__(448, 1) bwd_tc_kernel(const __grid_constant__ 
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars->prep_ready[i], 1);
+            mbar_init(&bars->t_full[i], 1);
             mbar_init(&bars->tpp_free[i], 1);
             mbar_init(&bars->drain[i], 1);
         }
@@ -197,121 +194,58 @@ __global__ void __launch_bounds__(448, 1) bwd_tc_kernel(const __grid_constant__ 
     const uint32_t tmem = *tmem_slot;
     const uint32_t s_sm = smem_u32(sm);
 
-    if ((tid >= 128 && tid < 256) || tid >= 320) {
-        // ============================== prep warpgroups ==============================
-        // As in the forward chunk kernel: Gram row r (TMEM lane r) is read by one thread of
-        // each warpgroup (columns 0-31 by warps 4-7, 32-63 by warps 10-13); rows 0-63 are
-        // K K^T (gate terms, A~), rows 64-127 are Q K^T (P).
-        const int half = tid >= 320 ? 1 : 0;
-        const int pi = half ? tid - 320 + 128 : tid - 128;
+    if (tid >= 128 && tid < 256) {
+        // =============================== prep warpgroup ===============================
+        // Gram row r is TMEM lane r; rows 64-127 are Q K^T (P), read by warps 6 and 7.
         const int quarter = warp & 3;
         const int row = quarter * 32 + (tid & 31);
-        const int col0 = half * 32;
         const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
-        const bool leader = pi == 0;
-        const bool gate_thr = row < C && (row >> 5) == half;
-        auto load_beta = [&](int it) {
-            if (it >= nchunks || !gate_thr) return 0.f;
-            const long t = (long)chunk_of(it) * C + row;
-            return t < p.T ? p.beta[((size_t)b * p.T + (size_t)t) * p.H + h] : 0.f;
-        };
-        float beta_next = load_beta(0);
+        const bool leader = tid == 128;
         for (int it = 0; it < nchunks; ++it) {
             const int buf = it & 1;
-            const long tok0 = (long)chunk_of(it) * C;
-            const int valid = (int)min((long)C, (long)p.T - tok0);
-            const float beta_t = beta_next;
-            beta_next = load_beta(it + 1);
+            uint8_t *tpp_buf = sm + OFF_TPP + buf * TPP_BYTES;
             bool ok = wait_bar_warp(&bars->g_done, it & 1, abort_flag, wait_ns);
             // this chunk's T''/P buffer was last read by the products of chunk it - 2
             if (it >= 2) ok = wait_bar_warp(&bars->tpp_free[buf], ((it - 2) >> 1) & 1, abort_flag, wait_ns) && ok;
+            if (leader && ok) {  // the forward's T'' of this chunk (the same tile this kernel would form)
+                mbar_arrive_expect_tx(&bars->t_full[buf], 16384);
+                bulk_load(tpp_buf, p.tpp + ((size_t)blockIdx.x * nchunks + chunk_of(it)) * 16384, 16384, &bars->t_full[buf]);
+            }
             tc_fence_after();
             {
-                float g[32];
-                tmem_ld32(lane_base + TM_G + col0, g);
-                tmem_ld_wait();
-                tc_fence_before();  // the next Gram may overwrite TM_G once every row is read
-                if (gate_thr) {     // this thread holds K K^T[t][t]: gate terms of row t
-                    const int t = row;
-                    float lam = 0.f;
-#pragma unroll
-                    for (int s = 0; s < 32; ++s) lam = (s == (t & 31)) ? g[s] : lam;
-                    const bool live = t < valid && lam > 0.f;
-                    const float invn = live ? rsqrtf(lam) : 0.f;
-                    const float gam = !live ? 0.f : p.euler ? beta_t * lam : -expm1f(-beta_t * lam);
-                    row_invn[t] = invn;
-                    row_gn[t] = gam * invn;
+                float g[64];
+                if (row >= C) {  // rows 64-127 of the Gram are Q K^T (rows 0-63, K K^T, are not needed)
+                    tmem_ld32(lane_base + TM_G, *reinterpret_cast<float(*)[32]>(g));
+                    tmem_ld32(lane_base + TM_G + 32, *reinterpret_cast<float(*)[32]>(g + 32));
+                    tmem_ld_wait();
                 }
-                if (named_bar_any(BAR_PREP, 256, !ok || *abort_flag)) {  // also spreads an abort
+                tc_fence_before();  // the next Gram may overwrite TM_G once every row is read
+                if (named_bar_any(BAR_PREP, 128, !ok || *abort_flag)) {  // also spreads an abort
                     *abort_flag = 1;
                     break;
                 }
                 if (leader) mbar_arrive(&bars->g_free);
-                if (row < C) {  // A~[t][col0 .. col0+31]
-                    const int t = row;
-                    const float rs = row_gn[t];
-                    float iv[32];
-#pragma unroll
-                    for (int s4 = 0; s4 < 8; ++s4) {
-                        const float4 f = reinterpret_cast<const float4 *>(row_invn + col0)[s4];
-                        iv[4 * s4] = f.x;
-                        iv[4 * s4 + 1] = f.y;
-                        iv[4 * s4 + 2] = f.z;
-                        iv[4 * s4 + 3] = f.w;
-                    }
-#pragma unroll
-                    for (int s4 = 0; s4 < 32; s4 += 4) {
-                        float4 w;
-                        w.x = col0 + s4 + 0 < t ? rs * iv[s4 + 0] * g[s4 + 0] : 0.f;
-                        w.y = col0 + s4 + 1 < t ? rs * iv[s4 + 1] * g[s4 + 1] : 0.f;
-                        w.z = col0 + s4 + 2 < t ? rs * iv[s4 + 2] * g[s4 + 2] : 0.f;
-                        w.w = col0 + s4 + 3 < t ? rs * iv[s4 + 3] * g[s4 + 3] : 0.f;
-                        *reinterpret_cast<float4 *>(At + t * AT_LD + col0 + s4) = w;
-                    }
-                } else {  // P[t][col0 .. col0+31] = Q K^T with the inclusive causal mask, bf16 hi/lo
+                if (row >= C) {  // P[t][s] = Q K^T with the inclusive causal mask, bf16 hi/lo
                     const int t = row - C;
 #pragma unroll
-                    for (int s = 0; s < 32; ++s) g[s] = col0 + s <= t ? g[s] : 0.f;
-                    uint8_t *phi = sm + OFF_TPP + buf * TPP_BYTES + 16384, *plo = phi + 8192;
+                    for (int s = 0; s < 64; ++s) g[s] = s <= t ? g[s] : 0.f;
+                    uint8_t *phi = tpp_buf + 16384, *plo = phi + 8192;
 #pragma unroll
-                    for (int c8 = 0; c8 < 32; c8 += 8) {
+                    for (int c8 = 0; c8 < 64; c8 += 8) {
                         uint32_t hh[4], ll[4];
                         split_pack<4>(g + c8, hh, ll);
-                        const uint32_t off = swz_offset(t, col0 + c8, 8192);
+                        const uint32_t off = swz_offset(t, c8, 8192);
                         *reinterpret_cast<uint4 *>(phi + off) = make_uint4(hh[0], hh[1], hh[2], hh[3]);
                         *reinterpret_cast<uint4 *>(plo + off) = make_uint4(ll[0], ll[1], ll[2], ll[3]);
                     }
                 }
             }
-            named_bar(BAR_PREP, 256);
-            invert_unit_lower<BAR_PREP, AT_LD>(At, pi);
-            {  // T'' = diag(1/n) T~ diag(gamma/n), lower triangle, as bf16 hi/lo [t][s]
-                const int t = pi >> 2, s0 = (pi & 3) * 16;
-                uint8_t *hi = sm + OFF_TPP + buf * TPP_BYTES, *lo = hi + 8192;
-                const float rsc = row_invn[t];
-#pragma unroll
-                for (int c8 = 0; c8 < 16; c8 += 8) {
-                    float tt8[8], gn8[8];
-                    *reinterpret_cast<float4 *>(tt8) = *reinterpret_cast<const float4 *>(At + t * AT_LD + s0 + c8);
-                    *reinterpret_cast<float4 *>(tt8 + 4) = *reinterpret_cast<const float4 *>(At + t * AT_LD + s0 + c8 + 4);
-                    *reinterpret_cast<float4 *>(gn8) = *reinterpret_cast<const float4 *>(row_gn + s0 + c8);
-                    *reinterpret_cast<float4 *>(gn8 + 4) = *reinterpret_cast<const float4 *>(row_gn + s0 + c8 + 4);
-                    float x[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int s = s0 + c8 + e;
-                        x[e] = s <= t ? rsc * tt8[e] * gn8[e] : 0.f;
-                    }
-                    uint32_t hh[4], ll[4];
-                    split_pack<4>(x, hh, ll);
-                    const uint32_t off = swz_offset(t, s0 + c8, 8192);
-                    *reinterpret_cast<uint4 *>(hi + off) = make_uint4(hh[0], hh[1], hh[2], hh[3]);
-                    *reinterpret_cast<uint4 *>(lo + off) = make_uint4(ll[0], ll[1], ll[2], ll[3]);
-                }
-            }
             fence_proxy_async_smem();
-            named_bar(BAR_PREP, 256);
-            if (leader) mbar_arrive(&bars->prep_ready[buf]);
+            named_bar(BAR_PREP, 128);
+            if (leader) {  // P written and T'' landed
+                ok = wait_bar(&bars->t_full[buf], (it >> 1) & 1, abort_flag, wait_ns) && ok;
+                mbar_arrive(&bars->prep_ready[buf]);
+            }
             if (!ok) *abort_flag = 1;
         }
     } else if (tid < 128) {
@@ -578,8 +512,8 @@ bool bwd_row_map(CUtensorMap *m, const void *ptr, int B, int T, int H) {
 // State gradients of the chunked backward on the tensor cores: bf16 q, k, d_k = d_v = 128,
 // T > 0.  do_split: 2 x B*T*H*128 bf16 of scratch (dO hi, then lo); g_out: B*T*H*128 fp32
 // (G of every token); dv receives dR.
-cudaError_t launch_bwd_state_tc(const BwdArgs &a, float *dse, void *do_split, float *g_out, void *dr_split,
-                                const char **why) {
+cudaError_t launch_bwd_state_tc(const BwdArgs &a, float *dse, const uint8_t *tpp, void *do_split, float *g_out,
+                                void *dr_split, const char **why) {
     const size_t n = (size_t)a.B * a.T * a.H * D;
     __nv_bfloat16 *hi = static_cast<__nv_bfloat16 *>(do_split), *lo = hi + n;
     int dev = 0, sms = 0;
@@ -607,6 +541,7 @@ cudaError_t launch_bwd_state_tc(const BwdArgs &a, float *dse, void *do_split, fl
     p.beta = a.beta;
     p.dST = a.dST;
     p.dse = dse;
+    p.tpp = tpp;
     p.dS0 = a.dS0;
     p.g_out = g_out;
     p.dr_out = a.dv;
@@ -628,7 +563,7 @@ cudaError_t launch_bwd_state_tc(const BwdArgs &a, float *dse, void *do_split, fl
         if (dev < 64) attr_done[dev] = true;
     }
     *why = "tcgen05 state-gradient kernel launch";
-    bwd_tc_kernel<<<(unsigned)((long)a.B * a.H), 448, SMEM_ALLOC, a.stream>>>(p);
+    bwd_tc_kernel<<<(unsigned)((long)a.B * a.H), 320, SMEM_ALLOC, a.stream>>>(p);
     return cudaGetLastError();
 }
 

@@ -131,6 +131,7 @@ struct TcParams {
     float *maps;
     float *states;               // chunk-start states [N, H, nchunks] x 64 KB (rows of [B, T]) or nullptr: S as
                                  // bf16 hi/lo operand tiles (put_col_split_tile) for the tensor-core backward
+    uint8_t *tpp;                // with states: every chunk's T'' tile as formed below (16 KB a chunk) or nullptr
     unsigned long long wait_ns;  // bound on every wait between roles (2 s unless a test lowers it)
     int debug_stall;             // test hook: the MMA thread first waits on a barrier nothing completes
 };
@@ -416,6 +417,8 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
             {  // T'' = diag(1/n) T~ diag(gamma/n), lower triangle, as bf16 hi/lo [t][s]
                 const int t = pi >> 2, s0 = (pi & 3) * 16;
                 uint8_t *hi = sm + OFF_TPP + buf * TPP_BYTES, *lo = hi + 8192;
+                // the same tile for the backward (a zero key's diagonal is 0 here; the backward sets it)
+                uint8_t *ghi = p.tpp ? p.tpp + ((size_t)blockIdx.x * nchunks + c) * 16384 : nullptr;
                 const float rsc = row_invn[t];
 #pragma unroll
                 for (int c8 = 0; c8 < 16; c8 += 8) {
@@ -435,6 +438,10 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
                     const uint32_t off = swz_offset(t, s0 + c8, 8192);
                     *reinterpret_cast<uint4 *>(hi + off) = make_uint4(hh[0], hh[1], hh[2], hh[3]);
                     *reinterpret_cast<uint4 *>(lo + off) = make_uint4(ll[0], ll[1], ll[2], ll[3]);
+                    if (ghi) {
+                        *reinterpret_cast<uint4 *>(ghi + off) = make_uint4(hh[0], hh[1], hh[2], hh[3]);
+                        *reinterpret_cast<uint4 *>(ghi + 8192 + off) = make_uint4(ll[0], ll[1], ll[2], ll[3]);
+                    }
                 }
             }
             fence_proxy_async_smem();
@@ -921,6 +928,7 @@ cudaError_t launch_chunk_tc(const FwdArgs &a, const char **why) {
     p.s_in = a.s_in;
     p.maps = a.maps;
     p.states = a.states;
+    p.tpp = a.tpp;
     p.wait_ns = wait_limit_ns();
     p.debug_stall = debug_stall() ? 1 : 0;
     *why = "tcgen05 chunk kernel launch";

@@ -367,10 +367,10 @@ efla_status efla_bwd_workspace(int B, int T, int H, int d_k, int d_v, size_t *by
     if (d_k != d_v || (d_k != 64 && d_k != 128))
         return fail(EFLA_ERR_UNSUPPORTED, "the chunked backward supports d_k = d_v in {64, 128} (got %d, %d)", d_k, d_v);
     const size_t nc = ((size_t)T + 63) / 64;
-    // chunk-start states and end-state gradients (4 bytes an element), dO as bf16 hi and lo,
-    // G (fp32), -dR as bf16 hi and lo
-    *bytes = 2 * (size_t)B * H * nc * d_k * d_v * sizeof(float) + 2 * (size_t)B * T * H * d_v * 2 +
-             (size_t)B * T * H * d_v * sizeof(float) + 2 * (size_t)B * T * H * d_v * 2;
+    // per chunk: start state and end-state gradient (4 bytes an element), T'' (64 x 64 x 4 bytes);
+    // per token: dO as bf16 hi and lo, G (fp32), -dR as bf16 hi and lo
+    *bytes = (size_t)B * H * nc * (2 * (size_t)d_k * d_v + 64 * 64) * sizeof(float) +
+             (size_t)B * T * H * d_v * (2 * 2 + sizeof(float) + 2 * 2);
     return EFLA_OK;
 }
 
@@ -422,7 +422,8 @@ efla_status efla_bwd_chunked(const void *q, const void *k, const void *v, const 
     const size_t state_floats = (size_t)B * H * (((size_t)T + 63) / 64) * d_k * d_v;
     float *states = static_cast<float *>(workspace);
     float *dse = states + state_floats;
-    void *do_split = dse + state_floats;
+    uint8_t *tpp = reinterpret_cast<uint8_t *>(dse + state_floats);
+    void *do_split = tpp + (size_t)B * H * (((size_t)T + 63) / 64) * 64 * 64 * 4;
     float *g_tok = reinterpret_cast<float *>(static_cast<char *>(do_split) + 2 * (size_t)B * T * H * d_v * 2);
     void *dr_split = g_tok + (size_t)B * T * H * d_v;
     cudaError_t e;
@@ -430,6 +431,7 @@ efla_status efla_bwd_chunked(const void *q, const void *k, const void *v, const 
         FwdArgs fa{q, k, v, beta, S0, nullptr, nullptr, nullptr, B, T, H, d_k, d_v, B, in_dtype, in_dtype,
                    64, cs, status, (int)update};
         fa.states = states;
+        fa.tpp = tpp;
         const char *why = "chunk kernel launch (backward states)";
         e = in_dtype == EFLA_BF16 && d_k == 128 ? launch_chunk_tc(fa, &why) : launch_chunk_simt(fa);
         if (e != cudaSuccess) return cuda_fail(e, why);
@@ -438,8 +440,8 @@ efla_status efla_bwd_chunked(const void *q, const void *k, const void *v, const 
     const bool tc = in_dtype == EFLA_BF16 && d_k == 128 && T > 0;  // the state pass on the tensor cores
     if (tc) {
         const char *why = "tcgen05 state-gradient kernel launch";
-        e = launch_bwd_state_tc(a, dse, do_split, g_tok, dr_split, &why);
-        if (e == cudaSuccess) e = launch_bwd_grad_tc(a, states, dse, do_split, g_tok, dr_split, &why);
+        e = launch_bwd_state_tc(a, dse, tpp, do_split, g_tok, dr_split, &why);
+        if (e == cudaSuccess) e = launch_bwd_grad_tc(a, states, dse, tpp, do_split, g_tok, dr_split, &why);
         if (e != cudaSuccess) return cuda_fail(e, why);
     } else {
         e = launch_bwd_chunked(a, states, dse);

@@ -43,6 +43,9 @@ struct FwdArgs {
     // (rows of [B, T] only; o may then be nullptr): fp32 row-major from the CUDA-core chunk
     // kernel, bf16 hi/lo operand tiles (tc::put_col_split_tile) from the tensor-core one.
     float *states = nullptr;
+    // With states, the tensor-core chunk kernel also writes every chunk's T'' (bf16 hi/lo operand
+    // tile, [64][64] each, 128-byte swizzle: 16 KB a chunk) here, or nowhere if nullptr.
+    uint8_t *tpp = nullptr;
 };
 
 struct DecodeArgs {
@@ -90,17 +93,18 @@ cudaError_t launch_bwd(const BwdArgs &a);
 // the chunks, then every chunk's gradients in parallel from `states` (the forward's chunk-start
 // states, filled first by a forward launch with FwdArgs::states).  dse: [B, H, nchunks, dk, dv].
 cudaError_t launch_bwd_chunked(const BwdArgs &a, const float *states, float *dse);
-// The same state pass on the tensor cores (bwd_tc.cu): bf16 q, k, d_k = d_v = 128, T > 0;
+// The same state pass on the tensor cores (bwd_tc.cu): bf16 q, k, d_k = d_v = 128, T > 0, after
+// the forward with chunk-start states and T'' tiles (tpp);
 // do_split is scratch for dO as bf16 hi and lo (2 x B*T*H*128 bf16); it also writes G of every
 // token into g_out (B*T*H*128 fp32), dR into dv, -dR as bf16 hi and lo into dr_split (like
 // do_split), and dse as bf16 hi/lo operand tiles, for launch_bwd_grad_tc.
-cudaError_t launch_bwd_state_tc(const BwdArgs &a, float *dse, void *do_split, float *g_out, void *dr_split,
-                                const char **why);
+cudaError_t launch_bwd_state_tc(const BwdArgs &a, float *dse, const uint8_t *tpp, void *do_split, float *g_out,
+                                void *dr_split, const char **why);
 // Per-chunk gradients on the tensor cores (bwd_grad_tc.cu) after launch_bwd_state_tc: reads the
-// forward's chunk-start states and dse (both as bf16 hi/lo operand tiles), do_split, G (g) and
-// dr_split; writes dq, dk, dbeta.
-cudaError_t launch_bwd_grad_tc(const BwdArgs &a, const float *states, const float *dse, const void *do_split,
-                               const float *g, const void *dr_split, const char **why);
+// forward's chunk-start states and T'' tiles (FwdArgs::states, ::tpp), dse (all as bf16 hi/lo
+// operand tiles), do_split, G (g) and dr_split; writes dq, dk, dbeta.
+cudaError_t launch_bwd_grad_tc(const BwdArgs &a, const float *states, const float *dse, const uint8_t *tpp,
+                               const void *do_split, const float *g, const void *dr_split, const char **why);
 // [B, T, H, 128] bf16 tensor map of the backward kernels: box 64 features x 1 head x 64 tokens
 // x 1, 128-byte swizzle (bwd_tc.cu).
 bool bwd_row_map(CUtensorMap *m, const void *ptr, int B, int T, int H);

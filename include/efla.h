@@ -237,10 +237,11 @@ efla_status efla_bwd_recurrent(const void *q, const void *k, const void *v, cons
  * independent, for every token's gradients (fp32 on CUDA cores).  For bf16 inputs with
  * d = 128 all three steps run on the tensor cores (split-bf16 operands, fp32 accumulation;
  * the last on persistent CTAs), after a pass that writes dO as bf16 hi and lo parts into the
- * workspace; the second also writes G and -dR (bf16 hi and lo) of every token there.
+ * workspace; the first also writes every chunk's T'' there, the second G and -dR (bf16 hi and
+ * lo) of every token.
  *
  *   workspace  device scratch owned by the caller, 16-byte aligned, at least the size
- *              efla_bwd_workspace reports (2 x B x H x ceil(T/64) x d_k x d_v x 4 bytes
+ *              efla_bwd_workspace reports (B x H x ceil(T/64) x (2 d_k d_v + 4096) x 4 bytes
  *              + B x T x H x d_v x 12 bytes);
  *              it must not overlap any argument.  Too small or NULL: EFLA_ERR_INVALID_ARG.
  * Supported: d_k = d_v in {64, 128} (other sizes: EFLA_ERR_UNSUPPORTED, use

@@ -322,9 +322,9 @@ def test_bwd_workspace_size(lib):
     f.argtypes = [ctypes.c_int] * 5 + [ctypes.POINTER(ctypes.c_size_t)]
     n = ctypes.c_size_t(0)
     assert f(8, 2048, 16, 128, 128, ctypes.byref(n)) == 0
-    # chunk-start states and end-state gradients, then per token: dO hi/lo, G, -dR hi/lo
-    assert n.value == 2 * 8 * 16 * 32 * 128 * 128 * 4 + 8 * 2048 * 16 * 128 * (4 + 4 + 4)
-    assert f(1, 65, 1, 64, 64, ctypes.byref(n)) == 0 and n.value == 2 * 2 * 64 * 64 * 4 + 65 * 64 * 12
+    # per chunk: start state, end-state gradient, T''; per token: dO hi/lo, G, -dR hi/lo
+    assert n.value == 8 * 16 * 32 * (2 * 128 * 128 + 64 * 64) * 4 + 8 * 2048 * 16 * 128 * (4 + 4 + 4)
+    assert f(1, 65, 1, 64, 64, ctypes.byref(n)) == 0 and n.value == 2 * (2 * 64 * 64 + 64 * 64) * 4 + 65 * 64 * 12
     assert f(1, 64, 1, 32, 32, ctypes.byref(n)) == UNSUPPORTED
     assert f(1, 64, 1, 128, 128, None) == INVALID
 
