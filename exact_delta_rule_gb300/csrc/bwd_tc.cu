@@ -19,13 +19,13 @@
 // per-chunk gradient kernel, which then forms neither.
 //
 // One CTA of 320 threads per (b, h):
-//   state warpgroup (warps 0-3): dS^T -> bf16 hi/lo operand (and dS' to HBM), G^T -> hi/lo,
-//     -dR^T -> hi/lo;
+//   state warpgroup (warps 0-3): dS^T -> bf16 hi/lo operand (and dS' to HBM), G^T -> hi/lo (and
+//     G to HBM), -dR^T -> hi/lo (and dv = dR, -dR as bf16 hi/lo to HBM);
 //   prep warpgroup (warps 4-7): per chunk, the bf16 hi/lo tile of P from the Gram rows Q K^T in
-//     TMEM (warps 6 and 7, TMEM lanes 64-127), and a bulk copy of the chunk's T'' tile, which the
-//     forward (run first with chunk-start states) formed and wrote out;
+//     TMEM (warps 6 and 7, TMEM lanes 64-127);
 //   MMA warp (warp 8); TMA producer (warp 9): K, Q, dO hi/lo of chunk (reverse index) it into
-//     stage it % 2.
+//     stage it % 2, and the forward's T'' tile of that chunk (formed and written out by the
+//     forward, run first with chunk-start states) into T''/P buffer it % 2.
 // Every wait is bounded; on expiry the CTA records EFLA_ERR_DEVICE_TIMEOUT and leaves.
 #include <cudaTypedefs.h>
 
@@ -201,53 +201,57 @@ __global__ void __launch_bounds__(320, 1) bwd_tc_kernel(const __grid_constant__ 
         const int row = quarter * 32 + (tid & 31);
         const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
         const bool leader = tid == 128;
-        for (int it = 0; it < nchunks; ++it) {
+        // P of chunk (reverse index) it; hands the chunk over once its T'' (bulk-copied by the TMA
+        // thread) has landed; false when the CTA aborts (the same answer in every prep thread)
+        auto make_p = [&](int it, bool ok) -> bool {
             const int buf = it & 1;
             uint8_t *tpp_buf = sm + OFF_TPP + buf * TPP_BYTES;
-            bool ok = wait_bar_warp(&bars->g_done, it & 1, abort_flag, wait_ns);
+            ok = ok && wait_bar_warp(&bars->g_done, it & 1, abort_flag, wait_ns);
             // this chunk's T''/P buffer was last read by the products of chunk it - 2
-            if (it >= 2) ok = wait_bar_warp(&bars->tpp_free[buf], ((it - 2) >> 1) & 1, abort_flag, wait_ns) && ok;
-            if (leader && ok) {  // the forward's T'' of this chunk (the same tile this kernel would form)
-                mbar_arrive_expect_tx(&bars->t_full[buf], 16384);
-                bulk_load(tpp_buf, p.tpp + ((size_t)blockIdx.x * nchunks + chunk_of(it)) * 16384, 16384, &bars->t_full[buf]);
-            }
+            if (it >= 2) ok = ok && wait_bar_warp(&bars->tpp_free[buf], ((it - 2) >> 1) & 1, abort_flag, wait_ns);
             tc_fence_after();
-            {
-                float g[64];
-                if (row >= C) {  // rows 64-127 of the Gram are Q K^T (rows 0-63, K K^T, are not needed)
-                    tmem_ld32(lane_base + TM_G, *reinterpret_cast<float(*)[32]>(g));
-                    tmem_ld32(lane_base + TM_G + 32, *reinterpret_cast<float(*)[32]>(g + 32));
-                    tmem_ld_wait();
-                }
-                tc_fence_before();  // the next Gram may overwrite TM_G once every row is read
-                if (named_bar_any(BAR_PREP, 128, !ok || *abort_flag)) {  // also spreads an abort
-                    *abort_flag = 1;
-                    break;
-                }
-                if (leader) mbar_arrive(&bars->g_free);
-                if (row >= C) {  // P[t][s] = Q K^T with the inclusive causal mask, bf16 hi/lo
-                    const int t = row - C;
+            // P[t][s] = Q K^T with the inclusive causal mask, bf16 hi/lo: rows 64-127 of the Gram
+            // (rows 0-63, K K^T, are not needed), read into registers 32 columns at a time
+            float g[2][32];
+            if (ok && row >= C) {
+                tmem_ld32(lane_base + TM_G, g[0]);
+                tmem_ld32(lane_base + TM_G + 32, g[1]);
+                tmem_ld_wait();
+            }
+            tc_fence_before();  // the next Gram may overwrite TM_G once every row is read
+            if (named_bar_any(BAR_PREP, 128, !ok || *abort_flag)) {  // also spreads an abort
+                *abort_flag = 1;
+                return false;
+            }
+            if (leader) mbar_arrive(&bars->g_free);
+            if (row >= C) {
+                const int t = row - C;
+                uint8_t *phi = tpp_buf + 16384, *plo = phi + 8192;
 #pragma unroll
-                    for (int s = 0; s < 64; ++s) g[s] = s <= t ? g[s] : 0.f;
-                    uint8_t *phi = tpp_buf + 16384, *plo = phi + 8192;
+                for (int hf = 0; hf < 2; ++hf)
 #pragma unroll
-                    for (int c8 = 0; c8 < 64; c8 += 8) {
+                    for (int c8 = 0; c8 < 32; c8 += 8) {
+                        float x[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) x[e] = 32 * hf + c8 + e <= t ? g[hf][c8 + e] : 0.f;
                         uint32_t hh[4], ll[4];
-                        split_pack<4>(g + c8, hh, ll);
-                        const uint32_t off = swz_offset(t, c8, 8192);
+                        split_pack<4>(x, hh, ll);
+                        const uint32_t off = swz_offset(t, 32 * hf + c8, 8192);
                         *reinterpret_cast<uint4 *>(phi + off) = make_uint4(hh[0], hh[1], hh[2], hh[3]);
                         *reinterpret_cast<uint4 *>(plo + off) = make_uint4(ll[0], ll[1], ll[2], ll[3]);
                     }
-                }
             }
             fence_proxy_async_smem();
             named_bar(BAR_PREP, 128);
             if (leader) {  // P written and T'' landed
-                ok = wait_bar(&bars->t_full[buf], (it >> 1) & 1, abort_flag, wait_ns) && ok;
+                ok = wait_bar(&bars->t_full[buf], (it >> 1) & 1, abort_flag, wait_ns);
                 mbar_arrive(&bars->prep_ready[buf]);
+                if (!ok) *abort_flag = 1;
             }
-            if (!ok) *abort_flag = 1;
-        }
+            return true;
+        };
+        for (int it = 0; it < nchunks; ++it)
+            if (!make_p(it, true)) break;
     } else if (tid < 128) {
         // =============================== state warpgroup ===============================
         const int j = tid;
@@ -335,9 +339,16 @@ __global__ void __launch_bounds__(320, 1) bwd_tc_kernel(const __grid_constant__ 
         prefetch_tensormap(&p.map_k);
         prefetch_tensormap(&p.map_doh);
         prefetch_tensormap(&p.map_dol);
-        int issued = 0;
+        int issued = 0, t_issued = 0;
         for (int it = 0; it < nchunks; ++it) {
-            const int st = it % NSTAGE;
+            const int st = it % NSTAGE, buf = it & 1;
+            // the forward's T'' of this chunk into its T''/P buffer, once chunk it - 2's products are
+            // done with that buffer (the prep warpgroup waits for it before handing the chunk over)
+            if (it >= 2 && !wait_bar(&bars->tpp_free[buf], ((it - 2) >> 1) & 1, abort_flag, wait_ns)) break;
+            mbar_arrive_expect_tx(&bars->t_full[buf], 16384);
+            bulk_load(sm + OFF_TPP + buf * TPP_BYTES, p.tpp + ((size_t)blockIdx.x * nchunks + chunk_of(it)) * 16384, 16384,
+                      &bars->t_full[buf]);
+            t_issued = it + 1;
             if (it >= NSTAGE && !wait_bar(&bars->s_free[st], ((it - NSTAGE) / NSTAGE) & 1, abort_flag, wait_ns)) break;
             uint8_t *dst = sm + OFF_STAGE + st * STAGE_BYTES;
             const int tok = chunk_of(it) * C;
@@ -357,6 +368,11 @@ __global__ void __launch_bounds__(320, 1) bwd_tc_kernel(const __grid_constant__ 
                    globaltimer_ns() - t0 < WAIT_NS) {
             }
         }
+        for (int cc = max(0, t_issued - 2); cc < t_issued; ++cc) {
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait_sleep(&bars->t_full[cc & 1], (cc >> 1) & 1, 20000) && globaltimer_ns() - t0 < WAIT_NS) {
+            }
+        }
     } else if (warp == 8) {
         // =============================== MMA warp ===============================
         bool ok = true;
@@ -366,8 +382,8 @@ __global__ void __launch_bounds__(320, 1) bwd_tc_kernel(const __grid_constant__ 
         auto issue_grams = [&](int limit, bool block) {
             while (ok && g_next <= limit && g_next < nchunks) {
                 if (!block) {
-                    const bool ready = (g_next == 0 || mbar_try_wait(&bars->g_free, (g_next - 1) & 1)) &&
-                                       mbar_try_wait(&bars->tma_full[g_next % NSTAGE], (g_next / NSTAGE) & 1);
+                    const bool ready = (g_next == 0 || mbar_test(&bars->g_free, (g_next - 1) & 1)) &&
+                                       mbar_test(&bars->tma_full[g_next % NSTAGE], (g_next / NSTAGE) & 1);
                     if (!__all_sync(0xffffffffu, ready)) break;
                 } else {
                     if (g_next > 0 && !(ok = wait_bar_warp(&bars->g_free, (g_next - 1) & 1, abort_flag, wait_ns))) break;

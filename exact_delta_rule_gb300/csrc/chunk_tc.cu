@@ -706,8 +706,8 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
         auto issue_grams = [&](int limit, bool block) {
             while (ok && g_next <= limit && g_next < nchunks && eos - (bos + (long)g_next * C) >= C) {
                 if (!block) {
-                    const bool ready = (g_next == 0 || mbar_try_wait(&bars->g_free, (g_next - 1) & 1)) &&
-                                       mbar_try_wait(&bars->tma_full[g_next % NSTAGE], (g_next / NSTAGE) & 1);
+                    const bool ready = (g_next == 0 || mbar_test(&bars->g_free, (g_next - 1) & 1)) &&
+                                       mbar_test(&bars->tma_full[g_next % NSTAGE], (g_next / NSTAGE) & 1);
                     if (!__all_sync(0xffffffffu, ready)) break;
                 } else {
                     if (g_next > 0 && !(ok = wait_bar_warp(&bars->g_free, (g_next - 1) & 1, abort_flag, wait_ns))) break;
