@@ -508,9 +508,10 @@ def bwd_figure(efla, dev, stream, q, k, v, beta, flush, peaks, steps=3):
             "ms_per_call": 1e3 * t, "tokens_per_s": B * T / t, "algorithmic_bytes": nbytes,
             "GB/s": nbytes / t / 1e9, "frac_hbm": nbytes / t / 1e9 / peaks["hbm_gbs"],
             "workspace_bytes": ws_bytes,
-            "path": "forward on the tensor cores writing every chunk-start state (workspace); reverse pass over "
-                    "chunks for the end-state gradients on the tensor cores (one CTA per (b, h)), also writing G "
-                    "and dv; per-chunk gradients (one CTA per (b, h, chunk)) on the tensor cores",
+            "path": "forward on the tensor cores writing every chunk-start state and T'' (workspace); dO split "
+                    "into bf16 hi/lo; reverse pass over chunks for the end-state gradients on the tensor cores (one "
+                    "CTA per (b, h)), also writing G, dv and -dR (hi/lo); per-chunk gradients on the tensor cores "
+                    "(persistent CTAs over the (b, h, chunk) items)",
             "ms_recurrent": 1e3 * t_rec, "gpu_launches": 4 * steps + 1}
 
 
