@@ -93,10 +93,19 @@ def test_bwd_zero_keys_and_zero_steps(efla, kind):
     _check(efla, c, kind=kind)
 
 
+@pytest.mark.parametrize("B,T,H", [(1, 1, 1), (1, 65, 1), (3, 333, 5), (2, 1000, 10)])
+def test_bwd_chunked_tensor_core_shapes(efla, B, T, H):
+    """bf16, d = 128 (every step on the tensor cores): a single token, one full chunk and one
+    token, ragged tails on several units, and 320 chunk items, so that each persistent CTA of the
+    gradient kernel walks two or three items and every mbarrier turns both parities."""
+    _check(efla, _case("bf16", B, T, H, 128, 128, seed=100 + B * T + H), kind="chunked")
+
+
 def test_bwd_chunked_tensor_core_path_zero_keys_zero_steps_and_euler(efla):
-    """bf16 with d = 128 takes the tensor-core state pass and the gradient kernel's hand-over
-    of G and dR: zero keys, beta = 0, the gate derivative's series branch, a ragged tail and
-    the delta-rule gate, against the oracle."""
+    """bf16 with d = 128 takes the tensor-core steps (the state pass's hand-over of G and -dR,
+    the forward's T'' in both later steps): zero keys (whose T'' diagonal the gradient kernel
+    sets), beta = 0, the gate derivative's series branch, a ragged tail and the delta-rule gate,
+    against the oracle."""
     c = _case("bf16", 1, 150, 2, 128, 128, seed=8)
     k = c["k"].clone()
     k[:, 3::7] = 0
