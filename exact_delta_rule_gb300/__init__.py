@@ -435,6 +435,8 @@ def set_wait_limit_ns(ns: int) -> None:
     load().efla_debug_set_wait_limit_ns(int(ns))
 
 
-def set_debug_stall(on: bool) -> None:
-    """Test hook (``efla_debug_set_stall``): make the chunk kernel's waits run out on purpose."""
-    load().efla_debug_set_stall(1 if on else 0)
+def set_debug_stall(on) -> None:
+    """Test hook (``efla_debug_set_stall``): make tensor-core kernels' waits run out on purpose.
+    True (or 1) names the chunk kernel; an int is the header's set of kernel bits (1 chunk
+    kernel, 2 backward state pass, 4 backward gradient kernel)."""
+    load().efla_debug_set_stall(int(on) & 7)

@@ -101,6 +101,7 @@ struct GtParams {
     int *status;
     int T, H, items;                             // items = B H nchunks
     int euler;
+    int debug_stall;  // test hook: the MMA warp first waits on a barrier nothing completes
     unsigned long long wait_ns;
 };
 
@@ -110,6 +111,7 @@ struct Bars {
     uint64_t g, m1a, m1b, u, a, b, m2;     // products complete (tcgen05.commit)
     uint64_t w_u, w_p3, w_p5, w_free;      // operands written / TMEM read by the CUDA-core warps (8 arrivals)
     uint64_t drain;
+    uint64_t never;                        // never completed (the debug_stall test hook waits on it)
 };
 static_assert(sizeof(Bars) <= 256, "mbarrier block exceeds its slot");
 
@@ -198,6 +200,7 @@ __global__ void __launch_bounds__(NTH, 1) bwd_grad_tc_kernel(const __grid_consta
         mbar_init(&bars->w_p5, 8);
         mbar_init(&bars->w_free, 8);
         mbar_init(&bars->drain, 1);
+        mbar_init(&bars->never, 1);
         fence_mbar_init();
         *abort_flag = 0;
     }
@@ -253,8 +256,10 @@ __global__ void __launch_bounds__(NTH, 1) bwd_grad_tc_kernel(const __grid_consta
             tc_fence_after();
             return ok;
         };
+        if (p.debug_stall) ok = wait_bar_warp(&bars->never, 0, abort_flag, wait_ns);
         for (int w = blockIdx.x; w < p.items; w += gridDim.x, ++it) {
             const int ph = it & 1;
+            if (!ok) break;
             const Item I = item_of(p, w, nc);
             // the previous item's last products are complete: every operand tile is free
             if (it > 0 && !wait(&bars->m2, ph ^ 1)) break;
@@ -598,7 +603,7 @@ __global__ void __launch_bounds__(NTH, 1) bwd_grad_tc_kernel(const __grid_consta
     }
 
     tc_fence_before();
-    __syncthreads();
+    __syncthreads();  // every role is done: an abort flagged by any of them is visible now
     if (tid == 0 && *abort_flag) atomicExch(p.status, (int)EFLA_ERR_DEVICE_TIMEOUT);
     if (warp == 0) tmem_dealloc(tmem, TM_COLS);
 }
@@ -639,6 +644,7 @@ cudaError_t launch_bwd_grad_tc(const BwdArgs &a, const float *states, const floa
     p.items = (int)items;
     p.euler = a.euler;
     p.wait_ns = wait_limit_ns();
+    p.debug_stall = (debug_stall() & STALL_BWD_GRAD) ? 1 : 0;
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);

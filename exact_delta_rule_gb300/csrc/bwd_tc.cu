@@ -82,6 +82,7 @@ struct BtParams {
     int *status;
     int B, T, H;
     int euler;
+    int debug_stall;  // test hook: the MMA warp first waits on a barrier nothing completes
     unsigned long long wait_ns;
 };
 
@@ -95,6 +96,7 @@ struct Bars {
     uint64_t x_done, u_done, s_done;
     uint64_t sa_ready, r_ready, u_ready;  // state warpgroup operands written (128 arrivals)
     uint64_t drain[2];
+    uint64_t never;             // never completed (the debug_stall test hook waits on it)
 };
 static_assert(sizeof(Bars) <= 256, "mbarrier block exceeds its slot");
 
@@ -178,6 +180,7 @@ __global__ void __launch_bounds__(320, 1) bwd_tc_kernel(const __grid_constant__ 
         mbar_init(&bars->x_done, 1);
         mbar_init(&bars->u_done, 1);
         mbar_init(&bars->s_done, 1);
+        mbar_init(&bars->never, 1);
         mbar_init(&bars->sa_ready, 128);
         mbar_init(&bars->r_ready, 128);
         mbar_init(&bars->u_ready, 128);
@@ -403,6 +406,7 @@ __global__ void __launch_bounds__(320, 1) bwd_tc_kernel(const __grid_constant__ 
                 ++g_next;
             }
         };
+        if (p.debug_stall) ok = wait_bar_warp(&bars->never, 0, abort_flag, wait_ns);
         issue_grams(0, true);
         for (int it = 0; it < nchunks && ok; ++it) {
             const int st = it % NSTAGE, buf = it & 1;
@@ -488,9 +492,9 @@ __global__ void __launch_bounds__(320, 1) bwd_tc_kernel(const __grid_constant__ 
         __syncwarp();
     }
 
-    if (*abort_flag && tid == 0) atomicExch(p.status, (int)EFLA_ERR_DEVICE_TIMEOUT);
     tc_fence_before();
-    __syncthreads();
+    __syncthreads();  // every role is done: an abort flagged by any of them is visible now
+    if (*abort_flag && tid == 0) atomicExch(p.status, (int)EFLA_ERR_DEVICE_TIMEOUT);
     if (warp == 0) tmem_dealloc(tmem, TM_COLS);
 }
 
@@ -569,6 +573,7 @@ cudaError_t launch_bwd_state_tc(const BwdArgs &a, float *dse, const uint8_t *tpp
     p.H = a.H;
     p.euler = a.euler;
     p.wait_ns = wait_limit_ns();
+    p.debug_stall = (debug_stall() & STALL_BWD_STATE) ? 1 : 0;
     static bool attr_done[64] = {};
     if (dev >= 64 || !attr_done[dev]) {
         e = cudaFuncSetAttribute(bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_ALLOC);

@@ -844,9 +844,9 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
         __syncwarp();
     }
 
-    if (*abort_flag && tid == 0) atomicExch(p.status, (int)EFLA_ERR_DEVICE_TIMEOUT);
     tc_fence_before();
-    __syncthreads();
+    __syncthreads();  // every role is done: an abort flagged by any of them is visible now
+    if (*abort_flag && tid == 0) atomicExch(p.status, (int)EFLA_ERR_DEVICE_TIMEOUT);
     if (warp == 0) tmem_dealloc(tmem, TM_COLS);
 }
 
@@ -930,7 +930,7 @@ cudaError_t launch_chunk_tc(const FwdArgs &a, const char **why) {
     p.states = a.states;
     p.tpp = a.tpp;
     p.wait_ns = wait_limit_ns();
-    p.debug_stall = debug_stall() ? 1 : 0;
+    p.debug_stall = (debug_stall() & STALL_CHUNK) ? 1 : 0;
     *why = "tcgen05 chunk kernel launch";
     const long units = a.seg_len > 0 ? (a.maps ? 2L * a.B * (a.G - 1) * a.H : (long)a.B * a.G * a.H) : (long)a.N * a.H;
     const unsigned grid = (unsigned)units;

@@ -540,9 +540,9 @@ __global__ void __launch_bounds__(THREADS, 1) decode_tc_kernel(const __grid_cons
         if (!ok) *abort_flag = 1;
     }
 
-    if (*abort_flag && tid == 0) atomicExch(p.status, (int)EFLA_ERR_DEVICE_TIMEOUT);
     tc_fence_before();
-    __syncthreads();
+    __syncthreads();  // every role is done: an abort flagged by any of them is visible now
+    if (*abort_flag && tid == 0) atomicExch(p.status, (int)EFLA_ERR_DEVICE_TIMEOUT);
     if (warp == 0) tmem_dealloc(tmem, TM_COLS);
 }
 

@@ -145,7 +145,7 @@ std::atomic<unsigned long long> g_wait_limit_ns{0};
 std::atomic<int> g_debug_stall{0};
 }
 
-bool debug_stall() { return g_debug_stall.load(std::memory_order_relaxed) != 0; }
+int debug_stall() { return g_debug_stall.load(std::memory_order_relaxed); }
 
 unsigned long long wait_limit_ns() {
     const unsigned long long v = g_wait_limit_ns.load(std::memory_order_relaxed);
@@ -612,7 +612,7 @@ const char *efla_get_error_string(efla_status s) {
 
 void efla_debug_set_wait_limit_ns(unsigned long long ns) { set_wait_limit_ns(ns); }
 
-void efla_debug_set_stall(int stall) { g_debug_stall.store(stall ? 1 : 0, std::memory_order_relaxed); }
+void efla_debug_set_stall(int stall) { g_debug_stall.store(stall & 7, std::memory_order_relaxed); }
 
 const char *efla_last_error(void) { return g_last_error.c_str(); }
 

@@ -16,9 +16,11 @@ namespace efla {
 int *device_status_ptr();
 // Bound on the chunk kernel's inter-role waits, in ns (efla_debug_set_wait_limit_ns; 2 s by default).
 unsigned long long wait_limit_ns();
-// Test hook (efla_debug_set_stall): the chunk kernel's MMA thread first waits on a barrier
-// that nothing completes, so that wait runs out and the kernel takes its abort path.
-bool debug_stall();
+// Test hook (efla_debug_set_stall): bit STALL_CHUNK, STALL_BWD_STATE or STALL_BWD_GRAD makes
+// that tensor-core kernel's MMA thread first wait on a barrier that nothing completes, so the
+// wait runs out and the kernel takes its abort path.
+enum { STALL_CHUNK = 1, STALL_BWD_STATE = 2, STALL_BWD_GRAD = 4 };
+int debug_stall();
 
 struct FwdArgs {
     const void *q, *k, *v;

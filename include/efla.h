@@ -337,13 +337,15 @@ const char *efla_get_error_string(efla_status status);
  * tensor memory keep their 2 s bound whatever this is set to. */
 void efla_debug_set_wait_limit_ns(unsigned long long ns);
 
-/* Test hook: with stall != 0, each launch of the tensor-core chunk kernel made
- * after the call has its tensor-core issuing thread first wait on a barrier that
- * nothing completes.  That wait runs out after the wait limit above; the kernel
- * then abandons its work, lets its own copies and tensor-core operations finish,
- * records EFLA_ERR_DEVICE_TIMEOUT in the status word and returns (its outputs are
- * unspecified).  This exercises the bounded-wait path without any fault.
- * stall = 0 (the default) restores normal launches. */
+/* Test hook: stall is a set of bits, each naming a tensor-core kernel: 1 the chunk
+ * kernel (the forward, also the first step of efla_bwd_chunked), 2 the backward's
+ * state pass, 4 the backward's per-chunk gradient kernel.  Each launch of a named
+ * kernel made after the call has its tensor-core issuing thread first wait on a
+ * barrier that nothing completes.  That wait runs out after the wait limit above;
+ * the kernel then abandons its work, lets its own copies and tensor-core
+ * operations finish, records EFLA_ERR_DEVICE_TIMEOUT in the status word and
+ * returns (its outputs are unspecified).  This exercises the bounded-wait path
+ * without any fault.  stall = 0 (the default) restores normal launches. */
 void efla_debug_set_stall(int stall);
 
 /* Reason for the most recent failing call on this host thread ("" if none). */

@@ -1,7 +1,8 @@
 """Device-side failure paths, exercised without any GPU fault.
 
-* A bounded wait that runs out: a test hook makes the chunk kernel's tensor-core issuing
-  thread wait on a barrier that nothing completes, with a short wait bound.  The kernel
+* A bounded wait that runs out: a test hook makes a tensor-core kernel's issuing thread (the
+  chunk kernel's, or the backward state pass's or gradient kernel's) wait on a barrier that
+  nothing completes, with a short wait bound.  The kernel
   must abandon its work, let its own copies and tensor-core operations finish, record
   EFLA_ERR_DEVICE_TIMEOUT in the device status word and return; the context stays usable
   and the next normal call is correct.
@@ -9,6 +10,7 @@
   sequence and record EFLA_ERR_INVALID_ARG; memory around the outputs is untouched, and a
   sequence that no other range overlaps is still correct.
 """
+import numpy as np
 import pytest
 import torch
 
@@ -57,6 +59,41 @@ def test_wait_expiry_reports_timeout_and_context_survives(efla, T):
     o_ref, S_ref = oracle.fwd(inp["q"], inp["k"], inp["v"], inp["beta"], inp["S0"], threads=0)
     check(o, o_ref, in_dtype="bf16", what="o after a timed-out launch")
     check(S, S_ref, in_dtype="bf16", what="S_T after a timed-out launch")
+    assert efla.device_status() == 0
+
+
+@pytest.mark.parametrize("stall,which", [(2, "state pass"), (4, "gradient kernel")])
+def test_backward_wait_expiry_reports_timeout_and_context_survives(efla, stall, which):
+    """The same for the backward's two tensor-core kernels (bf16, d = 128): a stalled state
+    pass or per-chunk gradient kernel records EFLA_ERR_DEVICE_TIMEOUT and returns; the next
+    backward call is correct."""
+    g = torch.Generator().manual_seed(79)
+    B, T, H, d = 1, 150, 2, 128
+    q = torch.randn((B, T, H, d), generator=g).to(torch.bfloat16)
+    k = torch.nn.functional.normalize(torch.randn((B, T, H, d), generator=g), dim=-1).to(torch.bfloat16)
+    v = torch.randn((B, T, H, d), generator=g).to(torch.bfloat16)
+    beta = torch.sigmoid(torch.randn((B, T, H), generator=g))
+    dO = torch.randn((B, T, H, d), generator=g)
+    dST = torch.randn((B, H, d, d), generator=g)
+    args = [x.to(DEV) for x in (q, k, v, beta)] + [None, dO.to(DEV), dST.to(DEV)]
+    assert efla.device_status() == 0
+    efla.set_wait_limit_ns(50_000_000)  # 50 ms
+    efla.set_debug_stall(stall)
+    try:
+        efla.bwd_chunked(*args)
+        torch.cuda.synchronize()
+    finally:
+        efla.set_debug_stall(False)
+        efla.set_wait_limit_ns(0)
+    assert efla.device_status() == TIMEOUT, which
+    assert efla.device_status() == 0
+    got = efla.bwd_chunked(*args)
+    torch.cuda.synchronize()
+    ref = oracle.bwd(q, k, v, beta, None, dO, dST)
+    for name in ("dq", "dk", "dv", "dbeta"):
+        a = got[name].double().cpu().numpy()
+        r = np.linalg.norm(a - ref[name]) / np.linalg.norm(ref[name])
+        assert r <= 1e-4, f"{name} after a timed-out {which}: rel-fro {r:.3e}"
     assert efla.device_status() == 0
 
 
