@@ -498,6 +498,14 @@ def bwd_figure(efla, dev, stream, q, k, v, beta, flush, peaks, steps=3):
     t = time_steps(lambda: efla.bwd_chunked(q, k, v, beta, None, dO, dST, workspace=ws, stream=stream), steps,
                    flush, stream)
     t_rec = time_steps(lambda: efla.bwd_recurrent(q, k, v, beta, None, dO, dST, stream=stream), 1, flush, stream)
+    # training: the forward that keeps the chunk-start states and T'' for the backward, and the
+    # backward from them (the workspace is not changed by the backward, so the timed calls reuse it)
+    o_t = torch.empty_like(q)
+    S_t = torch.empty((B, H, dk, dv), dtype=torch.float32, device=dev)
+    t_train = time_steps(lambda: efla.fwd_chunked_train(q, k, v, beta, None, workspace=ws, o=o_t, S_T=S_t,
+                                                        stream=stream), steps, flush, stream)
+    t_saved = time_steps(lambda: efla.bwd_chunked(q, k, v, beta, None, dO, dST, workspace=ws, saved=True,
+                                                  stream=stream), steps, flush, stream)
     th = B * T * H
     # each input read once and each output written once: q, k, v bf16 + beta + dO fp32 in; dq, dk, dv fp32 +
     # dbeta out; dS_T in and dS0 out per (b, h)
@@ -512,7 +520,12 @@ def bwd_figure(efla, dev, stream, q, k, v, beta, flush, peaks, steps=3):
                     "into bf16 hi/lo; reverse pass over chunks for the end-state gradients on the tensor cores (one "
                     "CTA per (b, h)), also writing G, dv and -dR (hi/lo); per-chunk gradients on the tensor cores "
                     "(persistent CTAs over the (b, h, chunk) items)",
-            "ms_recurrent": 1e3 * t_rec, "gpu_launches": 4 * steps + 1}
+            "ms_recurrent": 1e3 * t_rec,
+            "training": {"ms_forward_keeping_states": 1e3 * t_train, "ms_backward_from_saved": 1e3 * t_saved,
+                         "ms_step": 1e3 * (t_train + t_saved),
+                         "note": "efla_fwd_chunked_train then efla_bwd_chunked_saved: the backward does not "
+                                 "run the forward again"},
+            "gpu_launches": 4 * steps + 1 + steps + 3 * steps}
 
 
 def stiff_figure(efla, dev, stream, steps, flush, peaks):

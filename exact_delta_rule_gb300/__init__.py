@@ -25,6 +25,7 @@ import torch
 
 __all__ = ["EflaError", "lib_path", "load", "fwd_chunked", "fwd_chunked_scan", "fwd_chunked_scan_static",
            "scan_workspace", "fwd_recurrent", "decode_step", "decode_tokens", "bwd_recurrent", "bwd_chunked",
+           "fwd_chunked_train",
            "bwd_workspace", "prep", "device_status", "error_string", "set_wait_limit_ns", "set_debug_stall", "abi_version", "STATUS", "UPDATES"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -80,6 +81,10 @@ def load():
         L.efla_bwd_chunked.argtypes = [vp] * 12 + [ip] * 7 + [vp, ctypes.c_size_t, vp]
         L.efla_bwd_workspace.restype = ip
         L.efla_bwd_workspace.argtypes = [ip] * 5 + [ctypes.POINTER(ctypes.c_size_t)]
+        L.efla_bwd_chunked_saved.restype = ip
+        L.efla_bwd_chunked_saved.argtypes = [vp] * 12 + [ip] * 7 + [vp, ctypes.c_size_t, vp]
+        L.efla_fwd_chunked_train.restype = ip
+        L.efla_fwd_chunked_train.argtypes = [vp] * 7 + [ip] * 7 + [vp, ctypes.c_size_t, vp]
         L.efla_decode_tokens.restype = ip
         L.efla_decode_tokens.argtypes = [vp] * 6 + [ip] * 8 + [vp]
         L.efla_prep.restype = ip
@@ -338,10 +343,38 @@ def bwd_workspace(B: int, T: int, H: int, dk: int = 128, dv: int = 128) -> int:
 def bwd_chunked(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor,
                 S0: Optional[torch.Tensor], dO: torch.Tensor, dS_T: Optional[torch.Tensor] = None, *,
                 need_dS0: bool = True, workspace: Optional[torch.Tensor] = None, stream=None,
-                update: str = "exact") -> dict:
+                update: str = "exact", saved: bool = False) -> dict:
     """``bwd_recurrent`` evaluated in chunks of 64 tokens (``efla_bwd_chunked``); ``workspace``
-    (a CUDA tensor of at least ``bwd_workspace(...)`` bytes) is allocated here when not given."""
-    return _bwd("chunked", q, k, v, beta, S0, dO, dS_T, need_dS0, workspace, stream, update)
+    (a CUDA tensor of at least ``bwd_workspace(...)`` bytes) is allocated here when not given.
+    ``saved=True`` (``efla_bwd_chunked_saved``) takes the workspace that ``fwd_chunked_train``
+    filled for these inputs and does not run the forward again."""
+    if saved and workspace is None:
+        raise EflaError(1, "saved=True needs the workspace that fwd_chunked_train filled")
+    return _bwd("saved" if saved else "chunked", q, k, v, beta, S0, dO, dS_T, need_dS0, workspace, stream, update)
+
+
+def fwd_chunked_train(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor,
+                      S0: Optional[torch.Tensor] = None, *, workspace: Optional[torch.Tensor] = None,
+                      o: Optional[torch.Tensor] = None, S_T: Optional[torch.Tensor] = None, stream=None,
+                      update: str = "exact") -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    """``fwd_chunked`` (rows of [B, T], o in q's dtype) that also keeps, in ``workspace``, what
+    ``bwd_chunked`` would recompute (``efla_fwd_chunked_train``).  Returns (o, S_T, workspace);
+    pass the workspace to ``bwd_chunked(..., workspace=..., saved=True)`` with the same inputs."""
+    L = load()
+    _need(workspace, "workspace")
+    B, T, H, dk, dv, N = _check_fwd_inputs(q, k, v, beta, S0)
+    o, S_T = _outputs(q, o, S_T, None, True, B, T, H, dk, dv, N)
+    if o.dtype != q.dtype:
+        raise EflaError(1, "o must have q's dtype")
+    if update not in UPDATES:
+        raise EflaError(1, f"unknown update rule {update!r}")
+    need = bwd_workspace(B, T, H, dk, dv)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    _check(L.efla_fwd_chunked_train(_p(q), _p(k), _p(v), _p(beta), _p(S0), _p(o), _p(S_T), B, T, H, dk, dv,
+                                    _dt(q.dtype), UPDATES[update], _p(workspace),
+                                    workspace.numel() * workspace.element_size(), _stream(stream)))
+    return o, S_T, workspace
 
 
 def bwd_recurrent(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor,
@@ -380,7 +413,8 @@ def _bwd(kind, q, k, v, beta, S0, dO, dS_T, need_dS0, workspace, stream, update)
     need = bwd_workspace(B, T, H, dk, dv)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
-    _check(L.efla_bwd_chunked(*args, _p(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+    fn = L.efla_bwd_chunked_saved if kind == "saved" else L.efla_bwd_chunked
+    _check(fn(*args, _p(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
     return out
 
 

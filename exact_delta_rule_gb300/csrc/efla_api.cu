@@ -374,10 +374,13 @@ efla_status efla_bwd_workspace(int B, int T, int H, int d_k, int d_v, size_t *by
     return EFLA_OK;
 }
 
-efla_status efla_bwd_chunked(const void *q, const void *k, const void *v, const float *beta, const float *S0,
-                             const float *dO, const float *dS_T, float *dq, float *dk, float *dv, float *dbeta,
-                             float *dS0, int B, int T, int H, int d_k, int d_v, efla_dtype in_dtype,
-                             efla_update update, void *workspace, size_t workspace_bytes, efla_stream_t stream) {
+// The chunked backward; with `saved`, the workspace already holds the chunk-start states and T''
+// tiles of this forward (efla_fwd_chunked_train) and the forward is not run again.
+static efla_status bwd_chunked_impl(const void *q, const void *k, const void *v, const float *beta, const float *S0,
+                                    const float *dO, const float *dS_T, float *dq, float *dk, float *dv, float *dbeta,
+                                    float *dS0, int B, int T, int H, int d_k, int d_v, efla_dtype in_dtype,
+                                    efla_update update, void *workspace, size_t workspace_bytes, efla_stream_t stream,
+                                    bool saved) {
     if (!update_ok(update)) return fail(EFLA_ERR_INVALID_ARG, "unknown update rule %d", (int)update);
     if (B < 0 || T < 0 || H <= 0) return fail(EFLA_ERR_INVALID_ARG, "bad sizes B=%d T=%d H=%d", B, T, H);
     efla_status s = check_dims_common(d_k, d_v, in_dtype, EFLA_F32);
@@ -427,7 +430,7 @@ efla_status efla_bwd_chunked(const void *q, const void *k, const void *v, const 
     float *g_tok = reinterpret_cast<float *>(static_cast<char *>(do_split) + 2 * (size_t)B * T * H * d_v * 2);
     void *dr_split = g_tok + (size_t)B * T * H * d_v;
     cudaError_t e;
-    if (T > 0) {  // the forward, keeping the state at the start of every chunk (o and S_T not needed)
+    if (T > 0 && !saved) {  // the forward, keeping the state at the start of every chunk (o and S_T not needed)
         FwdArgs fa{q, k, v, beta, S0, nullptr, nullptr, nullptr, B, T, H, d_k, d_v, B, in_dtype, in_dtype,
                    64, cs, status, (int)update};
         fa.states = states;
@@ -447,6 +450,64 @@ efla_status efla_bwd_chunked(const void *q, const void *k, const void *v, const 
         e = launch_bwd_chunked(a, states, dse);
         if (e != cudaSuccess) return cuda_fail(e, "chunked backward kernel launch");
     }
+    g_last_error.clear();
+    return EFLA_OK;
+}
+
+efla_status efla_bwd_chunked(const void *q, const void *k, const void *v, const float *beta, const float *S0,
+                             const float *dO, const float *dS_T, float *dq, float *dk, float *dv, float *dbeta,
+                             float *dS0, int B, int T, int H, int d_k, int d_v, efla_dtype in_dtype,
+                             efla_update update, void *workspace, size_t workspace_bytes, efla_stream_t stream) {
+    return bwd_chunked_impl(q, k, v, beta, S0, dO, dS_T, dq, dk, dv, dbeta, dS0, B, T, H, d_k, d_v, in_dtype, update,
+                            workspace, workspace_bytes, stream, false);
+}
+
+efla_status efla_bwd_chunked_saved(const void *q, const void *k, const void *v, const float *beta, const float *S0,
+                                   const float *dO, const float *dS_T, float *dq, float *dk, float *dv,
+                                   float *dbeta, float *dS0, int B, int T, int H, int d_k, int d_v,
+                                   efla_dtype in_dtype, efla_update update, void *workspace, size_t workspace_bytes,
+                                   efla_stream_t stream) {
+    return bwd_chunked_impl(q, k, v, beta, S0, dO, dS_T, dq, dk, dv, dbeta, dS0, B, T, H, d_k, d_v, in_dtype, update,
+                            workspace, workspace_bytes, stream, true);
+}
+
+efla_status efla_fwd_chunked_train(const void *q, const void *k, const void *v, const float *beta, const float *S0,
+                                   void *o, float *S_T, int B, int T, int H, int d_k, int d_v, efla_dtype in_dtype,
+                                   efla_update update, void *workspace, size_t workspace_bytes,
+                                   efla_stream_t stream) {
+    if (!update_ok(update)) return fail(EFLA_ERR_INVALID_ARG, "unknown update rule %d", (int)update);
+    FwdArgs a{q, k, v, beta, S0, nullptr, o, S_T, B, T, H, d_k, d_v, B, in_dtype, in_dtype, 64,
+              reinterpret_cast<cudaStream_t>(stream), nullptr, (int)update};
+    efla_status s = validate_fwd(a, true);
+    if (s != EFLA_OK) return s;
+    size_t need = 0;
+    if ((s = efla_bwd_workspace(B, T, H, d_k, d_v, &need)) != EFLA_OK) return s;
+    if (need > 0 && (!workspace || workspace_bytes < need))
+        return fail(EFLA_ERR_INVALID_ARG, "workspace of %zu bytes needed (got %zu at %p)", need, workspace_bytes,
+                    workspace);
+    if (workspace && !aligned16(workspace))
+        return fail(EFLA_ERR_INVALID_ARG, "workspace=%p is not 16-byte aligned", workspace);
+    const size_t th = (size_t)B * T * H, st = (size_t)B * H * d_k * d_v * 4;
+    auto R = [](const char *n, const void *p, size_t bytes) {
+        uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+        return Range{n, lo, p ? lo + bytes : lo};
+    };
+    const Range ws = R("workspace", workspace, need);
+    const Range others[] = {R("q", q, th * d_k * dsize(in_dtype)), R("k", k, th * d_k * dsize(in_dtype)),
+                            R("v", v, th * d_v * dsize(in_dtype)), R("beta", beta, th * 4), R("S0", S0, st),
+                            R("o", o, th * d_v * dsize(in_dtype)), R("S_T", S_T, st)};
+    for (const Range &r : others)
+        if (overlap(ws, r)) return fail(EFLA_ERR_INVALID_ARG, "workspace overlaps %s", r.name);
+    if ((long long)B * H == 0 || T == 0) return run_fwd(a, true);
+    a.status = device_status_ptr();
+    if (!a.status) return fail(EFLA_ERR_CUDA, "cannot resolve the device status word");
+    const size_t state_floats = (size_t)B * H * (((size_t)T + 63) / 64) * d_k * d_v;
+    a.states = static_cast<float *>(workspace);
+    a.tpp = reinterpret_cast<uint8_t *>(a.states + 2 * state_floats);  // the layout efla_bwd_chunked uses
+    cudaError_t e;
+    const char *why = "chunk kernel launch (training forward)";
+    e = in_dtype == EFLA_BF16 && d_k == 128 ? launch_chunk_tc(a, &why) : launch_chunk_simt(a);
+    if (e != cudaSuccess) return cuda_fail(e, why);
     g_last_error.clear();
     return EFLA_OK;
 }

@@ -45,7 +45,7 @@
 extern "C" {
 #endif
 
-#define EFLA_ABI_VERSION 9
+#define EFLA_ABI_VERSION 10
 
 typedef enum {
     EFLA_OK = 0,
@@ -255,6 +255,36 @@ efla_status efla_bwd_chunked(const void *q, const void *k, const void *v, const 
 
 /* Workspace bytes efla_bwd_chunked needs for these sizes (into *bytes). */
 efla_status efla_bwd_workspace(int B, int T, int H, int d_k, int d_v, size_t *bytes);
+
+/*
+ * efla_fwd_chunked_train -- efla_fwd_chunked (rows of [B, T], no cu_seqlens, o in q's dtype,
+ * chunk 64) that also keeps what the chunked backward would otherwise recompute: the state at
+ * the start of every chunk (and, for bf16 with d = 128, every chunk's T'') go into `workspace`,
+ * laid out as efla_bwd_chunked lays them out.  A later efla_bwd_chunked_saved with the same
+ * inputs and that workspace then skips its forward.  The reverse mode of training: the forward
+ * keeps its activations for the backward ("Error-Free Linear Attention is a Free Lunch"
+ * (howistudyai), Step 4 "Chunkwise Parallelism").
+ *   workspace  device scratch owned by the caller, 16-byte aligned, at least the size
+ *              efla_bwd_workspace reports; it must not overlap any argument.
+ * Supported: d_k = d_v in {64, 128}.  Errors as efla_fwd_chunked and efla_bwd_chunked.
+ */
+efla_status efla_fwd_chunked_train(const void *q, const void *k, const void *v, const float *beta,
+                                   const float *S0, void *o, float *S_T, int B, int T, int H, int d_k,
+                                   int d_v, efla_dtype in_dtype, efla_update update, void *workspace,
+                                   size_t workspace_bytes, efla_stream_t stream);
+
+/*
+ * efla_bwd_chunked_saved -- efla_bwd_chunked on a workspace that efla_fwd_chunked_train filled
+ * for the same q, k, v, beta, S0, sizes, dtype and update rule, without running the forward
+ * again; the same arguments, outputs and rules.  That the workspace matches the inputs is the
+ * caller's contract and is not checked: other contents give unspecified gradients (every access
+ * still stays inside the workspace).
+ */
+efla_status efla_bwd_chunked_saved(const void *q, const void *k, const void *v, const float *beta,
+                                   const float *S0, const float *dO, const float *dS_T, float *dq,
+                                   float *dk, float *dv, float *dbeta, float *dS0, int B, int T, int H,
+                                   int d_k, int d_v, efla_dtype in_dtype, efla_update update,
+                                   void *workspace, size_t workspace_bytes, efla_stream_t stream);
 
 /*
  * efla_decode_tokens -- m tokens per sequence appended to a resident state,

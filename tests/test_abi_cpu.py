@@ -288,31 +288,65 @@ def test_bwd_rejects(lib, kw, code):
     assert _last(lib)
 
 
-def _bwc(lib, ws=0xA0000000, ws_bytes=None, **kw):
+def _bwd_need(lib, B, T, H, dk, dv):
+    f = lib.efla_bwd_workspace
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_int] * 5 + [ctypes.POINTER(ctypes.c_size_t)]
+    n = ctypes.c_size_t(0)
+    return n.value if f(B, T, H, dk, dv, ctypes.byref(n)) == 0 else 1 << 20
+
+
+def _bwc(lib, ws=0xA0000000, ws_bytes=None, entry="efla_bwd_chunked", **kw):
     a = dict(q=Q, k=K, v=V, beta=BETA, S0=None, dO=CU, dST=None, dq=O, dk=ST, dv=S0, db=0x90000000, dS0=None,
              B=1, T=64, H=2, dk_=128, dv_=128, ind=0, upd=0)
     a.update(kw)
     vp, ip = ctypes.c_void_p, ctypes.c_int
-    f = lib.efla_bwd_chunked
+    f = getattr(lib, entry)
     f.restype = ip
     f.argtypes = [vp] * 12 + [ip] * 7 + [vp, ctypes.c_size_t, vp]
-    need = 2 * a["B"] * a["H"] * ((max(a["T"], 0) + 63) // 64) * a["dk_"] * a["dv_"] * 4 + \
-        2 * a["B"] * max(a["T"], 0) * a["H"] * a["dv_"] * 2 + a["B"] * max(a["T"], 0) * a["H"] * a["dv_"] * 4
+    need = _bwd_need(lib, a["B"], max(a["T"], 0), max(a["H"], 1), a["dk_"], a["dv_"])
     return f(a["q"], a["k"], a["v"], a["beta"], a["S0"], a["dO"], a["dST"], a["dq"], a["dk"], a["dv"], a["db"],
              a["dS0"], a["B"], a["T"], a["H"], a["dk_"], a["dv_"], a["ind"], a["upd"], ws,
              need if ws_bytes is None else ws_bytes, None)
 
 
+@pytest.mark.parametrize("entry", ["efla_bwd_chunked", "efla_bwd_chunked_saved"])
 @pytest.mark.parametrize("kw,code", [
     (dict(T=-1), INVALID), (dict(H=0), INVALID), (dict(dk_=64, dv_=128), UNSUPPORTED),
     (dict(dk_=32, dv_=32), UNSUPPORTED), (dict(dq=None), INVALID), (dict(upd=3), INVALID),
     (dict(ws=None), INVALID), (dict(ws_bytes=1024), INVALID), (dict(ws=0xA0000000 + 8), INVALID),
     (dict(ws=Q), INVALID),
 ])
-def test_bwd_chunked_rejects(lib, kw, code):
-    """efla_bwd_chunked validates sizes, the supported shapes (d_k = d_v in {64, 128}) and its
-    workspace (present, large enough, aligned, overlapping no argument) before any launch."""
-    assert _bwc(lib, **kw) == code
+def test_bwd_chunked_rejects(lib, entry, kw, code):
+    """efla_bwd_chunked and efla_bwd_chunked_saved validate sizes, the supported shapes
+    (d_k = d_v in {64, 128}) and their workspace (present, large enough, aligned, overlapping no
+    argument) before any launch."""
+    assert _bwc(lib, entry=entry, **kw) == code
+    assert _last(lib)
+
+
+def _fwt(lib, ws=0xA0000000, ws_bytes=None, **kw):
+    a = dict(q=Q, k=K, v=V, beta=BETA, S0=None, o=O, S_T=ST, B=1, T=64, H=2, dk_=128, dv_=128, ind=0, upd=0)
+    a.update(kw)
+    vp, ip = ctypes.c_void_p, ctypes.c_int
+    f = lib.efla_fwd_chunked_train
+    f.restype = ip
+    f.argtypes = [vp] * 7 + [ip] * 7 + [vp, ctypes.c_size_t, vp]
+    need = _bwd_need(lib, a["B"], max(a["T"], 0), max(a["H"], 1), a["dk_"], a["dv_"])
+    return f(a["q"], a["k"], a["v"], a["beta"], a["S0"], a["o"], a["S_T"], a["B"], a["T"], a["H"], a["dk_"],
+             a["dv_"], a["ind"], a["upd"], ws, need if ws_bytes is None else ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(T=-1), INVALID), (dict(H=0), INVALID), (dict(dk_=32, dv_=32), UNSUPPORTED),
+    (dict(dk_=64, dv_=128), UNSUPPORTED), (dict(o=None), INVALID), (dict(upd=3), INVALID),
+    (dict(ws=None), INVALID), (dict(ws_bytes=1024), INVALID), (dict(ws=0xA0000000 + 8), INVALID),
+    (dict(ws=Q), INVALID),
+])
+def test_fwd_chunked_train_rejects(lib, kw, code):
+    """efla_fwd_chunked_train validates as efla_fwd_chunked does, plus the backward's supported
+    shapes and its workspace, before any launch."""
+    assert _fwt(lib, **kw) == code
     assert _last(lib)
 
 

@@ -79,6 +79,29 @@ def test_bwd_chunked_small(efla, d, dtype, T):
     _check(efla, _case(dtype, 2, T, 2, d, d, seed=d + T), kind="chunked")
 
 
+@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("bf16", 64), ("f32", 128)])
+def test_train_forward_then_saved_backward(efla, dtype, d):
+    """fwd_chunked_train gives fwd_chunked's o and S_T bit for bit and keeps the chunk-start
+    states (and T'') in the workspace; bwd_chunked(saved=True) on that workspace gives the
+    gradients of bwd_chunked (which runs the forward again) and of the oracle."""
+    c = _case(dtype, 2, 200, 3, d, d, seed=300 + d)
+    g = {x: (y.to(DEV) if y is not None else None) for x, y in c.items()}
+    o_ref, S_ref = efla.fwd_chunked(g["q"], g["k"], g["v"], g["beta"], g["S0"])
+    o, S_T, ws = efla.fwd_chunked_train(g["q"], g["k"], g["v"], g["beta"], g["S0"])
+    torch.cuda.synchronize()
+    assert torch.equal(o, o_ref) and torch.equal(S_T, S_ref)
+    got = efla.bwd_chunked(g["q"], g["k"], g["v"], g["beta"], g["S0"], g["dO"], g["dST"], workspace=ws, saved=True)
+    full = efla.bwd_chunked(g["q"], g["k"], g["v"], g["beta"], g["S0"], g["dO"], g["dST"])
+    torch.cuda.synchronize()
+    ref = oracle.bwd(c["q"], c["k"], c["v"], c["beta"], c["S0"], c["dO"], c["dST"])
+    for name in ("dq", "dk", "dv", "dbeta", "dS0"):
+        same = ((got[name] - full[name]).norm() / full[name].norm()).item()
+        assert same <= 1e-6, f"{name}: saved vs full backward rel-fro {same:.3e}"
+        r = _rel(got[name], ref[name])
+        assert r <= REL, f"{name}: rel-fro {r:.3e}"
+    assert efla.device_status() == 0
+
+
 @pytest.mark.parametrize("kind", KINDS)
 def test_bwd_no_state_no_state_gradient(efla, kind):
     _check(efla, _case("bf16", 1, 64, 3, 128, 128, seed=4, s0=False, dst=False), kind=kind)
