@@ -581,7 +581,6 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
                 uint32_t hi[16], lo[16];
                 tmem_ld32(lane_base + TM_S + g * 32, sv);
                 tmem_ld_wait();
-                if (st_c) put_col_split_tile(st_c, g * 32, j, sv);
                 split_pack<16>(sv, hi, lo);
                 tmem_st16u(lane_base + TM_SA + g * 16, hi);
                 tmem_st16u(lane_base + TM_SA + 64 + g * 16, lo);
@@ -589,6 +588,15 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(&bars->sa_ready);
+            if (st_c) {  // while the tensor core forms X: TM_S changes only at this chunk's state update
+#pragma unroll 1
+                for (int g = 0; g < 4; g = opaque(g + 1)) {
+                    float sv[32];
+                    tmem_ld32(lane_base + TM_S + g * 32, sv);
+                    tmem_ld_wait();
+                    put_col_split_tile(st_c, g * 32, j, sv);
+                }
+            }
             if (c >= 2) release_staging(c - 2);  // its stores were issued during chunk c - 1
             const long tok0 = bos + (long)c * C;
             const int valid = (int)min((long)C, eos - tok0);
