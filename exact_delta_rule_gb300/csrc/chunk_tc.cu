@@ -588,15 +588,18 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(&bars->sa_ready);
-            if (st_c) {  // while the tensor core forms X: TM_S changes only at this chunk's state update
+            // with `states`, rows 0-63 of the start state go out while the tensor core forms X and
+            // rows 64-127 while it forms u (TM_S changes only at this chunk's state update)
+            auto dump_state = [&](int g0) {
 #pragma unroll 1
-                for (int g = 0; g < 4; g = opaque(g + 1)) {
+                for (int g = g0; g < g0 + 2; g = opaque(g + 1)) {
                     float sv[32];
                     tmem_ld32(lane_base + TM_S + g * 32, sv);
                     tmem_ld_wait();
                     put_col_split_tile(st_c, g * 32, j, sv);
                 }
-            }
+            };
+            if (st_c) dump_state(0);
             if (c >= 2) release_staging(c - 2);  // its stores were issued during chunk c - 1
             const long tok0 = bos + (long)c * C;
             const int valid = (int)min((long)C, eos - tok0);
@@ -625,6 +628,7 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(&bars->r_ready);
+            if (st_c) dump_state(2);
             ok = wait_bar_warp(&bars->u_done, c & 1, abort_flag, wait_ns);
             if (!ok) break;
             tc_fence_after();
