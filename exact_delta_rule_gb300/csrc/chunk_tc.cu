@@ -170,6 +170,19 @@ __device__ __forceinline__ void issue_gram(uint32_t tmem, uint32_t s_sm, int c, 
     mma_commit(&bars->g_done);
 }
 
+// Rows 32 g0 .. 32 g0 + 63 of the state S (column j = this thread's TMEM lane, TMEM address
+// ts of S^T) into the backward's operand tile.  Out of line: only the forward that keeps its
+// chunk states calls it, and the per-chunk loop's code stays small for the instruction cache.
+__device__ __noinline__ void dump_state_rows(uint8_t *tile, uint32_t ts, int g0, int j) {
+#pragma unroll 1
+    for (int g = g0; g < g0 + 2; ++g) {
+        float sv[32];
+        tmem_ld32(ts + g * 32, sv);
+        tmem_ld_wait();
+        put_col_split_tile(tile, g * 32, j, sv);
+    }
+}
+
 template <bool OUT_BF16>
 __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant__ TcParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -590,16 +603,7 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
             mbar_arrive(&bars->sa_ready);
             // with `states`, rows 0-63 of the start state go out while the tensor core forms X and
             // rows 64-127 while it forms u (TM_S changes only at this chunk's state update)
-            auto dump_state = [&](int g0) {
-#pragma unroll 1
-                for (int g = g0; g < g0 + 2; g = opaque(g + 1)) {
-                    float sv[32];
-                    tmem_ld32(lane_base + TM_S + g * 32, sv);
-                    tmem_ld_wait();
-                    put_col_split_tile(st_c, g * 32, j, sv);
-                }
-            };
-            if (st_c) dump_state(0);
+            if (st_c) dump_state_rows(st_c, lane_base + TM_S, 0, j);
             if (c >= 2) release_staging(c - 2);  // its stores were issued during chunk c - 1
             const long tok0 = bos + (long)c * C;
             const int valid = (int)min((long)C, eos - tok0);
@@ -628,7 +632,7 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(&bars->r_ready);
-            if (st_c) dump_state(2);
+            if (st_c) dump_state_rows(st_c, lane_base + TM_S, 2, j);
             ok = wait_bar_warp(&bars->u_done, c & 1, abort_flag, wait_ns);
             if (!ok) break;
             tc_fence_after();
