@@ -102,6 +102,29 @@ def test_train_forward_then_saved_backward(efla, dtype, d):
     assert efla.device_status() == 0
 
 
+@pytest.mark.parametrize("B,T,H,s0,dst", [(1, 1, 1, True, True), (1, 64, 2, False, True), (2, 65, 3, True, False),
+                                           (1, 129, 2, False, False)])
+def test_train_pair_edge_shapes(efla, B, T, H, s0, dst):
+    """The training pair (bf16, d = 128, every step on the tensor cores) on a single token, one
+    full chunk, a full chunk and one token, and a ragged third chunk, with and without S0 and
+    dS_T: o and S_T bit for bit those of fwd_chunked, the saved backward against the oracle, and
+    the workspace reused by a second pair on other inputs of the same shape."""
+    ws = None
+    for seed in (400 + T, 500 + T):
+        c = _case("bf16", B, T, H, 128, 128, seed=seed, s0=s0, dst=dst)
+        g = {x: (y.to(DEV) if y is not None else None) for x, y in c.items()}
+        o, S_T, ws = efla.fwd_chunked_train(g["q"], g["k"], g["v"], g["beta"], g["S0"], workspace=ws)
+        got = efla.bwd_chunked(g["q"], g["k"], g["v"], g["beta"], g["S0"], g["dO"], g["dST"], workspace=ws, saved=True)
+        o_ref, S_ref = efla.fwd_chunked(g["q"], g["k"], g["v"], g["beta"], g["S0"])
+        torch.cuda.synchronize()
+        assert torch.equal(o, o_ref) and torch.equal(S_T, S_ref)
+        ref = oracle.bwd(c["q"], c["k"], c["v"], c["beta"], c["S0"], c["dO"], c["dST"])
+        for name in ("dq", "dk", "dv", "dbeta", "dS0"):
+            r = _rel(got[name], ref[name])
+            assert r <= REL, f"seed {seed} {name}: rel-fro {r:.3e}"
+    assert efla.device_status() == 0
+
+
 @pytest.mark.parametrize("kind", KINDS)
 def test_bwd_no_state_no_state_gradient(efla, kind):
     _check(efla, _case("bf16", 1, 64, 3, 128, 128, seed=4, s0=False, dst=False), kind=kind)
