@@ -52,11 +52,13 @@ constexpr uint32_t OFF_DOL = 49152;
 // Per chunk parity: T'' hi, lo, then P hi, lo, each [64][64] bf16 (8 KB).
 constexpr uint32_t OFF_TPP = NSTAGE * STAGE_BYTES;
 constexpr uint32_t TPP_BYTES = 32768;
-constexpr uint32_t OFF_BAR = OFF_TPP + 2 * TPP_BYTES;
+// -dR of a chunk as bf16 hi, then lo, [2 cb][64 rows][64] each (16 KB): the staging of its TMA stores
+constexpr uint32_t OFF_DRS = OFF_TPP + 2 * TPP_BYTES;
+constexpr uint32_t OFF_BAR = OFF_DRS + 32768;
 constexpr uint32_t OFF_MISC = OFF_BAR + 256;  // tmem base, abort flag
 constexpr uint32_t SMEM_USED = OFF_MISC + 16;
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;
-static_assert(OFF_TPP % 1024 == 0, "operand buffers must be 1024-byte aligned");
+static_assert(OFF_TPP % 1024 == 0 && OFF_DRS % 1024 == 0, "operand buffers must be 1024-byte aligned");
 static_assert(SMEM_ALLOC <= 232448, "exceeds the per-CTA shared memory limit");
 
 // TMEM columns
@@ -68,9 +70,11 @@ constexpr uint32_t TM_COLS = 512;
 
 constexpr uint64_t WAIT_NS = 2000000000ull;
 constexpr int BAR_PREP = 2;
+constexpr int BAR_STATE = 3;
 
 struct BtParams {
     CUtensorMap map_q, map_k, map_doh, map_dol;  // [B, T, H, 128] bf16: box 64 x 1 x 64 x 1, 128B swizzle
+    CUtensorMap map_drh, map_drl;                // the same over -dR as bf16 hi and lo (stores)
     const float *beta;                           // [B, T, H]
     const float *dST;                            // [B, H, 128, 128] or nullptr (zero)
     float *dse;                                  // [B, H, nchunks] x 64 KB: dS' of every chunk as bf16 hi/lo
@@ -78,7 +82,6 @@ struct BtParams {
     const uint8_t *tpp;                          // [B, H, nchunks] x 16 KB: the forward's T'' tiles
     float *dS0;                                  // [B, H, 128, 128] or nullptr
     float *g_out, *dr_out;                       // [B, T, H, 128] fp32: G and dR (= dv) of every token
-    __nv_bfloat16 *drs_hi, *drs_lo;              // [B, T, H, 128]: -dR as bf16 hi and lo
     int *status;
     int B, T, H;
     int euler;
@@ -147,6 +150,25 @@ __device__ __forceinline__ void store_cols(float *base, size_t row_stride, int v
 #pragma unroll
     for (int t = 0; t < 32; ++t)
         if (32 + t < valid) base[(size_t)(32 + t) * row_stride] = x1[t];
+}
+
+// Tokens 0-63 (x0: 0-31, x1: 32-63) of column j (this lane) of dR, negated, as bf16 hi and lo
+// (split_pack's split) into the staging tiles at stg: [2 column blocks][64 tokens][64] bf16 with
+// the 128-byte swizzle, hi then lo 16 KB on, the layout of the TMA boxes that store them.  Lanes
+// j and j ^ 1 pair up: the even lane writes the hi word of columns j, j + 1, the odd lane the lo.
+__device__ __forceinline__ void stage_neg_split(uint8_t *stg, int j, const float (&x0)[32], const float (&x1)[32]) {
+    const bool odd = (j & 1) != 0;
+    uint8_t *dst = stg + (odd ? 16384u : 0u);
+#pragma unroll
+    for (int t = 0; t < 64; ++t) {
+        const float v = -(t < 32 ? x0[t] : x1[t - 32]);
+        const uint32_t b = __float_as_uint(v);
+        const uint32_t h16 = b >> 16;
+        const uint32_t l16 = __float_as_uint(v - __uint_as_float(b & 0xffff0000u)) >> 16;
+        const uint32_t recv = __shfl_xor_sync(0xffffffffu, odd ? h16 : l16, 1);
+        *reinterpret_cast<uint32_t *>(dst + swz_offset(t, j & ~1, 8192)) =
+            odd ? (recv | (l16 << 16)) : (h16 | (recv << 16));
+    }
 }
 
 __global__ void __launch_bounds__(320, 1) bwd_tc_kernel(const __grid_constant__ BtParams p) {
@@ -270,56 +292,77 @@ __global__ void __launch_bounds__(320, 1) bwd_tc_kernel(const __grid_constant__ 
             tmem_st_wait();
         }
         bool ok = true;
-        for (int it = 0; it < nchunks && ok; ++it) {
+        uint8_t *stg = sm + OFF_DRS;
+        // A failed wait skips the work up to the chunk's consensus barrier, which every thread of
+        // the warpgroup reaches, so that the warpgroup leaves together.
+        for (int it = 0; it < nchunks; ++it) {
             if (it > 0) ok = wait_bar_warp(&bars->s_done, (it - 1) & 1, abort_flag, wait_ns);
-            if (!ok) break;
-            tc_fence_after();
-            // dS^T -> bf16 hi/lo operand
-#pragma unroll 1
-            for (int g = 0; g < 4; g = opaque(g + 1)) {
-                float sv[32];
-                uint32_t hi[16], lo[16];
-                tmem_ld32(lane_base + TM_S + g * 32, sv);
-                tmem_ld_wait();
-                split_pack<16>(sv, hi, lo);
-                tmem_st16u(lane_base + TM_SA + g * 16, hi);
-                tmem_st16u(lane_base + TM_SA + 64 + g * 16, lo);
-            }
-            tmem_st_wait();
-            tc_fence_before();
-            mbar_arrive(&bars->sa_ready);
-            {  // dS' of this chunk (the gradient of its end state) to HBM while the tensor core forms
-               // G^T; TM_S changes again only after r_ready, which this warpgroup arrives at later
-                uint8_t *dst = reinterpret_cast<uint8_t *>(p.dse + ((size_t)blockIdx.x * nchunks + chunk_of(it)) * D * D);
-#pragma unroll 1
-                for (int g = 0; g < 4; g = opaque(g + 1)) {
-                    float sv[32];
-                    tmem_ld32(lane_base + TM_S + g * 32, sv);
-                    tmem_ld_wait();
-                    put_col_split_tile(dst, g * 32, j, sv);
-                }
-            }
-            ok = wait_bar_warp(&bars->x_done, it & 1, abort_flag, wait_ns);
-            if (!ok) break;
-            tc_fence_after();
             const int c = chunk_of(it), valid = min(C, p.T - c * C);
             const size_t row0 = ((size_t)b * p.T + (size_t)c * C) * p.H + h;
             float x0[32], x1[32];
-            split64(lane_base, TM_X, 1.f, x0, x1);  // G^T
-            tc_fence_before();
-            mbar_arrive(&bars->r_ready);
-            // G for the per-chunk gradient kernel, sent while the tensor core forms dR
-            store_cols(p.g_out + row0 * D + j, (size_t)p.H * D, valid, x0, x1);
-            ok = wait_bar_warp(&bars->u_done, it & 1, abort_flag, wait_ns);
-            if (!ok) break;
-            tc_fence_after();
-            split64(lane_base, TM_SA, -1.f, x0, x1);  // -dR^T
-            tc_fence_before();
-            mbar_arrive(&bars->u_ready);
-            store_cols(p.dr_out + row0 * D + j, (size_t)p.H * D, valid, x0, x1);  // dv = dR
-            // -dR as bf16 hi/lo for the per-chunk gradient kernel
-            put_col_split_rows(p.drs_hi + row0 * D, p.drs_lo + row0 * D, (size_t)p.H * D, valid, 0, j, -1.f, x0);
-            put_col_split_rows(p.drs_hi + row0 * D, p.drs_lo + row0 * D, (size_t)p.H * D, valid, 32, j, -1.f, x1);
+            if (ok) {
+                tc_fence_after();
+                // dS^T -> bf16 hi/lo operand
+#pragma unroll 1
+                for (int g = 0; g < 4; g = opaque(g + 1)) {
+                    float sv[32];
+                    uint32_t hi[16], lo[16];
+                    tmem_ld32(lane_base + TM_S + g * 32, sv);
+                    tmem_ld_wait();
+                    split_pack<16>(sv, hi, lo);
+                    tmem_st16u(lane_base + TM_SA + g * 16, hi);
+                    tmem_st16u(lane_base + TM_SA + 64 + g * 16, lo);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(&bars->sa_ready);
+                {  // dS' of this chunk (the gradient of its end state) to HBM while the tensor core
+                   // forms G^T; TM_S changes again only after r_ready, which this warpgroup arrives at later
+                    uint8_t *dst = reinterpret_cast<uint8_t *>(p.dse + ((size_t)blockIdx.x * nchunks + c) * D * D);
+#pragma unroll 1
+                    for (int g = 0; g < 4; g = opaque(g + 1)) {
+                        float sv[32];
+                        tmem_ld32(lane_base + TM_S + g * 32, sv);
+                        tmem_ld_wait();
+                        put_col_split_tile(dst, g * 32, j, sv);
+                    }
+                }
+                ok = wait_bar_warp(&bars->x_done, it & 1, abort_flag, wait_ns);
+            }
+            if (ok) {
+                tc_fence_after();
+                split64(lane_base, TM_X, 1.f, x0, x1);  // G^T
+                tc_fence_before();
+                mbar_arrive(&bars->r_ready);
+                // G for the per-chunk gradient kernel, sent while the tensor core forms dR
+                store_cols(p.g_out + row0 * D + j, (size_t)p.H * D, valid, x0, x1);
+                ok = wait_bar_warp(&bars->u_done, it & 1, abort_flag, wait_ns);
+            }
+            if (ok) {
+                tc_fence_after();
+                split64(lane_base, TM_SA, -1.f, x0, x1);  // -dR^T
+                tc_fence_before();
+                mbar_arrive(&bars->u_ready);
+                store_cols(p.dr_out + row0 * D + j, (size_t)p.H * D, valid, x0, x1);  // dv = dR
+            }
+            // -dR as bf16 hi/lo for the per-chunk gradient kernel, staged in shared memory and
+            // stored by TMA (rows past the sequence end are clipped) once the previous chunk's
+            // stores have read the staging
+            if (tid == 0) bulk_wait_read0();
+            if (named_bar_any(BAR_STATE, 128, !ok)) {
+                ok = false;
+                break;
+            }
+            stage_neg_split(stg, j, x0, x1);
+            fence_proxy_async_smem();
+            named_bar(BAR_STATE, 128);
+            if (tid == 0) {
+                for (int cb = 0; cb < 2; ++cb) {
+                    tma_store_4d(&p.map_drh, stg + cb * 8192, cb * 64, h, c * C, b);
+                    tma_store_4d(&p.map_drl, stg + 16384 + cb * 8192, cb * 64, h, c * C, b);
+                }
+                bulk_commit();
+            }
         }
         if (ok) {  // dS0: the gradient of the first chunk's start state
             ok = wait_bar_warp(&bars->s_done, (nchunks - 1) & 1, abort_flag, wait_ns);
@@ -335,6 +378,7 @@ __global__ void __launch_bounds__(320, 1) bwd_tc_kernel(const __grid_constant__ 
                 }
             }
         }
+        if (tid == 0) bulk_wait0();  // the -dR stores have completed before the CTA leaves
         if (!ok) *abort_flag = 1;
     } else if (tid == 288) {
         // ============================ TMA producer (one thread) ============================
@@ -554,7 +598,9 @@ cudaError_t launch_bwd_state_tc(const BwdArgs &a, float *dse, const uint8_t *tpp
     BtParams p;
     memset(&p, 0, sizeof p);
     if (!bwd_row_map(&p.map_q, a.q, a.B, a.T, a.H) || !bwd_row_map(&p.map_k, a.k, a.B, a.T, a.H) ||
-        !bwd_row_map(&p.map_doh, hi, a.B, a.T, a.H) || !bwd_row_map(&p.map_dol, lo, a.B, a.T, a.H)) {
+        !bwd_row_map(&p.map_doh, hi, a.B, a.T, a.H) || !bwd_row_map(&p.map_dol, lo, a.B, a.T, a.H) ||
+        !bwd_row_map(&p.map_drh, dr_split, a.B, a.T, a.H) ||
+        !bwd_row_map(&p.map_drl, static_cast<__nv_bfloat16 *>(dr_split) + n, a.B, a.T, a.H)) {
         *why = "cuTensorMapEncodeTiled failed";
         return cudaErrorInvalidValue;
     }
@@ -565,8 +611,6 @@ cudaError_t launch_bwd_state_tc(const BwdArgs &a, float *dse, const uint8_t *tpp
     p.dS0 = a.dS0;
     p.g_out = g_out;
     p.dr_out = a.dv;
-    p.drs_hi = static_cast<__nv_bfloat16 *>(dr_split);
-    p.drs_lo = p.drs_hi + n;
     p.status = device_status_ptr();
     p.B = a.B;
     p.T = a.T;
