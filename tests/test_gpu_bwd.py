@@ -125,6 +125,27 @@ def test_train_pair_edge_shapes(efla, B, T, H, s0, dst):
     assert efla.device_status() == 0
 
 
+@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("f32", 64)])
+def test_train_pair_delta_rule_gate(efla, dtype, d):
+    """The training pair with the delta-rule gate (alpha = beta, unit-norm keys), against the
+    oracle's reverse mode of the same recurrence."""
+    c = _case(dtype, 2, 150, 2, d, d, seed=600 + d)
+    kf = torch.nn.functional.normalize(c["k"].float(), dim=-1)
+    c["k"] = (kf.to(torch.bfloat16) if dtype == "bf16" else kf).contiguous()
+    g = {x: (y.to(DEV) if y is not None else None) for x, y in c.items()}
+    o, S_T, ws = efla.fwd_chunked_train(g["q"], g["k"], g["v"], g["beta"], g["S0"], update="euler")
+    got = efla.bwd_chunked(g["q"], g["k"], g["v"], g["beta"], g["S0"], g["dO"], g["dST"], workspace=ws, saved=True,
+                           update="euler")
+    o_ref, S_ref = efla.fwd_chunked(g["q"], g["k"], g["v"], g["beta"], g["S0"], update="euler")
+    torch.cuda.synchronize()
+    assert torch.equal(o, o_ref) and torch.equal(S_T, S_ref)
+    ref = oracle.bwd(c["q"], c["k"], c["v"], c["beta"], c["S0"], c["dO"], c["dST"], update="euler")
+    for name in ("dq", "dk", "dv", "dbeta", "dS0"):
+        r = _rel(got[name], ref[name])
+        assert r <= REL, f"{name}: rel-fro {r:.3e}"
+    assert efla.device_status() == 0
+
+
 @pytest.mark.parametrize("kind", KINDS)
 def test_bwd_no_state_no_state_gradient(efla, kind):
     _check(efla, _case("bf16", 1, 64, 3, 128, 128, seed=4, s0=False, dst=False), kind=kind)
