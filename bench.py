@@ -66,19 +66,20 @@ def read_peaks():
 
 def profile_traffic(kernel_tag: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current source of the kernel (else None)."""
+    the current sources of the kernel (every source_file / source_sha256 pair it
+    lists, the kernel's file and the headers it includes; else None)."""
     path = os.path.join(ROOT, "profiles", f"{kernel_tag}.md")
     if not os.path.exists(path):
         return None
     text = open(path).read()
     m_b = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    m_s = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
-    m_f = re.search(r"source_file:\s*(\S+)", text)
-    if not (m_b and m_s and m_f):
+    pairs = re.findall(r"source_file:\s*(\S+)\s*\nsource_sha256:\s*([0-9a-f]{64})", text)
+    if not (m_b and pairs):
         return None
-    src = os.path.join(ROOT, m_f.group(1))
-    if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest() != m_s.group(1):
-        return None
+    for f, sha in pairs:
+        src = os.path.join(ROOT, f)
+        if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest() != sha:
+            return None
     return float(m_b.group(1))
 
 
