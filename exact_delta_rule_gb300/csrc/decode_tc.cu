@@ -137,9 +137,10 @@ __device__ __forceinline__ void split_pairs(const float *x, uint32_t *hi, uint32
     for (int c = 0; c < NP; ++c) {
         const uint32_t b0 = __float_as_uint(x[2 * c]), b1 = __float_as_uint(x[2 * c + 1]);
         hi[c] = __byte_perm(b0, b1, 0x7632);
-        const float r0 = x[2 * c] - __uint_as_float(b0 & 0xffff0000u);
-        const float r1 = x[2 * c + 1] - __uint_as_float(b1 & 0xffff0000u);
-        lo[c] = __byte_perm(__float_as_uint(r0), __float_as_uint(r1), 0x7632);
+        // the two remainders x - hi (exact) in one packed fp32x2 fma: hi * (-1) + x
+        const float2 r = __ffma2_rn(make_float2(__uint_as_float(b0 & 0xffff0000u), __uint_as_float(b1 & 0xffff0000u)),
+                                    make_float2(-1.f, -1.f), make_float2(x[2 * c], x[2 * c + 1]));
+        lo[c] = __byte_perm(__float_as_uint(r.x), __float_as_uint(r.y), 0x7632);
     }
 }
 
