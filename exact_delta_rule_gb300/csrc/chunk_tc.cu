@@ -400,13 +400,18 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
                         iv[4 * s4 + 2] = f.z;
                         iv[4 * s4 + 3] = f.w;
                     }
+                    const float2 rs2 = make_float2(rs, rs);
 #pragma unroll
-                    for (int s4 = 0; s4 < 32; s4 += 4) {
+                    for (int s4 = 0; s4 < 32; s4 += 4) {  // (rs iv) g, two columns per packed fp32x2 multiply
+                        const float2 a = __fmul2_rn(__fmul2_rn(rs2, make_float2(iv[s4], iv[s4 + 1])),
+                                                    make_float2(g[s4], g[s4 + 1]));
+                        const float2 c = __fmul2_rn(__fmul2_rn(rs2, make_float2(iv[s4 + 2], iv[s4 + 3])),
+                                                    make_float2(g[s4 + 2], g[s4 + 3]));
                         float4 w;
-                        w.x = col0 + s4 + 0 < t ? rs * iv[s4 + 0] * g[s4 + 0] : 0.f;
-                        w.y = col0 + s4 + 1 < t ? rs * iv[s4 + 1] * g[s4 + 1] : 0.f;
-                        w.z = col0 + s4 + 2 < t ? rs * iv[s4 + 2] * g[s4 + 2] : 0.f;
-                        w.w = col0 + s4 + 3 < t ? rs * iv[s4 + 3] * g[s4 + 3] : 0.f;
+                        w.x = col0 + s4 + 0 < t ? a.x : 0.f;
+                        w.y = col0 + s4 + 1 < t ? a.y : 0.f;
+                        w.z = col0 + s4 + 2 < t ? c.x : 0.f;
+                        w.w = col0 + s4 + 3 < t ? c.y : 0.f;
                         *reinterpret_cast<float4 *>(At + t * AT_LD + col0 + s4) = w;
                     }
                 } else if (write_o) {  // P[t][col0 .. col0+31] = Q K^T with the inclusive causal mask
@@ -442,9 +447,11 @@ __global__ void __launch_bounds__(448, 1) chunk_tc_kernel(const __grid_constant_
                     *reinterpret_cast<float4 *>(gn8 + 4) = *reinterpret_cast<const float4 *>(row_gn + s0 + c8 + 4);
                     float x[8];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int s = s0 + c8 + e;
-                        x[e] = s <= t ? rsc * tt8[e] * gn8[e] : 0.f;
+                    for (int e = 0; e < 8; e += 2) {  // (rsc T~) (gamma/n), two columns per packed multiply
+                        const float2 y = __fmul2_rn(__fmul2_rn(make_float2(rsc, rsc), make_float2(tt8[e], tt8[e + 1])),
+                                                    make_float2(gn8[e], gn8[e + 1]));
+                        x[e] = s0 + c8 + e <= t ? y.x : 0.f;
+                        x[e + 1] = s0 + c8 + e + 1 <= t ? y.y : 0.f;
                     }
                     uint32_t hh[4], ll[4];
                     split_pack<4>(x, hh, ll);
